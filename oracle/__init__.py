@@ -1,0 +1,193 @@
+"""CPU oracle for C <- alpha*(A x B) + beta*C (fp64 triple loop).
+
+TEST INFRASTRUCTURE ONLY.  The CUDA library is checked against this module;
+only the tests, the package smoke check and the benchmark's CPU-baseline leg
+may import it, and the library never does.  It shares no code with the CUDA
+path: the arithmetic lives in ``gemm_oracle.c`` (plain C, fp64, OpenMP over
+rows), compiled here with gcc and called through ctypes.
+
+The definition it follows is the GEMM of "GEMM Worklog I: Naive to Tiled"
+(opening equation: C = alpha (A x B) + beta C with A M x K, B K x N) and the
+SGEMM call of "A GEMM Kernel, Step by Step" ("The ladder we are climbing").
+Where the pages are silent (beta == 0, alpha == 0, K == 0, bf16 widening) the
+readings are stated in the C file's header.
+
+Every function here is pinned by tests that do not re-type its formula:
+identity and rank-1 closed forms, alpha/beta special cases, exact rational
+brute force on tiny shapes, numpy's float64 matmul as an independent routine,
+and transposition / permutation / linearity invariants.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gemm_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+
+_lock = threading.Lock()
+_default = None
+
+
+def compile_library(src: str, out_path: str) -> str:
+    """Compile an oracle C source into a shared library at out_path."""
+    os.makedirs(os.path.dirname(out_path), exist_ok=True)
+    tmp = out_path + ".tmp.%d" % os.getpid()
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+           "-fopenmp", "-fPIC", "-shared", src, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out_path)
+    return out_path
+
+
+def build(force: bool = False) -> str:
+    """Compile gemm_oracle.c into oracle/_build/liboracle.so; return its path."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    return compile_library(_SRC, _LIB_PATH)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _as_2d(x, dtype, rows, cols, name):
+    """Return (array, leading dimension) for a row-major matrix view.
+
+    Accepts a C-contiguous 2-D array, or a 2-D view whose rows are strided
+    (a slice of a wider matrix); the leading dimension is the row stride.
+    """
+    x = np.asarray(x)
+    if x.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, x.dtype))
+    if x.ndim != 2 or x.shape != (rows, cols):
+        raise ValueError("%s must have shape %s, got %s" % (name, (rows, cols), x.shape))
+    item = x.itemsize
+    if rows <= 1 and cols <= 1:
+        return np.ascontiguousarray(x), max(cols, 1)
+    if x.strides[1] != item and cols > 1:
+        x = np.ascontiguousarray(x)
+    ld = x.strides[0] // item if rows > 1 else max(cols, 1)
+    if ld < max(cols, 1) or x.strides[0] % item:
+        x = np.ascontiguousarray(x)
+        ld = max(cols, 1)
+    return x, ld
+
+
+class OracleLib:
+    """ctypes front end of one compiled oracle library."""
+
+    def __init__(self, path: str):
+        lib = ctypes.CDLL(path)
+        i64, dbl, ptr, cint = (ctypes.c_int64, ctypes.c_double,
+                               ctypes.c_void_p, ctypes.c_int)
+        for name in ("oracle_sgemm", "oracle_bf16gemm"):
+            fn = getattr(lib, name)
+            fn.restype = cint
+            fn.argtypes = [i64, i64, i64, dbl, ptr, i64, ptr, i64, dbl,
+                           ptr, i64, ptr, ptr, ptr, i64, cint]
+        lib.oracle_max_threads.restype = cint
+        lib.oracle_max_threads.argtypes = []
+        self._lib = lib
+        self.path = path
+
+    def max_threads(self) -> int:
+        return int(self._lib.oracle_max_threads())
+
+    def _run(self, fn_name, M, N, K, alpha, A, B, beta, C, in_dtype, nthreads, want64):
+        A2, lda = _as_2d(A, in_dtype, M, K, "A")
+        B2, ldb = _as_2d(B, in_dtype, K, N, "B")
+        if C is not None:
+            C2, ldc = _as_2d(C, np.float32, M, N, "C")
+        elif beta == 0.0:
+            C2, ldc = None, max(N, 1)
+        else:
+            raise ValueError("C is required when beta != 0")
+        out = np.empty((M, N), dtype=np.float32)
+        out64 = np.empty((M, N), dtype=np.float64) if want64 else None
+        den = np.empty((M, N), dtype=np.float64)
+        rc = getattr(self._lib, fn_name)(M, N, K, float(alpha), _ptr(A2), lda, _ptr(B2),
+                                         ldb, float(beta), _ptr(C2), ldc, _ptr(out),
+                                         _ptr(out64), _ptr(den), max(N, 1), int(nthreads))
+        if rc != 0:
+            raise RuntimeError("%s failed with code %d" % (fn_name, rc))
+        return out, out64, den
+
+    def sgemm(self, alpha, A, B, beta, C=None, nthreads=0, want64=False):
+        """fp32 SGEMM oracle.
+
+        A: (M, K) float32, B: (K, N) float32, C: (M, N) float32 (may be None
+        when beta == 0).  Returns (ref_fp32, ref_fp64 or None, den), where den
+        is |alpha| * (|A| |B|) + |beta| * |C| in fp64.
+        """
+        M, K = np.shape(A)
+        K2, N = np.shape(B)
+        if K2 != K:
+            raise ValueError("inner dimensions differ: %d vs %d" % (K, K2))
+        return self._run("oracle_sgemm", M, N, K, alpha, A, B, beta, C, np.float32,
+                         nthreads, want64)
+
+    def bf16gemm(self, alpha, A_bits, B_bits, beta, C=None, nthreads=0, want64=False):
+        """bf16-input / fp32-output oracle.
+
+        A_bits: (M, K) uint16 bf16 bit patterns, B_bits: (K, N) uint16, C
+        float32.  The inputs are widened exactly (bf16 is the top half of a
+        binary32).
+        """
+        M, K = np.shape(A_bits)
+        K2, N = np.shape(B_bits)
+        if K2 != K:
+            raise ValueError("inner dimensions differ: %d vs %d" % (K, K2))
+        return self._run("oracle_bf16gemm", M, N, K, alpha, A_bits, B_bits, beta, C,
+                         np.uint16, nthreads, want64)
+
+
+def default() -> OracleLib:
+    """The oracle built from gemm_oracle.c (compiled on first use)."""
+    global _default
+    with _lock:
+        if _default is None:
+            _default = OracleLib(build())
+    return _default
+
+
+def max_threads() -> int:
+    """Threads an oracle call with nthreads=0 uses (OpenMP's default)."""
+    return default().max_threads()
+
+
+def sgemm(alpha, A, B, beta, C=None, nthreads=0, want64=False):
+    """fp32 SGEMM oracle (see OracleLib.sgemm)."""
+    return default().sgemm(alpha, A, B, beta, C, nthreads, want64)
+
+
+def bf16gemm(alpha, A_bits, B_bits, beta, C=None, nthreads=0, want64=False):
+    """bf16-input oracle (see OracleLib.bf16gemm)."""
+    return default().bf16gemm(alpha, A_bits, B_bits, beta, C, nthreads, want64)
+
+
+def error_ratio(C_test, ref, den):
+    """max_ij |C_test - ref| / den, with den == 0 entries requiring equality.
+
+    Returns +inf if some entry with den == 0 differs from ref, or if C_test
+    holds a NaN where ref does not.
+    """
+    C_test = np.asarray(C_test, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    den = np.asarray(den, dtype=np.float64)
+    diff = np.abs(C_test - ref)
+    if np.any(np.isnan(diff)):
+        return float("inf")
+    zero = den == 0
+    if np.any(diff[zero] != 0):
+        return float("inf")
+    if not np.any(~zero):
+        return 0.0
+    return float(np.max(diff[~zero] / den[~zero]))
