@@ -1,0 +1,195 @@
+"""dense_gemm_12_gb300 -- GB300 (sm_103a) dense GEMM, C <- alpha*(A x B) + beta*C.
+
+Python binding of the C ABI in ``include/gemm12.h`` (``libgemm12.so``).  The
+functions named like the C entry points take the same arguments (device
+pointers as integers, a stream handle as an integer) and only marshal them;
+every step of the GEMM runs in the library's CUDA kernels.  The tensor
+helpers ``sgemm`` / ``bf16gemm`` derive pointers, leading dimensions and the
+current stream from torch tensors and call the same entry points.
+
+There is no fallback: if the compiled library is missing, loading fails with
+an error that says how to build it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import _build
+
+__all__ = [
+    "GemmError", "load_library", "library_path", "gemm_sgemm", "gemm_bf16gemm",
+    "gemm_status_string", "gemm_check_device_error", "gemm_shutdown",
+    "gemm_select_path", "gemm_quantization", "gemm_version", "sgemm", "bf16gemm",
+    "STATUS", "PATHS",
+]
+
+STATUS = {
+    0: "GEMM_OK", 1: "GEMM_ERR_INVALID_VALUE", 2: "GEMM_ERR_MISALIGNED",
+    3: "GEMM_ERR_UNSUPPORTED", 4: "GEMM_ERR_LAUNCH", 5: "GEMM_ERR_DEVICE_TIMEOUT",
+    6: "GEMM_ERR_NO_MEMORY",
+}
+PATHS = {
+    0: "none", 1: "scale_c", 2: "simt_tma", 3: "simt_generic", 4: "tc_bf16",
+    5: "tc_decode", 6: "simt_bf16",
+}
+
+
+class GemmError(RuntimeError):
+    """A C-ABI call returned a status other than GEMM_OK."""
+
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__("%s: %s" % (where, gemm_status_string(status)))
+
+
+class _Quantization(ctypes.Structure):
+    _fields_ = [
+        ("tiles_m", ctypes.c_int64), ("tiles_n", ctypes.c_int64), ("tiles", ctypes.c_int64),
+        ("covered_m", ctypes.c_int64), ("covered_n", ctypes.c_int64),
+        ("useful_fraction", ctypes.c_double), ("per_wave", ctypes.c_int64),
+        ("waves", ctypes.c_int64), ("wave_efficiency", ctypes.c_double),
+    ]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library(build_if_missing: bool = False):
+    """Load libgemm12.so (optionally compiling it first) and declare signatures."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB_PATH
+        if build_if_missing:
+            path = _build.build()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                "libgemm12.so is not built (expected at %s); run "
+                "`python -c 'import __graft_entry__ as g; g.build()'`" % path)
+        lib = ctypes.CDLL(path)
+        i64, f32, vp, cint = ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_int
+        gemm_args = [i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, vp]
+        lib.gemm_sgemm.argtypes = gemm_args
+        lib.gemm_sgemm.restype = cint
+        lib.gemm_bf16gemm.argtypes = gemm_args
+        lib.gemm_bf16gemm.restype = cint
+        lib.gemm_status_string.argtypes = [cint]
+        lib.gemm_status_string.restype = ctypes.c_char_p
+        lib.gemm_check_device_error.argtypes = [vp]
+        lib.gemm_check_device_error.restype = cint
+        lib.gemm_shutdown.argtypes = []
+        lib.gemm_shutdown.restype = cint
+        lib.gemm_select_path.argtypes = [cint, i64, i64, i64, f32, vp, i64, vp, i64]
+        lib.gemm_select_path.restype = cint
+        lib.gemm_quantization.argtypes = [i64, i64, i64, i64, i64, i64,
+                                          ctypes.POINTER(_Quantization)]
+        lib.gemm_quantization.restype = cint
+        lib.gemm_version.argtypes = []
+        lib.gemm_version.restype = cint
+        _lib = lib
+        return lib
+
+
+# ----------------------------------------------------------- C-ABI mirrors
+def gemm_sgemm(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0) -> int:
+    """fp32 SGEMM; pointers are device addresses (int). Returns the status."""
+    return load_library().gemm_sgemm(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream)
+
+
+def gemm_bf16gemm(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0) -> int:
+    """bf16-in / fp32-out GEMM; pointers are device addresses. Returns the status."""
+    return load_library().gemm_bf16gemm(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream)
+
+
+def gemm_status_string(status: int) -> str:
+    return load_library().gemm_status_string(int(status)).decode()
+
+
+def gemm_check_device_error(stream=0) -> int:
+    return load_library().gemm_check_device_error(stream)
+
+
+def gemm_shutdown() -> int:
+    return load_library().gemm_shutdown()
+
+
+def gemm_select_path(is_bf16, M, N, K, alpha, A, lda, B, ldb) -> str:
+    """Name of the kernel path a call with these arguments takes (host-only)."""
+    return PATHS[load_library().gemm_select_path(int(bool(is_bf16)), M, N, K, alpha, A, lda,
+                                                 B, ldb)]
+
+
+def gemm_quantization(M, N, BM, BN, num_sms, ctas_per_sm) -> dict:
+    """Tile / wave quantization of a launch (host-only arithmetic)."""
+    q = _Quantization()
+    st = load_library().gemm_quantization(M, N, BM, BN, num_sms, ctas_per_sm, ctypes.byref(q))
+    if st != 0:
+        raise GemmError(st, "gemm_quantization")
+    return {name: getattr(q, name) for name, _ in _Quantization._fields_}
+
+
+def gemm_version() -> int:
+    return load_library().gemm_version()
+
+
+# ------------------------------------------------------------ tensor helpers
+def _row_major_ld(t, name):
+    if t.dim() != 2:
+        raise ValueError("%s must be 2-D" % name)
+    rows, cols = t.shape
+    if cols > 1 and t.stride(1) != 1:
+        raise ValueError("%s must be row-major (unit column stride)" % name)
+    return t.stride(0) if rows > 1 else max(cols, 1)
+
+
+def _stream_handle(stream, device):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream
+
+
+def sgemm(A, B, C, alpha=1.0, beta=0.0, stream=None):
+    """C <- alpha*(A @ B) + beta*C in place for fp32 CUDA tensors (row-major views)."""
+    import torch
+    for t, n in ((A, "A"), (B, "B"), (C, "C")):
+        if t.dtype != torch.float32 or not t.is_cuda:
+            raise TypeError("%s must be a float32 CUDA tensor" % n)
+    M, K = A.shape
+    N = B.shape[1]
+    if B.shape[0] != K or tuple(C.shape) != (M, N):
+        raise ValueError("shape mismatch: A %s, B %s, C %s" % (tuple(A.shape), tuple(B.shape),
+                                                               tuple(C.shape)))
+    st = gemm_sgemm(M, N, K, float(alpha), A.data_ptr(), _row_major_ld(A, "A"), B.data_ptr(),
+                    _row_major_ld(B, "B"), float(beta), C.data_ptr(), _row_major_ld(C, "C"),
+                    _stream_handle(stream, C.device))
+    if st != 0:
+        raise GemmError(st, "gemm_sgemm")
+    return C
+
+
+def bf16gemm(A, B, C, alpha=1.0, beta=0.0, stream=None):
+    """C <- alpha*(A @ B) + beta*C in place; A, B bf16 CUDA tensors, C fp32."""
+    import torch
+    for t, n, dt in ((A, "A", torch.bfloat16), (B, "B", torch.bfloat16), (C, "C", torch.float32)):
+        if t.dtype != dt or not t.is_cuda:
+            raise TypeError("%s must be a %s CUDA tensor" % (n, dt))
+    M, K = A.shape
+    N = B.shape[1]
+    if B.shape[0] != K or tuple(C.shape) != (M, N):
+        raise ValueError("shape mismatch: A %s, B %s, C %s" % (tuple(A.shape), tuple(B.shape),
+                                                               tuple(C.shape)))
+    st = gemm_bf16gemm(M, N, K, float(alpha), A.data_ptr(), _row_major_ld(A, "A"), B.data_ptr(),
+                       _row_major_ld(B, "B"), float(beta), C.data_ptr(), _row_major_ld(C, "C"),
+                       _stream_handle(stream, C.device))
+    if st != 0:
+        raise GemmError(st, "gemm_bf16gemm")
+    return C

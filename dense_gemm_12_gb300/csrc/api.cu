@@ -1,0 +1,452 @@
+// api.cu -- the C ABI declared in include/gemm12.h: argument checks, kernel
+// path selection, TMA tensor-map encoding, the decode workspace, the device
+// error word, and the C <- beta*C kernel for the degenerate cases.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/gemm12.h"
+#include "internal.h"
+
+namespace g12 {
+
+// Error word shared by every kernel of this library on a device; its device
+// address is looked up once per device and passed to the kernels.
+__device__ uint32_t g_error_word = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int64_t kMaxDim = (int64_t{1} << 31) - 1;
+
+struct DeviceState {
+  std::once_flag once;
+  cudaError_t init_error = cudaSuccess;
+  int num_sms = 0;
+  int cc_major = 0, cc_minor = 0;
+  uint32_t* err_word = nullptr;
+  // decode workspace (grown on demand, freed by gemm_shutdown)
+  std::mutex ws_mutex;
+  float* ws = nullptr;
+  int64_t ws_floats = 0;
+  uint32_t* counters = nullptr;
+  int64_t counter_count = 0;
+};
+
+DeviceState g_dev[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+std::once_flag g_encode_once;
+EncodeTiledFn g_encode = nullptr;
+
+EncodeTiledFn encode_fn() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  });
+  return g_encode;
+}
+
+// Current device's state, initialised on first use.  Returns nullptr if
+// there is no usable device.
+DeviceState* device_state(gemm_status_t* status) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    *status = GEMM_ERR_UNSUPPORTED;
+    return nullptr;
+  }
+  DeviceState& st = g_dev[dev];
+  std::call_once(st.once, [&st, dev] {
+    cudaError_t e = cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+      e = cudaDeviceGetAttribute(&st.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e == cudaSuccess)
+      e = cudaDeviceGetAttribute(&st.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e == cudaSuccess) e = cudaGetSymbolAddress(reinterpret_cast<void**>(&st.err_word), g_error_word);
+    st.init_error = e;
+    if (e != cudaSuccess) cudaGetLastError();
+  });
+  if (st.init_error != cudaSuccess) {
+    *status = GEMM_ERR_UNSUPPORTED;
+    return nullptr;
+  }
+  // The kernels are built for sm_103a only.
+  if (!(st.cc_major == 10 && st.cc_minor == 3)) {
+    *status = GEMM_ERR_UNSUPPORTED;
+    return nullptr;
+  }
+  *status = GEMM_OK;
+  return &st;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// TMA can describe a row-major matrix when its base is 16-byte aligned and
+// its row pitch is a multiple of 16 bytes.
+bool tma_ok(const void* base, int64_t ld, int elem_bytes) {
+  return aligned16(base) && ((ld * elem_bytes) % 16 == 0);
+}
+
+// 2-D tensor map: dims {inner, outer}, row pitch ld elements, box {bx, by}.
+bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes, const void* base,
+               int64_t inner, int64_t outer, int64_t ld, uint32_t bx, uint32_t by,
+               CUtensorMapSwizzle swizzle) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * elem_bytes};
+  cuuint32_t box[2] = {bx, by};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+gemm_status_t check_common(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                           int64_t ldc) {
+  if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_VALUE;
+  if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return GEMM_ERR_INVALID_VALUE;
+  if (lda > kMaxDim || ldb > kMaxDim || ldc > kMaxDim) return GEMM_ERR_INVALID_VALUE;
+  if (lda < (K > 1 ? K : 1)) return GEMM_ERR_INVALID_VALUE;
+  if (ldb < (N > 1 ? N : 1)) return GEMM_ERR_INVALID_VALUE;
+  if (ldc < (N > 1 ? N : 1)) return GEMM_ERR_INVALID_VALUE;
+  return GEMM_OK;
+}
+
+gemm_path_t select_path(bool bf16, int64_t M, int64_t N, int64_t K, float alpha, const void* A,
+                        int64_t lda, const void* B, int64_t ldb) {
+  if (M == 0 || N == 0) return GEMM_PATH_NONE;
+  if (K == 0 || alpha == 0.0f) return GEMM_PATH_SCALE_C;
+  if (!bf16) {
+    const bool a_tma = tma_ok(A, lda, 4);
+    const bool b_tma = tma_ok(B, ldb, 4);
+    return (a_tma && b_tma) ? GEMM_PATH_SIMT_TMA : GEMM_PATH_SIMT_GENERIC;
+  }
+  const bool tma = tma_ok(A, lda, 2) && tma_ok(B, ldb, 2);
+  if (!tma) return GEMM_PATH_SIMT_BF16;
+  return M <= kDecBM ? GEMM_PATH_TC_DECODE : GEMM_PATH_TC_BF16;
+}
+
+gemm_status_t from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return GEMM_OK;
+  cudaGetLastError();
+  return e == cudaErrorMemoryAllocation ? GEMM_ERR_NO_MEMORY : GEMM_ERR_LAUNCH;
+}
+
+gemm_status_t run_scale(int64_t M, int64_t N, float beta, float* C, int64_t ldc,
+                        cudaStream_t stream) {
+  return from_cuda(launch_scale_c(static_cast<int>(M), static_cast<int>(N), beta, C, ldc, stream));
+}
+
+int c_vec4_ok(const float* C, int64_t ldc) { return (aligned16(C) && (ldc % 4 == 0)) ? 1 : 0; }
+
+gemm_status_t ensure_decode_workspace(DeviceState& st, int64_t floats, int64_t counters) {
+  if (st.ws_floats >= floats && st.counter_count >= counters) return GEMM_OK;
+  // Growing: the old buffers may still be read by kernels in flight.
+  if (cudaDeviceSynchronize() != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_LAUNCH;
+  }
+  if (st.ws_floats < floats) {
+    if (st.ws) cudaFree(st.ws);
+    st.ws = nullptr;
+    st.ws_floats = 0;
+    if (cudaMalloc(reinterpret_cast<void**>(&st.ws), floats * sizeof(float)) != cudaSuccess) {
+      cudaGetLastError();
+      st.ws = nullptr;
+      return GEMM_ERR_NO_MEMORY;
+    }
+    st.ws_floats = floats;
+  }
+  if (st.counter_count < counters) {
+    if (st.counters) cudaFree(st.counters);
+    st.counters = nullptr;
+    st.counter_count = 0;
+    if (cudaMalloc(reinterpret_cast<void**>(&st.counters), counters * sizeof(uint32_t)) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      st.counters = nullptr;
+      return GEMM_ERR_NO_MEMORY;
+    }
+    if (cudaMemset(st.counters, 0, counters * sizeof(uint32_t)) != cudaSuccess) {
+      cudaGetLastError();
+      return GEMM_ERR_LAUNCH;
+    }
+    st.counter_count = counters;
+  }
+  return GEMM_OK;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------ C <- beta*C
+namespace {
+__global__ void scale_c_kernel(int M, int N, float beta, float* C, int64_t ldc) {
+  const int64_t total = static_cast<int64_t>(M) * N;
+  for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t i = e / N, j = e - i * N;
+    float* c = C + i * ldc + j;
+    *c = (beta == 0.0f) ? 0.0f : beta * *c;
+  }
+}
+}  // namespace
+
+cudaError_t launch_scale_c(int M, int N, float beta, float* C, int64_t ldc, cudaStream_t stream) {
+  const int64_t total = static_cast<int64_t>(M) * N;
+  int64_t blocks = (total + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  if (blocks < 1) blocks = 1;
+  scale_c_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(M, N, beta, C, ldc);
+  return cudaGetLastError();
+}
+
+}  // namespace g12
+
+using namespace g12;
+
+extern "C" {
+
+int gemm_version(void) { return 100; }
+
+const char* gemm_status_string(gemm_status_t s) {
+  switch (s) {
+    case GEMM_OK: return "GEMM_OK: success";
+    case GEMM_ERR_INVALID_VALUE: return "GEMM_ERR_INVALID_VALUE: bad size, leading dimension or pointer";
+    case GEMM_ERR_MISALIGNED: return "GEMM_ERR_MISALIGNED: bf16 pointer not 2-byte aligned";
+    case GEMM_ERR_UNSUPPORTED: return "GEMM_ERR_UNSUPPORTED: no sm_103a device or unsupported size";
+    case GEMM_ERR_LAUNCH: return "GEMM_ERR_LAUNCH: kernel launch or CUDA runtime error";
+    case GEMM_ERR_DEVICE_TIMEOUT: return "GEMM_ERR_DEVICE_TIMEOUT: a bounded device wait ran out";
+    case GEMM_ERR_NO_MEMORY: return "GEMM_ERR_NO_MEMORY: workspace allocation failed";
+  }
+  return "unknown gemm status";
+}
+
+gemm_path_t gemm_select_path(int is_bf16, int64_t M, int64_t N, int64_t K, float alpha,
+                             const void* A, int64_t lda, const void* B, int64_t ldb) {
+  if (check_common(M, N, K, lda, ldb, N > 1 ? N : 1) != GEMM_OK) return GEMM_PATH_NONE;
+  return select_path(is_bf16 != 0, M, N, K, alpha, A, lda, B, ldb);
+}
+
+gemm_status_t gemm_quantization(int64_t M, int64_t N, int64_t BM, int64_t BN, int64_t num_sms,
+                                int64_t ctas_per_sm, gemm_quantization_t* out) {
+  if (out == nullptr || M < 0 || N < 0 || BM <= 0 || BN <= 0 || num_sms <= 0 || ctas_per_sm <= 0)
+    return GEMM_ERR_INVALID_VALUE;
+  gemm_quantization_t q{};
+  q.tiles_m = (M + BM - 1) / BM;
+  q.tiles_n = (N + BN - 1) / BN;
+  q.tiles = q.tiles_m * q.tiles_n;
+  q.covered_m = q.tiles_m * BM;
+  q.covered_n = q.tiles_n * BN;
+  q.per_wave = num_sms * ctas_per_sm;
+  q.waves = (q.tiles + q.per_wave - 1) / q.per_wave;
+  if (q.tiles == 0) {
+    q.useful_fraction = 1.0;
+    q.wave_efficiency = 1.0;
+  } else {
+    q.useful_fraction = (static_cast<double>(M) * static_cast<double>(N)) /
+                        (static_cast<double>(q.covered_m) * static_cast<double>(q.covered_n));
+    q.wave_efficiency =
+        static_cast<double>(q.tiles) / (static_cast<double>(q.waves) * q.per_wave);
+  }
+  *out = q;
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_sgemm(int64_t M, int64_t N, int64_t K, float alpha, const float* A,
+                         int64_t lda, const float* B, int64_t ldb, float beta, float* C,
+                         int64_t ldc, void* stream) {
+  gemm_status_t s = check_common(M, N, K, lda, ldb, ldc);
+  if (s != GEMM_OK) return s;
+  const gemm_path_t path = select_path(false, M, N, K, alpha, A, lda, B, ldb);
+  if (path == GEMM_PATH_NONE) return GEMM_OK;
+  if (C == nullptr) return GEMM_ERR_INVALID_VALUE;
+  if (path != GEMM_PATH_SCALE_C && (A == nullptr || B == nullptr)) return GEMM_ERR_INVALID_VALUE;
+  if ((reinterpret_cast<uintptr_t>(C) & 3u) ||
+      (path != GEMM_PATH_SCALE_C && ((reinterpret_cast<uintptr_t>(A) & 3u) ||
+                                     (reinterpret_cast<uintptr_t>(B) & 3u))))
+    return GEMM_ERR_INVALID_VALUE;
+  DeviceState* st = device_state(&s);
+  if (st == nullptr) return s;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (path == GEMM_PATH_SCALE_C) return run_scale(M, N, beta, C, ldc, cs);
+
+  SimtArgs a{};
+  a.M = static_cast<int>(M);
+  a.N = static_cast<int>(N);
+  a.K = static_cast<int>(K);
+  a.alpha = alpha;
+  a.beta = beta;
+  a.A = A;
+  a.lda = lda;
+  a.B = B;
+  a.ldb = ldb;
+  a.C = C;
+  a.ldc = ldc;
+  a.c_vec4 = c_vec4_ok(C, ldc);
+  a.err = st->err_word;
+  CUtensorMap tmA, tmB;
+  LoadMode ma = kLoadCpAsyncF32, mb = kLoadCpAsyncF32;
+  if (tma_ok(A, lda, 4) &&
+      encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, A, K, M, lda, kSimtBK, kSimtBM,
+                CU_TENSOR_MAP_SWIZZLE_128B))
+    ma = kLoadTma;
+  if (tma_ok(B, ldb, 4) &&
+      encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, B, N, K, ldb, kSimtBN, kSimtBK,
+                CU_TENSOR_MAP_SWIZZLE_NONE))
+    mb = kLoadTma;
+  return from_cuda(launch_simt(a, ma, mb, ma == kLoadTma ? &tmA : nullptr,
+                               mb == kLoadTma ? &tmB : nullptr, st->num_sms, cs));
+}
+
+gemm_status_t gemm_bf16gemm(int64_t M, int64_t N, int64_t K, float alpha, const void* A,
+                            int64_t lda, const void* B, int64_t ldb, float beta, float* C,
+                            int64_t ldc, void* stream) {
+  gemm_status_t s = check_common(M, N, K, lda, ldb, ldc);
+  if (s != GEMM_OK) return s;
+  const gemm_path_t path = select_path(true, M, N, K, alpha, A, lda, B, ldb);
+  if (path == GEMM_PATH_NONE) return GEMM_OK;
+  if (C == nullptr) return GEMM_ERR_INVALID_VALUE;
+  if (reinterpret_cast<uintptr_t>(C) & 3u) return GEMM_ERR_INVALID_VALUE;
+  if (path != GEMM_PATH_SCALE_C) {
+    if (A == nullptr || B == nullptr) return GEMM_ERR_INVALID_VALUE;
+    if ((reinterpret_cast<uintptr_t>(A) & 1u) || (reinterpret_cast<uintptr_t>(B) & 1u))
+      return GEMM_ERR_MISALIGNED;
+  }
+  DeviceState* st = device_state(&s);
+  if (st == nullptr) return s;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (path == GEMM_PATH_SCALE_C) return run_scale(M, N, beta, C, ldc, cs);
+
+  if (path == GEMM_PATH_SIMT_BF16) {
+    SimtArgs a{};
+    a.M = static_cast<int>(M);
+    a.N = static_cast<int>(N);
+    a.K = static_cast<int>(K);
+    a.alpha = alpha;
+    a.beta = beta;
+    a.A = A;
+    a.lda = lda;
+    a.B = B;
+    a.ldb = ldb;
+    a.C = C;
+    a.ldc = ldc;
+    a.c_vec4 = c_vec4_ok(C, ldc);
+    a.err = st->err_word;
+    return from_cuda(launch_simt(a, kLoadConvertBf16, kLoadConvertBf16, nullptr, nullptr,
+                                 st->num_sms, cs));
+  }
+
+  CUtensorMap tmA, tmB;
+  if (path == GEMM_PATH_TC_BF16) {
+    if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, K, M, lda, kTcBK, kTcBM,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, N, K, ldb, 64, kTcBK,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+      return GEMM_ERR_LAUNCH;
+    TcArgs a{};
+    a.M = static_cast<int>(M);
+    a.N = static_cast<int>(N);
+    a.K = static_cast<int>(K);
+    a.alpha = alpha;
+    a.beta = beta;
+    a.C = C;
+    a.ldc = ldc;
+    a.c_vec4 = c_vec4_ok(C, ldc);
+    a.err = st->err_word;
+    return from_cuda(launch_tc_bf16(a, &tmA, &tmB, st->num_sms, cs));
+  }
+
+  // GEMM_PATH_TC_DECODE
+  if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, K, M, lda, kDecBK, kDecBM,
+                 CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, N, K, ldb, 64, kDecBK,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
+    return GEMM_ERR_LAUNCH;
+  const int grid = decode_grid(static_cast<int>(N), static_cast<int>(K), st->num_sms);
+  DecodeArgs a{};
+  a.M = static_cast<int>(M);
+  a.N = static_cast<int>(N);
+  a.K = static_cast<int>(K);
+  a.alpha = alpha;
+  a.beta = beta;
+  a.C = C;
+  a.ldc = ldc;
+  a.err = st->err_word;
+  std::lock_guard<std::mutex> lock(st->ws_mutex);
+  s = ensure_decode_workspace(*st, decode_workspace_floats(a.N, a.K, grid),
+                              decode_counter_count(a.N));
+  if (s != GEMM_OK) return s;
+  a.workspace = st->ws;
+  a.counters = st->counters;
+  return from_cuda(launch_tc_decode(a, &tmA, &tmB, grid, cs));
+}
+
+gemm_status_t gemm_check_device_error(void* stream) {
+  gemm_status_t s;
+  DeviceState* st = device_state(&s);
+  if (st == nullptr) return s;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_LAUNCH;
+  }
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, st->err_word, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_LAUNCH;
+  }
+  if (word == 0) return GEMM_OK;
+  const uint32_t zero = 0;
+  cudaMemcpy(st->err_word, &zero, sizeof zero, cudaMemcpyHostToDevice);
+  // A decode launch that gave up may have left arrival counters non-zero.
+  {
+    std::lock_guard<std::mutex> lock(st->ws_mutex);
+    if (st->counters) cudaMemset(st->counters, 0, st->counter_count * sizeof(uint32_t));
+  }
+  cudaGetLastError();
+  return GEMM_ERR_DEVICE_TIMEOUT;
+}
+
+gemm_status_t gemm_shutdown(void) {
+  int n = 0;
+  if (cudaGetDeviceCount(&n) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_OK;
+  }
+  int cur = 0;
+  cudaGetDevice(&cur);
+  gemm_status_t result = GEMM_OK;
+  for (int d = 0; d < n && d < kMaxDevices; ++d) {
+    DeviceState& st = g_dev[d];
+    std::lock_guard<std::mutex> lock(st.ws_mutex);
+    if (st.ws == nullptr && st.counters == nullptr) continue;
+    if (cudaSetDevice(d) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+      cudaGetLastError();
+      result = GEMM_ERR_LAUNCH;
+      continue;
+    }
+    if (st.ws) cudaFree(st.ws);
+    if (st.counters) cudaFree(st.counters);
+    st.ws = nullptr;
+    st.counters = nullptr;
+    st.ws_floats = 0;
+    st.counter_count = 0;
+  }
+  cudaSetDevice(cur);
+  return result;
+}
+
+}  // extern "C"

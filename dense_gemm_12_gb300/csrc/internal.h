@@ -1,0 +1,78 @@
+// internal.h -- host-side interface between the C ABI (api.cu) and the kernel
+// translation units.  Not installed; not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace g12 {
+
+// How one operand of the CUDA-core kernel reaches shared memory.
+enum LoadMode : int {
+  kLoadTma = 0,         // tiled TMA copy (fp32, 16-B aligned base and pitch)
+  kLoadCpAsyncF32 = 1,  // 4-byte cp.async by producer warps (any fp32 layout)
+  kLoadConvertBf16 = 2, // bf16 loads widened to fp32 by producer warps
+};
+
+struct SimtArgs {
+  int M, N, K;
+  float alpha, beta;
+  const void* A;   // fp32 or bf16 elements
+  int64_t lda;
+  const void* B;
+  int64_t ldb;
+  float* C;
+  int64_t ldc;
+  int c_vec4;      // 1 if C rows may be written as aligned float4
+  uint32_t* err;   // device error word
+};
+
+// CUDA-core (FFMA) GEMM: 128 x 128 block tiles, warp tiles 32 x 64, 8 x 8
+// register micro-tiles.  tmA / tmB are used only for operands in kLoadTma mode.
+cudaError_t launch_simt(const SimtArgs& a, LoadMode mode_a, LoadMode mode_b,
+                        const CUtensorMap* tmA, const CUtensorMap* tmB, int num_sms,
+                        cudaStream_t stream);
+
+// Tile geometry of the CUDA-core kernel (also used by the launch planner).
+constexpr int kSimtBM = 128, kSimtBN = 128, kSimtBK = 32;
+
+struct TcArgs {
+  int M, N, K;
+  float alpha, beta;
+  float* C;
+  int64_t ldc;
+  int c_vec4;
+  uint32_t* err;
+};
+
+// bf16 tensor-core GEMM (tcgen05, accumulator in TMEM): 128 x 256 tiles.
+cudaError_t launch_tc_bf16(const TcArgs& a, const CUtensorMap* tmA, const CUtensorMap* tmB,
+                           int num_sms, cudaStream_t stream);
+constexpr int kTcBM = 128, kTcBN = 256, kTcBK = 64;
+
+struct DecodeArgs {
+  int M, N, K;
+  float alpha, beta;
+  float* C;
+  int64_t ldc;
+  float* workspace;     // partial sums, see decode_workspace_floats
+  uint32_t* counters;   // one arrival counter per 128-column n-tile, zeroed
+  uint32_t* err;
+};
+
+// bf16 decode GEMM (M <= 16): tcgen05 with the operands swapped
+// (D^T = B^T A^T, MMA M = 128 over N, MMA N = 16 over M), split over K.
+cudaError_t launch_tc_decode(const DecodeArgs& a, const CUtensorMap* tmA,
+                             const CUtensorMap* tmB, int num_ctas, cudaStream_t stream);
+constexpr int kDecBN = 128, kDecBM = 16, kDecBK = 64;
+// Workspace floats and counters a decode launch of this shape needs.
+int64_t decode_workspace_floats(int N, int K, int num_ctas);
+int64_t decode_counter_count(int N);
+int decode_grid(int N, int K, int num_sms);
+
+// C <- beta * C (beta == 0 writes zeros without reading C).
+cudaError_t launch_scale_c(int M, int N, float beta, float* C, int64_t ldc,
+                           cudaStream_t stream);
+
+}  // namespace g12

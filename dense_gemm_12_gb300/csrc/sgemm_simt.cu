@@ -1,0 +1,381 @@
+// sgemm_simt.cu -- fp32 GEMM on the CUDA cores (FFMA), C = alpha*A*B + beta*C.
+//
+// Structure (the register-tiled scheme of "Tiled matrix multiplication",
+// "How it works", and of "A GEMM Kernel, Step by Step", rungs four to six and
+// "The last rung", rebuilt for sm_103a):
+//   * persistent CTAs walk 128 x 128 output tiles in a grouped raster order so
+//     CTAs running at the same time share A row-panels and B column-panels in
+//     L2 ("Tiled matrix multiplication", "Complexity and constants");
+//   * a producer warp streams 128 x 32 slices of A and 32 x 128 slices of B
+//     into a STAGES-deep shared-memory ring with TMA (cp.async.bulk.tensor),
+//     completion tracked by full/empty mbarriers -- the multi-buffered copy
+//     pipeline the pages name for Hopper, which also frees the compute warps
+//     from issuing any load instruction to global memory;
+//   * 8 compute warps each own a 32 x 64 warp tile, every lane an 8 x 8
+//     register micro-tile; per k the lane reads 8 A values and 8 B values from
+//     shared memory with 128-bit loads and issues 64 FFMAs;
+//   * the A slice stays k-contiguous (TMA cannot transpose fp32); the 128-byte
+//     TMA swizzle plus a lane->row map of stride 4 keeps the 128-bit reads of
+//     four k values at once free of bank conflicts, which replaces the pages'
+//     transposed-and-padded A tile;
+//   * TMA zero-fills rows and columns past M, N, K, so ragged edges need no
+//     predicate in the hot loop; the epilogue applies alpha/beta and masks.
+// Operands TMA cannot describe (unaligned base or pitch, or bf16 to be widened)
+// are loaded by four producer warps with cp.async / plain loads into the same
+// shared-memory layout, so the compute warps are identical in every variant.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace g12 {
+namespace {
+
+constexpr int BM = kSimtBM, BN = kSimtBN, BK = kSimtBK;
+constexpr int STAGES = 4;
+constexpr int kComputeWarps = 8;
+constexpr int kComputeThreads = kComputeWarps * 32;
+constexpr int kStageBytesA = BM * BK * 4;  // 16 KB, rows of 128 B, 128-B swizzled
+constexpr int kStageBytesB = BK * BN * 4;  // 16 KB, rows of 512 B, not swizzled
+constexpr int kStageBytes = kStageBytesA + kStageBytesB;
+constexpr int kGroupM = 8;                 // raster group height in tiles
+
+struct __align__(8) SimtSmemTail {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  int abort_flag;
+};
+
+constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + STAGES * kStageBytes +
+                              sizeof(SimtSmemTail);
+
+__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int& tm, int& tn) {
+  const int per_group = kGroupM * tiles_n;
+  const int g = t / per_group;
+  const int first_m = g * kGroupM;
+  const int rows = min(tiles_m - first_m, kGroupM);
+  const int local = t - g * per_group;
+  tm = first_m + local % rows;
+  tn = local / rows;
+}
+
+// Byte offset of A element (m, k) inside a stage: 128-byte rows, the 16-byte
+// chunk index XOR-ed with (m mod 8) -- the layout TMA's 128-byte swizzle
+// writes into a 1024-byte aligned buffer.
+__device__ __forceinline__ uint32_t a_smem_offset(int m, int k) {
+  return static_cast<uint32_t>(m * 128 + ((((k >> 2) ^ (m & 7)) << 4)) + ((k & 3) << 2));
+}
+
+template <int MODE_A, int MODE_B>
+struct SimtTraits {
+  static constexpr bool kAnyGeneric = (MODE_A != kLoadTma) || (MODE_B != kLoadTma);
+  static constexpr bool kAnyTma = (MODE_A == kLoadTma) || (MODE_B == kLoadTma);
+  static constexpr int kProducerWarps = kAnyGeneric ? 4 : 1;
+  static constexpr int kThreads = kComputeThreads + kProducerWarps * 32;
+  // Arrivals that complete one phase of a full barrier: every generic
+  // producer thread arrives once, the TMA issuer once (with the byte count).
+  static constexpr uint32_t kFullCount = (kAnyGeneric ? 128u : 0u) + (kAnyTma ? 1u : 0u);
+  static constexpr uint32_t kTmaBytes =
+      (MODE_A == kLoadTma ? kStageBytesA : 0) + (MODE_B == kLoadTma ? kStageBytesB : 0);
+};
+
+// ------------------------------------------------------------------ loaders
+// Generic fp32 A slice: 128 rows x 32 k, 32 elements per producer thread,
+// consecutive threads on consecutive k (coalesced reads of row-major A).
+__device__ __forceinline__ void load_a_cpasync(uint8_t* sA, const float* A, int64_t lda, int M,
+                                               int K, int m0, int k0, int ptid) {
+#pragma unroll 8
+  for (int q = 0; q < (BM * BK) / 128; ++q) {
+    const int e = ptid + q * 128;
+    const int m = e >> 5, k = e & 31;
+    const int gm = m0 + m, gk = k0 + k;
+    const bool in = (gm < M) && (gk < K);
+    const float* src = in ? (A + static_cast<int64_t>(gm) * lda + gk) : A;
+    cp_async_4(sA + a_smem_offset(m, k), src, in ? 4u : 0u);
+  }
+}
+
+// Generic fp32 B slice: 32 k-rows x 128 n, consecutive threads on consecutive n.
+__device__ __forceinline__ void load_b_cpasync(uint8_t* sB, const float* B, int64_t ldb, int N,
+                                               int K, int n0, int k0, int ptid) {
+#pragma unroll 8
+  for (int q = 0; q < (BK * BN) / 128; ++q) {
+    const int e = ptid + q * 128;
+    const int k = e >> 7, n = e & 127;
+    const int gk = k0 + k, gn = n0 + n;
+    const bool in = (gk < K) && (gn < N);
+    const float* src = in ? (B + static_cast<int64_t>(gk) * ldb + gn) : B;
+    cp_async_4(sB + (k * BN + n) * 4, src, in ? 4u : 0u);
+  }
+}
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint16_t h) {
+  return __uint_as_float(static_cast<uint32_t>(h) << 16);
+}
+
+// bf16 A slice widened to fp32 (exact), same layout as the fp32 A slice.
+__device__ __forceinline__ void load_a_bf16(uint8_t* sA, const uint16_t* A, int64_t lda, int M,
+                                            int K, int m0, int k0, int ptid) {
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    uint16_t v[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const int e = ptid + (half * 16 + q) * 128;
+      const int m = e >> 5, k = e & 31;
+      const int gm = m0 + m, gk = k0 + k;
+      v[q] = (gm < M && gk < K) ? __ldg(A + static_cast<int64_t>(gm) * lda + gk) : uint16_t(0);
+    }
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const int e = ptid + (half * 16 + q) * 128;
+      const int m = e >> 5, k = e & 31;
+      *reinterpret_cast<float*>(sA + a_smem_offset(m, k)) = bf16_bits_to_f32(v[q]);
+    }
+  }
+}
+
+__device__ __forceinline__ void load_b_bf16(uint8_t* sB, const uint16_t* B, int64_t ldb, int N,
+                                            int K, int n0, int k0, int ptid) {
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    uint16_t v[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const int e = ptid + (half * 16 + q) * 128;
+      const int k = e >> 7, n = e & 127;
+      const int gk = k0 + k, gn = n0 + n;
+      v[q] = (gk < K && gn < N) ? __ldg(B + static_cast<int64_t>(gk) * ldb + gn) : uint16_t(0);
+    }
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const int e = ptid + (half * 16 + q) * 128;
+      const int k = e >> 7, n = e & 127;
+      *reinterpret_cast<float*>(sB + (k * BN + n) * 4) = bf16_bits_to_f32(v[q]);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ compute
+// One stage (BK = 32 values of k) of the 8 x 8 outer-product accumulation.
+// Lane layout inside the 32 x 64 warp tile: rg = lane / 8 picks rows
+// {rg, rg+4, ..., rg+28}; cg = lane % 8 picks columns {4cg..4cg+3} and
+// {32+4cg..32+4cg+3}.
+__device__ __forceinline__ void compute_stage(const uint8_t* sA, const uint8_t* sB,
+                                              float (&acc)[8][8], int wm, int wn, int rg,
+                                              int cg) {
+  const uint8_t* a_row0 = sA + (wm * 32 + rg) * 128;  // row rg of the warp tile
+  const float* b_base = reinterpret_cast<const float*>(sB) + wn * 64 + cg * 4;
+  const int x_even = rg;      // (row & 7) for rows rg + 4i, i even
+  const int x_odd = rg + 4;   // ... i odd
+#pragma unroll 2
+  for (int kq = 0; kq < BK / 4; ++kq) {
+    float4 a[8];
+    const int off_even = (kq ^ x_even) << 4;
+    const int off_odd = (kq ^ x_odd) << 4;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint8_t* p = a_row0 + i * 4 * 128 + ((i & 1) ? off_odd : off_even);
+      a[i] = *reinterpret_cast<const float4*>(p);
+    }
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const int k = kq * 4 + kk;
+      const float4 b0 = *reinterpret_cast<const float4*>(b_base + k * BN);
+      const float4 b1 = *reinterpret_cast<const float4*>(b_base + k * BN + 32);
+      const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float av = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av, bv[j], acc[i][j]);
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void epilogue(const SimtArgs& p, const float (&acc)[8][8], int tm,
+                                         int tn, int wm, int wn, int rg, int cg) {
+  const bool read_c = (p.beta != 0.0f);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int row = tm * BM + wm * 32 + rg + 4 * i;
+    if (row >= p.M) continue;
+    float* c_row = p.C + static_cast<int64_t>(row) * p.ldc;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int col = tn * BN + wn * 64 + h * 32 + cg * 4;
+      if (p.c_vec4 && col + 3 < p.N) {
+        float4 v = make_float4(acc[i][h * 4 + 0], acc[i][h * 4 + 1], acc[i][h * 4 + 2],
+                               acc[i][h * 4 + 3]);
+        float4* dst = reinterpret_cast<float4*>(c_row + col);
+        if (read_c) {
+          const float4 o = *dst;
+          v.x = fmaf(p.alpha, v.x, p.beta * o.x);
+          v.y = fmaf(p.alpha, v.y, p.beta * o.y);
+          v.z = fmaf(p.alpha, v.z, p.beta * o.z);
+          v.w = fmaf(p.alpha, v.w, p.beta * o.w);
+        } else {
+          v.x *= p.alpha;
+          v.y *= p.alpha;
+          v.z *= p.alpha;
+          v.w *= p.alpha;
+        }
+        *dst = v;
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          if (col + c < p.N) {
+            const float r = acc[i][h * 4 + c];
+            c_row[col + c] = read_c ? fmaf(p.alpha, r, p.beta * c_row[col + c]) : p.alpha * r;
+          }
+        }
+      }
+    }
+  }
+}
+
+template <int MODE_A, int MODE_B>
+__global__ void __launch_bounds__(SimtTraits<MODE_A, MODE_B>::kThreads, 1)
+    simt_gemm_kernel(const SimtArgs p, const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmB) {
+  using T = SimtTraits<MODE_A, MODE_B>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  SimtSmemTail* tail = reinterpret_cast<SimtSmemTail*>(smem + STAGES * kStageBytes);
+  auto stage_a = [&](int s) { return smem + s * kStageBytes; };
+  auto stage_b = [&](int s) { return smem + s * kStageBytes + kStageBytesA; };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int tiles_m = (p.M + BM - 1) / BM;
+  const int tiles_n = (p.N + BN - 1) / BN;
+  const int num_tiles = tiles_m * tiles_n;
+  const int num_kb = (p.K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&tail->full[s], T::kFullCount);
+      mbar_init(&tail->empty[s], kComputeThreads);
+    }
+    tail->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (MODE_A == kLoadTma && threadIdx.x == kComputeThreads) tma_prefetch_desc(&tmA);
+  if (MODE_B == kLoadTma && threadIdx.x == kComputeThreads) tma_prefetch_desc(&tmB);
+  __syncthreads();
+  volatile int* abort_flag = &tail->abort_flag;
+
+  if (warp >= kComputeWarps) {
+    // ------------------------------------------------------------ producers
+    const int ptid = threadIdx.x - kComputeThreads;
+    const bool tma_issuer = (ptid == 0) && T::kAnyTma;
+    if (!T::kAnyGeneric && ptid != 0) return;
+    uint32_t it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      int tm, tn;
+      tile_coords(t, tiles_m, tiles_n, tm, tn);
+      for (int kb = 0; kb < num_kb; ++kb, ++it) {
+        const int s = it % STAGES;
+        const uint32_t round = it / STAGES;
+        if (!mbar_wait(&tail->empty[s], (round & 1u) ^ 1u, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        if (tma_issuer) {
+          mbar_arrive_expect_tx(&tail->full[s], T::kTmaBytes);
+          if (MODE_A == kLoadTma) tma_load_2d(stage_a(s), &tmA, kb * BK, tm * BM, &tail->full[s]);
+          if (MODE_B == kLoadTma) tma_load_2d(stage_b(s), &tmB, tn * BN, kb * BK, &tail->full[s]);
+        }
+        if (T::kAnyGeneric) {
+          if (MODE_A == kLoadCpAsyncF32)
+            load_a_cpasync(stage_a(s), static_cast<const float*>(p.A), p.lda, p.M, p.K, tm * BM,
+                           kb * BK, ptid);
+          if (MODE_B == kLoadCpAsyncF32)
+            load_b_cpasync(stage_b(s), static_cast<const float*>(p.B), p.ldb, p.N, p.K, tn * BN,
+                           kb * BK, ptid);
+          if (MODE_A == kLoadConvertBf16)
+            load_a_bf16(stage_a(s), static_cast<const uint16_t*>(p.A), p.lda, p.M, p.K, tm * BM,
+                        kb * BK, ptid);
+          if (MODE_B == kLoadConvertBf16)
+            load_b_bf16(stage_b(s), static_cast<const uint16_t*>(p.B), p.ldb, p.N, p.K, tn * BN,
+                        kb * BK, ptid);
+          if (MODE_A == kLoadCpAsyncF32 || MODE_B == kLoadCpAsyncF32)
+            cp_async_mbar_arrive_noinc(&tail->full[s]);
+          else
+            mbar_arrive(&tail->full[s]);
+        }
+      }
+    }
+    if (!ok) {
+      // Drain this CTA's own copies still in flight before it may exit.
+      if (T::kAnyGeneric) cp_async_wait_all();
+      if (tma_issuer) {
+        const uint32_t first = it > STAGES ? it - STAGES : 0u;
+        for (uint32_t j = first; j < it; ++j) mbar_drain_wait(&tail->full[j % STAGES], (j / STAGES) & 1u);
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- compute
+  const int wm = warp >> 1, wn = warp & 1;
+  const int rg = lane >> 3, cg = lane & 7;
+  uint32_t it = 0;
+  for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+    int tm, tn;
+    tile_coords(t, tiles_m, tiles_n, tm, tn);
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+    for (int kb = 0; kb < num_kb; ++kb, ++it) {
+      const int s = it % STAGES;
+      const uint32_t round = it / STAGES;
+      if (!mbar_wait(&tail->full[s], round & 1u, abort_flag, p.err)) return;
+      compute_stage(stage_a(s), stage_b(s), acc, wm, wn, rg, cg);
+      mbar_arrive(&tail->empty[s]);
+    }
+    epilogue(p, acc, tm, tn, wm, wn, rg, cg);
+  }
+}
+
+template <int MODE_A, int MODE_B>
+cudaError_t launch_variant(const SimtArgs& a, const CUtensorMap* tmA, const CUtensorMap* tmB,
+                           int num_sms, cudaStream_t stream) {
+  using T = SimtTraits<MODE_A, MODE_B>;
+  auto kernel = simt_gemm_kernel<MODE_A, MODE_B>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kSmemBytes));
+  if (e != cudaSuccess) return e;
+  const int tiles = ((a.M + BM - 1) / BM) * ((a.N + BN - 1) / BN);
+  const int grid = tiles < num_sms ? tiles : num_sms;
+  CUtensorMap dummy{};
+  kernel<<<grid, T::kThreads, kSmemBytes, stream>>>(a, tmA ? *tmA : dummy, tmB ? *tmB : dummy);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_simt(const SimtArgs& a, LoadMode mode_a, LoadMode mode_b,
+                        const CUtensorMap* tmA, const CUtensorMap* tmB, int num_sms,
+                        cudaStream_t stream) {
+  if (mode_a == kLoadTma && mode_b == kLoadTma)
+    return launch_variant<kLoadTma, kLoadTma>(a, tmA, tmB, num_sms, stream);
+  if (mode_a == kLoadCpAsyncF32 && mode_b == kLoadTma)
+    return launch_variant<kLoadCpAsyncF32, kLoadTma>(a, tmA, tmB, num_sms, stream);
+  if (mode_a == kLoadTma && mode_b == kLoadCpAsyncF32)
+    return launch_variant<kLoadTma, kLoadCpAsyncF32>(a, tmA, tmB, num_sms, stream);
+  if (mode_a == kLoadCpAsyncF32 && mode_b == kLoadCpAsyncF32)
+    return launch_variant<kLoadCpAsyncF32, kLoadCpAsyncF32>(a, tmA, tmB, num_sms, stream);
+  if (mode_a == kLoadConvertBf16 && mode_b == kLoadConvertBf16)
+    return launch_variant<kLoadConvertBf16, kLoadConvertBf16>(a, tmA, tmB, num_sms, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace g12

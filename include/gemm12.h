@@ -1,0 +1,185 @@
+/*
+ * gemm12.h -- C ABI of the GB300 (sm_103a) dense GEMM library.
+ *
+ * Operation (both entry points):
+ *
+ *     C  <-  alpha * (A x B) + beta * C
+ *
+ * with A an M x K matrix, B a K x N matrix and C an M x N matrix, as defined
+ * in "GEMM Worklog I: Naive to Tiled" (opening equation) and used as the
+ * single SGEMM call of "A GEMM Kernel, Step by Step" ("The ladder we are
+ * climbing").  The pages' own host function takes (M, N, K, A, B, C, stream)
+ * with dense row-major operands ("Tiled matrix multiplication", section
+ * "Code"); this interface adds the scalars and leading dimensions.
+ *
+ * Conventions shared by every entry point below:
+ *
+ *  Layout     All matrices are ROW-MAJOR.  Element (i, k) of A is at
+ *             A[i * lda + k], element (k, j) of B at B[k * ldb + j] and
+ *             element (i, j) of C at C[i * ldc + j].  Requirements:
+ *             M, N, K >= 0; lda >= max(1, K); ldb >= max(1, N);
+ *             ldc >= max(1, N).  Each of M, N, K, lda, ldb, ldc must be below
+ *             2^31.  A violation returns GEMM_ERR_INVALID_VALUE and launches
+ *             nothing.
+ *  Pointers   A, B and C are DEVICE pointers (global memory of the current
+ *             device), owned by the caller; the library never frees them.
+ *             NULL is accepted only for an operand that is not read:
+ *             A and B when M, N or K is 0 or alpha == 0; C when M or N is 0.
+ *  Scalars    beta == 0: C is write-only (its old contents, NaN included, do
+ *             not reach the result).  alpha == 0 or K == 0: A and B are not
+ *             read and C <- beta * C (C <- 0 when beta == 0 too).  M == 0 or
+ *             N == 0: nothing is launched.
+ *  Alignment  None is required beyond the element size.  Operands whose
+ *             address or leading dimension the tensor-memory-accelerator
+ *             (TMA) copy engine cannot describe (base not 16-byte aligned,
+ *             row pitch not a multiple of 16 bytes) take generic-load kernels
+ *             instead; this changes speed, not the result's error bound.
+ *             A bf16 pointer that is not 2-byte aligned returns
+ *             GEMM_ERR_MISALIGNED.
+ *  Aliasing   C must not overlap A or B (not checked).
+ *  Streams    `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *             Calls are asynchronous: they enqueue kernels and return.  Launch
+ *             failures are reported as GEMM_ERR_LAUNCH; errors raised later
+ *             by the device are reported by the CUDA runtime at the next
+ *             synchronising call, and a kernel's bounded waits that ran out
+ *             are reported by gemm_check_device_error().
+ *  Threads    Entry points may be called from several host threads on
+ *             different streams.
+ *  Memory     gemm_sgemm never allocates.  gemm_bf16gemm allocates, on its
+ *             first decode-shaped call per device (M <= 16), a split-K
+ *             workspace and arrival counters that it keeps and reuses;
+ *             gemm_shutdown() frees them.  Concurrent decode-shaped calls on
+ *             different streams of the same device are serialised on the
+ *             host but must not overlap on the device (they share the
+ *             workspace).  Allocation failure returns GEMM_ERR_NO_MEMORY.
+ */
+#ifndef GEMM12_H
+#define GEMM12_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_VALUE = 1,   /* bad size, leading dimension or NULL   */
+    GEMM_ERR_MISALIGNED = 2,      /* bf16 pointer not 2-byte aligned        */
+    GEMM_ERR_UNSUPPORTED = 3,     /* no sm_103a device, or size too large   */
+    GEMM_ERR_LAUNCH = 4,          /* kernel launch or CUDA runtime error    */
+    GEMM_ERR_DEVICE_TIMEOUT = 5,  /* a bounded device wait ran out          */
+    GEMM_ERR_NO_MEMORY = 6        /* workspace allocation failed            */
+} gemm_status_t;
+
+/*
+ * gemm_sgemm -- fp32 SGEMM, C <- alpha*(A x B) + beta*C.
+ *
+ * A: M x K fp32 (lda), B: K x N fp32 (ldb), C: M x N fp32 (ldc), all device
+ * pointers, row-major.  Products are accumulated in fp32 with fused
+ * multiply-adds on the CUDA cores (the register-tiled outer-product scheme of
+ * "Tiled matrix multiplication", "How it works", and of "A GEMM Kernel, Step
+ * by Step", "Rungs four and five" and "The last rung").  The error against the
+ * exact result is within 2e-6 * sqrt(K) of |alpha|*(|A||B|)_ij +
+ * |beta|*|C_ij| per element; on integer-valued inputs whose partial sums stay
+ * below 2^24 in magnitude the result is exact.
+ */
+gemm_status_t gemm_sgemm(int64_t M, int64_t N, int64_t K, float alpha,
+                         const float *A, int64_t lda,
+                         const float *B, int64_t ldb,
+                         float beta, float *C, int64_t ldc, void *stream);
+
+/*
+ * gemm_bf16gemm -- bf16 inputs, fp32 accumulation, fp32 output:
+ * C <- alpha*(A x B) + beta*C.
+ *
+ * A: M x K bf16 (__nv_bfloat16 / uint16 bit patterns, lda), B: K x N bf16
+ * (ldb), C: M x N fp32 (ldc), device pointers, row-major.  The tensor-core
+ * path ("Tiled matrix multiplication", "How it works": tensor cores fed from
+ * shared memory by asynchronous copies) runs on the 5th-generation tensor
+ * cores with the accumulator in tensor memory.  M <= 16 takes the
+ * bandwidth-bound decode kernel (the "decode GEMV (M <= 16)" case of "Tiled
+ * matrix multiplication", "Avoid when"), which splits K across CTAs
+ * ("Split-K" in the same page's "Variants and alternatives") and reduces the
+ * partial sums in a fixed order, so results are deterministic.  Error bound:
+ * 8e-3 of |alpha|*(|A||B|)_ij + |beta|*|C_ij| against the exact product of the
+ * bf16 values.
+ */
+gemm_status_t gemm_bf16gemm(int64_t M, int64_t N, int64_t K, float alpha,
+                            const void *A, int64_t lda,
+                            const void *B, int64_t ldb,
+                            float beta, float *C, int64_t ldc, void *stream);
+
+/* Static, NUL-terminated description of a status code (never NULL). */
+const char *gemm_status_string(gemm_status_t status);
+
+/*
+ * gemm_check_device_error -- synchronise `stream`, then read and clear the
+ * current device's error word, which the kernels set when one of their
+ * bounded waits (on an mbarrier or on another CTA) runs out.  Returns
+ * GEMM_ERR_DEVICE_TIMEOUT if it was set, GEMM_ERR_LAUNCH if the
+ * synchronisation itself failed, else GEMM_OK.
+ */
+gemm_status_t gemm_check_device_error(void *stream);
+
+/* Free the per-device decode workspaces.  Call with no GEMM in flight. */
+gemm_status_t gemm_shutdown(void);
+
+/* Kernel paths a call can take (reported by gemm_select_path). */
+typedef enum {
+    GEMM_PATH_NONE = 0,           /* M == 0 or N == 0: nothing launched     */
+    GEMM_PATH_SCALE_C = 1,        /* alpha == 0 or K == 0: C <- beta*C      */
+    GEMM_PATH_SIMT_TMA = 2,       /* fp32 CUDA-core kernel, TMA operands    */
+    GEMM_PATH_SIMT_GENERIC = 3,   /* fp32 CUDA-core kernel, generic loads   */
+    GEMM_PATH_TC_BF16 = 4,        /* bf16 tensor-core (tcgen05) kernel      */
+    GEMM_PATH_TC_DECODE = 5,      /* bf16 tensor-core split-K decode kernel */
+    GEMM_PATH_SIMT_BF16 = 6       /* bf16 operands TMA cannot describe:
+                                     widened to fp32 on the CUDA cores     */
+} gemm_path_t;
+
+/*
+ * gemm_select_path -- host-only: the kernel path a call with these arguments
+ * takes.  `is_bf16` selects gemm_bf16gemm's rules instead of gemm_sgemm's.
+ * Pointers are only inspected for alignment, never dereferenced.  Returns
+ * GEMM_PATH_NONE (and writes nothing) for arguments the call would reject.
+ */
+gemm_path_t gemm_select_path(int is_bf16, int64_t M, int64_t N, int64_t K,
+                             float alpha, const void *A, int64_t lda,
+                             const void *B, int64_t ldb);
+
+/*
+ * Tile and wave quantization of a launch ("A GEMM Kernel, Step by Step",
+ * "The fringe and the last wave"; "Tiled matrix multiplication",
+ * "Complexity and constants", wave quantization).
+ */
+typedef struct {
+    int64_t tiles_m;        /* ceil(M / BM)                                 */
+    int64_t tiles_n;        /* ceil(N / BN)                                 */
+    int64_t tiles;          /* tiles_m * tiles_n                            */
+    int64_t covered_m;      /* tiles_m * BM: rows the tile grid covers      */
+    int64_t covered_n;      /* tiles_n * BN                                 */
+    double useful_fraction; /* (M * N) / (covered_m * covered_n)            */
+    int64_t per_wave;       /* num_sms * ctas_per_sm                        */
+    int64_t waves;          /* ceil(tiles / per_wave)                       */
+    double wave_efficiency; /* tiles / (waves * per_wave)                   */
+} gemm_quantization_t;
+
+/*
+ * gemm_quantization -- host-only, pure arithmetic: fill `out` for an M x N
+ * output cut into BM x BN tiles on `num_sms` multiprocessors holding
+ * `ctas_per_sm` blocks each.  Returns GEMM_ERR_INVALID_VALUE for negative
+ * sizes or non-positive tile sizes / slots or a NULL `out`.  For M == 0 or
+ * N == 0 the fractions are 1 and the counts 0.
+ */
+gemm_status_t gemm_quantization(int64_t M, int64_t N, int64_t BM, int64_t BN,
+                                int64_t num_sms, int64_t ctas_per_sm,
+                                gemm_quantization_t *out);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int gemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM12_H */
