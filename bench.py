@@ -49,12 +49,14 @@ MAX_SM_CLOCK_HZ = 2.07e9   # GB300 maximum SM clock
 def parse_args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-parts", action="store_true", help="headline workload only")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--only", choices=["sgemm", "bf16", "decode"], default=None,
+                   help="time one kernel's workload alone (profiling runs); prints its part")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target duration of the CPU-oracle sample")
     return p.parse_args()
@@ -90,7 +92,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu_index), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -251,17 +253,18 @@ def bench_decode(torch, g, wl, peaks, device, stream_obj):
             step(i, cap.cuda_stream)
         graph.capture_end()
     torch.cuda.synchronize()
-    graph.replay()
-    torch.cuda.synchronize()
     trial_ms = []
-    for _ in range(5):
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record(cap)
+    with torch.cuda.stream(cap):   # replay() launches on the current stream
         graph.replay()
-        b.record(cap)
         torch.cuda.synchronize()
-        trial_ms.append(a.elapsed_time(b) / reps)
+        for _ in range(5):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(cap)
+            graph.replay()
+            b.record(cap)
+            torch.cuda.synchronize()
+            trial_ms.append(a.elapsed_time(b) / reps)
     ms = statistics.median(trial_ms)
     gbs = bytes_alg / (ms * 1e-3) / 1e9
     peak = peaks["hbm_gbs"]
@@ -465,8 +468,42 @@ def run_ours(args):
         pg.destroy_process_group()
 
 
+def run_only(args):
+    """One kernel's workload alone, for profiler captures (not the contract line)."""
+    import torch
+
+    import dense_gemm_12_gb300 as g
+    from dense_gemm_12_gb300 import workloads as wl
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    g.load_library(build_if_missing=True)
+    peaks = load_peaks()
+    stream_obj = torch.cuda.current_stream(device)
+    if args.only == "bf16":
+        out = bench_bf16_8192(torch, g, wl, peaks, device, stream_obj)
+    elif args.only == "decode":
+        out = bench_decode(torch, g, wl, peaks, device, stream_obj)
+    else:
+        w = wl.WORKLOADS["sgemm_4092"]
+        w2 = wl.Workload(**{**w.__dict__, "seed": w.seed + 100, "name": "sgemm_4092_b"})
+        sets = [tuple(t.to(device) for t in wl.workload_inputs(x)) for x in (w, w2)]
+        step = sgemm_step_fn(g, sets, w, stream_obj.cuda_stream)
+        for i in range(args.warmup):
+            step(i)
+        ms = time_launches(torch, step, args.steps, stream_obj)
+        out = {"workload": "fp32 SGEMM 4092^3", "ms_per_launch": ms,
+               "gflops_median": w.flops / (statistics.median(ms) * 1e-3) / 1e9}
+    st = g.gemm_check_device_error(stream_obj.cuda_stream)
+    if st != 0:
+        raise RuntimeError("device error: " + g.gemm_status_string(st))
+    print(json.dumps({"only": args.only, **out}), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.only:
+        run_only(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -11,19 +11,22 @@
 // 128 columns of C and its N (16) over the rows of A, and no row of the MMA
 // is padding.
 //
-// Work split.  The (n-tile, k-block) units -- 128 columns x 64 k each -- are
-// numbered n-tile-major and every CTA takes one contiguous, equal-sized run of
-// them, so each SM streams the same number of bytes of B (no last wave).  A
-// run is cut into segments at n-tile boundaries.  A segment that spans the
-// whole k range of its n-tile writes C directly; otherwise it stores its
-// 128 x 16 fp32 partial in the workspace and bumps the n-tile's arrival
-// counter, and the CTA that arrives last adds the partials in k order (a
-// fixed order, so results are deterministic), applies alpha/beta, writes C and
-// resets the counter to zero for the next launch.
+// Work split.  B is cut into n-groups of NSUB x 128 columns; a unit is one
+// n-group x 64 values of k.  Units are numbered n-group-major and every CTA
+// takes one contiguous, equal-sized run of them, so each SM streams the same
+// number of bytes of B (no last wave), and every k-row of a unit is a
+// contiguous NSUB x 256-byte stretch of memory.  A run is cut into segments at
+// n-group boundaries.  A segment that spans the whole k range of its n-group
+// writes C directly; otherwise it stores its NW x 16 fp32 partial in the
+// workspace and bumps the n-group's arrival counter, and the CTA that arrives
+// last adds the partials in k order (a fixed order, so results are
+// deterministic), applies alpha/beta, writes C and resets the counter to zero
+// for the next launch.
 //
-// Roles: warp 0 TMA producer (two 64-column MN-major boxes of B and a 16 x 64
-// K-major box of A per stage), warp 1 TMEM owner and MMA issuer (128 x 16 x 16
-// MMAs, two accumulators), warps 2..5 epilogue / fix-up.
+// Roles: warp 0 TMA producer (2 x NSUB 64-column MN-major boxes of B and one
+// 16 x 64 K-major box of A per stage), warp 1 TMEM owner and MMA issuer
+// (128 x 16 x 16 MMAs, NSUB accumulators per segment, double-buffered),
+// warps 2..5 epilogue / fix-up.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -34,19 +37,43 @@
 namespace g12 {
 namespace {
 
-constexpr int BN = kDecBN;   // MMA M: columns of C per n-tile
-constexpr int BMr = kDecBM;  // MMA N: rows of A / C
+#ifndef G12_DECODE_NSUB
+#define G12_DECODE_NSUB 1
+#endif
+
+constexpr int BN = kDecBN;                 // MMA M: 128 columns of C per MMA tile
+constexpr int NSUB = G12_DECODE_NSUB;      // MMA tiles per n-group
+constexpr int NW = NSUB * BN;              // columns of C per n-group
+constexpr int BMr = kDecBM;                // MMA N: rows of A / C
 constexpr int BK = kDecBK;
-constexpr int STAGES = 8;
-constexpr int kStageBytesB = BK * BN * 2;   // 16 KB: two 64-column boxes
-constexpr int kBoxBytesB = BK * 64 * 2;     // 8 KB
-constexpr int kStageBytesA = BMr * BK * 2;  // 2 KB
-constexpr int kStageBytes = kStageBytesB + kStageBytesA;  // 18 KB (multiple of 1024)
+constexpr int kBoxBytesB = BK * 64 * 2;                   // one 64-column box, 8 KB
+constexpr int kStageBytesB = NSUB * 2 * kBoxBytesB;       // NSUB x 16 KB
+constexpr int kStageBytesA = BMr * BK * 2;                // 2 KB
+constexpr int kStageBytes = kStageBytesB + kStageBytesA;  // multiple of 1024
+#ifndef G12_DECODE_SMEM_KB
+#define G12_DECODE_SMEM_KB 200
+#endif
+#ifndef G12_DECODE_CTAS_PER_SM
+#define G12_DECODE_CTAS_PER_SM 1
+#endif
+#ifndef G12_DECODE_EARLY_UNITS
+#define G12_DECODE_EARLY_UNITS 2
+#endif
+constexpr int kCtasPerSm = G12_DECODE_CTAS_PER_SM;
+// Units of B each CTA asks L2 to fetch before it waits for the previous
+// kernel in the stream (more would delay its own first TMA loads).
+constexpr int kEarlyUnits = G12_DECODE_EARLY_UNITS;
+constexpr int kStageBudget = (G12_DECODE_SMEM_KB * 1024) / kStageBytes;
+constexpr int STAGES = kStageBudget > 10 ? 10 : kStageBudget;
 constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
-constexpr uint32_t kTmemCols = 32;
+constexpr uint32_t kAccCols = NSUB * BMr;                 // TMEM columns per segment
+constexpr uint32_t kTmemCols = 2 * kAccCols < 32 ? 32 : 2 * kAccCols;
 constexpr uint32_t kIdesc = idesc_bf16_f32(BN, BMr, /*A MN-major*/ 1, /*B MN-major*/ 0);
-constexpr int kPartialFloats = BMr * BN;    // 2048
+constexpr int kPartialFloats = BMr * NW;
+
+static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
+static_assert((kTmemCols & (kTmemCols - 1)) == 0, "TMEM allocation must be a power of 2");
 
 struct __align__(8) DecSmemTail {
   uint64_t full[STAGES];
@@ -57,29 +84,30 @@ struct __align__(8) DecSmemTail {
   uint32_t tmem_base;
   int abort_flag;
   int last_flag;
+  int others_ready;  // set once every other contributor of the segment's group has published
 };
 
 constexpr size_t kSmemBytes = 1024 + STAGES * kStageBytes + sizeof(DecSmemTail);
 
 struct Split {
-  int64_t units;       // n_tiles * kb_total
-  int kb_total;        // k-blocks per n-tile
+  int64_t units;       // n_groups * kb_total
+  int kb_total;        // k-blocks per n-group
   int grid;            // CTAs
   int segs_max;        // segment slots per CTA in the workspace
 };
 
 __host__ __device__ inline Split make_split(int N, int K, int grid) {
   Split s;
-  const int n_tiles = (N + BN - 1) / BN;
+  const int n_groups = (N + NW - 1) / NW;
   s.kb_total = (K + BK - 1) / BK;
-  s.units = static_cast<int64_t>(n_tiles) * s.kb_total;
+  s.units = static_cast<int64_t>(n_groups) * s.kb_total;
   s.grid = grid;
   const int64_t per_cta = (s.units + grid - 1) / grid;
   s.segs_max = static_cast<int>((per_cta + s.kb_total - 1) / s.kb_total) + 1;
   return s;
 }
 
-__device__ __forceinline__ int64_t run_start(const Split& s, int64_t c) {
+__host__ __device__ inline int64_t run_start(const Split& s, int64_t c) {
   return (c * s.units) / s.grid;
 }
 
@@ -92,12 +120,32 @@ __device__ __forceinline__ void named_bar_epi() {
   asm volatile("bar.sync 1, %0;" ::"r"(kEpiThreads) : "memory");
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+// Old values of column n of C (rows < M), loaded ahead of time so that the
+// final write of a column costs no read round trip.
+__device__ __forceinline__ void load_c_column(const DecodeArgs& p, int n, float (&old)[BMr]) {
+#pragma unroll
+  for (int m = 0; m < BMr; ++m)
+    old[m] = (p.beta != 0.0f && n < p.N && m < p.M) ? p.C[static_cast<int64_t>(m) * p.ldc + n]
+                                                     : 0.0f;
+}
+
+// C[m][n] = alpha * v[m] + beta * old[m] for the column n of this thread.
+__device__ __forceinline__ void store_c_column(const DecodeArgs& p, int n, const float (&v)[BMr],
+                                               const float (&old)[BMr]) {
+  if (n >= p.N) return;
+  float* c = p.C + n;
+#pragma unroll
+  for (int m = 0; m < BMr; ++m)
+    if (m < p.M)
+      c[static_cast<int64_t>(m) * p.ldc] =
+          (p.beta != 0.0f) ? fmaf(p.alpha, v[m], p.beta * old[m]) : p.alpha * v[m];
+}
+
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
     tc_decode_kernel(const DecodeArgs p, const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = align_smem<1024>(smem_raw);
   DecSmemTail* tail = reinterpret_cast<DecSmemTail*>(smem + STAGES * kStageBytes);
   volatile int* abort_flag = &tail->abort_flag;
 
@@ -119,6 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&tail->drain, 1);
     tail->abort_flag = 0;
     tail->last_flag = 0;
+    tail->others_ready = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
@@ -127,10 +176,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(&tail->tmem_base, kTmemCols);
     tmem_relinquish_alloc_permit();
   }
+  // Under programmatic dependent launch this prologue may run while the
+  // previous kernel in the stream is still finishing.  Before waiting for it,
+  // ask L2 for the first tiles of B this CTA will stream: an L2 prefetch is
+  // only a hint and L2 is the coherence point, so it cannot return stale data
+  // even if the previous kernel writes B.  Every other global access comes
+  // after grid_dependency_wait().
+  if (warp == 0 && lane == 0) {
+    for (int64_t v = u_begin; v < u_end && v < u_begin + kEarlyUnits; ++v) {
+      const int png = static_cast<int>(v / sp.kb_total);
+      const int pkb = static_cast<int>(v - static_cast<int64_t>(png) * sp.kb_total);
+#pragma unroll
+      for (int b = 0; b < 2 * NSUB; ++b) tma_prefetch_l2_2d(&tmB, png * NW + b * 64, pkb * BK);
+    }
+  }
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = tail->tmem_base;
+  grid_dependency_wait();
 
   if (warp == 0) {
     // -------------------------------------------------------- TMA producer
@@ -138,8 +202,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t it = 0;
       bool ok = true;
       for (int64_t u = u_begin; u < u_end; ++u, ++it) {
-        const int nt = static_cast<int>(u / sp.kb_total);
-        const int kb = static_cast<int>(u - static_cast<int64_t>(nt) * sp.kb_total);
+        const int ng = static_cast<int>(u / sp.kb_total);
+        const int kb = static_cast<int>(u - static_cast<int64_t>(ng) * sp.kb_total);
         const int s = it % STAGES;
         const uint32_t round = it / STAGES;
         if (!mbar_wait(&tail->empty[s], (round & 1u) ^ 1u, abort_flag, p.err)) {
@@ -149,10 +213,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* sb = smem + s * kStageBytes;
         uint8_t* sa = sb + kStageBytesB;
         mbar_arrive_expect_tx(&tail->full[s], kStageBytes);
-        tma_load_2d(sb, &tmB, nt * BN, kb * BK, &tail->full[s]);
-        tma_load_2d(sb + kBoxBytesB, &tmB, nt * BN + 64, kb * BK, &tail->full[s]);
+#pragma unroll
+        for (int b = 0; b < 2 * NSUB; ++b)
+          tma_load_2d(sb + b * kBoxBytesB, &tmB, ng * NW + b * 64, kb * BK, &tail->full[s]);
         tma_load_2d(sa, &tmA, kb * BK, 0, &tail->full[s]);
       }
+      // This CTA has issued all its loads: the next kernel in the stream may
+      // start launching (it waits for this grid's completion before use).
+      grid_launch_dependents();
       if (!ok) {
         const uint32_t first = it > STAGES ? it - STAGES : 0u;
         for (uint32_t j = first; j < it; ++j)
@@ -167,15 +235,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true, issued = false;
       int64_t u = u_begin;
       while (u < u_end && ok) {
-        const int nt = static_cast<int>(u / sp.kb_total);
-        const int64_t seg_end_u = min(u_end, static_cast<int64_t>(nt + 1) * sp.kb_total);
+        const int ng = static_cast<int>(u / sp.kb_total);
+        const int64_t seg_end_u = min(u_end, static_cast<int64_t>(ng + 1) * sp.kb_total);
         const uint32_t ab = seg & 1u, ar = seg >> 1;
         if (!mbar_wait(&tail->tmem_empty[ab], (ar & 1u) ^ 1u, abort_flag, p.err)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
-        const uint32_t d_tmem = tmem_base + ab * BMr;
+        const uint32_t d_tmem = tmem_base + ab * kAccCols;
         bool first = true;
         for (; u < seg_end_u; ++u, ++it) {
           const int s = it % STAGES;
@@ -189,13 +257,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sa = sb + kStageBytesB;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            // MMA A operand = B^T tile: MN-major, two 64-column boxes 8 KB
-            // apart (LBO), 8-row k groups 1024 B apart (SBO), k step 2048 B.
-            const uint64_t adesc = smem_desc_sw128(sb + kk * 2048, kBoxBytesB, 1024);
             // MMA B operand = A^T tile: K-major, 8-row groups 1024 B apart,
             // k step of 16 elements = 32 B.
             const uint64_t bdesc = smem_desc_sw128(sa + kk * 32, 16, 1024);
-            tc_mma_f16(d_tmem, adesc, bdesc, kIdesc, (first && kk == 0) ? 0u : 1u);
+#pragma unroll
+            for (int j = 0; j < NSUB; ++j) {
+              // MMA A operand = B^T tile j: MN-major, its two 64-column boxes
+              // 8 KB apart (LBO), 8-row k groups 1024 B apart (SBO), k step
+              // of 16 rows = 2048 B.
+              const uint64_t adesc =
+                  smem_desc_sw128(sb + j * 2 * kBoxBytesB + kk * 2048, kBoxBytesB, 1024);
+              tc_mma_f16(d_tmem + j * BMr, adesc, bdesc, kIdesc,
+                         (first && kk == 0) ? 0u : 1u);
+            }
           }
           first = false;
           issued = true;
@@ -214,76 +288,153 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // -------------------------------------------------------- epilogue
     const int quarter = warp & 3;
-    const int n_local = quarter * 32 + lane;
-    const int ept = threadIdx.x - 64;  // 0..127
+    const int n_local = quarter * 32 + lane;  // row of each MMA tile = column of C
+    const int ept = threadIdx.x - 64;         // 0..127
     uint32_t seg = 0;
     int64_t u = u_begin;
     while (u < u_end) {
-      const int nt = static_cast<int>(u / sp.kb_total);
-      const int64_t tile_u0 = static_cast<int64_t>(nt) * sp.kb_total;
-      const int64_t tile_u1 = tile_u0 + sp.kb_total;
-      const int64_t seg_end_u = min(u_end, tile_u1);
-      const bool whole = (u == tile_u0) && (seg_end_u == tile_u1);
+      const int ng = static_cast<int>(u / sp.kb_total);
+      const int64_t grp_u0 = static_cast<int64_t>(ng) * sp.kb_total;
+      const int64_t grp_u1 = grp_u0 + sp.kb_total;
+      const int64_t seg_end_u = min(u_end, grp_u1);
+      const bool whole = (u == grp_u0) && (seg_end_u == grp_u1);
+      const int64_t c_first = run_owner(sp, grp_u0);
+      const int64_t c_last = run_owner(sp, grp_u1 - 1);
+      const uint32_t nsegs = static_cast<uint32_t>(c_last - c_first + 1);
+      // While the MMAs of this segment run: fetch the old C values this
+      // thread may have to combine with, and watch whether every other
+      // contributor of the n-group has already published its partial sums --
+      // if so, preload them, so that once this segment's accumulator is ready
+      // the group's result is a few adds away.
+      float old[NSUB][BMr];
+#pragma unroll
+      for (int j = 0; j < NSUB; ++j) load_c_column(p, ng * NW + j * BN + n_local, old[j]);
+      constexpr int kPre = 2;  // partial sums of other CTAs held in registers
+      float pre[kPre][NSUB][BMr];
+      bool preloaded = false;
+      const bool can_preload = !whole && (nsegs - 1 <= static_cast<uint32_t>(kPre));
+      auto preload = [&]() {
+        // the kk-th contributor other than this CTA, in CTA order
+#pragma unroll
+        for (int kk = 0; kk < kPre; ++kk) {
+          int64_t cc = c_first + kk;
+          if (cc >= blockIdx.x) ++cc;
+          if (cc > c_last) break;
+          const int sl = static_cast<int>(ng - run_start(sp, cc) / sp.kb_total);
+          const float* src = p.workspace + (cc * sp.segs_max + sl) * kPartialFloats;
+#pragma unroll
+          for (int j = 0; j < NSUB; ++j)
+#pragma unroll
+            for (int m = 0; m < BMr; ++m) pre[kk][j][m] = __ldcg(src + m * NW + j * BN + n_local);
+        }
+      };
+
       const uint32_t ab = seg & 1u, ar = seg >> 1;
-      if (!mbar_wait(&tail->tmem_full[ab], ar & 1u, abort_flag, p.err)) break;
+      bool ok = true;
+      if (!mbar_try_wait(&tail->tmem_full[ab], ar & 1u)) {
+        const uint64_t t0 = globaltimer_ns();
+        uint32_t spins = 0;
+        while (!mbar_try_wait(&tail->tmem_full[ab], ar & 1u)) {
+          if ((++spins & 15u) != 0) continue;
+          if (*abort_flag) { ok = false; break; }
+          if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            atomicOr(p.err, kErrWaitTimeout);
+            ok = false;
+            break;
+          }
+          if (!whole && ept == 0 && !tail->others_ready &&
+              ld_acquire_gpu(p.counters + ng) == nsegs - 1)
+            st_release_cta_shared(&tail->others_ready, 1);
+          if (can_preload && !preloaded && ld_acquire_cta_shared(&tail->others_ready)) {
+            preload();
+            preloaded = true;
+          }
+        }
+      }
+      if (!ok) break;
       tc_fence_after_sync();
-      uint32_t r[16];
-      tmem_ld_32x32b_x16(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + ab * BMr, r);
+      uint32_t r[NSUB][16];
+#pragma unroll
+      for (int j = 0; j < NSUB; ++j)
+        tmem_ld_32x32b_x16(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                               ab * kAccCols + j * BMr,
+                           r[j]);
       tc_wait_ld();
       tc_fence_before_sync();
       mbar_arrive(&tail->tmem_empty[ab]);
 
-      const int n = nt * BN + n_local;
       if (whole) {
-        if (n < p.N) {
 #pragma unroll
-          for (int m = 0; m < BMr; ++m) {
-            if (m < p.M) {
-              float* c = p.C + static_cast<int64_t>(m) * p.ldc + n;
-              const float v = __uint_as_float(r[m]);
-              *c = (p.beta != 0.0f) ? fmaf(p.alpha, v, p.beta * *c) : p.alpha * v;
-            }
-          }
+        for (int j = 0; j < NSUB; ++j) {
+          float v[BMr];
+#pragma unroll
+          for (int m = 0; m < BMr; ++m) v[m] = __uint_as_float(r[j][m]);
+          store_c_column(p, ng * NW + j * BN + n_local, v, old[j]);
         }
       } else {
-        const int64_t first_u = u_begin;
-        const int seg_local = static_cast<int>(nt - first_u / sp.kb_total);
-        float* slot = p.workspace +
-                      (static_cast<int64_t>(blockIdx.x) * sp.segs_max + seg_local) * kPartialFloats;
-#pragma unroll
-        for (int m = 0; m < BMr; ++m) __stcg(slot + m * BN + n_local, __uint_as_float(r[m]));
-        __threadfence();
-        named_bar_epi();
-        const int64_t c_first = run_owner(sp, tile_u0);
-        const int64_t c_last = run_owner(sp, tile_u1 - 1);
+        // last_flag: 2 = every other contributor had already arrived (this
+        // CTA adds its own sum straight from registers and publishes nothing),
+        // 1 = this CTA's arrival was the last one, 0 = another CTA finishes.
         if (ept == 0) {
-          const uint32_t nsegs = static_cast<uint32_t>(c_last - c_first + 1);
-          const uint32_t before = atomicAdd(p.counters + nt, 1u);
-          tail->last_flag = (before == nsegs - 1) ? 1 : 0;
+          bool ready = tail->others_ready != 0;
+          if (!ready) ready = ld_acquire_gpu(p.counters + ng) == nsegs - 1;
+          tail->last_flag = ready ? 2 : 0;
         }
         named_bar_epi();
-        if (tail->last_flag) {
-          __threadfence();
-          float sum[BMr];
+        const int mode = tail->last_flag;
+        if (mode != 2) {
+          const int seg_local = static_cast<int>(ng - u_begin / sp.kb_total);
+          float* slot = p.workspace + (static_cast<int64_t>(blockIdx.x) * sp.segs_max + seg_local) *
+                                          kPartialFloats;
 #pragma unroll
-          for (int m = 0; m < BMr; ++m) sum[m] = 0.0f;
-          for (int64_t cc = c_first; cc <= c_last; ++cc) {
-            const int sl = static_cast<int>(nt - run_start(sp, cc) / sp.kb_total);
-            const float* src = p.workspace + (cc * sp.segs_max + sl) * kPartialFloats;
+          for (int j = 0; j < NSUB; ++j)
 #pragma unroll
-            for (int m = 0; m < BMr; ++m) sum[m] += __ldcg(src + m * BN + n_local);
+            for (int m = 0; m < BMr; ++m)
+              __stcg(slot + m * NW + j * BN + n_local, __uint_as_float(r[j][m]));
+          named_bar_epi();
+          if (ept == 0) {
+            __threadfence();  // publish the whole CTA's partial before arriving
+            const uint32_t before = atomicAdd(p.counters + ng, 1u);
+            tail->last_flag = (before == nsegs - 1) ? 1 : 0;
           }
-          if (n < p.N) {
+          named_bar_epi();
+        }
+        const int fin = tail->last_flag;
+        if (fin) {
+          if (fin == 1) __threadfence();  // acquire the other partials after the atomic
+          const bool use_pre = (fin == 2) && preloaded;
 #pragma unroll
-            for (int m = 0; m < BMr; ++m) {
-              if (m < p.M) {
-                float* c = p.C + static_cast<int64_t>(m) * p.ldc + n;
-                *c = (p.beta != 0.0f) ? fmaf(p.alpha, sum[m], p.beta * *c) : p.alpha * sum[m];
+          for (int j = 0; j < NSUB; ++j) {
+            // add the partial sums in k order (CTA order), whoever arrived last
+            float sum[BMr];
+#pragma unroll
+            for (int m = 0; m < BMr; ++m) sum[m] = 0.0f;
+            int k = 0;
+            for (int64_t cc = c_first; cc <= c_last; ++cc) {
+              if (cc == blockIdx.x) {
+#pragma unroll
+                for (int m = 0; m < BMr; ++m) sum[m] += __uint_as_float(r[j][m]);
+              } else if (use_pre) {
+#pragma unroll
+                for (int kk = 0; kk < kPre; ++kk)
+                  if (kk == k)
+#pragma unroll
+                    for (int m = 0; m < BMr; ++m) sum[m] += pre[kk][j][m];
+                ++k;
+              } else {
+                const int sl = static_cast<int>(ng - run_start(sp, cc) / sp.kb_total);
+                const float* src = p.workspace + (cc * sp.segs_max + sl) * kPartialFloats;
+#pragma unroll
+                for (int m = 0; m < BMr; ++m) sum[m] += __ldcg(src + m * NW + j * BN + n_local);
               }
             }
+            store_c_column(p, ng * NW + j * BN + n_local, sum, old[j]);
           }
-          if (ept == 0) p.counters[nt] = 0u;
+          if (ept == 0) p.counters[ng] = 0u;
         }
+        if (ept == 0) tail->others_ready = 0;
+        named_bar_epi();  // last_flag / others_ready are rewritten by the next segment
       }
       u = seg_end_u;
       ++seg;
@@ -299,8 +450,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 int decode_grid(int N, int K, int num_sms) {
-  const int64_t units = static_cast<int64_t>((N + BN - 1) / BN) * ((K + BK - 1) / BK);
-  return static_cast<int>(units < num_sms ? units : num_sms);
+  const int64_t units = static_cast<int64_t>((N + NW - 1) / NW) * ((K + BK - 1) / BK);
+  const int64_t slots = static_cast<int64_t>(num_sms) * kCtasPerSm;
+  return static_cast<int>(units < slots ? units : slots);
 }
 
 int64_t decode_workspace_floats(int N, int K, int num_ctas) {
@@ -308,7 +460,7 @@ int64_t decode_workspace_floats(int N, int K, int num_ctas) {
   return static_cast<int64_t>(num_ctas) * s.segs_max * kPartialFloats;
 }
 
-int64_t decode_counter_count(int N) { return (N + BN - 1) / BN; }
+int64_t decode_counter_count(int N) { return (N + NW - 1) / NW; }
 
 cudaError_t launch_tc_decode(const DecodeArgs& a, const CUtensorMap* tmA, const CUtensorMap* tmB,
                              int num_ctas, cudaStream_t stream) {
@@ -316,7 +468,20 @@ cudaError_t launch_tc_decode(const DecodeArgs& a, const CUtensorMap* tmA, const 
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
-  tc_decode_kernel<<<num_ctas, kThreads, kSmemBytes, stream>>>(a, *tmA, *tmB);
+  // Programmatic stream serialization: this launch may begin while the
+  // previous kernel in the stream drains (see grid_dependency_wait).
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(num_ctas);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, tc_decode_kernel, a, *tmA, *tmB);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -71,13 +71,19 @@ __device__ __forceinline__ void store_row_chunk(const TcArgs& p, int row, int co
   float* c_row = p.C + static_cast<int64_t>(row) * p.ldc;
   const bool read_c = (p.beta != 0.0f);
   if (p.c_vec4 && col0 + 31 < p.N) {
+    // Old values first, then the stores (see the note in the else branch).
+    float4 old[8];
+    if (read_c) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) old[q] = *reinterpret_cast<const float4*>(c_row + col0 + 4 * q);
+    }
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       float4* dst = reinterpret_cast<float4*>(c_row + col0 + 4 * q);
       float4 v = make_float4(__uint_as_float(r[4 * q + 0]), __uint_as_float(r[4 * q + 1]),
                              __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
       if (read_c) {
-        const float4 o = *dst;
+        const float4 o = old[q];
         v.x = fmaf(p.alpha, v.x, p.beta * o.x);
         v.y = fmaf(p.alpha, v.y, p.beta * o.y);
         v.z = fmaf(p.alpha, v.z, p.beta * o.z);
@@ -91,12 +97,18 @@ __device__ __forceinline__ void store_row_chunk(const TcArgs& p, int row, int co
       *dst = v;
     }
   } else {
+    // Ragged or unaligned edge.  Loading every old value before the first
+    // store keeps the loads independent; interleaved load/store pairs to
+    // possibly aliasing addresses would cost one memory round trip each.
+    float old[32];
+#pragma unroll
+    for (int c = 0; c < 32; ++c) old[c] = (read_c && col0 + c < p.N) ? c_row[col0 + c] : 0.0f;
 #pragma unroll
     for (int c = 0; c < 32; ++c) {
       const int col = col0 + c;
       if (col < p.N) {
         const float v = __uint_as_float(r[c]);
-        c_row[col] = read_c ? fmaf(p.alpha, v, p.beta * c_row[col]) : p.alpha * v;
+        c_row[col] = read_c ? fmaf(p.alpha, v, p.beta * old[c]) : p.alpha * v;
       }
     }
   }
@@ -105,9 +117,8 @@ __device__ __forceinline__ void store_row_chunk(const TcArgs& p, int row, int co
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bf16_kernel(const TcArgs p, const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = align_smem<1024>(smem_raw);
   TcSmemTail* tail = reinterpret_cast<TcSmemTail*>(smem + STAGES * kStageBytes);
   volatile int* abort_flag = &tail->abort_flag;
 

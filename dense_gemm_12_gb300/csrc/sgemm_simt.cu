@@ -196,40 +196,68 @@ __device__ __forceinline__ void compute_stage(const uint8_t* sA, const uint8_t* 
   }
 }
 
+// C = alpha * acc + beta * C for the thread's 8 x 8 micro-tile.  For each
+// 4-column half the old values of all 8 rows are loaded before any store, so
+// the loads overlap; interleaved load/store pairs to possibly aliasing rows
+// would serialise a memory round trip per row.
 __device__ __forceinline__ void epilogue(const SimtArgs& p, const float (&acc)[8][8], int tm,
                                          int tn, int wm, int wn, int rg, int cg) {
   const bool read_c = (p.beta != 0.0f);
+  const int row0 = tm * BM + wm * 32 + rg;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int row = tm * BM + wm * 32 + rg + 4 * i;
-    if (row >= p.M) continue;
-    float* c_row = p.C + static_cast<int64_t>(row) * p.ldc;
+  for (int h = 0; h < 2; ++h) {
+    const int col = tn * BN + wn * 64 + h * 32 + cg * 4;
+    if (p.c_vec4 && col + 3 < p.N) {
+      float4 old[8];
+      if (read_c) {
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int col = tn * BN + wn * 64 + h * 32 + cg * 4;
-      if (p.c_vec4 && col + 3 < p.N) {
+        for (int i = 0; i < 8; ++i) {
+          const int row = row0 + 4 * i;
+          old[i] = row < p.M ? *reinterpret_cast<const float4*>(
+                                   p.C + static_cast<int64_t>(row) * p.ldc + col)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int row = row0 + 4 * i;
+        if (row >= p.M) continue;
         float4 v = make_float4(acc[i][h * 4 + 0], acc[i][h * 4 + 1], acc[i][h * 4 + 2],
                                acc[i][h * 4 + 3]);
-        float4* dst = reinterpret_cast<float4*>(c_row + col);
         if (read_c) {
-          const float4 o = *dst;
-          v.x = fmaf(p.alpha, v.x, p.beta * o.x);
-          v.y = fmaf(p.alpha, v.y, p.beta * o.y);
-          v.z = fmaf(p.alpha, v.z, p.beta * o.z);
-          v.w = fmaf(p.alpha, v.w, p.beta * o.w);
+          v.x = fmaf(p.alpha, v.x, p.beta * old[i].x);
+          v.y = fmaf(p.alpha, v.y, p.beta * old[i].y);
+          v.z = fmaf(p.alpha, v.z, p.beta * old[i].z);
+          v.w = fmaf(p.alpha, v.w, p.beta * old[i].w);
         } else {
           v.x *= p.alpha;
           v.y *= p.alpha;
           v.z *= p.alpha;
           v.w *= p.alpha;
         }
-        *dst = v;
-      } else {
+        *reinterpret_cast<float4*>(p.C + static_cast<int64_t>(row) * p.ldc + col) = v;
+      }
+    } else {
+      float old[8][4];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int row = row0 + 4 * i;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          old[i][c] = (read_c && row < p.M && col + c < p.N)
+                          ? p.C[static_cast<int64_t>(row) * p.ldc + col + c]
+                          : 0.0f;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int row = row0 + 4 * i;
+        if (row >= p.M) continue;
+        float* c_row = p.C + static_cast<int64_t>(row) * p.ldc;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           if (col + c < p.N) {
             const float r = acc[i][h * 4 + c];
-            c_row[col + c] = read_c ? fmaf(p.alpha, r, p.beta * c_row[col + c]) : p.alpha * r;
+            c_row[col + c] = read_c ? fmaf(p.alpha, r, p.beta * old[i][c]) : p.alpha * r;
           }
         }
       }
@@ -242,9 +270,8 @@ __global__ void __launch_bounds__(SimtTraits<MODE_A, MODE_B>::kThreads, 1)
     simt_gemm_kernel(const SimtArgs p, const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB) {
   using T = SimtTraits<MODE_A, MODE_B>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = align_smem<1024>(smem_raw);
   SimtSmemTail* tail = reinterpret_cast<SimtSmemTail*>(smem + STAGES * kStageBytes);
   auto stage_a = [&](int s) { return smem + s * kStageBytes; };
   auto stage_b = [&](int s) { return smem + s * kStageBytes + kStageBytesA; };

@@ -59,6 +59,25 @@ def test_decode_shapes(M, N, K):
     check_device_error()
 
 
+@pytest.mark.parametrize("N,K", [(128, 8192), (384, 4096), (256, 16384), (1000, 2048)])
+def test_decode_many_contributors(N, K):
+    # few column groups, long k: up to ~128 CTAs add into one group, which
+    # exercises the arrival-counter hand-off and both fix-up paths
+    M = 16
+    A, B, C = make_inputs(M, N, K, ("normal", 1.0), ("normal", 0.02), ("uniform", None),
+                          seed=N + K, dtype="bf16")
+    outs = []
+    for _ in range(3):
+        out, st, _, _, dC = run_bf16gemm(A, B, C, 1.25, -0.75)
+        assert st == 0
+        outs.append(out)
+    _, ref64, den = oracle_bf16(A, B, C, 1.25, -0.75)
+    assert ratio(outs[0], ref64, den) <= TOL_BF16
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int32), outs[0].view(torch.int32))
+    check_device_error()
+
+
 def test_decode_beta_zero_nan():
     M, N, K = 16, 2048, 1024
     A, B, _ = make_inputs(M, N, K, seed=7, dtype="bf16")
