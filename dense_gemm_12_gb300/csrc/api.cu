@@ -371,9 +371,10 @@ gemm_status_t gemm_bf16gemm(int64_t M, int64_t N, int64_t K, float alpha, const 
   }
 
   // GEMM_PATH_TC_DECODE
-  if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, K, M, lda, kDecBK, kDecBM,
+  if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, K, M, lda, 64, kDecBM,
                  CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, N, K, ldb, 64, kDecBK,
+      !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, N, K, ldb, 64,
+                 static_cast<uint32_t>(decode_b_box_rows()),
                  CU_TENSOR_MAP_SWIZZLE_128B))
     return GEMM_ERR_LAUNCH;
   const int grid = decode_grid(static_cast<int>(N), static_cast<int>(K), st->num_sms);

@@ -11,22 +11,27 @@
 // 128 columns of C and its N (16) over the rows of A, and no row of the MMA
 // is padding.
 //
-// Work split.  B is cut into n-groups of NSUB x 128 columns; a unit is one
-// n-group x 64 values of k.  Units are numbered n-group-major and every CTA
-// takes one contiguous, equal-sized run of them, so each SM streams the same
-// number of bytes of B (no last wave), and every k-row of a unit is a
-// contiguous NSUB x 256-byte stretch of memory.  A run is cut into segments at
-// n-group boundaries.  A segment that spans the whole k range of its n-group
-// writes C directly; otherwise it stores its NW x 16 fp32 partial in the
-// workspace and bumps the n-group's arrival counter, and the CTA that arrives
-// last adds the partials in k order (a fixed order, so results are
-// deterministic), applies alpha/beta, writes C and resets the counter to zero
-// for the next launch.
+// Work split.  B is cut into n-groups of 128 columns; a unit is one n-group x
+// 128 values of k (32 KB of B, fetched as two 64 x 128 TMA boxes).  With at
+// least ~60 % as many n-groups as SMs (N = 12288 gives 96) every CTA streams
+// whole n-groups: no k range is split and nothing is exchanged.  Otherwise
+// units are numbered n-group-major and every CTA takes one contiguous,
+// equal-sized run of them, cut into segments at n-group boundaries (split-K).
+// A segment that spans the whole k range of its n-group writes C directly;
+// otherwise the CTA holding the group's first k-piece combines: it waits a
+// short, bounded time for the other contributors' partial sums (published in
+// the workspace, announced on the group's arrival counter) and preloads them
+// while its own MMAs drain; the others publish and never wait.  If the bound
+// runs out the combiner publishes too and whichever CTA arrives last adds the
+// partials.  Partials are always added in k order, so results are
+// deterministic, and the combiner resets the counter for the next launch.
 //
-// Roles: warp 0 TMA producer (2 x NSUB 64-column MN-major boxes of B and one
-// 16 x 64 K-major box of A per stage), warp 1 TMEM owner and MMA issuer
-// (128 x 16 x 16 MMAs, NSUB accumulators per segment, double-buffered),
-// warps 2..5 epilogue / fix-up.
+// Roles: warp 0 TMA producer (B boxes and two 16 x 64 K-major boxes of A per
+// stage), warps 1 and 6 issue the MMAs (128 x 16 x 16, alternate stages,
+// one accumulator each, double-buffered; warp 1 owns TMEM), warps 2..5 read
+// the accumulators, combine and write C.  The launch uses programmatic
+// dependent launch: the next kernel in the stream may set up while this one
+// drains, and every global access follows grid_dependency_wait().
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -40,34 +45,56 @@ namespace {
 #ifndef G12_DECODE_NSUB
 #define G12_DECODE_NSUB 1
 #endif
-
 constexpr int BN = kDecBN;                 // MMA M: 128 columns of C per MMA tile
 constexpr int NSUB = G12_DECODE_NSUB;      // MMA tiles per n-group
 constexpr int NW = NSUB * BN;              // columns of C per n-group
+constexpr int kBoxesPerTile = BN / 64;     // 64-column TMA boxes per MMA tile
+// Accumulator rows held by each epilogue warp (one 32-lane TMEM quarter each).
+constexpr int kRowsPerQuarter = 32;
 constexpr int BMr = kDecBM;                // MMA N: rows of A / C
-constexpr int BK = kDecBK;
-constexpr int kBoxBytesB = BK * 64 * 2;                   // one 64-column box, 8 KB
-constexpr int kStageBytesB = NSUB * 2 * kBoxBytesB;       // NSUB x 16 KB
+#ifndef G12_DECODE_BK
+#define G12_DECODE_BK 128
+#endif
+constexpr int BK = G12_DECODE_BK;          // k per stage (one unit)
+static_assert(BK == 64 || BK == 128, "k per stage must be 64 or 128");
+constexpr int kABoxes = BK / 64;           // 16 x 64 boxes of A per stage
+constexpr int kBoxBytesB = BK * 64 * 2;                   // one 64-column box of B
+constexpr int kStageBytesB = NSUB * kBoxesPerTile * kBoxBytesB;
 constexpr int kStageBytesA = BMr * BK * 2;                // 2 KB
 constexpr int kStageBytes = kStageBytesB + kStageBytesA;  // multiple of 1024
 #ifndef G12_DECODE_SMEM_KB
-#define G12_DECODE_SMEM_KB 200
-#endif
-#ifndef G12_DECODE_CTAS_PER_SM
-#define G12_DECODE_CTAS_PER_SM 1
+#define G12_DECODE_SMEM_KB 220
 #endif
 #ifndef G12_DECODE_EARLY_UNITS
 #define G12_DECODE_EARLY_UNITS 2
 #endif
-constexpr int kCtasPerSm = G12_DECODE_CTAS_PER_SM;
+// How long the combining CTA of a column group polls for the other
+// contributors' partial sums before it falls back to publishing its own.
+constexpr uint64_t kHandoffWaitNs = 20000;
 // Units of B each CTA asks L2 to fetch before it waits for the previous
 // kernel in the stream (more would delay its own first TMA loads).
 constexpr int kEarlyUnits = G12_DECODE_EARLY_UNITS;
 constexpr int kStageBudget = (G12_DECODE_SMEM_KB * 1024) / kStageBytes;
-constexpr int STAGES = kStageBudget > 10 ? 10 : kStageBudget;
-constexpr int kThreads = 192;
+#ifndef G12_DECODE_ISSUERS
+#define G12_DECODE_ISSUERS 2
+#endif
+// Threads issuing tcgen05.mma, each in its own warp and taking every
+// kIssuers-th stage into its own accumulator: with N = 16 the issue cost of
+// an MMA, not the tensor core, bounds how fast one thread can consume B.
+constexpr int kIssuers = G12_DECODE_ISSUERS;
+static_assert(kIssuers == 1 || kIssuers == 2, "one or two MMA issuers");
+constexpr int kThreads = 192 + (kIssuers - 1) * 32;
 constexpr int kEpiThreads = 128;
-constexpr uint32_t kAccCols = NSUB * BMr;                 // TMEM columns per segment
+constexpr int kSecondIssuerWarp = 6;
+// Stages are a multiple of the issuer count, so that every stage is always
+// consumed by the same issuer.  An issuer then waits for the rounds of its
+// stages strictly in order; if two issuers alternated on one stage, one could
+// wait for round r+1 before round r completed, which a parity wait cannot
+// tell apart.
+constexpr int STAGES = ((kStageBudget > 20 ? 20 : kStageBudget) / kIssuers) * kIssuers;
+static_assert(STAGES >= kIssuers && STAGES % kIssuers == 0, "stages per issuer");
+constexpr uint32_t kIssuerCols = NSUB * BMr;              // TMEM columns per issuer
+constexpr uint32_t kAccCols = kIssuers * kIssuerCols;     // TMEM columns per segment
 constexpr uint32_t kTmemCols = 2 * kAccCols < 32 ? 32 : 2 * kAccCols;
 constexpr uint32_t kIdesc = idesc_bf16_f32(BN, BMr, /*A MN-major*/ 1, /*B MN-major*/ 0);
 constexpr int kPartialFloats = BMr * NW;
@@ -80,7 +107,7 @@ struct __align__(8) DecSmemTail {
   uint64_t empty[STAGES];
   uint64_t tmem_full[2];
   uint64_t tmem_empty[2];
-  uint64_t drain;
+  uint64_t drain[2];
   uint32_t tmem_base;
   int abort_flag;
   int last_flag;
@@ -141,7 +168,7 @@ __device__ __forceinline__ void store_c_column(const DecodeArgs& p, int n, const
           (p.beta != 0.0f) ? fmaf(p.alpha, v[m], p.beta * old[m]) : p.alpha * v[m];
 }
 
-__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+__global__ void __launch_bounds__(kThreads, 1)
     tc_decode_kernel(const DecodeArgs p, const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -161,10 +188,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       mbar_init(&tail->empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&tail->tmem_full[b], 1);
+      mbar_init(&tail->tmem_full[b], kIssuers);
       mbar_init(&tail->tmem_empty[b], kEpiThreads);
     }
-    mbar_init(&tail->drain, 1);
+    for (int q = 0; q < 2; ++q) mbar_init(&tail->drain[q], 1);
     tail->abort_flag = 0;
     tail->last_flag = 0;
     tail->others_ready = 0;
@@ -187,7 +214,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       const int png = static_cast<int>(v / sp.kb_total);
       const int pkb = static_cast<int>(v - static_cast<int64_t>(png) * sp.kb_total);
 #pragma unroll
-      for (int b = 0; b < 2 * NSUB; ++b) tma_prefetch_l2_2d(&tmB, png * NW + b * 64, pkb * BK);
+      for (int b = 0; b < NSUB * kBoxesPerTile; ++b)
+        tma_prefetch_l2_2d(&tmB, png * NW + b * 64, pkb * BK);
     }
   }
   tc_fence_before_sync();
@@ -214,9 +242,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         uint8_t* sa = sb + kStageBytesB;
         mbar_arrive_expect_tx(&tail->full[s], kStageBytes);
 #pragma unroll
-        for (int b = 0; b < 2 * NSUB; ++b)
+        for (int b = 0; b < NSUB * kBoxesPerTile; ++b)
           tma_load_2d(sb + b * kBoxBytesB, &tmB, ng * NW + b * 64, kb * BK, &tail->full[s]);
-        tma_load_2d(sa, &tmA, kb * BK, 0, &tail->full[s]);
+#pragma unroll
+        for (int a = 0; a < kABoxes; ++a)
+          tma_load_2d(sa + a * (BMr * 64 * 2), &tmA, kb * BK + a * 64, 0, &tail->full[s]);
       }
       // This CTA has issued all its loads: the next kernel in the stream may
       // start launching (it waits for this grid's completion before use).
@@ -228,8 +258,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // -------------------------------------------------------- MMA issuer
+  } else if (warp == 1 || (kIssuers == 2 && warp == kSecondIssuerWarp)) {
+    // -------------------------------------------------------- MMA issuers
+    const uint32_t q = (warp == 1) ? 0u : 1u;  // this issuer's stage parity
     if (lane == 0) {
       uint32_t it = 0, seg = 0;
       bool ok = true, issued = false;
@@ -243,9 +274,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           break;
         }
         tc_fence_after_sync();
-        const uint32_t d_tmem = tmem_base + ab * kAccCols;
+        const uint32_t d_tmem = tmem_base + ab * kAccCols + q * kIssuerCols;
         bool first = true;
         for (; u < seg_end_u; ++u, ++it) {
+          if (it % kIssuers != q) continue;
           const int s = it % STAGES;
           const uint32_t round = it / STAGES;
           if (!mbar_wait(&tail->full[s], round & 1u, abort_flag, p.err)) {
@@ -259,14 +291,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           for (int kk = 0; kk < BK / 16; ++kk) {
             // MMA B operand = A^T tile: K-major, 8-row groups 1024 B apart,
             // k step of 16 elements = 32 B.
-            const uint64_t bdesc = smem_desc_sw128(sa + kk * 32, 16, 1024);
+            const uint64_t bdesc =
+                smem_desc_sw128(sa + (kk / 4) * (BMr * 64 * 2) + (kk % 4) * 32, 16, 1024);
 #pragma unroll
             for (int j = 0; j < NSUB; ++j) {
               // MMA A operand = B^T tile j: MN-major, its two 64-column boxes
               // 8 KB apart (LBO), 8-row k groups 1024 B apart (SBO), k step
               // of 16 rows = 2048 B.
-              const uint64_t adesc =
-                  smem_desc_sw128(sb + j * 2 * kBoxBytesB + kk * 2048, kBoxBytesB, 1024);
+              const uint64_t adesc = smem_desc_sw128(
+                  sb + j * kBoxesPerTile * kBoxBytesB + kk * 2048, kBoxBytesB, 1024);
               tc_mma_f16(d_tmem + j * BMr, adesc, bdesc, kIdesc,
                          (first && kk == 0) ? 0u : 1u);
             }
@@ -280,15 +313,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         ++seg;
       }
       if (!ok && issued) {
-        tc_commit(&tail->drain);
-        mbar_drain_wait(&tail->drain, 0);
+        tc_commit(&tail->drain[q]);
+        mbar_drain_wait(&tail->drain[q], 0);
       }
     }
     __syncwarp();
-  } else {
+  } else if (warp >= 2 && warp <= 5) {
     // -------------------------------------------------------- epilogue
     const int quarter = warp & 3;
-    const int n_local = quarter * 32 + lane;  // row of each MMA tile = column of C
+    // row of each MMA tile held by this thread = column of C within the tile
+    const int n_local = quarter * kRowsPerQuarter + lane;
+    const bool row_valid = lane < kRowsPerQuarter && n_local < BN;
     const int ept = threadIdx.x - 64;         // 0..127
     uint32_t seg = 0;
     int64_t u = u_begin;
@@ -308,11 +343,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       // the group's result is a few adds away.
       float old[NSUB][BMr];
 #pragma unroll
-      for (int j = 0; j < NSUB; ++j) load_c_column(p, ng * NW + j * BN + n_local, old[j]);
+      for (int j = 0; j < NSUB; ++j)
+        load_c_column(p, row_valid ? ng * NW + j * BN + n_local : p.N, old[j]);
       constexpr int kPre = 2;  // partial sums of other CTAs held in registers
       float pre[kPre][NSUB][BMr];
       bool preloaded = false;
-      const bool can_preload = !whole && (nsegs - 1 <= static_cast<uint32_t>(kPre));
+      const bool can_preload = row_valid && !whole && (nsegs - 1 <= static_cast<uint32_t>(kPre));
       auto preload = [&]() {
         // the kk-th contributor other than this CTA, in CTA order
 #pragma unroll
@@ -355,14 +391,40 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       if (!ok) break;
       tc_fence_after_sync();
       uint32_t r[NSUB][16];
+      {
+        uint32_t acc[kIssuers][NSUB][16];
 #pragma unroll
-      for (int j = 0; j < NSUB; ++j)
-        tmem_ld_32x32b_x16(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                               ab * kAccCols + j * BMr,
-                           r[j]);
-      tc_wait_ld();
-      tc_fence_before_sync();
-      mbar_arrive(&tail->tmem_empty[ab]);
+        for (int qq = 0; qq < kIssuers; ++qq)
+#pragma unroll
+          for (int j = 0; j < NSUB; ++j)
+            tmem_ld_32x32b_x16(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                   ab * kAccCols + qq * kIssuerCols + j * BMr,
+                               acc[qq][j]);
+        tc_wait_ld();
+        tc_fence_before_sync();
+        mbar_arrive(&tail->tmem_empty[ab]);
+        // Issuer qq wrote an accumulator for this segment iff one of the
+        // segment's units has stage index it = u - u_begin with it % kIssuers
+        // == qq; sum the written ones in issuer order.
+        const int64_t it0 = u - u_begin;
+        const int64_t len = seg_end_u - u;
+#pragma unroll
+        for (int j = 0; j < NSUB; ++j)
+#pragma unroll
+          for (int m = 0; m < BMr; ++m) {
+            float v = 0.0f;
+            bool any = false;
+#pragma unroll
+            for (int qq = 0; qq < kIssuers; ++qq) {
+              const bool wrote = len >= kIssuers || it0 % kIssuers == qq;
+              if (wrote) {
+                v = any ? v + __uint_as_float(acc[qq][j][m]) : __uint_as_float(acc[qq][j][m]);
+                any = true;
+              }
+            }
+            r[j][m] = __float_as_uint(v);
+          }
+      }
 
       if (whole) {
 #pragma unroll
@@ -370,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           float v[BMr];
 #pragma unroll
           for (int m = 0; m < BMr; ++m) v[m] = __uint_as_float(r[j][m]);
-          store_c_column(p, ng * NW + j * BN + n_local, v, old[j]);
+          store_c_column(p, row_valid ? ng * NW + j * BN + n_local : p.N, v, old[j]);
         }
       } else {
         // last_flag: 2 = every other contributor had already arrived (this
@@ -379,6 +441,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         if (ept == 0) {
           bool ready = tail->others_ready != 0;
           if (!ready) ready = ld_acquire_gpu(p.counters + ng) == nsegs - 1;
+          // The CTA holding the group's first k-piece finishes it last in its
+          // run, so it is the designated combiner: rather than publish its
+          // own partial it waits a short, bounded time for the others (which
+          // never wait on anyone), then falls back to the arrival protocol.
+          if (!ready && blockIdx.x == c_first) {
+            const uint64_t t0 = globaltimer_ns();
+            while (!ready && globaltimer_ns() - t0 < kHandoffWaitNs)
+              ready = ld_acquire_gpu(p.counters + ng) == nsegs - 1;
+          }
           tail->last_flag = ready ? 2 : 0;
         }
         named_bar_epi();
@@ -387,11 +458,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           const int seg_local = static_cast<int>(ng - u_begin / sp.kb_total);
           float* slot = p.workspace + (static_cast<int64_t>(blockIdx.x) * sp.segs_max + seg_local) *
                                           kPartialFloats;
+          if (row_valid) {
 #pragma unroll
-          for (int j = 0; j < NSUB; ++j)
+            for (int j = 0; j < NSUB; ++j)
 #pragma unroll
-            for (int m = 0; m < BMr; ++m)
-              __stcg(slot + m * NW + j * BN + n_local, __uint_as_float(r[j][m]));
+              for (int m = 0; m < BMr; ++m)
+                __stcg(slot + m * NW + j * BN + n_local, __uint_as_float(r[j][m]));
+          }
           named_bar_epi();
           if (ept == 0) {
             __threadfence();  // publish the whole CTA's partial before arriving
@@ -426,10 +499,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 const int sl = static_cast<int>(ng - run_start(sp, cc) / sp.kb_total);
                 const float* src = p.workspace + (cc * sp.segs_max + sl) * kPartialFloats;
 #pragma unroll
-                for (int m = 0; m < BMr; ++m) sum[m] += __ldcg(src + m * NW + j * BN + n_local);
+                for (int m = 0; m < BMr; ++m)
+                  sum[m] += row_valid ? __ldcg(src + m * NW + j * BN + n_local) : 0.0f;
               }
             }
-            store_c_column(p, ng * NW + j * BN + n_local, sum, old[j]);
+            store_c_column(p, row_valid ? ng * NW + j * BN + n_local : p.N, sum, old[j]);
           }
           if (ept == 0) p.counters[ng] = 0u;
         }
@@ -449,9 +523,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
 }  // namespace
 
+int decode_b_box_rows() { return BK; }
+
 int decode_grid(int N, int K, int num_sms) {
-  const int64_t units = static_cast<int64_t>((N + NW - 1) / NW) * ((K + BK - 1) / BK);
-  const int64_t slots = static_cast<int64_t>(num_sms) * kCtasPerSm;
+  const int64_t groups = (N + NW - 1) / NW;
+  const int64_t units = groups * ((K + BK - 1) / BK);
+  const int64_t slots = num_sms;
+  // Enough column groups to keep most SMs streaming: one CTA per group, so
+  // no group's k range is split and no partial sums are exchanged.  Fewer
+  // groups: split k over all SMs.  More groups than SMs: each CTA takes a run
+  // of whole groups (only the groups at run boundaries are split).
+  if (groups <= slots && groups * 5 >= slots * 3) return static_cast<int>(groups);
   return static_cast<int>(units < slots ? units : slots);
 }
 

@@ -65,7 +65,9 @@ struct DecodeArgs {
 // (D^T = B^T A^T, MMA M = 128 over N, MMA N = 16 over M), split over K.
 cudaError_t launch_tc_decode(const DecodeArgs& a, const CUtensorMap* tmA,
                              const CUtensorMap* tmB, int num_ctas, cudaStream_t stream);
-constexpr int kDecBN = 128, kDecBM = 16, kDecBK = 64;
+constexpr int kDecBN = 128, kDecBM = 16;
+// k-rows of B per TMA box of the decode kernel (the A box is always 64 wide).
+int decode_b_box_rows();
 // Workspace floats and counters a decode launch of this shape needs.
 int64_t decode_workspace_floats(int N, int K, int num_ctas);
 int64_t decode_counter_count(int N);
