@@ -20,6 +20,7 @@ from . import _build
 
 __all__ = [
     "GemmError", "load_library", "library_path", "gemm_sgemm", "gemm_bf16gemm",
+    "gemm_bf16gemm_decode_static",
     "gemm_status_string", "gemm_check_device_error", "gemm_shutdown",
     "gemm_select_path", "gemm_quantization", "gemm_version", "sgemm", "bf16gemm",
     "STATUS", "PATHS",
@@ -81,6 +82,8 @@ def load_library(build_if_missing: bool = False):
         lib.gemm_sgemm.restype = cint
         lib.gemm_bf16gemm.argtypes = gemm_args
         lib.gemm_bf16gemm.restype = cint
+        lib.gemm_bf16gemm_decode_static.argtypes = gemm_args
+        lib.gemm_bf16gemm_decode_static.restype = cint
         lib.gemm_status_string.argtypes = [cint]
         lib.gemm_status_string.restype = ctypes.c_char_p
         lib.gemm_check_device_error.argtypes = [vp]
@@ -107,6 +110,13 @@ def gemm_sgemm(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0) -> int:
 def gemm_bf16gemm(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0) -> int:
     """bf16-in / fp32-out GEMM; pointers are device addresses. Returns the status."""
     return load_library().gemm_bf16gemm(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream)
+
+
+def gemm_bf16gemm_decode_static(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0) -> int:
+    """Decode-shaped bf16 GEMM that allocates nothing (scratch in a fixed
+    library-owned array); see include/gemm12.h. Returns the status."""
+    return load_library().gemm_bf16gemm_decode_static(M, N, K, alpha, A, lda, B, ldb, beta, C,
+                                                      ldc, stream)
 
 
 def gemm_status_string(status: int) -> str:

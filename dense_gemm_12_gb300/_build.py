@@ -19,7 +19,7 @@ LIB_NAME = "libgemm12.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
-SOURCES = ["api.cu", "sgemm_simt.cu", "bf16_tc.cu", "bf16_decode.cu"]
+SOURCES = ["api.cu", "sgemm_simt.cu", "bf16_tc.cu", "bf16_decode.cu", "decode_noalloc.cu"]
 HEADERS = ["ptx.cuh", "internal.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -214,6 +214,32 @@ cudaError_t launch_scale_c(int M, int N, float beta, float* C, int64_t ldc, cuda
   return cudaGetLastError();
 }
 
+// Shared pieces of the C ABI for entry points defined in other translation
+// units (thin wrappers; the entry points above do not use them).
+gemm_status_t abi_check_args(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                             int64_t ldc) {
+  return check_common(M, N, K, lda, ldb, ldc);
+}
+
+bool abi_tma_ok(const void* base, int64_t ld, int elem_bytes) {
+  return tma_ok(base, ld, elem_bytes);
+}
+
+bool abi_encode_bf16_2d(CUtensorMap* map, const void* base, int64_t inner, int64_t outer,
+                        int64_t ld, uint32_t bx, uint32_t by) {
+  return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, inner, outer, ld, bx, by,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+gemm_status_t abi_device(int* num_sms, uint32_t** err_word) {
+  gemm_status_t s;
+  DeviceState* st = device_state(&s);
+  if (st == nullptr) return s;
+  *num_sms = st->num_sms;
+  *err_word = st->err_word;
+  return GEMM_OK;
+}
+
 }  // namespace g12
 
 using namespace g12;

@@ -73,6 +73,19 @@ int64_t decode_workspace_floats(int N, int K, int num_ctas);
 int64_t decode_counter_count(int N);
 int decode_grid(int N, int K, int num_sms);
 
+// Pieces of the C ABI shared with entry points in other translation units.
+}  // namespace g12
+#include "../../include/gemm12.h"
+namespace g12 {
+gemm_status_t abi_check_args(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                             int64_t ldc);
+bool abi_tma_ok(const void* base, int64_t ld, int elem_bytes);
+bool abi_encode_bf16_2d(CUtensorMap* map, const void* base, int64_t inner, int64_t outer,
+                        int64_t ld, uint32_t bx, uint32_t by);
+// Current device's SM count and error-word address (GEMM_OK), or the status
+// the entry points return when there is no usable sm_103a device.
+gemm_status_t abi_device(int* num_sms, uint32_t** err_word);
+
 // C <- beta * C (beta == 0 writes zeros without reading C).
 cudaError_t launch_scale_c(int M, int N, float beta, float* C, int64_t ldc,
                            cudaStream_t stream);

@@ -110,6 +110,37 @@ gemm_status_t gemm_bf16gemm(int64_t M, int64_t N, int64_t K, float alpha,
                             const void *B, int64_t ldb,
                             float beta, float *C, int64_t ldc, void *stream);
 
+/*
+ * gemm_bf16gemm_decode_static -- the decode-shaped bf16 GEMM of gemm_bf16gemm
+ * (M <= 16; same arguments, same kernel, same results) for callers that must
+ * not allocate device memory: for example a serving process that reserves all
+ * of its device memory at start-up and allows no allocation on its request
+ * path, or code that runs inside a memory allocator's own callbacks, where
+ * calling cudaMalloc again is not allowed.  The GEMM pages have no
+ * counterpart of this entry point; it exists for such callers only.
+ *
+ * Instead of allocating its split-K scratch (partial sums and per-column-group
+ * arrival counters) the call uses one fixed array of 4 MiB that the library
+ * holds on every device it is loaded onto, until the process exits.  It calls
+ * no cudaMalloc or cudaFree.  Limits: at most 4096 column groups of 128
+ * (N <= 524288) and a partial-sum area of about one million floats; shapes
+ * that need more return GEMM_ERR_UNSUPPORTED, as do M > 16 and operands the
+ * TMA engine cannot describe (base not 16-byte aligned, or a row pitch that
+ * is not a multiple of 16 bytes) -- use gemm_bf16gemm for those.  M == 0 or
+ * N == 0 does nothing; K == 0 or alpha == 0 computes C <- beta*C.
+ *
+ * Every call on a device shares that one array, and each call first clears
+ * the counters it needs (an asynchronous memset on `stream`).  Calls whose
+ * work overlaps on the GPU -- on different streams, or from different host
+ * threads -- race on the array and give wrong results: serialise them.  The
+ * first call on each device looks up the array's device address (once, with
+ * that device current); make that first call before any stream capture.
+ */
+gemm_status_t gemm_bf16gemm_decode_static(int64_t M, int64_t N, int64_t K, float alpha,
+                                          const void *A, int64_t lda,
+                                          const void *B, int64_t ldb,
+                                          float beta, float *C, int64_t ldc, void *stream);
+
 /* Static, NUL-terminated description of a status code (never NULL). */
 const char *gemm_status_string(gemm_status_t status);
 
