@@ -34,7 +34,16 @@ namespace g12 {
 namespace {
 
 constexpr int BM = kSimtBM, BN = kSimtBN, BK = kSimtBK;
-constexpr int STAGES = 4;
+#ifndef G12_SIMT_KQ_UNROLL
+#define G12_SIMT_KQ_UNROLL 8
+#endif
+#ifndef G12_SIMT_STAGES
+#define G12_SIMT_STAGES 4
+#endif
+constexpr int STAGES = G12_SIMT_STAGES;
+constexpr int kKqUnroll = G12_SIMT_KQ_UNROLL;  // unroll depth of the 4-k-step loop
+// The block is launched with 384 threads x 168 registers = 64512.
+constexpr int kLaunchRegs = 168;
 constexpr int kComputeWarps = 8;
 constexpr int kComputeThreads = kComputeWarps * 32;
 constexpr int kStageBytesA = BM * BK * 4;  // 16 KB, rows of 128 B, 128-B swizzled
@@ -72,11 +81,20 @@ template <int MODE_A, int MODE_B>
 struct SimtTraits {
   static constexpr bool kAnyGeneric = (MODE_A != kLoadTma) || (MODE_B != kLoadTma);
   static constexpr bool kAnyTma = (MODE_A == kLoadTma) || (MODE_B == kLoadTma);
-  static constexpr int kProducerWarps = kAnyGeneric ? 4 : 1;
+  // Always a full producer warpgroup, so the register split below works on
+  // whole warpgroups (only one lane issues TMA when both operands use it).
+  static constexpr int kProducerWarps = 4;
   static constexpr int kThreads = kComputeThreads + kProducerWarps * 32;
   // Arrivals that complete one phase of a full barrier: every generic
   // producer thread arrives once, the TMA issuer once (with the byte count).
   static constexpr uint32_t kFullCount = (kAnyGeneric ? 128u : 0u) + (kAnyTma ? 1u : 0u);
+  // Per-thread register split between the two compute warpgroups and the
+  // producer warpgroup; producers that widen bf16 keep more registers.
+  static constexpr bool kConvert = (MODE_A == kLoadConvertBf16) || (MODE_B == kLoadConvertBf16);
+  static constexpr int kProducerRegs = kConvert ? 96 : 56;
+  static constexpr int kComputeRegs = kConvert ? 200 : 224;
+  static_assert(256 * kComputeRegs + 128 * kProducerRegs <= 384 * kLaunchRegs,
+                "register split exceeds the launch allocation");
   static constexpr uint32_t kTmaBytes =
       (MODE_A == kLoadTma ? kStageBytesA : 0) + (MODE_B == kLoadTma ? kStageBytesB : 0);
 };
@@ -119,18 +137,18 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint16_t h) {
 __device__ __forceinline__ void load_a_bf16(uint8_t* sA, const uint16_t* A, int64_t lda, int M,
                                             int K, int m0, int k0, int ptid) {
 #pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    uint16_t v[16];
+  for (int part = 0; part < 4; ++part) {
+    uint16_t v[8];
 #pragma unroll
-    for (int q = 0; q < 16; ++q) {
-      const int e = ptid + (half * 16 + q) * 128;
+    for (int q = 0; q < 8; ++q) {
+      const int e = ptid + (part * 8 + q) * 128;
       const int m = e >> 5, k = e & 31;
       const int gm = m0 + m, gk = k0 + k;
       v[q] = (gm < M && gk < K) ? __ldg(A + static_cast<int64_t>(gm) * lda + gk) : uint16_t(0);
     }
 #pragma unroll
-    for (int q = 0; q < 16; ++q) {
-      const int e = ptid + (half * 16 + q) * 128;
+    for (int q = 0; q < 8; ++q) {
+      const int e = ptid + (part * 8 + q) * 128;
       const int m = e >> 5, k = e & 31;
       *reinterpret_cast<float*>(sA + a_smem_offset(m, k)) = bf16_bits_to_f32(v[q]);
     }
@@ -140,37 +158,61 @@ __device__ __forceinline__ void load_a_bf16(uint8_t* sA, const uint16_t* A, int6
 __device__ __forceinline__ void load_b_bf16(uint8_t* sB, const uint16_t* B, int64_t ldb, int N,
                                             int K, int n0, int k0, int ptid) {
 #pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    uint16_t v[16];
+  for (int part = 0; part < 4; ++part) {
+    uint16_t v[8];
 #pragma unroll
-    for (int q = 0; q < 16; ++q) {
-      const int e = ptid + (half * 16 + q) * 128;
+    for (int q = 0; q < 8; ++q) {
+      const int e = ptid + (part * 8 + q) * 128;
       const int k = e >> 7, n = e & 127;
       const int gk = k0 + k, gn = n0 + n;
       v[q] = (gk < K && gn < N) ? __ldg(B + static_cast<int64_t>(gk) * ldb + gn) : uint16_t(0);
     }
 #pragma unroll
-    for (int q = 0; q < 16; ++q) {
-      const int e = ptid + (half * 16 + q) * 128;
+    for (int q = 0; q < 8; ++q) {
+      const int e = ptid + (part * 8 + q) * 128;
       const int k = e >> 7, n = e & 127;
       *reinterpret_cast<float*>(sB + (k * BN + n) * 4) = bf16_bits_to_f32(v[q]);
     }
   }
 }
 
+// ------------------------------------------------------- packed fp32 pairs
+// sm_100-class GPUs execute two independent fp32 FMAs per lane from one
+// fma.rn.f32x2 instruction (each lane-half rounds exactly like fmaf).  One
+// issue slot then covers two FMA-pipe cycles, leaving slots free for the
+// shared loads and address arithmetic of the micro-tile loop.
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+__device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
 // ------------------------------------------------------------------ compute
 // One stage (BK = 32 values of k) of the 8 x 8 outer-product accumulation.
 // Lane layout inside the 32 x 64 warp tile: rg = lane / 8 picks rows
 // {rg, rg+4, ..., rg+28}; cg = lane % 8 picks columns {4cg..4cg+3} and
-// {32+4cg..32+4cg+3}.
-__device__ __forceinline__ void compute_stage(const uint8_t* sA, const uint8_t* sB,
-                                              float (&acc)[8][8], int wm, int wn, int rg,
-                                              int cg) {
-  const uint8_t* a_row0 = sA + (wm * 32 + rg) * 128;  // row rg of the warp tile
+// {32+4cg..32+4cg+3}.  A is read four k values at a time (one 128-bit load
+// per row), B one k row at a time as two 128-bit loads.  The accumulators
+// are fp32 pairs: acc2[i][q] holds the thread's columns 2q and 2q+1 of row i,
+// updated with fma.rn.f32x2 (A value duplicated into both halves).
+__device__ __forceinline__ void compute_stage_x2(const uint8_t* sA, const uint8_t* sB,
+                                                 uint64_t (&acc2)[8][4], int wm, int wn,
+                                                 int rg, int cg) {
+  const uint8_t* a_row0 = sA + (wm * 32 + rg) * 128;
   const float* b_base = reinterpret_cast<const float*>(sB) + wn * 64 + cg * 4;
-  const int x_even = rg;      // (row & 7) for rows rg + 4i, i even
-  const int x_odd = rg + 4;   // ... i odd
-#pragma unroll 2
+  const int x_even = rg;
+  const int x_odd = rg + 4;
+#pragma unroll kKqUnroll
   for (int kq = 0; kq < BK / 4; ++kq) {
     float4 a[8];
     const int off_even = (kq ^ x_even) << 4;
@@ -183,20 +225,21 @@ __device__ __forceinline__ void compute_stage(const uint8_t* sA, const uint8_t* 
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
       const int k = kq * 4 + kk;
-      const float4 b0 = *reinterpret_cast<const float4*>(b_base + k * BN);
-      const float4 b1 = *reinterpret_cast<const float4*>(b_base + k * BN + 32);
-      const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+      const ulonglong2 b0 = *reinterpret_cast<const ulonglong2*>(b_base + k * BN);
+      const ulonglong2 b1 = *reinterpret_cast<const ulonglong2*>(b_base + k * BN + 32);
+      const uint64_t bv[4] = {b0.x, b0.y, b1.x, b1.y};
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const float av = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
+        const uint64_t a2 = pack2(av, av);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av, bv[j], acc[i][j]);
+        for (int q = 0; q < 4; ++q) acc2[i][q] = ffma2(a2, bv[q], acc2[i][q]);
       }
     }
   }
 }
 
-// C = alpha * acc + beta * C for the thread's 8 x 8 micro-tile.  For each
+// C = alpha * acc + beta * C for the thread's 8 x 8 micro-tile.// C = alpha * acc + beta * C for the thread's 8 x 8 micro-tile.  For each
 // 4-column half the old values of all 8 rows are loaded before any store, so
 // the loads overlap; interleaved load/store pairs to possibly aliasing rows
 // would serialise a memory round trip per row.
@@ -298,6 +341,9 @@ __global__ void __launch_bounds__(SimtTraits<MODE_A, MODE_B>::kThreads, 1)
 
   if (warp >= kComputeWarps) {
     // ------------------------------------------------------------ producers
+    // Hand registers to the compute warpgroups (see SimtTraits: the split
+    // never exceeds the 384 x 168 the block is launched with).
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(T::kProducerRegs));
     const int ptid = threadIdx.x - kComputeThreads;
     const bool tma_issuer = (ptid == 0) && T::kAnyTma;
     if (!T::kAnyGeneric && ptid != 0) return;
@@ -350,24 +396,30 @@ __global__ void __launch_bounds__(SimtTraits<MODE_A, MODE_B>::kThreads, 1)
   }
 
   // -------------------------------------------------------------- compute
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(T::kComputeRegs));
   const int wm = warp >> 1, wn = warp & 1;
   const int rg = lane >> 3, cg = lane & 7;
   uint32_t it = 0;
   for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
     int tm, tn;
     tile_coords(t, tiles_m, tiles_n, tm, tn);
-    float acc[8][8];
+    uint64_t acc2[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-      for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+      for (int q = 0; q < 4; ++q) acc2[i][q] = 0ull;
     for (int kb = 0; kb < num_kb; ++kb, ++it) {
       const int s = it % STAGES;
       const uint32_t round = it / STAGES;
       if (!mbar_wait(&tail->full[s], round & 1u, abort_flag, p.err)) return;
-      compute_stage(stage_a(s), stage_b(s), acc, wm, wn, rg, cg);
+      compute_stage_x2(stage_a(s), stage_b(s), acc2, wm, wn, rg, cg);
       mbar_arrive(&tail->empty[s]);
     }
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) unpack2(acc2[i][q], acc[i][2 * q], acc[i][2 * q + 1]);
     epilogue(p, acc, tm, tn, wm, wn, rg, cg);
   }
 }
