@@ -75,6 +75,26 @@ def load_peaks():
             "source": "fallback"}
 
 
+def recorded_traffic(kernel):
+    """DRAM bytes of one launch of `kernel` from the committed ncu record, or
+    None if the kernel's sources changed since the capture."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)[kernel]
+        h = hashlib.sha256()
+        for src in (rec["source"], "dense_gemm_12_gb300/csrc/ptx.cuh",
+                    "dense_gemm_12_gb300/csrc/internal.h"):
+            with open(os.path.join(ROOT, src), "rb") as f:
+                h.update(f.read())
+        if h.hexdigest() != rec["source_sha256"]:
+            return None
+        return rec["dram_read_bytes"] + rec["dram_write_bytes"]
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle-reason sampling while the timed region runs."""
 
@@ -218,7 +238,7 @@ def bench_bf16_8192(torch, g, wl, peaks, device, stream_obj):
         "value": tflops * 1e3, "unit": "GFLOP/s", "ms_per_launch_median": ms,
         "ms_per_launch_min": min(times), "launches_timed": len(times),
         "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
-                     "frac": tflops / peak, "traffic": None,
+                     "frac": tflops / peak, "traffic": recorded_traffic("tc_bf16_kernel"),
                      "peak_note": "%s dense bf16 burst (cuBLAS); sustained %.1f" % (
                          peaks["source"], peaks["bf16_tflops_sustained"])},
         "l2": "operands 256 MB + C 256 MB per launch exceed the 129 MB L2",
@@ -277,7 +297,7 @@ def bench_decode(torch, g, wl, peaks, device, stream_obj):
         "us_per_launch_median": ms * 1e3, "launches_timed": reps * 5,
         "algorithmic_bytes": bytes_alg,
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
-                     "frac": gbs / peak, "traffic": None,
+                     "frac": gbs / peak, "traffic": recorded_traffic("tc_decode_kernel"),
                      "peak_note": "%s STREAM-style copy" % peaks["source"]},
         "l2": "3 copies of B (302 MB) cycled; launches replayed from a CUDA graph",
     }
@@ -291,7 +311,7 @@ def cpu_oracle_sample(wl, target_seconds):
     A, B, C = wl.workload_inputs(w)
     A, B, C = A.numpy(), B.numpy(), C.numpy()
     threads = oracle.max_threads()
-    rows = 4
+    rows = 4 * threads  # calibration sample: a few rows per thread
     t0 = time.perf_counter()
     oracle.sgemm(w.alpha, A[:rows], B, w.beta, C[:rows])
     t = time.perf_counter() - t0
@@ -453,7 +473,8 @@ def run_ours(args):
                        "l2": "two 201 MB input sets used in turn (inputs larger than L2)",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "roofline": {"bound": "alu", "achieved": achieved, "peak": fp32_peak,
-                         "unit": "TFLOP/s", "frac": achieved / fp32_peak, "traffic": None,
+                         "unit": "TFLOP/s", "frac": achieved / fp32_peak,
+                         "traffic": recorded_traffic("simt_gemm_kernel"),
                          "peak_note": "%d SMs x 128 fp32 lanes x 2 FLOP x 2.07 GHz max clock "
                                       "(derived)" % num_sms,
                          "kernel_ms_mean": kernel_ms, "kernel_ms_min": min(launch_ms)},
