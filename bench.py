@@ -174,16 +174,23 @@ def barrier(pg, device):
     import torch
     if pg is not None:
         pg.barrier()
-    torch.cuda.synchronize(device)
+    if torch.device(device).type == "cuda":
+        torch.cuda.synchronize(device)
 
 
 def max_over_ranks(pg, value, device):
+    """The largest `value` over all ranks (every rank gets it)."""
     import torch
     if pg is None:
         return value
     t = torch.tensor([value], dtype=torch.float64, device=device)
     pg.all_reduce(t, op=pg.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_gflops(world, flops_per_step_per_rank, steps, max_ms):
+    """Whole-job throughput: every rank's FLOPs over the slowest rank's time."""
+    return world * flops_per_step_per_rank * steps / (max_ms * 1e-3) / 1e9
 
 
 # ------------------------------------------------------------------ workloads
@@ -411,7 +418,7 @@ def run_ours(args):
         raise RuntimeError("device error: " + g.gemm_status_string(st))
 
     flops_step = w.flops
-    value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e9
+    value = whole_job_gflops(world, flops_step, args.steps, total_ms)
     kernel_ms = statistics.mean(launch_ms)
     achieved = flops_step / (kernel_ms * 1e-3) / 1e12
 
@@ -444,7 +451,7 @@ def run_ours(args):
         b.record(stream_obj)
         barrier(pg, device)
         e2e_ms = max_over_ranks(pg, a.elapsed_time(b), device)
-        e2e = {"value": world * flops_step * n_e2e / (e2e_ms * 1e-3) / 1e9, "unit": "GFLOP/s",
+        e2e = {"value": whole_job_gflops(world, flops_step, n_e2e, e2e_ms), "unit": "GFLOP/s",
                "h2d_bytes_per_step": 3 * w.M * w.K * 4 if w.M == w.K == w.N else None,
                "d2h_bytes_per_step": w.M * w.N * 4, "steps": n_e2e}
         e2e["h2d_bytes_per_step"] = (w.M * w.K + w.K * w.N + w.M * w.N) * 4
