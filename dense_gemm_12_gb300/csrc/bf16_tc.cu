@@ -21,7 +21,9 @@
 //                    masked stores; the second accumulator lets the MMAs of
 //                    the next tile run while this one drains.
 // Persistent CTAs (one per SM) walk the 128 x 256 tiles in a grouped raster
-// order for L2 reuse.  TMA zero-fills beyond M, N, K.
+// order for L2 reuse.  TMA zero-fills beyond M, N, K.  CTAs run in clusters of
+// two along M that share each 64 x 256 slice of B: each CTA loads one half and
+// multicasts it to both (see tc_bf16_kernel).
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -33,7 +35,13 @@ namespace g12 {
 namespace {
 
 constexpr int BM = kTcBM, BN = kTcBN, BK = kTcBK;
-constexpr int STAGES = 4;
+#ifndef G12_TC_STAGES
+#define G12_TC_STAGES 4
+#endif
+#ifndef G12_TC_GROUP_M
+#define G12_TC_GROUP_M 8
+#endif
+constexpr int STAGES = G12_TC_STAGES;
 constexpr int kStageBytesA = BM * BK * 2;            // 16 KB
 constexpr int kStageBytesB = BK * BN * 2;            // 32 KB
 constexpr int kBoxBytesB = BK * 64 * 2;              // one 64-column box, 8 KB
@@ -41,8 +49,13 @@ constexpr int kStageBytes = kStageBytesA + kStageBytesB;
 constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
 constexpr uint32_t kTmemCols = 512;
-constexpr int kGroupM = 16;
+constexpr int kGroupM = G12_TC_GROUP_M;  // raster group height (tile rows or row pairs)
 constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN, /*A MN-major*/ 0, /*B MN-major*/ 1);
+#ifndef G12_TC_CLUSTER_M
+#define G12_TC_CLUSTER_M 2
+#endif
+constexpr int kClusterM = G12_TC_CLUSTER_M;  // CTAs per cluster along M (1 or 2)
+static_assert(kClusterM == 1 || kClusterM == 2, "cluster of 1 or 2 CTAs");
 
 struct __align__(8) TcSmemTail {
   uint64_t full[STAGES];
@@ -114,6 +127,14 @@ __device__ __forceinline__ void store_row_chunk(const TcArgs& p, int row, int co
   }
 }
 
+// CL = CTAs per cluster along M (1 or 2).  With CL = 2 the two CTAs of a
+// cluster compute vertically adjacent tiles (2 pm and 2 pm + 1) of the same
+// 256 columns: each loads its own 128 x 64 slice of A and one half of the
+// shared 64 x 256 slice of B, multicast into both CTAs, so every CTA moves
+// 32 KB instead of 48 KB per k-block from L2.  A stage may be refilled only
+// after the MMAs of both CTAs have read it: each MMA thread commits to the
+// stage's empty barrier in both CTAs (count CL).
+template <int CL>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bf16_kernel(const TcArgs p, const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB) {
@@ -126,13 +147,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int tiles_m = (p.M + BM - 1) / BM;
   const int tiles_n = (p.N + BN - 1) / BN;
-  const int num_tiles = tiles_m * tiles_n;
+  const int groups_m = (tiles_m + CL - 1) / CL;   // tile rows handled per cluster item
+  const int num_items = groups_m * tiles_n;
   const int num_kb = (p.K + BK - 1) / BK;
+  const uint32_t rank = (CL > 1) ? cluster_cta_rank() : 0u;
+  const int first_item = static_cast<int>(blockIdx.x) / CL;
+  const int item_stride = static_cast<int>(gridDim.x) / CL;
+  constexpr uint16_t kPeers = static_cast<uint16_t>((1u << CL) - 1u);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&tail->full[s], 1);
-      mbar_init(&tail->empty[s], 1);
+      mbar_init(&tail->empty[s], CL);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tail->tmem_full[b], 1);
@@ -150,6 +176,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before_sync();
   __syncthreads();
+  // Peers multicast into this CTA's shared memory and barriers: all barriers
+  // of the cluster must be initialised first.
+  if (CL > 1) cluster_sync();
   tc_fence_after_sync();
   const uint32_t tmem_base = tail->tmem_base;
 
@@ -158,9 +187,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-        int tm, tn;
-        tile_coords(t, tiles_m, tiles_n, tm, tn);
+      for (int t = first_item; t < num_items && ok; t += item_stride) {
+        int pm, tn;
+        tile_coords(t, groups_m, tiles_n, pm, tn);
+        const int tm = pm * CL + static_cast<int>(rank);
         for (int kb = 0; kb < num_kb; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t round = it / STAGES;
@@ -170,11 +200,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint8_t* sa = smem + s * kStageBytes;
           uint8_t* sb = sa + kStageBytesA;
+          // all 48 KB arrive here: A from this CTA, B half from each CTA
           mbar_arrive_expect_tx(&tail->full[s], kStageBytes);
           tma_load_2d(sa, &tmA, kb * BK, tm * BM, &tail->full[s]);
+          if (CL == 1) {
 #pragma unroll
-          for (int j = 0; j < BN / 64; ++j)
-            tma_load_2d(sb + j * kBoxBytesB, &tmB, tn * BN + j * 64, kb * BK, &tail->full[s]);
+            for (int j = 0; j < BN / 64; ++j)
+              tma_load_2d(sb + j * kBoxBytesB, &tmB, tn * BN + j * 64, kb * BK, &tail->full[s]);
+          } else {
+#pragma unroll
+            for (int jj = 0; jj < BN / 64 / CL; ++jj) {
+              const int j = static_cast<int>(rank) * (BN / 64 / CL) + jj;
+              tma_load_2d_multicast(sb + j * kBoxBytesB, &tmB, tn * BN + j * 64, kb * BK,
+                                    &tail->full[s], kPeers);
+            }
+          }
         }
       }
       if (!ok) {
@@ -191,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t j = 0;
       bool ok = true;
       bool issued = false;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++j) {
+      for (int t = first_item; t < num_items && ok; t += item_stride, ++j) {
         const uint32_t ab = j & 1u, ar = j >> 1;
         if (!mbar_wait(&tail->tmem_empty[ab], (ar & 1u) ^ 1u, abort_flag, p.err)) {
           ok = false;
@@ -219,7 +259,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_mma_f16(d_tmem, adesc, bdesc, kIdesc, (kb | kk) != 0 ? 1u : 0u);
           }
           issued = true;
-          tc_commit(&tail->empty[s]);
+          if (CL == 1)
+            tc_commit(&tail->empty[s]);
+          else
+            tc_commit_multicast(&tail->empty[s], kPeers);  // frees the stage in both CTAs
         }
         if (!ok) break;
         tc_commit(&tail->tmem_full[ab]);
@@ -235,9 +278,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // -------------------------------------------------------- epilogue
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     uint32_t j = 0;
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++j) {
-      int tm, tn;
-      tile_coords(t, tiles_m, tiles_n, tm, tn);
+    for (int t = first_item; t < num_items; t += item_stride, ++j) {
+      int pm, tn;
+      tile_coords(t, groups_m, tiles_n, pm, tn);
+      const int tm = pm * CL + static_cast<int>(rank);
       const uint32_t ab = j & 1u, ar = j >> 1;
       if (!mbar_wait(&tail->tmem_full[ab], ar & 1u, abort_flag, p.err)) break;
       tc_fence_after_sync();
@@ -257,6 +301,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before_sync();
   __syncthreads();
+  // No CTA may exit while its peer can still multicast into it.
+  if (CL > 1) cluster_sync();
   tc_fence_after_sync();
   if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
 }
@@ -265,12 +311,47 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 cudaError_t launch_tc_bf16(const TcArgs& a, const CUtensorMap* tmA, const CUtensorMap* tmB,
                            int num_sms, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(tc_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const int tiles_m = (a.M + BM - 1) / BM;
+  const int tiles_n = (a.N + BN - 1) / BN;
+  if (kClusterM > 1 && tiles_m >= kClusterM) {
+    auto kernel = tc_bf16_kernel<kClusterM>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kClusterM;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // Persistent clusters: as many as can be resident at once, at most one
+    // per pair of tiles.
+    const int items = ((tiles_m + kClusterM - 1) / kClusterM) * tiles_n;
+    int max_clusters = 0;
+    cfg.gridDim = dim3(kClusterM * (num_sms / kClusterM));
+    if (cudaOccupancyMaxActiveClusters(&max_clusters, kernel, &cfg) != cudaSuccess ||
+        max_clusters < 1) {
+      cudaGetLastError();
+      max_clusters = num_sms / kClusterM;
+    }
+    const int clusters = items < max_clusters ? items : max_clusters;
+    cfg.gridDim = dim3(kClusterM * clusters);
+    e = cudaLaunchKernelEx(&cfg, kernel, a, *tmA, *tmB);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+  }
+  auto kernel = tc_bf16_kernel<1>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
-  const int tiles = ((a.M + BM - 1) / BM) * ((a.N + BN - 1) / BN);
+  const int tiles = tiles_m * tiles_n;
   const int grid = tiles < num_sms ? tiles : num_sms;
-  tc_bf16_kernel<<<grid, kThreads, kSmemBytes, stream>>>(a, *tmA, *tmB);
+  kernel<<<grid, kThreads, kSmemBytes, stream>>>(a, *tmA, *tmB);
   return cudaGetLastError();
 }
 
