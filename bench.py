@@ -252,6 +252,41 @@ def bench_bf16_8192(torch, g, wl, peaks, device, stream_obj):
     }
 
 
+def bench_bf16_8192_fused(torch, g, wl, peaks, device, stream_obj):
+    """The bf16 8192^3 GEMM with the fused output stage: bias + GELU, bf16 D."""
+    w = wl.WORKLOADS["bf16_8192"]
+    A, B, _ = wl.workload_inputs(w, with_c=False)
+    A, B = A.to(device), B.to(device)
+    bias = (torch.randn(w.N, generator=torch.Generator().manual_seed(9)) * 0.1).to(device)
+    D = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=device)
+    s = stream_obj.cuda_stream
+
+    def step(i):
+        st = g.gemm_bf16gemm_epilogue(w.M, w.N, w.K, w.alpha, A.data_ptr(), w.K, B.data_ptr(), w.N,
+                                      0.0, 0, w.N, bias.data_ptr(), g.ACT["gelu"], D.data_ptr(),
+                                      w.N, g.OUT["bf16"], s)
+        if st != 0:
+            raise RuntimeError("gemm_bf16gemm_epilogue: " + g.gemm_status_string(st))
+    for i in range(3):
+        step(i)
+    torch.cuda.synchronize()
+    times = time_launches(torch, step, 10, stream_obj)
+    ms = statistics.median(times)
+    tflops = w.flops / (ms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"]
+    del A, B, D, bias
+    torch.cuda.empty_cache()
+    return {
+        "workload": "bf16 GEMM M=N=K=8192 with fused bias + GELU, bf16 output",
+        "kernel": "tc_bf16_kernel (same kernel, fused output stage)",
+        "value": tflops * 1e3, "unit": "GFLOP/s", "ms_per_launch_median": ms,
+        "launches_timed": len(times),
+        "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                     "frac": tflops / peak, "traffic": None,
+                     "peak_note": "%s dense bf16 burst (cuBLAS)" % peaks["source"]},
+    }
+
+
 def bench_decode(torch, g, wl, peaks, device, stream_obj):
     w = wl.WORKLOADS["decode_16"]
     A, B, C0 = wl.workload_inputs(w)
@@ -422,46 +457,72 @@ def run_ours(args):
     kernel_ms = statistics.mean(launch_ms)
     achieved = flops_step / (kernel_ms * 1e-3) / 1e12
 
-    # e2e: host buffers through the C ABI, copies inside the timed region
+    # e2e: host buffers through the C ABI, copies inside the timed region.
+    # Every step copies its A, B, C in from pinned host memory and its C out.
+    # The copies are pipelined with the GEMMs on separate streams over the two
+    # device buffer sets: while step i computes on set i % 2, the inputs of
+    # step i + 1 are copied into the other set and the result of step i - 1 is
+    # copied out.
     e2e = None
     if not args.no_e2e:
         pinned = [tuple(t.pin_memory() for t in hs) for hs in host_sets]
-        out_host = torch.empty((w.M, w.N), dtype=torch.float32).pin_memory()
+        outs = [torch.empty((w.M, w.N), dtype=torch.float32).pin_memory() for _ in range(2)]
         dev_bufs = sets
+        s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
+        loaded = [torch.cuda.Event() for _ in range(2)]
+        computed = [torch.cuda.Event() for _ in range(2)]
+        freed = [None, None]
 
         def e2e_step(i):
-            hA, hB, hC = pinned[i % 2]
-            dA, dB, dC = dev_bufs[i % 2]
-            dA.copy_(hA, non_blocking=True)
-            dB.copy_(hB, non_blocking=True)
-            dC.copy_(hC, non_blocking=True)
+            k = i % 2
+            hA, hB, hC = pinned[k]
+            dA, dB, dC = dev_bufs[k]
+            with torch.cuda.stream(s_in):
+                if freed[k] is not None:
+                    s_in.wait_event(freed[k])      # step i-2 is done with set k
+                dA.copy_(hA, non_blocking=True)
+                dB.copy_(hB, non_blocking=True)
+                dC.copy_(hC, non_blocking=True)
+                loaded[k].record(s_in)
+            stream_obj.wait_event(loaded[k])
             s_ = g.gemm_sgemm(w.M, w.N, w.K, w.alpha, dA.data_ptr(), w.K, dB.data_ptr(), w.N,
                               w.beta, dC.data_ptr(), w.N, stream)
             if s_ != 0:
                 raise RuntimeError(g.gemm_status_string(s_))
-            out_host.copy_(dC, non_blocking=True)
+            computed[k].record(stream_obj)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(computed[k])
+                outs[k].copy_(dC, non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(s_out)
+                freed[k] = ev
         e2e_step(0)
+        e2e_step(1)
+        torch.cuda.synchronize(device)
         barrier(pg, device)
         n_e2e = max(3, min(args.steps, 10))
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
-        a.record(stream_obj)
+        a.record(s_in)
         for i in range(n_e2e):
             e2e_step(i)
-        b.record(stream_obj)
+        b.record(s_out)
+        torch.cuda.synchronize(device)
         barrier(pg, device)
         e2e_ms = max_over_ranks(pg, a.elapsed_time(b), device)
         e2e = {"value": whole_job_gflops(world, flops_step, n_e2e, e2e_ms), "unit": "GFLOP/s",
-               "h2d_bytes_per_step": 3 * w.M * w.K * 4 if w.M == w.K == w.N else None,
-               "d2h_bytes_per_step": w.M * w.N * 4, "steps": n_e2e}
-        e2e["h2d_bytes_per_step"] = (w.M * w.K + w.K * w.N + w.M * w.N) * 4
-        del pinned, out_host
+               "h2d_bytes_per_step": (w.M * w.K + w.K * w.N + w.M * w.N) * 4,
+               "d2h_bytes_per_step": w.M * w.N * 4, "steps": n_e2e,
+               "pipelined": "copies of step i+1 and i-1 overlap the GEMM of step i"}
+        del pinned, outs
 
     parts = {}
     if not args.no_parts and rank == 0:
         del sets
         torch.cuda.empty_cache()
         parts["bf16_8192"] = bench_bf16_8192(torch, g, wl, peaks, device, stream_obj)
+        parts["bf16_8192_bias_gelu_bf16out"] = bench_bf16_8192_fused(torch, g, wl, peaks, device,
+                                                                      stream_obj)
         parts["decode_16x12288x4096"] = bench_decode(torch, g, wl, peaks, device, stream_obj)
 
     cpu = None

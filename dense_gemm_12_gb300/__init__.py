@@ -20,7 +20,7 @@ from . import _build
 
 __all__ = [
     "GemmError", "load_library", "library_path", "gemm_sgemm", "gemm_bf16gemm",
-    "gemm_bf16gemm_decode_static",
+    "gemm_bf16gemm_decode_static", "gemm_bf16gemm_epilogue", "bf16gemm_epilogue", "ACT", "OUT",
     "gemm_status_string", "gemm_check_device_error", "gemm_shutdown",
     "gemm_select_path", "gemm_quantization", "gemm_version", "sgemm", "bf16gemm",
     "STATUS", "PATHS",
@@ -84,6 +84,9 @@ def load_library(build_if_missing: bool = False):
         lib.gemm_bf16gemm.restype = cint
         lib.gemm_bf16gemm_decode_static.argtypes = gemm_args
         lib.gemm_bf16gemm_decode_static.restype = cint
+        lib.gemm_bf16gemm_epilogue.argtypes = [i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64,
+                                               vp, cint, vp, i64, cint, vp]
+        lib.gemm_bf16gemm_epilogue.restype = cint
         lib.gemm_status_string.argtypes = [cint]
         lib.gemm_status_string.restype = ctypes.c_char_p
         lib.gemm_check_device_error.argtypes = [vp]
@@ -117,6 +120,18 @@ def gemm_bf16gemm_decode_static(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, st
     library-owned array); see include/gemm12.h. Returns the status."""
     return load_library().gemm_bf16gemm_decode_static(M, N, K, alpha, A, lda, B, ldb, beta, C,
                                                       ldc, stream)
+
+
+ACT = {"none": 0, "relu": 1, "gelu": 2}
+OUT = {"f32": 0, "bf16": 1}
+
+
+def gemm_bf16gemm_epilogue(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, bias, act, D, ldd,
+                           d_type, stream=0) -> int:
+    """bf16 GEMM with fused bias / activation / output type (see include/gemm12.h).
+    act and d_type are the C enum values (ACT / OUT). Returns the status."""
+    return load_library().gemm_bf16gemm_epilogue(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                                                 bias, act, D, ldd, d_type, stream)
 
 
 def gemm_status_string(status: int) -> str:
@@ -203,3 +218,36 @@ def bf16gemm(A, B, C, alpha=1.0, beta=0.0, stream=None):
     if st != 0:
         raise GemmError(st, "gemm_bf16gemm")
     return C
+
+
+def bf16gemm_epilogue(A, B, D, C=None, alpha=1.0, beta=0.0, bias=None, act="none", stream=None):
+    """D <- act(alpha*(A @ B) + beta*C + bias); A, B bf16, C and bias fp32, D fp32
+    or bf16 (all CUDA tensors, row-major)."""
+    import torch
+    for t, n in ((A, "A"), (B, "B")):
+        if t.dtype != torch.bfloat16 or not t.is_cuda:
+            raise TypeError("%s must be a bfloat16 CUDA tensor" % n)
+    if D.dtype not in (torch.float32, torch.bfloat16) or not D.is_cuda:
+        raise TypeError("D must be a float32 or bfloat16 CUDA tensor")
+    M, K = A.shape
+    N = B.shape[1]
+    if B.shape[0] != K or tuple(D.shape) != (M, N):
+        raise ValueError("shape mismatch")
+    c_ptr, ldc = 0, max(N, 1)
+    if C is not None:
+        if C.dtype != torch.float32 or tuple(C.shape) != (M, N):
+            raise TypeError("C must be a float32 (M, N) tensor")
+        c_ptr, ldc = C.data_ptr(), _row_major_ld(C, "C")
+    b_ptr = 0
+    if bias is not None:
+        if bias.dtype != torch.float32 or bias.numel() != N or not bias.is_contiguous():
+            raise TypeError("bias must be a contiguous float32 tensor of N values")
+        b_ptr = bias.data_ptr()
+    st = gemm_bf16gemm_epilogue(M, N, K, float(alpha), A.data_ptr(), _row_major_ld(A, "A"),
+                                B.data_ptr(), _row_major_ld(B, "B"), float(beta), c_ptr, ldc,
+                                b_ptr, ACT[act], D.data_ptr(), _row_major_ld(D, "D"),
+                                OUT["bf16" if D.dtype == torch.bfloat16 else "f32"],
+                                _stream_handle(stream, D.device))
+    if st != 0:
+        raise GemmError(st, "gemm_bf16gemm_epilogue")
+    return D

@@ -214,6 +214,50 @@ cudaError_t launch_scale_c(int M, int N, float beta, float* C, int64_t ldc, cuda
   return cudaGetLastError();
 }
 
+Epilogue plain_epilogue(float alpha, float beta, float* C, int64_t ldc) {
+  Epilogue e{};
+  e.alpha = alpha;
+  e.beta = beta;
+  e.C = C;
+  e.ldc = ldc;
+  e.D = C;
+  e.ldd = ldc;
+  e.bias = nullptr;
+  e.act = kActNone;
+  e.d_bf16 = 0;
+  const int v = (reinterpret_cast<uintptr_t>(C) & 15u) == 0 && ldc % 4 == 0 ? 1 : 0;
+  e.c_vec4 = v;
+  e.d_vec = v;
+  return e;
+}
+
+namespace {
+// D <- act(beta * C + bias): the fused output stage when the product is empty
+// (K == 0 or alpha == 0).
+__global__ void epilogue_only_kernel(int M, int N, Epilogue e) {
+  const int64_t total = static_cast<int64_t>(M) * N;
+  for (int64_t x = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; x < total;
+       x += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t i = x / N;
+    const int j = static_cast<int>(x - i * N);
+    const float c_old = (e.beta != 0.0f) ? e.C[i * e.ldc + j] : 0.0f;
+    float v = e.beta * c_old;
+    if (e.beta == 0.0f) v = 0.0f;
+    v += epi_bias(e, j);
+    epi_store1(e, i, j, epi_activate(e.act, v));
+  }
+}
+}  // namespace
+
+cudaError_t launch_epilogue_only(int M, int N, const Epilogue& e, cudaStream_t stream) {
+  const int64_t total = static_cast<int64_t>(M) * N;
+  int64_t blocks = (total + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  if (blocks < 1) blocks = 1;
+  epilogue_only_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(M, N, e);
+  return cudaGetLastError();
+}
+
 // Shared pieces of the C ABI for entry points defined in other translation
 // units (thin wrappers; the entry points above do not use them).
 gemm_status_t abi_check_args(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
@@ -338,6 +382,48 @@ gemm_status_t gemm_sgemm(int64_t M, int64_t N, int64_t K, float alpha, const flo
                                mb == kLoadTma ? &tmB : nullptr, st->num_sms, cs));
 }
 
+// Runs the tensor-core path (tile kernel or decode kernel) of a bf16 GEMM
+// whose operands TMA can describe, with output stage `epi`.
+static gemm_status_t run_bf16_tensor_core(DeviceState* st, gemm_path_t path, int64_t M, int64_t N,
+                                          int64_t K, const void* A, int64_t lda, const void* B,
+                                          int64_t ldb, const Epilogue& epi, cudaStream_t cs) {
+  CUtensorMap tmA, tmB;
+  if (path == GEMM_PATH_TC_BF16) {
+    if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, K, M, lda, kTcBK, kTcBM,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, N, K, ldb, 64, kTcBK,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+      return GEMM_ERR_LAUNCH;
+    TcArgs a{};
+    a.M = static_cast<int>(M);
+    a.N = static_cast<int>(N);
+    a.K = static_cast<int>(K);
+    a.epi = epi;
+    a.err = st->err_word;
+    return from_cuda(launch_tc_bf16(a, &tmA, &tmB, st->num_sms, cs));
+  }
+  // GEMM_PATH_TC_DECODE
+  if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, K, M, lda, 64, kDecBM,
+                 CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, N, K, ldb, 64,
+                 static_cast<uint32_t>(decode_b_box_rows()), CU_TENSOR_MAP_SWIZZLE_128B))
+    return GEMM_ERR_LAUNCH;
+  const int grid = decode_grid(static_cast<int>(N), static_cast<int>(K), st->num_sms);
+  DecodeArgs a{};
+  a.M = static_cast<int>(M);
+  a.N = static_cast<int>(N);
+  a.K = static_cast<int>(K);
+  a.epi = epi;
+  a.err = st->err_word;
+  std::lock_guard<std::mutex> lock(st->ws_mutex);
+  gemm_status_t s = ensure_decode_workspace(*st, decode_workspace_floats(a.N, a.K, grid),
+                                            decode_counter_count(a.N));
+  if (s != GEMM_OK) return s;
+  a.workspace = st->ws;
+  a.counters = st->counters;
+  return from_cuda(launch_tc_decode(a, &tmA, &tmB, grid, cs));
+}
+
 gemm_status_t gemm_bf16gemm(int64_t M, int64_t N, int64_t K, float alpha, const void* A,
                             int64_t lda, const void* B, int64_t ldb, float beta, float* C,
                             int64_t ldc, void* stream) {
@@ -375,51 +461,51 @@ gemm_status_t gemm_bf16gemm(int64_t M, int64_t N, int64_t K, float alpha, const 
     return from_cuda(launch_simt(a, kLoadConvertBf16, kLoadConvertBf16, nullptr, nullptr,
                                  st->num_sms, cs));
   }
+  return run_bf16_tensor_core(st, path, M, N, K, A, lda, B, ldb,
+                              plain_epilogue(alpha, beta, C, ldc), cs);
+}
 
-  CUtensorMap tmA, tmB;
-  if (path == GEMM_PATH_TC_BF16) {
-    if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, K, M, lda, kTcBK, kTcBM,
-                   CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, N, K, ldb, 64, kTcBK,
-                   CU_TENSOR_MAP_SWIZZLE_128B))
-      return GEMM_ERR_LAUNCH;
-    TcArgs a{};
-    a.M = static_cast<int>(M);
-    a.N = static_cast<int>(N);
-    a.K = static_cast<int>(K);
-    a.alpha = alpha;
-    a.beta = beta;
-    a.C = C;
-    a.ldc = ldc;
-    a.c_vec4 = c_vec4_ok(C, ldc);
-    a.err = st->err_word;
-    return from_cuda(launch_tc_bf16(a, &tmA, &tmB, st->num_sms, cs));
-  }
-
-  // GEMM_PATH_TC_DECODE
-  if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, K, M, lda, 64, kDecBM,
-                 CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, N, K, ldb, 64,
-                 static_cast<uint32_t>(decode_b_box_rows()),
-                 CU_TENSOR_MAP_SWIZZLE_128B))
-    return GEMM_ERR_LAUNCH;
-  const int grid = decode_grid(static_cast<int>(N), static_cast<int>(K), st->num_sms);
-  DecodeArgs a{};
-  a.M = static_cast<int>(M);
-  a.N = static_cast<int>(N);
-  a.K = static_cast<int>(K);
-  a.alpha = alpha;
-  a.beta = beta;
-  a.C = C;
-  a.ldc = ldc;
-  a.err = st->err_word;
-  std::lock_guard<std::mutex> lock(st->ws_mutex);
-  s = ensure_decode_workspace(*st, decode_workspace_floats(a.N, a.K, grid),
-                              decode_counter_count(a.N));
+gemm_status_t gemm_bf16gemm_epilogue(int64_t M, int64_t N, int64_t K, float alpha,
+                                     const void* A, int64_t lda, const void* B, int64_t ldb,
+                                     float beta, const float* C, int64_t ldc, const float* bias,
+                                     int act, void* D, int64_t ldd, int d_type, void* stream) {
+  if (act != GEMM_ACT_NONE && act != GEMM_ACT_RELU && act != GEMM_ACT_GELU)
+    return GEMM_ERR_INVALID_VALUE;
+  if (d_type != GEMM_OUT_F32 && d_type != GEMM_OUT_BF16) return GEMM_ERR_INVALID_VALUE;
+  gemm_status_t s = check_common(M, N, K, lda, ldb, beta != 0.0f ? ldc : (N > 1 ? N : 1));
   if (s != GEMM_OK) return s;
-  a.workspace = st->ws;
-  a.counters = st->counters;
-  return from_cuda(launch_tc_decode(a, &tmA, &tmB, grid, cs));
+  if (ldd < (N > 1 ? N : 1) || ldd > kMaxDim) return GEMM_ERR_INVALID_VALUE;
+  const gemm_path_t path = select_path(true, M, N, K, alpha, A, lda, B, ldb);
+  if (path == GEMM_PATH_NONE) return GEMM_OK;
+  const uintptr_t d_align = d_type == GEMM_OUT_BF16 ? 1u : 3u;
+  if (D == nullptr || (reinterpret_cast<uintptr_t>(D) & d_align)) return GEMM_ERR_INVALID_VALUE;
+  if (beta != 0.0f && (C == nullptr || (reinterpret_cast<uintptr_t>(C) & 3u)))
+    return GEMM_ERR_INVALID_VALUE;
+  if (bias != nullptr && (reinterpret_cast<uintptr_t>(bias) & 3u)) return GEMM_ERR_INVALID_VALUE;
+  if (path != GEMM_PATH_SCALE_C) {
+    if (A == nullptr || B == nullptr) return GEMM_ERR_INVALID_VALUE;
+    if ((reinterpret_cast<uintptr_t>(A) & 1u) || (reinterpret_cast<uintptr_t>(B) & 1u))
+      return GEMM_ERR_MISALIGNED;
+    if (path == GEMM_PATH_SIMT_BF16) return GEMM_ERR_UNSUPPORTED;
+  }
+  DeviceState* st = device_state(&s);
+  if (st == nullptr) return s;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  Epilogue epi{};
+  epi.alpha = alpha;
+  epi.beta = beta;
+  epi.C = C;
+  epi.ldc = ldc;
+  epi.D = D;
+  epi.ldd = ldd;
+  epi.bias = bias;
+  epi.act = act;
+  epi.d_bf16 = d_type == GEMM_OUT_BF16 ? 1 : 0;
+  epi.c_vec4 = (beta != 0.0f) ? c_vec4_ok(C, ldc) : 0;
+  epi.d_vec = aligned16(D) && (ldd % (epi.d_bf16 ? 8 : 4) == 0) ? 1 : 0;
+  if (path == GEMM_PATH_SCALE_C)
+    return from_cuda(launch_epilogue_only(static_cast<int>(M), static_cast<int>(N), epi, cs));
+  return run_bf16_tensor_core(st, path, M, N, K, A, lda, B, ldb, epi, cs);
 }
 
 gemm_status_t gemm_check_device_error(void* stream) {

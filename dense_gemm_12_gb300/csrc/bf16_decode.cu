@@ -150,26 +150,40 @@ __device__ __forceinline__ void named_bar_epi() {
 // Old values of column n of C (rows < M), loaded ahead of time so that the
 // final write of a column costs no read round trip.
 __device__ __forceinline__ void load_c_column(const DecodeArgs& p, int n, float (&old)[BMr]) {
+  const Epilogue& e = p.epi;
+  const float* c = e.C + n;
 #pragma unroll
   for (int m = 0; m < BMr; ++m)
-    old[m] = (p.beta != 0.0f && n < p.N && m < p.M) ? p.C[static_cast<int64_t>(m) * p.ldc + n]
-                                                     : 0.0f;
+    old[m] = (e.beta != 0.0f && n < p.N && m < p.M) ? c[static_cast<int64_t>(m) * e.ldc] : 0.0f;
 }
 
-// C[m][n] = alpha * v[m] + beta * old[m] for the column n of this thread.
+// D[m][n] = act(alpha * v[m] + beta * old[m] + bias[n]) for the column n of
+// this thread.  FUSED = false is the plain GEMM output (fp32, no bias, no
+// activation), compiled without the general stage.
+template <bool FUSED>
 __device__ __forceinline__ void store_c_column(const DecodeArgs& p, int n, const float (&v)[BMr],
                                                const float (&old)[BMr]) {
   if (n >= p.N) return;
-  float* c = p.C + n;
+  const Epilogue& e = p.epi;
+  if (!FUSED) {
+    // plain GEMM: D is C itself (fp32, ldd == ldc)
+    float* d = static_cast<float*>(e.D) + n;
+#pragma unroll
+    for (int m = 0; m < BMr; ++m)
+      if (m < p.M)
+        d[static_cast<int64_t>(m) * e.ldc] =
+            (e.beta != 0.0f) ? fmaf(e.alpha, v[m], e.beta * old[m]) : e.alpha * v[m];
+    return;
+  }
+  const float bias = epi_bias(e, n);  // one column: one bias value, loaded before any store
 #pragma unroll
   for (int m = 0; m < BMr; ++m)
-    if (m < p.M)
-      c[static_cast<int64_t>(m) * p.ldc] =
-          (p.beta != 0.0f) ? fmaf(p.alpha, v[m], p.beta * old[m]) : p.alpha * v[m];
+    if (m < p.M) epi_store1(e, m, n, epi_value(e, v[m], old[m], bias));
 }
 
+template <bool FUSED>
 __global__ void __launch_bounds__(kThreads, 1)
-    tc_decode_kernel(const DecodeArgs p, const __grid_constant__ CUtensorMap tmA,
+    tc_decode_kernel(const __grid_constant__ DecodeArgs p, const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = align_smem<1024>(smem_raw);
@@ -432,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float v[BMr];
 #pragma unroll
           for (int m = 0; m < BMr; ++m) v[m] = __uint_as_float(r[j][m]);
-          store_c_column(p, row_valid ? ng * NW + j * BN + n_local : p.N, v, old[j]);
+          store_c_column<FUSED>(p, row_valid ? ng * NW + j * BN + n_local : p.N, v, old[j]);
         }
       } else {
         // last_flag: 2 = every other contributor had already arrived (this
@@ -503,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   sum[m] += row_valid ? __ldcg(src + m * NW + j * BN + n_local) : 0.0f;
               }
             }
-            store_c_column(p, row_valid ? ng * NW + j * BN + n_local : p.N, sum, old[j]);
+            store_c_column<FUSED>(p, row_valid ? ng * NW + j * BN + n_local : p.N, sum, old[j]);
           }
           if (ept == 0) p.counters[ng] = 0u;
         }
@@ -546,8 +560,9 @@ int64_t decode_counter_count(int N) { return (N + NW - 1) / NW; }
 
 cudaError_t launch_tc_decode(const DecodeArgs& a, const CUtensorMap* tmA, const CUtensorMap* tmB,
                              int num_ctas, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(tc_decode_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const bool fused = a.epi.bias != nullptr || a.epi.act != kActNone || a.epi.d_bf16;
+  auto kernel = fused ? tc_decode_kernel<true> : tc_decode_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
   // Programmatic stream serialization: this launch may begin while the
@@ -562,7 +577,7 @@ cudaError_t launch_tc_decode(const DecodeArgs& a, const CUtensorMap* tmA, const 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, tc_decode_kernel, a, *tmA, *tmB);
+  e = cudaLaunchKernelEx(&cfg, kernel, a, *tmA, *tmB);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

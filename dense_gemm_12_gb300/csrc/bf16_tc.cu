@@ -79,50 +79,61 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
   tn = local / rows;
 }
 
+// One 32-column chunk of an accumulator row: D = act(alpha*acc + beta*C + bias).
+// Old C values are all loaded before the first store, so the loads overlap
+// (interleaved load/store pairs to possibly aliasing addresses would cost a
+// memory round trip each).
 __device__ __forceinline__ void store_row_chunk(const TcArgs& p, int row, int col0,
                                                 const uint32_t (&r)[32]) {
-  float* c_row = p.C + static_cast<int64_t>(row) * p.ldc;
-  const bool read_c = (p.beta != 0.0f);
-  if (p.c_vec4 && col0 + 31 < p.N) {
-    // Old values first, then the stores (see the note in the else branch).
-    float4 old[8];
+  const Epilogue& e = p.epi;
+  const bool read_c = (e.beta != 0.0f);
+  const float* c_row = e.C + static_cast<int64_t>(row) * e.ldc;
+  if (col0 + 31 < p.N) {
+    float old[32];
     if (read_c) {
+      if (e.c_vec4) {
 #pragma unroll
-      for (int q = 0; q < 8; ++q) old[q] = *reinterpret_cast<const float4*>(c_row + col0 + 4 * q);
-    }
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      float4* dst = reinterpret_cast<float4*>(c_row + col0 + 4 * q);
-      float4 v = make_float4(__uint_as_float(r[4 * q + 0]), __uint_as_float(r[4 * q + 1]),
-                             __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
-      if (read_c) {
-        const float4 o = old[q];
-        v.x = fmaf(p.alpha, v.x, p.beta * o.x);
-        v.y = fmaf(p.alpha, v.y, p.beta * o.y);
-        v.z = fmaf(p.alpha, v.z, p.beta * o.z);
-        v.w = fmaf(p.alpha, v.w, p.beta * o.w);
+        for (int q = 0; q < 8; ++q) {
+          const float4 o = *reinterpret_cast<const float4*>(c_row + col0 + 4 * q);
+          old[4 * q + 0] = o.x;
+          old[4 * q + 1] = o.y;
+          old[4 * q + 2] = o.z;
+          old[4 * q + 3] = o.w;
+        }
       } else {
-        v.x *= p.alpha;
-        v.y *= p.alpha;
-        v.z *= p.alpha;
-        v.w *= p.alpha;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) old[c] = c_row[col0 + c];
       }
-      *dst = v;
+    }
+    float bias[32];
+#pragma unroll
+    for (int c = 0; c < 32; ++c) bias[c] = epi_bias(e, col0 + c);
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      float v[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        v[c] = epi_value(e, __uint_as_float(r[8 * h + c]), read_c ? old[8 * h + c] : 0.0f,
+                         bias[8 * h + c]);
+      if (e.d_vec) {
+        epi_store8(e, row, col0 + 8 * h, v);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) epi_store1(e, row, col0 + 8 * h + c, v[c]);
+      }
     }
   } else {
-    // Ragged or unaligned edge.  Loading every old value before the first
-    // store keeps the loads independent; interleaved load/store pairs to
-    // possibly aliasing addresses would cost one memory round trip each.
-    float old[32];
+    // ragged right edge
+    float old[32], bias[32];
 #pragma unroll
-    for (int c = 0; c < 32; ++c) old[c] = (read_c && col0 + c < p.N) ? c_row[col0 + c] : 0.0f;
+    for (int c = 0; c < 32; ++c) {
+      old[c] = (read_c && col0 + c < p.N) ? c_row[col0 + c] : 0.0f;
+      bias[c] = (col0 + c < p.N) ? epi_bias(e, col0 + c) : 0.0f;
+    }
 #pragma unroll
     for (int c = 0; c < 32; ++c) {
       const int col = col0 + c;
-      if (col < p.N) {
-        const float v = __uint_as_float(r[c]);
-        c_row[col] = read_c ? fmaf(p.alpha, v, p.beta * old[c]) : p.alpha * v;
-      }
+      if (col < p.N) epi_store1(e, row, col, epi_value(e, __uint_as_float(r[c]), old[c], bias[c]));
     }
   }
 }
@@ -136,7 +147,7 @@ __device__ __forceinline__ void store_row_chunk(const TcArgs& p, int row, int co
 // stage's empty barrier in both CTAs (count CL).
 template <int CL>
 __global__ void __launch_bounds__(kThreads, 1)
-    tc_bf16_kernel(const TcArgs p, const __grid_constant__ CUtensorMap tmA,
+    tc_bf16_kernel(const __grid_constant__ TcArgs p, const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = align_smem<1024>(smem_raw);

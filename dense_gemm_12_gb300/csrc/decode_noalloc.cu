@@ -121,10 +121,7 @@ extern "C" gemm_status_t gemm_bf16gemm_decode_static(int64_t M, int64_t N, int64
   a.M = static_cast<int>(M);
   a.N = n;
   a.K = k;
-  a.alpha = alpha;
-  a.beta = beta;
-  a.C = C;
-  a.ldc = ldc;
+  a.epi = plain_epilogue(alpha, beta, C, ldc);
   a.counters = scratch;
   a.workspace = reinterpret_cast<float*>(scratch + kStaticCounters);
   a.err = err_word;

@@ -6,6 +6,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "epilogue.cuh"
+
 namespace g12 {
 
 // How one operand of the CUDA-core kernel reaches shared memory.
@@ -39,10 +41,7 @@ constexpr int kSimtBM = 128, kSimtBN = 128, kSimtBK = 32;
 
 struct TcArgs {
   int M, N, K;
-  float alpha, beta;
-  float* C;
-  int64_t ldc;
-  int c_vec4;
+  Epilogue epi;
   uint32_t* err;
 };
 
@@ -53,9 +52,7 @@ constexpr int kTcBM = 128, kTcBN = 256, kTcBK = 64;
 
 struct DecodeArgs {
   int M, N, K;
-  float alpha, beta;
-  float* C;
-  int64_t ldc;
+  Epilogue epi;
   float* workspace;     // partial sums, see decode_workspace_floats
   uint32_t* counters;   // one arrival counter per 128-column n-tile, zeroed
   uint32_t* err;
@@ -85,6 +82,12 @@ bool abi_encode_bf16_2d(CUtensorMap* map, const void* base, int64_t inner, int64
 // Current device's SM count and error-word address (GEMM_OK), or the status
 // the entry points return when there is no usable sm_103a device.
 gemm_status_t abi_device(int* num_sms, uint32_t** err_word);
+
+// The output stage of the plain GEMM: D = C (fp32, in place), no bias, no
+// activation.
+Epilogue plain_epilogue(float alpha, float beta, float* C, int64_t ldc);
+// D <- act(beta * C + bias) for an empty product.
+cudaError_t launch_epilogue_only(int M, int N, const Epilogue& e, cudaStream_t stream);
 
 // C <- beta * C (beta == 0 writes zeros without reading C).
 cudaError_t launch_scale_c(int M, int N, float beta, float* C, int64_t ldc,

@@ -110,6 +110,46 @@ gemm_status_t gemm_bf16gemm(int64_t M, int64_t N, int64_t K, float alpha,
                             const void *B, int64_t ldb,
                             float beta, float *C, int64_t ldc, void *stream);
 
+/* Activations and output types of gemm_bf16gemm_epilogue. */
+typedef enum {
+    GEMM_ACT_NONE = 0,   /* identity                                           */
+    GEMM_ACT_RELU = 1,   /* max(x, 0)                                          */
+    GEMM_ACT_GELU = 2    /* x * Phi(x) = 0.5 x (1 + erf(x / sqrt(2)))           */
+} gemm_act_t;
+
+typedef enum {
+    GEMM_OUT_F32 = 0,    /* D holds fp32                                       */
+    GEMM_OUT_BF16 = 1    /* D holds bf16, rounded to nearest even              */
+} gemm_out_t;
+
+/*
+ * gemm_bf16gemm_epilogue -- bf16 GEMM with a fused output stage:
+ *
+ *     D[i][j] = act(alpha * (A x B)[i][j] + beta * C[i][j] + bias[j])
+ *
+ * "Tiled matrix multiplication" ("Implementation notes"; "Efficiency",
+ * epilogue fusion): bias, activation and the narrowing to bf16 happen while
+ * the tile is still in registers, which saves a full read and write of the
+ * output.  A, B, lda, ldb as in gemm_bf16gemm.  C: M x N fp32 (ldc), read only
+ * when beta != 0 (may be NULL otherwise).  bias: N fp32 values, or NULL for
+ * none.  act: a gemm_act_t.  D: M x N output of type d_type (a gemm_out_t),
+ * leading dimension ldd >= max(1, N), 4-byte aligned for fp32 and 2-byte for
+ * bf16; D may be C itself only when d_type is GEMM_OUT_F32 and ldd == ldc,
+ * otherwise D must not overlap A, B, C or bias.  The same tensor-core kernels
+ * as gemm_bf16gemm run (including the decode kernel for M <= 16); operands
+ * the TMA engine cannot describe return GEMM_ERR_UNSUPPORTED, an unknown act
+ * or d_type GEMM_ERR_INVALID_VALUE.  K == 0 or alpha == 0: D = act(beta*C +
+ * bias).  Error bound: the bf16 GEMM's bound on the pre-activation value,
+ * times the activation's largest slope (1 for none and ReLU, 1.13 for GELU),
+ * plus the bf16 rounding of D when d_type is GEMM_OUT_BF16.
+ */
+gemm_status_t gemm_bf16gemm_epilogue(int64_t M, int64_t N, int64_t K, float alpha,
+                                     const void *A, int64_t lda,
+                                     const void *B, int64_t ldb,
+                                     float beta, const float *C, int64_t ldc,
+                                     const float *bias, int act,
+                                     void *D, int64_t ldd, int d_type, void *stream);
+
 /*
  * gemm_bf16gemm_decode_static -- the decode-shaped bf16 GEMM of gemm_bf16gemm
  * (M <= 16; same arguments, same kernel, same results) for callers that must

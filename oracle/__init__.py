@@ -173,6 +173,42 @@ def bf16gemm(alpha, A_bits, B_bits, beta, C=None, nthreads=0, want64=False):
     return default().bf16gemm(alpha, A_bits, B_bits, beta, C, nthreads, want64)
 
 
+def _erf(x):
+    """erf in fp64, element by element (math.erf: the C library's erf)."""
+    import math
+    return np.frompyfunc(math.erf, 1, 1)(np.asarray(x, dtype=np.float64)).astype(np.float64)
+
+
+def activation(x, act):
+    """The activations of the fused output stage, in fp64.
+
+    "none": x;  "relu": max(x, 0);  "gelu": x * Phi(x), Phi the standard
+    normal CDF, Phi(x) = (1 + erf(x / sqrt(2))) / 2.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    if act == "none":
+        return x.copy()
+    if act == "relu":
+        return np.where(x > 0.0, x, 0.0)
+    if act == "gelu":
+        return x * 0.5 * (1.0 + _erf(x / np.sqrt(2.0)))
+    raise ValueError("unknown activation %r" % (act,))
+
+
+def epilogue(ref64, bias=None, act="none"):
+    """Fused output stage on the fp64 GEMM result:
+    D[i][j] = act(ref64[i][j] + bias[j]) (bias broadcast over rows), fp64.
+
+    ref64 is alpha*(A x B) + beta*C from sgemm / bf16gemm (want64=True); the
+    pages' epilogue fusion ("Tiled matrix multiplication", "Implementation
+    notes") adds bias and an activation to that value before it is stored.
+    """
+    v = np.asarray(ref64, dtype=np.float64)
+    if bias is not None:
+        v = v + np.asarray(bias, dtype=np.float64)[None, :]
+    return activation(v, act)
+
+
 def error_ratio(C_test, ref, den):
     """max_ij |C_test - ref| / den, with den == 0 entries requiring equality.
 

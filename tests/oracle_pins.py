@@ -9,7 +9,9 @@ and raises AssertionError when the oracle disagrees with:
   * invariants: (AB)^T = B^T A^T, row permutation, scaling in alpha,
     leading dimensions larger than the row length;
   * the error scale den = |alpha| |A||B| + |beta| |C| on sign-mixed inputs;
-  * the definition of bf16 (the upper half of an IEEE binary32).
+  * the definition of bf16 (the upper half of an IEEE binary32);
+  * the fused output stage's activations: ReLU on signed values, GELU(0) = 0,
+    GELU(x) - GELU(-x) = x, and tabulated values of the normal CDF.
 
 The GEMM being pinned is C <- alpha (A x B) + beta C ("GEMM Worklog I: Naive
 to Tiled", opening equation; "A GEMM Kernel, Step by Step", "The ladder we
@@ -309,11 +311,43 @@ def pin_thread_count_invariance(orc):
     assert np.array_equal(r1, r4)
 
 
+def pin_epilogue_relu(orc):
+    """ReLU keeps non-negative values and zeroes negative ones."""
+    import oracle
+    x = np.array([[-2.5, -0.0, 0.0, 1e-30, 3.25]])
+    assert np.array_equal(oracle.activation(x, "relu"), np.array([[0.0, 0.0, 0.0, 1e-30, 3.25]]))
+    assert np.array_equal(oracle.activation(x, "none"), x)
+
+
+def pin_epilogue_gelu(orc):
+    """GELU(x) = x Phi(x): GELU(0) = 0, GELU(x) - GELU(-x) = x, and the
+    standard normal CDF at 1 and 3 (0.8413447460685429, 0.9986501019683699)."""
+    import oracle
+    g = lambda v: float(oracle.activation(np.array([[v]]), "gelu")[0, 0])
+    assert g(0.0) == 0.0
+    for v in (0.3, 1.0, 2.7, 5.0):
+        assert abs((g(v) - g(-v)) - v) <= 4e-16 * max(1.0, v)
+    assert abs(g(1.0) - 0.8413447460685429) <= 2e-16
+    assert abs(g(-1.0) + (1.0 - 0.8413447460685429)) <= 2e-16
+    assert abs(g(3.0) - 3.0 * 0.9986501019683699) <= 1e-15
+
+
+def pin_epilogue_bias_broadcast(orc):
+    """The bias is added per column, to every row."""
+    import oracle
+    ref = np.arange(6, dtype=np.float64).reshape(2, 3)
+    bias = np.array([10.0, -20.0, 0.5])
+    out = oracle.epilogue(ref, bias, "none")
+    assert np.array_equal(out, np.array([[10.0, -19.0, 2.5], [13.0, -16.0, 5.5]]))
+    assert np.array_equal(oracle.epilogue(ref, bias, "relu"), np.maximum(out, 0.0))
+
+
 ALL_PINS = [
     pin_identity, pin_identity_right, pin_rank1, pin_k1_outer, pin_alpha_zero,
     pin_beta_zero_nan, pin_beta_one_alpha_zero, pin_k_zero, pin_bruteforce_dyadic,
     pin_bruteforce_float, pin_numpy_matmul, pin_transpose, pin_row_permutation,
     pin_column_permutation, pin_alpha_scaling, pin_leading_dimensions, pin_denominator,
     pin_dims_nonsquare, pin_bf16_definition, pin_bf16_matches_widened_fp32,
-    pin_thread_count_invariance,
+    pin_thread_count_invariance, pin_epilogue_relu, pin_epilogue_gelu,
+    pin_epilogue_bias_broadcast,
 ]
