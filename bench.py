@@ -309,6 +309,8 @@ def bench_decode(torch, g, wl, peaks, device, stream_obj):
     reps = 60
     graph = torch.cuda.CUDAGraph()
     cap = torch.cuda.Stream()
+    step(0, cap.cuda_stream)   # any per-stream set-up happens before capture
+    torch.cuda.synchronize()
     with torch.cuda.stream(cap):
         graph.capture_begin()
         for i in range(reps):

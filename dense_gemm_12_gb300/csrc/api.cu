@@ -7,6 +7,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <map>
 #include <mutex>
 
 #include "../../include/gemm12.h"
@@ -23,18 +24,24 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr int64_t kMaxDim = (int64_t{1} << 31) - 1;
 
+struct Scratch {
+  float* ws = nullptr;
+  int64_t ws_floats = 0;
+  uint32_t* counters = nullptr;
+  int64_t counter_count = 0;
+};
+
 struct DeviceState {
   std::once_flag once;
   cudaError_t init_error = cudaSuccess;
   int num_sms = 0;
   int cc_major = 0, cc_minor = 0;
   uint32_t* err_word = nullptr;
-  // decode workspace (grown on demand, freed by gemm_shutdown)
+  // Split-K scratch (partial sums + arrival counters), one per stream: calls
+  // on one stream are ordered by it, calls on different streams never share
+  // a buffer.  Grown on demand, freed by gemm_shutdown.
   std::mutex ws_mutex;
-  float* ws = nullptr;
-  int64_t ws_floats = 0;
-  uint32_t* counters = nullptr;
-  int64_t counter_count = 0;
+  std::map<void*, Scratch> scratch;
 };
 
 DeviceState g_dev[kMaxDevices];
@@ -153,40 +160,68 @@ gemm_status_t run_scale(int64_t M, int64_t N, float beta, float* C, int64_t ldc,
 
 int c_vec4_ok(const float* C, int64_t ldc) { return (aligned16(C) && (ldc % 4 == 0)) ? 1 : 0; }
 
-gemm_status_t ensure_decode_workspace(DeviceState& st, int64_t floats, int64_t counters) {
-  if (st.ws_floats >= floats && st.counter_count >= counters) return GEMM_OK;
-  // Growing: the old buffers may still be read by kernels in flight.
-  if (cudaDeviceSynchronize() != cudaSuccess) {
+// The scratch area of `stream` on this device, grown to at least the given
+// sizes (new counters start at zero).  Caller holds st.ws_mutex.
+gemm_status_t ensure_scratch(DeviceState& st, cudaStream_t stream, int64_t floats,
+                             int64_t counters, Scratch** out) {
+  Scratch& sc = st.scratch[static_cast<void*>(stream)];
+  *out = &sc;
+  if (sc.ws_floats >= floats && sc.counter_count >= counters) return GEMM_OK;
+  // Growing: the old buffers may still be used by this stream's kernels.
+  if (cudaStreamSynchronize(stream) != cudaSuccess) {
     cudaGetLastError();
     return GEMM_ERR_LAUNCH;
   }
-  if (st.ws_floats < floats) {
-    if (st.ws) cudaFree(st.ws);
-    st.ws = nullptr;
-    st.ws_floats = 0;
-    if (cudaMalloc(reinterpret_cast<void**>(&st.ws), floats * sizeof(float)) != cudaSuccess) {
+  if (sc.ws_floats < floats) {
+    if (sc.ws) cudaFree(sc.ws);
+    sc.ws = nullptr;
+    sc.ws_floats = 0;
+    if (cudaMalloc(reinterpret_cast<void**>(&sc.ws), floats * sizeof(float)) != cudaSuccess) {
       cudaGetLastError();
-      st.ws = nullptr;
+      sc.ws = nullptr;
       return GEMM_ERR_NO_MEMORY;
     }
-    st.ws_floats = floats;
+    sc.ws_floats = floats;
   }
-  if (st.counter_count < counters) {
-    if (st.counters) cudaFree(st.counters);
-    st.counters = nullptr;
-    st.counter_count = 0;
-    if (cudaMalloc(reinterpret_cast<void**>(&st.counters), counters * sizeof(uint32_t)) !=
+  if (sc.counter_count < counters) {
+    if (sc.counters) cudaFree(sc.counters);
+    sc.counters = nullptr;
+    sc.counter_count = 0;
+    if (cudaMalloc(reinterpret_cast<void**>(&sc.counters), counters * sizeof(uint32_t)) !=
         cudaSuccess) {
       cudaGetLastError();
-      st.counters = nullptr;
+      sc.counters = nullptr;
       return GEMM_ERR_NO_MEMORY;
     }
-    if (cudaMemset(st.counters, 0, counters * sizeof(uint32_t)) != cudaSuccess) {
+    if (cudaMemset(sc.counters, 0, counters * sizeof(uint32_t)) != cudaSuccess) {
       cudaGetLastError();
       return GEMM_ERR_LAUNCH;
     }
-    st.counter_count = counters;
+    sc.counter_count = counters;
   }
+  return GEMM_OK;
+}
+
+// Work plan of the CUDA-core kernel for `a` (whole tiles, and the last wave's
+// tiles split along k when that balances the SMs better).  A split plan needs
+// this stream's scratch area; `lock` (on st->ws_mutex) is then held until the
+// caller has launched.
+gemm_status_t plan_simt(DeviceState* st, cudaStream_t cs, SimtArgs& a,
+                        std::unique_lock<std::mutex>& lock) {
+  const int tiles = ((a.M + kSimtBM - 1) / kSimtBM) * ((a.N + kSimtBN - 1) / kSimtBN);
+  const int num_kb = (a.K + kSimtBK - 1) / kSimtBK;
+  const SimtPlan pl = simt_plan(tiles, num_kb, st->num_sms);
+  a.full_items = pl.full_items;
+  a.split = pl.split;
+  a.ws = nullptr;
+  a.counters = nullptr;
+  if (pl.split == 1) return GEMM_OK;
+  lock.lock();
+  Scratch* sc = nullptr;
+  const gemm_status_t s = ensure_scratch(*st, cs, pl.ws_floats, pl.counters, &sc);
+  if (s != GEMM_OK) return s;
+  a.ws = sc->ws;
+  a.counters = sc->counters;
   return GEMM_OK;
 }
 
@@ -368,6 +403,9 @@ gemm_status_t gemm_sgemm(int64_t M, int64_t N, int64_t K, float alpha, const flo
   a.ldc = ldc;
   a.c_vec4 = c_vec4_ok(C, ldc);
   a.err = st->err_word;
+  std::unique_lock<std::mutex> lock(st->ws_mutex, std::defer_lock);
+  s = plan_simt(st, cs, a, lock);
+  if (s != GEMM_OK) return s;
   CUtensorMap tmA, tmB;
   LoadMode ma = kLoadCpAsyncF32, mb = kLoadCpAsyncF32;
   if (tma_ok(A, lda, 4) &&
@@ -415,12 +453,19 @@ static gemm_status_t run_bf16_tensor_core(DeviceState* st, gemm_path_t path, int
   a.K = static_cast<int>(K);
   a.epi = epi;
   a.err = st->err_word;
+  // One CTA per column group: nothing is split, no scratch is touched.
+  if (grid == decode_counter_count(a.N)) {
+    a.workspace = nullptr;
+    a.counters = nullptr;
+    return from_cuda(launch_tc_decode(a, &tmA, &tmB, grid, cs));
+  }
   std::lock_guard<std::mutex> lock(st->ws_mutex);
-  gemm_status_t s = ensure_decode_workspace(*st, decode_workspace_floats(a.N, a.K, grid),
-                                            decode_counter_count(a.N));
+  Scratch* sc = nullptr;
+  gemm_status_t s = ensure_scratch(*st, cs, decode_workspace_floats(a.N, a.K, grid),
+                                   decode_counter_count(a.N), &sc);
   if (s != GEMM_OK) return s;
-  a.workspace = st->ws;
-  a.counters = st->counters;
+  a.workspace = sc->ws;
+  a.counters = sc->counters;
   return from_cuda(launch_tc_decode(a, &tmA, &tmB, grid, cs));
 }
 
@@ -458,6 +503,9 @@ gemm_status_t gemm_bf16gemm(int64_t M, int64_t N, int64_t K, float alpha, const 
     a.ldc = ldc;
     a.c_vec4 = c_vec4_ok(C, ldc);
     a.err = st->err_word;
+    std::unique_lock<std::mutex> lock(st->ws_mutex, std::defer_lock);
+    s = plan_simt(st, cs, a, lock);
+    if (s != GEMM_OK) return s;
     return from_cuda(launch_simt(a, kLoadConvertBf16, kLoadConvertBf16, nullptr, nullptr,
                                  st->num_sms, cs));
   }
@@ -527,7 +575,9 @@ gemm_status_t gemm_check_device_error(void* stream) {
   // A decode launch that gave up may have left arrival counters non-zero.
   {
     std::lock_guard<std::mutex> lock(st->ws_mutex);
-    if (st->counters) cudaMemset(st->counters, 0, st->counter_count * sizeof(uint32_t));
+    for (auto& kv : st->scratch)
+      if (kv.second.counters)
+        cudaMemset(kv.second.counters, 0, kv.second.counter_count * sizeof(uint32_t));
   }
   cudaGetLastError();
   return GEMM_ERR_DEVICE_TIMEOUT;
@@ -545,18 +595,17 @@ gemm_status_t gemm_shutdown(void) {
   for (int d = 0; d < n && d < kMaxDevices; ++d) {
     DeviceState& st = g_dev[d];
     std::lock_guard<std::mutex> lock(st.ws_mutex);
-    if (st.ws == nullptr && st.counters == nullptr) continue;
+    if (st.scratch.empty()) continue;
     if (cudaSetDevice(d) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
       cudaGetLastError();
       result = GEMM_ERR_LAUNCH;
       continue;
     }
-    if (st.ws) cudaFree(st.ws);
-    if (st.counters) cudaFree(st.counters);
-    st.ws = nullptr;
-    st.counters = nullptr;
-    st.ws_floats = 0;
-    st.counter_count = 0;
+    for (auto& kv : st.scratch) {
+      if (kv.second.ws) cudaFree(kv.second.ws);
+      if (kv.second.counters) cudaFree(kv.second.counters);
+    }
+    st.scratch.clear();
   }
   cudaSetDevice(cur);
   return result;

@@ -402,7 +402,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (!ok) break;
+      // Leave together if a wait ran out anywhere (see named_bar_any).
+      if (named_bar_any(1, kEpiThreads, !ok)) break;
       tc_fence_after_sync();
       uint32_t r[NSUB][16];
       {

@@ -28,7 +28,27 @@ struct SimtArgs {
   int64_t ldc;
   int c_vec4;      // 1 if C rows may be written as aligned float4
   uint32_t* err;   // device error word
+  // Work plan (see simt_plan): items [0, full_items) are whole tiles in
+  // raster order; every later tile is cut into `split` k-ranges whose partial
+  // sums meet in `ws` (split x 64 KB per tile) and are added by the last of
+  // them to arrive on the tile's counter in `counters` (zero between launches).
+  int full_items;
+  int split;
+  float* ws;
+  uint32_t* counters;
 };
+
+// Work plan of the CUDA-core kernel for tiles output tiles, num_kb k-blocks
+// and up to num_sms persistent CTAs: how many tiles run whole, how the rest
+// are split along k, and the grid.
+struct SimtPlan {
+  int full_items;
+  int split;
+  int grid;
+  int64_t ws_floats;   // workspace the split tiles need
+  int64_t counters;    // counters the split tiles need
+};
+SimtPlan simt_plan(int tiles, int num_kb, int num_sms);
 
 // CUDA-core (FFMA) GEMM: 128 x 128 block tiles, warp tiles 32 x 64, 8 x 8
 // register micro-tiles.  tmA / tmB are used only for operands in kLoadTma mode.

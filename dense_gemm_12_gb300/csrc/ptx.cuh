@@ -106,6 +106,23 @@ __device__ __forceinline__ void mbar_drain_wait(uint64_t* bar, uint32_t parity) 
   }
 }
 
+// Named barrier `id` over `nthreads` threads that also ORs a predicate: every
+// participant gets true if any of them passed true.  Used to leave a loop
+// together when a bounded wait ran out in some of the threads, so that no
+// thread is left waiting at a later barrier for threads that have gone.
+__device__ __forceinline__ bool named_bar_any(uint32_t id, uint32_t nthreads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pin, pout;\n\t"
+      "setp.ne.u32 pin, %1, 0;\n\t"
+      "bar.red.or.pred pout, %2, %3, pin;\n\t"
+      "selp.u32 %0, 1, 0, pout;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
 // ------------------------------------------- programmatic dependent launch
 // Block until every grid this one depends on (the previous kernel in the
 // stream, when launched with programmatic stream serialization) has completed

@@ -55,6 +55,15 @@ struct __align__(8) SimtSmemTail {
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
   int abort_flag;
+  int last_flag;
+};
+
+// Tile and k-range of work item i (see SimtArgs).
+struct SimtItem {
+  int tm, tn;
+  int kb0, kb1;    // k-blocks [kb0, kb1)
+  int split_tile;  // -1 for a whole tile, else the index of the split tile
+  int part;        // which of the split k-ranges
 };
 
 constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + STAGES * kStageBytes +
@@ -70,11 +79,38 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
   tn = local / rows;
 }
 
+__device__ __forceinline__ SimtItem simt_item(const SimtArgs& p, int i, int tiles_m, int tiles_n,
+                                              int num_kb) {
+  SimtItem it;
+  int tile;
+  if (i < p.full_items) {
+    tile = i;
+    it.kb0 = 0;
+    it.kb1 = num_kb;
+    it.split_tile = -1;
+    it.part = 0;
+  } else {
+    const int j = i - p.full_items;
+    it.split_tile = j / p.split;
+    it.part = j - it.split_tile * p.split;
+    tile = p.full_items + it.split_tile;
+    it.kb0 = static_cast<int>(static_cast<int64_t>(it.part) * num_kb / p.split);
+    it.kb1 = static_cast<int>(static_cast<int64_t>(it.part + 1) * num_kb / p.split);
+  }
+  tile_coords(tile, tiles_m, tiles_n, it.tm, it.tn);
+  return it;
+}
+
 // Byte offset of A element (m, k) inside a stage: 128-byte rows, the 16-byte
 // chunk index XOR-ed with (m mod 8) -- the layout TMA's 128-byte swizzle
 // writes into a 1024-byte aligned buffer.
 __device__ __forceinline__ uint32_t a_smem_offset(int m, int k) {
   return static_cast<uint32_t>(m * 128 + ((((k >> 2) ^ (m & 7)) << 4)) + ((k & 3) << 2));
+}
+
+// Barrier among the 256 compute threads only (the producer warps never join).
+__device__ __forceinline__ void compute_bar() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kComputeThreads) : "memory");
 }
 
 template <int MODE_A, int MODE_B>
@@ -325,6 +361,7 @@ __global__ void __launch_bounds__(SimtTraits<MODE_A, MODE_B>::kThreads, 1)
   const int tiles_n = (p.N + BN - 1) / BN;
   const int num_tiles = tiles_m * tiles_n;
   const int num_kb = (p.K + BK - 1) / BK;
+  const int num_items = p.full_items + (num_tiles - p.full_items) * p.split;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -332,6 +369,7 @@ __global__ void __launch_bounds__(SimtTraits<MODE_A, MODE_B>::kThreads, 1)
       mbar_init(&tail->empty[s], kComputeThreads);
     }
     tail->abort_flag = 0;
+    tail->last_flag = 0;
     fence_barrier_init();
   }
   if (MODE_A == kLoadTma && threadIdx.x == kComputeThreads) tma_prefetch_desc(&tmA);
@@ -349,10 +387,10 @@ __global__ void __launch_bounds__(SimtTraits<MODE_A, MODE_B>::kThreads, 1)
     if (!T::kAnyGeneric && ptid != 0) return;
     uint32_t it = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-      int tm, tn;
-      tile_coords(t, tiles_m, tiles_n, tm, tn);
-      for (int kb = 0; kb < num_kb; ++kb, ++it) {
+    for (int i = blockIdx.x; i < num_items && ok; i += gridDim.x) {
+      const SimtItem w = simt_item(p, i, tiles_m, tiles_n, num_kb);
+      const int tm = w.tm, tn = w.tn;
+      for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
         const int s = it % STAGES;
         const uint32_t round = it / STAGES;
         if (!mbar_wait(&tail->empty[s], (round & 1u) ^ 1u, abort_flag, p.err)) {
@@ -399,28 +437,88 @@ __global__ void __launch_bounds__(SimtTraits<MODE_A, MODE_B>::kThreads, 1)
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(T::kComputeRegs));
   const int wm = warp >> 1, wn = warp & 1;
   const int rg = lane >> 3, cg = lane & 7;
+  const int ctid = threadIdx.x;  // 0..255
   uint32_t it = 0;
-  for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
-    int tm, tn;
-    tile_coords(t, tiles_m, tiles_n, tm, tn);
+  for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
+    const SimtItem w = simt_item(p, item, tiles_m, tiles_n, num_kb);
     uint64_t acc2[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
       for (int q = 0; q < 4; ++q) acc2[i][q] = 0ull;
-    for (int kb = 0; kb < num_kb; ++kb, ++it) {
+    bool failed = false;
+    for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
       const int s = it % STAGES;
       const uint32_t round = it / STAGES;
-      if (!mbar_wait(&tail->full[s], round & 1u, abort_flag, p.err)) return;
+      if (!mbar_wait(&tail->full[s], round & 1u, abort_flag, p.err)) {
+        failed = true;
+        break;
+      }
       compute_stage_x2(stage_a(s), stage_b(s), acc2, wm, wn, rg, cg);
       mbar_arrive(&tail->empty[s]);
     }
+    // Leave together if a wait ran out anywhere (see named_bar_any).
+    if (named_bar_any(1, kComputeThreads, failed)) return;
     float acc[8][8];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
       for (int q = 0; q < 4; ++q) unpack2(acc2[i][q], acc[i][2 * q], acc[i][2 * q + 1]);
-    epilogue(p, acc, tm, tn, wm, wn, rg, cg);
+    if (w.split_tile < 0) {
+      epilogue(p, acc, w.tm, w.tn, wm, wn, rg, cg);
+      continue;
+    }
+    // Split tile: publish this k-range's partial sums (64 per thread, stored
+    // contiguously per thread), then count the arrival; the last of the
+    // tile's `split` parts adds all partials in part order -- a fixed order,
+    // so the result does not depend on which part finishes last.
+    float* mine = p.ws + (static_cast<int64_t>(w.split_tile * p.split + w.part) *
+                              kComputeThreads + ctid) * 64;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      __stcg(reinterpret_cast<float4*>(mine + 8 * i),
+             make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]));
+      __stcg(reinterpret_cast<float4*>(mine + 8 * i + 4),
+             make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]));
+    }
+    compute_bar();
+    if (ctid == 0) {
+      __threadfence();  // publish the whole CTA's partial before arriving
+      const uint32_t before = atomicAdd(p.counters + w.split_tile, 1u);
+      tail->last_flag = (before == static_cast<uint32_t>(p.split - 1)) ? 1 : 0;
+    }
+    compute_bar();
+    const int last = tail->last_flag;
+    if (last) {
+      __threadfence();
+      float sum[8][8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) sum[i][j] = 0.0f;
+      for (int part = 0; part < p.split; ++part) {
+        const float* src = p.ws + (static_cast<int64_t>(w.split_tile * p.split + part) *
+                                       kComputeThreads + ctid) * 64;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          float v[8];
+          if (part == w.part) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = acc[i][j];
+          } else {
+            const float4 lo = __ldcg(reinterpret_cast<const float4*>(src + 8 * i));
+            const float4 hi = __ldcg(reinterpret_cast<const float4*>(src + 8 * i + 4));
+            v[0] = lo.x; v[1] = lo.y; v[2] = lo.z; v[3] = lo.w;
+            v[4] = hi.x; v[5] = hi.y; v[6] = hi.z; v[7] = hi.w;
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) sum[i][j] += v[j];
+        }
+      }
+      epilogue(p, sum, w.tm, w.tn, wm, wn, rg, cg);
+      if (ctid == 0) p.counters[w.split_tile] = 0u;
+    }
+    compute_bar();  // last_flag is rewritten by the next split item
   }
 }
 
@@ -433,13 +531,42 @@ cudaError_t launch_variant(const SimtArgs& a, const CUtensorMap* tmA, const CUte
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
   const int tiles = ((a.M + BM - 1) / BM) * ((a.N + BN - 1) / BN);
-  const int grid = tiles < num_sms ? tiles : num_sms;
+  const int num_items = a.full_items + (tiles - a.full_items) * a.split;
+  const int grid = num_items < num_sms ? num_items : num_sms;
   CUtensorMap dummy{};
   kernel<<<grid, T::kThreads, kSmemBytes, stream>>>(a, tmA ? *tmA : dummy, tmB ? *tmB : dummy);
   return cudaGetLastError();
 }
 
 }  // namespace
+
+SimtPlan simt_plan(int tiles, int num_kb, int num_sms) {
+  SimtPlan pl{tiles, 1, tiles < num_sms ? tiles : num_sms, 0, 0};
+  if (tiles <= 0 || num_sms <= 0) return pl;
+  // Tiles beyond the last full wave (all of them when there are fewer tiles
+  // than SMs) are split along k when that shortens the last wave: with S
+  // parts the tail takes ceil(tail * S / sms) / S tile-times instead of 1.
+  // Every part keeps at least 4 k-blocks.
+  const int tail = tiles >= num_sms ? tiles % num_sms : tiles;
+  if (tail == 0) return pl;
+  int best_s = 1;
+  double best = 1.0;
+  for (int s = 2; s <= 8 && s * 4 <= num_kb; ++s) {
+    const double t = static_cast<double>((static_cast<int64_t>(tail) * s + num_sms - 1) / num_sms) / s;
+    if (t < best - 1e-9) {
+      best = t;
+      best_s = s;
+    }
+  }
+  if (best_s == 1) return pl;
+  pl.full_items = tiles - tail;
+  pl.split = best_s;
+  const int items = pl.full_items + tail * best_s;
+  pl.grid = items < num_sms ? items : num_sms;
+  pl.ws_floats = static_cast<int64_t>(tail) * best_s * kComputeThreads * 64;
+  pl.counters = tail;
+  return pl;
+}
 
 cudaError_t launch_simt(const SimtArgs& a, LoadMode mode_a, LoadMode mode_b,
                         const CUtensorMap* tmA, const CUtensorMap* tmB, int num_sms,

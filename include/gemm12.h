@@ -45,13 +45,19 @@
  *             are reported by gemm_check_device_error().
  *  Threads    Entry points may be called from several host threads on
  *             different streams.
- *  Memory     gemm_sgemm never allocates.  gemm_bf16gemm allocates, on its
- *             first decode-shaped call per device (M <= 16), a split-K
- *             workspace and arrival counters that it keeps and reuses;
- *             gemm_shutdown() frees them.  Concurrent decode-shaped calls on
- *             different streams of the same device are serialised on the
- *             host but must not overlap on the device (they share the
- *             workspace).  Allocation failure returns GEMM_ERR_NO_MEMORY.
+ *  Memory     Calls whose work is split along k -- the decode kernel of
+ *             gemm_bf16gemm (M <= 16), and gemm_sgemm / gemm_bf16gemm when
+ *             the last wave of output tiles is split to balance the SMs --
+ *             need scratch memory (partial sums and arrival counters).  The
+ *             library allocates it per device and per stream the first time a
+ *             call on that stream needs it (or more of it), keeps and reuses
+ *             it, and gemm_shutdown() frees it; calls on different streams
+ *             never share scratch, calls on one stream are ordered by it.
+ *             Growing a stream's scratch synchronises that stream, so the
+ *             first such call on a stream must come before that stream is
+ *             captured into a CUDA graph.  Allocation failure returns
+ *             GEMM_ERR_NO_MEMORY.  See also gemm_bf16gemm_decode_static,
+ *             which allocates nothing.
  */
 #ifndef GEMM12_H
 #define GEMM12_H

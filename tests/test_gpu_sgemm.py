@@ -189,3 +189,32 @@ def test_tensor_helper():
     torch.cuda.synchronize()
     _, ref64, den = oracle_sgemm(A, B, C, 0.5, 0.25)
     assert ratio(dC.cpu(), ref64, den) <= tol_fp32(K)
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (128 * 13, 128 * 13, 2048),   # 169 tiles: 152 whole, the last 17 split along k
+    (128 * 16, 128 * 10, 1024),   # 160 tiles: 8-tile tail
+    (512, 512, 2048),             # 16 tiles, fewer than the SMs: every tile split
+    (100, 3000, 4096),            # one tile row, ragged
+])
+def test_split_k_tiles_match_oracle_and_repeat(M, N, K):
+    A, B, C = _inputs(M, N, K, seed=M + N + K)
+    outs = [run_sgemm(A, B, C, 0.7, 0.3)[0] for _ in range(3)]
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int32), outs[0].view(torch.int32))
+    gen = torch.Generator().manual_seed(1)
+    idx = torch.randperm(M, generator=gen)[:64].sort().values
+    idx = torch.cat([idx, torch.tensor([0, M - 1])]).unique()
+    _, ref64, den = oracle_sgemm(A[idx].contiguous(), B, C[idx].contiguous(), 0.7, 0.3)
+    assert ratio(outs[0][idx], ref64, den) <= tol_fp32(K)
+    check_device_error()
+
+
+def test_split_k_integers_exact():
+    # small integers: every partial sum and their total are exact in fp32
+    M, N, K = 512, 640, 1024
+    A, B, C = make_inputs(M, N, K, ("int", None), ("int", None), ("int", None), seed=9)
+    out, st, _, _, _ = run_sgemm(A, B, C, 1.5, -0.5)
+    assert st == 0
+    ref32, _, _ = oracle_sgemm(A, B, C, 1.5, -0.5)
+    assert np.array_equal(out.numpy().view(np.uint32), ref32.view(np.uint32))
