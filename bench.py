@@ -85,7 +85,8 @@ def recorded_traffic(kernel):
             rec = json.load(f)[kernel]
         h = hashlib.sha256()
         for src in (rec["source"], "dense_gemm_12_gb300/csrc/ptx.cuh",
-                    "dense_gemm_12_gb300/csrc/internal.h"):
+                    "dense_gemm_12_gb300/csrc/internal.h",
+                    "dense_gemm_12_gb300/csrc/epilogue.cuh"):
             with open(os.path.join(ROOT, src), "rb") as f:
                 h.update(f.read())
         if h.hexdigest() != rec["source_sha256"]:
