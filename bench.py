@@ -242,11 +242,11 @@ def bench_bf16_8192(torch, g, wl, peaks, device, stream_obj):
     torch.cuda.empty_cache()
     return {
         "workload": "bf16 in / fp32 out GEMM M=N=K=8192, alpha=1, beta=0, N(0,0.02)",
-        "kernel": "tc_bf16_kernel (tcgen05, 128x256 tiles, TMEM accumulators)",
+        "kernel": "tc_bf16_pair_kernel (tcgen05 cta_group::2: CTA pairs on 256x256 tiles, TMEM accumulators)",
         "value": tflops * 1e3, "unit": "GFLOP/s", "ms_per_launch_median": ms,
         "ms_per_launch_min": min(times), "launches_timed": len(times),
         "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
-                     "frac": tflops / peak, "traffic": recorded_traffic("tc_bf16_kernel"),
+                     "frac": tflops / peak, "traffic": recorded_traffic("tc_bf16_pair_kernel"),
                      "peak_note": "%s dense bf16 burst (cuBLAS); sustained %.1f" % (
                          peaks["source"], peaks["bf16_tflops_sustained"])},
         "l2": "operands 256 MB + C 256 MB per launch exceed the 129 MB L2",
@@ -279,7 +279,7 @@ def bench_bf16_8192_fused(torch, g, wl, peaks, device, stream_obj):
     torch.cuda.empty_cache()
     return {
         "workload": "bf16 GEMM M=N=K=8192 with fused bias + GELU, bf16 output",
-        "kernel": "tc_bf16_kernel (same kernel, fused output stage)",
+        "kernel": "tc_bf16_pair_kernel (same kernel, fused output stage)",
         "value": tflops * 1e3, "unit": "GFLOP/s", "ms_per_launch_median": ms,
         "launches_timed": len(times),
         "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",

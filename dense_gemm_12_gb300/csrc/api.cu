@@ -144,7 +144,8 @@ gemm_path_t select_path(bool bf16, int64_t M, int64_t N, int64_t K, float alpha,
   }
   const bool tma = tma_ok(A, lda, 2) && tma_ok(B, ldb, 2);
   if (!tma) return GEMM_PATH_SIMT_BF16;
-  return M <= kDecBM ? GEMM_PATH_TC_DECODE : GEMM_PATH_TC_BF16;
+  if (M <= kDecBM) return GEMM_PATH_TC_DECODE;
+  return M <= kTcBM ? GEMM_PATH_TC_BF16 : GEMM_PATH_TC_BF16_PAIR;
 }
 
 gemm_status_t from_cuda(cudaError_t e) {
@@ -426,7 +427,8 @@ static gemm_status_t run_bf16_tensor_core(DeviceState* st, gemm_path_t path, int
                                           int64_t K, const void* A, int64_t lda, const void* B,
                                           int64_t ldb, const Epilogue& epi, cudaStream_t cs) {
   CUtensorMap tmA, tmB;
-  if (path == GEMM_PATH_TC_BF16) {
+  if (path == GEMM_PATH_TC_BF16 || path == GEMM_PATH_TC_BF16_PAIR) {
+    // launch_tc_bf16 runs the CTA-pair kernel exactly when M > kTcBM
     if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, K, M, lda, kTcBK, kTcBM,
                    CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, N, K, ldb, 64, kTcBK,

@@ -21,9 +21,12 @@
 //                    masked stores; the second accumulator lets the MMAs of
 //                    the next tile run while this one drains.
 // Persistent CTAs (one per SM) walk the 128 x 256 tiles in a grouped raster
-// order for L2 reuse.  TMA zero-fills beyond M, N, K.  CTAs run in clusters of
-// two along M that share each 64 x 256 slice of B: each CTA loads one half and
-// multicasts it to both (see tc_bf16_kernel).
+// order for L2 reuse.  TMA zero-fills beyond M, N, K.
+//
+// That single-CTA kernel serves M <= 128.  Larger problems run on CTA pairs
+// (tc_bf16_pair_kernel below): two SMs share one 256 x 256 tile and one MMA
+// stream, which cuts the shared-memory operand bytes each SM's tensor core
+// reads per MMA from 12 KB to 8 KB.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -51,11 +54,6 @@ constexpr int kEpiThreads = 128;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kGroupM = G12_TC_GROUP_M;  // raster group height (tile rows or row pairs)
 constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN, /*A MN-major*/ 0, /*B MN-major*/ 1);
-#ifndef G12_TC_CLUSTER_M
-#define G12_TC_CLUSTER_M 2
-#endif
-constexpr int kClusterM = G12_TC_CLUSTER_M;  // CTAs per cluster along M (1 or 2)
-static_assert(kClusterM == 1 || kClusterM == 2, "cluster of 1 or 2 CTAs");
 
 struct __align__(8) TcSmemTail {
   uint64_t full[STAGES];
@@ -138,14 +136,6 @@ __device__ __forceinline__ void store_row_chunk(const TcArgs& p, int row, int co
   }
 }
 
-// CL = CTAs per cluster along M (1 or 2).  With CL = 2 the two CTAs of a
-// cluster compute vertically adjacent tiles (2 pm and 2 pm + 1) of the same
-// 256 columns: each loads its own 128 x 64 slice of A and one half of the
-// shared 64 x 256 slice of B, multicast into both CTAs, so every CTA moves
-// 32 KB instead of 48 KB per k-block from L2.  A stage may be refilled only
-// after the MMAs of both CTAs have read it: each MMA thread commits to the
-// stage's empty barrier in both CTAs (count CL).
-template <int CL>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bf16_kernel(const __grid_constant__ TcArgs p, const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB) {
@@ -158,18 +148,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int tiles_m = (p.M + BM - 1) / BM;
   const int tiles_n = (p.N + BN - 1) / BN;
-  const int groups_m = (tiles_m + CL - 1) / CL;   // tile rows handled per cluster item
-  const int num_items = groups_m * tiles_n;
+  const int num_tiles = tiles_m * tiles_n;
   const int num_kb = (p.K + BK - 1) / BK;
-  const uint32_t rank = (CL > 1) ? cluster_cta_rank() : 0u;
-  const int first_item = static_cast<int>(blockIdx.x) / CL;
-  const int item_stride = static_cast<int>(gridDim.x) / CL;
-  constexpr uint16_t kPeers = static_cast<uint16_t>((1u << CL) - 1u);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&tail->full[s], 1);
-      mbar_init(&tail->empty[s], CL);
+      mbar_init(&tail->empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tail->tmem_full[b], 1);
@@ -187,9 +172,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before_sync();
   __syncthreads();
-  // Peers multicast into this CTA's shared memory and barriers: all barriers
-  // of the cluster must be initialised first.
-  if (CL > 1) cluster_sync();
   tc_fence_after_sync();
   const uint32_t tmem_base = tail->tmem_base;
 
@@ -198,10 +180,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
-      for (int t = first_item; t < num_items && ok; t += item_stride) {
-        int pm, tn;
-        tile_coords(t, groups_m, tiles_n, pm, tn);
-        const int tm = pm * CL + static_cast<int>(rank);
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        int tm, tn;
+        tile_coords(t, tiles_m, tiles_n, tm, tn);
         for (int kb = 0; kb < num_kb; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t round = it / STAGES;
@@ -211,21 +192,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint8_t* sa = smem + s * kStageBytes;
           uint8_t* sb = sa + kStageBytesA;
-          // all 48 KB arrive here: A from this CTA, B half from each CTA
           mbar_arrive_expect_tx(&tail->full[s], kStageBytes);
           tma_load_2d(sa, &tmA, kb * BK, tm * BM, &tail->full[s]);
-          if (CL == 1) {
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j)
-              tma_load_2d(sb + j * kBoxBytesB, &tmB, tn * BN + j * 64, kb * BK, &tail->full[s]);
-          } else {
-#pragma unroll
-            for (int jj = 0; jj < BN / 64 / CL; ++jj) {
-              const int j = static_cast<int>(rank) * (BN / 64 / CL) + jj;
-              tma_load_2d_multicast(sb + j * kBoxBytesB, &tmB, tn * BN + j * 64, kb * BK,
-                                    &tail->full[s], kPeers);
-            }
-          }
+          for (int j = 0; j < BN / 64; ++j)
+            tma_load_2d(sb + j * kBoxBytesB, &tmB, tn * BN + j * 64, kb * BK, &tail->full[s]);
         }
       }
       if (!ok) {
@@ -242,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t j = 0;
       bool ok = true;
       bool issued = false;
-      for (int t = first_item; t < num_items && ok; t += item_stride, ++j) {
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++j) {
         const uint32_t ab = j & 1u, ar = j >> 1;
         if (!mbar_wait(&tail->tmem_empty[ab], (ar & 1u) ^ 1u, abort_flag, p.err)) {
           ok = false;
@@ -270,10 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_mma_f16(d_tmem, adesc, bdesc, kIdesc, (kb | kk) != 0 ? 1u : 0u);
           }
           issued = true;
-          if (CL == 1)
-            tc_commit(&tail->empty[s]);
-          else
-            tc_commit_multicast(&tail->empty[s], kPeers);  // frees the stage in both CTAs
+          tc_commit(&tail->empty[s]);
         }
         if (!ok) break;
         tc_commit(&tail->tmem_full[ab]);
@@ -289,10 +257,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // -------------------------------------------------------- epilogue
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     uint32_t j = 0;
-    for (int t = first_item; t < num_items; t += item_stride, ++j) {
-      int pm, tn;
-      tile_coords(t, groups_m, tiles_n, pm, tn);
-      const int tm = pm * CL + static_cast<int>(rank);
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++j) {
+      int tm, tn;
+      tile_coords(t, tiles_m, tiles_n, tm, tn);
       const uint32_t ab = j & 1u, ar = j >> 1;
       if (!mbar_wait(&tail->tmem_full[ab], ar & 1u, abort_flag, p.err)) break;
       tc_fence_after_sync();
@@ -312,10 +279,221 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before_sync();
   __syncthreads();
-  // No CTA may exit while its peer can still multicast into it.
-  if (CL > 1) cluster_sync();
   tc_fence_after_sync();
   if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+// ------------------------------------------------------------------------
+// CTA-pair kernel (cta_group::2): the two CTAs of a cluster compute one
+// 256 x 256 tile with a single stream of M=256, N=256, K=16 MMAs issued by the
+// even CTA.  Each CTA holds its own 128 x 64 slice of A and one 64 x 128 half
+// of B (columns rank * 128 ...) per stage, 32 KB instead of 48 KB, and the
+// tensor core of each SM reads only that from its own shared memory (the B
+// half of the other SM arrives over the pair link).  Each CTA's TMEM holds its
+// 128 rows of the tile, so the epilogue is the one above, per CTA.
+//
+// Barriers (same offsets in both CTAs):
+//   full[s]       even CTA only: one arrival (its producer, announcing the
+//                 bytes of both CTAs) + the transaction bytes of both CTAs'
+//                 copies, which signal it from either CTA;
+//   empty[s]      in each CTA, one arrival from the MMA commit, multicast to
+//                 both when the MMAs have read the stage;
+//   tmem_full[b]  in each CTA, from the commit after a tile's last k-block;
+//   tmem_empty[b] even CTA only: one arrival per epilogue warp of both CTAs.
+#ifndef G12_TC_PAIR_STAGES
+#define G12_TC_PAIR_STAGES 6
+#endif
+constexpr int PS = G12_TC_PAIR_STAGES;
+constexpr int kPairBN = BN / 2;                         // B columns held per CTA
+constexpr int kPairStageBytesA = BM * BK * 2;           // 16 KB
+constexpr int kPairStageBytesB = BK * kPairBN * 2;      // 16 KB
+constexpr int kPairStageBytes = kPairStageBytesA + kPairStageBytesB;
+constexpr int kEpiWarps = kEpiThreads / 32;
+constexpr uint16_t kPairMask = 0x3;
+constexpr uint32_t kPairIdesc = idesc_bf16_f32(2 * BM, BN, /*A MN-major*/ 0, /*B MN-major*/ 1);
+
+struct __align__(8) PairSmemTail {
+  uint64_t full[PS];
+  uint64_t empty[PS];
+  uint64_t tmem_full[2];
+  uint64_t tmem_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+constexpr size_t kPairSmemBytes = 1024 + PS * kPairStageBytes + sizeof(PairSmemTail);
+static_assert(kPairSmemBytes <= 227 * 1024, "pair kernel shared memory");
+
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_bf16_pair_kernel(const __grid_constant__ TcArgs p, const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = align_smem<1024>(smem_raw);
+  PairSmemTail* tail = reinterpret_cast<PairSmemTail*>(smem + PS * kPairStageBytes);
+  volatile int* abort_flag = &tail->abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int tiles_m = (p.M + BM - 1) / BM;
+  const int tiles_n = (p.N + BN - 1) / BN;
+  const int pairs_m = (tiles_m + 1) / 2;
+  const int num_items = pairs_m * tiles_n;
+  const int num_kb = (p.K + BK - 1) / BK;
+  const uint32_t rank = cluster_cta_rank() & 1u;
+  const bool even = (rank == 0);
+  const int first_item = static_cast<int>(blockIdx.x) / 2;
+  const int item_stride = static_cast<int>(gridDim.x) / 2;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < PS; ++s) {
+      mbar_init(&tail->full[s], 1);
+      mbar_init(&tail->empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tail->tmem_full[b], 1);
+      mbar_init(&tail->tmem_empty[b], 2 * kEpiWarps);
+    }
+    mbar_init(&tail->drain, 1);
+    tail->abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(&tail->tmem_base, kTmemCols);
+    tmem_relinquish_alloc_permit_pair();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  // Both CTAs signal barriers of the even CTA: all must be initialised first.
+  cluster_sync();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = tail->tmem_base;
+
+  if (warp == 0) {
+    // -------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      const uint32_t full0 = mapa_shared(smem_u32(&tail->full[0]), 0);
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = first_item; t < num_items && ok; t += item_stride) {
+        int pm, tn;
+        tile_coords(t, pairs_m, tiles_n, pm, tn);
+        const int tm = pm * 2 + static_cast<int>(rank);
+        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+          const int s = it % PS;
+          const uint32_t round = it / PS;
+          if (!mbar_wait(&tail->empty[s], (round & 1u) ^ 1u, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + s * kPairStageBytes;
+          uint8_t* sb = sa + kPairStageBytesA;
+          const uint32_t full = full0 + static_cast<uint32_t>(s * sizeof(uint64_t));
+          if (even) mbar_arrive_expect_tx(&tail->full[s], 2 * kPairStageBytes);
+          tma_load_2d_pair(sa, &tmA, kb * BK, tm * BM, full);
+#pragma unroll
+          for (int j = 0; j < kPairBN / 64; ++j)
+            tma_load_2d_pair(sb + j * kBoxBytesB, &tmB,
+                             tn * BN + static_cast<int>(rank) * kPairBN + j * 64, kb * BK, full);
+        }
+      }
+      // Leave only after the MMAs have read every stage this CTA filled: then
+      // all of its copies have landed and every commit aimed at its barriers
+      // has arrived.  After an abort the stages may never be read; the wait
+      // then gives up at the time limit, long after any copy has landed.
+      const uint64_t t0 = globaltimer_ns();
+      for (uint32_t j = it > PS ? it - PS : 0u; j < it; ++j) {
+        while (!mbar_try_wait(&tail->empty[j % PS], (j / PS) & 1u)) {
+          if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ----------------------------------------- MMA issuer (even CTA only)
+    if (even && lane == 0) {
+      uint32_t it = 0;
+      uint32_t j = 0;
+      bool ok = true;
+      bool issued = false;
+      for (int t = first_item; t < num_items && ok; t += item_stride, ++j) {
+        const uint32_t ab = j & 1u, ar = j >> 1;
+        if (!mbar_wait(&tail->tmem_empty[ab], (ar & 1u) ^ 1u, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + ab * BN;
+        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+          const int s = it % PS;
+          const uint32_t round = it / PS;
+          if (!mbar_wait(&tail->full[s], round & 1u, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t sa = smem_u32(smem + s * kPairStageBytes);
+          const uint32_t sb = sa + kPairStageBytesA;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t adesc = smem_desc_sw128(sa + kk * 32, 16, 1024);
+            const uint64_t bdesc = smem_desc_sw128(sb + kk * 2048, kBoxBytesB, 1024);
+            tc_mma_f16_pair(d_tmem, adesc, bdesc, kPairIdesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          issued = true;
+          tc_commit_pair_multicast(&tail->empty[s], kPairMask);
+        }
+        if (!ok) break;
+        tc_commit_pair_multicast(&tail->tmem_full[ab], kPairMask);
+      }
+      if (ok) {
+        // Wait for both CTAs' epilogues to release the last accumulators, so
+        // that no arrival from the odd CTA is still on its way at exit.
+        for (uint32_t jj = j > 2 ? j - 2 : 0u; jj < j; ++jj)
+          if (!mbar_wait(&tail->tmem_empty[jj & 1u], (jj >> 1) & 1u, abort_flag, p.err)) break;
+      } else if (issued) {
+        // Let every MMA this thread issued finish before TMEM is released.
+        tc_commit_pair(&tail->drain);
+        mbar_drain_wait(&tail->drain, 0);
+      }
+    }
+    __syncwarp();
+  } else {
+    // -------------------------------------------------------- epilogue
+    const int quarter = warp & 3;  // TMEM lanes this warp may access
+    const uint32_t tmem_empty0 = mapa_shared(smem_u32(&tail->tmem_empty[0]), 0);
+    uint32_t j = 0;
+    for (int t = first_item; t < num_items; t += item_stride, ++j) {
+      int pm, tn;
+      tile_coords(t, pairs_m, tiles_n, pm, tn);
+      const int tm = pm * 2 + static_cast<int>(rank);
+      const uint32_t ab = j & 1u, ar = j >> 1;
+      if (!mbar_wait(&tail->tmem_full[ab], ar & 1u, abort_flag, p.err)) break;
+      tc_fence_after_sync();
+      const int row = tm * BM + quarter * 32 + lane;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + ab * BN;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(taddr + c * 32, r);
+        tc_wait_ld();
+        if (row < p.M) store_row_chunk(p, row, tn * BN + c * 32, r);
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(tmem_empty0 + ab * static_cast<uint32_t>(sizeof(uint64_t)));
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  // Neither CTA releases TMEM or exits while the pair's MMAs or copies can
+  // still touch it.
+  cluster_sync();
+  tc_fence_after_sync();
+  if (warp == 1) tmem_dealloc_pair(tmem_base, kTmemCols);
 }
 
 }  // namespace
@@ -324,39 +502,37 @@ cudaError_t launch_tc_bf16(const TcArgs& a, const CUtensorMap* tmA, const CUtens
                            int num_sms, cudaStream_t stream) {
   const int tiles_m = (a.M + BM - 1) / BM;
   const int tiles_n = (a.N + BN - 1) / BN;
-  if (kClusterM > 1 && tiles_m >= kClusterM) {
-    auto kernel = tc_bf16_kernel<kClusterM>;
+  if (tiles_m >= 2) {
+    auto kernel = tc_bf16_pair_kernel;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kSmemBytes));
+                                         static_cast<int>(kPairSmemBytes));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kClusterM;
+    attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.dynamicSmemBytes = kPairSmemBytes;
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    // Persistent clusters: as many as can be resident at once, at most one
-    // per pair of tiles.
-    const int items = ((tiles_m + kClusterM - 1) / kClusterM) * tiles_n;
+    const int items = ((tiles_m + 1) / 2) * tiles_n;
     int max_clusters = 0;
-    cfg.gridDim = dim3(kClusterM * (num_sms / kClusterM));
+    cfg.gridDim = dim3(2 * (num_sms / 2));
     if (cudaOccupancyMaxActiveClusters(&max_clusters, kernel, &cfg) != cudaSuccess ||
         max_clusters < 1) {
       cudaGetLastError();
-      max_clusters = num_sms / kClusterM;
+      max_clusters = num_sms / 2;
     }
     const int clusters = items < max_clusters ? items : max_clusters;
-    cfg.gridDim = dim3(kClusterM * clusters);
+    cfg.gridDim = dim3(2 * clusters);
     e = cudaLaunchKernelEx(&cfg, kernel, a, *tmA, *tmB);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
   }
-  auto kernel = tc_bf16_kernel<1>;
+  auto kernel = tc_bf16_kernel;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;

@@ -208,10 +208,13 @@ typedef enum {
     GEMM_PATH_SCALE_C = 1,        /* alpha == 0 or K == 0: C <- beta*C      */
     GEMM_PATH_SIMT_TMA = 2,       /* fp32 CUDA-core kernel, TMA operands    */
     GEMM_PATH_SIMT_GENERIC = 3,   /* fp32 CUDA-core kernel, generic loads   */
-    GEMM_PATH_TC_BF16 = 4,        /* bf16 tensor-core (tcgen05) kernel      */
+    GEMM_PATH_TC_BF16 = 4,        /* bf16 tensor-core (tcgen05) kernel,
+                                     one CTA per 128x256 tile (M <= 128)   */
     GEMM_PATH_TC_DECODE = 5,      /* bf16 tensor-core split-K decode kernel */
-    GEMM_PATH_SIMT_BF16 = 6       /* bf16 operands TMA cannot describe:
+    GEMM_PATH_SIMT_BF16 = 6,      /* bf16 operands TMA cannot describe:
                                      widened to fp32 on the CUDA cores     */
+    GEMM_PATH_TC_BF16_PAIR = 7    /* bf16 tensor-core kernel on CTA pairs:
+                                     two SMs per 256x256 tile (M > 128)    */
 } gemm_path_t;
 
 /*

@@ -58,7 +58,8 @@ def test_ragged_tensor_core(M, N, K):
     A, B, C = _inputs(M, N, K, seed=M + N + K)
     out, st, _, _, dC = run_bf16gemm(A, B, C, 0.7, 0.3)
     assert st == 0
-    assert g.gemm_select_path(1, M, N, K, 0.7, 1 << 20, K, 1 << 20, N) == "tc_bf16"
+    expect = "tc_bf16" if M <= 128 else "tc_bf16_pair"
+    assert g.gemm_select_path(1, M, N, K, 0.7, 1 << 20, K, 1 << 20, N) == expect
     _, ref64, den = oracle_bf16(A, B, C, 0.7, 0.3)
     r = ratio(out, ref64, den)
     assert r <= TOL_BF16, r
@@ -112,7 +113,8 @@ def test_full_8192_sampled_rows():
     check_device_error()
     gen = torch.Generator().manual_seed(0)
     idx = torch.randperm(w.M, generator=gen)[:24].sort().values
-    idx = torch.cat([idx, torch.tensor([0, 127, 128, w.M - 1])]).unique()
+    # tile (128) and CTA-pair tile (256) boundaries
+    idx = torch.cat([idx, torch.tensor([0, 127, 128, 255, 256, 383, 384, w.M - 1])]).unique()
     _, ref64, den = oracle_bf16(A[idx].contiguous(), B, C[idx].contiguous(), w.alpha, w.beta)
     r = ratio(out[idx], ref64, den)
     assert r <= TOL_BF16, r
