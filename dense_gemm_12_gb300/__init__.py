@@ -22,7 +22,7 @@ __all__ = [
     "GemmError", "load_library", "library_path", "gemm_sgemm", "gemm_bf16gemm",
     "gemm_bf16gemm_decode_static", "gemm_bf16gemm_epilogue", "bf16gemm_epilogue", "ACT", "OUT",
     "gemm_status_string", "gemm_check_device_error", "gemm_shutdown",
-    "gemm_select_path", "gemm_quantization", "gemm_version", "sgemm", "bf16gemm",
+    "gemm_select_path", "gemm_split_parts", "gemm_quantization", "gemm_version", "sgemm", "bf16gemm",
     "STATUS", "PATHS",
 ]
 
@@ -98,6 +98,8 @@ def load_library(build_if_missing: bool = False):
         lib.gemm_quantization.argtypes = [i64, i64, i64, i64, i64, i64,
                                           ctypes.POINTER(_Quantization)]
         lib.gemm_quantization.restype = cint
+        lib.gemm_split_parts.argtypes = [cint, i64, i64, i64]
+        lib.gemm_split_parts.restype = cint
         lib.gemm_version.argtypes = []
         lib.gemm_version.restype = cint
         _lib = lib
@@ -150,6 +152,11 @@ def gemm_select_path(is_bf16, M, N, K, alpha, A, lda, B, ldb) -> str:
     """Name of the kernel path a call with these arguments takes (host-only)."""
     return PATHS[load_library().gemm_select_path(int(bool(is_bf16)), M, N, K, alpha, A, lda,
                                                  B, ldb)]
+
+
+def gemm_split_parts(is_bf16, M, N, K) -> int:
+    """k-ranges per work item of the last round (1 = no split; 0 = no device)."""
+    return load_library().gemm_split_parts(int(bool(is_bf16)), M, N, K)
 
 
 def gemm_quantization(M, N, BM, BN, num_sms, ctas_per_sm) -> dict:

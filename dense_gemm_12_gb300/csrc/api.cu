@@ -207,6 +207,28 @@ gemm_status_t ensure_scratch(DeviceState& st, cudaStream_t stream, int64_t float
 // tiles split along k when that balances the SMs better).  A split plan needs
 // this stream's scratch area; `lock` (on st->ws_mutex) is then held until the
 // caller has launched.
+}  // namespace
+
+int tail_split(int items, int num_kb, int workers, double part_cost_kb) {
+  if (items <= 0 || workers <= 0 || num_kb <= 0) return 1;
+  const int tail = items >= workers ? items % workers : items;
+  if (tail == 0) return 1;
+  int best_s = 1;
+  double best = 1.0;
+  for (int s = 2; s <= 8 && s * 4 <= num_kb; ++s) {
+    const double t =
+        static_cast<double>((static_cast<int64_t>(tail) * s + workers - 1) / workers) / s +
+        s * part_cost_kb / num_kb;
+    if (t < best - 1e-9) {
+      best = t;
+      best_s = s;
+    }
+  }
+  return best_s;
+}
+
+namespace {
+
 gemm_status_t plan_simt(DeviceState* st, cudaStream_t cs, SimtArgs& a,
                         std::unique_lock<std::mutex>& lock) {
   const int tiles = ((a.M + kSimtBM - 1) / kSimtBM) * ((a.N + kSimtBN - 1) / kSimtBN);
@@ -347,6 +369,21 @@ gemm_path_t gemm_select_path(int is_bf16, int64_t M, int64_t N, int64_t K, float
   return select_path(is_bf16 != 0, M, N, K, alpha, A, lda, B, ldb);
 }
 
+int gemm_split_parts(int is_bf16, int64_t M, int64_t N, int64_t K) {
+  if (M < 0 || N < 0 || K < 0 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return 0;
+  gemm_status_t s;
+  DeviceState* st = device_state(&s);
+  if (st == nullptr) return 0;
+  if (M == 0 || N == 0 || K == 0) return 1;
+  const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
+  if (is_bf16) {
+    if (M <= kDecBM) return 1;
+    return tc_plan(m, n, k, st->num_sms).split;
+  }
+  const int tiles = ((m + kSimtBM - 1) / kSimtBM) * ((n + kSimtBN - 1) / kSimtBN);
+  return simt_plan(tiles, (k + kSimtBK - 1) / kSimtBK, st->num_sms).split;
+}
+
 gemm_status_t gemm_quantization(int64_t M, int64_t N, int64_t BM, int64_t BN, int64_t num_sms,
                                 int64_t ctas_per_sm, gemm_quantization_t* out) {
   if (out == nullptr || M < 0 || N < 0 || BM <= 0 || BN <= 0 || num_sms <= 0 || ctas_per_sm <= 0)
@@ -428,7 +465,7 @@ static gemm_status_t run_bf16_tensor_core(DeviceState* st, gemm_path_t path, int
                                           int64_t ldb, const Epilogue& epi, cudaStream_t cs) {
   CUtensorMap tmA, tmB;
   if (path == GEMM_PATH_TC_BF16 || path == GEMM_PATH_TC_BF16_PAIR) {
-    // launch_tc_bf16 runs the CTA-pair kernel exactly when M > kTcBM
+    // tc_plan picks the CTA-pair kernel exactly when M > kTcBM
     if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, K, M, lda, kTcBK, kTcBM,
                    CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, N, K, ldb, 64, kTcBK,
@@ -440,7 +477,21 @@ static gemm_status_t run_bf16_tensor_core(DeviceState* st, gemm_path_t path, int
     a.K = static_cast<int>(K);
     a.epi = epi;
     a.err = st->err_word;
-    return from_cuda(launch_tc_bf16(a, &tmA, &tmB, st->num_sms, cs));
+    const TcPlan pl = tc_plan(a.M, a.N, a.K, st->num_sms);
+    a.full_items = pl.full_items;
+    a.split = pl.split;
+    a.ws = nullptr;
+    a.counters = nullptr;
+    if (pl.split == 1) return from_cuda(launch_tc_bf16(a, pl, &tmA, &tmB, cs));
+    // Split items: the stream's scratch stays locked until the launch is
+    // queued, so no other thread can regrow it underneath.
+    std::lock_guard<std::mutex> lock(st->ws_mutex);
+    Scratch* sc = nullptr;
+    const gemm_status_t s = ensure_scratch(*st, cs, pl.ws_floats, pl.counters, &sc);
+    if (s != GEMM_OK) return s;
+    a.ws = sc->ws;
+    a.counters = sc->counters;
+    return from_cuda(launch_tc_bf16(a, pl, &tmA, &tmB, cs));
   }
   // GEMM_PATH_TC_DECODE
   if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, K, M, lda, 64, kDecBM,

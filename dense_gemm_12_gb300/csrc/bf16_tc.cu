@@ -27,8 +27,15 @@
 // (tc_bf16_pair_kernel below): two SMs share one 256 x 256 tile and one MMA
 // stream, which cuts the shared-memory operand bytes each SM's tensor core
 // reads per MMA from 12 KB to 8 KB.
+//
+// Both kernels walk work units instead of tiles: the tiles that would leave
+// the last round of the persistent grid partly idle ("A GEMM Kernel, Step by
+// Step", "The fringe and the last wave") are cut along k, the split-K of its
+// "What is left": each part's partial sums go to a workspace, and the last
+// part to finish a tile adds them in part order before the output stage.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "internal.h"
@@ -44,6 +51,12 @@ constexpr int BM = kTcBM, BN = kTcBN, BK = kTcBK;
 #ifndef G12_TC_GROUP_M
 #define G12_TC_GROUP_M 8
 #endif
+// Cost of storing or loading one split part's partial sums, in k-block times
+// (see tail_split): a 128 KB partial per CTA moves in about 1.1 us at the
+// ~120 GB/s one SM gets from L2, some 3 k-blocks of the tensor core.
+#ifndef G12_TC_PART_COST
+#define G12_TC_PART_COST 3.0
+#endif
 constexpr int STAGES = G12_TC_STAGES;
 constexpr int kStageBytesA = BM * BK * 2;            // 16 KB
 constexpr int kStageBytesB = BK * BN * 2;            // 32 KB
@@ -51,9 +64,14 @@ constexpr int kBoxBytesB = BK * 64 * 2;              // one 64-column box, 8 KB
 constexpr int kStageBytes = kStageBytesA + kStageBytesB;
 constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
+constexpr int kEpiWarps = kEpiThreads / 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kGroupM = G12_TC_GROUP_M;  // raster group height (tile rows or row pairs)
 constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN, /*A MN-major*/ 0, /*B MN-major*/ 1);
+// Named barriers of the epilogue warps (0 is __syncthreads).
+constexpr uint32_t kEpiBarSync = 1, kEpiBarAny = 2;
+// Partial sums of one split part of one CTA's 128 x 256 tile.
+constexpr int64_t kPartFloats = static_cast<int64_t>(BM) * BN;
 
 struct __align__(8) TcSmemTail {
   uint64_t full[STAGES];
@@ -63,6 +81,7 @@ struct __align__(8) TcSmemTail {
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
+  int last_flag;
 };
 
 constexpr size_t kSmemBytes = 1024 + STAGES * kStageBytes + sizeof(TcSmemTail);
@@ -75,6 +94,35 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
   const int local = t - g * per_group;
   tm = first_m + local % rows;
   tn = local / rows;
+}
+
+// One work unit: item (tile or pair tile), its k-block range and, for a
+// split item, its part index and tail index (part = -1 for a whole item).
+struct Unit {
+  int item, kb0, kb1, part, tail;
+};
+
+__device__ __forceinline__ int num_units(const TcArgs& p, int num_items) {
+  return p.full_items + (num_items - p.full_items) * p.split;
+}
+
+__device__ __forceinline__ Unit unit_of(const TcArgs& p, int u, int num_kb) {
+  Unit w;
+  if (u < p.full_items) {
+    w.item = u;
+    w.kb0 = 0;
+    w.kb1 = num_kb;
+    w.part = -1;
+    w.tail = -1;
+    return w;
+  }
+  const int v = u - p.full_items;
+  w.tail = v / p.split;
+  w.part = v - w.tail * p.split;
+  w.item = p.full_items + w.tail;
+  w.kb0 = w.part * num_kb / p.split;
+  w.kb1 = (w.part + 1) * num_kb / p.split;
+  return w;
 }
 
 // One 32-column chunk of an accumulator row: D = act(alpha*acc + beta*C + bias).
@@ -136,6 +184,89 @@ __device__ __forceinline__ void store_row_chunk(const TcArgs& p, int row, int co
   }
 }
 
+__device__ __forceinline__ void epi_bar() {
+  asm volatile("bar.sync %0, %1;" ::"n"(kEpiBarSync), "n"(kEpiThreads) : "memory");
+}
+
+// Output stage of one work unit, run by the 4 epilogue warps of a CTA (thread
+// et = TMEM lane et = row et of the CTA's 128-row tile).  taddr: this warp's
+// lanes of the accumulator.  slot: this CTA's index among the split items'
+// counters (-1 for a whole item).
+//
+// A split part stores its partial sums (thread-major float4s, coalesced per
+// warp), then counts its arrival; the last of the `split` parts re-reads its
+// own accumulator and adds all parts in part order -- a fixed order, so the
+// result does not depend on which part finishes last -- and writes D.
+__device__ __forceinline__ void epilogue_unit(const TcArgs& p, uint32_t taddr, int row, int tn,
+                                              int slot, int part, int et, int* last_flag) {
+  if (slot < 0) {
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(taddr + c * 32, r);
+      tc_wait_ld();
+      if (row < p.M) store_row_chunk(p, row, tn * BN + c * 32, r);
+    }
+    return;
+  }
+  float4* const ws4 = reinterpret_cast<float4*>(p.ws);
+  const int64_t slot_base = static_cast<int64_t>(slot) * p.split;  // in parts
+  {
+    float4* mine = ws4 + (slot_base + part) * (kPartFloats / 4);
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(taddr + c * 32, r);
+      tc_wait_ld();
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        __stcg(mine + (c * 8 + q) * kEpiThreads + et,
+               make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                           __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3])));
+    }
+  }
+  epi_bar();
+  if (et == 0) {
+    __threadfence();  // publish the whole CTA's partial before arriving
+    const uint32_t before = atomicAdd(p.counters + slot, 1u);
+    *last_flag = (before == static_cast<uint32_t>(p.split - 1)) ? 1 : 0;
+  }
+  epi_bar();
+  if (*reinterpret_cast<volatile int*>(last_flag)) {
+    __threadfence();
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(taddr + c * 32, r);
+      tc_wait_ld();
+      float sum[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) sum[i] = 0.0f;
+      for (int q_part = 0; q_part < p.split; ++q_part) {
+        if (q_part == part) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) sum[i] += __uint_as_float(r[i]);
+        } else {
+          const float4* src = ws4 + (slot_base + q_part) * (kPartFloats / 4);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 v = __ldcg(src + (c * 8 + q) * kEpiThreads + et);
+            sum[4 * q] += v.x;
+            sum[4 * q + 1] += v.y;
+            sum[4 * q + 2] += v.z;
+            sum[4 * q + 3] += v.w;
+          }
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(sum[i]);
+      if (row < p.M) store_row_chunk(p, row, tn * BN + c * 32, r);
+    }
+    if (et == 0) p.counters[slot] = 0u;
+  }
+  epi_bar();  // last_flag is rewritten by the next split unit
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bf16_kernel(const __grid_constant__ TcArgs p, const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB) {
@@ -148,8 +279,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int tiles_m = (p.M + BM - 1) / BM;
   const int tiles_n = (p.N + BN - 1) / BN;
-  const int num_tiles = tiles_m * tiles_n;
   const int num_kb = (p.K + BK - 1) / BK;
+  const int units = num_units(p, tiles_m * tiles_n);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -162,6 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&tail->drain, 1);
     tail->abort_flag = 0;
+    tail->last_flag = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
@@ -180,10 +312,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        const Unit w = unit_of(p, u, num_kb);
         int tm, tn;
-        tile_coords(t, tiles_m, tiles_n, tm, tn);
-        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+        tile_coords(w.item, tiles_m, tiles_n, tm, tn);
+        for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t round = it / STAGES;
           if (!mbar_wait(&tail->empty[s], (round & 1u) ^ 1u, abort_flag, p.err)) {
@@ -213,7 +346,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t j = 0;
       bool ok = true;
       bool issued = false;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++j) {
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++j) {
+        const Unit w = unit_of(p, u, num_kb);
         const uint32_t ab = j & 1u, ar = j >> 1;
         if (!mbar_wait(&tail->tmem_empty[ab], (ar & 1u) ^ 1u, abort_flag, p.err)) {
           ok = false;
@@ -221,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + ab * BN;
-        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+        for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t round = it / STAGES;
           if (!mbar_wait(&tail->full[s], round & 1u, abort_flag, p.err)) {
@@ -238,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // B: MN-major, 64-column boxes 8 KB apart (LBO), 8-row k groups
             // 1024 B apart (SBO); a K step of 16 rows is 2048 B.
             const uint64_t bdesc = smem_desc_sw128(sb + kk * 2048, kBoxBytesB, 1024);
-            tc_mma_f16(d_tmem, adesc, bdesc, kIdesc, (kb | kk) != 0 ? 1u : 0u);
+            tc_mma_f16(d_tmem, adesc, bdesc, kIdesc, (kb != w.kb0 || kk != 0) ? 1u : 0u);
           }
           issued = true;
           tc_commit(&tail->empty[s]);
@@ -256,22 +390,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // -------------------------------------------------------- epilogue
     const int quarter = warp & 3;  // TMEM lanes this warp may access
+    const int et = quarter * 32 + lane;
     uint32_t j = 0;
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++j) {
+    for (int u = blockIdx.x; u < units; u += gridDim.x, ++j) {
+      const Unit w = unit_of(p, u, num_kb);
       int tm, tn;
-      tile_coords(t, tiles_m, tiles_n, tm, tn);
+      tile_coords(w.item, tiles_m, tiles_n, tm, tn);
       const uint32_t ab = j & 1u, ar = j >> 1;
-      if (!mbar_wait(&tail->tmem_full[ab], ar & 1u, abort_flag, p.err)) break;
+      const bool ok = mbar_wait(&tail->tmem_full[ab], ar & 1u, abort_flag, p.err);
+      // Leave together if a wait ran out anywhere (see named_bar_any).
+      if (named_bar_any(kEpiBarAny, kEpiThreads, !ok)) break;
       tc_fence_after_sync();
-      const int row = tm * BM + quarter * 32 + lane;
+      const int row = tm * BM + et;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + ab * BN;
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(taddr + c * 32, r);
-        tc_wait_ld();
-        if (row < p.M) store_row_chunk(p, row, tn * BN + c * 32, r);
-      }
+      epilogue_unit(p, taddr, row, tn, w.tail, w.part, et, &tail->last_flag);
       tc_fence_before_sync();
       mbar_arrive(&tail->tmem_empty[ab]);
     }
@@ -308,7 +440,6 @@ constexpr int kPairBN = BN / 2;                         // B columns held per CT
 constexpr int kPairStageBytesA = BM * BK * 2;           // 16 KB
 constexpr int kPairStageBytesB = BK * kPairBN * 2;      // 16 KB
 constexpr int kPairStageBytes = kPairStageBytesA + kPairStageBytesB;
-constexpr int kEpiWarps = kEpiThreads / 32;
 constexpr uint16_t kPairMask = 0x3;
 constexpr uint32_t kPairIdesc = idesc_bf16_f32(2 * BM, BN, /*A MN-major*/ 0, /*B MN-major*/ 1);
 
@@ -320,6 +451,7 @@ struct __align__(8) PairSmemTail {
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
+  int last_flag;
 };
 
 constexpr size_t kPairSmemBytes = 1024 + PS * kPairStageBytes + sizeof(PairSmemTail);
@@ -338,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tiles_m = (p.M + BM - 1) / BM;
   const int tiles_n = (p.N + BN - 1) / BN;
   const int pairs_m = (tiles_m + 1) / 2;
-  const int num_items = pairs_m * tiles_n;
+  const int units = num_units(p, pairs_m * tiles_n);
   const int num_kb = (p.K + BK - 1) / BK;
   const uint32_t rank = cluster_cta_rank() & 1u;
   const bool even = (rank == 0);
@@ -356,6 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&tail->drain, 1);
     tail->abort_flag = 0;
+    tail->last_flag = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
@@ -377,11 +510,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t full0 = mapa_shared(smem_u32(&tail->full[0]), 0);
       uint32_t it = 0;
       bool ok = true;
-      for (int t = first_item; t < num_items && ok; t += item_stride) {
+      for (int u = first_item; u < units && ok; u += item_stride) {
+        const Unit w = unit_of(p, u, num_kb);
         int pm, tn;
-        tile_coords(t, pairs_m, tiles_n, pm, tn);
+        tile_coords(w.item, pairs_m, tiles_n, pm, tn);
         const int tm = pm * 2 + static_cast<int>(rank);
-        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+        for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
           const int s = it % PS;
           const uint32_t round = it / PS;
           if (!mbar_wait(&tail->empty[s], (round & 1u) ^ 1u, abort_flag, p.err)) {
@@ -418,7 +552,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t j = 0;
       bool ok = true;
       bool issued = false;
-      for (int t = first_item; t < num_items && ok; t += item_stride, ++j) {
+      for (int u = first_item; u < units && ok; u += item_stride, ++j) {
+        const Unit w = unit_of(p, u, num_kb);
         const uint32_t ab = j & 1u, ar = j >> 1;
         if (!mbar_wait(&tail->tmem_empty[ab], (ar & 1u) ^ 1u, abort_flag, p.err)) {
           ok = false;
@@ -426,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + ab * BN;
-        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+        for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
           const int s = it % PS;
           const uint32_t round = it / PS;
           if (!mbar_wait(&tail->full[s], round & 1u, abort_flag, p.err)) {
@@ -440,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint64_t adesc = smem_desc_sw128(sa + kk * 32, 16, 1024);
             const uint64_t bdesc = smem_desc_sw128(sb + kk * 2048, kBoxBytesB, 1024);
-            tc_mma_f16_pair(d_tmem, adesc, bdesc, kPairIdesc, (kb | kk) != 0 ? 1u : 0u);
+            tc_mma_f16_pair(d_tmem, adesc, bdesc, kPairIdesc, (kb != w.kb0 || kk != 0) ? 1u : 0u);
           }
           issued = true;
           tc_commit_pair_multicast(&tail->empty[s], kPairMask);
@@ -463,24 +598,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // -------------------------------------------------------- epilogue
     const int quarter = warp & 3;  // TMEM lanes this warp may access
+    const int et = quarter * 32 + lane;
     const uint32_t tmem_empty0 = mapa_shared(smem_u32(&tail->tmem_empty[0]), 0);
     uint32_t j = 0;
-    for (int t = first_item; t < num_items; t += item_stride, ++j) {
+    for (int u = first_item; u < units; u += item_stride, ++j) {
+      const Unit w = unit_of(p, u, num_kb);
       int pm, tn;
-      tile_coords(t, pairs_m, tiles_n, pm, tn);
+      tile_coords(w.item, pairs_m, tiles_n, pm, tn);
       const int tm = pm * 2 + static_cast<int>(rank);
       const uint32_t ab = j & 1u, ar = j >> 1;
-      if (!mbar_wait(&tail->tmem_full[ab], ar & 1u, abort_flag, p.err)) break;
+      const bool ok = mbar_wait(&tail->tmem_full[ab], ar & 1u, abort_flag, p.err);
+      if (named_bar_any(kEpiBarAny, kEpiThreads, !ok)) break;
       tc_fence_after_sync();
-      const int row = tm * BM + quarter * 32 + lane;
+      const int row = tm * BM + et;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + ab * BN;
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(taddr + c * 32, r);
-        tc_wait_ld();
-        if (row < p.M) store_row_chunk(p, row, tn * BN + c * 32, r);
-      }
+      // each CTA of the pair owns the counter and partials of its 128 rows
+      const int slot = w.tail < 0 ? -1 : w.tail * 2 + static_cast<int>(rank);
+      epilogue_unit(p, taddr, row, tn, slot, w.part, et, &tail->last_flag);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(tmem_empty0 + ab * static_cast<uint32_t>(sizeof(uint64_t)));
@@ -498,11 +632,63 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_tc_bf16(const TcArgs& a, const CUtensorMap* tmA, const CUtensorMap* tmB,
-                           int num_sms, cudaStream_t stream) {
-  const int tiles_m = (a.M + BM - 1) / BM;
-  const int tiles_n = (a.N + BN - 1) / BN;
-  if (tiles_m >= 2) {
+// Clusters of the pair kernel that can be resident at once on the current
+// device (one query per device).
+static int pair_max_clusters(int num_sms) {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return num_sms / 2;
+  }
+  const int known = cache[dev].load(std::memory_order_relaxed);
+  if (known > 0) return known;
+  int clusters = 0;
+  auto kernel = tc_bf16_pair_kernel;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kPairSmemBytes)) == cudaSuccess) {
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * (num_sms / 2));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kPairSmemBytes;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess) clusters = 0;
+  }
+  cudaGetLastError();
+  if (clusters < 1) clusters = num_sms / 2;
+  cache[dev].store(clusters, std::memory_order_relaxed);
+  return clusters;
+}
+
+TcPlan tc_plan(int M, int N, int K, int num_sms) {
+  TcPlan pl{};
+  const int tiles_m = (M + BM - 1) / BM;
+  const int tiles_n = (N + BN - 1) / BN;
+  const int num_kb = (K + BK - 1) / BK;
+  pl.pair = tiles_m >= 2;
+  const int ctas_per_item = pl.pair ? 2 : 1;
+  const int items = pl.pair ? ((tiles_m + 1) / 2) * tiles_n : tiles_m * tiles_n;
+  const int workers = pl.pair ? pair_max_clusters(num_sms) : num_sms;
+  pl.split = tail_split(items, num_kb, workers, G12_TC_PART_COST);
+  const int tail = pl.split > 1 ? (items >= workers ? items % workers : items) : 0;
+  pl.full_items = items - tail;
+  const int units = pl.full_items + tail * pl.split;
+  pl.grid = ctas_per_item * (units < workers ? units : workers);
+  pl.ws_floats = static_cast<int64_t>(tail) * pl.split * ctas_per_item * kPartFloats;
+  pl.counters = static_cast<int64_t>(tail) * ctas_per_item;
+  return pl;
+}
+
+cudaError_t launch_tc_bf16(const TcArgs& a, const TcPlan& plan, const CUtensorMap* tmA,
+                           const CUtensorMap* tmB, cudaStream_t stream) {
+  if (plan.grid < 1) return cudaSuccess;
+  if (plan.pair) {
     auto kernel = tc_bf16_pair_kernel;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kPairSmemBytes));
@@ -513,21 +699,12 @@ cudaError_t launch_tc_bf16(const TcArgs& a, const CUtensorMap* tmA, const CUtens
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(plan.grid);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kPairSmemBytes;
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const int items = ((tiles_m + 1) / 2) * tiles_n;
-    int max_clusters = 0;
-    cfg.gridDim = dim3(2 * (num_sms / 2));
-    if (cudaOccupancyMaxActiveClusters(&max_clusters, kernel, &cfg) != cudaSuccess ||
-        max_clusters < 1) {
-      cudaGetLastError();
-      max_clusters = num_sms / 2;
-    }
-    const int clusters = items < max_clusters ? items : max_clusters;
-    cfg.gridDim = dim3(2 * clusters);
     e = cudaLaunchKernelEx(&cfg, kernel, a, *tmA, *tmB);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
@@ -536,9 +713,7 @@ cudaError_t launch_tc_bf16(const TcArgs& a, const CUtensorMap* tmA, const CUtens
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
-  const int tiles = tiles_m * tiles_n;
-  const int grid = tiles < num_sms ? tiles : num_sms;
-  kernel<<<grid, kThreads, kSmemBytes, stream>>>(a, *tmA, *tmB);
+  kernel<<<plan.grid, kThreads, kSmemBytes, stream>>>(a, *tmA, *tmB);
   return cudaGetLastError();
 }
 

@@ -59,15 +59,46 @@ cudaError_t launch_simt(const SimtArgs& a, LoadMode mode_a, LoadMode mode_b,
 // Tile geometry of the CUDA-core kernel (also used by the launch planner).
 constexpr int kSimtBM = 128, kSimtBN = 128, kSimtBK = 32;
 
+// Number of k-parts S (1 = none) into which the items of the last round are
+// cut when `items` equal work items of num_kb k-blocks run on `workers`
+// persistent workers.  In item-times the tail then takes
+//     ceil(tail * S / workers) / S  +  S * part_cost_kb / num_kb
+// instead of 1, where part_cost_kb is the time to store or load one part's
+// partial sums in k-block times (the last part to finish writes its own and
+// reads the other S - 1).  Every part keeps at least 4 k-blocks.
+int tail_split(int items, int num_kb, int workers, double part_cost_kb);
+
 struct TcArgs {
   int M, N, K;
   Epilogue epi;
   uint32_t* err;
+  // Work plan (see tc_plan): work items are tiles (128 x 256) or, on CTA
+  // pairs, pair tiles (256 x 256) in raster order.  Items [0, full_items) run
+  // whole; every later one is cut into `split` k-ranges whose partial sums
+  // meet in `ws` (128 x 256 floats per part and CTA) and are added, in part
+  // order, by the last part to arrive on its counter in `counters` (one per
+  // item and CTA, zero between launches).
+  int full_items;
+  int split;
+  float* ws;
+  uint32_t* counters;
 };
 
-// bf16 tensor-core GEMM (tcgen05, accumulator in TMEM): 128 x 256 tiles.
-cudaError_t launch_tc_bf16(const TcArgs& a, const CUtensorMap* tmA, const CUtensorMap* tmB,
-                           int num_sms, cudaStream_t stream);
+// Launch plan of the bf16 tensor-core GEMM for one shape.
+struct TcPlan {
+  bool pair;          // CTA-pair kernel (M > 128) or single-CTA kernel
+  int full_items;
+  int split;
+  int grid;           // CTAs to launch (pairs: twice the clusters)
+  int64_t ws_floats;  // workspace the split items need
+  int64_t counters;   // counters the split items need
+};
+TcPlan tc_plan(int M, int N, int K, int num_sms);
+
+// bf16 tensor-core GEMM (tcgen05, accumulator in TMEM): 128 x 256 tiles on
+// one CTA, or 256 x 256 tiles on CTA pairs, as planned by tc_plan.
+cudaError_t launch_tc_bf16(const TcArgs& a, const TcPlan& plan, const CUtensorMap* tmA,
+                           const CUtensorMap* tmB, cudaStream_t stream);
 constexpr int kTcBM = 128, kTcBN = 256, kTcBK = 64;
 
 struct DecodeArgs {

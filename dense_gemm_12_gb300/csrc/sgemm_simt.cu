@@ -544,21 +544,12 @@ SimtPlan simt_plan(int tiles, int num_kb, int num_sms) {
   SimtPlan pl{tiles, 1, tiles < num_sms ? tiles : num_sms, 0, 0};
   if (tiles <= 0 || num_sms <= 0) return pl;
   // Tiles beyond the last full wave (all of them when there are fewer tiles
-  // than SMs) are split along k when that shortens the last wave: with S
-  // parts the tail takes ceil(tail * S / sms) / S tile-times instead of 1.
-  // Every part keeps at least 4 k-blocks.
-  const int tail = tiles >= num_sms ? tiles % num_sms : tiles;
-  if (tail == 0) return pl;
-  int best_s = 1;
-  double best = 1.0;
-  for (int s = 2; s <= 8 && s * 4 <= num_kb; ++s) {
-    const double t = static_cast<double>((static_cast<int64_t>(tail) * s + num_sms - 1) / num_sms) / s;
-    if (t < best - 1e-9) {
-      best = t;
-      best_s = s;
-    }
-  }
+  // than SMs) are split along k when that shortens the last wave.
+  // A 64 KB partial moves in about a quarter of a 128 x 128 x 32 k-block's
+  // FFMA time.
+  const int best_s = tail_split(tiles, num_kb, num_sms, 0.3);
   if (best_s == 1) return pl;
+  const int tail = tiles >= num_sms ? tiles % num_sms : tiles;
   pl.full_items = tiles - tail;
   pl.split = best_s;
   const int items = pl.full_items + tail * best_s;

@@ -228,6 +228,19 @@ gemm_path_t gemm_select_path(int is_bf16, int64_t M, int64_t N, int64_t K,
                              const void *B, int64_t ldb);
 
 /*
+ * gemm_split_parts -- host-only diagnostics: into how many k-ranges the tile
+ * kernel for an M x N x K problem cuts each work item of the persistent
+ * grid's last round ("A GEMM Kernel, Step by Step": the partial last wave of
+ * "The fringe and the last wave", filled by the split-K of "What is left").
+ * 1 means no item is split.  `is_bf16`
+ * selects gemm_bf16gemm's tensor-core kernels (M > 16) instead of
+ * gemm_sgemm's CUDA-core kernel; the decode kernel (bf16, M <= 16) plans its
+ * own split and reports 1 here.  Returns 0 for negative sizes or when there
+ * is no usable sm_103a device (the plan depends on its SM count).
+ */
+int gemm_split_parts(int is_bf16, int64_t M, int64_t N, int64_t K);
+
+/*
  * Tile and wave quantization of a launch ("A GEMM Kernel, Step by Step",
  * "The fringe and the last wave"; "Tiled matrix multiplication",
  * "Complexity and constants", wave quantization).

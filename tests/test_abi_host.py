@@ -140,3 +140,11 @@ def test_fails_loudly_without_device(gemm_lib):
     assert gemm_lib.gemm_sgemm(4, 4, 4, 1.0, P, 4, P, 4, 0.0, P, 4, 0) == UNSUPPORTED
     assert gemm_lib.gemm_bf16gemm(4, 4, 4, 1.0, P, 4, P, 4, 0.0, P, 4, 0) == UNSUPPORTED
     assert gemm_lib.gemm_sgemm(4, 4, 0, 1.0, P, 4, P, 4, 2.0, P, 4, 0) == UNSUPPORTED
+    # the split plan depends on the device's SM count: no device, no plan
+    assert gemm_lib.gemm_split_parts(0, 4096, 4096, 4096) == 0
+    assert gemm_lib.gemm_split_parts(1, 8192, 8192, 8192) == 0
+
+
+def test_split_parts_rejects_negative_sizes(gemm_lib):
+    assert gemm_lib.gemm_split_parts(0, -1, 4, 4) == 0
+    assert gemm_lib.gemm_split_parts(1, 4, 4, -4) == 0

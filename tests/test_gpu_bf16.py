@@ -119,3 +119,53 @@ def test_full_8192_sampled_rows():
     r = ratio(out[idx], ref64, den)
     assert r <= TOL_BF16, r
     assert dC.untouched_outside()
+
+
+# ---- the last round's work items cut along k (split-K tail) ---------------
+# The plan depends on how many CTAs (pairs) are resident; each case asserts
+# that it really splits.
+
+@pytest.mark.parametrize("M,N,K", [
+    (2560, 4096, 1024),   # pair kernel: 80 pair tiles on at most 76 clusters
+    (64, 2048, 2048),     # single-CTA kernel: 8 tiles on 152 SMs
+])
+def test_split_integers_exact(M, N, K):
+    # |partial sums| <= 16 K < 2^24: exact in fp32 in any order and any split
+    assert g.gemm_split_parts(1, M, N, K) > 1
+    A, B, C = make_inputs(M, N, K, ("int", None), ("int", None), ("int", None), seed=31,
+                          dtype="bf16")
+    out, st, _, _, dC = run_bf16gemm(A, B, C, 1.5, -0.5)
+    assert st == 0
+    ref32, _, _ = oracle_bf16(A, B, C, 1.5, -0.5)
+    assert np.array_equal(out.numpy(), ref32)
+    assert dC.untouched_outside()
+    check_device_error()
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (2560, 4096, 1024),   # pair kernel
+    (2304, 4296, 2000),   # pair kernel, ragged N and K (last part ends on a partial k-block)
+    (100, 1024, 4096),    # single-CTA kernel
+])
+def test_split_matches_oracle_and_repeats(M, N, K):
+    assert g.gemm_split_parts(1, M, N, K) > 1
+    A, B, C = _inputs(M, N, K, seed=M + K)
+    outs = [run_bf16gemm(A, B, C, 0.7, 0.3)[0] for _ in range(3)]
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int32), outs[0].view(torch.int32))
+    gen = torch.Generator().manual_seed(2)
+    idx = torch.randperm(M, generator=gen)[:48].sort().values
+    idx = torch.cat([idx, torch.tensor([0, M - 1])]).unique()
+    _, ref64, den = oracle_bf16(A[idx].contiguous(), B, C[idx].contiguous(), 0.7, 0.3)
+    r = ratio(outs[0][idx], ref64, den)
+    assert r <= TOL_BF16, r
+    check_device_error()
+
+
+def test_split_parts_of_the_benchmark_shapes():
+    # 8192^3: 1024 pair tiles on up to 76 clusters leave a partial round
+    assert g.gemm_split_parts(1, 8192, 8192, 8192) >= 1
+    # decode shapes plan their own split
+    assert g.gemm_split_parts(1, 16, 12288, 4096) == 1
+    # fp32 4092^3: 1024 tiles on 152 SMs, tail of 112 tiles split
+    assert g.gemm_split_parts(0, 4092, 4092, 4092) > 1

@@ -77,6 +77,21 @@ def test_decode_kernel_epilogues(act, out):
     check_device_error()
 
 
+@pytest.mark.parametrize("M,N,K,act,out", [
+    (100, 1024, 4096, "gelu", "bf16"),   # single-CTA kernel, tiles split along k
+    (2560, 4096, 1024, "relu", "f32"),   # pair kernel, last round split along k
+])
+def test_split_tiles_epilogue(M, N, K, act, out):
+    # the output stage runs once, on the summed parts
+    assert g.gemm_split_parts(1, M, N, K) > 1
+    A, B, C = make_inputs(M, N, K, ("normal", 1.0), ("normal", 0.05), ("uniform", None),
+                          seed=15, dtype="bf16")
+    bias = torch.randn(N, generator=torch.Generator().manual_seed(8))
+    D = _run(A, B, C, 0.9, 0.5, bias, act, out)
+    _check(A, B, C, 0.9, 0.5, bias, act, out, D)
+    check_device_error()
+
+
 def test_padded_output_and_ragged():
     M, N, K = 129, 264, 72
     A, B, C = make_inputs(M, N, K, seed=13, dtype="bf16")
