@@ -288,6 +288,48 @@ def bench_bf16_8192_fused(torch, g, wl, peaks, device, stream_obj):
     }
 
 
+def bench_bf16_8192_fp8(torch, g, wl, peaks, device, stream_obj):
+    """The bf16 8192^3 GEMM quantised in its output stage: bias + GELU, fp8 E4M3
+    D scaled by d_scale, and the amax of the unscaled values."""
+    w = wl.WORKLOADS["bf16_8192"]
+    A, B, _ = wl.workload_inputs(w, with_c=False)
+    A, B = A.to(device), B.to(device)
+    bias = (torch.randn(w.N, generator=torch.Generator().manual_seed(9)) * 0.1).to(device)
+    D = torch.empty((w.M, w.N), dtype=torch.uint8, device=device)
+    amax = torch.zeros(1, dtype=torch.float32, device=device)
+    s = stream_obj.cuda_stream
+    o = g.GemmOutput()
+    o.beta, o.C, o.ldc = 0.0, 0, w.N
+    o.bias, o.act = bias.data_ptr(), g.ACT["gelu"]
+    o.residual, o.ldr = 0, w.N
+    o.d_scale, o.amax = 64.0, amax.data_ptr()
+    o.D, o.ldd, o.d_type = D.data_ptr(), w.N, g.OUT["f8e4m3"]
+
+    def step(i):
+        st = g.gemm_bf16gemm_fused(w.M, w.N, w.K, w.alpha, A.data_ptr(), w.K, B.data_ptr(), w.N,
+                                   o, s)
+        if st != 0:
+            raise RuntimeError("gemm_bf16gemm_fused: " + g.gemm_status_string(st))
+    for i in range(3):
+        step(i)
+    torch.cuda.synchronize()
+    times = time_launches(torch, step, 10, stream_obj)
+    ms = statistics.median(times)
+    tflops = w.flops / (ms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"]
+    del A, B, D, bias, amax
+    torch.cuda.empty_cache()
+    return {
+        "workload": "bf16 GEMM M=N=K=8192 with fused bias + GELU, fp8 E4M3 output (scale 64) + amax",
+        "kernel": "tc_bf16_pair_kernel (same kernel, fused output stage)",
+        "value": tflops * 1e3, "unit": "GFLOP/s", "ms_per_launch_median": ms,
+        "launches_timed": len(times),
+        "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                     "frac": tflops / peak, "traffic": None,
+                     "peak_note": "%s dense bf16 burst (cuBLAS)" % peaks["source"]},
+    }
+
+
 def bench_decode(torch, g, wl, peaks, device, stream_obj):
     w = wl.WORKLOADS["decode_16"]
     A, B, C0 = wl.workload_inputs(w)
@@ -526,6 +568,8 @@ def run_ours(args):
         parts["bf16_8192"] = bench_bf16_8192(torch, g, wl, peaks, device, stream_obj)
         parts["bf16_8192_bias_gelu_bf16out"] = bench_bf16_8192_fused(torch, g, wl, peaks, device,
                                                                       stream_obj)
+        parts["bf16_8192_bias_gelu_fp8out_amax"] = bench_bf16_8192_fp8(torch, g, wl, peaks,
+                                                                        device, stream_obj)
         parts["decode_16x12288x4096"] = bench_decode(torch, g, wl, peaks, device, stream_obj)
 
     cpu = None

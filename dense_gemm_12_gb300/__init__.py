@@ -21,6 +21,7 @@ from . import _build
 __all__ = [
     "GemmError", "load_library", "library_path", "gemm_sgemm", "gemm_bf16gemm",
     "gemm_bf16gemm_decode_static", "gemm_bf16gemm_epilogue", "bf16gemm_epilogue", "ACT", "OUT",
+    "gemm_bf16gemm_fused", "bf16gemm_fused", "GemmOutput",
     "gemm_status_string", "gemm_check_device_error", "gemm_shutdown",
     "gemm_select_path", "gemm_split_parts", "gemm_quantization", "gemm_version", "sgemm", "bf16gemm",
     "STATUS", "PATHS",
@@ -43,6 +44,17 @@ class GemmError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = int(status)
         super().__init__("%s: %s" % (where, gemm_status_string(status)))
+
+
+class GemmOutput(ctypes.Structure):
+    """Mirror of gemm_output_t (include/gemm12.h)."""
+    _fields_ = [
+        ("beta", ctypes.c_float), ("C", ctypes.c_void_p), ("ldc", ctypes.c_int64),
+        ("bias", ctypes.c_void_p), ("act", ctypes.c_int),
+        ("residual", ctypes.c_void_p), ("ldr", ctypes.c_int64),
+        ("d_scale", ctypes.c_float), ("amax", ctypes.c_void_p),
+        ("D", ctypes.c_void_p), ("ldd", ctypes.c_int64), ("d_type", ctypes.c_int),
+    ]
 
 
 class _Quantization(ctypes.Structure):
@@ -87,6 +99,9 @@ def load_library(build_if_missing: bool = False):
         lib.gemm_bf16gemm_epilogue.argtypes = [i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64,
                                                vp, cint, vp, i64, cint, vp]
         lib.gemm_bf16gemm_epilogue.restype = cint
+        lib.gemm_bf16gemm_fused.argtypes = [i64, i64, i64, f32, vp, i64, vp, i64,
+                                            ctypes.POINTER(GemmOutput), vp]
+        lib.gemm_bf16gemm_fused.restype = cint
         lib.gemm_status_string.argtypes = [cint]
         lib.gemm_status_string.restype = ctypes.c_char_p
         lib.gemm_check_device_error.argtypes = [vp]
@@ -125,7 +140,7 @@ def gemm_bf16gemm_decode_static(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, st
 
 
 ACT = {"none": 0, "relu": 1, "gelu": 2}
-OUT = {"f32": 0, "bf16": 1}
+OUT = {"f32": 0, "bf16": 1, "f8e4m3": 2, "s8": 3}
 
 
 def gemm_bf16gemm_epilogue(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, bias, act, D, ldd,
@@ -134,6 +149,12 @@ def gemm_bf16gemm_epilogue(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, bias, a
     act and d_type are the C enum values (ACT / OUT). Returns the status."""
     return load_library().gemm_bf16gemm_epilogue(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
                                                  bias, act, D, ldd, d_type, stream)
+
+
+def gemm_bf16gemm_fused(M, N, K, alpha, A, lda, B, ldb, out: "GemmOutput", stream=0) -> int:
+    """bf16 GEMM with the general output stage (gemm_output_t). Returns the status."""
+    return load_library().gemm_bf16gemm_fused(M, N, K, alpha, A, lda, B, ldb, ctypes.byref(out),
+                                              stream)
 
 
 def gemm_status_string(status: int) -> str:
@@ -257,4 +278,58 @@ def bf16gemm_epilogue(A, B, D, C=None, alpha=1.0, beta=0.0, bias=None, act="none
                                 _stream_handle(stream, D.device))
     if st != 0:
         raise GemmError(st, "gemm_bf16gemm_epilogue")
+    return D
+
+
+def _out_type(torch, D):
+    kinds = {torch.float32: "f32", torch.bfloat16: "bf16", torch.int8: "s8"}
+    if hasattr(torch, "float8_e4m3fn"):
+        kinds[torch.float8_e4m3fn] = "f8e4m3"
+    if D.dtype not in kinds or not D.is_cuda:
+        raise TypeError("D must be a float32, bfloat16, float8_e4m3fn or int8 CUDA tensor")
+    return OUT[kinds[D.dtype]]
+
+
+def bf16gemm_fused(A, B, D, C=None, alpha=1.0, beta=0.0, bias=None, act="none", residual=None,
+                   d_scale=1.0, amax=None, stream=None):
+    """v = act(alpha*(A @ B) + beta*C + bias) + residual; D <- convert(d_scale * v) in D's
+    dtype (float32, bfloat16, float8_e4m3fn or int8); amax (a float32 CUDA tensor of one
+    element, or None) is raised to max |v|.  A, B bf16; C, bias, residual fp32."""
+    import torch
+    for t, n in ((A, "A"), (B, "B")):
+        if t.dtype != torch.bfloat16 or not t.is_cuda:
+            raise TypeError("%s must be a bfloat16 CUDA tensor" % n)
+    M, K = A.shape
+    N = B.shape[1]
+    if B.shape[0] != K or tuple(D.shape) != (M, N):
+        raise ValueError("shape mismatch")
+    o = GemmOutput()
+    o.beta = float(beta)
+    o.C, o.ldc = 0, max(N, 1)
+    if C is not None:
+        if C.dtype != torch.float32 or tuple(C.shape) != (M, N):
+            raise TypeError("C must be a float32 (M, N) tensor")
+        o.C, o.ldc = C.data_ptr(), _row_major_ld(C, "C")
+    o.bias = 0
+    if bias is not None:
+        if bias.dtype != torch.float32 or bias.numel() != N or not bias.is_contiguous():
+            raise TypeError("bias must be a contiguous float32 tensor of N values")
+        o.bias = bias.data_ptr()
+    o.act = ACT[act]
+    o.residual, o.ldr = 0, max(N, 1)
+    if residual is not None:
+        if residual.dtype != torch.float32 or tuple(residual.shape) != (M, N):
+            raise TypeError("residual must be a float32 (M, N) tensor")
+        o.residual, o.ldr = residual.data_ptr(), _row_major_ld(residual, "residual")
+    o.d_scale = float(d_scale)
+    o.amax = 0
+    if amax is not None:
+        if amax.dtype != torch.float32 or amax.numel() != 1 or not amax.is_cuda:
+            raise TypeError("amax must be a float32 CUDA tensor of one element")
+        o.amax = amax.data_ptr()
+    o.D, o.ldd, o.d_type = D.data_ptr(), _row_major_ld(D, "D"), _out_type(torch, D)
+    st = gemm_bf16gemm_fused(M, N, K, float(alpha), A.data_ptr(), _row_major_ld(A, "A"),
+                             B.data_ptr(), _row_major_ld(B, "B"), o, _stream_handle(stream, D.device))
+    if st != 0:
+        raise GemmError(st, "gemm_bf16gemm_fused")
     return D

@@ -281,8 +281,12 @@ Epilogue plain_epilogue(float alpha, float beta, float* C, int64_t ldc) {
   e.D = C;
   e.ldd = ldc;
   e.bias = nullptr;
+  e.R = nullptr;
+  e.ldr = 0;
+  e.d_scale = 1.0f;
+  e.amax = nullptr;
   e.act = kActNone;
-  e.d_bf16 = 0;
+  e.d_type = kOutF32;
   const int v = (reinterpret_cast<uintptr_t>(C) & 15u) == 0 && ldc % 4 == 0 ? 1 : 0;
   e.c_vec4 = v;
   e.d_vec = v;
@@ -292,18 +296,24 @@ Epilogue plain_epilogue(float alpha, float beta, float* C, int64_t ldc) {
 namespace {
 // D <- act(beta * C + bias): the fused output stage when the product is empty
 // (K == 0 or alpha == 0).
+// The output stage of an empty product (K == 0 or alpha == 0): the
+// accumulator is 0, so v = act(beta * C + bias) + R.
 __global__ void epilogue_only_kernel(int M, int N, Epilogue e) {
   const int64_t total = static_cast<int64_t>(M) * N;
+  float amax_acc = 0.0f;
   for (int64_t x = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; x < total;
        x += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t i = x / N;
     const int j = static_cast<int>(x - i * N);
-    const float c_old = (e.beta != 0.0f) ? e.C[i * e.ldc + j] : 0.0f;
-    float v = e.beta * c_old;
-    if (e.beta == 0.0f) v = 0.0f;
-    v += epi_bias(e, j);
-    epi_store1(e, i, j, epi_activate(e.act, v));
+    // alpha never enters: alpha * 0 would be NaN for an infinite alpha
+    float v = (e.beta != 0.0f) ? e.beta * e.C[i * e.ldc + j] : 0.0f;
+    if (e.bias != nullptr) v += e.bias[j];
+    v = epi_activate(e.act, v);
+    if (e.R != nullptr) v += epi_residual(e, i, j);
+    epi_track(e, amax_acc, v);
+    epi_store1(e, i, j, v);
   }
+  epi_flush_amax(e, amax_acc);
 }
 }  // namespace
 
@@ -566,27 +576,36 @@ gemm_status_t gemm_bf16gemm(int64_t M, int64_t N, int64_t K, float alpha, const 
                               plain_epilogue(alpha, beta, C, ldc), cs);
 }
 
-gemm_status_t gemm_bf16gemm_epilogue(int64_t M, int64_t N, int64_t K, float alpha,
-                                     const void* A, int64_t lda, const void* B, int64_t ldb,
-                                     float beta, const float* C, int64_t ldc, const float* bias,
-                                     int act, void* D, int64_t ldd, int d_type, void* stream) {
-  if (act != GEMM_ACT_NONE && act != GEMM_ACT_RELU && act != GEMM_ACT_GELU)
+gemm_status_t gemm_bf16gemm_fused(int64_t M, int64_t N, int64_t K, float alpha, const void* A,
+                                  int64_t lda, const void* B, int64_t ldb,
+                                  const gemm_output_t* out, void* stream) {
+  if (out == nullptr) return GEMM_ERR_INVALID_VALUE;
+  const gemm_output_t& o = *out;
+  if (o.act != GEMM_ACT_NONE && o.act != GEMM_ACT_RELU && o.act != GEMM_ACT_GELU)
     return GEMM_ERR_INVALID_VALUE;
-  if (d_type != GEMM_OUT_F32 && d_type != GEMM_OUT_BF16) return GEMM_ERR_INVALID_VALUE;
-  gemm_status_t s = check_common(M, N, K, lda, ldb, beta != 0.0f ? ldc : (N > 1 ? N : 1));
+  if (o.d_type != GEMM_OUT_F32 && o.d_type != GEMM_OUT_BF16 && o.d_type != GEMM_OUT_F8E4M3 &&
+      o.d_type != GEMM_OUT_S8)
+    return GEMM_ERR_INVALID_VALUE;
+  const int64_t min_ld = N > 1 ? N : 1;
+  gemm_status_t s = check_common(M, N, K, lda, ldb, o.beta != 0.0f ? o.ldc : min_ld);
   if (s != GEMM_OK) return s;
-  if (ldd < (N > 1 ? N : 1) || ldd > kMaxDim) return GEMM_ERR_INVALID_VALUE;
+  if (o.ldd < min_ld || o.ldd > kMaxDim) return GEMM_ERR_INVALID_VALUE;
+  if (o.residual != nullptr && (o.ldr < min_ld || o.ldr > kMaxDim)) return GEMM_ERR_INVALID_VALUE;
   const gemm_path_t path = select_path(true, M, N, K, alpha, A, lda, B, ldb);
   if (path == GEMM_PATH_NONE) return GEMM_OK;
-  const uintptr_t d_align = d_type == GEMM_OUT_BF16 ? 1u : 3u;
-  if (D == nullptr || (reinterpret_cast<uintptr_t>(D) & d_align)) return GEMM_ERR_INVALID_VALUE;
-  if (beta != 0.0f && (C == nullptr || (reinterpret_cast<uintptr_t>(C) & 3u)))
+  const int d_bytes = o.d_type == GEMM_OUT_F32 ? 4 : (o.d_type == GEMM_OUT_BF16 ? 2 : 1);
+  auto misaligned = [](const void* p, uintptr_t mask) {
+    return (reinterpret_cast<uintptr_t>(p) & mask) != 0;
+  };
+  if (o.D == nullptr || misaligned(o.D, static_cast<uintptr_t>(d_bytes - 1)))
     return GEMM_ERR_INVALID_VALUE;
-  if (bias != nullptr && (reinterpret_cast<uintptr_t>(bias) & 3u)) return GEMM_ERR_INVALID_VALUE;
+  if (o.beta != 0.0f && (o.C == nullptr || misaligned(o.C, 3u))) return GEMM_ERR_INVALID_VALUE;
+  if (o.bias != nullptr && misaligned(o.bias, 3u)) return GEMM_ERR_INVALID_VALUE;
+  if (o.residual != nullptr && misaligned(o.residual, 3u)) return GEMM_ERR_INVALID_VALUE;
+  if (o.amax != nullptr && misaligned(o.amax, 3u)) return GEMM_ERR_INVALID_VALUE;
   if (path != GEMM_PATH_SCALE_C) {
     if (A == nullptr || B == nullptr) return GEMM_ERR_INVALID_VALUE;
-    if ((reinterpret_cast<uintptr_t>(A) & 1u) || (reinterpret_cast<uintptr_t>(B) & 1u))
-      return GEMM_ERR_MISALIGNED;
+    if (misaligned(A, 1u) || misaligned(B, 1u)) return GEMM_ERR_MISALIGNED;
     if (path == GEMM_PATH_SIMT_BF16) return GEMM_ERR_UNSUPPORTED;
   }
   DeviceState* st = device_state(&s);
@@ -594,19 +613,46 @@ gemm_status_t gemm_bf16gemm_epilogue(int64_t M, int64_t N, int64_t K, float alph
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   Epilogue epi{};
   epi.alpha = alpha;
-  epi.beta = beta;
-  epi.C = C;
-  epi.ldc = ldc;
-  epi.D = D;
-  epi.ldd = ldd;
-  epi.bias = bias;
-  epi.act = act;
-  epi.d_bf16 = d_type == GEMM_OUT_BF16 ? 1 : 0;
-  epi.c_vec4 = (beta != 0.0f) ? c_vec4_ok(C, ldc) : 0;
-  epi.d_vec = aligned16(D) && (ldd % (epi.d_bf16 ? 8 : 4) == 0) ? 1 : 0;
+  epi.beta = o.beta;
+  epi.C = o.C;
+  epi.ldc = o.ldc;
+  epi.D = o.D;
+  epi.ldd = o.ldd;
+  epi.bias = o.bias;
+  epi.R = o.residual;
+  epi.ldr = o.ldr;
+  epi.d_scale = o.d_scale;
+  epi.amax = o.amax;
+  epi.act = o.act;
+  epi.d_type = o.d_type;  // gemm_out_t and the kernels' kOut* agree
+  epi.c_vec4 = (o.beta != 0.0f) ? c_vec4_ok(o.C, o.ldc) : 0;
+  // 8-element stores: 16 bytes for fp32 (two float4) and bf16, 8 for bytes
+  const uintptr_t vec_mask = d_bytes == 1 ? 7u : 15u;
+  epi.d_vec = !misaligned(o.D, vec_mask) && (o.ldd % (d_bytes == 4 ? 4 : 8) == 0) ? 1 : 0;
   if (path == GEMM_PATH_SCALE_C)
     return from_cuda(launch_epilogue_only(static_cast<int>(M), static_cast<int>(N), epi, cs));
   return run_bf16_tensor_core(st, path, M, N, K, A, lda, B, ldb, epi, cs);
+}
+
+gemm_status_t gemm_bf16gemm_epilogue(int64_t M, int64_t N, int64_t K, float alpha,
+                                     const void* A, int64_t lda, const void* B, int64_t ldb,
+                                     float beta, const float* C, int64_t ldc, const float* bias,
+                                     int act, void* D, int64_t ldd, int d_type, void* stream) {
+  if (d_type != GEMM_OUT_F32 && d_type != GEMM_OUT_BF16) return GEMM_ERR_INVALID_VALUE;
+  gemm_output_t o{};
+  o.beta = beta;
+  o.C = C;
+  o.ldc = ldc;
+  o.bias = bias;
+  o.act = act;
+  o.residual = nullptr;
+  o.ldr = 0;
+  o.d_scale = 1.0f;
+  o.amax = nullptr;
+  o.D = D;
+  o.ldd = ldd;
+  o.d_type = d_type;
+  return gemm_bf16gemm_fused(M, N, K, alpha, A, lda, B, ldb, &o, stream);
 }
 
 gemm_status_t gemm_check_device_error(void* stream) {

@@ -157,12 +157,23 @@ __device__ __forceinline__ void load_c_column(const DecodeArgs& p, int n, float 
     old[m] = (e.beta != 0.0f && n < p.N && m < p.M) ? c[static_cast<int64_t>(m) * e.ldc] : 0.0f;
 }
 
-// D[m][n] = act(alpha * v[m] + beta * old[m] + bias[n]) for the column n of
-// this thread.  FUSED = false is the plain GEMM output (fp32, no bias, no
-// activation), compiled without the general stage.
+// Residual values of column n (rows < M), loaded ahead like old C values.
+__device__ __forceinline__ void load_r_column(const DecodeArgs& p, int n, float (&res)[BMr]) {
+  const Epilogue& e = p.epi;
+#pragma unroll
+  for (int m = 0; m < BMr; ++m)
+    res[m] = (e.R != nullptr && n < p.N && m < p.M) ? e.R[static_cast<int64_t>(m) * e.ldr + n]
+                                                     : 0.0f;
+}
+
+// Column n of this thread through the output stage (see epilogue.cuh).
+// FUSED = false is the plain GEMM output (fp32 D = C, no bias, no
+// activation, no residual, d_scale 1, no amax), compiled without the general
+// stage.
 template <bool FUSED>
 __device__ __forceinline__ void store_c_column(const DecodeArgs& p, int n, const float (&v)[BMr],
-                                               const float (&old)[BMr]) {
+                                               const float (&old)[BMr], const float (&res)[BMr],
+                                               float& amax_acc) {
   if (n >= p.N) return;
   const Epilogue& e = p.epi;
   if (!FUSED) {
@@ -178,7 +189,11 @@ __device__ __forceinline__ void store_c_column(const DecodeArgs& p, int n, const
   const float bias = epi_bias(e, n);  // one column: one bias value, loaded before any store
 #pragma unroll
   for (int m = 0; m < BMr; ++m)
-    if (m < p.M) epi_store1(e, m, n, epi_value(e, v[m], old[m], bias));
+    if (m < p.M) {
+      const float val = epi_value(e, v[m], old[m], bias, res[m]);
+      epi_track(e, amax_acc, val);
+      epi_store1(e, m, n, val);
+    }
 }
 
 template <bool FUSED>
@@ -339,6 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_local = quarter * kRowsPerQuarter + lane;
     const bool row_valid = lane < kRowsPerQuarter && n_local < BN;
     const int ept = threadIdx.x - 64;         // 0..127
+    float amax_acc = 0.0f;
     uint32_t seg = 0;
     int64_t u = u_begin;
     while (u < u_end) {
@@ -355,10 +371,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // contributor of the n-group has already published its partial sums --
       // if so, preload them, so that once this segment's accumulator is ready
       // the group's result is a few adds away.
-      float old[NSUB][BMr];
+      float old[NSUB][BMr], res[NSUB][BMr];
 #pragma unroll
-      for (int j = 0; j < NSUB; ++j)
+      for (int j = 0; j < NSUB; ++j) {
         load_c_column(p, row_valid ? ng * NW + j * BN + n_local : p.N, old[j]);
+        if (FUSED) load_r_column(p, row_valid ? ng * NW + j * BN + n_local : p.N, res[j]);
+      }
       constexpr int kPre = 2;  // partial sums of other CTAs held in registers
       float pre[kPre][NSUB][BMr];
       bool preloaded = false;
@@ -447,7 +465,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           float v[BMr];
 #pragma unroll
           for (int m = 0; m < BMr; ++m) v[m] = __uint_as_float(r[j][m]);
-          store_c_column<FUSED>(p, row_valid ? ng * NW + j * BN + n_local : p.N, v, old[j]);
+          store_c_column<FUSED>(p, row_valid ? ng * NW + j * BN + n_local : p.N, v, old[j], res[j],
+                                amax_acc);
         }
       } else {
         // last_flag: 2 = every other contributor had already arrived (this
@@ -518,7 +537,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                   sum[m] += row_valid ? __ldcg(src + m * NW + j * BN + n_local) : 0.0f;
               }
             }
-            store_c_column<FUSED>(p, row_valid ? ng * NW + j * BN + n_local : p.N, sum, old[j]);
+            store_c_column<FUSED>(p, row_valid ? ng * NW + j * BN + n_local : p.N, sum, old[j],
+                                  res[j], amax_acc);
           }
           if (ept == 0) p.counters[ng] = 0u;
         }
@@ -528,6 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       u = seg_end_u;
       ++seg;
     }
+    if (FUSED) epi_flush_amax(p.epi, amax_acc);
   }
 
   tc_fence_before_sync();
@@ -561,7 +582,10 @@ int64_t decode_counter_count(int N) { return (N + NW - 1) / NW; }
 
 cudaError_t launch_tc_decode(const DecodeArgs& a, const CUtensorMap* tmA, const CUtensorMap* tmB,
                              int num_ctas, cudaStream_t stream) {
-  const bool fused = a.epi.bias != nullptr || a.epi.act != kActNone || a.epi.d_bf16;
+  const Epilogue& ep = a.epi;
+  const bool fused = ep.bias != nullptr || ep.act != kActNone || ep.R != nullptr ||
+                     ep.d_type != kOutF32 || ep.d_scale != 1.0f || ep.amax != nullptr ||
+                     ep.D != static_cast<const void*>(ep.C) || ep.ldd != ep.ldc;
   auto kernel = fused ? tc_decode_kernel<true> : tc_decode_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));

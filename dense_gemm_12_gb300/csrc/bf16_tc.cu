@@ -125,12 +125,13 @@ __device__ __forceinline__ Unit unit_of(const TcArgs& p, int u, int num_kb) {
   return w;
 }
 
-// One 32-column chunk of an accumulator row: D = act(alpha*acc + beta*C + bias).
-// Old C values are all loaded before the first store, so the loads overlap
-// (interleaved load/store pairs to possibly aliasing addresses would cost a
-// memory round trip each).
+// One 32-column chunk of an accumulator row through the output stage (see
+// epilogue.cuh).  Old C, bias and residual values are all loaded before the
+// first store, so the loads overlap (interleaved load/store pairs to possibly
+// aliasing addresses would cost a memory round trip each).  amax_acc: this
+// thread's running max |v|.
 __device__ __forceinline__ void store_row_chunk(const TcArgs& p, int row, int col0,
-                                                const uint32_t (&r)[32]) {
+                                                const uint32_t (&r)[32], float& amax_acc) {
   const Epilogue& e = p.epi;
   const bool read_c = (e.beta != 0.0f);
   const float* c_row = e.C + static_cast<int64_t>(row) * e.ldc;
@@ -151,16 +152,21 @@ __device__ __forceinline__ void store_row_chunk(const TcArgs& p, int row, int co
         for (int c = 0; c < 32; ++c) old[c] = c_row[col0 + c];
       }
     }
-    float bias[32];
+    float bias[32], res[32];
 #pragma unroll
-    for (int c = 0; c < 32; ++c) bias[c] = epi_bias(e, col0 + c);
+    for (int c = 0; c < 32; ++c) {
+      bias[c] = epi_bias(e, col0 + c);
+      res[c] = epi_residual(e, row, col0 + c);
+    }
 #pragma unroll
     for (int h = 0; h < 4; ++h) {
       float v[8];
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
+      for (int c = 0; c < 8; ++c) {
         v[c] = epi_value(e, __uint_as_float(r[8 * h + c]), read_c ? old[8 * h + c] : 0.0f,
-                         bias[8 * h + c]);
+                         bias[8 * h + c], res[8 * h + c]);
+        epi_track(e, amax_acc, v[c]);
+      }
       if (e.d_vec) {
         epi_store8(e, row, col0 + 8 * h, v);
       } else {
@@ -170,16 +176,22 @@ __device__ __forceinline__ void store_row_chunk(const TcArgs& p, int row, int co
     }
   } else {
     // ragged right edge
-    float old[32], bias[32];
+    float old[32], bias[32], res[32];
 #pragma unroll
     for (int c = 0; c < 32; ++c) {
-      old[c] = (read_c && col0 + c < p.N) ? c_row[col0 + c] : 0.0f;
-      bias[c] = (col0 + c < p.N) ? epi_bias(e, col0 + c) : 0.0f;
+      const bool in = col0 + c < p.N;
+      old[c] = (read_c && in) ? c_row[col0 + c] : 0.0f;
+      bias[c] = in ? epi_bias(e, col0 + c) : 0.0f;
+      res[c] = in ? epi_residual(e, row, col0 + c) : 0.0f;
     }
 #pragma unroll
     for (int c = 0; c < 32; ++c) {
       const int col = col0 + c;
-      if (col < p.N) epi_store1(e, row, col, epi_value(e, __uint_as_float(r[c]), old[c], bias[c]));
+      if (col < p.N) {
+        const float v = epi_value(e, __uint_as_float(r[c]), old[c], bias[c], res[c]);
+        epi_track(e, amax_acc, v);
+        epi_store1(e, row, col, v);
+      }
     }
   }
 }
@@ -198,14 +210,15 @@ __device__ __forceinline__ void epi_bar() {
 // own accumulator and adds all parts in part order -- a fixed order, so the
 // result does not depend on which part finishes last -- and writes D.
 __device__ __forceinline__ void epilogue_unit(const TcArgs& p, uint32_t taddr, int row, int tn,
-                                              int slot, int part, int et, int* last_flag) {
+                                              int slot, int part, int et, int* last_flag,
+                                              float& amax_acc) {
   if (slot < 0) {
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
       uint32_t r[32];
       tmem_ld_32x32b_x32(taddr + c * 32, r);
       tc_wait_ld();
-      if (row < p.M) store_row_chunk(p, row, tn * BN + c * 32, r);
+      if (row < p.M) store_row_chunk(p, row, tn * BN + c * 32, r, amax_acc);
     }
     return;
   }
@@ -260,7 +273,7 @@ __device__ __forceinline__ void epilogue_unit(const TcArgs& p, uint32_t taddr, i
       }
 #pragma unroll
       for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(sum[i]);
-      if (row < p.M) store_row_chunk(p, row, tn * BN + c * 32, r);
+      if (row < p.M) store_row_chunk(p, row, tn * BN + c * 32, r, amax_acc);
     }
     if (et == 0) p.counters[slot] = 0u;
   }
@@ -391,6 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // -------------------------------------------------------- epilogue
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     const int et = quarter * 32 + lane;
+    float amax_acc = 0.0f;
     uint32_t j = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++j) {
       const Unit w = unit_of(p, u, num_kb);
@@ -403,10 +417,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after_sync();
       const int row = tm * BM + et;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + ab * BN;
-      epilogue_unit(p, taddr, row, tn, w.tail, w.part, et, &tail->last_flag);
+      epilogue_unit(p, taddr, row, tn, w.tail, w.part, et, &tail->last_flag, amax_acc);
       tc_fence_before_sync();
       mbar_arrive(&tail->tmem_empty[ab]);
     }
+    epi_flush_amax(p.epi, amax_acc);
   }
 
   tc_fence_before_sync();
@@ -599,6 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // -------------------------------------------------------- epilogue
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     const int et = quarter * 32 + lane;
+    float amax_acc = 0.0f;
     const uint32_t tmem_empty0 = mapa_shared(smem_u32(&tail->tmem_empty[0]), 0);
     uint32_t j = 0;
     for (int u = first_item; u < units; u += item_stride, ++j) {
@@ -614,11 +630,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + ab * BN;
       // each CTA of the pair owns the counter and partials of its 128 rows
       const int slot = w.tail < 0 ? -1 : w.tail * 2 + static_cast<int>(rank);
-      epilogue_unit(p, taddr, row, tn, slot, w.part, et, &tail->last_flag);
+      epilogue_unit(p, taddr, row, tn, slot, w.part, et, &tail->last_flag, amax_acc);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(tmem_empty0 + ab * static_cast<uint32_t>(sizeof(uint64_t)));
     }
+    epi_flush_amax(p.epi, amax_acc);
   }
 
   tc_fence_before_sync();

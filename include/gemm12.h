@@ -116,7 +116,7 @@ gemm_status_t gemm_bf16gemm(int64_t M, int64_t N, int64_t K, float alpha,
                             const void *B, int64_t ldb,
                             float beta, float *C, int64_t ldc, void *stream);
 
-/* Activations and output types of gemm_bf16gemm_epilogue. */
+/* Activations and output types of gemm_bf16gemm_fused / _epilogue. */
 typedef enum {
     GEMM_ACT_NONE = 0,   /* identity                                           */
     GEMM_ACT_RELU = 1,   /* max(x, 0)                                          */
@@ -125,11 +125,74 @@ typedef enum {
 
 typedef enum {
     GEMM_OUT_F32 = 0,    /* D holds fp32                                       */
-    GEMM_OUT_BF16 = 1    /* D holds bf16, rounded to nearest even              */
+    GEMM_OUT_BF16 = 1,   /* D holds bf16, rounded to nearest even              */
+    GEMM_OUT_F8E4M3 = 2, /* D holds fp8 E4M3 (1 sign, 4 exponent bits with bias
+                            7, 3 mantissa bits; no infinities; largest finite
+                            value 448; S.1111.111 is NaN), rounded to nearest
+                            even, saturated to +-448; NaN stays NaN          */
+    GEMM_OUT_S8 = 3      /* D holds int8: rounded half to even, saturated to
+                            [-128, 127]; NaN becomes 0                        */
 } gemm_out_t;
 
 /*
- * gemm_bf16gemm_epilogue -- bf16 GEMM with a fused output stage:
+ * Output stage of gemm_bf16gemm_fused.  With P = A x B (fp32 accumulation):
+ *
+ *     v[i][j] = act(alpha * P[i][j] + beta * C[i][j] + bias[j]) + R[i][j]
+ *     D[i][j] = convert_{d_type}(d_scale * v[i][j])
+ *     *amax   = max(*amax, max over i, j of |v[i][j]|)
+ *
+ * "Tiled matrix multiplication" ("Implementation notes", fusing the
+ * epilogue): bias, activation, residual, scaling and fp8/int8 quantisation
+ * are applied while the tile is still in registers.  All matrices row-major;
+ * every pointer is a device pointer owned by the caller.
+ */
+typedef struct {
+    float beta;            /* weight of C; C is not read when beta == 0      */
+    const float *C;        /* M x N fp32 (ldc >= max(1, N)), 4-byte aligned;
+                              may be NULL when beta == 0                     */
+    int64_t ldc;
+    const float *bias;     /* N fp32 values (4-byte aligned) or NULL         */
+    int act;               /* a gemm_act_t                                   */
+    const float *residual; /* R: M x N fp32 (ldr >= max(1, N)), 4-byte
+                              aligned, added after the activation; or NULL   */
+    int64_t ldr;
+    float d_scale;         /* multiplies v before the conversion (1 = none)  */
+    float *amax;           /* one fp32 (4-byte aligned) raised to the largest
+                              |v| over the output (NaN values never raise
+                              it; the caller sets the start value, e.g. 0),
+                              or NULL                                       */
+    void *D;               /* M x N output of type d_type, aligned to its
+                              element size                                   */
+    int64_t ldd;           /* >= max(1, N)                                   */
+    int d_type;            /* a gemm_out_t                                   */
+} gemm_output_t;
+
+/*
+ * gemm_bf16gemm_fused -- bf16 GEMM (A, B, lda, ldb as in gemm_bf16gemm) with
+ * the output stage `out` (see gemm_output_t).  The same tensor-core kernels
+ * as gemm_bf16gemm run (including the decode kernel for M <= 16).
+ * Aliasing: D may be C itself only when d_type is GEMM_OUT_F32 and
+ * ldd == ldc, and may be the residual itself only when d_type is
+ * GEMM_OUT_F32 and ldd == ldr (each output element is read before it is
+ * written, by the thread that writes it); otherwise D must not overlap A, B,
+ * C, bias, residual or amax.  Errors: out == NULL, an unknown act or d_type,
+ * a NULL or misaligned D, C (beta != 0), bias, residual or amax, or a leading
+ * dimension below max(1, N) return GEMM_ERR_INVALID_VALUE; operands the TMA
+ * engine cannot describe (base not 16-byte aligned, pitch not a multiple of
+ * 16 bytes) return GEMM_ERR_UNSUPPORTED.  K == 0 or alpha == 0:
+ * v = act(beta * C + bias) + R (alpha is not used).  Accuracy: v carries the
+ * bf16 GEMM's bound on the pre-activation value times the activation's
+ * largest slope (1 for none and ReLU, 1.13 for GELU); D adds the rounding of
+ * its conversion.
+ */
+gemm_status_t gemm_bf16gemm_fused(int64_t M, int64_t N, int64_t K, float alpha,
+                                  const void *A, int64_t lda,
+                                  const void *B, int64_t ldb,
+                                  const gemm_output_t *out, void *stream);
+
+/*
+ * gemm_bf16gemm_epilogue -- gemm_bf16gemm_fused without residual, scaling or
+ * amax, and with fp32 or bf16 output only:
  *
  *     D[i][j] = act(alpha * (A x B)[i][j] + beta * C[i][j] + bias[j])
  *
@@ -144,7 +207,8 @@ typedef enum {
  * otherwise D must not overlap A, B, C or bias.  The same tensor-core kernels
  * as gemm_bf16gemm run (including the decode kernel for M <= 16); operands
  * the TMA engine cannot describe return GEMM_ERR_UNSUPPORTED, an unknown act
- * or d_type GEMM_ERR_INVALID_VALUE.  K == 0 or alpha == 0: D = act(beta*C +
+ * or a d_type other than GEMM_OUT_F32 and GEMM_OUT_BF16
+ * GEMM_ERR_INVALID_VALUE.  K == 0 or alpha == 0: D = act(beta*C +
  * bias).  Error bound: the bf16 GEMM's bound on the pre-activation value,
  * times the activation's largest slope (1 for none and ReLU, 1.13 for GELU),
  * plus the bf16 rounding of D when d_type is GEMM_OUT_BF16.

@@ -195,18 +195,91 @@ def activation(x, act):
     raise ValueError("unknown activation %r" % (act,))
 
 
-def epilogue(ref64, bias=None, act="none"):
-    """Fused output stage on the fp64 GEMM result:
-    D[i][j] = act(ref64[i][j] + bias[j]) (bias broadcast over rows), fp64.
+def epilogue(ref64, bias=None, act="none", residual=None):
+    """Fused output stage on the fp64 GEMM result, in fp64:
 
-    ref64 is alpha*(A x B) + beta*C from sgemm / bf16gemm (want64=True); the
-    pages' epilogue fusion ("Tiled matrix multiplication", "Implementation
-    notes") adds bias and an activation to that value before it is stored.
+        v[i][j] = act(ref64[i][j] + bias[j]) + residual[i][j]
+
+    (bias broadcast over rows; either may be None).  ref64 is
+    alpha*(A x B) + beta*C from sgemm / bf16gemm (want64=True).  The pages'
+    epilogue fusion ("Tiled matrix multiplication", "Implementation notes")
+    applies bias, activation, residual, scaling and quantisation, in that
+    order, before the tile is stored; scaling and quantisation are
+    ``quantize``.
     """
     v = np.asarray(ref64, dtype=np.float64)
     if bias is not None:
         v = v + np.asarray(bias, dtype=np.float64)[None, :]
-    return activation(v, act)
+    v = activation(v, act)
+    if residual is not None:
+        v = v + np.asarray(residual, dtype=np.float64)
+    return v
+
+
+# ---------------------------------------------------------------- quantise
+# fp8 E4M3 as the OCP 8-bit floating point format defines it ("E4M3"): sign
+# bit, 4 exponent bits with bias 7, 3 mantissa bits; exponent field 0 holds
+# the subnormals m * 2^-9; no infinities; S.1111.111 is NaN, so the largest
+# finite value is S.1111.110 = 1.75 * 2^8 = 448.
+E4M3_MAX = 448.0
+_E4M3_MIN_NORMAL = 2.0 ** -6
+_E4M3_SUBNORMAL_STEP = 2.0 ** -9
+
+
+def e4m3_encode(x):
+    """fp32 values -> E4M3 codes (uint8), rounding to nearest, ties to even,
+    saturating finite overflow (and infinities) to +-448; NaN -> 0x7F."""
+    x = np.asarray(x, dtype=np.float32).astype(np.float64)   # exact
+    sign = np.signbit(x).astype(np.uint8) << 7
+    nan = np.isnan(x)
+    a = np.minimum(np.abs(np.where(nan, 0.0, x)), E4M3_MAX)
+    # spacing of representable values around a: 2^-9 below the smallest
+    # normal, 2^(e - 3) in the binade [2^e, 2^(e+1))
+    _, E = np.frexp(a)                      # a = f 2^E, f in [0.5, 1)
+    e = E.astype(np.int64) - 1
+    step = np.where(a < _E4M3_MIN_NORMAL, _E4M3_SUBNORMAL_STEP, np.ldexp(1.0, e - 3))
+    y = np.rint(a / step) * step            # np.rint: half to even; a/step exact
+    # encode y (0 <= y <= 448, representable)
+    _, Ey = np.frexp(y)
+    ey = Ey.astype(np.int64) - 1
+    normal = y >= _E4M3_MIN_NORMAL
+    exp_field = np.where(normal, ey + 7, 0)
+    mant = np.where(normal, np.ldexp(y, -ey) * 8.0 - 8.0, y / _E4M3_SUBNORMAL_STEP)
+    code = (exp_field.astype(np.uint8) << 3) | mant.astype(np.uint8)
+    code = np.where(nan, np.uint8(0x7F), code | sign)
+    return code.astype(np.uint8)
+
+
+def e4m3_decode(code):
+    """E4M3 codes (uint8) -> their values as fp64 (NaN for S.1111.111)."""
+    c = np.asarray(code, dtype=np.uint8).astype(np.int64)
+    s = np.where(c >> 7, -1.0, 1.0)
+    ef = (c >> 3) & 0xF
+    m = c & 0x7
+    mag = np.where(ef == 0, m * _E4M3_SUBNORMAL_STEP, np.ldexp(1.0 + m / 8.0, ef - 7))
+    return np.where((ef == 0xF) & (m == 0x7), np.nan, s * mag)
+
+
+def s8_encode(x):
+    """fp32 values -> int8: round half to even, saturate to [-128, 127],
+    NaN -> 0."""
+    x = np.asarray(x, dtype=np.float32).astype(np.float64)
+    r = np.clip(np.rint(np.where(np.isnan(x), 0.0, x)), -128.0, 127.0)
+    return r.astype(np.int8)
+
+
+def quantize(v, d_type, d_scale=1.0):
+    """Output conversion of the fused stage, taken in fp32 like the kernel:
+    x = fp32(d_scale) * fp32(v) (one fp32 multiply), then
+    "f32": x;  "f8e4m3": e4m3_encode(x);  "s8": s8_encode(x)."""
+    x = np.asarray(v, dtype=np.float32) * np.float32(d_scale)
+    if d_type == "f32":
+        return x
+    if d_type == "f8e4m3":
+        return e4m3_encode(x)
+    if d_type == "s8":
+        return s8_encode(x)
+    raise ValueError("unknown output type %r" % (d_type,))
 
 
 def error_ratio(C_test, ref, den):

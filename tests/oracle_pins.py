@@ -23,6 +23,7 @@ import itertools
 from fractions import Fraction
 
 import numpy as np
+import pytest
 
 F32 = np.float32
 
@@ -342,6 +343,96 @@ def pin_epilogue_bias_broadcast(orc):
     assert np.array_equal(oracle.epilogue(ref, bias, "relu"), np.maximum(out, 0.0))
 
 
+def pin_epilogue_residual(orc):
+    """The residual is added after the activation, element by element."""
+    import oracle
+    ref = np.array([[-3.0, 2.0], [0.5, -0.25]])
+    res = np.array([[1.0, -1.0], [10.0, 0.75]])
+    out = oracle.epilogue(ref, None, "relu", res)
+    assert np.array_equal(out, np.array([[1.0, 1.0], [10.5, 0.75]]))
+    bias = np.array([4.0, 0.0])
+    assert np.array_equal(oracle.epilogue(ref, bias, "none", res),
+                          np.array([[2.0, 1.0], [14.5, 0.5]]))
+
+
+def pin_e4m3_format_values(orc):
+    """Values of the OCP 8-bit floating point (E4M3) definition: largest
+    finite 448 = 0x7E, smallest normal 2^-6 = 0x08, largest subnormal
+    7 * 2^-9 = 0x07, smallest subnormal 2^-9 = 0x01, 1 = 0x38, -2 = 0xC0,
+    NaN = S.1111.111; saturation of anything larger to 448."""
+    import oracle
+    enc = lambda v: int(oracle.e4m3_encode(np.array([v], dtype=np.float32))[0])
+    assert enc(448.0) == 0x7E and enc(-448.0) == 0xFE
+    assert enc(2.0 ** -6) == 0x08 and enc(7 * 2.0 ** -9) == 0x07 and enc(2.0 ** -9) == 0x01
+    assert enc(1.0) == 0x38 and enc(-2.0) == 0xC0 and enc(0.0) == 0x00
+    assert enc(1e6) == 0x7E and enc(-np.inf) == 0xFE and enc(np.inf) == 0x7E
+    assert enc(np.nan) & 0x7F == 0x7F
+    assert np.isnan(oracle.e4m3_decode(np.array([0x7F, 0xFF], dtype=np.uint8))).all()
+    assert oracle.e4m3_decode(np.array([0x7E], dtype=np.uint8))[0] == 448.0
+
+
+def pin_e4m3_ties_to_even(orc):
+    """Halfway cases go to the even mantissa: 2^-10 -> 0, 3 * 2^-10 -> 2^-8,
+    1 + 1/16 -> 1, 1 + 3/16 -> 1.25, 17 -> 16, 19 -> 20, 464 (halfway to the
+    NaN pattern's slot) -> 448."""
+    import oracle
+    x = np.array([2.0 ** -10, 3 * 2.0 ** -10, 1 + 1 / 16, 1 + 3 / 16, 17.0, 19.0, 464.0],
+                 dtype=np.float32)
+    got = oracle.e4m3_decode(oracle.e4m3_encode(x))
+    assert np.array_equal(got, [0.0, 2.0 ** -8, 1.0, 1.25, 16.0, 20.0, 448.0])
+
+
+def pin_e4m3_matches_torch(orc):
+    """Inside +-448, torch's float8_e4m3fn cast (round to nearest even; an
+    independent implementation) gives the same values on random fp32 inputs
+    spread over every binade, subnormals included."""
+    import oracle
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("torch without float8_e4m3fn")
+    rng = _rng(41)
+    mag = np.ldexp(rng.uniform(1.0, 2.0, 20000), rng.integers(-12, 9, 20000))
+    x = (mag * rng.choice([-1.0, 1.0], 20000)).astype(np.float32)
+    x = x[np.abs(x) <= 448.0]
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).to(torch.float32).numpy()
+    assert np.array_equal(oracle.e4m3_decode(oracle.e4m3_encode(x)), ref.astype(np.float64))
+
+
+def pin_e4m3_roundtrip_and_order(orc):
+    """Every finite code decodes to a value that encodes back to the same
+    code (-0 included), and encoding is monotone in the value."""
+    import oracle
+    codes = np.array([c for c in range(256) if c & 0x7F != 0x7F], dtype=np.uint8)
+    vals = oracle.e4m3_decode(codes).astype(np.float32)
+    assert np.array_equal(oracle.e4m3_encode(vals), codes)
+    x = np.sort(_rng(42).uniform(-500, 500, 5000)).astype(np.float32)
+    dec = oracle.e4m3_decode(oracle.e4m3_encode(x))
+    assert np.all(np.diff(dec) >= 0)
+
+
+def pin_s8_rounding(orc):
+    """int8 output: half to even (as torch.round), saturation, NaN -> 0."""
+    import oracle
+    torch = pytest.importorskip("torch")
+    x = np.array([0.5, 1.5, 2.5, -0.5, -1.5, -2.5, 126.5, 127.49, 127.6, 1e9, -128.4,
+                  -128.6, -1e9, 3.7, -3.7], dtype=np.float32)
+    want = np.clip(torch.round(torch.from_numpy(x)).numpy(), -128, 127).astype(np.int8)
+    assert np.array_equal(oracle.s8_encode(x), want)
+    assert oracle.s8_encode(np.array([np.nan], dtype=np.float32))[0] == 0
+    assert np.array_equal(oracle.s8_encode(np.array([126.5, -0.5], dtype=np.float32)), [126, 0])
+
+
+def pin_quantize_scales_in_fp32(orc):
+    """quantize multiplies by d_scale in fp32 before converting: 0.1 * 3
+    rounds to fp32 first, and a power-of-two scale commutes with the codes."""
+    import oracle
+    v = np.array([3.0], dtype=np.float32)
+    assert oracle.quantize(v, "f32", 0.1)[0] == np.float32(np.float32(0.1) * np.float32(3.0))
+    x = _rng(43).uniform(-100, 100, 1000).astype(np.float32)
+    assert np.array_equal(oracle.e4m3_decode(oracle.quantize(x, "f8e4m3", 0.25)),
+                          oracle.e4m3_decode(oracle.e4m3_encode(x * np.float32(0.25))))
+
+
 ALL_PINS = [
     pin_identity, pin_identity_right, pin_rank1, pin_k1_outer, pin_alpha_zero,
     pin_beta_zero_nan, pin_beta_one_alpha_zero, pin_k_zero, pin_bruteforce_dyadic,
@@ -349,5 +440,7 @@ ALL_PINS = [
     pin_column_permutation, pin_alpha_scaling, pin_leading_dimensions, pin_denominator,
     pin_dims_nonsquare, pin_bf16_definition, pin_bf16_matches_widened_fp32,
     pin_thread_count_invariance, pin_epilogue_relu, pin_epilogue_gelu,
-    pin_epilogue_bias_broadcast,
+    pin_epilogue_bias_broadcast, pin_epilogue_residual, pin_e4m3_format_values,
+    pin_e4m3_ties_to_even, pin_e4m3_matches_torch, pin_e4m3_roundtrip_and_order, pin_s8_rounding,
+    pin_quantize_scales_in_fp32,
 ]
