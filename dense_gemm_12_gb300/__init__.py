@@ -22,6 +22,7 @@ __all__ = [
     "GemmError", "load_library", "library_path", "gemm_sgemm", "gemm_bf16gemm",
     "gemm_bf16gemm_decode_static", "gemm_bf16gemm_epilogue", "bf16gemm_epilogue", "ACT", "OUT",
     "gemm_bf16gemm_fused", "bf16gemm_fused", "GemmOutput",
+    "gemm_sgemm_config", "gemm_bf16gemm_config", "gemm_get_config", "GemmConfig", "KERNELS",
     "gemm_status_string", "gemm_check_device_error", "gemm_shutdown",
     "gemm_select_path", "gemm_split_parts", "gemm_quantization", "gemm_version", "sgemm", "bf16gemm",
     "STATUS", "PATHS",
@@ -55,6 +56,14 @@ class GemmOutput(ctypes.Structure):
         ("d_scale", ctypes.c_float), ("amax", ctypes.c_void_p),
         ("D", ctypes.c_void_p), ("ldd", ctypes.c_int64), ("d_type", ctypes.c_int),
     ]
+
+
+class GemmConfig(ctypes.Structure):
+    """Mirror of gemm_config_t (include/gemm12.h)."""
+    _fields_ = [("kernel", ctypes.c_int), ("split", ctypes.c_int), ("group_m", ctypes.c_int)]
+
+
+KERNELS = {"auto": 0, "single_cta": 1, "cta_pair": 2}
 
 
 class _Quantization(ctypes.Structure):
@@ -102,6 +111,13 @@ def load_library(build_if_missing: bool = False):
         lib.gemm_bf16gemm_fused.argtypes = [i64, i64, i64, f32, vp, i64, vp, i64,
                                             ctypes.POINTER(GemmOutput), vp]
         lib.gemm_bf16gemm_fused.restype = cint
+        cfg_p = ctypes.POINTER(GemmConfig)
+        lib.gemm_sgemm_config.argtypes = gemm_args[:-1] + [cfg_p, vp]
+        lib.gemm_sgemm_config.restype = cint
+        lib.gemm_bf16gemm_config.argtypes = gemm_args[:-1] + [cfg_p, vp]
+        lib.gemm_bf16gemm_config.restype = cint
+        lib.gemm_get_config.argtypes = [cint, i64, i64, i64, cfg_p, ctypes.POINTER(cint)]
+        lib.gemm_get_config.restype = cint
         lib.gemm_status_string.argtypes = [cint]
         lib.gemm_status_string.restype = ctypes.c_char_p
         lib.gemm_check_device_error.argtypes = [vp]
@@ -155,6 +171,43 @@ def gemm_bf16gemm_fused(M, N, K, alpha, A, lda, B, ldb, out: "GemmOutput", strea
     """bf16 GEMM with the general output stage (gemm_output_t). Returns the status."""
     return load_library().gemm_bf16gemm_fused(M, N, K, alpha, A, lda, B, ldb, ctypes.byref(out),
                                               stream)
+
+
+def _config(cfg):
+    if cfg is None:
+        return None
+    if isinstance(cfg, GemmConfig):
+        return ctypes.byref(cfg)
+    kernel = cfg.get("kernel", 0)
+    c = GemmConfig(KERNELS[kernel] if isinstance(kernel, str) else int(kernel),
+                   int(cfg.get("split", 0)), int(cfg.get("group_m", 0)))
+    return ctypes.byref(c)
+
+
+def gemm_sgemm_config(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, cfg, stream=0) -> int:
+    """gemm_sgemm with a pinned launch configuration (GemmConfig or a dict with
+    kernel / split / group_m; None = automatic). Returns the status."""
+    return load_library().gemm_sgemm_config(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                                            _config(cfg), stream)
+
+
+def gemm_bf16gemm_config(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, cfg, stream=0) -> int:
+    """gemm_bf16gemm with a pinned launch configuration. Returns the status."""
+    return load_library().gemm_bf16gemm_config(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                                               _config(cfg), stream)
+
+
+def gemm_get_config(is_bf16, M, N, K):
+    """(config dict, from_table) automatic dispatch uses for a shape on the current
+    device; raises GemmError without a usable device."""
+    c = GemmConfig()
+    t = ctypes.c_int(0)
+    st = load_library().gemm_get_config(int(bool(is_bf16)), M, N, K, ctypes.byref(c),
+                                        ctypes.byref(t))
+    if st != 0:
+        raise GemmError(st, "gemm_get_config")
+    names = {v: k for k, v in KERNELS.items()}
+    return {"kernel": names[c.kernel], "split": c.split, "group_m": c.group_m}, bool(t.value)
 
 
 def gemm_status_string(status: int) -> str:

@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 SOURCES = ["api.cu", "sgemm_simt.cu", "bf16_tc.cu", "bf16_decode.cu", "decode_noalloc.cu"]
-HEADERS = ["ptx.cuh", "internal.h", "epilogue.cuh"]
+HEADERS = ["ptx.cuh", "internal.h", "epilogue.cuh", "dispatch_table.inc"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",

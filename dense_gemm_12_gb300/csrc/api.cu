@@ -209,16 +209,16 @@ gemm_status_t ensure_scratch(DeviceState& st, cudaStream_t stream, int64_t float
 // caller has launched.
 }  // namespace
 
-int tail_split(int items, int num_kb, int workers, double part_cost_kb) {
+int tail_split(int items, int num_kb, int workers, double fixup_kb) {
   if (items <= 0 || workers <= 0 || num_kb <= 0) return 1;
   const int tail = items >= workers ? items % workers : items;
   if (tail == 0) return 1;
   int best_s = 1;
   double best = 1.0;
   for (int s = 2; s <= 8 && s * 4 <= num_kb; ++s) {
-    const double t =
-        static_cast<double>((static_cast<int64_t>(tail) * s + workers - 1) / workers) / s +
-        s * part_cost_kb / num_kb;
+    const double rounds =
+        static_cast<double>((static_cast<int64_t>(tail) * s + workers - 1) / workers);
+    const double t = rounds / s + rounds * s * fixup_kb / num_kb;
     if (t < best - 1e-9) {
       best = t;
       best_s = s;
@@ -227,15 +227,68 @@ int tail_split(int items, int num_kb, int workers, double part_cost_kb) {
   return best_s;
 }
 
+// ------------------------------------------------ launch configuration
+// Entries of the offline sweep's table (dispatch_table.inc).
+struct TunedEntry {
+  int is_bf16, log2_m, log2_n, log2_k;
+  int kernel, split, group_m;
+};
+#include "dispatch_table.inc"
+
 namespace {
 
-gemm_status_t plan_simt(DeviceState* st, cudaStream_t cs, SimtArgs& a,
+int ceil_log2(int64_t x) {
+  int b = 0;
+  while ((int64_t{1} << b) < x) ++b;
+  return b;
+}
+
+bool config_fields_valid(const gemm_config_t* c, bool bf16) {
+  if (c == nullptr) return true;
+  const bool kernel_ok = c->kernel == GEMM_KERNEL_AUTO || c->kernel == GEMM_KERNEL_SINGLE_CTA ||
+                         (bf16 && c->kernel == GEMM_KERNEL_CTA_PAIR);
+  return kernel_ok && c->split >= 0 && c->split <= 8 && c->group_m >= 0 && c->group_m <= 64;
+}
+
+// The tile-kernel configuration of one call: the sweep's table entry for the
+// shape's class (on the GPU it was measured on), then every non-zero field of
+// `user` on top.  Fields left 0 are decided by the planners (cost model).
+TileConfig resolve_config(bool bf16, int64_t M, int64_t N, int64_t K, int num_sms,
+                          const gemm_config_t* user, bool* from_table) {
+  TileConfig c{GEMM_KERNEL_AUTO, 0, 0};
+  bool table = false;
+  if (num_sms == kTunedSms) {
+    const int lm = ceil_log2(M), ln = ceil_log2(N), lk = ceil_log2(K);
+    for (const TunedEntry& e : kTuned) {
+      if (e.is_bf16 < 0) break;
+      if (e.is_bf16 == (bf16 ? 1 : 0) && e.log2_m == lm && e.log2_n == ln && e.log2_k == lk) {
+        c = TileConfig{e.kernel, e.split, e.group_m};
+        table = true;
+        break;
+      }
+    }
+  }
+  if (user != nullptr) {
+    if (user->kernel != GEMM_KERNEL_AUTO) c.kernel = user->kernel;
+    if (user->split != 0) c.split = user->split;
+    if (user->group_m != 0) c.group_m = user->group_m;
+  }
+  if (from_table != nullptr) *from_table = table;
+  return c;
+}
+
+}  // namespace
+
+namespace {
+
+gemm_status_t plan_simt(DeviceState* st, cudaStream_t cs, SimtArgs& a, const TileConfig& tc,
                         std::unique_lock<std::mutex>& lock) {
   const int tiles = ((a.M + kSimtBM - 1) / kSimtBM) * ((a.N + kSimtBN - 1) / kSimtBN);
   const int num_kb = (a.K + kSimtBK - 1) / kSimtBK;
-  const SimtPlan pl = simt_plan(tiles, num_kb, st->num_sms);
+  const SimtPlan pl = simt_plan(tiles, num_kb, st->num_sms, &tc);
   a.full_items = pl.full_items;
   a.split = pl.split;
+  a.group_m = pl.group_m;
   a.ws = nullptr;
   a.counters = nullptr;
   if (pl.split == 1) return GEMM_OK;
@@ -289,6 +342,8 @@ Epilogue plain_epilogue(float alpha, float beta, float* C, int64_t ldc) {
   e.d_type = kOutF32;
   const int v = (reinterpret_cast<uintptr_t>(C) & 15u) == 0 && ldc % 4 == 0 ? 1 : 0;
   e.c_vec4 = v;
+  e.r_vec4 = 0;
+  e.bias_vec4 = 0;
   e.d_vec = v;
   return e;
 }
@@ -386,12 +441,13 @@ int gemm_split_parts(int is_bf16, int64_t M, int64_t N, int64_t K) {
   if (st == nullptr) return 0;
   if (M == 0 || N == 0 || K == 0) return 1;
   const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
+  const TileConfig tc = resolve_config(is_bf16 != 0, M, N, K, st->num_sms, nullptr, nullptr);
   if (is_bf16) {
     if (M <= kDecBM) return 1;
-    return tc_plan(m, n, k, st->num_sms).split;
+    return tc_plan(m, n, k, st->num_sms, &tc).split;
   }
   const int tiles = ((m + kSimtBM - 1) / kSimtBM) * ((n + kSimtBN - 1) / kSimtBN);
-  return simt_plan(tiles, (k + kSimtBK - 1) / kSimtBK, st->num_sms).split;
+  return simt_plan(tiles, (k + kSimtBK - 1) / kSimtBK, st->num_sms, &tc).split;
 }
 
 gemm_status_t gemm_quantization(int64_t M, int64_t N, int64_t BM, int64_t BN, int64_t num_sms,
@@ -419,9 +475,10 @@ gemm_status_t gemm_quantization(int64_t M, int64_t N, int64_t BM, int64_t BN, in
   return GEMM_OK;
 }
 
-gemm_status_t gemm_sgemm(int64_t M, int64_t N, int64_t K, float alpha, const float* A,
-                         int64_t lda, const float* B, int64_t ldb, float beta, float* C,
-                         int64_t ldc, void* stream) {
+static gemm_status_t sgemm_impl(int64_t M, int64_t N, int64_t K, float alpha, const float* A,
+                                int64_t lda, const float* B, int64_t ldb, float beta, float* C,
+                                int64_t ldc, const gemm_config_t* cfg, void* stream) {
+  if (!config_fields_valid(cfg, false)) return GEMM_ERR_INVALID_VALUE;
   gemm_status_t s = check_common(M, N, K, lda, ldb, ldc);
   if (s != GEMM_OK) return s;
   const gemm_path_t path = select_path(false, M, N, K, alpha, A, lda, B, ldb);
@@ -451,8 +508,9 @@ gemm_status_t gemm_sgemm(int64_t M, int64_t N, int64_t K, float alpha, const flo
   a.ldc = ldc;
   a.c_vec4 = c_vec4_ok(C, ldc);
   a.err = st->err_word;
+  const TileConfig tc = resolve_config(false, M, N, K, st->num_sms, cfg, nullptr);
   std::unique_lock<std::mutex> lock(st->ws_mutex, std::defer_lock);
-  s = plan_simt(st, cs, a, lock);
+  s = plan_simt(st, cs, a, tc, lock);
   if (s != GEMM_OK) return s;
   CUtensorMap tmA, tmB;
   LoadMode ma = kLoadCpAsyncF32, mb = kLoadCpAsyncF32;
@@ -468,11 +526,24 @@ gemm_status_t gemm_sgemm(int64_t M, int64_t N, int64_t K, float alpha, const flo
                                mb == kLoadTma ? &tmB : nullptr, st->num_sms, cs));
 }
 
+gemm_status_t gemm_sgemm(int64_t M, int64_t N, int64_t K, float alpha, const float* A,
+                         int64_t lda, const float* B, int64_t ldb, float beta, float* C,
+                         int64_t ldc, void* stream) {
+  return sgemm_impl(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, nullptr, stream);
+}
+
+gemm_status_t gemm_sgemm_config(int64_t M, int64_t N, int64_t K, float alpha, const float* A,
+                                int64_t lda, const float* B, int64_t ldb, float beta, float* C,
+                                int64_t ldc, const gemm_config_t* cfg, void* stream) {
+  return sgemm_impl(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, cfg, stream);
+}
+
 // Runs the tensor-core path (tile kernel or decode kernel) of a bf16 GEMM
 // whose operands TMA can describe, with output stage `epi`.
 static gemm_status_t run_bf16_tensor_core(DeviceState* st, gemm_path_t path, int64_t M, int64_t N,
                                           int64_t K, const void* A, int64_t lda, const void* B,
-                                          int64_t ldb, const Epilogue& epi, cudaStream_t cs) {
+                                          int64_t ldb, const Epilogue& epi, cudaStream_t cs,
+                                          const gemm_config_t* cfg) {
   CUtensorMap tmA, tmB;
   if (path == GEMM_PATH_TC_BF16 || path == GEMM_PATH_TC_BF16_PAIR) {
     // tc_plan picks the CTA-pair kernel exactly when M > kTcBM
@@ -487,9 +558,11 @@ static gemm_status_t run_bf16_tensor_core(DeviceState* st, gemm_path_t path, int
     a.K = static_cast<int>(K);
     a.epi = epi;
     a.err = st->err_word;
-    const TcPlan pl = tc_plan(a.M, a.N, a.K, st->num_sms);
+    const TileConfig tc = resolve_config(true, M, N, K, st->num_sms, cfg, nullptr);
+    const TcPlan pl = tc_plan(a.M, a.N, a.K, st->num_sms, &tc);
     a.full_items = pl.full_items;
     a.split = pl.split;
+    a.group_m = pl.group_m;
     a.ws = nullptr;
     a.counters = nullptr;
     if (pl.split == 1) return from_cuda(launch_tc_bf16(a, pl, &tmA, &tmB, cs));
@@ -532,12 +605,16 @@ static gemm_status_t run_bf16_tensor_core(DeviceState* st, gemm_path_t path, int
   return from_cuda(launch_tc_decode(a, &tmA, &tmB, grid, cs));
 }
 
-gemm_status_t gemm_bf16gemm(int64_t M, int64_t N, int64_t K, float alpha, const void* A,
-                            int64_t lda, const void* B, int64_t ldb, float beta, float* C,
-                            int64_t ldc, void* stream) {
+static gemm_status_t bf16gemm_impl(int64_t M, int64_t N, int64_t K, float alpha, const void* A,
+                                   int64_t lda, const void* B, int64_t ldb, float beta, float* C,
+                                   int64_t ldc, const gemm_config_t* cfg, void* stream) {
+  if (!config_fields_valid(cfg, true)) return GEMM_ERR_INVALID_VALUE;
   gemm_status_t s = check_common(M, N, K, lda, ldb, ldc);
   if (s != GEMM_OK) return s;
-  const gemm_path_t path = select_path(true, M, N, K, alpha, A, lda, B, ldb);
+  gemm_path_t path = select_path(true, M, N, K, alpha, A, lda, B, ldb);
+  // a pinned kernel runs the tile kernels, also for decode shapes
+  if (path == GEMM_PATH_TC_DECODE && cfg != nullptr && cfg->kernel != GEMM_KERNEL_AUTO)
+    path = cfg->kernel == GEMM_KERNEL_CTA_PAIR ? GEMM_PATH_TC_BF16_PAIR : GEMM_PATH_TC_BF16;
   if (path == GEMM_PATH_NONE) return GEMM_OK;
   if (C == nullptr) return GEMM_ERR_INVALID_VALUE;
   if (reinterpret_cast<uintptr_t>(C) & 3u) return GEMM_ERR_INVALID_VALUE;
@@ -566,14 +643,55 @@ gemm_status_t gemm_bf16gemm(int64_t M, int64_t N, int64_t K, float alpha, const 
     a.ldc = ldc;
     a.c_vec4 = c_vec4_ok(C, ldc);
     a.err = st->err_word;
+    // the CUDA-core kernel's table entries are the fp32 ones
+    gemm_config_t simt_cfg{GEMM_KERNEL_AUTO, cfg ? cfg->split : 0, cfg ? cfg->group_m : 0};
+    const TileConfig tc = resolve_config(false, M, N, K, st->num_sms, &simt_cfg, nullptr);
     std::unique_lock<std::mutex> lock(st->ws_mutex, std::defer_lock);
-    s = plan_simt(st, cs, a, lock);
+    s = plan_simt(st, cs, a, tc, lock);
     if (s != GEMM_OK) return s;
     return from_cuda(launch_simt(a, kLoadConvertBf16, kLoadConvertBf16, nullptr, nullptr,
                                  st->num_sms, cs));
   }
   return run_bf16_tensor_core(st, path, M, N, K, A, lda, B, ldb,
-                              plain_epilogue(alpha, beta, C, ldc), cs);
+                              plain_epilogue(alpha, beta, C, ldc), cs, cfg);
+}
+
+gemm_status_t gemm_bf16gemm(int64_t M, int64_t N, int64_t K, float alpha, const void* A,
+                            int64_t lda, const void* B, int64_t ldb, float beta, float* C,
+                            int64_t ldc, void* stream) {
+  return bf16gemm_impl(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, nullptr, stream);
+}
+
+gemm_status_t gemm_bf16gemm_config(int64_t M, int64_t N, int64_t K, float alpha, const void* A,
+                                   int64_t lda, const void* B, int64_t ldb, float beta, float* C,
+                                   int64_t ldc, const gemm_config_t* cfg, void* stream) {
+  return bf16gemm_impl(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, cfg, stream);
+}
+
+gemm_status_t gemm_get_config(int is_bf16, int64_t M, int64_t N, int64_t K, gemm_config_t* out,
+                              int* from_table) {
+  if (out == nullptr || M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+    return GEMM_ERR_INVALID_VALUE;
+  gemm_status_t s;
+  DeviceState* st = device_state(&s);
+  if (st == nullptr) return s;
+  *out = gemm_config_t{GEMM_KERNEL_AUTO, 0, 0};
+  if (from_table != nullptr) *from_table = 0;
+  if (is_bf16 && M <= kDecBM) return GEMM_OK;  // the decode kernel plans itself
+  bool table = false;
+  const TileConfig tc = resolve_config(is_bf16 != 0, M, N, K, st->num_sms, nullptr, &table);
+  const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
+  if (is_bf16) {
+    const TcPlan pl = tc_plan(m, n, k, st->num_sms, &tc);
+    *out = gemm_config_t{pl.pair ? GEMM_KERNEL_CTA_PAIR : GEMM_KERNEL_SINGLE_CTA, pl.split,
+                         pl.group_m};
+  } else {
+    const int tiles = ((m + kSimtBM - 1) / kSimtBM) * ((n + kSimtBN - 1) / kSimtBN);
+    const SimtPlan pl = simt_plan(tiles, (k + kSimtBK - 1) / kSimtBK, st->num_sms, &tc);
+    *out = gemm_config_t{GEMM_KERNEL_SINGLE_CTA, pl.split, pl.group_m};
+  }
+  if (from_table != nullptr) *from_table = table ? 1 : 0;
+  return GEMM_OK;
 }
 
 gemm_status_t gemm_bf16gemm_fused(int64_t M, int64_t N, int64_t K, float alpha, const void* A,
@@ -626,12 +744,14 @@ gemm_status_t gemm_bf16gemm_fused(int64_t M, int64_t N, int64_t K, float alpha, 
   epi.act = o.act;
   epi.d_type = o.d_type;  // gemm_out_t and the kernels' kOut* agree
   epi.c_vec4 = (o.beta != 0.0f) ? c_vec4_ok(o.C, o.ldc) : 0;
+  epi.r_vec4 = (o.residual != nullptr) ? c_vec4_ok(o.residual, o.ldr) : 0;
+  epi.bias_vec4 = (o.bias != nullptr && aligned16(o.bias)) ? 1 : 0;
   // 8-element stores: 16 bytes for fp32 (two float4) and bf16, 8 for bytes
   const uintptr_t vec_mask = d_bytes == 1 ? 7u : 15u;
   epi.d_vec = !misaligned(o.D, vec_mask) && (o.ldd % (d_bytes == 4 ? 4 : 8) == 0) ? 1 : 0;
   if (path == GEMM_PATH_SCALE_C)
     return from_cuda(launch_epilogue_only(static_cast<int>(M), static_cast<int>(N), epi, cs));
-  return run_bf16_tensor_core(st, path, M, N, K, A, lda, B, ldb, epi, cs);
+  return run_bf16_tensor_core(st, path, M, N, K, A, lda, B, ldb, epi, cs, nullptr);
 }
 
 gemm_status_t gemm_bf16gemm_epilogue(int64_t M, int64_t N, int64_t K, float alpha,

@@ -48,14 +48,12 @@ constexpr int BM = kTcBM, BN = kTcBN, BK = kTcBK;
 #ifndef G12_TC_STAGES
 #define G12_TC_STAGES 4
 #endif
-#ifndef G12_TC_GROUP_M
-#define G12_TC_GROUP_M 8
-#endif
-// Cost of storing or loading one split part's partial sums, in k-block times
-// (see tail_split): a 128 KB partial per CTA moves in about 1.1 us at the
-// ~120 GB/s one SM gets from L2, some 3 k-blocks of the tensor core.
-#ifndef G12_TC_PART_COST
-#define G12_TC_PART_COST 3.0
+// Split overhead per part and round, in k-block times of the tensor core
+// (~0.35 us each; see tail_split): storing a 128 KB partial per CTA, and for a
+// tile's last part reading the others and writing the tile, measured at
+// roughly 3 us per part.
+#ifndef G12_TC_FIXUP_KB
+#define G12_TC_FIXUP_KB 8.0
 #endif
 constexpr int STAGES = G12_TC_STAGES;
 constexpr int kStageBytesA = BM * BK * 2;            // 16 KB
@@ -66,7 +64,6 @@ constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
 constexpr int kEpiWarps = kEpiThreads / 32;
 constexpr uint32_t kTmemCols = 512;
-constexpr int kGroupM = G12_TC_GROUP_M;  // raster group height (tile rows or row pairs)
 constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN, /*A MN-major*/ 0, /*B MN-major*/ 1);
 // Named barriers of the epilogue warps (0 is __syncthreads).
 constexpr uint32_t kEpiBarSync = 1, kEpiBarAny = 2;
@@ -84,13 +81,19 @@ struct __align__(8) TcSmemTail {
   int last_flag;
 };
 
-constexpr size_t kSmemBytes = 1024 + STAGES * kStageBytes + sizeof(TcSmemTail);
+// Output staging: 4 KB (32 rows x 32 fp32) per epilogue warp.
+constexpr int kEpiStageBytes = kEpiWarps * 32 * 32 * 4;
+constexpr size_t kSmemBytes = 1024 + STAGES * kStageBytes + kEpiStageBytes + sizeof(TcSmemTail);
+static_assert(kSmemBytes <= 227 * 1024, "single-CTA kernel shared memory");
 
-__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int& tm, int& tn) {
-  const int per_group = kGroupM * tiles_n;
+// Grouped raster: items walk column by column through groups of group_m item
+// rows, so neighbouring CTAs share A row panels and B column panels in L2.
+__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int group_m, int& tm,
+                                            int& tn) {
+  const int per_group = group_m * tiles_n;
   const int g = t / per_group;
-  const int first_m = g * kGroupM;
-  const int rows = min(tiles_m - first_m, kGroupM);
+  const int first_m = g * group_m;
+  const int rows = min(tiles_m - first_m, group_m);
   const int local = t - g * per_group;
   tm = first_m + local % rows;
   tn = local / rows;
@@ -125,75 +128,166 @@ __device__ __forceinline__ Unit unit_of(const TcArgs& p, int u, int num_kb) {
   return w;
 }
 
-// One 32-column chunk of an accumulator row through the output stage (see
-// epilogue.cuh).  Old C, bias and residual values are all loaded before the
-// first store, so the loads overlap (interleaved load/store pairs to possibly
-// aliasing addresses would cost a memory round trip each).  amax_acc: this
-// thread's running max |v|.
-__device__ __forceinline__ void store_row_chunk(const TcArgs& p, int row, int col0,
-                                                const uint32_t (&r)[32], float& amax_acc) {
+// One 32-column chunk of this warp's 32 accumulator rows through the output
+// stage (see epilogue.cuh).  tcgen05.ld hands each thread one row (r), so a
+// direct store would send each warp instruction to 32 rows in 16-byte pieces.
+// The chunk is turned around in the warp's 4 KB of shared memory instead --
+// 16-byte pieces XOR-swizzled by row, so that neither the row-wise writes nor
+// the column-wise reads conflict on banks -- and then 8 lanes cover one row's
+// 128 bytes: C, bias and residual loads and the stores of D move whole
+// lines.  The fused inputs of all 8 passes are loaded before the first store
+// (a load after a store to a possibly aliasing address could not be issued
+// early).  All 32 lanes call this together.  row_base: the warp's first row.
+//
+// FUSED = false is the plain GEMM output (fp32 D = alpha * acc + beta * C, no
+// bias, activation, residual, scaling or amax), compiled without the general
+// stage: the general stage unrolled over a chunk is large enough that its
+// instruction fetches, not its memory traffic, set the pace.
+template <bool FUSED>
+__device__ __forceinline__ void store_chunk(const TcArgs& p, float4* stg, int row_base, int col0,
+                                            const uint32_t (&r)[32], float& amax_acc) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+    stg[lane * 8 + (q ^ (lane & 7))] =
+        make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                    __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+  __syncwarp();
   const Epilogue& e = p.epi;
-  const bool read_c = (e.beta != 0.0f);
-  const float* c_row = e.C + static_cast<int64_t>(row) * e.ldc;
-  if (col0 + 31 < p.N) {
-    float old[32];
-    if (read_c) {
-      if (e.c_vec4) {
+  const int ch = lane & 7;              // this lane's 4 columns: col .. col + 3
+  const int col = col0 + 4 * ch;
+  const bool full = col + 3 < p.N;
+  if (!FUSED) {
+    float cold[8][4];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const float4 o = *reinterpret_cast<const float4*>(c_row + col0 + 4 * q);
-          old[4 * q + 0] = o.x;
-          old[4 * q + 1] = o.y;
-          old[4 * q + 2] = o.z;
-          old[4 * q + 3] = o.w;
+    for (int i = 0; i < 8; ++i) {
+      const int row = row_base + i * 4 + (lane >> 3);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) cold[i][k] = 0.0f;
+      if (row < p.M && e.beta != 0.0f) {
+        const float* c = e.C + static_cast<int64_t>(row) * e.ldc + col;
+        if (full && e.c_vec4) {
+          const float4 o = *reinterpret_cast<const float4*>(c);
+          cold[i][0] = o.x; cold[i][1] = o.y; cold[i][2] = o.z; cold[i][3] = o.w;
+        } else {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) cold[i][k] = col + k < p.N ? c[k] : 0.0f;
         }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int rr = i * 4 + (lane >> 3);
+      const int row = row_base + rr;
+      const float4 a = stg[rr * 8 + (ch ^ (rr & 7))];
+      const float acc[4] = {a.x, a.y, a.z, a.w};
+      float v[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        v[k] = (e.beta != 0.0f) ? fmaf(e.alpha, acc[k], e.beta * cold[i][k]) : e.alpha * acc[k];
+      if (row < p.M) {
+        float* d = static_cast<float*>(e.D) + static_cast<int64_t>(row) * e.ldd + col;
+        if (full && e.d_vec) {
+          *reinterpret_cast<float4*>(d) = make_float4(v[0], v[1], v[2], v[3]);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            if (col + k < p.N) d[k] = v[k];
+        }
+      }
+    }
+    __syncwarp();  // the next chunk rewrites the staging area
+    return;
+  }
+  float bias[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  if (e.bias != nullptr) {
+    if (full && e.bias_vec4) {
+      const float4 b = *reinterpret_cast<const float4*>(e.bias + col);
+      bias[0] = b.x; bias[1] = b.y; bias[2] = b.z; bias[3] = b.w;
+    } else {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) bias[k] = col + k < p.N ? e.bias[col + k] : 0.0f;
+    }
+  }
+  if (e.beta == 0.0f && e.R == nullptr) {
+    // No per-row inputs to load ahead: one row at a time keeps the code of
+    // the general stage (activation, conversions) to one copy.
+#pragma unroll 1
+    for (int i = 0; i < 8; ++i) {
+      const int rr = i * 4 + (lane >> 3);
+      const int row = row_base + rr;
+      const float4 a = stg[rr * 8 + (ch ^ (rr & 7))];
+      const float acc[4] = {a.x, a.y, a.z, a.w};
+      float v[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        v[k] = epi_value(e, acc[k], 0.0f, bias[k], 0.0f);
+        if (row < p.M && col + k < p.N) epi_track(e, amax_acc, v[k]);
+      }
+      if (row < p.M) {
+        if (full && e.d_vec) {
+          epi_store4(e, row, col, v);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            if (col + k < p.N) epi_store1(e, row, col + k, v[k]);
+        }
+      }
+    }
+    __syncwarp();  // the next chunk rewrites the staging area
+    return;
+  }
+  float cold[8][4], res[8][4];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int row = row_base + i * 4 + (lane >> 3);
+    const bool in = row < p.M;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) cold[i][k] = res[i][k] = 0.0f;
+    if (in && e.beta != 0.0f) {
+      const float* c = e.C + static_cast<int64_t>(row) * e.ldc + col;
+      if (full && e.c_vec4) {
+        const float4 o = *reinterpret_cast<const float4*>(c);
+        cold[i][0] = o.x; cold[i][1] = o.y; cold[i][2] = o.z; cold[i][3] = o.w;
       } else {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) old[c] = c_row[col0 + c];
+        for (int k = 0; k < 4; ++k) cold[i][k] = col + k < p.N ? c[k] : 0.0f;
       }
     }
-    float bias[32], res[32];
-#pragma unroll
-    for (int c = 0; c < 32; ++c) {
-      bias[c] = epi_bias(e, col0 + c);
-      res[c] = epi_residual(e, row, col0 + c);
-    }
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      float v[8];
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        v[c] = epi_value(e, __uint_as_float(r[8 * h + c]), read_c ? old[8 * h + c] : 0.0f,
-                         bias[8 * h + c], res[8 * h + c]);
-        epi_track(e, amax_acc, v[c]);
-      }
-      if (e.d_vec) {
-        epi_store8(e, row, col0 + 8 * h, v);
+    if (in && e.R != nullptr) {
+      const float* rr = e.R + static_cast<int64_t>(row) * e.ldr + col;
+      if (full && e.r_vec4) {
+        const float4 o = *reinterpret_cast<const float4*>(rr);
+        res[i][0] = o.x; res[i][1] = o.y; res[i][2] = o.z; res[i][3] = o.w;
       } else {
 #pragma unroll
-        for (int c = 0; c < 8; ++c) epi_store1(e, row, col0 + 8 * h + c, v[c]);
-      }
-    }
-  } else {
-    // ragged right edge
-    float old[32], bias[32], res[32];
-#pragma unroll
-    for (int c = 0; c < 32; ++c) {
-      const bool in = col0 + c < p.N;
-      old[c] = (read_c && in) ? c_row[col0 + c] : 0.0f;
-      bias[c] = in ? epi_bias(e, col0 + c) : 0.0f;
-      res[c] = in ? epi_residual(e, row, col0 + c) : 0.0f;
-    }
-#pragma unroll
-    for (int c = 0; c < 32; ++c) {
-      const int col = col0 + c;
-      if (col < p.N) {
-        const float v = epi_value(e, __uint_as_float(r[c]), old[c], bias[c], res[c]);
-        epi_track(e, amax_acc, v);
-        epi_store1(e, row, col, v);
+        for (int k = 0; k < 4; ++k) res[i][k] = col + k < p.N ? rr[k] : 0.0f;
       }
     }
   }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int rr = i * 4 + (lane >> 3);
+    const int row = row_base + rr;
+    const float4 a = stg[rr * 8 + (ch ^ (rr & 7))];
+    const float acc[4] = {a.x, a.y, a.z, a.w};
+    float v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      v[k] = epi_value(e, acc[k], cold[i][k], bias[k], res[i][k]);
+      if (row < p.M && col + k < p.N) epi_track(e, amax_acc, v[k]);
+    }
+    if (row < p.M) {
+      if (full && e.d_vec) {
+        epi_store4(e, row, col, v);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if (col + k < p.N) epi_store1(e, row, col + k, v[k]);
+      }
+    }
+  }
+  __syncwarp();  // the next chunk rewrites the staging area
 }
 
 __device__ __forceinline__ void epi_bar() {
@@ -209,16 +303,17 @@ __device__ __forceinline__ void epi_bar() {
 // warp), then counts its arrival; the last of the `split` parts re-reads its
 // own accumulator and adds all parts in part order -- a fixed order, so the
 // result does not depend on which part finishes last -- and writes D.
-__device__ __forceinline__ void epilogue_unit(const TcArgs& p, uint32_t taddr, int row, int tn,
-                                              int slot, int part, int et, int* last_flag,
-                                              float& amax_acc) {
+template <bool FUSED>
+__device__ __forceinline__ void epilogue_unit(const TcArgs& p, uint32_t taddr, float4* stg,
+                                              int row_base, int tn, int slot, int part, int et,
+                                              int* last_flag, float& amax_acc) {
   if (slot < 0) {
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
       uint32_t r[32];
       tmem_ld_32x32b_x32(taddr + c * 32, r);
       tc_wait_ld();
-      if (row < p.M) store_row_chunk(p, row, tn * BN + c * 32, r, amax_acc);
+      store_chunk<FUSED>(p, stg, row_base, tn * BN + c * 32, r, amax_acc);
     }
     return;
   }
@@ -240,52 +335,78 @@ __device__ __forceinline__ void epilogue_unit(const TcArgs& p, uint32_t taddr, i
   }
   epi_bar();
   if (et == 0) {
-    __threadfence();  // publish the whole CTA's partial before arriving
-    const uint32_t before = atomicAdd(p.counters + slot, 1u);
+    const uint32_t before = atomic_add_acq_rel_gpu(p.counters + slot, 1u);
     *last_flag = (before == static_cast<uint32_t>(p.split - 1)) ? 1 : 0;
   }
   epi_bar();
   if (*reinterpret_cast<volatile int*>(last_flag)) {
-    __threadfence();
+    // Parts are added in part order; the other parts' partial sums are read
+    // two parts per round trip (the loads of a pair are independent), and
+    // this part's own accumulator comes from TMEM.
+    const float4 zero4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
-      uint32_t r[32];
-      tmem_ld_32x32b_x32(taddr + c * 32, r);
-      tc_wait_ld();
       float sum[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) sum[i] = 0.0f;
-      for (int q_part = 0; q_part < p.split; ++q_part) {
-        if (q_part == part) {
+      uint32_t r[32];
+#pragma unroll 1
+      for (int q0 = 0; q0 < p.split; q0 += 2) {
+        const bool has_b = q0 + 1 < p.split;
+        const bool load_a = q0 != part;
+        const bool load_b = has_b && q0 + 1 != part;
+        const float4* src_a = ws4 + (slot_base + q0) * (kPartFloats / 4) + c * 8 * kEpiThreads + et;
+        const float4* src_b = src_a + kPartFloats / 4;
+        float4 va[8], vb[8];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) sum[i] += __uint_as_float(r[i]);
-        } else {
-          const float4* src = ws4 + (slot_base + q_part) * (kPartFloats / 4);
+        for (int q = 0; q < 8; ++q) {
+          va[q] = load_a ? __ldcg(src_a + q * kEpiThreads) : zero4;
+          vb[q] = load_b ? __ldcg(src_b + q * kEpiThreads) : zero4;
+        }
+        if (!load_a || (has_b && !load_b)) {  // this pair holds the own part
+          tmem_ld_32x32b_x32(taddr + c * 32, r);
+          tc_wait_ld();
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float4 a4 = load_a ? va[q] : make_float4(__uint_as_float(r[4 * q]),
+              __uint_as_float(r[4 * q + 1]), __uint_as_float(r[4 * q + 2]),
+              __uint_as_float(r[4 * q + 3]));
+          sum[4 * q] += a4.x;
+          sum[4 * q + 1] += a4.y;
+          sum[4 * q + 2] += a4.z;
+          sum[4 * q + 3] += a4.w;
+        }
+        if (has_b) {
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
-            const float4 v = __ldcg(src + (c * 8 + q) * kEpiThreads + et);
-            sum[4 * q] += v.x;
-            sum[4 * q + 1] += v.y;
-            sum[4 * q + 2] += v.z;
-            sum[4 * q + 3] += v.w;
+            const float4 b4 = load_b ? vb[q] : make_float4(__uint_as_float(r[4 * q]),
+                __uint_as_float(r[4 * q + 1]), __uint_as_float(r[4 * q + 2]),
+                __uint_as_float(r[4 * q + 3]));
+            sum[4 * q] += b4.x;
+            sum[4 * q + 1] += b4.y;
+            sum[4 * q + 2] += b4.z;
+            sum[4 * q + 3] += b4.w;
           }
         }
       }
 #pragma unroll
       for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(sum[i]);
-      if (row < p.M) store_row_chunk(p, row, tn * BN + c * 32, r, amax_acc);
+      store_chunk<FUSED>(p, stg, row_base, tn * BN + c * 32, r, amax_acc);
     }
     if (et == 0) p.counters[slot] = 0u;
   }
   epi_bar();  // last_flag is rewritten by the next split unit
 }
 
+template <bool FUSED>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bf16_kernel(const __grid_constant__ TcArgs p, const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = align_smem<1024>(smem_raw);
-  TcSmemTail* tail = reinterpret_cast<TcSmemTail*>(smem + STAGES * kStageBytes);
+  uint8_t* epi_stage = smem + STAGES * kStageBytes;
+  TcSmemTail* tail = reinterpret_cast<TcSmemTail*>(epi_stage + kEpiStageBytes);
   volatile int* abort_flag = &tail->abort_flag;
 
   const int warp = threadIdx.x >> 5;
@@ -328,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
         const Unit w = unit_of(p, u, num_kb);
         int tm, tn;
-        tile_coords(w.item, tiles_m, tiles_n, tm, tn);
+        tile_coords(w.item, tiles_m, tiles_n, p.group_m, tm, tn);
         for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t round = it / STAGES;
@@ -404,24 +525,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     // -------------------------------------------------------- epilogue
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     const int et = quarter * 32 + lane;
+    float4* stg = reinterpret_cast<float4*>(epi_stage + quarter * 4096);
     float amax_acc = 0.0f;
     uint32_t j = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++j) {
       const Unit w = unit_of(p, u, num_kb);
       int tm, tn;
-      tile_coords(w.item, tiles_m, tiles_n, tm, tn);
+      tile_coords(w.item, tiles_m, tiles_n, p.group_m, tm, tn);
       const uint32_t ab = j & 1u, ar = j >> 1;
       const bool ok = mbar_wait(&tail->tmem_full[ab], ar & 1u, abort_flag, p.err);
       // Leave together if a wait ran out anywhere (see named_bar_any).
       if (named_bar_any(kEpiBarAny, kEpiThreads, !ok)) break;
       tc_fence_after_sync();
-      const int row = tm * BM + et;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + ab * BN;
-      epilogue_unit(p, taddr, row, tn, w.tail, w.part, et, &tail->last_flag, amax_acc);
+      epilogue_unit<FUSED>(p, taddr, stg, tm * BM + quarter * 32, tn, w.tail, w.part, et,
+                    &tail->last_flag, amax_acc);
       tc_fence_before_sync();
       mbar_arrive(&tail->tmem_empty[ab]);
     }
-    epi_flush_amax(p.epi, amax_acc);
+    if (FUSED) epi_flush_amax(p.epi, amax_acc);
   }
 
   tc_fence_before_sync();
@@ -469,15 +591,18 @@ struct __align__(8) PairSmemTail {
   int last_flag;
 };
 
-constexpr size_t kPairSmemBytes = 1024 + PS * kPairStageBytes + sizeof(PairSmemTail);
+constexpr size_t kPairSmemBytes =
+    1024 + PS * kPairStageBytes + kEpiStageBytes + sizeof(PairSmemTail);
 static_assert(kPairSmemBytes <= 227 * 1024, "pair kernel shared memory");
 
+template <bool FUSED>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bf16_pair_kernel(const __grid_constant__ TcArgs p, const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = align_smem<1024>(smem_raw);
-  PairSmemTail* tail = reinterpret_cast<PairSmemTail*>(smem + PS * kPairStageBytes);
+  uint8_t* epi_stage = smem + PS * kPairStageBytes;
+  PairSmemTail* tail = reinterpret_cast<PairSmemTail*>(epi_stage + kEpiStageBytes);
   volatile int* abort_flag = &tail->abort_flag;
 
   const int warp = threadIdx.x >> 5;
@@ -528,7 +653,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = first_item; u < units && ok; u += item_stride) {
         const Unit w = unit_of(p, u, num_kb);
         int pm, tn;
-        tile_coords(w.item, pairs_m, tiles_n, pm, tn);
+        tile_coords(w.item, pairs_m, tiles_n, p.group_m, pm, tn);
         const int tm = pm * 2 + static_cast<int>(rank);
         for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
           const int s = it % PS;
@@ -614,28 +739,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     // -------------------------------------------------------- epilogue
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     const int et = quarter * 32 + lane;
+    float4* stg = reinterpret_cast<float4*>(epi_stage + quarter * 4096);
     float amax_acc = 0.0f;
     const uint32_t tmem_empty0 = mapa_shared(smem_u32(&tail->tmem_empty[0]), 0);
     uint32_t j = 0;
     for (int u = first_item; u < units; u += item_stride, ++j) {
       const Unit w = unit_of(p, u, num_kb);
       int pm, tn;
-      tile_coords(w.item, pairs_m, tiles_n, pm, tn);
+      tile_coords(w.item, pairs_m, tiles_n, p.group_m, pm, tn);
       const int tm = pm * 2 + static_cast<int>(rank);
       const uint32_t ab = j & 1u, ar = j >> 1;
       const bool ok = mbar_wait(&tail->tmem_full[ab], ar & 1u, abort_flag, p.err);
       if (named_bar_any(kEpiBarAny, kEpiThreads, !ok)) break;
       tc_fence_after_sync();
-      const int row = tm * BM + et;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + ab * BN;
       // each CTA of the pair owns the counter and partials of its 128 rows
       const int slot = w.tail < 0 ? -1 : w.tail * 2 + static_cast<int>(rank);
-      epilogue_unit(p, taddr, row, tn, slot, w.part, et, &tail->last_flag, amax_acc);
+      epilogue_unit<FUSED>(p, taddr, stg, tm * BM + quarter * 32, tn, slot, w.part, et,
+                    &tail->last_flag, amax_acc);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(tmem_empty0 + ab * static_cast<uint32_t>(sizeof(uint64_t)));
     }
-    epi_flush_amax(p.epi, amax_acc);
+    if (FUSED) epi_flush_amax(p.epi, amax_acc);
   }
 
   tc_fence_before_sync();
@@ -661,7 +787,7 @@ static int pair_max_clusters(int num_sms) {
   const int known = cache[dev].load(std::memory_order_relaxed);
   if (known > 0) return known;
   int clusters = 0;
-  auto kernel = tc_bf16_pair_kernel;
+  auto kernel = tc_bf16_pair_kernel<false>;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(kPairSmemBytes)) == cudaSuccess) {
     cudaLaunchConfig_t cfg{};
@@ -683,17 +809,25 @@ static int pair_max_clusters(int num_sms) {
   return clusters;
 }
 
-TcPlan tc_plan(int M, int N, int K, int num_sms) {
+TcPlan tc_plan(int M, int N, int K, int num_sms, const TileConfig* fixed) {
   TcPlan pl{};
   const int tiles_m = (M + BM - 1) / BM;
   const int tiles_n = (N + BN - 1) / BN;
   const int num_kb = (K + BK - 1) / BK;
-  pl.pair = tiles_m >= 2;
+  const bool pinned = fixed != nullptr && fixed->kernel != GEMM_KERNEL_AUTO;
+  pl.pair = pinned ? fixed->kernel == GEMM_KERNEL_CTA_PAIR : tiles_m >= 2;
+  pl.group_m = (fixed != nullptr && fixed->group_m > 0) ? fixed->group_m : 8;
   const int ctas_per_item = pl.pair ? 2 : 1;
   const int items = pl.pair ? ((tiles_m + 1) / 2) * tiles_n : tiles_m * tiles_n;
   const int workers = pl.pair ? pair_max_clusters(num_sms) : num_sms;
-  pl.split = tail_split(items, num_kb, workers, G12_TC_PART_COST);
-  const int tail = pl.split > 1 ? (items >= workers ? items % workers : items) : 0;
+  // a pinned split is capped at one k-block per part
+  pl.split = (fixed != nullptr && fixed->split > 0)
+                 ? (fixed->split < num_kb ? fixed->split : num_kb)
+                 : tail_split(items, num_kb, workers, G12_TC_FIXUP_KB);
+  if (pl.split < 1) pl.split = 1;
+  const int tail_items = items >= workers ? items % workers : items;
+  if (tail_items == 0) pl.split = 1;
+  const int tail = pl.split > 1 ? tail_items : 0;
   pl.full_items = items - tail;
   const int units = pl.full_items + tail * pl.split;
   pl.grid = ctas_per_item * (units < workers ? units : workers);
@@ -705,8 +839,11 @@ TcPlan tc_plan(int M, int N, int K, int num_sms) {
 cudaError_t launch_tc_bf16(const TcArgs& a, const TcPlan& plan, const CUtensorMap* tmA,
                            const CUtensorMap* tmB, cudaStream_t stream) {
   if (plan.grid < 1) return cudaSuccess;
+  const Epilogue& ep = a.epi;
+  const bool fused = ep.bias != nullptr || ep.act != kActNone || ep.R != nullptr ||
+                     ep.d_type != kOutF32 || ep.d_scale != 1.0f || ep.amax != nullptr;
   if (plan.pair) {
-    auto kernel = tc_bf16_pair_kernel;
+    auto kernel = fused ? tc_bf16_pair_kernel<true> : tc_bf16_pair_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kPairSmemBytes));
     if (e != cudaSuccess) return e;
@@ -726,7 +863,7 @@ cudaError_t launch_tc_bf16(const TcArgs& a, const TcPlan& plan, const CUtensorMa
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
   }
-  auto kernel = tc_bf16_kernel;
+  auto kernel = fused ? tc_bf16_kernel<true> : tc_bf16_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;

@@ -34,12 +34,18 @@ struct Epilogue {
   int act;             // kActNone / kActRelu / kActGelu
   int d_type;          // kOutF32 / kOutBf16 / kOutE4M3 / kOutS8
   int c_vec4;          // C rows may be read as aligned float4
-  int d_vec;           // D rows may be written 8 elements at a time (aligned)
+  int r_vec4;          // residual rows may be read as aligned float4
+  int bias_vec4;       // bias may be read as aligned float4
+  int d_vec;           // D rows may be written 8 (and 4) elements at a time (aligned)
 };
+
+__device__ __forceinline__ float epi_gelu(float x) {
+  return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
+}
 
 __device__ __forceinline__ float epi_activate(int act, float x) {
   if (act == kActRelu) return x > 0.0f ? x : 0.0f;
-  if (act == kActGelu) return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
+  if (act == kActGelu) return epi_gelu(x);
   return x;
 }
 
@@ -104,6 +110,28 @@ __device__ __forceinline__ void epi_store1(const Epilogue& e, int64_t row, int c
     static_cast<__nv_bfloat16*>(e.D)[at] = __float2bfloat16_rn(e.d_scale * v);
   else
     static_cast<uint8_t*>(e.D)[at] = epi_to_byte(e, v);
+}
+
+// Store 4 consecutive elements of D starting at a column that is a multiple
+// of 4 (requires d_vec): one 16-, 8- or 4-byte store.
+__device__ __forceinline__ void epi_store4(const Epilogue& e, int64_t row, int col,
+                                           const float (&v)[4]) {
+  const int64_t at = row * e.ldd + col;
+  const float s = e.d_scale;
+  if (e.d_type == kOutF32) {
+    *reinterpret_cast<float4*>(static_cast<float*>(e.D) + at) =
+        make_float4(s * v[0], s * v[1], s * v[2], s * v[3]);
+  } else if (e.d_type == kOutBf16) {
+    __nv_bfloat162 h[2] = {__floats2bfloat162_rn(s * v[0], s * v[1]),
+                           __floats2bfloat162_rn(s * v[2], s * v[3])};
+    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(e.D) + at) =
+        *reinterpret_cast<const uint2*>(h);
+  } else {
+    uint32_t w = 0u;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) w |= static_cast<uint32_t>(epi_to_byte(e, v[q])) << (8 * q);
+    *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(e.D) + at) = w;
+  }
 }
 
 // Store 8 consecutive elements of D starting at a column that is a multiple

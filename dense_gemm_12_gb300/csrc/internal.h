@@ -36,19 +36,30 @@ struct SimtArgs {
   int split;
   float* ws;
   uint32_t* counters;
+  int group_m;     // raster group height in tile rows
+};
+
+// A launch configuration of the tile kernels: gemm_config_t of the C ABI
+// with every field resolved (no "auto" values).
+struct TileConfig {
+  int kernel;    // GEMM_KERNEL_SINGLE_CTA or GEMM_KERNEL_CTA_PAIR
+  int split;     // k-ranges per item of the last round, 1..8
+  int group_m;   // raster group height, 1..64
 };
 
 // Work plan of the CUDA-core kernel for tiles output tiles, num_kb k-blocks
 // and up to num_sms persistent CTAs: how many tiles run whole, how the rest
-// are split along k, and the grid.
+// are split along k, and the grid.  `fixed` pins the split (and carries the
+// group height); nullptr lets the cost model choose.
 struct SimtPlan {
   int full_items;
   int split;
   int grid;
+  int group_m;
   int64_t ws_floats;   // workspace the split tiles need
   int64_t counters;    // counters the split tiles need
 };
-SimtPlan simt_plan(int tiles, int num_kb, int num_sms);
+SimtPlan simt_plan(int tiles, int num_kb, int num_sms, const TileConfig* fixed);
 
 // CUDA-core (FFMA) GEMM: 128 x 128 block tiles, warp tiles 32 x 64, 8 x 8
 // register micro-tiles.  tmA / tmB are used only for operands in kLoadTma mode.
@@ -61,12 +72,14 @@ constexpr int kSimtBM = 128, kSimtBN = 128, kSimtBK = 32;
 
 // Number of k-parts S (1 = none) into which the items of the last round are
 // cut when `items` equal work items of num_kb k-blocks run on `workers`
-// persistent workers.  In item-times the tail then takes
-//     ceil(tail * S / workers) / S  +  S * part_cost_kb / num_kb
-// instead of 1, where part_cost_kb is the time to store or load one part's
-// partial sums in k-block times (the last part to finish writes its own and
-// reads the other S - 1).  Every part keeps at least 4 k-blocks.
-int tail_split(int items, int num_kb, int workers, double part_cost_kb);
+// persistent workers.  With R = ceil(tail * S / workers) rounds of parts the
+// tail takes, in item-times,
+//     R / S  +  R * S * fixup_kb / num_kb
+// instead of 1: each round of parts also pays the split's own work (storing
+// partial sums, and for the last part of a tile reading the other S - 1 and
+// writing the tile), measured at about fixup_kb k-block times per part.
+// Every part keeps at least 4 k-blocks.
+int tail_split(int items, int num_kb, int workers, double fixup_kb);
 
 struct TcArgs {
   int M, N, K;
@@ -82,18 +95,22 @@ struct TcArgs {
   int split;
   float* ws;
   uint32_t* counters;
+  int group_m;     // raster group height in tile rows (pair-tile rows on pairs)
 };
 
 // Launch plan of the bf16 tensor-core GEMM for one shape.
 struct TcPlan {
-  bool pair;          // CTA-pair kernel (M > 128) or single-CTA kernel
+  bool pair;          // CTA-pair kernel or single-CTA kernel
   int full_items;
   int split;
   int grid;           // CTAs to launch (pairs: twice the clusters)
+  int group_m;
   int64_t ws_floats;  // workspace the split items need
   int64_t counters;   // counters the split items need
 };
-TcPlan tc_plan(int M, int N, int K, int num_sms);
+// `fixed` pins kernel, split and group height; nullptr: the pair kernel for
+// M > 128, the cost model's split, groups of 8.
+TcPlan tc_plan(int M, int N, int K, int num_sms, const TileConfig* fixed);
 
 // bf16 tensor-core GEMM (tcgen05, accumulator in TMEM): 128 x 256 tiles on
 // one CTA, or 256 x 256 tiles on CTA pairs, as planned by tc_plan.

@@ -144,6 +144,19 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
   return v;
 }
 
+// Arrival on a split tile's counter by one thread of a CTA, after a CTA
+// barrier that follows every thread's partial-sum stores: the release half
+// publishes those stores (cumulatively, through the barrier) before the
+// count; the acquire half lets the thread that sees the last count read the
+// other CTAs' partial sums after a second CTA barrier.  Returns the count
+// before the add.
+__device__ __forceinline__ uint32_t atomic_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+               : "memory");
+  return old;
+}
+
 __device__ __forceinline__ void st_release_cta_shared(int* p, int v) {
   asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
 }

@@ -49,7 +49,6 @@ constexpr int kComputeThreads = kComputeWarps * 32;
 constexpr int kStageBytesA = BM * BK * 4;  // 16 KB, rows of 128 B, 128-B swizzled
 constexpr int kStageBytesB = BK * BN * 4;  // 16 KB, rows of 512 B, not swizzled
 constexpr int kStageBytes = kStageBytesA + kStageBytesB;
-constexpr int kGroupM = 8;                 // raster group height in tiles
 
 struct __align__(8) SimtSmemTail {
   uint64_t full[STAGES];
@@ -69,11 +68,14 @@ struct SimtItem {
 constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + STAGES * kStageBytes +
                               sizeof(SimtSmemTail);
 
-__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int& tm, int& tn) {
-  const int per_group = kGroupM * tiles_n;
+// Grouped raster: tiles walk column by column through groups of group_m
+// tile rows, so neighbouring CTAs share A row panels and B column panels in L2.
+__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int group_m, int& tm,
+                                            int& tn) {
+  const int per_group = group_m * tiles_n;
   const int g = t / per_group;
-  const int first_m = g * kGroupM;
-  const int rows = min(tiles_m - first_m, kGroupM);
+  const int first_m = g * group_m;
+  const int rows = min(tiles_m - first_m, group_m);
   const int local = t - g * per_group;
   tm = first_m + local % rows;
   tn = local / rows;
@@ -97,7 +99,7 @@ __device__ __forceinline__ SimtItem simt_item(const SimtArgs& p, int i, int tile
     it.kb0 = static_cast<int>(static_cast<int64_t>(it.part) * num_kb / p.split);
     it.kb1 = static_cast<int>(static_cast<int64_t>(it.part + 1) * num_kb / p.split);
   }
-  tile_coords(tile, tiles_m, tiles_n, it.tm, it.tn);
+  tile_coords(tile, tiles_m, tiles_n, p.group_m, it.tm, it.tn);
   return it;
 }
 
@@ -483,14 +485,12 @@ __global__ void __launch_bounds__(SimtTraits<MODE_A, MODE_B>::kThreads, 1)
     }
     compute_bar();
     if (ctid == 0) {
-      __threadfence();  // publish the whole CTA's partial before arriving
-      const uint32_t before = atomicAdd(p.counters + w.split_tile, 1u);
+      const uint32_t before = atomic_add_acq_rel_gpu(p.counters + w.split_tile, 1u);
       tail->last_flag = (before == static_cast<uint32_t>(p.split - 1)) ? 1 : 0;
     }
     compute_bar();
     const int last = tail->last_flag;
     if (last) {
-      __threadfence();
       float sum[8][8];
 #pragma unroll
       for (int i = 0; i < 8; ++i)
@@ -540,16 +540,19 @@ cudaError_t launch_variant(const SimtArgs& a, const CUtensorMap* tmA, const CUte
 
 }  // namespace
 
-SimtPlan simt_plan(int tiles, int num_kb, int num_sms) {
-  SimtPlan pl{tiles, 1, tiles < num_sms ? tiles : num_sms, 0, 0};
+SimtPlan simt_plan(int tiles, int num_kb, int num_sms, const TileConfig* fixed) {
+  const int group_m = (fixed != nullptr && fixed->group_m > 0) ? fixed->group_m : 8;
+  SimtPlan pl{tiles, 1, tiles < num_sms ? tiles : num_sms, group_m, 0, 0};
   if (tiles <= 0 || num_sms <= 0) return pl;
   // Tiles beyond the last full wave (all of them when there are fewer tiles
   // than SMs) are split along k when that shortens the last wave.
-  // A 64 KB partial moves in about a quarter of a 128 x 128 x 32 k-block's
-  // FFMA time.
-  const int best_s = tail_split(tiles, num_kb, num_sms, 0.3);
-  if (best_s == 1) return pl;
+  // Measured split overhead: about 2 k-block times (2.6 us each) per part
+  // and round.  A pinned split is capped at one k-block per part.
+  int best_s = (fixed != nullptr && fixed->split > 0) ? fixed->split
+                                                      : tail_split(tiles, num_kb, num_sms, 2.0);
+  if (best_s > num_kb) best_s = num_kb;
   const int tail = tiles >= num_sms ? tiles % num_sms : tiles;
+  if (best_s <= 1 || tail == 0) return pl;
   pl.full_items = tiles - tail;
   pl.split = best_s;
   const int items = pl.full_items + tail * best_s;

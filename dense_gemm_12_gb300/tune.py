@@ -1,0 +1,225 @@
+"""Offline launch-configuration sweep for the tile kernels (run on the GPU).
+
+"A GEMM Kernel, Step by Step" ("Six parameters, found by search"): the best
+tiling depends on the card and the shape, so it is searched for.  The tile
+sizes, stages and warp layouts of this library are fixed per kernel at build
+time (chosen by earlier sweeps); what varies per call is which kernel runs
+(bf16: one CTA per 128 x 256 tile or a CTA pair per 256 x 256 tile), how the
+last round's work items are cut along k, and the raster group height.  This
+script times every such configuration on one representative shape per class
+(class = ceil(log2) of M, N, K), keeps the configurations that beat automatic
+dispatch by a margin on a second, longer timing, and writes
+
+  * the table automatic dispatch reads (``csrc/dispatch_table.inc``; rebuild
+    the library afterwards), and
+  * a summary of every class (markdown).
+
+Every candidate's result is compared with the automatic configuration's
+before it is timed; a configuration whose result differs beyond the GEMM's
+error bound is reported and never enters the table.
+
+    python -m dense_gemm_12_gb300.tune --table dense_gemm_12_gb300/csrc/dispatch_table.inc \\
+        --summary sweep.md
+"""
+from __future__ import annotations
+
+import argparse
+import datetime
+import itertools
+import math
+import statistics
+import sys
+
+BF16_M = [64, 256, 1024, 2048, 4096, 8192]
+BF16_NK = [1024, 4096, 8192]
+FP32_M = [128, 512, 1024, 2048, 4092]
+FP32_NK = [1024, 4092, 8192]
+SPLITS = [1, 2, 3, 4, 6, 8]
+GROUPS = [4, 8, 16]
+
+
+def ceil_log2(x: int) -> int:
+    b = 0
+    while (1 << b) < x:
+        b += 1
+    return b
+
+
+def candidates(is_bf16: bool, M: int, K: int):
+    """Every pinned configuration worth timing for a shape."""
+    kernels = ["single_cta"]
+    if is_bf16 and M > 128:
+        kernels = ["cta_pair", "single_cta"]
+    num_kb = -(-K // (64 if is_bf16 else 32))
+    for kernel, split, group in itertools.product(kernels, SPLITS, GROUPS):
+        if split <= num_kb:
+            yield {"kernel": kernel, "split": split, "group_m": group}
+
+
+def table_lines(entries, num_sms: int, gpu: str, date: str):
+    """Text of dispatch_table.inc for `entries` (dicts with is_bf16, M, N, K,
+    kernel, split, group_m and the timings)."""
+    kid = {"single_cta": 1, "cta_pair": 2}
+    out = [
+        "// dispatch_table.inc -- launch configurations chosen by the offline sweep",
+        "// (dense_gemm_12_gb300/tune.py) for the tile kernels, keyed by ceil(log2) of",
+        "// M, N and K.  Written by that script; edit by re-running it.",
+        "//",
+        "// Measured on %s (%d SMs), %s.  Shapes whose class has no entry use" % (gpu, num_sms, date),
+        "// the cost model.",
+        "constexpr int kTunedSms = %d;" % num_sms,
+        "constexpr TunedEntry kTuned[] = {",
+        "    // {is_bf16, log2 M, log2 N, log2 K, kernel, split, group_m}",
+    ]
+    for e in sorted(entries, key=lambda e: (e["is_bf16"], e["M"], e["N"], e["K"])):
+        out.append("    {%d, %d, %d, %d, %d, %d, %d},  // %dx%dx%d: %.4f ms, automatic %.4f ms" % (
+            e["is_bf16"], ceil_log2(e["M"]), ceil_log2(e["N"]), ceil_log2(e["K"]),
+            kid[e["kernel"]], e["split"], e["group_m"], e["M"], e["N"], e["K"],
+            e["best_ms"], e["auto_ms"]))
+    out.append("    {-1, 0, 0, 0, 0, 0, 0},  // end")
+    out.append("};")
+    return "\n".join(out) + "\n"
+
+
+def choose(results, margin: float):
+    """Table entries: shapes whose confirmed best configuration beats automatic
+    dispatch by more than `margin` (relative)."""
+    return [r for r in results
+            if r.get("best") is not None and r["best_ms"] < r["auto_ms"] * (1.0 - margin)]
+
+
+def _run(torch, g, is_bf16, M, N, K, tensors, cfg, stream):
+    A, B, C = tensors
+    fn = g.gemm_bf16gemm_config if is_bf16 else g.gemm_sgemm_config
+    st = fn(M, N, K, 1.0, A.data_ptr(), K, B.data_ptr(), N, 0.0, C.data_ptr(), N, cfg,
+            stream.cuda_stream)
+    if st != 0:
+        raise RuntimeError("%s: %s" % (cfg, g.gemm_status_string(st)))
+
+
+def _time(torch, g, is_bf16, M, N, K, tensors, cfg, stream, reps):
+    for _ in range(2):
+        _run(torch, g, is_bf16, M, N, K, tensors, cfg, stream)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * reps)]
+    for i in range(reps):
+        ev[2 * i].record(stream)
+        _run(torch, g, is_bf16, M, N, K, tensors, cfg, stream)
+        ev[2 * i + 1].record(stream)
+    torch.cuda.synchronize()
+    return statistics.median(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(reps))
+
+
+def sweep_shape(torch, g, is_bf16, M, N, K, stream, reps=5, confirm_reps=20):
+    dev = torch.device("cuda", torch.cuda.current_device())
+    gen = torch.Generator(device=dev).manual_seed(M * 131 + N * 17 + K)
+    dt = torch.bfloat16 if is_bf16 else torch.float32
+    A = torch.randn(M, K, device=dev, generator=gen).to(dt)
+    B = (torch.randn(K, N, device=dev, generator=gen) * 0.05).to(dt)
+    C = torch.empty(M, N, device=dev, dtype=torch.float32)
+    tensors = (A, B, C)
+    auto_cfg, _ = g.gemm_get_config(is_bf16, M, N, K)
+    _run(torch, g, is_bf16, M, N, K, tensors, None, stream)
+    torch.cuda.synchronize()
+    ref = C.clone()
+    # error scale of this GEMM: |A||B| per element bounds every order's error
+    den = (A.float().abs() @ B.float().abs())
+    tol = (8e-3 if is_bf16 else 2e-6 * math.sqrt(K)) * den
+    timed, rejected = [], []
+    for cfg in candidates(is_bf16, M, K):
+        _run(torch, g, is_bf16, M, N, K, tensors, cfg, stream)
+        torch.cuda.synchronize()
+        if not bool(((C - ref).abs() <= tol).all()):
+            rejected.append(cfg)
+            continue
+        timed.append((_time(torch, g, is_bf16, M, N, K, tensors, cfg, stream, reps), cfg))
+    auto_ms = _time(torch, g, is_bf16, M, N, K, tensors, None, stream, confirm_reps)
+    timed.sort(key=lambda t: t[0])
+    best_ms, best = None, None
+    if timed:
+        best = timed[0][1]
+        best_ms = _time(torch, g, is_bf16, M, N, K, tensors, best, stream, confirm_reps)
+    del A, B, C, ref, den, tol
+    torch.cuda.empty_cache()
+    return {"is_bf16": int(is_bf16), "M": M, "N": N, "K": K, "auto": auto_cfg,
+            "auto_ms": auto_ms, "best": best, "best_ms": best_ms,
+            "kernel": best["kernel"] if best else None, "split": best["split"] if best else None,
+            "group_m": best["group_m"] if best else None, "rejected": rejected,
+            "candidates": len(timed)}
+
+
+def summary_lines(results, chosen, gpu, num_sms, command):
+    flops = lambda r: 2.0 * r["M"] * r["N"] * r["K"]
+    lines = ["# Launch-configuration sweep of the tile kernels", "",
+             "Command (%s, %d SMs):" % (gpu, num_sms), "", "    " + command, "",
+             "Per class (ceil(log2) of M, N, K), one representative shape; automatic = "
+             "the cost model (split of the last round, pair kernel for bf16 M > 128, "
+             "raster groups of 8); best = fastest pinned configuration, re-timed "
+             "(median of 20).  Entries marked `table` beat automatic by more than the "
+             "margin and were written to `csrc/dispatch_table.inc`.", "",
+             "| type | M x N x K | automatic (kernel, split, group) | ms | TFLOP/s | best | ms "
+             "| TFLOP/s | gain | |", "|---|---|---|---:|---:|---|---:|---:|---:|---|"]
+    chosen_keys = {(c["is_bf16"], c["M"], c["N"], c["K"]) for c in chosen}
+    for r in results:
+        a = r["auto"]
+        b = r["best"] or {}
+        gain = r["auto_ms"] / r["best_ms"] - 1.0 if r["best_ms"] else 0.0
+        lines.append("| %s | %dx%dx%d | %s, %d, %d | %.4f | %.1f | %s, %s, %s | %.4f | %.1f | "
+                     "%+.1f %% | %s |" % (
+                         "bf16" if r["is_bf16"] else "fp32", r["M"], r["N"], r["K"],
+                         a["kernel"], a["split"], a["group_m"], r["auto_ms"],
+                         flops(r) / r["auto_ms"] / 1e9, b.get("kernel"), b.get("split"),
+                         b.get("group_m"), r["best_ms"] or 0.0,
+                         flops(r) / r["best_ms"] / 1e9 if r["best_ms"] else 0.0, 100 * gain,
+                         "table" if (r["is_bf16"], r["M"], r["N"], r["K"]) in chosen_keys
+                         else ""))
+    bad = [(r, c) for r in results for c in r["rejected"]]
+    lines += ["", "Configurations rejected by the result check: %d." % len(bad)]
+    for r, c in bad:
+        lines.append("- %dx%dx%d %s" % (r["M"], r["N"], r["K"], c))
+    return "\n".join(lines) + "\n"
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--table", required=True, help="where to write dispatch_table.inc")
+    ap.add_argument("--summary", required=True, help="where to write the markdown summary")
+    ap.add_argument("--margin", type=float, default=0.03,
+                    help="relative gain over automatic dispatch a table entry needs")
+    ap.add_argument("--only", choices=["bf16", "fp32"], default=None)
+    args = ap.parse_args(argv)
+
+    import torch
+
+    import dense_gemm_12_gb300 as g
+    g.load_library(build_if_missing=True)
+    dev = torch.cuda.current_device()
+    props = torch.cuda.get_device_properties(dev)
+    num_sms = props.multi_processor_count
+    stream = torch.cuda.current_stream(dev)
+    shapes = []
+    if args.only in (None, "bf16"):
+        shapes += [(True, M, N, K) for M in BF16_M for N in BF16_NK for K in BF16_NK]
+    if args.only in (None, "fp32"):
+        shapes += [(False, M, N, K) for M in FP32_M for N in FP32_NK for K in FP32_NK]
+    results = []
+    for is_bf16, M, N, K in shapes:
+        r = sweep_shape(torch, g, is_bf16, M, N, K, stream)
+        results.append(r)
+        print("%s %dx%dx%d auto %.4f best %s %.4f" % ("bf16" if is_bf16 else "fp32", M, N, K,
+                                                     r["auto_ms"], r["best"], r["best_ms"] or 0),
+              flush=True)
+    st = g.gemm_check_device_error(stream.cuda_stream)
+    if st != 0:
+        raise RuntimeError("device error during the sweep: " + g.gemm_status_string(st))
+    chosen = choose(results, args.margin)
+    date = datetime.date.today().isoformat()
+    with open(args.table, "w") as f:
+        f.write(table_lines(chosen, num_sms, props.name, date))
+    command = "python -m dense_gemm_12_gb300.tune " + " ".join(argv or sys.argv[1:])
+    with open(args.summary, "w") as f:
+        f.write(summary_lines(results, chosen, props.name, num_sms, command))
+    print("%d of %d classes written to the table" % (len(chosen), len(results)))
+
+
+if __name__ == "__main__":
+    main()

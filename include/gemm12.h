@@ -305,6 +305,72 @@ gemm_path_t gemm_select_path(int is_bf16, int64_t M, int64_t N, int64_t K,
 int gemm_split_parts(int is_bf16, int64_t M, int64_t N, int64_t K);
 
 /*
+ * Launch configurations of the tile kernels ("A GEMM Kernel, Step by Step",
+ * "Six parameters, found by search": the best tiling depends on the card and
+ * the shape, so it is searched for rather than derived).  Tile sizes, stages
+ * and warp layout are fixed per kernel at build time; what can change per
+ * call is which kernel runs, how the last round's work items are cut along k
+ * and the raster order.  Automatic dispatch takes these from a table written
+ * by an offline sweep on this GPU (dense_gemm_12_gb300/tune.py), keyed by
+ * ceil(log2) of M, N and K, and falls back to a cost model for shapes the
+ * table does not hold.
+ */
+typedef enum {
+    GEMM_KERNEL_AUTO = 0,        /* the library chooses                        */
+    GEMM_KERNEL_SINGLE_CTA = 1,  /* one CTA per tile: the CUDA-core kernel's
+                                    128 x 128 tiles (fp32), the tcgen05
+                                    kernel's 128 x 256 tiles (bf16)            */
+    GEMM_KERNEL_CTA_PAIR = 2     /* bf16 only: two CTAs of a cluster per
+                                    256 x 256 tile (tcgen05 cta_group::2)      */
+} gemm_kernel_t;
+
+typedef struct {
+    int kernel;   /* a gemm_kernel_t                                          */
+    int split;    /* k-ranges per work item of the persistent grid's last
+                     round: 0 = automatic, 1 = none, 2..8 (capped at one
+                     k-block per range)                                      */
+    int group_m;  /* raster order: work items walk column by column through
+                     groups of this many item rows; 0 = automatic, 1..64     */
+} gemm_config_t;
+
+/*
+ * gemm_sgemm_config / gemm_bf16gemm_config -- gemm_sgemm / gemm_bf16gemm with
+ * the launch configuration pinned by cfg (cfg == NULL or all fields 0: the
+ * same as the plain call).  The result is the same GEMM within the same bound
+ * for every configuration (bit-identical where the sums are exact).  A pinned
+ * bf16 kernel always runs the tcgen05 tile kernels, also for M <= 16 (the
+ * decode kernel runs only under GEMM_KERNEL_AUTO).  The fp32 path has one
+ * kernel: GEMM_KERNEL_CTA_PAIR is invalid there, and so is every field for
+ * the paths without tiles (M, N, K or alpha zero: nothing to configure, the
+ * fields are ignored).  Errors: fields out of range give
+ * GEMM_ERR_INVALID_VALUE; otherwise as the plain calls.  bf16 operands that
+ * TMA cannot describe run on the CUDA cores, where only split and group_m
+ * apply.
+ */
+gemm_status_t gemm_sgemm_config(int64_t M, int64_t N, int64_t K, float alpha,
+                                const float *A, int64_t lda,
+                                const float *B, int64_t ldb,
+                                float beta, float *C, int64_t ldc,
+                                const gemm_config_t *cfg, void *stream);
+gemm_status_t gemm_bf16gemm_config(int64_t M, int64_t N, int64_t K, float alpha,
+                                   const void *A, int64_t lda,
+                                   const void *B, int64_t ldb,
+                                   float beta, float *C, int64_t ldc,
+                                   const gemm_config_t *cfg, void *stream);
+
+/*
+ * gemm_get_config -- host-only: the configuration automatic dispatch uses for
+ * an M x N x K problem on the current device (every field resolved; for the
+ * bf16 decode shapes, M <= 16, kernel is GEMM_KERNEL_AUTO and the other
+ * fields 0: the decode kernel plans itself).  *from_table (may be NULL) is
+ * set to 1 when the entry came from the sweep's table, 0 for the cost model.
+ * Errors: out == NULL or negative sizes: GEMM_ERR_INVALID_VALUE; no usable
+ * sm_103a device: GEMM_ERR_UNSUPPORTED.
+ */
+gemm_status_t gemm_get_config(int is_bf16, int64_t M, int64_t N, int64_t K,
+                              gemm_config_t *out, int *from_table);
+
+/*
  * Tile and wave quantization of a launch ("A GEMM Kernel, Step by Step",
  * "The fringe and the last wave"; "Tiled matrix multiplication",
  * "Complexity and constants", wave quantization).

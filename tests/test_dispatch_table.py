@@ -1,0 +1,66 @@
+"""Host logic of the launch-configuration sweep and the committed table
+(no GPU): the table parses, every entry is a valid configuration, classes are
+unique, and the sweep's selection and writer behave as documented."""
+import os
+import re
+
+from dense_gemm_12_gb300 import tune
+
+TABLE = os.path.join(os.path.dirname(__file__), "..", "dense_gemm_12_gb300", "csrc",
+                     "dispatch_table.inc")
+ENTRY = re.compile(r"^\s*\{(-?\d+),\s*(\d+),\s*(\d+),\s*(\d+),\s*(\d+),\s*(\d+),\s*(\d+)\}")
+
+
+def parse_table(text):
+    sms = int(re.search(r"kTunedSms\s*=\s*(\d+);", text).group(1))
+    rows = [tuple(int(x) for x in m.groups()) for m in map(ENTRY.match, text.splitlines()) if m]
+    return sms, rows
+
+
+def test_committed_table_is_well_formed():
+    sms, rows = parse_table(open(TABLE).read())
+    assert sms > 0
+    assert rows and rows[-1][0] == -1, "the table ends with the sentinel"
+    body = rows[:-1]
+    keys = [r[:4] for r in body]
+    assert len(keys) == len(set(keys)), "one entry per class"
+    for is_bf16, lm, ln, lk, kernel, split, group in body:
+        assert is_bf16 in (0, 1)
+        assert all(0 <= v <= 31 for v in (lm, ln, lk))
+        assert kernel in (1, 2) and (kernel == 1 or is_bf16 == 1)
+        assert 1 <= split <= 8 and 1 <= group <= 64
+
+
+def test_ceil_log2_buckets():
+    assert [tune.ceil_log2(x) for x in (1, 2, 3, 4092, 4096, 4097, 8192)] == \
+        [0, 1, 2, 12, 12, 13, 13]
+
+
+def test_candidates_respect_kernel_and_k():
+    c = list(tune.candidates(True, 64, 4096))
+    assert {x["kernel"] for x in c} == {"single_cta"}          # M <= 128: no pairs
+    c = list(tune.candidates(True, 1024, 128))                  # 2 k-blocks
+    assert {x["kernel"] for x in c} == {"single_cta", "cta_pair"}
+    assert max(x["split"] for x in c) == 2
+    assert {x["kernel"] for x in tune.candidates(False, 4092, 4092)} == {"single_cta"}
+
+
+def _result(M, auto_ms, best_ms, is_bf16=1):
+    return {"is_bf16": is_bf16, "M": M, "N": 1024, "K": 1024, "auto_ms": auto_ms,
+            "best_ms": best_ms, "best": {"kernel": "cta_pair", "split": 2, "group_m": 4},
+            "kernel": "cta_pair", "split": 2, "group_m": 4,
+            "auto": {"kernel": "cta_pair", "split": 1, "group_m": 8}, "rejected": []}
+
+
+def test_choose_needs_the_margin():
+    rs = [_result(256, 1.0, 0.99), _result(512, 1.0, 0.96), _result(1024, 1.0, 1.2)]
+    chosen = tune.choose(rs, 0.03)
+    assert [r["M"] for r in chosen] == [512]
+
+
+def test_table_writer_round_trips():
+    text = tune.table_lines([_result(512, 1.0, 0.9), _result(300, 2.0, 1.0, is_bf16=0)], 152,
+                            "GPU", "2026-01-01")
+    sms, rows = parse_table(text)
+    assert sms == 152
+    assert rows == [(0, 9, 10, 10, 2, 2, 4), (1, 9, 10, 10, 2, 2, 4), (-1, 0, 0, 0, 0, 0, 0)]

@@ -122,12 +122,13 @@ def test_full_8192_sampled_rows():
 
 
 # ---- the last round's work items cut along k (split-K tail) ---------------
-# The plan depends on how many CTAs (pairs) are resident; each case asserts
-# that it really splits.
+# The plan depends on how many CTAs (pairs) are resident and on the sweep's
+# table; each case asserts that it really splits (the shapes lie in classes
+# the table leaves to the cost model).
 
 @pytest.mark.parametrize("M,N,K", [
-    (2560, 4096, 1024),   # pair kernel: 80 pair tiles on at most 76 clusters
-    (64, 2048, 2048),     # single-CTA kernel: 8 tiles on 152 SMs
+    (512, 10240, 4096),   # pair kernel: 80 pair tiles on at most 76 clusters
+    (64, 2048, 4096),     # single-CTA kernel: 8 tiles on 152 SMs
 ])
 def test_split_integers_exact(M, N, K):
     # |partial sums| <= 16 K < 2^24: exact in fp32 in any order and any split
@@ -143,8 +144,8 @@ def test_split_integers_exact(M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K", [
-    (2560, 4096, 1024),   # pair kernel
-    (2304, 4296, 2000),   # pair kernel, ragged N and K (last part ends on a partial k-block)
+    (512, 10240, 4096),   # pair kernel
+    (500, 10232, 4000),   # pair kernel, ragged M, N and K (last part ends on a partial k-block)
     (100, 1024, 4096),    # single-CTA kernel
 ])
 def test_split_matches_oracle_and_repeats(M, N, K):
