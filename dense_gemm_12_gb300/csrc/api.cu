@@ -546,12 +546,6 @@ static gemm_status_t run_bf16_tensor_core(DeviceState* st, gemm_path_t path, int
                                           const gemm_config_t* cfg) {
   CUtensorMap tmA, tmB;
   if (path == GEMM_PATH_TC_BF16 || path == GEMM_PATH_TC_BF16_PAIR) {
-    // tc_plan picks the CTA-pair kernel exactly when M > kTcBM
-    if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, K, M, lda, kTcBK, kTcBM,
-                   CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, N, K, ldb, 64, kTcBK,
-                   CU_TENSOR_MAP_SWIZZLE_128B))
-      return GEMM_ERR_LAUNCH;
     TcArgs a{};
     a.M = static_cast<int>(M);
     a.N = static_cast<int>(N);
@@ -560,6 +554,12 @@ static gemm_status_t run_bf16_tensor_core(DeviceState* st, gemm_path_t path, int
     a.err = st->err_word;
     const TileConfig tc = resolve_config(true, M, N, K, st->num_sms, cfg, nullptr);
     const TcPlan pl = tc_plan(a.M, a.N, a.K, st->num_sms, &tc);
+    const uint32_t b_rows = static_cast<uint32_t>(tc_b_box_rows(pl.pair));
+    if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, K, M, lda, 64, kTcBM,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, N, K, ldb, 64, b_rows,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+      return GEMM_ERR_LAUNCH;
     a.full_items = pl.full_items;
     a.split = pl.split;
     a.group_m = pl.group_m;

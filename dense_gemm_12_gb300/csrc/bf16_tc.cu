@@ -569,13 +569,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 //                 both when the MMAs have read the stage;
 //   tmem_full[b]  in each CTA, from the commit after a tile's last k-block;
 //   tmem_empty[b] even CTA only: one arrival per epilogue warp of both CTAs.
+#ifndef G12_TC_PAIR_BK
+#define G12_TC_PAIR_BK 128
+#endif
+constexpr int PBK = G12_TC_PAIR_BK;                      // k per stage (64 or 128)
+static_assert(PBK == 64 || PBK == 128, "pair kernel k-block");
 #ifndef G12_TC_PAIR_STAGES
-#define G12_TC_PAIR_STAGES 6
+#define G12_TC_PAIR_STAGES (PBK == 64 ? 6 : 3)
 #endif
 constexpr int PS = G12_TC_PAIR_STAGES;
 constexpr int kPairBN = BN / 2;                         // B columns held per CTA
-constexpr int kPairStageBytesA = BM * BK * 2;           // 16 KB
-constexpr int kPairStageBytesB = BK * kPairBN * 2;      // 16 KB
+constexpr int kABoxBytes = BM * 64 * 2;                 // one 64-wide swizzled A box, 16 KB
+constexpr int kPairStageBytesA = BM * PBK * 2;          // PBK / 64 A boxes
+constexpr int kPairBoxBytesB = PBK * 64 * 2;            // one 64-column B box of PBK rows
+constexpr int kPairStageBytesB = PBK * kPairBN * 2;     // two B boxes
 constexpr int kPairStageBytes = kPairStageBytesA + kPairStageBytesB;
 constexpr uint16_t kPairMask = 0x3;
 constexpr uint32_t kPairIdesc = idesc_bf16_f32(2 * BM, BN, /*A MN-major*/ 0, /*B MN-major*/ 1);
@@ -611,7 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tiles_n = (p.N + BN - 1) / BN;
   const int pairs_m = (tiles_m + 1) / 2;
   const int units = num_units(p, pairs_m * tiles_n);
-  const int num_kb = (p.K + BK - 1) / BK;
+  const int num_kb = (p.K + PBK - 1) / PBK;
   const uint32_t rank = cluster_cta_rank() & 1u;
   const bool even = (rank == 0);
   const int first_item = static_cast<int>(blockIdx.x) / 2;
@@ -666,11 +673,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* sb = sa + kPairStageBytesA;
           const uint32_t full = full0 + static_cast<uint32_t>(s * sizeof(uint64_t));
           if (even) mbar_arrive_expect_tx(&tail->full[s], 2 * kPairStageBytes);
-          tma_load_2d_pair(sa, &tmA, kb * BK, tm * BM, full);
+#pragma unroll
+          for (int q = 0; q < PBK / 64; ++q)
+            tma_load_2d_pair(sa + q * kABoxBytes, &tmA, kb * PBK + q * 64, tm * BM, full);
 #pragma unroll
           for (int j = 0; j < kPairBN / 64; ++j)
-            tma_load_2d_pair(sb + j * kBoxBytesB, &tmB,
-                             tn * BN + static_cast<int>(rank) * kPairBN + j * 64, kb * BK, full);
+            tma_load_2d_pair(sb + j * kPairBoxBytesB, &tmB,
+                             tn * BN + static_cast<int>(rank) * kPairBN + j * 64, kb * PBK, full);
         }
       }
       // Leave only after the MMAs have read every stage this CTA filled: then
@@ -712,9 +721,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sa = smem_u32(smem + s * kPairStageBytes);
           const uint32_t sb = sa + kPairStageBytesA;
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t adesc = smem_desc_sw128(sa + kk * 32, 16, 1024);
-            const uint64_t bdesc = smem_desc_sw128(sb + kk * 2048, kBoxBytesB, 1024);
+          for (int kk = 0; kk < PBK / 16; ++kk) {
+            // A: K-major, 64-wide boxes 16 KB apart; B: MN-major, 64-column
+            // boxes of PBK rows, a K step of 16 rows is 2048 B.
+            const uint64_t adesc =
+                smem_desc_sw128(sa + (kk / 4) * kABoxBytes + (kk % 4) * 32, 16, 1024);
+            const uint64_t bdesc = smem_desc_sw128(sb + kk * 2048, kPairBoxBytesB, 1024);
             tc_mma_f16_pair(d_tmem, adesc, bdesc, kPairIdesc, (kb != w.kb0 || kk != 0) ? 1u : 0u);
           }
           issued = true;
@@ -809,13 +821,16 @@ static int pair_max_clusters(int num_sms) {
   return clusters;
 }
 
+int tc_b_box_rows(bool pair) { return pair ? PBK : BK; }
+
 TcPlan tc_plan(int M, int N, int K, int num_sms, const TileConfig* fixed) {
   TcPlan pl{};
   const int tiles_m = (M + BM - 1) / BM;
   const int tiles_n = (N + BN - 1) / BN;
-  const int num_kb = (K + BK - 1) / BK;
   const bool pinned = fixed != nullptr && fixed->kernel != GEMM_KERNEL_AUTO;
   pl.pair = pinned ? fixed->kernel == GEMM_KERNEL_CTA_PAIR : tiles_m >= 2;
+  const int kblock = pl.pair ? PBK : BK;
+  const int num_kb = (K + kblock - 1) / kblock;
   pl.group_m = (fixed != nullptr && fixed->group_m > 0) ? fixed->group_m : 8;
   const int ctas_per_item = pl.pair ? 2 : 1;
   const int items = pl.pair ? ((tiles_m + 1) / 2) * tiles_n : tiles_m * tiles_n;
@@ -823,7 +838,7 @@ TcPlan tc_plan(int M, int N, int K, int num_sms, const TileConfig* fixed) {
   // a pinned split is capped at one k-block per part
   pl.split = (fixed != nullptr && fixed->split > 0)
                  ? (fixed->split < num_kb ? fixed->split : num_kb)
-                 : tail_split(items, num_kb, workers, G12_TC_FIXUP_KB);
+                 : tail_split(items, num_kb, workers, G12_TC_FIXUP_KB * BK / kblock);
   if (pl.split < 1) pl.split = 1;
   const int tail_items = items >= workers ? items % workers : items;
   if (tail_items == 0) pl.split = 1;

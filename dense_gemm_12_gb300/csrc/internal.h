@@ -111,6 +111,8 @@ struct TcPlan {
 // `fixed` pins kernel, split and group height; nullptr: the pair kernel for
 // M > 128, the cost model's split, groups of 8.
 TcPlan tc_plan(int M, int N, int K, int num_sms, const TileConfig* fixed);
+// k-rows of B per TMA box of the single-CTA (pair = false) or pair kernel.
+int tc_b_box_rows(bool pair);
 
 // bf16 tensor-core GEMM (tcgen05, accumulator in TMEM): 128 x 256 tiles on
 // one CTA, or 256 x 256 tiles on CTA pairs, as planned by tc_plan.
