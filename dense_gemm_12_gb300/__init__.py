@@ -22,7 +22,8 @@ __all__ = [
     "GemmError", "load_library", "library_path", "gemm_sgemm", "gemm_bf16gemm",
     "gemm_bf16gemm_decode_static", "gemm_bf16gemm_epilogue", "bf16gemm_epilogue", "ACT", "OUT",
     "gemm_bf16gemm_fused", "bf16gemm_fused", "GemmOutput",
-    "gemm_sgemm_config", "gemm_bf16gemm_config", "gemm_get_config", "GemmConfig", "KERNELS",
+    "gemm_sgemm_config", "gemm_bf16gemm_config", "gemm_get_config", "gemm_get_model_config",
+    "GemmConfig", "KERNELS",
     "gemm_status_string", "gemm_check_device_error", "gemm_shutdown",
     "gemm_select_path", "gemm_split_parts", "gemm_quantization", "gemm_version", "sgemm", "bf16gemm",
     "STATUS", "PATHS",
@@ -118,6 +119,8 @@ def load_library(build_if_missing: bool = False):
         lib.gemm_bf16gemm_config.restype = cint
         lib.gemm_get_config.argtypes = [cint, i64, i64, i64, cfg_p, ctypes.POINTER(cint)]
         lib.gemm_get_config.restype = cint
+        lib.gemm_get_model_config.argtypes = [cint, i64, i64, i64, cfg_p]
+        lib.gemm_get_model_config.restype = cint
         lib.gemm_status_string.argtypes = [cint]
         lib.gemm_status_string.restype = ctypes.c_char_p
         lib.gemm_check_device_error.argtypes = [vp]
@@ -208,6 +211,16 @@ def gemm_get_config(is_bf16, M, N, K):
         raise GemmError(st, "gemm_get_config")
     names = {v: k for k, v in KERNELS.items()}
     return {"kernel": names[c.kernel], "split": c.split, "group_m": c.group_m}, bool(t.value)
+
+
+def gemm_get_model_config(is_bf16, M, N, K):
+    """The configuration the cost model alone chooses (ignoring the sweep's table)."""
+    c = GemmConfig()
+    st = load_library().gemm_get_model_config(int(bool(is_bf16)), M, N, K, ctypes.byref(c))
+    if st != 0:
+        raise GemmError(st, "gemm_get_model_config")
+    names = {v: k for k, v in KERNELS.items()}
+    return {"kernel": names[c.kernel], "split": c.split, "group_m": c.group_m}
 
 
 def gemm_status_string(status: int) -> str:

@@ -254,10 +254,10 @@ bool config_fields_valid(const gemm_config_t* c, bool bf16) {
 // shape's class (on the GPU it was measured on), then every non-zero field of
 // `user` on top.  Fields left 0 are decided by the planners (cost model).
 TileConfig resolve_config(bool bf16, int64_t M, int64_t N, int64_t K, int num_sms,
-                          const gemm_config_t* user, bool* from_table) {
+                          const gemm_config_t* user, bool* from_table, bool use_table = true) {
   TileConfig c{GEMM_KERNEL_AUTO, 0, 0};
   bool table = false;
-  if (num_sms == kTunedSms) {
+  if (use_table && num_sms == kTunedSms) {
     const int lm = ceil_log2(M), ln = ceil_log2(N), lk = ceil_log2(K);
     for (const TunedEntry& e : kTuned) {
       if (e.is_bf16 < 0) break;
@@ -668,8 +668,8 @@ gemm_status_t gemm_bf16gemm_config(int64_t M, int64_t N, int64_t K, float alpha,
   return bf16gemm_impl(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, cfg, stream);
 }
 
-gemm_status_t gemm_get_config(int is_bf16, int64_t M, int64_t N, int64_t K, gemm_config_t* out,
-                              int* from_table) {
+static gemm_status_t get_config(int is_bf16, int64_t M, int64_t N, int64_t K, gemm_config_t* out,
+                                int* from_table, bool use_table) {
   if (out == nullptr || M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
     return GEMM_ERR_INVALID_VALUE;
   gemm_status_t s;
@@ -679,7 +679,8 @@ gemm_status_t gemm_get_config(int is_bf16, int64_t M, int64_t N, int64_t K, gemm
   if (from_table != nullptr) *from_table = 0;
   if (is_bf16 && M <= kDecBM) return GEMM_OK;  // the decode kernel plans itself
   bool table = false;
-  const TileConfig tc = resolve_config(is_bf16 != 0, M, N, K, st->num_sms, nullptr, &table);
+  const TileConfig tc =
+      resolve_config(is_bf16 != 0, M, N, K, st->num_sms, nullptr, &table, use_table);
   const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
   if (is_bf16) {
     const TcPlan pl = tc_plan(m, n, k, st->num_sms, &tc);
@@ -692,6 +693,16 @@ gemm_status_t gemm_get_config(int is_bf16, int64_t M, int64_t N, int64_t K, gemm
   }
   if (from_table != nullptr) *from_table = table ? 1 : 0;
   return GEMM_OK;
+}
+
+gemm_status_t gemm_get_config(int is_bf16, int64_t M, int64_t N, int64_t K, gemm_config_t* out,
+                              int* from_table) {
+  return get_config(is_bf16, M, N, K, out, from_table, true);
+}
+
+gemm_status_t gemm_get_model_config(int is_bf16, int64_t M, int64_t N, int64_t K,
+                                    gemm_config_t* out) {
+  return get_config(is_bf16, M, N, K, out, nullptr, false);
 }
 
 gemm_status_t gemm_bf16gemm_fused(int64_t M, int64_t N, int64_t K, float alpha, const void* A,

@@ -277,7 +277,7 @@ __device__ __forceinline__ void compute_stage_x2(const uint8_t* sA, const uint8_
   }
 }
 
-// C = alpha * acc + beta * C for the thread's 8 x 8 micro-tile.// C = alpha * acc + beta * C for the thread's 8 x 8 micro-tile.  For each
+// C = alpha * acc + beta * C for the thread's 8 x 8 micro-tile.  For each
 // 4-column half the old values of all 8 rows are loaded before any store, so
 // the loads overlap; interleaved load/store pairs to possibly aliasing rows
 // would serialise a memory round trip per row.

@@ -371,6 +371,14 @@ gemm_status_t gemm_get_config(int is_bf16, int64_t M, int64_t N, int64_t K,
                               gemm_config_t *out, int *from_table);
 
 /*
+ * gemm_get_model_config -- as gemm_get_config, but the configuration the
+ * cost model alone chooses, ignoring the sweep's table (the baseline the
+ * sweep measures table entries against).
+ */
+gemm_status_t gemm_get_model_config(int is_bf16, int64_t M, int64_t N, int64_t K,
+                                    gemm_config_t *out);
+
+/*
  * Tile and wave quantization of a launch ("A GEMM Kernel, Step by Step",
  * "The fringe and the last wave"; "Tiled matrix multiplication",
  * "Complexity and constants", wave quantization).

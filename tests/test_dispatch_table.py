@@ -58,6 +58,12 @@ def test_choose_needs_the_margin():
     assert [r["M"] for r in chosen] == [512]
 
 
+def test_choose_skips_the_models_own_choice():
+    r = _result(512, 1.0, 0.9)
+    r["auto"] = dict(r["best"])       # the model already picks the best
+    assert tune.choose([r], 0.03) == []
+
+
 def test_table_writer_round_trips():
     text = tune.table_lines([_result(512, 1.0, 0.9), _result(300, 2.0, 1.0, is_bf16=0)], 152,
                             "GPU", "2026-01-01")
