@@ -129,8 +129,8 @@ struct SimtTraits {
   // Per-thread register split between the two compute warpgroups and the
   // producer warpgroup; producers that widen bf16 keep more registers.
   static constexpr bool kConvert = (MODE_A == kLoadConvertBf16) || (MODE_B == kLoadConvertBf16);
-  static constexpr int kProducerRegs = kConvert ? 96 : 56;
-  static constexpr int kComputeRegs = kConvert ? 200 : 224;
+  static constexpr int kProducerRegs = kConvert ? 72 : 56;
+  static constexpr int kComputeRegs = kConvert ? 216 : 224;
   static_assert(256 * kComputeRegs + 128 * kProducerRegs <= 384 * kLaunchRegs,
                 "register split exceeds the launch allocation");
   static constexpr uint32_t kTmaBytes =
@@ -172,9 +172,11 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint16_t h) {
 }
 
 // bf16 A slice widened to fp32 (exact), same layout as the fp32 A slice.
+// Parts stay rolled: each issues its 8 loads before its 8 stores, and the
+// producer keeps few registers (the compute warps hold the rest).
 __device__ __forceinline__ void load_a_bf16(uint8_t* sA, const uint16_t* A, int64_t lda, int M,
                                             int K, int m0, int k0, int ptid) {
-#pragma unroll
+#pragma unroll 1
   for (int part = 0; part < 4; ++part) {
     uint16_t v[8];
 #pragma unroll
@@ -195,7 +197,7 @@ __device__ __forceinline__ void load_a_bf16(uint8_t* sA, const uint16_t* A, int6
 
 __device__ __forceinline__ void load_b_bf16(uint8_t* sB, const uint16_t* B, int64_t ldb, int N,
                                             int K, int n0, int k0, int ptid) {
-#pragma unroll
+#pragma unroll 1
   for (int part = 0; part < 4; ++part) {
     uint16_t v[8];
 #pragma unroll
@@ -496,13 +498,18 @@ __global__ void __launch_bounds__(SimtTraits<MODE_A, MODE_B>::kThreads, 1)
       for (int i = 0; i < 8; ++i)
 #pragma unroll
         for (int j = 0; j < 8; ++j) sum[i][j] = 0.0f;
+      // Parts are added in part order.  The variants whose producers widen
+      // bf16 leave the compute warps fewer registers: there this thread's own
+      // partial is read back from the workspace like the others (same
+      // values, same order) so that its accumulators need not stay live;
+      // elsewhere it comes from the accumulators, one round trip fewer.
       for (int part = 0; part < p.split; ++part) {
         const float* src = p.ws + (static_cast<int64_t>(w.split_tile * p.split + part) *
                                        kComputeThreads + ctid) * 64;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           float v[8];
-          if (part == w.part) {
+          if (!T::kConvert && part == w.part) {
 #pragma unroll
             for (int j = 0; j < 8; ++j) v[j] = acc[i][j];
           } else {
