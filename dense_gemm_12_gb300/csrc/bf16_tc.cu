@@ -440,6 +440,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = tail->tmem_base;
+  // Launched with programmatic stream serialization: everything above touches
+  // no global memory and may overlap the previous kernel's last CTAs; every
+  // global access below follows its completion.
+  grid_dependency_wait();
+  if (threadIdx.x == 0) grid_launch_dependents();
 
   if (warp == 0) {
     // -------------------------------------------------------- TMA producer
@@ -650,6 +655,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync();
   tc_fence_after_sync();
   const uint32_t tmem_base = tail->tmem_base;
+  // Launched with programmatic stream serialization: everything above touches
+  // no global memory and may overlap the previous kernel's last CTAs; every
+  // global access below follows its completion.
+  grid_dependency_wait();
+  if (threadIdx.x == 0) grid_launch_dependents();
 
   if (warp == 0) {
     // -------------------------------------------------------- TMA producer
@@ -863,17 +873,19 @@ cudaError_t launch_tc_bf16(const TcArgs& a, const TcPlan& plan, const CUtensorMa
                                          static_cast<int>(kPairSmemBytes));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = dim3(plan.grid);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kPairSmemBytes;
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     e = cudaLaunchKernelEx(&cfg, kernel, a, *tmA, *tmB);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
@@ -882,7 +894,18 @@ cudaError_t launch_tc_bf16(const TcArgs& a, const TcPlan& plan, const CUtensorMa
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
-  kernel<<<plan.grid, kThreads, kSmemBytes, stream>>>(a, *tmA, *tmB);
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(plan.grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kernel, a, *tmA, *tmB);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -100,15 +100,20 @@ def _run(torch, g, is_bf16, M, N, K, tensors, cfg, stream):
 
 
 def _time(torch, g, is_bf16, M, N, K, tensors, cfg, stream, reps):
+    """Milliseconds per launch of `reps` launches queued back to back between two
+    events (per-launch events would time the host's launch latency too on
+    short kernels, and leave nothing for launches to overlap with)."""
     for _ in range(2):
         _run(torch, g, is_bf16, M, N, K, tensors, cfg, stream)
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * reps)]
-    for i in range(reps):
-        ev[2 * i].record(stream)
-        _run(torch, g, is_bf16, M, N, K, tensors, cfg, stream)
-        ev[2 * i + 1].record(stream)
     torch.cuda.synchronize()
-    return statistics.median(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(reps))
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        _run(torch, g, is_bf16, M, N, K, tensors, cfg, stream)
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps
 
 
 def sweep_shape(torch, g, is_bf16, M, N, K, stream, reps=5, confirm_reps=20):
@@ -164,7 +169,7 @@ def summary_lines(results, chosen, gpu, num_sms, command):
              "Per class (ceil(log2) of M, N, K), one representative shape; model = "
              "the cost model's choice without the table (split of the last round, pair "
              "kernel for bf16 M > 128, raster groups of 8); best = fastest pinned "
-             "configuration; both re-timed in turn (4 x 5 launches, median).  Entries "
+             "configuration; both re-timed in turn (4 x 5 back-to-back launches, median).  Entries "
              "marked `table` beat the model by more than the margin and were written "
              "to `csrc/dispatch_table.inc`.", "",
              "| type | M x N x K | model (kernel, split, group) | ms | TFLOP/s | best | ms "
