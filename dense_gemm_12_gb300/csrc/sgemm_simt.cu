@@ -380,12 +380,17 @@ __global__ void __launch_bounds__(SimtTraits<MODE_A, MODE_B>::kThreads, 1)
   if (MODE_B == kLoadTma && threadIdx.x == kComputeThreads) tma_prefetch_desc(&tmB);
   __syncthreads();
   volatile int* abort_flag = &tail->abort_flag;
+  // Launched with programmatic stream serialization: the set-up above touches
+  // no global memory and may overlap the previous kernel's last CTAs; both
+  // roles wait for its completion (grid_dependency_wait) before their first
+  // global access.
 
   if (warp >= kComputeWarps) {
     // ------------------------------------------------------------ producers
     // Hand registers to the compute warpgroups (see SimtTraits: the split
     // never exceeds the 384 x 168 the block is launched with).
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(T::kProducerRegs));
+    grid_dependency_wait();
     const int ptid = threadIdx.x - kComputeThreads;
     const bool tma_issuer = (ptid == 0) && T::kAnyTma;
     if (!T::kAnyGeneric && ptid != 0) return;
@@ -439,6 +444,8 @@ __global__ void __launch_bounds__(SimtTraits<MODE_A, MODE_B>::kThreads, 1)
 
   // -------------------------------------------------------------- compute
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(T::kComputeRegs));
+  grid_dependency_wait();
+  if (threadIdx.x == 0) grid_launch_dependents();
   const int wm = warp >> 1, wn = warp & 1;
   const int rg = lane >> 3, cg = lane & 7;
   const int ctid = threadIdx.x;  // 0..255
@@ -541,7 +548,18 @@ cudaError_t launch_variant(const SimtArgs& a, const CUtensorMap* tmA, const CUte
   const int num_items = a.full_items + (tiles - a.full_items) * a.split;
   const int grid = num_items < num_sms ? num_items : num_sms;
   CUtensorMap dummy{};
-  kernel<<<grid, T::kThreads, kSmemBytes, stream>>>(a, tmA ? *tmA : dummy, tmB ? *tmB : dummy);
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(T::kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kernel, a, tmA ? *tmA : dummy, tmB ? *tmB : dummy);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
