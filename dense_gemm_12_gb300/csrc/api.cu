@@ -802,12 +802,17 @@ gemm_status_t gemm_check_device_error(void* stream) {
   if (word == 0) return GEMM_OK;
   const uint32_t zero = 0;
   cudaMemcpy(st->err_word, &zero, sizeof zero, cudaMemcpyHostToDevice);
-  // A decode launch that gave up may have left arrival counters non-zero.
+  // A split launch that gave up may have left arrival counters non-zero, on
+  // whichever stream it ran (the word does not say): let every stream's
+  // work finish, then reset them all -- clearing counters under a split
+  // kernel still running on another stream would break that kernel.
   {
     std::lock_guard<std::mutex> lock(st->ws_mutex);
+    cudaDeviceSynchronize();
     for (auto& kv : st->scratch)
       if (kv.second.counters)
         cudaMemset(kv.second.counters, 0, kv.second.counter_count * sizeof(uint32_t));
+    cudaDeviceSynchronize();
   }
   cudaGetLastError();
   return GEMM_ERR_DEVICE_TIMEOUT;

@@ -259,7 +259,11 @@ const char *gemm_status_string(gemm_status_t status);
  * current device's error word, which the kernels set when one of their
  * bounded waits (on an mbarrier or on another CTA) runs out.  Returns
  * GEMM_ERR_DEVICE_TIMEOUT if it was set, GEMM_ERR_LAUNCH if the
- * synchronisation itself failed, else GEMM_OK.
+ * synchronisation itself failed, else GEMM_OK.  When the word was set, a
+ * launch that gave up may have left split-K arrival counters non-zero on
+ * whichever stream it ran: the call then synchronises the whole device
+ * (every stream's GEMMs finish first) and resets the counters of every
+ * stream's scratch, so that later split launches start clean.
  */
 gemm_status_t gemm_check_device_error(void *stream);
 
