@@ -23,7 +23,7 @@ __all__ = [
     "gemm_bf16gemm_decode_static", "gemm_bf16gemm_epilogue", "bf16gemm_epilogue", "ACT", "OUT",
     "gemm_bf16gemm_fused", "bf16gemm_fused", "GemmOutput",
     "gemm_sgemm_config", "gemm_bf16gemm_config", "gemm_get_config", "gemm_get_model_config",
-    "GemmConfig", "KERNELS",
+    "GemmConfig", "KERNELS", "SPLIT_STREAM",
     "gemm_status_string", "gemm_check_device_error", "gemm_shutdown",
     "gemm_select_path", "gemm_split_parts", "gemm_quantization", "gemm_version", "sgemm", "bf16gemm",
     "STATUS", "PATHS",
@@ -64,7 +64,9 @@ class GemmConfig(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int), ("split", ctypes.c_int), ("group_m", ctypes.c_int)]
 
 
-KERNELS = {"auto": 0, "single_cta": 1, "cta_pair": 2}
+KERNELS = {"auto": 0, "single_cta": 1, "cta_pair": 2, "wide": 3}
+# gemm_config_t.split value for the stream-K tail (fp32 only): GEMM_SPLIT_STREAM.
+SPLIT_STREAM = -1
 
 
 class _Quantization(ctypes.Structure):
@@ -182,8 +184,9 @@ def _config(cfg):
     if isinstance(cfg, GemmConfig):
         return ctypes.byref(cfg)
     kernel = cfg.get("kernel", 0)
+    split = cfg.get("split", 0)
     c = GemmConfig(KERNELS[kernel] if isinstance(kernel, str) else int(kernel),
-                   int(cfg.get("split", 0)), int(cfg.get("group_m", 0)))
+                   SPLIT_STREAM if split == "stream" else int(split), int(cfg.get("group_m", 0)))
     return ctypes.byref(c)
 
 

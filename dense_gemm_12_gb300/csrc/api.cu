@@ -246,8 +246,10 @@ int ceil_log2(int64_t x) {
 bool config_fields_valid(const gemm_config_t* c, bool bf16) {
   if (c == nullptr) return true;
   const bool kernel_ok = c->kernel == GEMM_KERNEL_AUTO || c->kernel == GEMM_KERNEL_SINGLE_CTA ||
-                         (bf16 && c->kernel == GEMM_KERNEL_CTA_PAIR);
-  return kernel_ok && c->split >= 0 && c->split <= 8 && c->group_m >= 0 && c->group_m <= 64;
+                         (bf16 && c->kernel == GEMM_KERNEL_CTA_PAIR) ||
+                         (!bf16 && c->kernel == GEMM_KERNEL_WIDE);
+  const bool split_ok = (c->split >= 0 && c->split <= 8) || (!bf16 && c->split == GEMM_SPLIT_STREAM);
+  return kernel_ok && split_ok && c->group_m >= 0 && c->group_m <= 64;
 }
 
 // The tile-kernel configuration of one call: the sweep's table entry for the
@@ -281,17 +283,15 @@ TileConfig resolve_config(bool bf16, int64_t M, int64_t N, int64_t K, int num_sm
 
 namespace {
 
-gemm_status_t plan_simt(DeviceState* st, cudaStream_t cs, SimtArgs& a, const TileConfig& tc,
+gemm_status_t plan_simt(DeviceState* st, cudaStream_t cs, SimtArgs& a, const SimtPlan& pl,
                         std::unique_lock<std::mutex>& lock) {
-  const int tiles = ((a.M + kSimtBM - 1) / kSimtBM) * ((a.N + kSimtBN - 1) / kSimtBN);
-  const int num_kb = (a.K + kSimtBK - 1) / kSimtBK;
-  const SimtPlan pl = simt_plan(tiles, num_kb, st->num_sms, &tc);
   a.full_items = pl.full_items;
   a.split = pl.split;
+  a.sk_workers = pl.sk_workers;
   a.group_m = pl.group_m;
   a.ws = nullptr;
   a.counters = nullptr;
-  if (pl.split == 1) return GEMM_OK;
+  if (pl.split == 1 && pl.sk_workers == 0) return GEMM_OK;
   lock.lock();
   Scratch* sc = nullptr;
   const gemm_status_t s = ensure_scratch(*st, cs, pl.ws_floats, pl.counters, &sc);
@@ -446,8 +446,7 @@ int gemm_split_parts(int is_bf16, int64_t M, int64_t N, int64_t K) {
     if (M <= kDecBM) return 1;
     return tc_plan(m, n, k, st->num_sms, &tc).split;
   }
-  const int tiles = ((m + kSimtBM - 1) / kSimtBM) * ((n + kSimtBN - 1) / kSimtBN);
-  return simt_plan(tiles, (k + kSimtBK - 1) / kSimtBK, st->num_sms, &tc).split;
+  return simt_plan_max_parts(simt_plan(m, n, k, st->num_sms, &tc, true), m, n, k);
 }
 
 gemm_status_t gemm_quantization(int64_t M, int64_t N, int64_t BM, int64_t BN, int64_t num_sms,
@@ -509,21 +508,30 @@ static gemm_status_t sgemm_impl(int64_t M, int64_t N, int64_t K, float alpha, co
   a.c_vec4 = c_vec4_ok(C, ldc);
   a.err = st->err_word;
   const TileConfig tc = resolve_config(false, M, N, K, st->num_sms, cfg, nullptr);
-  std::unique_lock<std::mutex> lock(st->ws_mutex, std::defer_lock);
-  s = plan_simt(st, cs, a, tc, lock);
-  if (s != GEMM_OK) return s;
   CUtensorMap tmA, tmB;
   LoadMode ma = kLoadCpAsyncF32, mb = kLoadCpAsyncF32;
   if (tma_ok(A, lda, 4) &&
       encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, A, K, M, lda, kSimtBK, kSimtBM,
                 CU_TENSOR_MAP_SWIZZLE_128B))
     ma = kLoadTma;
-  if (tma_ok(B, ldb, 4) &&
-      encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, B, N, K, ldb, kSimtBN, kSimtBK,
-                CU_TENSOR_MAP_SWIZZLE_NONE))
-    mb = kLoadTma;
-  return from_cuda(launch_simt(a, ma, mb, ma == kLoadTma ? &tmA : nullptr,
-                               mb == kLoadTma ? &tmB : nullptr, st->num_sms, cs));
+  // The wide tile runs only with both operands on TMA; its B box is 256 wide.
+  SimtPlan pl = simt_plan(a.M, a.N, a.K, st->num_sms, &tc, ma == kLoadTma && tma_ok(B, ldb, 4));
+  if (tma_ok(B, ldb, 4)) {
+    if (encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, B, N, K, ldb, simt_bn(pl.wide),
+                  kSimtBK, CU_TENSOR_MAP_SWIZZLE_NONE)) {
+      mb = kLoadTma;
+    } else if (pl.wide) {
+      pl = simt_plan(a.M, a.N, a.K, st->num_sms, &tc, false);
+      if (encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, B, N, K, ldb, simt_bn(false),
+                    kSimtBK, CU_TENSOR_MAP_SWIZZLE_NONE))
+        mb = kLoadTma;
+    }
+  }
+  std::unique_lock<std::mutex> lock(st->ws_mutex, std::defer_lock);
+  s = plan_simt(st, cs, a, pl, lock);
+  if (s != GEMM_OK) return s;
+  return from_cuda(launch_simt(a, pl, ma, mb, ma == kLoadTma ? &tmA : nullptr,
+                               mb == kLoadTma ? &tmB : nullptr, cs));
 }
 
 gemm_status_t gemm_sgemm(int64_t M, int64_t N, int64_t K, float alpha, const float* A,
@@ -646,11 +654,12 @@ static gemm_status_t bf16gemm_impl(int64_t M, int64_t N, int64_t K, float alpha,
     // the CUDA-core kernel's table entries are the fp32 ones
     gemm_config_t simt_cfg{GEMM_KERNEL_AUTO, cfg ? cfg->split : 0, cfg ? cfg->group_m : 0};
     const TileConfig tc = resolve_config(false, M, N, K, st->num_sms, &simt_cfg, nullptr);
+    const SimtPlan pl = simt_plan(a.M, a.N, a.K, st->num_sms, &tc, false);
     std::unique_lock<std::mutex> lock(st->ws_mutex, std::defer_lock);
-    s = plan_simt(st, cs, a, tc, lock);
+    s = plan_simt(st, cs, a, pl, lock);
     if (s != GEMM_OK) return s;
-    return from_cuda(launch_simt(a, kLoadConvertBf16, kLoadConvertBf16, nullptr, nullptr,
-                                 st->num_sms, cs));
+    return from_cuda(launch_simt(a, pl, kLoadConvertBf16, kLoadConvertBf16, nullptr, nullptr,
+                                 cs));
   }
   return run_bf16_tensor_core(st, path, M, N, K, A, lda, B, ldb,
                               plain_epilogue(alpha, beta, C, ldc), cs, cfg);
@@ -687,9 +696,9 @@ static gemm_status_t get_config(int is_bf16, int64_t M, int64_t N, int64_t K, ge
     *out = gemm_config_t{pl.pair ? GEMM_KERNEL_CTA_PAIR : GEMM_KERNEL_SINGLE_CTA, pl.split,
                          pl.group_m};
   } else {
-    const int tiles = ((m + kSimtBM - 1) / kSimtBM) * ((n + kSimtBN - 1) / kSimtBN);
-    const SimtPlan pl = simt_plan(tiles, (k + kSimtBK - 1) / kSimtBK, st->num_sms, &tc);
-    *out = gemm_config_t{GEMM_KERNEL_SINGLE_CTA, pl.split, pl.group_m};
+    const SimtPlan pl = simt_plan(m, n, k, st->num_sms, &tc, true);
+    *out = gemm_config_t{pl.wide ? GEMM_KERNEL_WIDE : GEMM_KERNEL_SINGLE_CTA,
+                         pl.sk_workers > 0 ? GEMM_SPLIT_STREAM : pl.split, pl.group_m};
   }
   if (from_table != nullptr) *from_table = table ? 1 : 0;
   return GEMM_OK;

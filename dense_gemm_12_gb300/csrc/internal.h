@@ -29,11 +29,15 @@ struct SimtArgs {
   int c_vec4;      // 1 if C rows may be written as aligned float4
   uint32_t* err;   // device error word
   // Work plan (see simt_plan): items [0, full_items) are whole tiles in
-  // raster order; every later tile is cut into `split` k-ranges whose partial
-  // sums meet in `ws` (split x 64 KB per tile) and are added by the last of
-  // them to arrive on the tile's counter in `counters` (zero between launches).
+  // raster order.  The later ("tail") tiles are either cut into `split`
+  // equal k-ranges each (sk_workers == 0), or, with sk_workers = G > 0, their
+  // k-blocks taken together are dealt out evenly to G workers (stream-K, see
+  // sk_range).  Partial sums meet in `ws` (one tile of floats per part) and
+  // are added, in k order, by the last part to arrive on the tile's counter
+  // in `counters` (zero between launches).
   int full_items;
   int split;
+  int sk_workers;
   float* ws;
   uint32_t* counters;
   int group_m;     // raster group height in tile rows
@@ -42,33 +46,53 @@ struct SimtArgs {
 // A launch configuration of the tile kernels: gemm_config_t of the C ABI
 // with every field resolved (no "auto" values).
 struct TileConfig {
-  int kernel;    // GEMM_KERNEL_SINGLE_CTA or GEMM_KERNEL_CTA_PAIR
-  int split;     // k-ranges per item of the last round, 1..8
+  int kernel;    // GEMM_KERNEL_SINGLE_CTA, GEMM_KERNEL_CTA_PAIR or GEMM_KERNEL_WIDE
+  int split;     // k-ranges per item of the last round, 1..8, or GEMM_SPLIT_STREAM
   int group_m;   // raster group height, 1..64
 };
 
-// Work plan of the CUDA-core kernel for tiles output tiles, num_kb k-blocks
-// and up to num_sms persistent CTAs: how many tiles run whole, how the rest
-// are split along k, and the grid.  `fixed` pins the split (and carries the
-// group height); nullptr lets the cost model choose.
+// Work plan of the CUDA-core kernel for an M x N x K problem on up to
+// num_sms persistent CTAs: the tile width, how many tiles run whole, how the
+// rest are cut along k, and the grid.  `fixed` pins the kernel (tile width),
+// the split (or stream-K) and the group height; nullptr or zero fields let
+// the cost model choose.  allow_wide = false keeps 128-wide tiles.
 struct SimtPlan {
+  bool wide;           // 128 x 256 tiles (else 128 x 128)
   int full_items;
   int split;
+  int sk_workers;      // > 0: stream-K tail over this many workers
   int grid;
   int group_m;
   int64_t ws_floats;   // workspace the split tiles need
   int64_t counters;    // counters the split tiles need
 };
-SimtPlan simt_plan(int tiles, int num_kb, int num_sms, const TileConfig* fixed);
+SimtPlan simt_plan(int M, int N, int K, int num_sms, const TileConfig* fixed, bool allow_wide);
+// Largest number of parts any tail tile of the plan is cut into (1 = none).
+int simt_plan_max_parts(const SimtPlan& pl, int M, int N, int K);
 
-// CUDA-core (FFMA) GEMM: 128 x 128 block tiles, warp tiles 32 x 64, 8 x 8
-// register micro-tiles.  tmA / tmB are used only for operands in kLoadTma mode.
-cudaError_t launch_simt(const SimtArgs& a, LoadMode mode_a, LoadMode mode_b,
-                        const CUtensorMap* tmA, const CUtensorMap* tmB, int num_sms,
+// CUDA-core (FFMA) GEMM: 128 x 128 block tiles (warp tiles 32 x 64, 8 x 8
+// register micro-tiles) or 128 x 256 (warp tiles 32 x 128, 8 x 16), as
+// planned.  tmA / tmB are used only for operands in kLoadTma mode; tmB's box
+// is simt_bn(plan.wide) columns wide.
+cudaError_t launch_simt(const SimtArgs& a, const SimtPlan& plan, LoadMode mode_a,
+                        LoadMode mode_b, const CUtensorMap* tmA, const CUtensorMap* tmB,
                         cudaStream_t stream);
 
 // Tile geometry of the CUDA-core kernel (also used by the launch planner).
-constexpr int kSimtBM = 128, kSimtBN = 128, kSimtBK = 32;
+constexpr int kSimtBM = 128, kSimtBK = 32;
+constexpr int simt_bn(bool wide) { return wide ? 256 : 128; }
+
+// Stream-K tail: the tail's W = tail_tiles x num_kb k-blocks, taken tile after
+// tile, are dealt to G workers in contiguous ranges [lo(j), lo(j + 1)) with
+// lo(j) = floor(j W / G).  With G >= tail_tiles a range is at most one tile
+// long, so it touches one or two tiles: its first segment (s = 0) lies in
+// tile lo(j) / num_kb, its second (s = 1), if any, in the next tile.  The
+// partial sums of worker j's segment s go to workspace slot 2 j + s.
+__host__ __device__ inline int64_t sk_lo(int64_t j, int64_t W, int64_t G) { return j * W / G; }
+// The worker whose range holds k-block x of the tail: the largest j with lo(j) <= x.
+__host__ __device__ inline int64_t sk_worker(int64_t x, int64_t W, int64_t G) {
+  return ((x + 1) * G - 1) / W;
+}
 
 // Number of k-parts S (1 = none) into which the items of the last round are
 // cut when `items` equal work items of num_kb k-blocks run on `workers`

@@ -3,23 +3,30 @@
 // Structure (the register-tiled scheme of "Tiled matrix multiplication",
 // "How it works", and of "A GEMM Kernel, Step by Step", rungs four to six and
 // "The last rung", rebuilt for sm_103a):
-//   * persistent CTAs walk 128 x 128 output tiles in a grouped raster order so
-//     CTAs running at the same time share A row-panels and B column-panels in
-//     L2 ("Tiled matrix multiplication", "Complexity and constants");
-//   * a producer warp streams 128 x 32 slices of A and 32 x 128 slices of B
+//   * persistent CTAs walk 128 x BN output tiles (BN = 128 or 256) in a
+//     grouped raster order so CTAs running at the same time share A
+//     row-panels and B column-panels in L2 ("Tiled matrix multiplication",
+//     "Complexity and constants");
+//   * a producer warp streams 128 x 32 slices of A and 32 x BN slices of B
 //     into a STAGES-deep shared-memory ring with TMA (cp.async.bulk.tensor),
 //     completion tracked by full/empty mbarriers -- the multi-buffered copy
 //     pipeline the pages name for Hopper, which also frees the compute warps
 //     from issuing any load instruction to global memory;
-//   * 8 compute warps each own a 32 x 64 warp tile, every lane an 8 x 8
-//     register micro-tile; per k the lane reads 8 A values and 8 B values from
-//     shared memory with 128-bit loads and issues 64 FFMAs;
+//   * 8 compute warps each own a 32 x BN/2 warp tile, every lane an 8 x BN/16
+//     register micro-tile; per k the lane reads 8 A values and BN/16 B values
+//     from shared memory with 128-bit loads and issues 8 x BN/16 FFMAs.  The
+//     wide tile (8 x 16 per lane) reads fewer shared-memory bytes per FMA;
+//     the narrow one gives twice as many tiles for small problems;
 //   * the A slice stays k-contiguous (TMA cannot transpose fp32); the 128-byte
 //     TMA swizzle plus a lane->row map of stride 4 keeps the 128-bit reads of
 //     four k values at once free of bank conflicts, which replaces the pages'
 //     transposed-and-padded A tile;
 //   * TMA zero-fills rows and columns past M, N, K, so ragged edges need no
-//     predicate in the hot loop; the epilogue applies alpha/beta and masks.
+//     predicate in the hot loop; the epilogue applies alpha/beta and masks;
+//   * the tiles of the last, partial round are cut along k -- into equal
+//     parts, or (stream-K) by dealing their k-blocks out evenly to all CTAs --
+//     so that the last round keeps every SM busy ("A GEMM Kernel, Step by
+//     Step", "The fringe and the last wave" and "What is left").
 // Operands TMA cannot describe (unaligned base or pitch, or bf16 to be widened)
 // are loaded by four producer warps with cp.async / plain loads into the same
 // shared-memory layout, so the compute warps are identical in every variant.
@@ -33,7 +40,7 @@
 namespace g12 {
 namespace {
 
-constexpr int BM = kSimtBM, BN = kSimtBN, BK = kSimtBK;
+constexpr int BM = kSimtBM, BK = kSimtBK;
 #ifndef G12_SIMT_KQ_UNROLL
 #define G12_SIMT_KQ_UNROLL 8
 #endif
@@ -47,8 +54,17 @@ constexpr int kLaunchRegs = 168;
 constexpr int kComputeWarps = 8;
 constexpr int kComputeThreads = kComputeWarps * 32;
 constexpr int kStageBytesA = BM * BK * 4;  // 16 KB, rows of 128 B, 128-B swizzled
-constexpr int kStageBytesB = BK * BN * 4;  // 16 KB, rows of 512 B, not swizzled
-constexpr int kStageBytes = kStageBytesA + kStageBytesB;
+
+// Geometry that depends on the tile width BN.
+template <int BN>
+struct Geom {
+  static_assert(BN == 128 || BN == 256, "tile width");
+  static constexpr int kColGroups = BN / 64;            // 4-column groups per lane
+  static constexpr int kCols = 4 * kColGroups;          // columns per lane
+  static constexpr int kAcc = 8 * kCols;                // accumulators per lane
+  static constexpr int kStageBytesB = BK * BN * 4;      // rows of BN x 4 B, not swizzled
+  static constexpr int kStageBytes = kStageBytesA + kStageBytesB;
+};
 
 struct __align__(8) SimtSmemTail {
   uint64_t full[STAGES];
@@ -57,16 +73,20 @@ struct __align__(8) SimtSmemTail {
   int last_flag;
 };
 
+template <int BN>
+constexpr size_t smem_bytes() {
+  return 1024 /*alignment slack*/ + STAGES * Geom<BN>::kStageBytes + sizeof(SimtSmemTail);
+}
+
 // Tile and k-range of work item i (see SimtArgs).
 struct SimtItem {
   int tm, tn;
-  int kb0, kb1;    // k-blocks [kb0, kb1)
-  int split_tile;  // -1 for a whole tile, else the index of the split tile
-  int part;        // which of the split k-ranges
+  int kb0, kb1;    // k-blocks [kb0, kb1); empty items (kb0 == kb1) are skipped
+  int tail_tile;   // -1 for a whole tile, else the index of the tail tile
+  int part;        // this item's place among the tile's parts, in k order
+  int parts;       // number of parts of the tile
+  int slot;        // workspace slot of this part's partial sums
 };
-
-constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + STAGES * kStageBytes +
-                              sizeof(SimtSmemTail);
 
 // Grouped raster: tiles walk column by column through groups of group_m
 // tile rows, so neighbouring CTAs share A row panels and B column panels in L2.
@@ -81,23 +101,65 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
   tn = local / rows;
 }
 
+// Workspace slot of part `idx` (k order) of tail tile t.
+__device__ __forceinline__ int part_slot(const SimtArgs& p, int t, int idx, int num_kb,
+                                         int64_t W) {
+  if (p.sk_workers == 0) return t * p.split + idx;
+  const int64_t G = p.sk_workers;
+  const int64_t first = sk_worker(static_cast<int64_t>(t) * num_kb, W, G);
+  const int64_t j = first + idx;
+  return static_cast<int>(2 * j + (sk_lo(j, W, G) < static_cast<int64_t>(t) * num_kb ? 1 : 0));
+}
+
 __device__ __forceinline__ SimtItem simt_item(const SimtArgs& p, int i, int tiles_m, int tiles_n,
                                               int num_kb) {
   SimtItem it;
   int tile;
+  it.tail_tile = -1;
+  it.part = 0;
+  it.parts = 1;
+  it.slot = 0;
   if (i < p.full_items) {
     tile = i;
     it.kb0 = 0;
     it.kb1 = num_kb;
-    it.split_tile = -1;
-    it.part = 0;
-  } else {
+  } else if (p.sk_workers == 0) {
     const int j = i - p.full_items;
-    it.split_tile = j / p.split;
-    it.part = j - it.split_tile * p.split;
-    tile = p.full_items + it.split_tile;
+    it.tail_tile = j / p.split;
+    it.part = j - it.tail_tile * p.split;
+    it.parts = p.split;
+    it.slot = j;
+    tile = p.full_items + it.tail_tile;
     it.kb0 = static_cast<int>(static_cast<int64_t>(it.part) * num_kb / p.split);
     it.kb1 = static_cast<int>(static_cast<int64_t>(it.part + 1) * num_kb / p.split);
+  } else {
+    // Stream-K: items full_items + s * gridDim.x + w are segment s of worker w.
+    const int j = i - p.full_items;
+    const int s = j / static_cast<int>(gridDim.x);
+    const int w = j - s * static_cast<int>(gridDim.x);
+    const int64_t G = p.sk_workers;
+    const int64_t W = static_cast<int64_t>(tiles_m * tiles_n - p.full_items) * num_kb;
+    it.kb0 = it.kb1 = 0;
+    it.tm = it.tn = 0;
+    if (w >= G) return it;
+    const int64_t lo = sk_lo(w, W, G), hi = sk_lo(w + 1, W, G);
+    int64_t t = lo / num_kb;
+    int64_t a = lo - t * num_kb, b = min(hi - t * num_kb, static_cast<int64_t>(num_kb));
+    if (s == 1) {
+      if (hi <= (t + 1) * num_kb) return it;
+      ++t;
+      a = 0;
+      b = hi - t * num_kb;
+    }
+    it.tail_tile = static_cast<int>(t);
+    it.kb0 = static_cast<int>(a);
+    it.kb1 = static_cast<int>(b);
+    const int64_t first = sk_worker(t * num_kb, W, G);
+    const int64_t last = sk_worker((t + 1) * num_kb - 1, W, G);
+    it.part = static_cast<int>(w - first);
+    it.parts = static_cast<int>(last - first + 1);
+    it.slot = 2 * w + s;
+    tile = p.full_items + it.tail_tile;
   }
   tile_coords(tile, tiles_m, tiles_n, p.group_m, it.tm, it.tn);
   return it;
@@ -133,8 +195,6 @@ struct SimtTraits {
   static constexpr int kComputeRegs = kConvert ? 216 : 224;
   static_assert(256 * kComputeRegs + 128 * kProducerRegs <= 384 * kLaunchRegs,
                 "register split exceeds the launch allocation");
-  static constexpr uint32_t kTmaBytes =
-      (MODE_A == kLoadTma ? kStageBytesA : 0) + (MODE_B == kLoadTma ? kStageBytesB : 0);
 };
 
 // ------------------------------------------------------------------ loaders
@@ -153,13 +213,14 @@ __device__ __forceinline__ void load_a_cpasync(uint8_t* sA, const float* A, int6
   }
 }
 
-// Generic fp32 B slice: 32 k-rows x 128 n, consecutive threads on consecutive n.
+// Generic fp32 B slice: 32 k-rows x BN n, consecutive threads on consecutive n.
+template <int BN>
 __device__ __forceinline__ void load_b_cpasync(uint8_t* sB, const float* B, int64_t ldb, int N,
                                                int K, int n0, int k0, int ptid) {
 #pragma unroll 8
   for (int q = 0; q < (BK * BN) / 128; ++q) {
     const int e = ptid + q * 128;
-    const int k = e >> 7, n = e & 127;
+    const int k = e / BN, n = e % BN;
     const int gk = k0 + k, gn = n0 + n;
     const bool in = (gk < K) && (gn < N);
     const float* src = in ? (B + static_cast<int64_t>(gk) * ldb + gn) : B;
@@ -177,7 +238,7 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint16_t h) {
 __device__ __forceinline__ void load_a_bf16(uint8_t* sA, const uint16_t* A, int64_t lda, int M,
                                             int K, int m0, int k0, int ptid) {
 #pragma unroll 1
-  for (int part = 0; part < 4; ++part) {
+  for (int part = 0; part < (BM * BK) / 1024; ++part) {
     uint16_t v[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
@@ -195,22 +256,23 @@ __device__ __forceinline__ void load_a_bf16(uint8_t* sA, const uint16_t* A, int6
   }
 }
 
+template <int BN>
 __device__ __forceinline__ void load_b_bf16(uint8_t* sB, const uint16_t* B, int64_t ldb, int N,
                                             int K, int n0, int k0, int ptid) {
 #pragma unroll 1
-  for (int part = 0; part < 4; ++part) {
+  for (int part = 0; part < (BK * BN) / 1024; ++part) {
     uint16_t v[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       const int e = ptid + (part * 8 + q) * 128;
-      const int k = e >> 7, n = e & 127;
+      const int k = e / BN, n = e % BN;
       const int gk = k0 + k, gn = n0 + n;
       v[q] = (gk < K && gn < N) ? __ldg(B + static_cast<int64_t>(gk) * ldb + gn) : uint16_t(0);
     }
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       const int e = ptid + (part * 8 + q) * 128;
-      const int k = e >> 7, n = e & 127;
+      const int k = e / BN, n = e % BN;
       *reinterpret_cast<float*>(sB + (k * BN + n) * 4) = bf16_bits_to_f32(v[q]);
     }
   }
@@ -238,18 +300,21 @@ __device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
 }
 
 // ------------------------------------------------------------------ compute
-// One stage (BK = 32 values of k) of the 8 x 8 outer-product accumulation.
-// Lane layout inside the 32 x 64 warp tile: rg = lane / 8 picks rows
-// {rg, rg+4, ..., rg+28}; cg = lane % 8 picks columns {4cg..4cg+3} and
-// {32+4cg..32+4cg+3}.  A is read four k values at a time (one 128-bit load
-// per row), B one k row at a time as two 128-bit loads.  The accumulators
-// are fp32 pairs: acc2[i][q] holds the thread's columns 2q and 2q+1 of row i,
-// updated with fma.rn.f32x2 (A value duplicated into both halves).
+// One stage (BK = 32 values of k) of the 8 x kCols outer-product
+// accumulation.  Lane layout inside the 32 x BN/2 warp tile: rg = lane / 8
+// picks rows {rg, rg+4, ..., rg+28}; cg = lane % 8 picks the columns
+// {32j + 4cg .. 32j + 4cg + 3}, j < kColGroups.  A is read four k values at a
+// time (one 128-bit load per row), B one k row at a time as kColGroups
+// 128-bit loads.  The accumulators are fp32 pairs: acc2[i][2j + h] holds
+// columns 32j + 4cg + 2h and +1 of row i, updated with fma.rn.f32x2 (the A
+// value duplicated into both halves).
+template <int BN>
 __device__ __forceinline__ void compute_stage_x2(const uint8_t* sA, const uint8_t* sB,
-                                                 uint64_t (&acc2)[8][4], int wm, int wn,
-                                                 int rg, int cg) {
+                                                 uint64_t (&acc2)[8][Geom<BN>::kCols / 2],
+                                                 int wm, int wn, int rg, int cg) {
+  constexpr int kGroups = Geom<BN>::kColGroups;
   const uint8_t* a_row0 = sA + (wm * 32 + rg) * 128;
-  const float* b_base = reinterpret_cast<const float*>(sB) + wn * 64 + cg * 4;
+  const float* b_base = reinterpret_cast<const float*>(sB) + wn * (BN / 2) + cg * 4;
   const int x_even = rg;
   const int x_odd = rg + 4;
 #pragma unroll kKqUnroll
@@ -265,99 +330,122 @@ __device__ __forceinline__ void compute_stage_x2(const uint8_t* sA, const uint8_
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
       const int k = kq * 4 + kk;
-      const ulonglong2 b0 = *reinterpret_cast<const ulonglong2*>(b_base + k * BN);
-      const ulonglong2 b1 = *reinterpret_cast<const ulonglong2*>(b_base + k * BN + 32);
-      const uint64_t bv[4] = {b0.x, b0.y, b1.x, b1.y};
+      uint64_t bv[2 * kGroups];
+#pragma unroll
+      for (int j = 0; j < kGroups; ++j) {
+        const ulonglong2 b = *reinterpret_cast<const ulonglong2*>(b_base + k * BN + 32 * j);
+        bv[2 * j] = b.x;
+        bv[2 * j + 1] = b.y;
+      }
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const float av = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
         const uint64_t a2 = pack2(av, av);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) acc2[i][q] = ffma2(a2, bv[q], acc2[i][q]);
+        for (int q = 0; q < 2 * kGroups; ++q) acc2[i][q] = ffma2(a2, bv[q], acc2[i][q]);
       }
     }
   }
 }
 
-// C = alpha * acc + beta * C for the thread's 8 x 8 micro-tile.  For each
-// 4-column half the old values of all 8 rows are loaded before any store, so
-// the loads overlap; interleaved load/store pairs to possibly aliasing rows
-// would serialise a memory round trip per row.
-__device__ __forceinline__ void epilogue(const SimtArgs& p, const float (&acc)[8][8], int tm,
-                                         int tn, int wm, int wn, int rg, int cg) {
+// C = alpha * acc + beta * C for the thread's 8 x kCols micro-tile, kRows rows
+// at a time: the old values of a chunk's rows are all loaded before any of
+// them is stored, so their round trips overlap (a load issued after a store
+// to a possibly aliasing address would wait for it).  The narrow tile takes
+// all 8 rows at once; the wide tile one row (4 float4) at a time, as more old
+// values next to its 128 accumulators would spill.
+template <int BN>
+__device__ __forceinline__ void epilogue(const SimtArgs& p, const float (&acc)[8][Geom<BN>::kCols],
+                                         int tm, int tn, int wm, int wn, int rg, int cg) {
+  constexpr int kGroups = Geom<BN>::kColGroups;
+  constexpr int kRows = BN == 128 ? 8 : 1;
   const bool read_c = (p.beta != 0.0f);
   const int row0 = tm * BM + wm * 32 + rg;
+  const int col0 = tn * BN + wn * (BN / 2) + cg * 4;
+  const bool vec = p.c_vec4 && col0 + 32 * (kGroups - 1) + 3 < p.N;
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int col = tn * BN + wn * 64 + h * 32 + cg * 4;
-    if (p.c_vec4 && col + 3 < p.N) {
-      float4 old[8];
-      if (read_c) {
+  for (int i0 = 0; i0 < 8; i0 += kRows) {
+    if (vec) {
+      float4 old[kRows][kGroups];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int row = row0 + 4 * i;
-          old[i] = row < p.M ? *reinterpret_cast<const float4*>(
-                                   p.C + static_cast<int64_t>(row) * p.ldc + col)
-                             : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
+      for (int r = 0; r < kRows; ++r) {
+        const int row = row0 + 4 * (i0 + r);
+        const float* c_row = p.C + static_cast<int64_t>(row) * p.ldc + col0;
+#pragma unroll
+        for (int h = 0; h < kGroups; ++h)
+          old[r][h] = (read_c && row < p.M) ? *reinterpret_cast<const float4*>(c_row + 32 * h)
+                                            : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int r = 0; r < kRows; ++r) {
+        const int i = i0 + r;
         const int row = row0 + 4 * i;
         if (row >= p.M) continue;
-        float4 v = make_float4(acc[i][h * 4 + 0], acc[i][h * 4 + 1], acc[i][h * 4 + 2],
-                               acc[i][h * 4 + 3]);
-        if (read_c) {
-          v.x = fmaf(p.alpha, v.x, p.beta * old[i].x);
-          v.y = fmaf(p.alpha, v.y, p.beta * old[i].y);
-          v.z = fmaf(p.alpha, v.z, p.beta * old[i].z);
-          v.w = fmaf(p.alpha, v.w, p.beta * old[i].w);
-        } else {
-          v.x *= p.alpha;
-          v.y *= p.alpha;
-          v.z *= p.alpha;
-          v.w *= p.alpha;
+        float* c_row = p.C + static_cast<int64_t>(row) * p.ldc + col0;
+#pragma unroll
+        for (int h = 0; h < kGroups; ++h) {
+          float4 v = make_float4(acc[i][4 * h], acc[i][4 * h + 1], acc[i][4 * h + 2],
+                                 acc[i][4 * h + 3]);
+          if (read_c) {
+            v.x = fmaf(p.alpha, v.x, p.beta * old[r][h].x);
+            v.y = fmaf(p.alpha, v.y, p.beta * old[r][h].y);
+            v.z = fmaf(p.alpha, v.z, p.beta * old[r][h].z);
+            v.w = fmaf(p.alpha, v.w, p.beta * old[r][h].w);
+          } else {
+            v.x *= p.alpha;
+            v.y *= p.alpha;
+            v.z *= p.alpha;
+            v.w *= p.alpha;
+          }
+          *reinterpret_cast<float4*>(c_row + 32 * h) = v;
         }
-        *reinterpret_cast<float4*>(p.C + static_cast<int64_t>(row) * p.ldc + col) = v;
       }
     } else {
-      float old[8][4];
+      float old[kRows][4 * kGroups];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int row = row0 + 4 * i;
+      for (int r = 0; r < kRows; ++r) {
+        const int row = row0 + 4 * (i0 + r);
+        const float* c_row = p.C + static_cast<int64_t>(row) * p.ldc;
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          old[i][c] = (read_c && row < p.M && col + c < p.N)
-                          ? p.C[static_cast<int64_t>(row) * p.ldc + col + c]
-                          : 0.0f;
+        for (int h = 0; h < kGroups; ++h)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int col = col0 + 32 * h + c;
+            old[r][4 * h + c] = (read_c && row < p.M && col < p.N) ? c_row[col] : 0.0f;
+          }
       }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int r = 0; r < kRows; ++r) {
+        const int i = i0 + r;
         const int row = row0 + 4 * i;
         if (row >= p.M) continue;
         float* c_row = p.C + static_cast<int64_t>(row) * p.ldc;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          if (col + c < p.N) {
-            const float r = acc[i][h * 4 + c];
-            c_row[col + c] = read_c ? fmaf(p.alpha, r, p.beta * old[i][c]) : p.alpha * r;
+        for (int h = 0; h < kGroups; ++h)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int col = col0 + 32 * h + c;
+            if (col < p.N) {
+              const float x = acc[i][4 * h + c];
+              c_row[col] = read_c ? fmaf(p.alpha, x, p.beta * old[r][4 * h + c]) : p.alpha * x;
+            }
           }
-        }
       }
     }
   }
 }
 
-template <int MODE_A, int MODE_B>
+template <int MODE_A, int MODE_B, int BN>
 __global__ void __launch_bounds__(SimtTraits<MODE_A, MODE_B>::kThreads, 1)
     simt_gemm_kernel(const SimtArgs p, const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB) {
   using T = SimtTraits<MODE_A, MODE_B>;
+  using Gm = Geom<BN>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = align_smem<1024>(smem_raw);
-  SimtSmemTail* tail = reinterpret_cast<SimtSmemTail*>(smem + STAGES * kStageBytes);
-  auto stage_a = [&](int s) { return smem + s * kStageBytes; };
-  auto stage_b = [&](int s) { return smem + s * kStageBytes + kStageBytesA; };
+  SimtSmemTail* tail = reinterpret_cast<SimtSmemTail*>(smem + STAGES * Gm::kStageBytes);
+  auto stage_a = [&](int s) { return smem + s * Gm::kStageBytes; };
+  auto stage_b = [&](int s) { return smem + s * Gm::kStageBytes + kStageBytesA; };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -365,12 +453,14 @@ __global__ void __launch_bounds__(SimtTraits<MODE_A, MODE_B>::kThreads, 1)
   const int tiles_n = (p.N + BN - 1) / BN;
   const int num_tiles = tiles_m * tiles_n;
   const int num_kb = (p.K + BK - 1) / BK;
-  const int num_items = p.full_items + (num_tiles - p.full_items) * p.split;
+  const int num_items = p.sk_workers > 0
+                            ? p.full_items + 2 * static_cast<int>(gridDim.x)
+                            : p.full_items + (num_tiles - p.full_items) * p.split;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&tail->full[s], T::kFullCount);
-      mbar_init(&tail->empty[s], kComputeThreads);
+      mbar_init(&tail->empty[s], kComputeWarps);
     }
     tail->abort_flag = 0;
     tail->last_flag = 0;
@@ -407,7 +497,9 @@ __global__ void __launch_bounds__(SimtTraits<MODE_A, MODE_B>::kThreads, 1)
           break;
         }
         if (tma_issuer) {
-          mbar_arrive_expect_tx(&tail->full[s], T::kTmaBytes);
+          constexpr uint32_t kTmaBytes = (MODE_A == kLoadTma ? kStageBytesA : 0) +
+                                         (MODE_B == kLoadTma ? Gm::kStageBytesB : 0);
+          mbar_arrive_expect_tx(&tail->full[s], kTmaBytes);
           if (MODE_A == kLoadTma) tma_load_2d(stage_a(s), &tmA, kb * BK, tm * BM, &tail->full[s]);
           if (MODE_B == kLoadTma) tma_load_2d(stage_b(s), &tmB, tn * BN, kb * BK, &tail->full[s]);
         }
@@ -416,14 +508,14 @@ __global__ void __launch_bounds__(SimtTraits<MODE_A, MODE_B>::kThreads, 1)
             load_a_cpasync(stage_a(s), static_cast<const float*>(p.A), p.lda, p.M, p.K, tm * BM,
                            kb * BK, ptid);
           if (MODE_B == kLoadCpAsyncF32)
-            load_b_cpasync(stage_b(s), static_cast<const float*>(p.B), p.ldb, p.N, p.K, tn * BN,
-                           kb * BK, ptid);
+            load_b_cpasync<BN>(stage_b(s), static_cast<const float*>(p.B), p.ldb, p.N, p.K,
+                               tn * BN, kb * BK, ptid);
           if (MODE_A == kLoadConvertBf16)
             load_a_bf16(stage_a(s), static_cast<const uint16_t*>(p.A), p.lda, p.M, p.K, tm * BM,
                         kb * BK, ptid);
           if (MODE_B == kLoadConvertBf16)
-            load_b_bf16(stage_b(s), static_cast<const uint16_t*>(p.B), p.ldb, p.N, p.K, tn * BN,
-                        kb * BK, ptid);
+            load_b_bf16<BN>(stage_b(s), static_cast<const uint16_t*>(p.B), p.ldb, p.N, p.K,
+                            tn * BN, kb * BK, ptid);
           if (MODE_A == kLoadCpAsyncF32 || MODE_B == kLoadCpAsyncF32)
             cp_async_mbar_arrive_noinc(&tail->full[s]);
           else
@@ -449,14 +541,16 @@ __global__ void __launch_bounds__(SimtTraits<MODE_A, MODE_B>::kThreads, 1)
   const int wm = warp >> 1, wn = warp & 1;
   const int rg = lane >> 3, cg = lane & 7;
   const int ctid = threadIdx.x;  // 0..255
+  const int64_t tail_kb = static_cast<int64_t>(num_tiles - p.full_items) * num_kb;
   uint32_t it = 0;
   for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
     const SimtItem w = simt_item(p, item, tiles_m, tiles_n, num_kb);
-    uint64_t acc2[8][4];
+    if (w.kb0 == w.kb1) continue;  // an empty stream-K segment
+    uint64_t acc2[8][Gm::kCols / 2];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-      for (int q = 0; q < 4; ++q) acc2[i][q] = 0ull;
+      for (int q = 0; q < Gm::kCols / 2; ++q) acc2[i][q] = 0ull;
     bool failed = false;
     for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
       const int s = it % STAGES;
@@ -465,88 +559,92 @@ __global__ void __launch_bounds__(SimtTraits<MODE_A, MODE_B>::kThreads, 1)
         failed = true;
         break;
       }
-      compute_stage_x2(stage_a(s), stage_b(s), acc2, wm, wn, rg, cg);
-      mbar_arrive(&tail->empty[s]);
+      compute_stage_x2<BN>(stage_a(s), stage_b(s), acc2, wm, wn, rg, cg);
+      // One arrival per warp, after all its lanes' shared-memory reads.
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tail->empty[s]);
     }
     // Leave together if a wait ran out anywhere (see named_bar_any).
     if (named_bar_any(1, kComputeThreads, failed)) return;
-    float acc[8][8];
+    float acc[8][Gm::kCols];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-      for (int q = 0; q < 4; ++q) unpack2(acc2[i][q], acc[i][2 * q], acc[i][2 * q + 1]);
-    if (w.split_tile < 0) {
-      epilogue(p, acc, w.tm, w.tn, wm, wn, rg, cg);
+      for (int q = 0; q < Gm::kCols / 2; ++q) unpack2(acc2[i][q], acc[i][2 * q], acc[i][2 * q + 1]);
+    if (w.tail_tile < 0) {
+      epilogue<BN>(p, acc, w.tm, w.tn, wm, wn, rg, cg);
       continue;
     }
-    // Split tile: publish this k-range's partial sums (64 per thread, stored
+    // Part of a tail tile: publish this k-range's partial sums (stored
     // contiguously per thread), then count the arrival; the last of the
-    // tile's `split` parts adds all partials in part order -- a fixed order,
-    // so the result does not depend on which part finishes last.
-    float* mine = p.ws + (static_cast<int64_t>(w.split_tile * p.split + w.part) *
-                              kComputeThreads + ctid) * 64;
+    // tile's parts adds all partials in k order -- a fixed order, so the
+    // result does not depend on which part finishes last.
+    float* mine = p.ws + (static_cast<int64_t>(w.slot) * kComputeThreads + ctid) * Gm::kAcc;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      __stcg(reinterpret_cast<float4*>(mine + 8 * i),
-             make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]));
-      __stcg(reinterpret_cast<float4*>(mine + 8 * i + 4),
-             make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]));
-    }
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int h = 0; h < Gm::kColGroups; ++h)
+        __stcg(reinterpret_cast<float4*>(mine + 4 * (Gm::kColGroups * i + h)),
+               make_float4(acc[i][4 * h], acc[i][4 * h + 1], acc[i][4 * h + 2], acc[i][4 * h + 3]));
     compute_bar();
     if (ctid == 0) {
-      const uint32_t before = atomic_add_acq_rel_gpu(p.counters + w.split_tile, 1u);
-      tail->last_flag = (before == static_cast<uint32_t>(p.split - 1)) ? 1 : 0;
+      const uint32_t before = atomic_add_acq_rel_gpu(p.counters + w.tail_tile, 1u);
+      tail->last_flag = (before == static_cast<uint32_t>(w.parts - 1)) ? 1 : 0;
     }
     compute_bar();
     const int last = tail->last_flag;
     if (last) {
-      float sum[8][8];
+      float sum[8][Gm::kCols];
 #pragma unroll
       for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) sum[i][j] = 0.0f;
-      // Parts are added in part order.  The variants whose producers widen
-      // bf16 leave the compute warps fewer registers: there this thread's own
-      // partial is read back from the workspace like the others (same
-      // values, same order) so that its accumulators need not stay live;
-      // elsewhere it comes from the accumulators, one round trip fewer.
-      for (int part = 0; part < p.split; ++part) {
-        const float* src = p.ws + (static_cast<int64_t>(w.split_tile * p.split + part) *
-                                       kComputeThreads + ctid) * 64;
+        for (int j = 0; j < Gm::kCols; ++j) sum[i][j] = 0.0f;
+      // Parts are added in k order.  This thread's own partial comes from
+      // its accumulators where registers allow (the narrow tile with fp32
+      // producers), else it is read back from the workspace like the others
+      // (same values, same order), so that the accumulators need not stay
+      // live next to the sums.
+      constexpr bool kKeepOwn = (Gm::kAcc <= 64) && !T::kConvert;
+      for (int part = 0; part < w.parts; ++part) {
+        const float* src =
+            p.ws + (static_cast<int64_t>(part_slot(p, w.tail_tile, part, num_kb, tail_kb)) *
+                        kComputeThreads + ctid) * Gm::kAcc;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          float v[8];
-          if (!T::kConvert && part == w.part) {
+          float v[Gm::kCols];
+          if (kKeepOwn && part == w.part) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) v[j] = acc[i][j];
+            for (int j = 0; j < Gm::kCols; ++j) v[j] = acc[i][j];
           } else {
-            const float4 lo = __ldcg(reinterpret_cast<const float4*>(src + 8 * i));
-            const float4 hi = __ldcg(reinterpret_cast<const float4*>(src + 8 * i + 4));
-            v[0] = lo.x; v[1] = lo.y; v[2] = lo.z; v[3] = lo.w;
-            v[4] = hi.x; v[5] = hi.y; v[6] = hi.z; v[7] = hi.w;
+#pragma unroll
+            for (int h = 0; h < Gm::kColGroups; ++h) {
+              const float4 q = __ldcg(reinterpret_cast<const float4*>(src + 4 * (Gm::kColGroups * i + h)));
+              v[4 * h] = q.x;
+              v[4 * h + 1] = q.y;
+              v[4 * h + 2] = q.z;
+              v[4 * h + 3] = q.w;
+            }
           }
 #pragma unroll
-          for (int j = 0; j < 8; ++j) sum[i][j] += v[j];
+          for (int j = 0; j < Gm::kCols; ++j) sum[i][j] += v[j];
         }
       }
-      epilogue(p, sum, w.tm, w.tn, wm, wn, rg, cg);
-      if (ctid == 0) p.counters[w.split_tile] = 0u;
+      epilogue<BN>(p, sum, w.tm, w.tn, wm, wn, rg, cg);
+      if (ctid == 0) p.counters[w.tail_tile] = 0u;
     }
-    compute_bar();  // last_flag is rewritten by the next split item
+    compute_bar();  // last_flag is rewritten by the next tail item
   }
 }
 
-template <int MODE_A, int MODE_B>
-cudaError_t launch_variant(const SimtArgs& a, const CUtensorMap* tmA, const CUtensorMap* tmB,
-                           int num_sms, cudaStream_t stream) {
+template <int MODE_A, int MODE_B, int BN>
+cudaError_t launch_variant(const SimtArgs& a, int grid, const CUtensorMap* tmA,
+                           const CUtensorMap* tmB, cudaStream_t stream) {
   using T = SimtTraits<MODE_A, MODE_B>;
-  auto kernel = simt_gemm_kernel<MODE_A, MODE_B>;
+  constexpr size_t kSmem = smem_bytes<BN>();
+  auto kernel = simt_gemm_kernel<MODE_A, MODE_B, BN>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kSmemBytes));
+                                       static_cast<int>(kSmem));
   if (e != cudaSuccess) return e;
-  const int tiles = ((a.M + BM - 1) / BM) * ((a.N + BN - 1) / BN);
-  const int num_items = a.full_items + (tiles - a.full_items) * a.split;
-  const int grid = num_items < num_sms ? num_items : num_sms;
   CUtensorMap dummy{};
   cudaLaunchConfig_t cfg{};
   cudaLaunchAttribute attr[1];
@@ -554,7 +652,7 @@ cudaError_t launch_variant(const SimtArgs& a, const CUtensorMap* tmA, const CUte
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(T::kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = kSmem;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
@@ -563,44 +661,174 @@ cudaError_t launch_variant(const SimtArgs& a, const CUtensorMap* tmA, const CUte
   return cudaGetLastError();
 }
 
+template <int BN>
+cudaError_t launch_width(const SimtArgs& a, int grid, LoadMode mode_a, LoadMode mode_b,
+                         const CUtensorMap* tmA, const CUtensorMap* tmB, cudaStream_t stream) {
+  if (mode_a == kLoadTma && mode_b == kLoadTma)
+    return launch_variant<kLoadTma, kLoadTma, BN>(a, grid, tmA, tmB, stream);
+  if (mode_a == kLoadCpAsyncF32 && mode_b == kLoadTma)
+    return launch_variant<kLoadCpAsyncF32, kLoadTma, BN>(a, grid, tmA, tmB, stream);
+  if (mode_a == kLoadTma && mode_b == kLoadCpAsyncF32)
+    return launch_variant<kLoadTma, kLoadCpAsyncF32, BN>(a, grid, tmA, tmB, stream);
+  if (mode_a == kLoadCpAsyncF32 && mode_b == kLoadCpAsyncF32)
+    return launch_variant<kLoadCpAsyncF32, kLoadCpAsyncF32, BN>(a, grid, tmA, tmB, stream);
+  if (mode_a == kLoadConvertBf16 && mode_b == kLoadConvertBf16)
+    return launch_variant<kLoadConvertBf16, kLoadConvertBf16, BN>(a, grid, tmA, tmB, stream);
+  return cudaErrorInvalidValue;
+}
+
+// ------------------------------------------------------------- planning
+// Measured cost of cutting a tile into parts: about 2 k-block times per part
+// (storing its partial sums, and for the last part reading the others and
+// writing the tile), in k-blocks of the tile's own width.
+constexpr double kSplitFixupKb = 2.0;
+// A k-block of a 128 x 256 tile costs about 1.94 k-blocks of a 128 x 128 tile
+// (twice the FMAs at ~3 % better FMA-pipe use: fewer shared-memory reads).
+constexpr double kWideKbCost = 1.94;
+// Least k-blocks per stream-K range the cost model picks (a pinned stream-K
+// tail goes down to one).
+constexpr int kStreamMinKb = 4;
+
+struct TailChoice {
+  int split;        // equal parts per tail tile (1 = none)
+  int sk_workers;   // > 0: stream-K instead
+  double cost;      // in k-blocks of this tile width
+};
+
+// Cost, in k-blocks, of the tail of `tail` tiles cut into S equal parts
+// each, run R = ceil(tail S / workers) rounds deep.
+double split_cost(int tail, int S, int num_kb, int workers) {
+  const int R = (tail * S + workers - 1) / workers;
+  if (S <= 1) return static_cast<double>(R) * num_kb;
+  const double per_part = static_cast<double>(num_kb) / S;
+  return R * (per_part + S * kSplitFixupKb);
+}
+
+// Stream-K tail over G workers: each runs ceil(W / G) k-blocks, stores at
+// most two partial tiles and, when it finishes a tile, reads up to
+// ceil(G / tail) + 1 of them.
+double stream_cost(int tail, int num_kb, int G) {
+  const int64_t W = static_cast<int64_t>(tail) * num_kb;
+  const int64_t per = (W + G - 1) / G;
+  const int parts = (G + tail - 1) / tail + 1;
+  return static_cast<double>(per) + 0.5 * kSplitFixupKb * (2 + parts);
+}
+
+TailChoice choose_tail(int tail, int num_kb, int num_sms, const TileConfig* fixed) {
+  TailChoice c{1, 0, 0.0};
+  if (tail <= 0) return c;
+  const int64_t W = static_cast<int64_t>(tail) * num_kb;
+  const int pinned = fixed != nullptr ? fixed->split : 0;
+  if (pinned == GEMM_SPLIT_STREAM) {
+    c.sk_workers = static_cast<int>(W < num_sms ? W : num_sms);
+    c.cost = stream_cost(tail, num_kb, c.sk_workers);
+    return c;
+  }
+  if (pinned > 0) {
+    c.split = pinned > num_kb ? num_kb : pinned;
+    c.cost = split_cost(tail, c.split, num_kb, num_sms);
+    return c;
+  }
+  c.split = tail_split(tail, num_kb, num_sms, kSplitFixupKb);
+  c.cost = split_cost(tail, c.split, num_kb, num_sms);
+  int G = num_sms;
+  if (W / G < kStreamMinKb) G = static_cast<int>(W / kStreamMinKb);
+  if (G >= tail && G > 1) {
+    const double sc = stream_cost(tail, num_kb, G);
+    if (sc < c.cost) {
+      c.split = 1;
+      c.sk_workers = G;
+      c.cost = sc;
+    }
+  }
+  return c;
+}
+
+// Estimated time of the whole launch in 128 x 128 k-block units.
+double plan_time(int M, int N, int num_kb, int num_sms, bool wide, const TileConfig* fixed,
+                 TailChoice* tail_out, int* full_out) {
+  const int bn = simt_bn(wide);
+  const int tiles = ((M + BM - 1) / BM) * ((N + bn - 1) / bn);
+  const int tail = tiles >= num_sms ? tiles % num_sms : tiles;
+  const int full = tiles - tail;
+  const TailChoice t = choose_tail(tail, num_kb, num_sms, fixed);
+  *tail_out = t;
+  *full_out = full;
+  const double kb = (static_cast<double>(full) / num_sms) * num_kb + t.cost;
+  return kb * (wide ? kWideKbCost : 1.0);
+}
+
 }  // namespace
 
-SimtPlan simt_plan(int tiles, int num_kb, int num_sms, const TileConfig* fixed) {
-  const int group_m = (fixed != nullptr && fixed->group_m > 0) ? fixed->group_m : 8;
-  SimtPlan pl{tiles, 1, tiles < num_sms ? tiles : num_sms, group_m, 0, 0};
-  if (tiles <= 0 || num_sms <= 0) return pl;
-  // Tiles beyond the last full wave (all of them when there are fewer tiles
-  // than SMs) are split along k when that shortens the last wave.
-  // Measured split overhead: about 2 k-block times (2.6 us each) per part
-  // and round.  A pinned split is capped at one k-block per part.
-  int best_s = (fixed != nullptr && fixed->split > 0) ? fixed->split
-                                                      : tail_split(tiles, num_kb, num_sms, 2.0);
-  if (best_s > num_kb) best_s = num_kb;
-  const int tail = tiles >= num_sms ? tiles % num_sms : tiles;
-  if (best_s <= 1 || tail == 0) return pl;
+SimtPlan simt_plan(int M, int N, int K, int num_sms, const TileConfig* fixed, bool allow_wide) {
+  SimtPlan pl{};
+  pl.group_m = (fixed != nullptr && fixed->group_m > 0) ? fixed->group_m : 8;
+  pl.split = 1;
+  if (M <= 0 || N <= 0 || K <= 0 || num_sms <= 0) {
+    pl.grid = 1;
+    return pl;
+  }
+  const int num_kb = (K + BK - 1) / BK;
+  const int pinned_kernel = fixed != nullptr ? fixed->kernel : GEMM_KERNEL_AUTO;
+  TailChoice tn{}, tw{};
+  int full_n = 0, full_w = 0;
+  const double time_n = plan_time(M, N, num_kb, num_sms, false, fixed, &tn, &full_n);
+  bool wide = allow_wide && pinned_kernel == GEMM_KERNEL_WIDE;
+  if (allow_wide && pinned_kernel == GEMM_KERNEL_AUTO) {
+    const double time_w = plan_time(M, N, num_kb, num_sms, true, fixed, &tw, &full_w);
+    wide = time_w < time_n;
+  } else if (wide) {
+    plan_time(M, N, num_kb, num_sms, true, fixed, &tw, &full_w);
+  }
+  const TailChoice& t = wide ? tw : tn;
+  const int bn = simt_bn(wide);
+  const int tiles = ((M + BM - 1) / BM) * ((N + bn - 1) / bn);
+  const int tail = tiles - (wide ? full_w : full_n);
+  pl.wide = wide;
+  pl.full_items = tiles;
+  pl.grid = tiles < num_sms ? tiles : num_sms;
+  if (tail == 0 || (t.split <= 1 && t.sk_workers == 0)) return pl;
   pl.full_items = tiles - tail;
-  pl.split = best_s;
-  const int items = pl.full_items + tail * best_s;
-  pl.grid = items < num_sms ? items : num_sms;
-  pl.ws_floats = static_cast<int64_t>(tail) * best_s * kComputeThreads * 64;
+  const int64_t tile_floats = static_cast<int64_t>(BM) * bn;
+  if (t.sk_workers > 0) {
+    pl.sk_workers = t.sk_workers;
+    pl.grid = num_sms;
+    pl.ws_floats = 2 * static_cast<int64_t>(t.sk_workers) * tile_floats;
+  } else {
+    pl.split = t.split;
+    const int items = pl.full_items + tail * t.split;
+    pl.grid = items < num_sms ? items : num_sms;
+    pl.ws_floats = static_cast<int64_t>(tail) * t.split * tile_floats;
+  }
   pl.counters = tail;
   return pl;
 }
 
-cudaError_t launch_simt(const SimtArgs& a, LoadMode mode_a, LoadMode mode_b,
-                        const CUtensorMap* tmA, const CUtensorMap* tmB, int num_sms,
+int simt_plan_max_parts(const SimtPlan& pl, int M, int N, int K) {
+  if (pl.sk_workers == 0) return pl.split;
+  const int bn = simt_bn(pl.wide);
+  const int tiles = ((M + BM - 1) / BM) * ((N + bn - 1) / bn);
+  const int tail = tiles - pl.full_items;
+  const int64_t num_kb = (K + BK - 1) / BK;
+  const int64_t W = static_cast<int64_t>(tail) * num_kb, G = pl.sk_workers;
+  int most = 1;
+  for (int64_t t = 0; t < tail; ++t) {
+    const int64_t parts =
+        sk_worker((t + 1) * num_kb - 1, W, G) - sk_worker(t * num_kb, W, G) + 1;
+    if (parts > most) most = static_cast<int>(parts);
+  }
+  return most;
+}
+
+cudaError_t launch_simt(const SimtArgs& a, const SimtPlan& plan, LoadMode mode_a,
+                        LoadMode mode_b, const CUtensorMap* tmA, const CUtensorMap* tmB,
                         cudaStream_t stream) {
-  if (mode_a == kLoadTma && mode_b == kLoadTma)
-    return launch_variant<kLoadTma, kLoadTma>(a, tmA, tmB, num_sms, stream);
-  if (mode_a == kLoadCpAsyncF32 && mode_b == kLoadTma)
-    return launch_variant<kLoadCpAsyncF32, kLoadTma>(a, tmA, tmB, num_sms, stream);
-  if (mode_a == kLoadTma && mode_b == kLoadCpAsyncF32)
-    return launch_variant<kLoadTma, kLoadCpAsyncF32>(a, tmA, tmB, num_sms, stream);
-  if (mode_a == kLoadCpAsyncF32 && mode_b == kLoadCpAsyncF32)
-    return launch_variant<kLoadCpAsyncF32, kLoadCpAsyncF32>(a, tmA, tmB, num_sms, stream);
-  if (mode_a == kLoadConvertBf16 && mode_b == kLoadConvertBf16)
-    return launch_variant<kLoadConvertBf16, kLoadConvertBf16>(a, tmA, tmB, num_sms, stream);
-  return cudaErrorInvalidValue;
+  // The planner picks the wide tile only when both operands are on TMA.
+  if (plan.wide) {
+    if (mode_a != kLoadTma || mode_b != kLoadTma) return cudaErrorInvalidValue;
+    return launch_variant<kLoadTma, kLoadTma, 256>(a, plan.grid, tmA, tmB, stream);
+  }
+  return launch_width<128>(a, plan.grid, mode_a, mode_b, tmA, tmB, stream);
 }
 
 }  // namespace g12

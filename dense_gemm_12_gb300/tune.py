@@ -48,11 +48,12 @@ def ceil_log2(x: int) -> int:
 
 def candidates(is_bf16: bool, M: int, K: int):
     """Every pinned configuration worth timing for a shape."""
-    kernels = ["single_cta"]
+    kernels = ["single_cta"] if is_bf16 else ["single_cta", "wide"]
     if is_bf16 and M > 128:
         kernels = ["cta_pair", "single_cta"]
+    splits = SPLITS if is_bf16 else SPLITS + [-1]   # -1: the stream-K tail (fp32)
     num_kb = -(-K // (64 if is_bf16 else 32))
-    for kernel, split, group in itertools.product(kernels, SPLITS, GROUPS):
+    for kernel, split, group in itertools.product(kernels, splits, GROUPS):
         if split <= num_kb:
             yield {"kernel": kernel, "split": split, "group_m": group}
 
@@ -60,7 +61,7 @@ def candidates(is_bf16: bool, M: int, K: int):
 def table_lines(entries, num_sms: int, gpu: str, date: str):
     """Text of dispatch_table.inc for `entries` (dicts with is_bf16, M, N, K,
     kernel, split, group_m and the timings)."""
-    kid = {"single_cta": 1, "cta_pair": 2}
+    kid = {"single_cta": 1, "cta_pair": 2, "wide": 3}
     out = [
         "// dispatch_table.inc -- launch configurations chosen by the offline sweep",
         "// (dense_gemm_12_gb300/tune.py) for the tile kernels, keyed by ceil(log2) of",

@@ -300,7 +300,9 @@ gemm_path_t gemm_select_path(int is_bf16, int64_t M, int64_t N, int64_t K,
  * kernel for an M x N x K problem cuts each work item of the persistent
  * grid's last round ("A GEMM Kernel, Step by Step": the partial last wave of
  * "The fringe and the last wave", filled by the split-K of "What is left").
- * 1 means no item is split.  `is_bf16`
+ * 1 means no item is split.  Under the stream-K tail (GEMM_SPLIT_STREAM)
+ * the tail tiles are cut into differing numbers of k-ranges; the largest is
+ * reported.  `is_bf16`
  * selects gemm_bf16gemm's tensor-core kernels (M > 16) instead of
  * gemm_sgemm's CUDA-core kernel; the decode kernel (bf16, M <= 16) plans its
  * own split and reports 1 here.  Returns 0 for negative sizes or when there
@@ -324,15 +326,25 @@ typedef enum {
     GEMM_KERNEL_SINGLE_CTA = 1,  /* one CTA per tile: the CUDA-core kernel's
                                     128 x 128 tiles (fp32), the tcgen05
                                     kernel's 128 x 256 tiles (bf16)            */
-    GEMM_KERNEL_CTA_PAIR = 2     /* bf16 only: two CTAs of a cluster per
+    GEMM_KERNEL_CTA_PAIR = 2,    /* bf16 only: two CTAs of a cluster per
                                     256 x 256 tile (tcgen05 cta_group::2)      */
+    GEMM_KERNEL_WIDE = 3         /* fp32 only: the CUDA-core kernel on
+                                    128 x 256 tiles (8 x 16 values per thread:
+                                    fewer shared-memory reads per FMA, half
+                                    as many tiles)                             */
 } gemm_kernel_t;
+
+/* gemm_config_t.split value (fp32 only): stream-K tail.  The k-blocks of all
+ * tiles past the last whole round are dealt out evenly to the persistent
+ * CTAs in contiguous ranges that may cross a tile boundary; each tile's
+ * partial sums are added in k order by the last range to finish it. */
+#define GEMM_SPLIT_STREAM (-1)
 
 typedef struct {
     int kernel;   /* a gemm_kernel_t                                          */
     int split;    /* k-ranges per work item of the persistent grid's last
                      round: 0 = automatic, 1 = none, 2..8 (capped at one
-                     k-block per range)                                      */
+                     k-block per range), or GEMM_SPLIT_STREAM (fp32)          */
     int group_m;  /* raster order: work items walk column by column through
                      groups of this many item rows; 0 = automatic, 1..64     */
 } gemm_config_t;
@@ -343,13 +355,16 @@ typedef struct {
  * same as the plain call).  The result is the same GEMM within the same bound
  * for every configuration (bit-identical where the sums are exact).  A pinned
  * bf16 kernel always runs the tcgen05 tile kernels, also for M <= 16 (the
- * decode kernel runs only under GEMM_KERNEL_AUTO).  The fp32 path has one
- * kernel: GEMM_KERNEL_CTA_PAIR is invalid there, and so is every field for
- * the paths without tiles (M, N, K or alpha zero: nothing to configure, the
- * fields are ignored).  Errors: fields out of range give
+ * decode kernel runs only under GEMM_KERNEL_AUTO).  The fp32 path has two
+ * tile widths (GEMM_KERNEL_SINGLE_CTA: 128 x 128, GEMM_KERNEL_WIDE:
+ * 128 x 256); GEMM_KERNEL_CTA_PAIR is invalid there, and GEMM_KERNEL_WIDE
+ * and GEMM_SPLIT_STREAM are invalid for bf16.  The fields are ignored on
+ * the paths without tiles (M, N, K or alpha zero: nothing to configure).
+ * Errors: fields out of range give
  * GEMM_ERR_INVALID_VALUE; otherwise as the plain calls.  bf16 operands that
- * TMA cannot describe run on the CUDA cores, where only split and group_m
- * apply.
+ * TMA cannot describe run on the CUDA cores (128 x 128 tiles), where only
+ * split and group_m apply; fp32 operands that TMA cannot describe always
+ * run on 128 x 128 tiles.
  */
 gemm_status_t gemm_sgemm_config(int64_t M, int64_t N, int64_t K, float alpha,
                                 const float *A, int64_t lda,

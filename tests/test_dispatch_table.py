@@ -8,7 +8,7 @@ from dense_gemm_12_gb300 import tune
 
 TABLE = os.path.join(os.path.dirname(__file__), "..", "dense_gemm_12_gb300", "csrc",
                      "dispatch_table.inc")
-ENTRY = re.compile(r"^\s*\{(-?\d+),\s*(\d+),\s*(\d+),\s*(\d+),\s*(\d+),\s*(\d+),\s*(\d+)\}")
+ENTRY = re.compile(r"^\s*\{(-?\d+),\s*(\d+),\s*(\d+),\s*(\d+),\s*(\d+),\s*(-?\d+),\s*(\d+)\}")
 
 
 def parse_table(text):
@@ -27,8 +27,12 @@ def test_committed_table_is_well_formed():
     for is_bf16, lm, ln, lk, kernel, split, group in body:
         assert is_bf16 in (0, 1)
         assert all(0 <= v <= 31 for v in (lm, ln, lk))
-        assert kernel in (1, 2) and (kernel == 1 or is_bf16 == 1)
-        assert 1 <= split <= 8 and 1 <= group <= 64
+        # the CTA-pair kernel is bf16's, the wide tile and stream-K are fp32's
+        assert kernel in (1, 2, 3)
+        assert kernel != 2 or is_bf16 == 1
+        assert kernel != 3 or is_bf16 == 0
+        assert 1 <= split <= 8 or (split == -1 and is_bf16 == 0)
+        assert 1 <= group <= 64
 
 
 def test_ceil_log2_buckets():
@@ -42,7 +46,10 @@ def test_candidates_respect_kernel_and_k():
     c = list(tune.candidates(True, 1024, 128))                  # 2 k-blocks
     assert {x["kernel"] for x in c} == {"single_cta", "cta_pair"}
     assert max(x["split"] for x in c) == 2
-    assert {x["kernel"] for x in tune.candidates(False, 4092, 4092)} == {"single_cta"}
+    c = list(tune.candidates(False, 4092, 4092))
+    assert {x["kernel"] for x in c} == {"single_cta", "wide"}
+    assert -1 in {x["split"] for x in c}                        # stream-K tail, fp32 only
+    assert -1 not in {x["split"] for x in tune.candidates(True, 1024, 4096)}
 
 
 def _result(M, auto_ms, best_ms, is_bf16=1):
@@ -70,3 +77,10 @@ def test_table_writer_round_trips():
     sms, rows = parse_table(text)
     assert sms == 152
     assert rows == [(0, 9, 10, 10, 2, 2, 4), (1, 9, 10, 10, 2, 2, 4), (-1, 0, 0, 0, 0, 0, 0)]
+
+
+def test_table_writer_keeps_wide_and_stream_entries():
+    r = _result(4092, 2.0, 1.5, is_bf16=0)
+    r.update(kernel="wide", split=-1, group_m=8)
+    sms, rows = parse_table(tune.table_lines([r], 152, "GPU", "2026-01-01"))
+    assert rows[0] == (0, 12, 10, 10, 3, -1, 8)

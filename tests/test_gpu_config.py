@@ -57,17 +57,50 @@ def test_bf16_every_config_exact(M, N, K):
     check_device_error()
 
 
-@pytest.mark.parametrize("M,N,K", [(100, 260, 1024), (1000, 1300, 600), (2048, 1280, 1024)])
+@pytest.mark.parametrize("M,N,K", [(100, 260, 1024), (1000, 1300, 600), (2048, 1280, 1024),
+                                   (2600, 2900, 333)])
 def test_fp32_every_config_exact(M, N, K):
+    # both tile widths, equal k-splits and the stream-K tail (-1): 2600 x 2900
+    # has whole rounds and a tail on either width
     A, B, C = make_inputs(M, N, K, ("int", None), ("int", None), ("int", None), seed=M + K)
     ref32, _, _ = oracle_sgemm(A, B, C, 1.5, -0.5)
-    for s in (1, 2, 7):
-        for gm in (1, 3, 16):
-            cfg = {"kernel": "single_cta", "split": s, "group_m": gm}
-            st, out = _run(False, A, B, C, 1.5, -0.5, cfg)
-            assert st == 0, cfg
-            assert np.array_equal(out.numpy().view(np.uint32), ref32.view(np.uint32)), cfg
+    for kernel in ("single_cta", "wide"):
+        for s in (1, 2, 7, -1):
+            for gm in (1, 3, 16):
+                cfg = {"kernel": kernel, "split": s, "group_m": gm}
+                st, out = _run(False, A, B, C, 1.5, -0.5, cfg)
+                assert st == 0, cfg
+                assert np.array_equal(out.numpy().view(np.uint32), ref32.view(np.uint32)), cfg
     check_device_error()
+
+
+@pytest.mark.parametrize("M,N,K", [(4092, 4092, 4092), (3000, 5000, 1999), (129, 4100, 3000)])
+def test_fp32_stream_k_and_wide_within_bound(M, N, K):
+    # random inputs at the sizes the planner sends to the stream-K tail; rows
+    # sampled against the oracle, and every configuration must agree with the
+    # others within the bound (the k order of the sums differs between them)
+    A, B, C = make_inputs(M, N, K, ("uniform", None), ("uniform", None), ("uniform", None),
+                          seed=M % 97 + K)
+    idx = torch.arange(0, M, max(1, M // 23))
+    _, ref64, den = oracle_sgemm(A[idx].contiguous(), B, C[idx].contiguous(), 0.7, 0.3)
+    tol = 2e-6 * K ** 0.5
+    for cfg in ({"kernel": "wide", "split": -1}, {"kernel": "single_cta", "split": -1},
+                {"kernel": "wide", "split": 2}, None):
+        st, out = _run(False, A, B, C, 0.7, 0.3, cfg)
+        assert st == 0, cfg
+        assert ratio(out[idx], ref64, den) <= tol, cfg
+    check_device_error()
+
+
+def test_fp32_stream_k_is_reproducible():
+    # fixed segment boundaries and a fixed order of the partial sums: two
+    # launches give the same bits
+    M, N, K = 3000, 5000, 1999
+    A, B, C = make_inputs(M, N, K, ("uniform", None), ("uniform", None), ("uniform", None), seed=9)
+    cfg = {"kernel": "wide", "split": -1}
+    _, a = _run(False, A, B, C, 0.7, 0.3, cfg)
+    _, b = _run(False, A, B, C, 0.7, 0.3, cfg)
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
 
 
 def test_pinned_split_beyond_k_blocks_is_capped():
@@ -106,8 +139,9 @@ def test_invalid_configs_rejected():
         assert g.gemm_bf16gemm_config(M, N, K, 1.0, A.data_ptr(), K, B.data_ptr(), N, 0.0,
                                       C.data_ptr(), N, cfg, s) == 1, cfg
     Af, Bf = A.float(), B.float()
-    assert g.gemm_sgemm_config(M, N, K, 1.0, Af.data_ptr(), K, Bf.data_ptr(), N, 0.0,
-                               C.data_ptr(), N, {"kernel": "cta_pair"}, s) == 1
+    for cfg in ({"kernel": "cta_pair"}, {"kernel": 4}, {"split": -2}, {"split": 9}):
+        assert g.gemm_sgemm_config(M, N, K, 1.0, Af.data_ptr(), K, Bf.data_ptr(), N, 0.0,
+                                   C.data_ptr(), N, cfg, s) == 1, cfg
     torch.cuda.synchronize()
 
 
@@ -123,14 +157,17 @@ def test_table_entries_are_what_dispatch_uses():
     sms, rows = _table_rows()
     if torch.cuda.get_device_properties(0).multi_processor_count != sms:
         pytest.skip("table measured on a GPU with another SM count")
-    names = {1: "single_cta", 2: "cta_pair"}
+    names = {1: "single_cta", 2: "cta_pair", 3: "wide"}
     for is_bf16, lm, ln, lk, kernel, split, group in rows:
         M, N, K = 1 << lm, 1 << ln, 1 << lk
         cfg, from_table = g.gemm_get_config(is_bf16, M, N, K)
         assert from_table, (M, N, K)
         assert cfg["kernel"] == names[kernel] and cfg["group_m"] == group
         # a split is capped by the k-blocks and dropped when no round is partial
-        assert 1 <= cfg["split"] <= split
+        if split == -1:
+            assert cfg["split"] in (-1, 1)
+        else:
+            assert 1 <= cfg["split"] <= split
 
 
 def test_get_config_for_the_benchmark_shapes():
@@ -139,4 +176,5 @@ def test_get_config_for_the_benchmark_shapes():
     cfg, _ = g.gemm_get_config(True, 16, 12288, 4096)
     assert cfg == {"kernel": "auto", "split": 0, "group_m": 0}   # the decode kernel
     cfg, _ = g.gemm_get_config(False, 4092, 4092, 4092)
-    assert cfg["kernel"] == "single_cta" and cfg["split"] >= 1 and cfg["group_m"] >= 1
+    assert cfg["kernel"] in ("single_cta", "wide") and cfg["group_m"] >= 1
+    assert cfg["split"] >= 1 or cfg["split"] == g.SPLIT_STREAM
