@@ -688,6 +688,11 @@ constexpr double kWideKbCost = 1.94;
 // Least k-blocks per stream-K range the cost model picks (a pinned stream-K
 // tail goes down to one).
 constexpr int kStreamMinKb = 4;
+// Measured fixed cost of each of a stream-K worker's (up to two) segments, in
+// k-blocks: storing its partial tile, the arrival, and restarting the k loop.
+// Fitted on the shapes where short ranges made stream-K lose to an equal
+// split (e.g. 128x1024x1024: 33 us split in 8, 52 us stream-K).
+constexpr double kStreamSegmentKb = 3.0;
 
 struct TailChoice {
   int split;        // equal parts per tail tile (1 = none)
@@ -704,14 +709,14 @@ double split_cost(int tail, int S, int num_kb, int workers) {
   return R * (per_part + S * kSplitFixupKb);
 }
 
-// Stream-K tail over G workers: each runs ceil(W / G) k-blocks, stores at
-// most two partial tiles and, when it finishes a tile, reads up to
-// ceil(G / tail) + 1 of them.
+// Stream-K tail over G workers: each runs ceil(W / G) k-blocks in up to two
+// segments and, when it finishes a tile, reads up to ceil(G / tail) + 1
+// partial tiles.
 double stream_cost(int tail, int num_kb, int G) {
   const int64_t W = static_cast<int64_t>(tail) * num_kb;
   const int64_t per = (W + G - 1) / G;
   const int parts = (G + tail - 1) / tail + 1;
-  return static_cast<double>(per) + 0.5 * kSplitFixupKb * (2 + parts);
+  return static_cast<double>(per) + 2 * kStreamSegmentKb + 0.5 * kSplitFixupKb * parts;
 }
 
 TailChoice choose_tail(int tail, int num_kb, int num_sms, const TileConfig* fixed) {

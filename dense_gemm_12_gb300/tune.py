@@ -168,8 +168,9 @@ def summary_lines(results, chosen, gpu, num_sms, command):
     lines = ["# Launch-configuration sweep of the tile kernels", "",
              "Command (%s, %d SMs):" % (gpu, num_sms), "", "    " + command, "",
              "Per class (ceil(log2) of M, N, K), one representative shape; model = "
-             "the cost model's choice without the table (split of the last round, pair "
-             "kernel for bf16 M > 128, raster groups of 8); best = fastest pinned "
+             "the cost model's choice without the table (split of the last round, -1 = "
+             "stream-K; pair kernel for bf16 M > 128; fp32 tile width single_cta = "
+             "128x128 or wide = 128x256; raster groups of 8); best = fastest pinned "
              "configuration; both re-timed in turn (4 x 5 back-to-back launches, median).  Entries "
              "marked `table` beat the model by more than the margin and were written "
              "to `csrc/dispatch_table.inc`.", "",
