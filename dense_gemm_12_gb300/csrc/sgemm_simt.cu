@@ -337,13 +337,23 @@ __device__ __forceinline__ void compute_stage_x2(const uint8_t* sA, const uint8_
         bv[2 * j] = b.x;
         bv[2 * j + 1] = b.y;
       }
+      uint64_t a2[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const float av = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
-        const uint64_t a2 = pack2(av, av);
-#pragma unroll
-        for (int q = 0; q < 2 * kGroups; ++q) acc2[i][q] = ffma2(a2, bv[q], acc2[i][q]);
+        a2[i] = pack2(av, av);
       }
+      // Column pairs outermost, rows in a snake (0..7, then 7..0): each FMA
+      // shares its B pair with the previous one, and at a turn also its A
+      // pair.  Measured against rows outermost (the same FMAs in another
+      // order, bitwise the same sums): 2.080 vs 2.135 ms at 4092^3.
+#pragma unroll
+      for (int q = 0; q < 2 * kGroups; ++q)
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          const int i = (q & 1) ? 7 - r : r;
+          acc2[i][q] = ffma2(a2[i], bv[q], acc2[i][q]);
+        }
     }
   }
 }
