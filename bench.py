@@ -218,6 +218,36 @@ def time_launches(torch, step, n, stream_obj):
     return [a.elapsed_time(b) for a, b in evs]
 
 
+def bench_sgemm_shape(torch, g, wl, name, fp32_peak, device, stream_obj):
+    """Another fp32 workload on the CUDA-core kernel (4096^3, or the ragged
+    3000x5000x1999 whose K = 1999 rows are not 16-byte multiples, so A is
+    loaded by the generic cp.async producers).  Two input sets in turn, each
+    larger than L2."""
+    w = wl.WORKLOADS[name]
+    w2 = wl.Workload(**{**w.__dict__, "seed": w.seed + 100, "name": name + "_b"})
+    sets = [tuple(t.to(device) for t in wl.workload_inputs(x)) for x in (w, w2)]
+    step = sgemm_step_fn(g, sets, w, stream_obj.cuda_stream)
+    for i in range(3):
+        step(i)
+    torch.cuda.synchronize()
+    times = time_launches(torch, step, 20, stream_obj)
+    ms = statistics.median(times)
+    tflops = w.flops / (ms * 1e-3) / 1e12
+    del sets
+    torch.cuda.empty_cache()
+    return {
+        "workload": "fp32 SGEMM M=%d N=%d K=%d, alpha=%g, beta=%g" % (w.M, w.N, w.K, w.alpha,
+                                                                      w.beta),
+        "kernel": "simt_gemm_kernel (CUDA cores, fma.rn.f32x2)",
+        "value": tflops * 1e3, "unit": "GFLOP/s", "ms_per_launch_median": ms,
+        "launches_timed": len(times),
+        "roofline": {"bound": "alu", "achieved": tflops, "peak": fp32_peak, "unit": "TFLOP/s",
+                     "frac": tflops / fp32_peak, "traffic": None,
+                     "peak_note": "derived fp32 FFMA peak, as the headline"},
+        "l2": "two input sets used in turn, each larger than L2",
+    }
+
+
 def bench_bf16_8192(torch, g, wl, peaks, device, stream_obj):
     w = wl.WORKLOADS["bf16_8192"]
     A, B, _ = wl.workload_inputs(w, with_c=False)
@@ -567,6 +597,10 @@ def run_ours(args):
     if not args.no_parts and rank == 0:
         del sets
         torch.cuda.empty_cache()
+        for name in ("sgemm_4096", "sgemm_ragged"):
+            w_ = wl.WORKLOADS[name]
+            parts["sgemm_%dx%dx%d" % (w_.M, w_.N, w_.K)] = bench_sgemm_shape(
+                torch, g, wl, name, fp32_peak, device, stream_obj)
         parts["bf16_8192"] = bench_bf16_8192(torch, g, wl, peaks, device, stream_obj)
         parts["bf16_8192_bias_gelu_bf16out"] = bench_bf16_8192_fused(torch, g, wl, peaks, device,
                                                                       stream_obj)
