@@ -36,7 +36,7 @@ STATUS = {
 }
 PATHS = {
     0: "none", 1: "scale_c", 2: "simt_tma", 3: "simt_generic", 4: "tc_bf16",
-    5: "tc_decode", 6: "simt_bf16", 7: "tc_bf16_pair",
+    5: "tc_decode", 6: "simt_bf16", 7: "tc_bf16_pair", 8: "simt_staged", 9: "tc_staged",
 }
 
 

@@ -29,6 +29,9 @@ struct Scratch {
   int64_t ws_floats = 0;
   uint32_t* counters = nullptr;
   int64_t counter_count = 0;
+  // Aligned copies of operands the TMA engine cannot describe (stage_operands).
+  uint8_t* stage = nullptr;
+  int64_t stage_bytes = 0;
 };
 
 struct DeviceState {
@@ -37,9 +40,10 @@ struct DeviceState {
   int num_sms = 0;
   int cc_major = 0, cc_minor = 0;
   uint32_t* err_word = nullptr;
-  // Split-K scratch (partial sums + arrival counters), one per stream: calls
-  // on one stream are ordered by it, calls on different streams never share
-  // a buffer.  Grown on demand, freed by gemm_shutdown.
+  // Split-K scratch (partial sums + arrival counters) and operand staging
+  // copies, one set per stream: calls on one stream are ordered by it, calls
+  // on different streams never share a buffer.  Grown on demand, freed by
+  // gemm_shutdown.
   std::mutex ws_mutex;
   std::map<void*, Scratch> scratch;
 };
@@ -203,6 +207,86 @@ gemm_status_t ensure_scratch(DeviceState& st, cudaStream_t stream, int64_t float
   return GEMM_OK;
 }
 
+// The operand staging area of `stream` on this device, grown to at least
+// `bytes`.  Caller holds st.ws_mutex.
+gemm_status_t ensure_stage(DeviceState& st, cudaStream_t stream, int64_t bytes, uint8_t** out) {
+  Scratch& sc = st.scratch[static_cast<void*>(stream)];
+  if (sc.stage_bytes < bytes) {
+    // Growing: the old buffer may still be read by this stream's kernels.
+    if (cudaStreamSynchronize(stream) != cudaSuccess) {
+      cudaGetLastError();
+      return GEMM_ERR_LAUNCH;
+    }
+    if (sc.stage) cudaFree(sc.stage);
+    sc.stage = nullptr;
+    sc.stage_bytes = 0;
+    if (cudaMalloc(reinterpret_cast<void**>(&sc.stage), static_cast<size_t>(bytes)) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      sc.stage = nullptr;
+      return GEMM_ERR_NO_MEMORY;
+    }
+    sc.stage_bytes = bytes;
+  }
+  *out = sc.stage;
+  return GEMM_OK;
+}
+
+// Whether a call first copies the operands the TMA engine cannot describe
+// into an aligned staging buffer and then runs the TMA-fed kernels, instead
+// of the generic-load kernels on the operands as given.  fp32: the TMA-fed
+// kernel is ~20 % faster (3000x5000x1999: wide tiles and a stream-K tail
+// instead of 128x128 tiles with 4-byte copies), so the copy -- one read and
+// one write of the operand -- must be small next to the GEMM: at least 2^31
+// FLOPs, and N >= 256 when A is copied (M >= 256 for B), which keeps the
+// copy under ~2 % of the GEMM.  bf16: the tensor cores are ~25x faster than
+// the CUDA-core fallback, so any tile-kernel shape of at least 2^24 FLOPs is
+// copied; decode shapes (M <= 16) read B once and keep the fallback.
+bool stage_wanted(bool bf16, int64_t M, int64_t N, int64_t K, bool a_ok, bool b_ok) {
+  if (a_ok && b_ok) return false;
+  const double flops = 2.0 * static_cast<double>(M) * static_cast<double>(N) *
+                       static_cast<double>(K);
+  if (!bf16) {
+    if (flops < 2147483648.0) return false;
+    if (!a_ok && N < 256) return false;
+    if (!b_ok && M < 256) return false;
+    return true;
+  }
+  return M > kDecBM && flops >= 16777216.0;
+}
+
+// Copies each operand the TMA engine cannot describe into this stream's
+// staging area (rows padded to a 16-byte pitch, 256-byte aligned) and points
+// A / B and lda / ldb at the copy.  The copy kernels are queued on `cs`
+// ahead of the GEMM; the caller holds st.ws_mutex until the GEMM is queued.
+// GEMM_ERR_NO_MEMORY: the staging area could not be grown, nothing changed.
+gemm_status_t stage_operands(DeviceState& st, cudaStream_t cs, int elem_bytes, int64_t M,
+                             int64_t N, int64_t K, const void*& A, int64_t& lda, const void*& B,
+                             int64_t& ldb) {
+  const int64_t per = 16 / elem_bytes;
+  const bool sa = !tma_ok(A, lda, elem_bytes), sb = !tma_ok(B, ldb, elem_bytes);
+  const int64_t lda2 = (K + per - 1) / per * per, ldb2 = (N + per - 1) / per * per;
+  const int64_t bytes_a = sa ? (M * lda2 * elem_bytes + 255) / 256 * 256 : 0;
+  const int64_t bytes_b = sb ? K * ldb2 * elem_bytes : 0;
+  uint8_t* base = nullptr;
+  const gemm_status_t s = ensure_stage(st, cs, bytes_a + bytes_b, &base);
+  if (s != GEMM_OK) return s;
+  if (sa) {
+    const cudaError_t e = launch_stage_rows(elem_bytes, A, lda, base, lda2, M, K, st.num_sms, cs);
+    if (e != cudaSuccess) return from_cuda(e);
+    A = base;
+    lda = lda2;
+  }
+  if (sb) {
+    const cudaError_t e =
+        launch_stage_rows(elem_bytes, B, ldb, base + bytes_a, ldb2, K, N, st.num_sms, cs);
+    if (e != cudaSuccess) return from_cuda(e);
+    B = base + bytes_a;
+    ldb = ldb2;
+  }
+  return GEMM_OK;
+}
+
 // Work plan of the CUDA-core kernel for `a` (whole tiles, and the last wave's
 // tiles split along k when that balances the SMs better).  A split plan needs
 // this stream's scratch area; `lock` (on st->ws_mutex) is then held until the
@@ -292,7 +376,7 @@ gemm_status_t plan_simt(DeviceState* st, cudaStream_t cs, SimtArgs& a, const Sim
   a.ws = nullptr;
   a.counters = nullptr;
   if (pl.split == 1 && pl.sk_workers == 0) return GEMM_OK;
-  lock.lock();
+  if (!lock.owns_lock()) lock.lock();
   Scratch* sc = nullptr;
   const gemm_status_t s = ensure_scratch(*st, cs, pl.ws_floats, pl.counters, &sc);
   if (s != GEMM_OK) return s;
@@ -322,6 +406,54 @@ cudaError_t launch_scale_c(int M, int N, float beta, float* C, int64_t ldc, cuda
   if (blocks > 4096) blocks = 4096;
   if (blocks < 1) blocks = 1;
   scale_c_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(M, N, beta, C, ldc);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------ operand staging copy
+namespace {
+// Copies a rows x cols matrix of T (2- or 4-byte bit patterns, copied
+// unchanged) from src (row pitch lds elements, any T-aligned address) to dst
+// (row pitch ldd elements, ldd * sizeof(T) a multiple of 16, dst 16-byte
+// aligned).  Item t of the grid-stride loop is the 16-byte piece t % pieces
+// of row t / pieces: consecutive threads read consecutive elements of a row
+// and write whole 16-byte pieces; columns past `cols` in a row's last piece
+// are written as zero bits.
+template <typename T>
+__global__ void stage_rows_kernel(const T* __restrict__ src, int64_t lds, T* __restrict__ dst,
+                                  int64_t ldd, int64_t rows, int64_t cols) {
+  constexpr int kPer = 16 / static_cast<int>(sizeof(T));
+  const int64_t pieces = (cols + kPer - 1) / kPer;
+  const int64_t total = rows * pieces;
+  for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; t < total;
+       t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = t / pieces;
+    const int64_t c0 = (t - r * pieces) * kPer;
+    const T* s = src + r * lds + c0;
+    union {
+      T e[kPer];
+      uint4 v;
+    } u;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) u.e[i] = (c0 + i < cols) ? s[i] : T(0);
+    *reinterpret_cast<uint4*>(dst + r * ldd + c0) = u.v;
+  }
+}
+}  // namespace
+
+cudaError_t launch_stage_rows(int elem_bytes, const void* src, int64_t lds, void* dst, int64_t ldd,
+                              int64_t rows, int64_t cols, int num_sms, cudaStream_t stream) {
+  const int64_t per = 16 / elem_bytes;
+  const int64_t total = rows * ((cols + per - 1) / per);
+  int64_t blocks = (total + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(num_sms > 0 ? num_sms : 1) * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  if (elem_bytes == 4)
+    stage_rows_kernel<uint32_t><<<static_cast<int>(blocks), 256, 0, stream>>>(
+        static_cast<const uint32_t*>(src), lds, static_cast<uint32_t*>(dst), ldd, rows, cols);
+  else
+    stage_rows_kernel<uint16_t><<<static_cast<int>(blocks), 256, 0, stream>>>(
+        static_cast<const uint16_t*>(src), lds, static_cast<uint16_t*>(dst), ldd, rows, cols);
   return cudaGetLastError();
 }
 
@@ -431,7 +563,13 @@ const char* gemm_status_string(gemm_status_t s) {
 gemm_path_t gemm_select_path(int is_bf16, int64_t M, int64_t N, int64_t K, float alpha,
                              const void* A, int64_t lda, const void* B, int64_t ldb) {
   if (check_common(M, N, K, lda, ldb, N > 1 ? N : 1) != GEMM_OK) return GEMM_PATH_NONE;
-  return select_path(is_bf16 != 0, M, N, K, alpha, A, lda, B, ldb);
+  const bool bf16 = is_bf16 != 0;
+  const gemm_path_t p = select_path(bf16, M, N, K, alpha, A, lda, B, ldb);
+  const int eb = bf16 ? 2 : 4;
+  if ((p == GEMM_PATH_SIMT_GENERIC || p == GEMM_PATH_SIMT_BF16) &&
+      stage_wanted(bf16, M, N, K, tma_ok(A, lda, eb), tma_ok(B, ldb, eb)))
+    return bf16 ? GEMM_PATH_TC_STAGED : GEMM_PATH_SIMT_STAGED;
+  return p;
 }
 
 int gemm_split_parts(int is_bf16, int64_t M, int64_t N, int64_t K) {
@@ -493,6 +631,25 @@ static gemm_status_t sgemm_impl(int64_t M, int64_t N, int64_t K, float alpha, co
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   if (path == GEMM_PATH_SCALE_C) return run_scale(M, N, beta, C, ldc, cs);
 
+  // Held from staging (if any) until the kernel is queued: the staging copy
+  // and the split-K scratch of this stream must not be regrown meanwhile.
+  std::unique_lock<std::mutex> lock(st->ws_mutex, std::defer_lock);
+  if (path == GEMM_PATH_SIMT_GENERIC &&
+      stage_wanted(false, M, N, K, tma_ok(A, lda, 4), tma_ok(B, ldb, 4))) {
+    lock.lock();
+    const void* sa = A;
+    const void* sb = B;
+    s = stage_operands(*st, cs, 4, M, N, K, sa, lda, sb, ldb);
+    if (s == GEMM_OK) {
+      A = static_cast<const float*>(sa);
+      B = static_cast<const float*>(sb);
+    } else if (s != GEMM_ERR_NO_MEMORY) {
+      return s;
+    }
+    // No memory for the copies: the generic-load kernel reads the operands
+    // as given.
+  }
+
   SimtArgs a{};
   a.M = static_cast<int>(M);
   a.N = static_cast<int>(N);
@@ -527,7 +684,6 @@ static gemm_status_t sgemm_impl(int64_t M, int64_t N, int64_t K, float alpha, co
         mb = kLoadTma;
     }
   }
-  std::unique_lock<std::mutex> lock(st->ws_mutex, std::defer_lock);
   s = plan_simt(st, cs, a, pl, lock);
   if (s != GEMM_OK) return s;
   return from_cuda(launch_simt(a, pl, ma, mb, ma == kLoadTma ? &tmA : nullptr,
@@ -548,10 +704,13 @@ gemm_status_t gemm_sgemm_config(int64_t M, int64_t N, int64_t K, float alpha, co
 
 // Runs the tensor-core path (tile kernel or decode kernel) of a bf16 GEMM
 // whose operands TMA can describe, with output stage `epi`.
+// `lock` (on st->ws_mutex) is taken here when the launch needs this stream's
+// scratch, unless the caller already holds it (operands staged).
 static gemm_status_t run_bf16_tensor_core(DeviceState* st, gemm_path_t path, int64_t M, int64_t N,
                                           int64_t K, const void* A, int64_t lda, const void* B,
                                           int64_t ldb, const Epilogue& epi, cudaStream_t cs,
-                                          const gemm_config_t* cfg) {
+                                          const gemm_config_t* cfg,
+                                          std::unique_lock<std::mutex>& lock) {
   CUtensorMap tmA, tmB;
   if (path == GEMM_PATH_TC_BF16 || path == GEMM_PATH_TC_BF16_PAIR) {
     TcArgs a{};
@@ -576,7 +735,7 @@ static gemm_status_t run_bf16_tensor_core(DeviceState* st, gemm_path_t path, int
     if (pl.split == 1) return from_cuda(launch_tc_bf16(a, pl, &tmA, &tmB, cs));
     // Split items: the stream's scratch stays locked until the launch is
     // queued, so no other thread can regrow it underneath.
-    std::lock_guard<std::mutex> lock(st->ws_mutex);
+    if (!lock.owns_lock()) lock.lock();
     Scratch* sc = nullptr;
     const gemm_status_t s = ensure_scratch(*st, cs, pl.ws_floats, pl.counters, &sc);
     if (s != GEMM_OK) return s;
@@ -603,7 +762,7 @@ static gemm_status_t run_bf16_tensor_core(DeviceState* st, gemm_path_t path, int
     a.counters = nullptr;
     return from_cuda(launch_tc_decode(a, &tmA, &tmB, grid, cs));
   }
-  std::lock_guard<std::mutex> lock(st->ws_mutex);
+  if (!lock.owns_lock()) lock.lock();
   Scratch* sc = nullptr;
   gemm_status_t s = ensure_scratch(*st, cs, decode_workspace_floats(a.N, a.K, grid),
                                    decode_counter_count(a.N), &sc);
@@ -636,6 +795,19 @@ static gemm_status_t bf16gemm_impl(int64_t M, int64_t N, int64_t K, float alpha,
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   if (path == GEMM_PATH_SCALE_C) return run_scale(M, N, beta, C, ldc, cs);
 
+  std::unique_lock<std::mutex> lock(st->ws_mutex, std::defer_lock);
+  if (path == GEMM_PATH_SIMT_BF16 &&
+      stage_wanted(true, M, N, K, tma_ok(A, lda, 2), tma_ok(B, ldb, 2))) {
+    lock.lock();
+    s = stage_operands(*st, cs, 2, M, N, K, A, lda, B, ldb);
+    if (s == GEMM_OK)
+      path = M <= kTcBM ? GEMM_PATH_TC_BF16 : GEMM_PATH_TC_BF16_PAIR;
+    else if (s != GEMM_ERR_NO_MEMORY)
+      return s;
+    // No memory for the copies: the CUDA-core kernel reads the operands as
+    // given.
+  }
+
   if (path == GEMM_PATH_SIMT_BF16) {
     SimtArgs a{};
     a.M = static_cast<int>(M);
@@ -655,14 +827,13 @@ static gemm_status_t bf16gemm_impl(int64_t M, int64_t N, int64_t K, float alpha,
     gemm_config_t simt_cfg{GEMM_KERNEL_AUTO, cfg ? cfg->split : 0, cfg ? cfg->group_m : 0};
     const TileConfig tc = resolve_config(false, M, N, K, st->num_sms, &simt_cfg, nullptr);
     const SimtPlan pl = simt_plan(a.M, a.N, a.K, st->num_sms, &tc, false);
-    std::unique_lock<std::mutex> lock(st->ws_mutex, std::defer_lock);
     s = plan_simt(st, cs, a, pl, lock);
     if (s != GEMM_OK) return s;
     return from_cuda(launch_simt(a, pl, kLoadConvertBf16, kLoadConvertBf16, nullptr, nullptr,
                                  cs));
   }
   return run_bf16_tensor_core(st, path, M, N, K, A, lda, B, ldb,
-                              plain_epilogue(alpha, beta, C, ldc), cs, cfg);
+                              plain_epilogue(alpha, beta, C, ldc), cs, cfg, lock);
 }
 
 gemm_status_t gemm_bf16gemm(int64_t M, int64_t N, int64_t K, float alpha, const void* A,
@@ -744,7 +915,6 @@ gemm_status_t gemm_bf16gemm_fused(int64_t M, int64_t N, int64_t K, float alpha, 
   if (path != GEMM_PATH_SCALE_C) {
     if (A == nullptr || B == nullptr) return GEMM_ERR_INVALID_VALUE;
     if (misaligned(A, 1u) || misaligned(B, 1u)) return GEMM_ERR_MISALIGNED;
-    if (path == GEMM_PATH_SIMT_BF16) return GEMM_ERR_UNSUPPORTED;
   }
   DeviceState* st = device_state(&s);
   if (st == nullptr) return s;
@@ -771,7 +941,18 @@ gemm_status_t gemm_bf16gemm_fused(int64_t M, int64_t N, int64_t K, float alpha, 
   epi.d_vec = !misaligned(o.D, vec_mask) && (o.ldd % (d_bytes == 4 ? 4 : 8) == 0) ? 1 : 0;
   if (path == GEMM_PATH_SCALE_C)
     return from_cuda(launch_epilogue_only(static_cast<int>(M), static_cast<int>(N), epi, cs));
-  return run_bf16_tensor_core(st, path, M, N, K, A, lda, B, ldb, epi, cs, nullptr);
+  std::unique_lock<std::mutex> lock(st->ws_mutex, std::defer_lock);
+  gemm_path_t run_path = path;
+  if (path == GEMM_PATH_SIMT_BF16) {
+    // The output stage lives only in the tensor-core kernels: operands the
+    // TMA engine cannot describe are always staged here, whatever the size.
+    lock.lock();
+    s = stage_operands(*st, cs, 2, M, N, K, A, lda, B, ldb);
+    if (s != GEMM_OK) return s;
+    run_path = M <= kDecBM ? GEMM_PATH_TC_DECODE
+                           : (M <= kTcBM ? GEMM_PATH_TC_BF16 : GEMM_PATH_TC_BF16_PAIR);
+  }
+  return run_bf16_tensor_core(st, run_path, M, N, K, A, lda, B, ldb, epi, cs, nullptr, lock);
 }
 
 gemm_status_t gemm_bf16gemm_epilogue(int64_t M, int64_t N, int64_t K, float alpha,
@@ -848,6 +1029,7 @@ gemm_status_t gemm_shutdown(void) {
     for (auto& kv : st.scratch) {
       if (kv.second.ws) cudaFree(kv.second.ws);
       if (kv.second.counters) cudaFree(kv.second.counters);
+      if (kv.second.stage) cudaFree(kv.second.stage);
     }
     st.scratch.clear();
   }

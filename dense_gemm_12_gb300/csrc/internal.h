@@ -184,6 +184,11 @@ Epilogue plain_epilogue(float alpha, float beta, float* C, int64_t ldc);
 cudaError_t launch_epilogue_only(int M, int N, const Epilogue& e, cudaStream_t stream);
 
 // C <- beta * C (beta == 0 writes zeros without reading C).
+// Copies a rows x cols row-major matrix of elem_bytes-wide elements (2 or 4)
+// from src (pitch lds elements) into dst (pitch ldd elements; dst 16-byte
+// aligned, ldd * elem_bytes a multiple of 16), zero-filling each row's pad.
+cudaError_t launch_stage_rows(int elem_bytes, const void* src, int64_t lds, void* dst, int64_t ldd,
+                              int64_t rows, int64_t cols, int num_sms, cudaStream_t stream);
 cudaError_t launch_scale_c(int M, int N, float beta, float* C, int64_t ldc,
                            cudaStream_t stream);
 

@@ -32,8 +32,12 @@
  *  Alignment  None is required beyond the element size.  Operands whose
  *             address or leading dimension the tensor-memory-accelerator
  *             (TMA) copy engine cannot describe (base not 16-byte aligned,
- *             row pitch not a multiple of 16 bytes) take generic-load kernels
- *             instead; this changes speed, not the result's error bound.
+ *             row pitch not a multiple of 16 bytes) are, for large enough
+ *             problems, first copied into an aligned per-stream staging
+ *             buffer (one read and one write of the operand) so that the
+ *             TMA-fed kernels run; smaller problems take generic-load
+ *             kernels on the operands as given (see gemm_select_path).
+ *             Either way this changes speed, not the result's error bound.
  *             A bf16 pointer that is not 2-byte aligned returns
  *             GEMM_ERR_MISALIGNED.
  *  Aliasing   C must not overlap A or B (not checked).
@@ -53,10 +57,16 @@
  *             call on that stream needs it (or more of it), keeps and reuses
  *             it, and gemm_shutdown() frees it; calls on different streams
  *             never share scratch, calls on one stream are ordered by it.
+ *             The staging copies of operands the TMA engine cannot describe
+ *             (see Alignment) live in a second per-stream buffer, kept,
+ *             grown and freed the same way (at most the size of the copied
+ *             operands, rows padded to 16 bytes).
  *             Growing a stream's scratch synchronises that stream, so the
  *             first such call on a stream must come before that stream is
  *             captured into a CUDA graph.  Allocation failure returns
- *             GEMM_ERR_NO_MEMORY.  See also gemm_bf16gemm_decode_static,
+ *             GEMM_ERR_NO_MEMORY, except for a staging copy of gemm_sgemm or
+ *             gemm_bf16gemm, which then runs the generic-load kernel on the
+ *             operands as given.  See also gemm_bf16gemm_decode_static,
  *             which allocates nothing.
  */
 #ifndef GEMM12_H
@@ -177,9 +187,11 @@ typedef struct {
  * written, by the thread that writes it); otherwise D must not overlap A, B,
  * C, bias, residual or amax.  Errors: out == NULL, an unknown act or d_type,
  * a NULL or misaligned D, C (beta != 0), bias, residual or amax, or a leading
- * dimension below max(1, N) return GEMM_ERR_INVALID_VALUE; operands the TMA
+ * dimension below max(1, N) return GEMM_ERR_INVALID_VALUE.  Operands the TMA
  * engine cannot describe (base not 16-byte aligned, pitch not a multiple of
- * 16 bytes) return GEMM_ERR_UNSUPPORTED.  K == 0 or alpha == 0:
+ * 16 bytes) are always copied into the stream's staging buffer first (see
+ * Memory), whatever the size, since the output stage exists only in the
+ * tensor-core kernels.  K == 0 or alpha == 0:
  * v = act(beta * C + bias) + R (alpha is not used).  Accuracy: v carries the
  * bf16 GEMM's bound on the pre-activation value times the activation's
  * largest slope (1 for none and ReLU, 1.13 for GELU); D adds the rounding of
@@ -206,8 +218,8 @@ gemm_status_t gemm_bf16gemm_fused(int64_t M, int64_t N, int64_t K, float alpha,
  * bf16; D may be C itself only when d_type is GEMM_OUT_F32 and ldd == ldc,
  * otherwise D must not overlap A, B, C or bias.  The same tensor-core kernels
  * as gemm_bf16gemm run (including the decode kernel for M <= 16); operands
- * the TMA engine cannot describe return GEMM_ERR_UNSUPPORTED, an unknown act
- * or a d_type other than GEMM_OUT_F32 and GEMM_OUT_BF16
+ * the TMA engine cannot describe are staged as in gemm_bf16gemm_fused; an
+ * unknown act or a d_type other than GEMM_OUT_F32 and GEMM_OUT_BF16 returns
  * GEMM_ERR_INVALID_VALUE.  K == 0 or alpha == 0: D = act(beta*C +
  * bias).  Error bound: the bf16 GEMM's bound on the pre-activation value,
  * times the activation's largest slope (1 for none and ReLU, 1.13 for GELU),
@@ -281,13 +293,25 @@ typedef enum {
     GEMM_PATH_TC_DECODE = 5,      /* bf16 tensor-core split-K decode kernel */
     GEMM_PATH_SIMT_BF16 = 6,      /* bf16 operands TMA cannot describe:
                                      widened to fp32 on the CUDA cores     */
-    GEMM_PATH_TC_BF16_PAIR = 7    /* bf16 tensor-core kernel on CTA pairs:
+    GEMM_PATH_TC_BF16_PAIR = 7,   /* bf16 tensor-core kernel on CTA pairs:
                                      two SMs per 256x256 tile (M > 128)    */
+    GEMM_PATH_SIMT_STAGED = 8,    /* fp32 operands TMA cannot describe are
+                                     first copied into an aligned staging
+                                     buffer, then GEMM_PATH_SIMT_TMA       */
+    GEMM_PATH_TC_STAGED = 9       /* bf16 operands TMA cannot describe are
+                                     first copied into an aligned staging
+                                     buffer, then the tcgen05 tile kernels
+                                     (GEMM_PATH_TC_BF16 or _PAIR)          */
 } gemm_path_t;
 
 /*
  * gemm_select_path -- host-only: the kernel path a call with these arguments
  * takes.  `is_bf16` selects gemm_bf16gemm's rules instead of gemm_sgemm's.
+ * Operands the TMA engine cannot describe are staged (GEMM_PATH_SIMT_STAGED,
+ * GEMM_PATH_TC_STAGED) when the copy is cheap next to the GEMM: fp32 with at
+ * least 2^31 FLOPs (2*M*N*K) and N >= 256 if A is copied, M >= 256 if B is;
+ * bf16 with M > 16 and at least 2^24 FLOPs.  Otherwise GEMM_PATH_SIMT_GENERIC
+ * or GEMM_PATH_SIMT_BF16 (also when the staging buffer cannot be allocated).
  * Pointers are only inspected for alignment, never dereferenced.  Returns
  * GEMM_PATH_NONE (and writes nothing) for arguments the call would reject.
  */
@@ -361,10 +385,10 @@ typedef struct {
  * and GEMM_SPLIT_STREAM are invalid for bf16.  The fields are ignored on
  * the paths without tiles (M, N, K or alpha zero: nothing to configure).
  * Errors: fields out of range give
- * GEMM_ERR_INVALID_VALUE; otherwise as the plain calls.  bf16 operands that
- * TMA cannot describe run on the CUDA cores (128 x 128 tiles), where only
- * split and group_m apply; fp32 operands that TMA cannot describe always
- * run on 128 x 128 tiles.
+ * GEMM_ERR_INVALID_VALUE; otherwise as the plain calls.  Operands that TMA
+ * cannot describe are staged as in the plain calls; unstaged, bf16 ones run
+ * on the CUDA cores (128 x 128 tiles), where only split and group_m apply,
+ * and fp32 ones always on 128 x 128 tiles.
  */
 gemm_status_t gemm_sgemm_config(int64_t M, int64_t N, int64_t K, float alpha,
                                 const float *A, int64_t lda,

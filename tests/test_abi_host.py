@@ -66,7 +66,14 @@ P = 1 << 20
     (dict(bf16=0, M=5, N=5, K=0), "scale_c"),
     (dict(bf16=0, M=5, N=5, K=5, alpha=0.0), "scale_c"),
     (dict(bf16=0, M=4092, N=4092, K=4092), "simt_tma"),
-    (dict(bf16=0, M=3000, N=5000, K=1999), "simt_generic"),       # lda*4 = 7996 B
+    # operands TMA cannot describe: staged when the copy is cheap next to the
+    # GEMM (fp32: >= 2^31 FLOPs, N >= 256 to copy A, M >= 256 to copy B)
+    (dict(bf16=0, M=3000, N=5000, K=1999), "simt_staged"),        # lda*4 = 7996 B
+    (dict(bf16=0, M=1000, N=1000, K=999), "simt_generic"),        # 2.0e9 < 2^31 FLOPs
+    (dict(bf16=0, M=8192, N=255, K=1023), "simt_generic"),        # A copy too large
+    (dict(bf16=0, M=255, N=8192, K=1024, ldb=8193), "simt_generic"),  # B copy too large
+    (dict(bf16=0, M=256, N=8192, K=1024, ldb=8193), "simt_staged"),
+    (dict(bf16=0, M=2048, N=2048, K=2048, A=P + 4), "simt_staged"),  # A base + 4 B
     (dict(bf16=0, M=64, N=64, K=64, A=P + 4), "simt_generic"),     # A not 16-B aligned
     (dict(bf16=0, M=64, N=64, K=64, ldb=66), "simt_generic"),      # B pitch 264 B
     (dict(bf16=1, M=8192, N=8192, K=8192), "tc_bf16_pair"),
@@ -77,6 +84,12 @@ P = 1 << 20
     (dict(bf16=1, M=17, N=12288, K=4096), "tc_bf16"),
     (dict(bf16=1, M=64, N=64, K=60), "simt_bf16"),                 # lda*2 = 120 B
     (dict(bf16=1, M=64, N=64, K=64, B=P + 2), "simt_bf16"),
+    # bf16: staged for the tile kernels (M > 16) from 2^24 FLOPs
+    (dict(bf16=1, M=256, N=256, K=127), "simt_bf16"),             # 1.66e7 < 2^24
+    (dict(bf16=1, M=256, N=256, K=129), "tc_staged"),
+    (dict(bf16=1, M=17, N=4096, K=4095), "tc_staged"),
+    (dict(bf16=1, M=16, N=4096, K=4095), "simt_bf16"),            # decode shape
+    (dict(bf16=1, M=4096, N=4096, K=4096, A=P + 2), "tc_staged"),
     (dict(bf16=0, M=5, N=5, K=5, lda=4), "none"),                  # invalid: lda < K
 ])
 def test_select_path(gemm_lib, case, expect):
