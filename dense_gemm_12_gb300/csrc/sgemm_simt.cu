@@ -698,9 +698,12 @@ cudaError_t launch_width(const SimtArgs& a, int grid, LoadMode mode_a, LoadMode 
 // (storing its partial sums, and for the last part reading the others and
 // writing the tile), in k-blocks of the tile's own width.
 constexpr double kSplitFixupKb = 2.0;
-// A k-block of a 128 x 256 tile costs about 1.94 k-blocks of a 128 x 128 tile
-// (twice the FMAs at ~3 % better FMA-pipe use: fewer shared-memory reads).
-constexpr double kWideKbCost = 1.94;
+// A k-block of a 128 x 256 tile costs about 1.86 k-blocks of a 128 x 128 tile
+// (twice the FMAs at ~7 % better FMA-pipe use: fewer shared-memory reads per
+// FMA, and the 4-fold unroll of its k loop).  Measured on shapes that both
+// widths cover in whole rounds (2432 x {2048, 4096, 8192} x {1024, 2048,
+// 4096}): 1.845-1.867.
+constexpr double kWideKbCost = 1.86;
 // Least k-blocks per stream-K range the cost model picks (a pinned stream-K
 // tail goes down to one).
 constexpr int kStreamMinKb = 4;
