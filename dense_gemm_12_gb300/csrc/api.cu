@@ -756,8 +756,10 @@ static gemm_status_t run_bf16_tensor_core(DeviceState* st, gemm_path_t path, int
   a.K = static_cast<int>(K);
   a.epi = epi;
   a.err = st->err_word;
-  // One CTA per column group: nothing is split, no scratch is touched.
-  if (grid == decode_counter_count(a.N)) {
+  a.cluster = decode_cluster(a.N, a.K, st->num_sms);
+  // One CTA per column group, or clusters that exchange their partial sums
+  // in shared memory: no scratch is touched.
+  if (grid == decode_counter_count(a.N) || a.cluster > 1) {
     a.workspace = nullptr;
     a.counters = nullptr;
     return from_cuda(launch_tc_decode(a, &tmA, &tmB, grid, cs));

@@ -14,9 +14,14 @@
 // Work split.  B is cut into n-groups of 128 columns; a unit is one n-group x
 // 128 values of k (32 KB of B, fetched as two 64 x 128 TMA boxes).  With at
 // least ~60 % as many n-groups as SMs (N = 12288 gives 96) every CTA streams
-// whole n-groups: no k range is split and nothing is exchanged.  Otherwise
-// units are numbered n-group-major and every CTA takes one contiguous,
-// equal-sized run of them, cut into segments at n-group boundaries (split-K).
+// whole n-groups: no k range is split and nothing is exchanged.  With fewer
+// n-groups, clusters of S CTAs (S a power of two up to 8, groups x S <= SMs)
+// split each n-group's k range into S equal runs (split-K); the S partial
+// sums are exchanged through distributed shared memory and each CTA adds the
+// S values of its 128 / S columns in rank order, which is k order
+// (cluster_reduce_store).  With more n-groups than SMs, units are numbered
+// n-group-major and every CTA takes one contiguous, equal-sized run of them,
+// cut into segments at n-group boundaries.
 // A segment that spans the whole k range of its n-group writes C directly;
 // otherwise the CTA holding the group's first k-piece combines: it waits a
 // short, bounded time for the other contributors' partial sums (published in
@@ -34,6 +39,7 @@
 // drains, and every global access follows grid_dependency_wait().
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "internal.h"
@@ -196,6 +202,62 @@ __device__ __forceinline__ void store_c_column(const DecodeArgs& p, int n, const
       epi_track(e, amax_acc, val);
       epi_store1(e, m, n, val);
     }
+}
+
+// Cluster split (p.cluster = S > 1): the S CTAs of a cluster hold the partial
+// sums of one column group over S consecutive k ranges (rank order = k
+// order), each as a BMr x NW fp32 array at shared address `part` (same offset
+// in every CTA).  CTA `rank` writes columns [rank NW / S, (rank + 1) NW / S)
+// of the group: epilogue thread ept takes one of them and 16 / S of its rows,
+// reads the S partial sums of each element from the cluster's shared memory,
+// adds them in rank order (a fixed order: results do not depend on timing)
+// and runs the output stage.  Called by the 128 epilogue threads between two
+// cluster barriers.
+template <bool FUSED>
+__device__ __forceinline__ void cluster_reduce_store(const DecodeArgs& p, uint32_t part, int ept) {
+  const int S = p.cluster;
+  const int rank = static_cast<int>(cluster_cta_rank());
+  const int ng = static_cast<int>(blockIdx.x) / S;
+  const int slice = NW / S;                      // columns written by this CTA
+  const int rows = BMr * slice / kEpiThreads;    // rows per thread: 16 / S
+  const int col = rank * slice + ept % slice;
+  const int m0 = (ept / slice) * rows;
+  const int n = ng * NW + col;
+  const Epilogue& e = p.epi;
+  float amax_acc = 0.0f;
+  if (n < p.N) {
+    constexpr int kMaxRows = BMr / 2;  // S >= 2
+    float v[kMaxRows], old[kMaxRows], res[kMaxRows];
+    const float bias = FUSED ? epi_bias(e, n) : 0.0f;
+#pragma unroll
+    for (int i = 0; i < kMaxRows; ++i) {
+      const int m = m0 + i;
+      v[i] = old[i] = res[i] = 0.0f;
+      if (i < rows && m < p.M) {
+        if (e.beta != 0.0f) old[i] = e.C[static_cast<int64_t>(m) * e.ldc + n];
+        if (FUSED) res[i] = epi_residual(e, m, n);
+        const uint32_t a = part + static_cast<uint32_t>((m * NW + col) * 4);
+        v[i] = ld_shared_cluster_f32(mapa_shared(a, 0));
+        for (int q = 1; q < S; ++q) v[i] += ld_shared_cluster_f32(mapa_shared(a, q));
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kMaxRows; ++i) {
+      const int m = m0 + i;
+      if (i < rows && m < p.M) {
+        if (!FUSED) {
+          // plain GEMM: D is C itself (fp32, ldd == ldc)
+          static_cast<float*>(e.D)[static_cast<int64_t>(m) * e.ldc + n] =
+              (e.beta != 0.0f) ? fmaf(e.alpha, v[i], e.beta * old[i]) : e.alpha * v[i];
+        } else {
+          const float val = epi_value(e, v[i], old[i], bias, res[i]);
+          epi_track(e, amax_acc, val);
+          epi_store1(e, m, n, val);
+        }
+      }
+    }
+  }
+  if (FUSED) epi_flush_amax(e, amax_acc);
 }
 
 template <bool FUSED>
@@ -373,16 +435,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       // contributor of the n-group has already published its partial sums --
       // if so, preload them, so that once this segment's accumulator is ready
       // the group's result is a few adds away.
+      const bool clustered = p.cluster > 1;
       float old[NSUB][BMr], res[NSUB][BMr];
 #pragma unroll
       for (int j = 0; j < NSUB; ++j) {
-        load_c_column(p, row_valid ? ng * NW + j * BN + n_local : p.N, old[j]);
-        if (FUSED) load_r_column(p, row_valid ? ng * NW + j * BN + n_local : p.N, res[j]);
+        // (a cluster split loads C and the residual in cluster_reduce_store)
+        const int nc = (row_valid && !clustered) ? ng * NW + j * BN + n_local : p.N;
+        load_c_column(p, nc, old[j]);
+        if (FUSED) load_r_column(p, nc, res[j]);
       }
       constexpr int kPre = 2;  // partial sums of other CTAs held in registers
       float pre[kPre][NSUB][BMr];
       bool preloaded = false;
-      const bool can_preload = row_valid && !whole && (nsegs - 1 <= static_cast<uint32_t>(kPre));
+      const bool can_preload =
+          row_valid && !whole && !clustered && (nsegs - 1 <= static_cast<uint32_t>(kPre));
       auto preload = [&]() {
         // the kk-th contributor other than this CTA, in CTA order
 #pragma unroll
@@ -413,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          if (!whole && ept == 0 && !tail->others_ready &&
+          if (!whole && !clustered && ept == 0 && !tail->others_ready &&
               ld_acquire_gpu(p.counters + ng) == nsegs - 1)
             st_release_cta_shared(&tail->others_ready, 1);
           if (can_preload && !preloaded && ld_acquire_cta_shared(&tail->others_ready)) {
@@ -461,7 +527,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
       }
 
-      if (whole) {
+      if (clustered) {
+        // This CTA's k range is its run's only segment: every MMA has read
+        // its stage and every copy has landed, so stage 0 holds the partial
+        // sums for the exchange after the loop.
+        float* part = reinterpret_cast<float*>(smem);
+        if (row_valid) {
+#pragma unroll
+          for (int j = 0; j < NSUB; ++j)
+#pragma unroll
+            for (int m = 0; m < BMr; ++m) part[m * NW + j * BN + n_local] = __uint_as_float(r[j][m]);
+        }
+      } else if (whole) {
 #pragma unroll
         for (int j = 0; j < NSUB; ++j) {
           float v[BMr];
@@ -555,6 +632,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before_sync();
   __syncthreads();
+  if (p.cluster > 1) {
+    // Every CTA of the cluster reaches these barriers, also after a wait ran
+    // out (each wait above is bounded), so none can hang here.
+    cluster_sync();  // the partial sums of every CTA of the cluster are written
+    if (warp >= 2 && warp <= 5)
+      cluster_reduce_store<FUSED>(p, smem_u32(smem), static_cast<int>(threadIdx.x) - 64);
+    cluster_sync();  // no CTA leaves while another may still read its shared memory
+  }
   tc_fence_after_sync();
   if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
 }
@@ -563,15 +648,73 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 int decode_b_box_rows() { return BK; }
 
+// Clusters of S decode CTAs that can be resident at once on the current
+// device (cudaOccupancyMaxActiveClusters; one CTA per SM, and a cluster must
+// fit in one GPC: on a 152-SM GB300, 76 of 2, 36 of 4, 15 of 8).  Queried
+// once per device and size.
+int decode_max_clusters(int S) {
+  constexpr int kMaxDev = 64;
+  static std::atomic<int> cache[kMaxDev][4];  // S = 1, 2, 4, 8; 0 = not yet known
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) {
+    cudaGetLastError();
+    return 0;
+  }
+  const int slot = S >= 8 ? 3 : S >= 4 ? 2 : S >= 2 ? 1 : 0;
+  const int known = cache[dev][slot].load(std::memory_order_relaxed);
+  if (known != 0) return known;
+  auto kernel = tc_decode_kernel<false>;
+  int n = 0;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kSmemBytes)) == cudaSuccess) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(S));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(S);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) n = 0;
+  }
+  cudaGetLastError();
+  if (n > 0) cache[dev][slot].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+int decode_cluster(int N, int K, int num_sms) {
+  const int64_t groups = (N + NW - 1) / NW;
+  const int64_t kb_total = (K + BK - 1) / BK;
+  const int64_t slots = num_sms;
+  if (groups * 5 >= slots * 3) return 1;  // whole groups, or runs of them
+  // The largest power of two S <= 8 (portable cluster size) with at least
+  // one k-block per CTA and all groups' clusters resident at once (more would
+  // run in two waves: 16 clusters of 8 took twice as long as 8).
+  int S = 1;
+  while (S < 8 && groups * S * 2 <= slots && S * 2 <= kb_total &&
+         groups <= decode_max_clusters(S * 2))
+    S *= 2;
+  return S;
+}
+
 int decode_grid(int N, int K, int num_sms) {
   const int64_t groups = (N + NW - 1) / NW;
   const int64_t units = groups * ((K + BK - 1) / BK);
   const int64_t slots = num_sms;
-  // Enough column groups to keep most SMs streaming: one CTA per group, so
-  // no group's k range is split and no partial sums are exchanged.  Fewer
-  // groups: split k over all SMs.  More groups than SMs: each CTA takes a run
-  // of whole groups (only the groups at run boundaries are split).
-  if (groups <= slots && groups * 5 >= slots * 3) return static_cast<int>(groups);
+  // Enough column groups to keep most SMs streaming (>= ~60 % of them): one
+  // CTA per group, so no group's k range is split and no partial sums are
+  // exchanged.  Fewer groups: clusters of S CTAs per group split its k range
+  // evenly (run_start then never crosses a group) and add their partial sums
+  // through distributed shared memory; where no S >= 2 fits, whole groups
+  // again.  More groups than SMs: each CTA takes a run of whole groups (only
+  // the groups at run boundaries are split, through the workspace).
+  if (groups <= slots) {
+    const int S = decode_cluster(N, K, num_sms);
+    return static_cast<int>(groups * S);
+  }
   return static_cast<int>(units < slots ? units : slots);
 }
 
@@ -599,11 +742,19 @@ cudaError_t launch_tc_decode(const DecodeArgs& a, const CUtensorMap* tmA, const 
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (a.cluster > 1) {
+    if (num_ctas % a.cluster != 0) return cudaErrorInvalidValue;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = static_cast<unsigned>(a.cluster);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
   e = cudaLaunchKernelEx(&cfg, kernel, a, *tmA, *tmB);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

@@ -125,6 +125,7 @@ extern "C" gemm_status_t gemm_bf16gemm_decode_static(int64_t M, int64_t N, int64
   a.counters = scratch;
   a.workspace = reinterpret_cast<float*>(scratch + kStaticCounters);
   a.err = err_word;
+  a.cluster = decode_cluster(n, k, num_sms);
   const cudaError_t e = launch_tc_decode(a, &tmA, &tmB, grid, cs);
   if (e != cudaSuccess) {
     cudaGetLastError();

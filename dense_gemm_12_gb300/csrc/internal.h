@@ -150,6 +150,8 @@ struct DecodeArgs {
   float* workspace;     // partial sums, see decode_workspace_floats
   uint32_t* counters;   // one arrival counter per 128-column n-tile, zeroed
   uint32_t* err;
+  int cluster;          // > 1: clusters of this many CTAs split each column
+                        // group's k range (decode_cluster); 0 or 1: none
 };
 
 // bf16 decode GEMM (M <= 16): tcgen05 with the operands swapped
@@ -163,6 +165,10 @@ int decode_b_box_rows();
 int64_t decode_workspace_floats(int N, int K, int num_ctas);
 int64_t decode_counter_count(int N);
 int decode_grid(int N, int K, int num_sms);
+// CTAs per cluster of the decode launch (1: no clusters): when the column
+// groups are few, the CTAs of a cluster split one group's k range and add
+// their partial sums through distributed shared memory (no workspace).
+int decode_cluster(int N, int K, int num_sms);
 
 // Pieces of the C ABI shared with entry points in other translation units.
 }  // namespace g12

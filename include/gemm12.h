@@ -49,10 +49,13 @@
  *             are reported by gemm_check_device_error().
  *  Threads    Entry points may be called from several host threads on
  *             different streams.
- *  Memory     Calls whose work is split along k -- the decode kernel of
- *             gemm_bf16gemm (M <= 16), and gemm_sgemm / gemm_bf16gemm when
- *             the last wave of output tiles is split to balance the SMs --
- *             need scratch memory (partial sums and arrival counters).  The
+ *  Memory     Calls whose work is split along k through global memory --
+ *             the decode kernel of gemm_bf16gemm (M <= 16) when N exceeds
+ *             128 x the SM count (narrower decode shapes exchange partial
+ *             sums in shared memory and need none), and gemm_sgemm /
+ *             gemm_bf16gemm when the last wave of output tiles is split to
+ *             balance the SMs -- need scratch memory (partial sums and
+ *             arrival counters).  The
  *             library allocates it per device and per stream the first time a
  *             call on that stream needs it (or more of it), keeps and reuses
  *             it, and gemm_shutdown() frees it; calls on different streams

@@ -59,10 +59,53 @@ def test_decode_shapes(M, N, K):
     check_device_error()
 
 
+@pytest.mark.parametrize("M,N,K", [
+    (16, 1024, 4096),   # 8 column groups: clusters of 8 CTAs
+    (8, 2048, 1000),    # 16 groups: clusters of 4 (16 clusters of 8 do not fit at once)
+    (16, 4096, 4096),   # 32 groups x 4
+    (5, 8192, 2048),    # 64 groups x 2
+    (16, 1000, 300),    # ragged N; 3 k-blocks: clusters of 2
+    (3, 200, 8192),     # 2 groups x 8, the last one mostly past N
+    (1, 9000, 777),     # 71 groups x 2, K not a multiple of 128
+])
+def test_decode_cluster_split_integers_exact(M, N, K):
+    # few column groups: clusters of CTAs split each group's k range and add
+    # their partial sums, in k order, through distributed shared memory
+    A, B, C = make_inputs(M, N, K, ("int", None), ("int", None), ("int", None),
+                          seed=M + N + K, dtype="bf16")
+    ref32, _, _ = oracle_bf16(A, B, C, 1.5, -0.5)
+    outs = []
+    for _ in range(3):
+        out, st, _, _, dC = run_bf16gemm(A, B, C, 1.5, -0.5, ldc=N + 3)
+        assert st == 0
+        assert np.array_equal(out.numpy().view(np.uint32), ref32.view(np.uint32))
+        assert dC.untouched_outside()
+        outs.append(out)
+    check_device_error()
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 28672, 2048), (1, 20000, 1024), (7, 19500, 3000)])
+def test_decode_runs_of_groups(M, N, K):
+    # more column groups than SMs: each CTA takes a run of whole groups and
+    # the groups at run boundaries are combined through the workspace
+    A, B, C = make_inputs(M, N, K, ("normal", 1.0), ("normal", 0.02), ("uniform", None),
+                          seed=N + K, dtype="bf16")
+    outs = []
+    for _ in range(3):
+        out, st, _, _, dC = run_bf16gemm(A, B, C, 0.75, 0.5)
+        assert st == 0
+        assert dC.untouched_outside()
+        outs.append(out)
+    _, ref64, den = oracle_bf16(A, B, C, 0.75, 0.5)
+    assert ratio(outs[0], ref64, den) <= TOL_BF16
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int32), outs[0].view(torch.int32))
+    check_device_error()
+
+
 @pytest.mark.parametrize("N,K", [(128, 8192), (384, 4096), (256, 16384), (1000, 2048)])
 def test_decode_many_contributors(N, K):
-    # few column groups, long k: up to ~128 CTAs add into one group, which
-    # exercises the arrival-counter hand-off and both fix-up paths
+    # few column groups, long k: clusters of 8 CTAs per group
     M = 16
     A, B, C = make_inputs(M, N, K, ("normal", 1.0), ("normal", 0.02), ("uniform", None),
                           seed=N + K, dtype="bf16")
