@@ -148,7 +148,7 @@ gemm_path_t select_path(bool bf16, int64_t M, int64_t N, int64_t K, float alpha,
   }
   const bool tma = tma_ok(A, lda, 2) && tma_ok(B, ldb, 2);
   if (!tma) return GEMM_PATH_SIMT_BF16;
-  if (M <= kDecBM) return GEMM_PATH_TC_DECODE;
+  if (decode_path(M, N, K)) return GEMM_PATH_TC_DECODE;
   return M <= kTcBM ? GEMM_PATH_TC_BF16 : GEMM_PATH_TC_BF16_PAIR;
 }
 
@@ -581,7 +581,7 @@ int gemm_split_parts(int is_bf16, int64_t M, int64_t N, int64_t K) {
   const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
   const TileConfig tc = resolve_config(is_bf16 != 0, M, N, K, st->num_sms, nullptr, nullptr);
   if (is_bf16) {
-    if (M <= kDecBM) return 1;
+    if (decode_path(M, N, K)) return 1;
     return tc_plan(m, n, k, st->num_sms, &tc).split;
   }
   return simt_plan_max_parts(simt_plan(m, n, k, st->num_sms, &tc, true), m, n, k);
@@ -744,19 +744,21 @@ static gemm_status_t run_bf16_tensor_core(DeviceState* st, gemm_path_t path, int
     return from_cuda(launch_tc_bf16(a, pl, &tmA, &tmB, cs));
   }
   // GEMM_PATH_TC_DECODE
-  if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, K, M, lda, 64, kDecBM,
+  if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, K, M, lda, 64,
+                 static_cast<uint32_t>(decode_rows(static_cast<int>(M))),
                  CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, N, K, ldb, 64,
                  static_cast<uint32_t>(decode_b_box_rows()), CU_TENSOR_MAP_SWIZZLE_128B))
     return GEMM_ERR_LAUNCH;
-  const int grid = decode_grid(static_cast<int>(N), static_cast<int>(K), st->num_sms);
+  const int grid =
+      decode_grid(static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), st->num_sms);
   DecodeArgs a{};
   a.M = static_cast<int>(M);
   a.N = static_cast<int>(N);
   a.K = static_cast<int>(K);
   a.epi = epi;
   a.err = st->err_word;
-  a.cluster = decode_cluster(a.N, a.K, st->num_sms);
+  a.cluster = decode_cluster(a.M, a.N, a.K, st->num_sms);
   // One CTA per column group, or clusters that exchange their partial sums
   // in shared memory: no scratch is touched.
   if (grid == decode_counter_count(a.N) || a.cluster > 1) {
@@ -766,7 +768,7 @@ static gemm_status_t run_bf16_tensor_core(DeviceState* st, gemm_path_t path, int
   }
   if (!lock.owns_lock()) lock.lock();
   Scratch* sc = nullptr;
-  gemm_status_t s = ensure_scratch(*st, cs, decode_workspace_floats(a.N, a.K, grid),
+  gemm_status_t s = ensure_scratch(*st, cs, decode_workspace_floats(a.M, a.N, a.K, grid),
                                    decode_counter_count(a.N), &sc);
   if (s != GEMM_OK) return s;
   a.workspace = sc->ws;
@@ -803,7 +805,7 @@ static gemm_status_t bf16gemm_impl(int64_t M, int64_t N, int64_t K, float alpha,
     lock.lock();
     s = stage_operands(*st, cs, 2, M, N, K, A, lda, B, ldb);
     if (s == GEMM_OK)
-      path = M <= kTcBM ? GEMM_PATH_TC_BF16 : GEMM_PATH_TC_BF16_PAIR;
+      path = select_path(true, M, N, K, alpha, A, lda, B, ldb);  // on the aligned copies
     else if (s != GEMM_ERR_NO_MEMORY)
       return s;
     // No memory for the copies: the CUDA-core kernel reads the operands as
@@ -859,7 +861,7 @@ static gemm_status_t get_config(int is_bf16, int64_t M, int64_t N, int64_t K, ge
   if (st == nullptr) return s;
   *out = gemm_config_t{GEMM_KERNEL_AUTO, 0, 0};
   if (from_table != nullptr) *from_table = 0;
-  if (is_bf16 && M <= kDecBM) return GEMM_OK;  // the decode kernel plans itself
+  if (is_bf16 && decode_path(M, N, K)) return GEMM_OK;  // the decode kernel plans itself
   bool table = false;
   const TileConfig tc =
       resolve_config(is_bf16 != 0, M, N, K, st->num_sms, nullptr, &table, use_table);
@@ -951,8 +953,7 @@ gemm_status_t gemm_bf16gemm_fused(int64_t M, int64_t N, int64_t K, float alpha, 
     lock.lock();
     s = stage_operands(*st, cs, 2, M, N, K, A, lda, B, ldb);
     if (s != GEMM_OK) return s;
-    run_path = M <= kDecBM ? GEMM_PATH_TC_DECODE
-                           : (M <= kTcBM ? GEMM_PATH_TC_BF16 : GEMM_PATH_TC_BF16_PAIR);
+    run_path = select_path(true, M, N, K, alpha, A, lda, B, ldb);  // on the aligned copies
   }
   return run_bf16_tensor_core(st, run_path, M, N, K, A, lda, B, ldb, epi, cs, nullptr, lock);
 }

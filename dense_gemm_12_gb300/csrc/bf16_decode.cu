@@ -57,17 +57,16 @@ constexpr int NW = NSUB * BN;              // columns of C per n-group
 constexpr int kBoxesPerTile = BN / 64;     // 64-column TMA boxes per MMA tile
 // Accumulator rows held by each epilogue warp (one 32-lane TMEM quarter each).
 constexpr int kRowsPerQuarter = 32;
-constexpr int BMr = kDecBM;                // MMA N: rows of A / C
 #ifndef G12_DECODE_BK
 #define G12_DECODE_BK 128
 #endif
 constexpr int BK = G12_DECODE_BK;          // k per stage (one unit)
 static_assert(BK == 64 || BK == 128, "k per stage must be 64 or 128");
-constexpr int kABoxes = BK / 64;           // 16 x 64 boxes of A per stage
+constexpr int kABoxes = BK / 64;           // BMr x 64 boxes of A per stage
 constexpr int kBoxBytesB = BK * 64 * 2;                   // one 64-column box of B
 constexpr int kStageBytesB = NSUB * kBoxesPerTile * kBoxBytesB;
-constexpr int kStageBytesA = BMr * BK * 2;                // 2 KB
-constexpr int kStageBytes = kStageBytesB + kStageBytesA;  // multiple of 1024
+// Rows of C the output stage handles at a time (one 32x32b.x16 TMEM load).
+constexpr int kChunk = 16;
 #ifndef G12_DECODE_SMEM_KB
 #define G12_DECODE_SMEM_KB 220
 #endif
@@ -82,7 +81,6 @@ constexpr uint64_t kHandoffWaitNs = 20000;
 // 0 units 17.92 us, 2 17.75, 4 17.68, 6 17.65, 8 17.77 -- more delays the
 // CTA's own first TMA loads).
 constexpr int kEarlyUnits = G12_DECODE_EARLY_UNITS;
-constexpr int kStageBudget = (G12_DECODE_SMEM_KB * 1024) / kStageBytes;
 #ifndef G12_DECODE_ISSUERS
 #define G12_DECODE_ISSUERS 2
 #endif
@@ -94,35 +92,45 @@ static_assert(kIssuers == 1 || kIssuers == 2, "one or two MMA issuers");
 constexpr int kThreads = 192 + (kIssuers - 1) * 32;
 constexpr int kEpiThreads = 128;
 constexpr int kSecondIssuerWarp = 6;
-// Stages are a multiple of the issuer count, so that every stage is always
-// consumed by the same issuer.  An issuer then waits for the rounds of its
-// stages strictly in order; if two issuers alternated on one stage, one could
-// wait for round r+1 before round r completed, which a parity wait cannot
-// tell apart.
-constexpr int STAGES = ((kStageBudget > 20 ? 20 : kStageBudget) / kIssuers) * kIssuers;
-static_assert(STAGES >= kIssuers && STAGES % kIssuers == 0, "stages per issuer");
-constexpr uint32_t kIssuerCols = NSUB * BMr;              // TMEM columns per issuer
-constexpr uint32_t kAccCols = kIssuers * kIssuerCols;     // TMEM columns per segment
-constexpr uint32_t kTmemCols = 2 * kAccCols < 32 ? 32 : 2 * kAccCols;
-constexpr uint32_t kIdesc = idesc_bf16_f32(BN, BMr, /*A MN-major*/ 1, /*B MN-major*/ 0);
-constexpr int kPartialFloats = BMr * NW;
+// Shape of one instance of the kernel: BMR rows of A and C (the MMA's N:
+// 16, 32 or 64; a launch with M rows uses the smallest BMR >= M).
+template <int BMR>
+struct DecCfg {
+  static_assert(BMR == 16 || BMR == 32 || BMR == 64, "rows of a decode launch");
+  static constexpr int BMr = BMR;
+  static constexpr int kChunks = BMR / kChunk;
+  static constexpr int kStageBytesA = BMR * BK * 2;                  // 4, 8 or 16 KB
+  static constexpr int kStageBytes = kStageBytesB + kStageBytesA;    // multiple of 1024
+  static constexpr int kStageBudget = (G12_DECODE_SMEM_KB * 1024) / kStageBytes;
+  // Stages are a multiple of the issuer count, so that every stage is always
+  // consumed by the same issuer.  An issuer then waits for the rounds of its
+  // stages strictly in order; if two issuers alternated on one stage, one
+  // could wait for round r+1 before round r completed, which a parity wait
+  // cannot tell apart.
+  static constexpr int STAGES = ((kStageBudget > 20 ? 20 : kStageBudget) / kIssuers) * kIssuers;
+  static_assert(STAGES >= kIssuers && STAGES % kIssuers == 0, "stages per issuer");
+  static constexpr uint32_t kIssuerCols = NSUB * BMR;           // TMEM columns per issuer
+  static constexpr uint32_t kAccCols = kIssuers * kIssuerCols;  // TMEM columns per segment
+  static constexpr uint32_t kTmemCols = 2 * kAccCols < 32 ? 32 : 2 * kAccCols;
+  static constexpr uint32_t kIdesc = idesc_bf16_f32(BN, BMR, /*A MN-major*/ 1, /*B MN-major*/ 0);
+  static constexpr int kPartialFloats = BMR * NW;
+  static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
+  static_assert((kTmemCols & (kTmemCols - 1)) == 0, "TMEM allocation must be a power of 2");
+  static_assert(kPartialFloats * 4 <= kStageBytes, "a cluster's partial sums fit in stage 0");
 
-static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
-static_assert((kTmemCols & (kTmemCols - 1)) == 0, "TMEM allocation must be a power of 2");
-
-struct __align__(8) DecSmemTail {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
-  uint64_t tmem_full[2];
-  uint64_t tmem_empty[2];
-  uint64_t drain[2];
-  uint32_t tmem_base;
-  int abort_flag;
-  int last_flag;
-  int others_ready;  // set once every other contributor of the segment's group has published
+  struct __align__(8) Tail {
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t tmem_full[2];
+    uint64_t tmem_empty[2];
+    uint64_t drain[2];
+    uint32_t tmem_base;
+    int abort_flag;
+    int last_flag;
+    int others_ready;  // set once every other contributor of the segment's group has published
+  };
+  static constexpr size_t kSmemBytes = 1024 + STAGES * kStageBytes + sizeof(Tail);
 };
-
-constexpr size_t kSmemBytes = 1024 + STAGES * kStageBytes + sizeof(DecSmemTail);
 
 struct Split {
   int64_t units;       // n_groups * kb_total
@@ -155,23 +163,30 @@ __device__ __forceinline__ void named_bar_epi() {
   asm volatile("bar.sync 1, %0;" ::"r"(kEpiThreads) : "memory");
 }
 
-// Old values of column n of C (rows < M), loaded ahead of time so that the
-// final write of a column costs no read round trip.
-__device__ __forceinline__ void load_c_column(const DecodeArgs& p, int n, float (&old)[BMr]) {
+// Old values of rows m0 .. m0 + kChunk - 1 of column n of C (rows < M; the
+// first chunk is loaded ahead of time so that its final write costs no read
+// round trip).
+__device__ __forceinline__ void load_c_column(const DecodeArgs& p, int n, int m0,
+                                              float (&old)[kChunk]) {
   const Epilogue& e = p.epi;
   const float* c = e.C + n;
 #pragma unroll
-  for (int m = 0; m < BMr; ++m)
-    old[m] = (e.beta != 0.0f && n < p.N && m < p.M) ? c[static_cast<int64_t>(m) * e.ldc] : 0.0f;
+  for (int i = 0; i < kChunk; ++i) {
+    const int m = m0 + i;
+    old[i] = (e.beta != 0.0f && n < p.N && m < p.M) ? c[static_cast<int64_t>(m) * e.ldc] : 0.0f;
+  }
 }
 
-// Residual values of column n (rows < M), loaded ahead like old C values.
-__device__ __forceinline__ void load_r_column(const DecodeArgs& p, int n, float (&res)[BMr]) {
+// Residual values of the same rows of column n, loaded like old C values.
+__device__ __forceinline__ void load_r_column(const DecodeArgs& p, int n, int m0,
+                                              float (&res)[kChunk]) {
   const Epilogue& e = p.epi;
 #pragma unroll
-  for (int m = 0; m < BMr; ++m)
-    res[m] = (e.R != nullptr && n < p.N && m < p.M) ? e.R[static_cast<int64_t>(m) * e.ldr + n]
+  for (int i = 0; i < kChunk; ++i) {
+    const int m = m0 + i;
+    res[i] = (e.R != nullptr && n < p.N && m < p.M) ? e.R[static_cast<int64_t>(m) * e.ldr + n]
                                                      : 0.0f;
+  }
 }
 
 // Column n of this thread through the output stage (see epilogue.cuh).
@@ -179,54 +194,59 @@ __device__ __forceinline__ void load_r_column(const DecodeArgs& p, int n, float 
 // activation, no residual, d_scale 1, no amax), compiled without the general
 // stage.
 template <bool FUSED>
-__device__ __forceinline__ void store_c_column(const DecodeArgs& p, int n, const float (&v)[BMr],
-                                               const float (&old)[BMr], const float (&res)[BMr],
-                                               float& amax_acc) {
+__device__ __forceinline__ void store_c_column(const DecodeArgs& p, int n, int m0,
+                                               const float (&v)[kChunk],
+                                               const float (&old)[kChunk],
+                                               const float (&res)[kChunk], float& amax_acc) {
   if (n >= p.N) return;
   const Epilogue& e = p.epi;
   if (!FUSED) {
     // plain GEMM: D is C itself (fp32, ldd == ldc)
     float* d = static_cast<float*>(e.D) + n;
 #pragma unroll
-    for (int m = 0; m < BMr; ++m)
+    for (int i = 0; i < kChunk; ++i) {
+      const int m = m0 + i;
       if (m < p.M)
         d[static_cast<int64_t>(m) * e.ldc] =
-            (e.beta != 0.0f) ? fmaf(e.alpha, v[m], e.beta * old[m]) : e.alpha * v[m];
+            (e.beta != 0.0f) ? fmaf(e.alpha, v[i], e.beta * old[i]) : e.alpha * v[i];
+    }
     return;
   }
   const float bias = epi_bias(e, n);  // one column: one bias value, loaded before any store
 #pragma unroll
-  for (int m = 0; m < BMr; ++m)
+  for (int i = 0; i < kChunk; ++i) {
+    const int m = m0 + i;
     if (m < p.M) {
-      const float val = epi_value(e, v[m], old[m], bias, res[m]);
+      const float val = epi_value(e, v[i], old[i], bias, res[i]);
       epi_track(e, amax_acc, val);
       epi_store1(e, m, n, val);
     }
+  }
 }
 
 // Cluster split (p.cluster = S > 1): the S CTAs of a cluster hold the partial
 // sums of one column group over S consecutive k ranges (rank order = k
-// order), each as a BMr x NW fp32 array at shared address `part` (same offset
+// order), each as a BMR x NW fp32 array at shared address `part` (same offset
 // in every CTA).  CTA `rank` writes columns [rank NW / S, (rank + 1) NW / S)
-// of the group: epilogue thread ept takes one of them and 16 / S of its rows,
+// of the group: epilogue thread ept takes one of them and BMR / S of its rows,
 // reads the S partial sums of each element from the cluster's shared memory,
 // adds them in rank order (a fixed order: results do not depend on timing)
 // and runs the output stage.  Called by the 128 epilogue threads between two
 // cluster barriers.
-template <bool FUSED>
+template <bool FUSED, int BMR>
 __device__ __forceinline__ void cluster_reduce_store(const DecodeArgs& p, uint32_t part, int ept) {
   const int S = p.cluster;
   const int rank = static_cast<int>(cluster_cta_rank());
   const int ng = static_cast<int>(blockIdx.x) / S;
   const int slice = NW / S;                      // columns written by this CTA
-  const int rows = BMr * slice / kEpiThreads;    // rows per thread: 16 / S
+  const int rows = BMR * slice / kEpiThreads;    // rows per thread: BMR / S
   const int col = rank * slice + ept % slice;
   const int m0 = (ept / slice) * rows;
   const int n = ng * NW + col;
   const Epilogue& e = p.epi;
   float amax_acc = 0.0f;
   if (n < p.N) {
-    constexpr int kMaxRows = BMr / 2;  // S >= 2
+    constexpr int kMaxRows = BMR / 2;  // S >= 2
     float v[kMaxRows], old[kMaxRows], res[kMaxRows];
     const float bias = FUSED ? epi_bias(e, n) : 0.0f;
 #pragma unroll
@@ -260,13 +280,22 @@ __device__ __forceinline__ void cluster_reduce_store(const DecodeArgs& p, uint32
   if (FUSED) epi_flush_amax(e, amax_acc);
 }
 
-template <bool FUSED>
+template <bool FUSED, int BMR>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_decode_kernel(const __grid_constant__ DecodeArgs p, const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB) {
+  using Cfg = DecCfg<BMR>;
+  constexpr int BMr = BMR;
+  constexpr int STAGES = Cfg::STAGES;
+  constexpr int kStageBytes = Cfg::kStageBytes;
+  constexpr uint32_t kIssuerCols = Cfg::kIssuerCols;
+  constexpr uint32_t kAccCols = Cfg::kAccCols;
+  constexpr uint32_t kTmemCols = Cfg::kTmemCols;
+  constexpr uint32_t kIdesc = Cfg::kIdesc;
+  constexpr int kPartialFloats = Cfg::kPartialFloats;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = align_smem<1024>(smem_raw);
-  DecSmemTail* tail = reinterpret_cast<DecSmemTail*>(smem + STAGES * kStageBytes);
+  auto* tail = reinterpret_cast<typename Cfg::Tail*>(smem + STAGES * kStageBytes);
   volatile int* abort_flag = &tail->abort_flag;
 
   const int warp = threadIdx.x >> 5;
@@ -436,19 +465,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       // if so, preload them, so that once this segment's accumulator is ready
       // the group's result is a few adds away.
       const bool clustered = p.cluster > 1;
-      float old[NSUB][BMr], res[NSUB][BMr];
+      // Old C and residual values of the first 16-row chunk (the only chunk
+      // when BMr == 16), loaded while the MMAs of this segment run; further
+      // chunks are loaded when stored.  (A cluster split loads them in
+      // cluster_reduce_store.)
+      float old[NSUB][kChunk], res[NSUB][kChunk];
 #pragma unroll
       for (int j = 0; j < NSUB; ++j) {
-        // (a cluster split loads C and the residual in cluster_reduce_store)
         const int nc = (row_valid && !clustered) ? ng * NW + j * BN + n_local : p.N;
-        load_c_column(p, nc, old[j]);
-        if (FUSED) load_r_column(p, nc, res[j]);
+        load_c_column(p, nc, 0, old[j]);
+        if (FUSED) load_r_column(p, nc, 0, res[j]);
       }
+      // While the MMAs of this segment run, watch whether every other
+      // contributor of the n-group has already published its partial sums --
+      // if so, preload them (one 16-row chunk: BMr == 16 only), so that once
+      // this segment's accumulator is ready the group's result is a few adds
+      // away.
       constexpr int kPre = 2;  // partial sums of other CTAs held in registers
-      float pre[kPre][NSUB][BMr];
+      float pre[kPre][NSUB][kChunk];
       bool preloaded = false;
-      const bool can_preload =
-          row_valid && !whole && !clustered && (nsegs - 1 <= static_cast<uint32_t>(kPre));
+      const bool can_preload = Cfg::kChunks == 1 && row_valid && !whole && !clustered &&
+                               (nsegs - 1 <= static_cast<uint32_t>(kPre));
       auto preload = [&]() {
         // the kk-th contributor other than this CTA, in CTA order
 #pragma unroll
@@ -461,7 +498,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < NSUB; ++j)
 #pragma unroll
-            for (int m = 0; m < BMr; ++m) pre[kk][j][m] = __ldcg(src + m * NW + j * BN + n_local);
+            for (int m = 0; m < kChunk; ++m)
+              pre[kk][j][m] = __ldcg(src + m * NW + j * BN + n_local);
         }
       };
 
@@ -491,41 +529,61 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Leave together if a wait ran out anywhere (see named_bar_any).
       if (named_bar_any(1, kEpiThreads, !ok)) break;
       tc_fence_after_sync();
-      uint32_t r[NSUB][16];
+      // This thread's column of the segment's sums, BMr rows, read from TMEM
+      // 16 rows at a time.  Issuer qq wrote an accumulator for this segment
+      // iff one of the segment's units has stage index it = u - u_begin with
+      // it % kIssuers == qq; the written ones are added in issuer order.
+      uint32_t r[NSUB][BMr];
       {
-        uint32_t acc[kIssuers][NSUB][16];
-#pragma unroll
-        for (int qq = 0; qq < kIssuers; ++qq)
-#pragma unroll
-          for (int j = 0; j < NSUB; ++j)
-            tmem_ld_32x32b_x16(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                   ab * kAccCols + qq * kIssuerCols + j * BMr,
-                               acc[qq][j]);
-        tc_wait_ld();
-        tc_fence_before_sync();
-        mbar_arrive(&tail->tmem_empty[ab]);
-        // Issuer qq wrote an accumulator for this segment iff one of the
-        // segment's units has stage index it = u - u_begin with it % kIssuers
-        // == qq; sum the written ones in issuer order.
         const int64_t it0 = u - u_begin;
         const int64_t len = seg_end_u - u;
 #pragma unroll
-        for (int j = 0; j < NSUB; ++j)
+        for (int c = 0; c < Cfg::kChunks; ++c) {
+          uint32_t acc[kIssuers][NSUB][kChunk];
 #pragma unroll
-          for (int m = 0; m < BMr; ++m) {
-            float v = 0.0f;
-            bool any = false;
+          for (int qq = 0; qq < kIssuers; ++qq)
 #pragma unroll
-            for (int qq = 0; qq < kIssuers; ++qq) {
-              const bool wrote = len >= kIssuers || it0 % kIssuers == qq;
-              if (wrote) {
-                v = any ? v + __uint_as_float(acc[qq][j][m]) : __uint_as_float(acc[qq][j][m]);
-                any = true;
+            for (int j = 0; j < NSUB; ++j)
+              tmem_ld_32x32b_x16(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                     ab * kAccCols + qq * kIssuerCols + j * BMr + c * kChunk,
+                                 acc[qq][j]);
+          tc_wait_ld();
+#pragma unroll
+          for (int j = 0; j < NSUB; ++j)
+#pragma unroll
+            for (int i = 0; i < kChunk; ++i) {
+              float v = 0.0f;
+              bool any = false;
+#pragma unroll
+              for (int qq = 0; qq < kIssuers; ++qq) {
+                const bool wrote = len >= kIssuers || it0 % kIssuers == qq;
+                if (wrote) {
+                  v = any ? v + __uint_as_float(acc[qq][j][i]) : __uint_as_float(acc[qq][j][i]);
+                  any = true;
+                }
               }
+              r[j][c * kChunk + i] = __float_as_uint(v);
             }
-            r[j][m] = __float_as_uint(v);
-          }
+        }
+        tc_fence_before_sync();
+        mbar_arrive(&tail->tmem_empty[ab]);
       }
+      // Output stage of rows c*16 .. c*16 + 15 of column n: old C and
+      // residual values of chunk 0 were loaded ahead.
+      auto store_chunk = [&](int j, int c, const float (&v)[kChunk]) {
+        const int n = row_valid ? ng * NW + j * BN + n_local : p.N;
+        if (c == 0) {
+          store_c_column<FUSED>(p, n, 0, v, old[j], res[j], amax_acc);
+        } else {
+          float oc[kChunk], rc[kChunk];
+          load_c_column(p, n, c * kChunk, oc);
+          if (FUSED) load_r_column(p, n, c * kChunk, rc);
+          else
+#pragma unroll
+            for (int i = 0; i < kChunk; ++i) rc[i] = 0.0f;
+          store_c_column<FUSED>(p, n, c * kChunk, v, oc, rc, amax_acc);
+        }
+      };
 
       if (clustered) {
         // This CTA's k range is its run's only segment: every MMA has read
@@ -540,13 +598,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else if (whole) {
 #pragma unroll
-        for (int j = 0; j < NSUB; ++j) {
-          float v[BMr];
+        for (int j = 0; j < NSUB; ++j)
 #pragma unroll
-          for (int m = 0; m < BMr; ++m) v[m] = __uint_as_float(r[j][m]);
-          store_c_column<FUSED>(p, row_valid ? ng * NW + j * BN + n_local : p.N, v, old[j], res[j],
-                                amax_acc);
-        }
+          for (int c = 0; c < Cfg::kChunks; ++c) {
+            float v[kChunk];
+#pragma unroll
+            for (int i = 0; i < kChunk; ++i) v[i] = __uint_as_float(r[j][c * kChunk + i]);
+            store_chunk(j, c, v);
+          }
       } else {
         // last_flag: 2 = every other contributor had already arrived (this
         // CTA adds its own sum straight from registers and publishes nothing),
@@ -591,34 +650,36 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (fin == 1) __threadfence();  // acquire the other partials after the atomic
           const bool use_pre = (fin == 2) && preloaded;
 #pragma unroll
-          for (int j = 0; j < NSUB; ++j) {
-            // add the partial sums in k order (CTA order), whoever arrived last
-            float sum[BMr];
+          for (int j = 0; j < NSUB; ++j)
 #pragma unroll
-            for (int m = 0; m < BMr; ++m) sum[m] = 0.0f;
-            int k = 0;
-            for (int64_t cc = c_first; cc <= c_last; ++cc) {
-              if (cc == blockIdx.x) {
+            for (int c = 0; c < Cfg::kChunks; ++c) {
+              // add the partial sums in k order (CTA order), whoever arrived last
+              float sum[kChunk];
 #pragma unroll
-                for (int m = 0; m < BMr; ++m) sum[m] += __uint_as_float(r[j][m]);
-              } else if (use_pre) {
+              for (int i = 0; i < kChunk; ++i) sum[i] = 0.0f;
+              int k = 0;
+              for (int64_t cc = c_first; cc <= c_last; ++cc) {
+                if (cc == blockIdx.x) {
 #pragma unroll
-                for (int kk = 0; kk < kPre; ++kk)
-                  if (kk == k)
+                  for (int i = 0; i < kChunk; ++i) sum[i] += __uint_as_float(r[j][c * kChunk + i]);
+                } else if (use_pre) {
 #pragma unroll
-                    for (int m = 0; m < BMr; ++m) sum[m] += pre[kk][j][m];
-                ++k;
-              } else {
-                const int sl = static_cast<int>(ng - run_start(sp, cc) / sp.kb_total);
-                const float* src = p.workspace + (cc * sp.segs_max + sl) * kPartialFloats;
+                  for (int kk = 0; kk < kPre; ++kk)
+                    if (kk == k)
 #pragma unroll
-                for (int m = 0; m < BMr; ++m)
-                  sum[m] += row_valid ? __ldcg(src + m * NW + j * BN + n_local) : 0.0f;
+                      for (int i = 0; i < kChunk; ++i) sum[i] += pre[kk][j][i];
+                  ++k;
+                } else {
+                  const int sl = static_cast<int>(ng - run_start(sp, cc) / sp.kb_total);
+                  const float* src = p.workspace + (cc * sp.segs_max + sl) * kPartialFloats;
+#pragma unroll
+                  for (int i = 0; i < kChunk; ++i)
+                    sum[i] += row_valid ? __ldcg(src + (c * kChunk + i) * NW + j * BN + n_local)
+                                        : 0.0f;
+                }
               }
+              store_chunk(j, c, sum);
             }
-            store_c_column<FUSED>(p, row_valid ? ng * NW + j * BN + n_local : p.N, sum, old[j],
-                                  res[j], amax_acc);
-          }
           if (ept == 0) p.counters[ng] = 0u;
         }
         if (ept == 0) tail->others_ready = 0;
@@ -637,22 +698,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     // out (each wait above is bounded), so none can hang here.
     cluster_sync();  // the partial sums of every CTA of the cluster are written
     if (warp >= 2 && warp <= 5)
-      cluster_reduce_store<FUSED>(p, smem_u32(smem), static_cast<int>(threadIdx.x) - 64);
+      cluster_reduce_store<FUSED, BMR>(p, smem_u32(smem), static_cast<int>(threadIdx.x) - 64);
     cluster_sync();  // no CTA leaves while another may still read its shared memory
   }
   tc_fence_after_sync();
   if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
 }
 
-}  // namespace
-
-int decode_b_box_rows() { return BK; }
-
 // Clusters of S decode CTAs that can be resident at once on the current
 // device (cudaOccupancyMaxActiveClusters; one CTA per SM, and a cluster must
 // fit in one GPC: on a 152-SM GB300, 76 of 2, 36 of 4, 15 of 8).  Queried
-// once per device and size.
-int decode_max_clusters(int S) {
+// once per device, kernel instance and size.
+template <int BMR>
+int max_clusters_of(int S) {
   constexpr int kMaxDev = 64;
   static std::atomic<int> cache[kMaxDev][4];  // S = 1, 2, 4, 8; 0 = not yet known
   int dev = 0;
@@ -663,14 +721,14 @@ int decode_max_clusters(int S) {
   const int slot = S >= 8 ? 3 : S >= 4 ? 2 : S >= 2 ? 1 : 0;
   const int known = cache[dev][slot].load(std::memory_order_relaxed);
   if (known != 0) return known;
-  auto kernel = tc_decode_kernel<false>;
+  auto kernel = tc_decode_kernel<false, BMR>;
   int n = 0;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(kSmemBytes)) == cudaSuccess) {
+                           static_cast<int>(DecCfg<BMR>::kSmemBytes)) == cudaSuccess) {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(S));
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.dynamicSmemBytes = DecCfg<BMR>::kSmemBytes;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = static_cast<unsigned>(S);
@@ -685,53 +743,16 @@ int decode_max_clusters(int S) {
   return n;
 }
 
-int decode_cluster(int N, int K, int num_sms) {
-  const int64_t groups = (N + NW - 1) / NW;
-  const int64_t kb_total = (K + BK - 1) / BK;
-  const int64_t slots = num_sms;
-  if (groups * 5 >= slots * 3) return 1;  // whole groups, or runs of them
-  // The largest power of two S <= 8 (portable cluster size) with at least
-  // one k-block per CTA and all groups' clusters resident at once (more would
-  // run in two waves: 16 clusters of 8 took twice as long as 8).
-  int S = 1;
-  while (S < 8 && groups * S * 2 <= slots && S * 2 <= kb_total &&
-         groups <= decode_max_clusters(S * 2))
-    S *= 2;
-  return S;
+int decode_max_clusters(int S, int rows) {
+  return rows <= 16 ? max_clusters_of<16>(S) : rows <= 32 ? max_clusters_of<32>(S)
+                                                          : max_clusters_of<64>(S);
 }
 
-int decode_grid(int N, int K, int num_sms) {
-  const int64_t groups = (N + NW - 1) / NW;
-  const int64_t units = groups * ((K + BK - 1) / BK);
-  const int64_t slots = num_sms;
-  // Enough column groups to keep most SMs streaming (>= ~60 % of them): one
-  // CTA per group, so no group's k range is split and no partial sums are
-  // exchanged.  Fewer groups: clusters of S CTAs per group split its k range
-  // evenly (run_start then never crosses a group) and add their partial sums
-  // through distributed shared memory; where no S >= 2 fits, whole groups
-  // again.  More groups than SMs: each CTA takes a run of whole groups (only
-  // the groups at run boundaries are split, through the workspace).
-  if (groups <= slots) {
-    const int S = decode_cluster(N, K, num_sms);
-    return static_cast<int>(groups * S);
-  }
-  return static_cast<int>(units < slots ? units : slots);
-}
-
-int64_t decode_workspace_floats(int N, int K, int num_ctas) {
-  const Split s = make_split(N, K, num_ctas);
-  return static_cast<int64_t>(num_ctas) * s.segs_max * kPartialFloats;
-}
-
-int64_t decode_counter_count(int N) { return (N + NW - 1) / NW; }
-
-cudaError_t launch_tc_decode(const DecodeArgs& a, const CUtensorMap* tmA, const CUtensorMap* tmB,
-                             int num_ctas, cudaStream_t stream) {
-  const Epilogue& ep = a.epi;
-  const bool fused = ep.bias != nullptr || ep.act != kActNone || ep.R != nullptr ||
-                     ep.d_type != kOutF32 || ep.d_scale != 1.0f || ep.amax != nullptr ||
-                     ep.D != static_cast<const void*>(ep.C) || ep.ldd != ep.ldc;
-  auto kernel = fused ? tc_decode_kernel<true> : tc_decode_kernel<false>;
+template <int BMR>
+cudaError_t launch_rows(const DecodeArgs& a, const CUtensorMap* tmA, const CUtensorMap* tmB,
+                        int num_ctas, bool fused, cudaStream_t stream) {
+  constexpr size_t kSmemBytes = DecCfg<BMR>::kSmemBytes;
+  auto kernel = fused ? tc_decode_kernel<true, BMR> : tc_decode_kernel<false, BMR>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
@@ -758,6 +779,66 @@ cudaError_t launch_tc_decode(const DecodeArgs& a, const CUtensorMap* tmA, const 
   e = cudaLaunchKernelEx(&cfg, kernel, a, *tmA, *tmB);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+}  // namespace
+
+int decode_b_box_rows() { return BK; }
+
+int decode_rows(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : 64; }
+
+int decode_cluster(int M, int N, int K, int num_sms) {
+  const int64_t groups = (N + NW - 1) / NW;
+  const int64_t kb_total = (K + BK - 1) / BK;
+  const int64_t slots = num_sms;
+  if (groups * 5 >= slots * 3) return 1;  // whole groups, or runs of them
+  // The largest power of two S <= 8 (portable cluster size) with at least
+  // one k-block per CTA and all groups' clusters resident at once (more would
+  // run in two waves: 16 clusters of 8 took twice as long as 8).
+  const int rows = decode_rows(M);
+  int S = 1;
+  while (S < 8 && groups * S * 2 <= slots && S * 2 <= kb_total &&
+         groups <= decode_max_clusters(S * 2, rows))
+    S *= 2;
+  return S;
+}
+
+int decode_grid(int M, int N, int K, int num_sms) {
+  const int64_t groups = (N + NW - 1) / NW;
+  const int64_t units = groups * ((K + BK - 1) / BK);
+  const int64_t slots = num_sms;
+  // Enough column groups to keep most SMs streaming (>= ~60 % of them): one
+  // CTA per group, so no group's k range is split and no partial sums are
+  // exchanged.  Fewer groups: clusters of S CTAs per group split its k range
+  // evenly (run_start then never crosses a group) and add their partial sums
+  // through distributed shared memory; where no S >= 2 fits, whole groups
+  // again.  More groups than SMs: each CTA takes a run of whole groups (only
+  // the groups at run boundaries are split, through the workspace).
+  if (groups <= slots) {
+    const int S = decode_cluster(M, N, K, num_sms);
+    return static_cast<int>(groups * S);
+  }
+  return static_cast<int>(units < slots ? units : slots);
+}
+
+int64_t decode_workspace_floats(int M, int N, int K, int num_ctas) {
+  const Split s = make_split(N, K, num_ctas);
+  return static_cast<int64_t>(num_ctas) * s.segs_max * decode_rows(M) * NW;
+}
+
+int64_t decode_counter_count(int N) { return (N + NW - 1) / NW; }
+
+cudaError_t launch_tc_decode(const DecodeArgs& a, const CUtensorMap* tmA, const CUtensorMap* tmB,
+                             int num_ctas, cudaStream_t stream) {
+  const Epilogue& ep = a.epi;
+  const bool fused = ep.bias != nullptr || ep.act != kActNone || ep.R != nullptr ||
+                     ep.d_type != kOutF32 || ep.d_scale != 1.0f || ep.amax != nullptr ||
+                     ep.D != static_cast<const void*>(ep.C) || ep.ldd != ep.ldc;
+  if (a.M < 1 || a.M > kDecMaxM) return cudaErrorInvalidValue;
+  const int rows = decode_rows(a.M);
+  if (rows == 16) return launch_rows<16>(a, tmA, tmB, num_ctas, fused, stream);
+  if (rows == 32) return launch_rows<32>(a, tmA, tmB, num_ctas, fused, stream);
+  return launch_rows<64>(a, tmA, tmB, num_ctas, fused, stream);
 }
 
 }  // namespace g12

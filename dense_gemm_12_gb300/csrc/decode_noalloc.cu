@@ -98,9 +98,10 @@ extern "C" gemm_status_t gemm_bf16gemm_decode_static(int64_t M, int64_t N, int64
   if (s != GEMM_OK) return s;
 
   const int n = static_cast<int>(N), k = static_cast<int>(K);
-  const int grid = decode_grid(n, k, num_sms);
+  const int m = static_cast<int>(M);
+  const int grid = decode_grid(m, n, k, num_sms);
   const int64_t counters = decode_counter_count(n);
-  const int64_t partials = decode_workspace_floats(n, k, grid);
+  const int64_t partials = decode_workspace_floats(m, n, k, grid);
   if (counters > kStaticCounters || partials > kStaticPartialFloats) return GEMM_ERR_UNSUPPORTED;
 
   uint32_t* scratch = scratch_on_current_device(&s);
@@ -125,7 +126,7 @@ extern "C" gemm_status_t gemm_bf16gemm_decode_static(int64_t M, int64_t N, int64
   a.counters = scratch;
   a.workspace = reinterpret_cast<float*>(scratch + kStaticCounters);
   a.err = err_word;
-  a.cluster = decode_cluster(n, k, num_sms);
+  a.cluster = decode_cluster(m, n, k, num_sms);
   const cudaError_t e = launch_tc_decode(a, &tmA, &tmB, grid, cs);
   if (e != cudaSuccess) {
     cudaGetLastError();

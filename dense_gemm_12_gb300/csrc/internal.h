@@ -159,16 +159,31 @@ struct DecodeArgs {
 cudaError_t launch_tc_decode(const DecodeArgs& a, const CUtensorMap* tmA,
                              const CUtensorMap* tmB, int num_ctas, cudaStream_t stream);
 constexpr int kDecBN = 128, kDecBM = 16;
+// Largest M the decode kernel takes (instances for 16, 32 and 64 rows: the
+// MMA's N); larger M runs on the tile kernels.
+constexpr int kDecMaxM = 64;
+// Whether automatic dispatch runs a bf16 M x N x K GEMM on the decode kernel:
+// every M <= 32, and 32 < M <= 64 while B has fewer than 2^26 elements.
+// Measured against the tile kernels (back-to-back launches): M = 17-64 with
+// N x K = 4096 x 4096, 1024 x 4096 and 12288 x 4096 1.2-1.9x faster on the
+// decode kernel; M = 64 with 8192 x 8192 66 us vs 50 us and 28672 x 4096
+// 53 us vs 51 us on the tile kernels.
+inline bool decode_path(int64_t M, int64_t N, int64_t K) {
+  if (M > kDecMaxM) return false;
+  return M <= 32 || N * K < (int64_t{1} << 26);
+}
+// Rows of the kernel instance a launch with M rows uses (16, 32 or 64).
+int decode_rows(int M);
 // k-rows of B per TMA box of the decode kernel (the A box is always 64 wide).
 int decode_b_box_rows();
 // Workspace floats and counters a decode launch of this shape needs.
-int64_t decode_workspace_floats(int N, int K, int num_ctas);
+int64_t decode_workspace_floats(int M, int N, int K, int num_ctas);
 int64_t decode_counter_count(int N);
-int decode_grid(int N, int K, int num_sms);
+int decode_grid(int M, int N, int K, int num_sms);
 // CTAs per cluster of the decode launch (1: no clusters): when the column
 // groups are few, the CTAs of a cluster split one group's k range and add
 // their partial sums through distributed shared memory (no workspace).
-int decode_cluster(int N, int K, int num_sms);
+int decode_cluster(int M, int N, int K, int num_sms);
 
 // Pieces of the C ABI shared with entry points in other translation units.
 }  // namespace g12

@@ -50,7 +50,7 @@
  *  Threads    Entry points may be called from several host threads on
  *             different streams.
  *  Memory     Calls whose work is split along k through global memory --
- *             the decode kernel of gemm_bf16gemm (M <= 16) when N exceeds
+ *             the decode kernel of gemm_bf16gemm (small M) when N exceeds
  *             128 x the SM count (narrower decode shapes exchange partial
  *             sums in shared memory and need none), and gemm_sgemm /
  *             gemm_bf16gemm when the last wave of output tiles is split to
@@ -116,9 +116,11 @@ gemm_status_t gemm_sgemm(int64_t M, int64_t N, int64_t K, float alpha,
  * (ldb), C: M x N fp32 (ldc), device pointers, row-major.  The tensor-core
  * path ("Tiled matrix multiplication", "How it works": tensor cores fed from
  * shared memory by asynchronous copies) runs on the 5th-generation tensor
- * cores with the accumulator in tensor memory.  M <= 16 takes the
+ * cores with the accumulator in tensor memory.  Small M takes the
  * bandwidth-bound decode kernel (the "decode GEMV (M <= 16)" case of "Tiled
- * matrix multiplication", "Avoid when"), which splits K across CTAs
+ * matrix multiplication", "Avoid when", widened here to every M <= 32, and
+ * to 32 < M <= 64 while N * K < 2^26, where it measured faster than the tile
+ * kernels; gemm_select_path reports GEMM_PATH_TC_DECODE), which splits K across CTAs
  * ("Split-K" in the same page's "Variants and alternatives") and reduces the
  * partial sums in a fixed order, so results are deterministic.  Error bound:
  * 8e-3 of |alpha|*(|A||B|)_ij + |beta|*|C_ij| against the exact product of the
@@ -183,7 +185,7 @@ typedef struct {
 /*
  * gemm_bf16gemm_fused -- bf16 GEMM (A, B, lda, ldb as in gemm_bf16gemm) with
  * the output stage `out` (see gemm_output_t).  The same tensor-core kernels
- * as gemm_bf16gemm run (including the decode kernel for M <= 16).
+ * as gemm_bf16gemm run (including the decode kernel for small M).
  * Aliasing: D may be C itself only when d_type is GEMM_OUT_F32 and
  * ldd == ldc, and may be the residual itself only when d_type is
  * GEMM_OUT_F32 and ldd == ldr (each output element is read before it is
@@ -220,7 +222,7 @@ gemm_status_t gemm_bf16gemm_fused(int64_t M, int64_t N, int64_t K, float alpha,
  * leading dimension ldd >= max(1, N), 4-byte aligned for fp32 and 2-byte for
  * bf16; D may be C itself only when d_type is GEMM_OUT_F32 and ldd == ldc,
  * otherwise D must not overlap A, B, C or bias.  The same tensor-core kernels
- * as gemm_bf16gemm run (including the decode kernel for M <= 16); operands
+ * as gemm_bf16gemm run (including the decode kernel for small M); operands
  * the TMA engine cannot describe are staged as in gemm_bf16gemm_fused; an
  * unknown act or a d_type other than GEMM_OUT_F32 and GEMM_OUT_BF16 returns
  * GEMM_ERR_INVALID_VALUE.  K == 0 or alpha == 0: D = act(beta*C +
@@ -330,8 +332,8 @@ gemm_path_t gemm_select_path(int is_bf16, int64_t M, int64_t N, int64_t K,
  * 1 means no item is split.  Under the stream-K tail (GEMM_SPLIT_STREAM)
  * the tail tiles are cut into differing numbers of k-ranges; the largest is
  * reported.  `is_bf16`
- * selects gemm_bf16gemm's tensor-core kernels (M > 16) instead of
- * gemm_sgemm's CUDA-core kernel; the decode kernel (bf16, M <= 16) plans its
+ * selects gemm_bf16gemm's tensor-core tile kernels instead of gemm_sgemm's
+ * CUDA-core kernel; the decode kernel (bf16, small M) plans its
  * own split and reports 1 here.  Returns 0 for negative sizes or when there
  * is no usable sm_103a device (the plan depends on its SM count).
  */
@@ -381,7 +383,7 @@ typedef struct {
  * the launch configuration pinned by cfg (cfg == NULL or all fields 0: the
  * same as the plain call).  The result is the same GEMM within the same bound
  * for every configuration (bit-identical where the sums are exact).  A pinned
- * bf16 kernel always runs the tcgen05 tile kernels, also for M <= 16 (the
+ * bf16 kernel always runs the tcgen05 tile kernels, also for small M (the
  * decode kernel runs only under GEMM_KERNEL_AUTO).  The fp32 path has two
  * tile widths (GEMM_KERNEL_SINGLE_CTA: 128 x 128, GEMM_KERNEL_WIDE:
  * 128 x 256); GEMM_KERNEL_CTA_PAIR is invalid there, and GEMM_KERNEL_WIDE
@@ -407,7 +409,7 @@ gemm_status_t gemm_bf16gemm_config(int64_t M, int64_t N, int64_t K, float alpha,
 /*
  * gemm_get_config -- host-only: the configuration automatic dispatch uses for
  * an M x N x K problem on the current device (every field resolved; for the
- * bf16 decode shapes, M <= 16, kernel is GEMM_KERNEL_AUTO and the other
+ * bf16 shapes of the decode kernel, kernel is GEMM_KERNEL_AUTO and the other
  * fields 0: the decode kernel plans itself).  *from_table (may be NULL) is
  * set to 1 when the entry came from the sweep's table, 0 for the cost model.
  * Errors: out == NULL or negative sizes: GEMM_ERR_INVALID_VALUE; no usable

@@ -4,8 +4,9 @@ The header allows calls from several host threads on different streams; the
 split-K paths then need each stream's own scratch (partial sums, arrival
 counters), created and grown on first use under a lock.  Each thread runs
 GEMMs whose work is split along k -- the CUDA-core kernel with a pinned
-split, the CTA-pair kernel's split tail, the decode kernel split over all
-SMs -- in a different order and with scratch growing at different times, and
+split, the CTA-pair kernel's split tail, the decode kernel's runs of column
+groups combined through scratch, and its cluster split, which needs none --
+in a different order and with scratch growing at different times, and
 every result must equal, bit for bit, the same call run alone beforehand
 (fixed plans sum their parts in a fixed order, so results are reproducible).
 """
@@ -55,17 +56,30 @@ def _cases():
                              0.5, out.data_ptr(), 10240, stream.cuda_stream)
         assert st == 0
     cases.append(("bf16_pair_split", pair, (512, 10240)))
-    # decode kernel: 32 column groups, k split over all SMs (scratch needed)
-    A3, B3, C3 = make_inputs(16, 4096, 4096, ("normal", 1.0), ("normal", 0.05),
+    # decode kernel: 160 column groups, more than SMs, so CTAs take runs of
+    # groups and combine the split ones through the stream's scratch
+    A3, B3, C3 = make_inputs(16, 20480, 2048, ("normal", 1.0), ("normal", 0.05),
                              ("uniform", None), seed=43, dtype="bf16")
     dA3, dB3, C30 = A3.cuda(), B3.cuda(), C3.cuda()
 
     def decode(stream, out):
         out.copy_(C30)
-        st = g.gemm_bf16gemm(16, 4096, 4096, 1.0, dA3.data_ptr(), 4096, dB3.data_ptr(), 4096,
+        st = g.gemm_bf16gemm(16, 20480, 2048, 1.0, dA3.data_ptr(), 2048, dB3.data_ptr(), 20480,
+                             1.0, out.data_ptr(), 20480, stream.cuda_stream)
+        assert st == 0
+    cases.append(("decode_split", decode, (16, 20480)))
+    # decode kernel, 32 groups: clusters of 4 add their partial sums in
+    # shared memory (no scratch)
+    A4, B4, C4 = make_inputs(40, 4096, 4096, ("normal", 1.0), ("normal", 0.05),
+                             ("uniform", None), seed=44, dtype="bf16")
+    dA4, dB4, C40 = A4.cuda(), B4.cuda(), C4.cuda()
+
+    def decode_cluster(stream, out):
+        out.copy_(C40)
+        st = g.gemm_bf16gemm(40, 4096, 4096, 1.0, dA4.data_ptr(), 4096, dB4.data_ptr(), 4096,
                              1.0, out.data_ptr(), 4096, stream.cuda_stream)
         assert st == 0
-    cases.append(("decode_split", decode, (16, 4096)))
+    cases.append(("decode_cluster", decode_cluster, (40, 4096)))
     return cases
 
 

@@ -44,11 +44,12 @@ def test_decode_integers_exact():
     assert np.array_equal(out.numpy(), ref32)
 
 
-@pytest.mark.parametrize("M", [1, 2, 5, 8, 15, 16])
+@pytest.mark.parametrize("M", [1, 2, 5, 8, 15, 16, 17, 31, 32, 40, 64])
 @pytest.mark.parametrize("N,K", [(128, 64), (1000, 1000), (12288, 4096), (200, 8192), (4096, 72)])
 def test_decode_shapes(M, N, K):
-    if N * K > 12288 * 4096 // 2 and M not in (1, 16):
-        pytest.skip("large shape checked at M = 1 and 16 only")
+    # M <= 16, <= 32 and <= 64 run the kernel's 16-, 32- and 64-row instances
+    if N * K > 12288 * 4096 // 2 and M not in (1, 16, 32, 64):
+        pytest.skip("large shape checked at M = 1, 16, 32 and 64 only")
     A, B, C = make_inputs(M, N, K, ("normal", 1.0), ("normal", 0.02), ("uniform", None),
                           seed=M * 1000 + N + K, dtype="bf16")
     out, st, _, _, dC = run_bf16gemm(A, B, C, 0.5, 1.0)
@@ -69,6 +70,21 @@ def test_decode_shapes(M, N, K):
     (1, 9000, 777),     # 71 groups x 2, K not a multiple of 128
 ])
 def test_decode_cluster_split_integers_exact(M, N, K):
+    _cluster_exact(M, N, K)
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (32, 1024, 4096),   # 32-row instance, clusters of 8
+    (64, 2048, 1000),   # 64-row instance, clusters of 4
+    (48, 8192, 2048),   # 64-row instance, clusters of 2
+    (20, 12288, 512),   # 32-row instance, whole groups
+    (64, 200, 8192),    # ragged N, clusters of 8
+])
+def test_decode_wide_rows_integers_exact(M, N, K):
+    _cluster_exact(M, N, K)
+
+
+def _cluster_exact(M, N, K):
     # few column groups: clusters of CTAs split each group's k range and add
     # their partial sums, in k order, through distributed shared memory
     A, B, C = make_inputs(M, N, K, ("int", None), ("int", None), ("int", None),
@@ -84,7 +100,8 @@ def test_decode_cluster_split_integers_exact(M, N, K):
     check_device_error()
 
 
-@pytest.mark.parametrize("M,N,K", [(16, 28672, 2048), (1, 20000, 1024), (7, 19500, 3000)])
+@pytest.mark.parametrize("M,N,K", [(16, 28672, 2048), (1, 20000, 1024), (7, 19500, 3000),
+                                   (64, 20000, 1024), (24, 19500, 2000)])
 def test_decode_runs_of_groups(M, N, K):
     # more column groups than SMs: each CTA takes a run of whole groups and
     # the groups at run boundaries are combined through the workspace

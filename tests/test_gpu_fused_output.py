@@ -103,7 +103,9 @@ def _int_case(M, N, K, seed):
 # Integer inputs: every partial sum is an integer below 2^24 and the scales
 # are powers of two, so v and d_scale * v are exact on both sides.
 INT_SHAPES = [
-    (8, 1000, 512),       # decode kernel (M <= 16)
+    (8, 1000, 512),       # decode kernel (M <= 16), clusters of 4
+    (40, 1000, 512),      # decode kernel, 64-row instance
+    (24, 16384, 256),     # decode kernel, 32-row instance, whole column groups
     (100, 520, 256),      # single-CTA kernel, ragged N
     (384, 512, 256),      # CTA-pair kernel, odd number of tile rows
     (100, 1024, 4096),    # single-CTA kernel, tiles split along k
@@ -139,6 +141,7 @@ def test_empty_product_integers_exact(M, N, K):
 
 @pytest.mark.parametrize("M,N,K", [
     (16, 12288, 1024),    # decode kernel
+    (64, 4096, 2048),     # decode kernel, 64-row instance, clusters of 4
     (128, 2048, 512),     # single-CTA kernel
     (640, 1280, 1000),    # CTA-pair kernel, ragged K
     (512, 10240, 4096),   # CTA-pair kernel, last round split along k
