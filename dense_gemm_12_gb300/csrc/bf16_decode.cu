@@ -1,15 +1,17 @@
-// bf16_decode.cu -- decode-shaped GEMM (M <= 16): C = alpha * A * B + beta * C
-// with bf16 A (M x K) and B (K x N), fp32 accumulation and fp32 C.
+// bf16_decode.cu -- decode-shaped GEMM (small M, up to 64): C = alpha * A * B +
+// beta * C with bf16 A (M x K) and B (K x N), fp32 accumulation and fp32 C.
 //
 // "Tiled matrix multiplication" ("Avoid when") notes that a decode GEMV with
-// M <= 16 is bound by memory bandwidth: the whole cost is streaming B once.
-// With M = 16 no tile of C is big enough to fill the machine, so the k range
+// M <= 16 is bound by memory bandwidth: the whole cost is streaming B once
+// (and so it stays for a few times that M).  With M = 16 no tile of C is big
+// enough to fill the machine, so the k range
 // is split across CTAs and the partial sums are reduced afterwards ("Split-K"
 // in the same page's "Variants and alternatives"; "A GEMM Kernel, Step by
 // Step", "What is left").  On sm_103a the tensor core's smallest M is 128, so
 // the product is computed transposed, D^T = B^T A^T: the MMA's M runs over
-// 128 columns of C and its N (16) over the rows of A, and no row of the MMA
-// is padding.
+// 128 columns of C and its N over the rows of A: the kernel has instances
+// for N = 16, 32 and 64 (a launch with M rows takes the smallest that holds
+// them), and no row of the MMA's M is padding.
 //
 // Work split.  B is cut into n-groups of 128 columns; a unit is one n-group x
 // 128 values of k (32 KB of B, fetched as two 64 x 128 TMA boxes).  With at
@@ -31,8 +33,8 @@
 // partials.  Partials are always added in k order, so results are
 // deterministic, and the combiner resets the counter for the next launch.
 //
-// Roles: warp 0 TMA producer (B boxes and two 16 x 64 K-major boxes of A per
-// stage), warps 1 and 6 issue the MMAs (128 x 16 x 16, alternate stages,
+// Roles: warp 0 TMA producer (B boxes and two BMr x 64 K-major boxes of A per
+// stage), warps 1 and 6 issue the MMAs (128 x BMr x 16, alternate stages,
 // one accumulator each, double-buffered; warp 1 owns TMEM), warps 2..5 read
 // the accumulators, combine and write C.  The launch uses programmatic
 // dependent launch: the next kernel in the stream may set up while this one

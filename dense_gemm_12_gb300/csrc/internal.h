@@ -154,8 +154,9 @@ struct DecodeArgs {
                         // group's k range (decode_cluster); 0 or 1: none
 };
 
-// bf16 decode GEMM (M <= 16): tcgen05 with the operands swapped
-// (D^T = B^T A^T, MMA M = 128 over N, MMA N = 16 over M), split over K.
+// bf16 decode GEMM (M <= kDecMaxM): tcgen05 with the operands swapped
+// (D^T = B^T A^T, MMA M = 128 over N, MMA N = 16, 32 or 64 over M), split
+// over K.
 cudaError_t launch_tc_decode(const DecodeArgs& a, const CUtensorMap* tmA,
                              const CUtensorMap* tmB, int num_ctas, cudaStream_t stream);
 constexpr int kDecBN = 128, kDecBM = 16;
