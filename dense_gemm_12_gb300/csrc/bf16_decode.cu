@@ -235,51 +235,68 @@ __device__ __forceinline__ void store_c_column(const DecodeArgs& p, int n, int m
 // adds them in rank order (a fixed order: results do not depend on timing)
 // and runs the output stage.  Called by the 128 epilogue threads between two
 // cluster barriers.
-template <bool FUSED, int BMR>
-__device__ __forceinline__ void cluster_reduce_store(const DecodeArgs& p, uint32_t part, int ept) {
-  const int S = p.cluster;
+template <bool FUSED, int BMR, int S>
+__device__ __forceinline__ void cluster_reduce_store_s(const DecodeArgs& p, uint32_t part,
+                                                       int ept) {
+  constexpr int slice = NW / S;                    // columns written by this CTA
+  constexpr int rows = BMR * slice / kEpiThreads;  // rows per thread: BMR / S
+  static_assert(rows >= 1 && rows * S == BMR, "rows per thread");
   const int rank = static_cast<int>(cluster_cta_rank());
   const int ng = static_cast<int>(blockIdx.x) / S;
-  const int slice = NW / S;                      // columns written by this CTA
-  const int rows = BMR * slice / kEpiThreads;    // rows per thread: BMR / S
   const int col = rank * slice + ept % slice;
   const int m0 = (ept / slice) * rows;
   const int n = ng * NW + col;
   const Epilogue& e = p.epi;
   float amax_acc = 0.0f;
   if (n < p.N) {
-    constexpr int kMaxRows = BMR / 2;  // S >= 2
-    float v[kMaxRows], old[kMaxRows], res[kMaxRows];
-    const float bias = FUSED ? epi_bias(e, n) : 0.0f;
+    // Every load is issued before any sum: the S x rows partial sums of this
+    // thread's elements from the cluster's shared memory, and the old C and
+    // residual values (one round trip in all, not one per element).
+    float val[S][rows], old[rows], res[rows];
+    const uint32_t a0 = part + static_cast<uint32_t>((m0 * NW + col) * 4);
 #pragma unroll
-    for (int i = 0; i < kMaxRows; ++i) {
-      const int m = m0 + i;
-      v[i] = old[i] = res[i] = 0.0f;
-      if (i < rows && m < p.M) {
-        if (e.beta != 0.0f) old[i] = e.C[static_cast<int64_t>(m) * e.ldc + n];
-        if (FUSED) res[i] = epi_residual(e, m, n);
-        const uint32_t a = part + static_cast<uint32_t>((m * NW + col) * 4);
-        v[i] = ld_shared_cluster_f32(mapa_shared(a, 0));
-        for (int q = 1; q < S; ++q) v[i] += ld_shared_cluster_f32(mapa_shared(a, q));
-      }
+    for (int q = 0; q < S; ++q) {
+      const uint32_t aq = mapa_shared(a0, static_cast<uint32_t>(q));
+#pragma unroll
+      for (int i = 0; i < rows; ++i) val[q][i] = ld_shared_cluster_f32(aq + i * NW * 4);
     }
 #pragma unroll
-    for (int i = 0; i < kMaxRows; ++i) {
+    for (int i = 0; i < rows; ++i) {
       const int m = m0 + i;
-      if (i < rows && m < p.M) {
+      old[i] = (e.beta != 0.0f && m < p.M) ? e.C[static_cast<int64_t>(m) * e.ldc + n] : 0.0f;
+      res[i] = (FUSED && m < p.M) ? epi_residual(e, m, n) : 0.0f;
+    }
+    const float bias = FUSED ? epi_bias(e, n) : 0.0f;
+#pragma unroll
+    for (int i = 0; i < rows; ++i) {
+      const int m = m0 + i;
+      float v = val[0][i];
+#pragma unroll
+      for (int q = 1; q < S; ++q) v += val[q][i];  // rank order = k order
+      if (m < p.M) {
         if (!FUSED) {
           // plain GEMM: D is C itself (fp32, ldd == ldc)
           static_cast<float*>(e.D)[static_cast<int64_t>(m) * e.ldc + n] =
-              (e.beta != 0.0f) ? fmaf(e.alpha, v[i], e.beta * old[i]) : e.alpha * v[i];
+              (e.beta != 0.0f) ? fmaf(e.alpha, v, e.beta * old[i]) : e.alpha * v;
         } else {
-          const float val = epi_value(e, v[i], old[i], bias, res[i]);
-          epi_track(e, amax_acc, val);
-          epi_store1(e, m, n, val);
+          const float out = epi_value(e, v, old[i], bias, res[i]);
+          epi_track(e, amax_acc, out);
+          epi_store1(e, m, n, out);
         }
       }
     }
   }
   if (FUSED) epi_flush_amax(e, amax_acc);
+}
+
+template <bool FUSED, int BMR>
+__device__ __forceinline__ void cluster_reduce_store(const DecodeArgs& p, uint32_t part, int ept) {
+  if (p.cluster == 2)
+    cluster_reduce_store_s<FUSED, BMR, 2>(p, part, ept);
+  else if (p.cluster == 4)
+    cluster_reduce_store_s<FUSED, BMR, 4>(p, part, ept);
+  else
+    cluster_reduce_store_s<FUSED, BMR, 8>(p, part, ept);
 }
 
 template <bool FUSED, int BMR>

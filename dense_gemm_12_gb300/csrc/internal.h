@@ -164,14 +164,15 @@ constexpr int kDecBN = 128, kDecBM = 16;
 // MMA's N); larger M runs on the tile kernels.
 constexpr int kDecMaxM = 64;
 // Whether automatic dispatch runs a bf16 M x N x K GEMM on the decode kernel:
-// every M <= 32, and 32 < M <= 64 while B has fewer than 2^26 elements.
-// Measured against the tile kernels (back-to-back launches): M = 17-64 with
-// N x K = 4096 x 4096, 1024 x 4096 and 12288 x 4096 1.2-1.9x faster on the
-// decode kernel; M = 64 with 8192 x 8192 66 us vs 50 us and 28672 x 4096
-// 53 us vs 51 us on the tile kernels.
+// every M <= 32, and 32 < M <= 64 up to N = 16384.  Measured against the tile
+// kernels (back-to-back launches, us): M = 17, 32, 48, 64 at 4096 x 4096:
+// 10.3, 10.2, 11.9, 11.9 against 27.0-28.7; M = 64 at 8192 x 8192 27.8 vs
+// 49.8, at 12288 x 4096 24.6 vs 43.3; but at N = 28672 (more column groups
+// than SMs) 52.8 vs 51.1 on the tile kernel.
 inline bool decode_path(int64_t M, int64_t N, int64_t K) {
+  (void)K;
   if (M > kDecMaxM) return false;
-  return M <= 32 || N * K < (int64_t{1} << 26);
+  return M <= 32 || N <= 16384;
 }
 // Rows of the kernel instance a launch with M rows uses (16, 32 or 64).
 int decode_rows(int M);

@@ -119,7 +119,7 @@ gemm_status_t gemm_sgemm(int64_t M, int64_t N, int64_t K, float alpha,
  * cores with the accumulator in tensor memory.  Small M takes the
  * bandwidth-bound decode kernel (the "decode GEMV (M <= 16)" case of "Tiled
  * matrix multiplication", "Avoid when", widened here to every M <= 32, and
- * to 32 < M <= 64 while N * K < 2^26, where it measured faster than the tile
+ * to 32 < M <= 64 up to N = 16384, where it measured faster than the tile
  * kernels; gemm_select_path reports GEMM_PATH_TC_DECODE), which splits K across CTAs
  * ("Split-K" in the same page's "Variants and alternatives") and reduces the
  * partial sums in a fixed order, so results are deterministic.  Error bound:

@@ -84,8 +84,9 @@ P = 1 << 20
     (dict(bf16=1, M=17, N=12288, K=4096), "tc_decode"),
     (dict(bf16=1, M=64, N=4096, K=4096), "tc_decode"),
     (dict(bf16=1, M=65, N=4096, K=4096), "tc_bf16"),
-    (dict(bf16=1, M=32, N=8192, K=8192), "tc_decode"),
-    (dict(bf16=1, M=33, N=8192, K=8192), "tc_bf16"),             # B of 2^26 elements
+    (dict(bf16=1, M=32, N=28672, K=4096), "tc_decode"),
+    (dict(bf16=1, M=33, N=16384, K=8192), "tc_decode"),
+    (dict(bf16=1, M=33, N=16392, K=4096), "tc_bf16"),            # wide N: tile kernels
     (dict(bf16=1, M=64, N=64, K=60), "simt_bf16"),                 # lda*2 = 120 B
     (dict(bf16=1, M=64, N=64, K=64, B=P + 2), "simt_bf16"),
     # bf16: staged for the tile kernels (M > 16) from 2^24 FLOPs

@@ -101,7 +101,7 @@ def _cluster_exact(M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K", [(16, 28672, 2048), (1, 20000, 1024), (7, 19500, 3000),
-                                   (64, 20000, 1024), (24, 19500, 2000)])
+                                   (32, 20000, 1024), (24, 19500, 2000)])
 def test_decode_runs_of_groups(M, N, K):
     # more column groups than SMs: each CTA takes a run of whole groups and
     # the groups at run boundaries are combined through the workspace
