@@ -33,9 +33,9 @@ import sys
 
 # (bf16 with M <= 64 runs the decode kernel, which plans itself: no classes)
 BF16_M = [256, 1024, 2048, 4096, 8192]
-BF16_NK = [1024, 4096, 8192]
-FP32_M = [128, 512, 1024, 2048, 4092]
-FP32_NK = [1024, 4092, 8192]
+BF16_NK = [256, 1024, 4096, 8192]
+FP32_M = [128, 256, 512, 1024, 2048, 4092]
+FP32_NK = [256, 1024, 4092, 8192]
 SPLITS = [1, 2, 3, 4, 6, 8]
 GROUPS = [4, 8, 16]
 
