@@ -420,28 +420,40 @@ def bench_decode(torch, g, wl, peaks, device, stream_obj):
     }
 
 
+class OracleSampler:
+    """Times the oracle on whole rows of the 4092^3 workload: the inputs are
+    drawn and the rate calibrated once, then each sample runs as many rows as
+    fit its time budget."""
+
+    def __init__(self, wl):
+        import oracle
+        self.w = wl.WORKLOADS["sgemm_4092"]
+        A, B, C = wl.workload_inputs(self.w)
+        self.A, self.B, self.C = A.numpy(), B.numpy(), C.numpy()
+        self.threads = oracle.max_threads()
+        rows = 4 * self.threads  # calibration: a few rows per thread
+        t0 = time.perf_counter()
+        oracle.sgemm(self.w.alpha, self.A[:rows], self.B, self.w.beta, self.C[:rows])
+        self.sec_per_row = max(time.perf_counter() - t0, 1e-6) / rows
+
+    def sample(self, target_seconds):
+        import oracle
+        w = self.w
+        rows = int(max(1, min(w.M, target_seconds / self.sec_per_row)))
+        t0 = time.perf_counter()
+        oracle.sgemm(w.alpha, self.A[:rows], self.B, w.beta, self.C[:rows])
+        t = time.perf_counter() - t0
+        flops = 2.0 * rows * w.N * w.K
+        return {"value": flops / t / 1e9, "unit": "GFLOP/s", "cores": self.threads,
+                "kind": "oracle",
+                "sample": "%d of 4092 rows of the fp32 4092^3 workload (fp64 triple loop, "
+                          "%.2f s, %s)" % (rows, t, os.uname().machine),
+                "seconds": t}
+
+
 def cpu_oracle_sample(wl, target_seconds):
-    """Time the oracle on whole rows of the 4092^3 workload, sized to ~target."""
-    import numpy as np
-    import oracle
-    w = wl.WORKLOADS["sgemm_4092"]
-    A, B, C = wl.workload_inputs(w)
-    A, B, C = A.numpy(), B.numpy(), C.numpy()
-    threads = oracle.max_threads()
-    rows = 4 * threads  # calibration sample: a few rows per thread
-    t0 = time.perf_counter()
-    oracle.sgemm(w.alpha, A[:rows], B, w.beta, C[:rows])
-    t = time.perf_counter() - t0
-    rows = int(max(4, min(w.M, rows * target_seconds / max(t, 1e-3))))
-    t0 = time.perf_counter()
-    oracle.sgemm(w.alpha, A[:rows], B, w.beta, C[:rows])
-    t = time.perf_counter() - t0
-    flops = 2.0 * rows * w.N * w.K
-    del np
-    return {"value": flops / t / 1e9, "unit": "GFLOP/s", "cores": threads, "kind": "oracle",
-            "sample": "%d of 4092 rows of the fp32 4092^3 workload (fp64 triple loop, "
-                      "%.1f s, %s)" % (rows, t, os.uname().machine),
-            "seconds": t}
+    """One oracle sample of about `target_seconds` on the 4092^3 workload."""
+    return OracleSampler(wl).sample(target_seconds)
 
 
 # ------------------------------------------------------------------ main arms
@@ -452,10 +464,12 @@ def run_reference(args):
         return
     from dense_gemm_12_gb300 import workloads as wl
     w = wl.WORKLOADS["sgemm_4092"]
-    per_step = max(2.0, min(20.0, 150.0 / max(args.steps + args.warmup, 1)))
+    # About 150 s of oracle time for the whole run, whatever --steps is.
+    per_step = max(0.05, min(20.0, 150.0 / max(args.steps + args.warmup, 1)))
+    sampler = OracleSampler(wl)
     for _ in range(args.warmup):
-        cpu_oracle_sample(wl, per_step / 4)
-    samples = [cpu_oracle_sample(wl, per_step) for _ in range(args.steps)]
+        sampler.sample(per_step / 4)
+    samples = [sampler.sample(per_step) for _ in range(args.steps)]
     total_flops = sum(s["value"] * 1e9 * s["seconds"] for s in samples)
     total_t = sum(s["seconds"] for s in samples)
     value = total_flops / total_t / 1e9
