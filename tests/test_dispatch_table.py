@@ -33,6 +33,13 @@ def test_committed_table_is_well_formed():
         assert kernel != 3 or is_bf16 == 0
         assert 1 <= split <= 8 or (split == -1 and is_bf16 == 0)
         assert 1 <= group <= 64
+        # bf16 with M <= 64 runs the decode kernel, which never reads the table
+        assert not (is_bf16 and lm <= 6), "dead bf16 entry for M <= 64"
+
+
+def test_sweep_grid_leaves_decode_shapes_out():
+    assert min(tune.BF16_M) > 64
+    assert min(tune.FP32_M) >= 128 and min(tune.FP32_NK) >= 256
 
 
 def test_ceil_log2_buckets():
