@@ -239,7 +239,11 @@ def gemm_shutdown() -> int:
 
 
 def gemm_select_path(is_bf16, M, N, K, alpha, A, lda, B, ldb) -> str:
-    """Name of the kernel path a call with these arguments takes (host-only)."""
+    """Name of the kernel path a call with these arguments takes (host-only):
+    "simt_tma" / "simt_generic" / "simt_staged" (fp32 on the CUDA cores, with
+    operands loaded by TMA, by generic loads, or from an aligned staging copy),
+    "tc_bf16" / "tc_bf16_pair" / "tc_decode" / "tc_staged" (bf16 on the tensor
+    cores), "simt_bf16" (bf16 widened on the CUDA cores), "scale_c", "none"."""
     return PATHS[load_library().gemm_select_path(int(bool(is_bf16)), M, N, K, alpha, A, lda,
                                                  B, ldb)]
 
