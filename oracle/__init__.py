@@ -217,6 +217,14 @@ def epilogue(ref64, bias=None, act="none", residual=None):
 
 
 # ---------------------------------------------------------------- quantise
+# The output conversion of the fused stage ("Tiled matrix multiplication",
+# "Implementation notes": scaling, then fp8/int8 quantisation).  Reading: the
+# value stored is the exact product d_scale * v rounded ONCE to the output
+# format (round to nearest, ties to even), with d_scale the fp32 number the
+# caller passes.  Nothing in between is rounded to fp32: where a kernel
+# rounds d_scale * v to fp32 first, its extra rounding is part of the error
+# a test allows, not of the definition.
+#
 # fp8 E4M3 as the OCP 8-bit floating point format defines it ("E4M3"): sign
 # bit, 4 exponent bits with bias 7, 3 mantissa bits; exponent field 0 holds
 # the subnormals m * 2^-9; no infinities; S.1111.111 is NaN, so the largest
@@ -226,19 +234,67 @@ _E4M3_MIN_NORMAL = 2.0 ** -6
 _E4M3_SUBNORMAL_STEP = 2.0 ** -9
 
 
-def e4m3_encode(x):
-    """fp32 values -> E4M3 codes (uint8), rounding to nearest, ties to even,
-    saturating finite overflow (and infinities) to +-448; NaN -> 0x7F."""
-    x = np.asarray(x, dtype=np.float32).astype(np.float64)   # exact
-    sign = np.signbit(x).astype(np.uint8) << 7
-    nan = np.isnan(x)
-    a = np.minimum(np.abs(np.where(nan, 0.0, x)), E4M3_MAX)
+def _exact_product(v, d_scale):
+    """d_scale * v as an unevaluated sum hi + lo of two fp64 arrays (exact).
+
+    d_scale is taken as the fp32 number it rounds to (24 significant bits),
+    v as fp64.  v is split (Veltkamp) into halves of at most 27 significant
+    bits each, so both partial products are exact in fp64; their sum is then
+    re-split exactly (Knuth's TwoSum) into hi = fl(hi + lo) and the error lo.
+    Exact for |v| between 2^-900 and 2^900 (no underflow or overflow of the
+    pieces); outside that only lo may be inexact.
+    """
+    s = float(np.float32(d_scale))
+    v = np.asarray(v, dtype=np.float64)
+    with np.errstate(over="ignore", invalid="ignore"):
+        c = 134217729.0 * v                     # 2^27 + 1
+        vh = c - (c - v)
+        vh = np.where(np.isfinite(vh), vh, v)   # huge or non-finite v: no split
+        vl = v - vh
+        a = s * vh
+        b = s * vl
+        hi = a + b
+        bb = hi - a
+        lo = (a - (hi - bb)) + (b - bb)
+    lo = np.where(np.isfinite(hi), lo, 0.0)
+    return hi, lo
+
+
+def _round_on_grid(mag, lo, step):
+    """Round the exact non-negative value mag + lo to the nearest multiple of
+    `step` (a power of two per element), ties to even.
+
+    mag and step are fp64 arrays with mag / step exact and below 2^52; lo is
+    the exact value's part below mag's last bit (|lo| <= half an fp64 ulp of
+    mag).  A rounding boundary (an odd multiple of step / 2) is itself an fp64
+    number, so lo can move the result only when mag lies exactly on one: then
+    the sign of lo says on which side the exact value is, and a zero lo is a
+    true tie, broken toward the even multiple.
+    """
+    q = mag / step
+    f = np.floor(q)
+    r = q - f
+    up = (r > 0.5) | ((r == 0.5) & ((lo > 0) | ((lo == 0) & (np.fmod(f, 2.0) == 1.0))))
+    return (f + up) * step
+
+
+def _e4m3_codes(hi, lo):
+    """E4M3 codes of the exact values hi + lo (see e4m3_encode)."""
+    hi = np.asarray(hi, dtype=np.float64)
+    lo = np.broadcast_to(np.asarray(lo, dtype=np.float64), hi.shape)
+    sign = np.signbit(hi).astype(np.uint8) << 7
+    nan = np.isnan(hi)
+    a = np.abs(np.where(nan, 0.0, hi))
+    lo_mag = np.where(np.signbit(hi), -lo, lo)
+    over = a > E4M3_MAX                     # saturates whatever lo is
+    a = np.where(over, E4M3_MAX, a)
+    lo_mag = np.where(over, 0.0, lo_mag)
     # spacing of representable values around a: 2^-9 below the smallest
     # normal, 2^(e - 3) in the binade [2^e, 2^(e+1))
     _, E = np.frexp(a)                      # a = f 2^E, f in [0.5, 1)
     e = E.astype(np.int64) - 1
     step = np.where(a < _E4M3_MIN_NORMAL, _E4M3_SUBNORMAL_STEP, np.ldexp(1.0, e - 3))
-    y = np.rint(a / step) * step            # np.rint: half to even; a/step exact
+    y = np.minimum(_round_on_grid(a, lo_mag, step), E4M3_MAX)
     # encode y (0 <= y <= 448, representable)
     _, Ey = np.frexp(y)
     ey = Ey.astype(np.int64) - 1
@@ -248,6 +304,13 @@ def e4m3_encode(x):
     code = (exp_field.astype(np.uint8) << 3) | mant.astype(np.uint8)
     code = np.where(nan, np.uint8(0x7F), code | sign)
     return code.astype(np.uint8)
+
+
+def e4m3_encode(x):
+    """Values (taken as fp64) -> E4M3 codes (uint8): round to nearest, ties to
+    even, finite overflow and infinities saturated to +-448, NaN -> 0x7F."""
+    x = np.asarray(x, dtype=np.float64)
+    return _e4m3_codes(x, np.zeros_like(x))
 
 
 def e4m3_decode(code):
@@ -260,25 +323,53 @@ def e4m3_decode(code):
     return np.where((ef == 0xF) & (m == 0x7), np.nan, s * mag)
 
 
+def _s8_codes(hi, lo):
+    """int8 of the exact values hi + lo (see s8_encode)."""
+    hi = np.asarray(hi, dtype=np.float64)
+    lo = np.broadcast_to(np.asarray(lo, dtype=np.float64), hi.shape)
+    nan = np.isnan(hi)
+    a = np.abs(np.where(nan, 0.0, hi))
+    lo_mag = np.where(np.signbit(hi), -lo, lo)
+    big = a >= 256.0                        # saturates whatever lo is
+    r = _round_on_grid(np.where(big, 256.0, a), np.where(big, 0.0, lo_mag), np.ones_like(a))
+    r = np.where(np.signbit(hi), -r, r)
+    return np.clip(r, -128.0, 127.0).astype(np.int8)
+
+
 def s8_encode(x):
-    """fp32 values -> int8: round half to even, saturate to [-128, 127],
-    NaN -> 0."""
-    x = np.asarray(x, dtype=np.float32).astype(np.float64)
-    r = np.clip(np.rint(np.where(np.isnan(x), 0.0, x)), -128.0, 127.0)
-    return r.astype(np.int8)
+    """Values (taken as fp64) -> int8: round half to even, saturate to
+    [-128, 127], NaN -> 0."""
+    x = np.asarray(x, dtype=np.float64)
+    return _s8_codes(x, np.zeros_like(x))
+
+
+def _f32_of(hi, lo):
+    """fp32 nearest to the exact values hi + lo (ties to even), for |hi|
+    between the smallest normal fp32 and the largest finite one."""
+    hi = np.asarray(hi, dtype=np.float64)
+    lo = np.broadcast_to(np.asarray(lo, dtype=np.float64), hi.shape)
+    a = np.abs(hi)
+    lo_mag = np.where(np.signbit(hi), -lo, lo)
+    _, E = np.frexp(np.where(a > 0, a, 1.0))
+    step = np.ldexp(1.0, E.astype(np.int64) - 1 - 23)   # fp32 spacing in a's binade
+    y = _round_on_grid(a, lo_mag, step)
+    y = np.where(np.isfinite(hi), y, a)
+    return np.where(np.signbit(hi), -y, y).astype(np.float32)
 
 
 def quantize(v, d_type, d_scale=1.0):
-    """Output conversion of the fused stage, taken in fp32 like the kernel:
-    x = fp32(d_scale) * fp32(v) (one fp32 multiply), then
-    "f32": x;  "f8e4m3": e4m3_encode(x);  "s8": s8_encode(x)."""
-    x = np.asarray(v, dtype=np.float32) * np.float32(d_scale)
+    """Output conversion of the fused stage: the exact product x = d_scale * v
+    (d_scale the fp32 scale argument, v the fp64 value of the stage) rounded
+    once to the output format:
+    "f32": the nearest fp32;  "f8e4m3": E4M3 codes;  "s8": int8 codes
+    (rounding and saturation as in e4m3_encode / s8_encode)."""
+    hi, lo = _exact_product(v, d_scale)
     if d_type == "f32":
-        return x
+        return _f32_of(hi, lo)
     if d_type == "f8e4m3":
-        return e4m3_encode(x)
+        return _e4m3_codes(hi, lo)
     if d_type == "s8":
-        return s8_encode(x)
+        return _s8_codes(hi, lo)
     raise ValueError("unknown output type %r" % (d_type,))
 
 

@@ -422,15 +422,157 @@ def pin_s8_rounding(orc):
     assert np.array_equal(oracle.s8_encode(np.array([126.5, -0.5], dtype=np.float32)), [126, 0])
 
 
-def pin_quantize_scales_in_fp32(orc):
-    """quantize multiplies by d_scale in fp32 before converting: 0.1 * 3
-    rounds to fp32 first, and a power-of-two scale commutes with the codes."""
+def _e4m3_table():
+    """(value, code) of every non-negative finite E4M3 number, from the OCP
+    8-bit floating point definition: exponent field 0 holds m * 2^-9,
+    exponent field E > 0 holds (1 + m/8) * 2^(E - 7); S.1111.111 is NaN."""
+    out = []
+    for ef in range(16):
+        for m in range(8):
+            if ef == 15 and m == 7:
+                continue
+            val = Fraction(m, 512) if ef == 0 else (1 + Fraction(m, 8)) * Fraction(2) ** (ef - 7)
+            out.append((val, (ef << 3) | m))
+    out.sort()
+    return out
+
+
+def _nearest_even(x, grid):
+    """The entry of the sorted (value, code) grid nearest to the Fraction
+    x >= 0 (ties: the entry whose code is even); x beyond the grid saturates."""
+    import bisect
+    vals = [g[0] for g in grid]
+    i = bisect.bisect_left(vals, x)
+    if i == 0:
+        return grid[0]
+    if i == len(grid):
+        return grid[-1]
+    lo, hi = grid[i - 1], grid[i]
+    dl, dh = x - lo[0], hi[0] - x
+    if dl < dh:
+        return lo
+    if dh < dl:
+        return hi
+    return lo if lo[1] % 2 == 0 else hi
+
+
+def _exact_codes_e4m3(vs, s):
+    grid = _e4m3_table()
+    out = []
+    for v in vs:
+        x = Fraction(float(np.float32(s))) * Fraction(float(v))
+        code = _nearest_even(abs(x), grid)[1]
+        out.append(code | (0x80 if x < 0 or (x == 0 and np.signbit(v)) else 0))
+    return np.array(out, dtype=np.uint8)
+
+
+def _exact_s8(vs, s):
+    out = []
+    for v in vs:
+        x = Fraction(float(np.float32(s))) * Fraction(float(v))
+        f = x.numerator // x.denominator            # floor
+        r = x - f
+        n = f + 1 if (r > Fraction(1, 2) or (r == Fraction(1, 2) and f % 2 == 1)) else f
+        out.append(min(127, max(-128, n)))
+    return np.array(out, dtype=np.int8)
+
+
+def _exact_f32(vs, s):
+    out = []
+    for v in vs:
+        x = Fraction(float(np.float32(s))) * Fraction(float(v))
+        c = np.float32(float(x))
+        cands = {c, np.nextafter(c, np.float32(np.inf)), np.nextafter(c, np.float32(-np.inf))}
+        best = sorted(cands, key=lambda y: (abs(Fraction(float(y)) - x),
+                                            int(np.array(y, np.float32).view(np.uint32)) & 1))
+        out.append(best[0])
+    return np.array(out, dtype=np.float32)
+
+
+def _near_ties(ties, scales, rng):
+    """fp64 values v whose exact products s * v fall exactly on, or within a
+    few fp64 ulps either side of, the given ties."""
+    vs, ss = [], []
+    for t in ties:
+        for s in scales:
+            base = float(t) / float(np.float32(s))
+            for k in (-3, -1, 0, 1, 3):
+                v = base
+                for _ in range(abs(k)):
+                    v = np.nextafter(v, np.inf if k > 0 else -np.inf)
+                sign = rng.choice([-1.0, 1.0])
+                vs.append(sign * v)
+                ss.append(s)
+    return vs, ss
+
+
+def pin_quantize_single_rounding(orc):
+    """The stored code is d_scale * v rounded once: a value just above an
+    E4M3 tie goes up even though its nearest fp32 is the tie itself (rounding
+    through fp32 first would give the even neighbour below): 1.0625 + 2^-40
+    -> 1.125, not 1.0; likewise int8 2.5 + 2^-30 -> 3, not 2; and fp32 output
+    1 + 2^-24 + 2^-40 -> 1 + 2^-23.  An exact tie still goes to even."""
     import oracle
-    v = np.array([3.0], dtype=np.float32)
+    v = np.array([1.0625 + 2.0 ** -40, 1.0625, -(1.0625 + 2.0 ** -40), 17.0 + 2.0 ** -30])
+    assert np.array_equal(oracle.e4m3_decode(oracle.quantize(v, "f8e4m3", 1.0)),
+                          [1.125, 1.0, -1.125, 18.0])
+    assert np.array_equal(oracle.quantize(np.array([2.5 + 2.0 ** -30, 2.5, -2.5 - 2.0 ** -30]),
+                                          "s8", 1.0), [3, 2, -3])
+    assert oracle.quantize(np.array([1.0 + 2.0 ** -24 + 2.0 ** -40]), "f32", 1.0)[0] == \
+        np.float32(1.0 + 2.0 ** -23)
+    assert oracle.quantize(np.array([1.0 + 2.0 ** -24]), "f32", 1.0)[0] == np.float32(1.0)
+
+
+def pin_quantize_exact_rational(orc):
+    """quantize against exact rational arithmetic (fractions.Fraction): the
+    exact product of the fp32 scale and the fp64 value, rounded to the nearest
+    E4M3 value of the format definition (ties to the even code, saturation at
+    448), to the nearest integer (ties to even, clamp to [-128, 127]) and to
+    the nearest fp32 -- on random values over many binades and on values whose
+    exact products sit on, or a few fp64 ulps beside, the formats' ties."""
+    import oracle
+    rng = _rng(44)
+    grid = _e4m3_table()
+    e4m3_ties = [(grid[i][0] + grid[i + 1][0]) / 2 for i in range(len(grid) - 1)]
+    scales = [1.0, 0.1, 3.0, 40.0, 2.0 ** -5, 0.7]
+    vs, ss = _near_ties(e4m3_ties[::3], scales, rng)
+    for s in scales:
+        mag = np.ldexp(rng.uniform(1.0, 2.0, 150), rng.integers(-14, 10, 150))
+        vs += list(mag * rng.choice([-1.0, 1.0], 150) / float(np.float32(s)))
+        ss += [s] * 150
+    vs, ss = np.array(vs), np.array(ss)
+    for s in scales:
+        sel = ss == s
+        got = oracle.quantize(vs[sel], "f8e4m3", s)
+        want = _exact_codes_e4m3(vs[sel], s)
+        zero = (want & 0x7F) == 0               # +0 and -0 are both zero
+        assert np.array_equal(got[~zero], want[~zero])
+        assert np.all((got[zero] & 0x7F) == 0)
+    s8_ties = [Fraction(2 * k + 1, 2) for k in range(-130, 130, 7)]
+    vs8, ss8 = _near_ties(s8_ties, [1.0, 0.1, 3.0], rng)
+    vs8, ss8 = np.array(vs8), np.array(ss8)
+    for s in (1.0, 0.1, 3.0):
+        sel = ss8 == s
+        assert np.array_equal(oracle.quantize(vs8[sel], "s8", s), _exact_s8(vs8[sel], s))
+    f32_ties = [Fraction(float(np.float32(x))) + Fraction(2) ** (int(np.floor(np.log2(x))) - 24)
+                for x in rng.uniform(0.5, 1000.0, 40)]
+    vf, sf = _near_ties(f32_ties, [1.0, 3.0, 0.1], rng)
+    vf, sf = np.array(vf), np.array(sf)
+    for s in (1.0, 3.0, 0.1):
+        sel = sf == s
+        assert np.array_equal(oracle.quantize(vf[sel], "f32", s), _exact_f32(vf[sel], s))
+
+
+def pin_quantize_scale_is_fp32(orc):
+    """d_scale enters as the fp32 number the caller passes: 0.1 becomes
+    fp32(0.1), so 3 * fp32(0.1) rounds to the fp32 product of the two; and a
+    power-of-two scale commutes with the codes."""
+    import oracle
+    v = np.array([3.0])
     assert oracle.quantize(v, "f32", 0.1)[0] == np.float32(np.float32(0.1) * np.float32(3.0))
-    x = _rng(43).uniform(-100, 100, 1000).astype(np.float32)
+    x = _rng(43).uniform(-100, 100, 1000)
     assert np.array_equal(oracle.e4m3_decode(oracle.quantize(x, "f8e4m3", 0.25)),
-                          oracle.e4m3_decode(oracle.e4m3_encode(x * np.float32(0.25))))
+                          oracle.e4m3_decode(oracle.e4m3_encode(x * 0.25)))
 
 
 ALL_PINS = [
@@ -442,5 +584,5 @@ ALL_PINS = [
     pin_thread_count_invariance, pin_epilogue_relu, pin_epilogue_gelu,
     pin_epilogue_bias_broadcast, pin_epilogue_residual, pin_e4m3_format_values,
     pin_e4m3_ties_to_even, pin_e4m3_matches_torch, pin_e4m3_roundtrip_and_order, pin_s8_rounding,
-    pin_quantize_scales_in_fp32,
+    pin_quantize_single_rounding, pin_quantize_exact_rational, pin_quantize_scale_is_fp32,
 ]

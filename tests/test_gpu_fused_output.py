@@ -3,15 +3,19 @@
     v = act(alpha*A*B + beta*C + bias) + R,   D = convert(d_scale * v),
     amax = max |v|
 
-on the GPU against the oracle (oracle.epilogue for v in fp64,
-oracle.quantize for the conversion, taken in fp32 like the kernel).
+on the GPU against the oracle: oracle.epilogue gives v in fp64, and
+oracle.quantize rounds the exact product d_scale * v once to the output
+format (the plain reading of "scaling, then fp8/int8 quantisation" in "Tiled
+matrix multiplication", "Implementation notes").
 
-Integer inputs with power-of-two scales make v exact on both sides, so the
-fp8 E4M3 / int8 codes must be identical.  Otherwise v carries the bf16 GEMM's
-bound b = slope * 8e-3 * (den + |bias|) (+ the fp32 rounding of the residual
-add and the scaling, 2^-23 |v|), and each code must lie between the codes of
-d_scale * (v - b) and d_scale * (v + b): the conversion is monotone, so that
-is exactly the set of codes a value within the bound can produce.
+Integer inputs with power-of-two scales make v and d_scale * v exact on both
+sides, so the fp8 E4M3 / int8 codes must be identical.  Otherwise the
+kernel's value carries the bf16 GEMM's bound slope * 8e-3 * (den + |bias|),
+plus two fp32 roundings the definition does not have -- the residual add and
+the product d_scale * v, which the kernel forms in fp32 before converting --
+of at most 2^-24 |v| each.  With b their sum, each code must lie between the
+codes of d_scale * (v - b) and d_scale * (v + b): the conversion is monotone,
+so that is exactly the set of codes a value within the bound can produce.
 """
 import numpy as np
 import pytest
@@ -78,7 +82,9 @@ def _reference(A, B, C, alpha, beta, bias, act, residual):
     v = oracle.epilogue(ref64, bias.numpy() if bias is not None else None, act,
                         residual.numpy() if residual is not None else None)
     scale = den + (np.abs(bias.numpy())[None, :] if bias is not None else 0.0)
-    b = SLOPE[act] * TOL_BF16 * scale + 2.0 ** -23 * np.abs(v) + 1e-30
+    # the GEMM's bound through the activation, plus the kernel's fp32
+    # roundings of the residual add and of d_scale * v (2^-24 |v| each)
+    b = SLOPE[act] * TOL_BF16 * scale + 2 * 2.0 ** -24 * np.abs(v) + 1e-30
     return v, b
 
 

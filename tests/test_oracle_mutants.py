@@ -7,6 +7,8 @@ that at least one pin fails.  The committed oracle is never modified.
 """
 import os
 
+import numpy as np
+
 import pytest
 
 import oracle
@@ -72,3 +74,45 @@ def test_mutant_is_caught(tmp_path, name):
     lib_path = oracle.compile_library(str(src), str(tmp_path / "libmutant.so"))
     failed = _run_pins_isolated(lib_path)
     assert failed, "no pin caught mutant %s" % name
+
+
+# Plausible mistakes in the output conversion of the fused stage, planted by
+# swapping oracle.quantize for a wrong version while the pins run.
+def _quantize_through_fp32(v, d_type, d_scale=1.0):
+    x = np.asarray(v, dtype=np.float32) * np.float32(d_scale)   # rounds twice
+    return _QUANTIZE(x.astype(np.float64), d_type, 1.0)
+
+
+def _quantize_scale_ignored(v, d_type, d_scale=1.0):
+    return _QUANTIZE(v, d_type, 1.0)
+
+
+def _quantize_ties_away(v, d_type, d_scale=1.0):
+    x = np.asarray(v, dtype=np.float64) * float(np.float32(d_scale))
+    if d_type == "s8":
+        r = np.sign(x) * np.floor(np.abs(x) + 0.5)
+        return np.clip(np.where(np.isnan(x), 0.0, r), -128, 127).astype(np.int8)
+    return _QUANTIZE(v, d_type, d_scale)
+
+
+_QUANTIZE = oracle.quantize
+QUANTIZE_MUTANTS = {
+    "rounded_to_fp32_first": _quantize_through_fp32,
+    "scale_ignored": _quantize_scale_ignored,
+    "s8_ties_away_from_zero": _quantize_ties_away,
+}
+
+
+@pytest.mark.parametrize("name", sorted(QUANTIZE_MUTANTS))
+def test_quantize_mutant_is_caught(monkeypatch, name):
+    monkeypatch.setattr(oracle, "quantize", QUANTIZE_MUTANTS[name])
+    orc = oracle.default()
+    failed = []
+    for pin in ALL_PINS:
+        if "quantize" not in pin.__name__:
+            continue
+        try:
+            pin(orc)
+        except AssertionError:
+            failed.append(pin.__name__)
+    assert failed, "no pin caught quantize mutant %s" % name
