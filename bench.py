@@ -43,7 +43,9 @@ if ROOT not in sys.path:
 
 METRIC = "GFLOP/s and % of roofline: fp32 4092^3 SIMT, bf16 8192^3 tcgen05, M=16 HBM GB/s"
 SM_LANES_FP32 = 128        # fp32 FFMA lanes per SM (4 partitions x 32)
-MAX_SM_CLOCK_HZ = 2.07e9   # GB300 maximum SM clock
+MIN_TRIAL_MS = 200.0       # each timed trial of a part lasts at least this long
+TRIALS = 5                 # trials per part; the median is reported
+SUSTAINED_MS = 2000.0      # the sustained bf16 part runs back to back this long
 
 
 def parse_args():
@@ -55,7 +57,8 @@ def parse_args():
     p.add_argument("--no-parts", action="store_true", help="headline workload only")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
-    p.add_argument("--only", choices=["sgemm", "bf16", "decode"], default=None,
+    p.add_argument("--only", choices=["sgemm", "sgemm4096", "ragged", "bf16", "decode"],
+                   default=None,
                    help="time one kernel's workload alone (profiling runs); prints its part")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target duration of the CPU-oracle sample")
@@ -63,16 +66,45 @@ def parse_args():
 
 
 # ------------------------------------------------------------------ helpers
+def _smi_max_sm_mhz():
+    try:
+        out = subprocess.run(["nvidia-smi", "-i", "0", "--query-gpu=clocks.max.sm",
+                              "--format=csv,noheader,nounits"], capture_output=True, text=True,
+                             timeout=30).stdout.split()
+        return float(out[0]) if out else None
+    except (OSError, ValueError, subprocess.TimeoutExpired):
+        return None
+
+
 def load_peaks():
+    """Roofline denominators: HBM GB/s and dense bf16 TFLOP/s (burst and
+    sustained) measured on this machine (MEASURED_PEAKS.json), and the maximum
+    SM clock the fp32 FFMA peak is derived from (the same file, else the
+    device's own clocks.max.sm)."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    d = {}
     if os.path.exists(path):
         with open(path) as f:
             d = json.load(f)
-        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
-                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
-                "source": "measured"}
-    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
-            "source": "fallback"}
+    if "hbm_gbs" in d and "bf16_tflops" in d:
+        peaks = {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                 "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                 "source": "measured"}
+    else:
+        peaks = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                 "source": "fallback"}
+    if d.get("sm_max_mhz"):
+        peaks["sm_max_mhz"], peaks["sm_clock_source"] = float(d["sm_max_mhz"]), "MEASURED_PEAKS.json"
+    else:
+        mhz = _smi_max_sm_mhz()
+        peaks["sm_max_mhz"], peaks["sm_clock_source"] = (
+            (mhz, "nvidia-smi clocks.max.sm") if mhz else (2070.0, "fallback (GB300 maximum)"))
+    return peaks
+
+
+def fp32_ffma_peak(num_sms, peaks):
+    """Derived fp32 FFMA peak in TFLOP/s: SMs x 128 lanes x 2 FLOP x max SM clock."""
+    return num_sms * SM_LANES_FP32 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
 
 
 def recorded_traffic(kernel):
@@ -218,29 +250,66 @@ def time_launches(torch, step, n, stream_obj):
     return [a.elapsed_time(b) for a, b in evs]
 
 
-def bench_sgemm_shape(torch, g, wl, name, fp32_peak, device, stream_obj):
+def time_window(torch, step, reps, stream_obj, first=0):
+    """Duration (ms) of `reps` back-to-back calls of step(first..), between two
+    CUDA events on the launching stream."""
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream_obj)
+    for i in range(reps):
+        step(first + i)
+    b.record(stream_obj)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b)
+
+
+def measure_part(torch, step, stream_obj, gpu_index, units_per_call=1, warmup=3,
+                 min_trial_ms=MIN_TRIAL_MS, trials=TRIALS):
+    """The timing protocol of every part: `warmup` untimed calls, then
+    `trials` trials of R back-to-back calls each, R chosen so that a trial
+    lasts at least `min_trial_ms`; nvidia-smi samples the clocks over the
+    trials.  A call may run several launches (`units_per_call`, e.g. a CUDA
+    graph); times are reported per launch.  Returns the per-launch median,
+    the spread over trials, R and the clock record."""
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+    est = time_window(torch, step, 3, stream_obj, first=warmup) / 3
+    reps = max(1, int(math.ceil(min_trial_ms / max(est, 1e-3))))
+    sampler = ClockSampler(gpu_index)
+    sampler.start()
+    time.sleep(0.3)
+    per = []
+    first = warmup + 3
+    for _ in range(trials):
+        per.append(time_window(torch, step, reps, stream_obj, first) / (reps * units_per_call))
+        first += reps
+    clocks = sampler.stop()
+    med = statistics.median(per)
+    return {"ms_per_launch_median": med, "ms_per_launch_min": min(per),
+            "ms_per_launch_max": max(per), "trial_spread": (max(per) - min(per)) / med,
+            "trials": trials, "launches_per_trial": reps * units_per_call,
+            "trial_ms_median": med * reps * units_per_call, "clocks": clocks}
+
+
+def bench_sgemm_shape(torch, g, wl, name, fp32_peak, device, stream_obj, gpu_index):
     """Another fp32 workload on the CUDA-core kernel (4096^3, or the ragged
     3000x5000x1999 whose K = 1999 rows are not 16-byte multiples, so A is
-    loaded by the generic cp.async producers).  Two input sets in turn, each
-    larger than L2."""
+    first copied to a 16-byte pitch; the copy is inside the timed launch).
+    Two input sets in turn, each larger than L2."""
     w = wl.WORKLOADS[name]
     w2 = wl.Workload(**{**w.__dict__, "seed": w.seed + 100, "name": name + "_b"})
     sets = [tuple(t.to(device) for t in wl.workload_inputs(x)) for x in (w, w2)]
     step = sgemm_step_fn(g, sets, w, stream_obj.cuda_stream)
-    for i in range(3):
-        step(i)
-    torch.cuda.synchronize()
-    times = time_launches(torch, step, 20, stream_obj)
-    ms = statistics.median(times)
-    tflops = w.flops / (ms * 1e-3) / 1e12
+    t = measure_part(torch, step, stream_obj, gpu_index)
+    tflops = w.flops / (t["ms_per_launch_median"] * 1e-3) / 1e12
     del sets
     torch.cuda.empty_cache()
     return {
         "workload": "fp32 SGEMM M=%d N=%d K=%d, alpha=%g, beta=%g" % (w.M, w.N, w.K, w.alpha,
                                                                       w.beta),
         "kernel": "simt_gemm_kernel (CUDA cores, fma.rn.f32x2)",
-        "value": tflops * 1e3, "unit": "GFLOP/s", "ms_per_launch_median": ms,
-        "launches_timed": len(times),
+        "value": tflops * 1e3, "unit": "GFLOP/s", **t,
         "roofline": {"bound": "alu", "achieved": tflops, "peak": fp32_peak, "unit": "TFLOP/s",
                      "frac": tflops / fp32_peak, "traffic": None,
                      "peak_note": "derived fp32 FFMA peak, as the headline"},
@@ -248,10 +317,14 @@ def bench_sgemm_shape(torch, g, wl, name, fp32_peak, device, stream_obj):
     }
 
 
-def bench_bf16_8192(torch, g, wl, peaks, device, stream_obj):
+def _bf16_8192_operands(torch, wl, device):
     w = wl.WORKLOADS["bf16_8192"]
     A, B, _ = wl.workload_inputs(w, with_c=False)
-    A, B = A.to(device), B.to(device)
+    return w, A.to(device), B.to(device)
+
+
+def bench_bf16_8192(torch, g, wl, peaks, device, stream_obj, gpu_index):
+    w, A, B = _bf16_8192_operands(torch, wl, device)
     C = torch.empty((w.M, w.N), dtype=torch.float32, device=device)
     s = stream_obj.cuda_stream
 
@@ -260,34 +333,40 @@ def bench_bf16_8192(torch, g, wl, peaks, device, stream_obj):
                              w.beta, C.data_ptr(), w.N, s)
         if st != 0:
             raise RuntimeError("gemm_bf16gemm: " + g.gemm_status_string(st))
-    for i in range(3):
-        step(i)
-    torch.cuda.synchronize()
-    times = time_launches(torch, step, 10, stream_obj)
-    ms = statistics.median(times)
-    flops = w.flops
-    tflops = flops / (ms * 1e-3) / 1e12
-    peak = peaks["bf16_tflops"]
+    t = measure_part(torch, step, stream_obj, gpu_index)
+    tflops = w.flops / (t["ms_per_launch_median"] * 1e-3) / 1e12
+    # the same kernel back to back for seconds, against the sustained peak
+    sustained = measure_part(torch, step, stream_obj, gpu_index, warmup=0,
+                             min_trial_ms=SUSTAINED_MS, trials=1)
+    s_tflops = w.flops / (sustained["ms_per_launch_median"] * 1e-3) / 1e12
     del A, B, C
     torch.cuda.empty_cache()
+    burst, sus = peaks["bf16_tflops"], peaks["bf16_tflops_sustained"]
     return {
         "workload": "bf16 in / fp32 out GEMM M=N=K=8192, alpha=1, beta=0, N(0,0.02)",
         "kernel": "tc_bf16_pair_kernel (tcgen05 cta_group::2: CTA pairs on 256x256 tiles, TMEM accumulators)",
-        "value": tflops * 1e3, "unit": "GFLOP/s", "ms_per_launch_median": ms,
-        "ms_per_launch_min": min(times), "launches_timed": len(times),
-        "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
-                     "frac": tflops / peak, "traffic": recorded_traffic("tc_bf16_pair_kernel"),
-                     "peak_note": "%s dense bf16 burst (cuBLAS); sustained %.1f" % (
-                         peaks["source"], peaks["bf16_tflops_sustained"])},
+        "value": tflops * 1e3, "unit": "GFLOP/s", **t,
+        "roofline": {"bound": "tensor", "achieved": tflops, "peak": burst, "unit": "TFLOP/s",
+                     "frac": tflops / burst, "frac_of_sustained": tflops / sus,
+                     "traffic": recorded_traffic("tc_bf16_pair_kernel"),
+                     "peak_note": "%s dense bf16 burst (cuBLAS, best of 10); sustained %.1f" % (
+                         peaks["source"], sus)},
+        "sustained": {"value": s_tflops * 1e3, "unit": "GFLOP/s",
+                      "seconds": sustained["trial_ms_median"] / 1e3,
+                      "launches": sustained["launches_per_trial"],
+                      "ms_per_launch": sustained["ms_per_launch_median"],
+                      "roofline": {"bound": "tensor", "achieved": s_tflops, "peak": sus,
+                                   "unit": "TFLOP/s", "frac": s_tflops / sus,
+                                   "peak_note": "%s dense bf16 sustained (cuBLAS, 4 s back to "
+                                                "back)" % peaks["source"]},
+                      "clocks": sustained["clocks"]},
         "l2": "operands 256 MB + C 256 MB per launch exceed the 129 MB L2",
     }
 
 
-def bench_bf16_8192_fused(torch, g, wl, peaks, device, stream_obj):
+def bench_bf16_8192_fused(torch, g, wl, peaks, device, stream_obj, gpu_index):
     """The bf16 8192^3 GEMM with the fused output stage: bias + GELU, bf16 D."""
-    w = wl.WORKLOADS["bf16_8192"]
-    A, B, _ = wl.workload_inputs(w, with_c=False)
-    A, B = A.to(device), B.to(device)
+    w, A, B = _bf16_8192_operands(torch, wl, device)
     bias = (torch.randn(w.N, generator=torch.Generator().manual_seed(9)) * 0.1).to(device)
     D = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=device)
     s = stream_obj.cuda_stream
@@ -298,32 +377,27 @@ def bench_bf16_8192_fused(torch, g, wl, peaks, device, stream_obj):
                                       w.N, g.OUT["bf16"], s)
         if st != 0:
             raise RuntimeError("gemm_bf16gemm_epilogue: " + g.gemm_status_string(st))
-    for i in range(3):
-        step(i)
-    torch.cuda.synchronize()
-    times = time_launches(torch, step, 10, stream_obj)
-    ms = statistics.median(times)
-    tflops = w.flops / (ms * 1e-3) / 1e12
+    t = measure_part(torch, step, stream_obj, gpu_index)
+    tflops = w.flops / (t["ms_per_launch_median"] * 1e-3) / 1e12
     peak = peaks["bf16_tflops"]
     del A, B, D, bias
     torch.cuda.empty_cache()
     return {
         "workload": "bf16 GEMM M=N=K=8192 with fused bias + GELU, bf16 output",
         "kernel": "tc_bf16_pair_kernel (same kernel, fused output stage)",
-        "value": tflops * 1e3, "unit": "GFLOP/s", "ms_per_launch_median": ms,
-        "launches_timed": len(times),
+        "value": tflops * 1e3, "unit": "GFLOP/s", **t,
         "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
-                     "frac": tflops / peak, "traffic": None,
+                     "frac": tflops / peak,
+                     "frac_of_sustained": tflops / peaks["bf16_tflops_sustained"],
+                     "traffic": None,
                      "peak_note": "%s dense bf16 burst (cuBLAS)" % peaks["source"]},
     }
 
 
-def bench_bf16_8192_fp8(torch, g, wl, peaks, device, stream_obj):
+def bench_bf16_8192_fp8(torch, g, wl, peaks, device, stream_obj, gpu_index):
     """The bf16 8192^3 GEMM quantised in its output stage: bias + GELU, fp8 E4M3
     D scaled by d_scale, and the amax of the unscaled values."""
-    w = wl.WORKLOADS["bf16_8192"]
-    A, B, _ = wl.workload_inputs(w, with_c=False)
-    A, B = A.to(device), B.to(device)
+    w, A, B = _bf16_8192_operands(torch, wl, device)
     bias = (torch.randn(w.N, generator=torch.Generator().manual_seed(9)) * 0.1).to(device)
     D = torch.empty((w.M, w.N), dtype=torch.uint8, device=device)
     amax = torch.zeros(1, dtype=torch.float32, device=device)
@@ -340,83 +414,69 @@ def bench_bf16_8192_fp8(torch, g, wl, peaks, device, stream_obj):
                                    o, s)
         if st != 0:
             raise RuntimeError("gemm_bf16gemm_fused: " + g.gemm_status_string(st))
-    for i in range(3):
-        step(i)
-    torch.cuda.synchronize()
-    times = time_launches(torch, step, 10, stream_obj)
-    ms = statistics.median(times)
-    tflops = w.flops / (ms * 1e-3) / 1e12
+    t = measure_part(torch, step, stream_obj, gpu_index)
+    tflops = w.flops / (t["ms_per_launch_median"] * 1e-3) / 1e12
     peak = peaks["bf16_tflops"]
     del A, B, D, bias, amax
     torch.cuda.empty_cache()
     return {
         "workload": "bf16 GEMM M=N=K=8192 with fused bias + GELU, fp8 E4M3 output (scale 64) + amax",
         "kernel": "tc_bf16_pair_kernel (same kernel, fused output stage)",
-        "value": tflops * 1e3, "unit": "GFLOP/s", "ms_per_launch_median": ms,
-        "launches_timed": len(times),
+        "value": tflops * 1e3, "unit": "GFLOP/s", **t,
         "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
-                     "frac": tflops / peak, "traffic": None,
+                     "frac": tflops / peak,
+                     "frac_of_sustained": tflops / peaks["bf16_tflops_sustained"],
+                     "traffic": None,
                      "peak_note": "%s dense bf16 burst (cuBLAS)" % peaks["source"]},
     }
 
 
-def bench_decode(torch, g, wl, peaks, device, stream_obj):
+DECODE_GRAPH_LAUNCHES = 200
+
+
+def bench_decode(torch, g, wl, peaks, device, stream_obj, gpu_index):
     w = wl.WORKLOADS["decode_16"]
     A, B, C0 = wl.workload_inputs(w)
     A = A.to(device)
     Bs = [B.to(device) for _ in range(3)]  # 3 x 100.7 MB, cycled: each launch reads a cold B
     C = C0.to(device)
     bytes_alg = (w.M * w.K + w.K * w.N) * 2 + 2 * w.M * w.N * 4
-    s = stream_obj
 
-    def step(i, stream_handle):
+    def launch(i, stream_handle):
         Bi = Bs[i % 3]
         st = g.gemm_bf16gemm(w.M, w.N, w.K, w.alpha, A.data_ptr(), w.K, Bi.data_ptr(), w.N,
                              w.beta, C.data_ptr(), w.N, stream_handle)
         if st != 0:
             raise RuntimeError("gemm_bf16gemm (decode): " + g.gemm_status_string(st))
-    # warm-up (also allocates the split-K workspace before capture)
-    for i in range(6):
-        step(i, s.cuda_stream)
-    torch.cuda.synchronize()
-    reps = 60
+    reps = DECODE_GRAPH_LAUNCHES   # a multiple of 3: the graph ends on the B it began with
     graph = torch.cuda.CUDAGraph()
     cap = torch.cuda.Stream()
-    step(0, cap.cuda_stream)   # any per-stream set-up happens before capture
+    for i in range(6):
+        launch(i, cap.cuda_stream)   # any per-stream set-up happens before capture
     torch.cuda.synchronize()
     with torch.cuda.stream(cap):
         graph.capture_begin()
         for i in range(reps):
-            step(i, cap.cuda_stream)
+            launch(i, cap.cuda_stream)
         graph.capture_end()
     torch.cuda.synchronize()
-    trial_ms = []
     with torch.cuda.stream(cap):   # replay() launches on the current stream
-        graph.replay()
-        torch.cuda.synchronize()
-        for _ in range(5):
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record(cap)
-            graph.replay()
-            b.record(cap)
-            torch.cuda.synchronize()
-            trial_ms.append(a.elapsed_time(b) / reps)
-    ms = statistics.median(trial_ms)
+        t = measure_part(torch, lambda i: graph.replay(), cap, gpu_index, units_per_call=reps)
+    ms = t["ms_per_launch_median"]
     gbs = bytes_alg / (ms * 1e-3) / 1e9
     peak = peaks["hbm_gbs"]
     del A, Bs, C, graph
     torch.cuda.empty_cache()
     return {
         "workload": "decode bf16 GEMM M=16, N=12288, K=4096, alpha=1, beta=1",
-        "kernel": "tc_decode_kernel (tcgen05 swap-AB, split-K, fixed-order fix-up)",
+        "kernel": "tc_decode_kernel (tcgen05 swap-AB, one CTA per 128-column group)",
         "value": gbs, "unit": "GB/s", "gflops": w.flops / (ms * 1e-3) / 1e9,
-        "us_per_launch_median": ms * 1e3, "launches_timed": reps * 5,
+        "us_per_launch_median": ms * 1e3, **t,
         "algorithmic_bytes": bytes_alg,
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
                      "frac": gbs / peak, "traffic": recorded_traffic("tc_decode_kernel"),
                      "peak_note": "%s STREAM-style copy" % peaks["source"]},
-        "l2": "3 copies of B (302 MB) cycled; launches replayed from a CUDA graph",
+        "l2": "3 copies of B (302 MB) cycled; launches replayed from a CUDA graph of %d" % reps,
     }
 
 
@@ -457,6 +517,13 @@ def cpu_oracle_sample(wl, target_seconds):
 
 
 # ------------------------------------------------------------------ main arms
+def headline_config(world):
+    """The `config` of the JSON line, identical in both arms."""
+    return {"workload": "fp32 SGEMM M=N=K=4092, alpha=0.7, beta=0.3, A,B,C ~ U[-1,1), row-major",
+            "l2": "two 201 MB input sets used in turn (inputs larger than L2)",
+            "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
 def run_reference(args):
     """The oracle timed on the host cores, on the headline workload's config."""
     rank = int(os.environ.get("RANK", "0"))
@@ -478,9 +545,9 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": total_t / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "fp32 SGEMM M=N=K=4092, alpha=0.7, beta=0.3, U[-1,1)",
-                   "step": "a bounded sample of whole rows of the workload per step",
-                   "l2": "n/a (CPU)"},
+        "config": headline_config(int(os.environ.get("WORLD_SIZE", "1"))),
+        "step": "the CPU oracle on a bounded sample of whole rows of the workload per step "
+                "(host cores; L2 flushing does not apply)",
         "cpu_baseline": {"value": value, "unit": "GFLOP/s", "cores": samples[0]["cores"],
                          "kind": "oracle", "sample": samples[0]["sample"]},
         "e2e": {"value": value, "unit": "GFLOP/s", "h2d_bytes_per_step": 0,
@@ -502,7 +569,7 @@ def run_ours(args):
     g.load_library(build_if_missing=True)
     peaks = load_peaks()
     num_sms = torch.cuda.get_device_properties(device).multi_processor_count
-    fp32_peak = num_sms * SM_LANES_FP32 * 2 * MAX_SM_CLOCK_HZ / 1e12  # TFLOP/s
+    fp32_peak = fp32_ffma_peak(num_sms, peaks)  # TFLOP/s
 
     w = wl.WORKLOADS["sgemm_4092"]
     stream_obj = torch.cuda.current_stream(device)
@@ -614,13 +681,19 @@ def run_ours(args):
         for name in ("sgemm_4096", "sgemm_ragged"):
             w_ = wl.WORKLOADS[name]
             parts["sgemm_%dx%dx%d" % (w_.M, w_.N, w_.K)] = bench_sgemm_shape(
-                torch, g, wl, name, fp32_peak, device, stream_obj)
-        parts["bf16_8192"] = bench_bf16_8192(torch, g, wl, peaks, device, stream_obj)
-        parts["bf16_8192_bias_gelu_bf16out"] = bench_bf16_8192_fused(torch, g, wl, peaks, device,
-                                                                      stream_obj)
-        parts["bf16_8192_bias_gelu_fp8out_amax"] = bench_bf16_8192_fp8(torch, g, wl, peaks,
-                                                                        device, stream_obj)
-        parts["decode_16x12288x4096"] = bench_decode(torch, g, wl, peaks, device, stream_obj)
+                torch, g, wl, name, fp32_peak, device, stream_obj, local)
+        parts["bf16_8192"] = bench_bf16_8192(torch, g, wl, peaks, device, stream_obj, local)
+        parts["bf16_8192_bias_gelu_bf16out"] = bench_bf16_8192_fused(
+            torch, g, wl, peaks, device, stream_obj, local)
+        parts["bf16_8192_bias_gelu_fp8out_amax"] = bench_bf16_8192_fp8(
+            torch, g, wl, peaks, device, stream_obj, local)
+        parts["decode_16x12288x4096"] = bench_decode(torch, g, wl, peaks, device, stream_obj,
+                                                     local)
+        parts["protocol"] = ("every part: 3 warm-up launches, then %d trials of back-to-back "
+                             "launches lasting >= %d ms each between CUDA events on the "
+                             "launching stream; median per launch reported with the spread; "
+                             "clocks sampled by nvidia-smi over the trials"
+                             % (TRIALS, MIN_TRIAL_MS))
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -633,15 +706,13 @@ def run_ours(args):
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": total_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": "fp32 SGEMM M=N=K=4092, alpha=0.7, beta=0.3, "
-                                   "A,B,C ~ U[-1,1), row-major",
-                       "l2": "two 201 MB input sets used in turn (inputs larger than L2)",
-                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "config": headline_config(world),
             "roofline": {"bound": "alu", "achieved": achieved, "peak": fp32_peak,
                          "unit": "TFLOP/s", "frac": achieved / fp32_peak,
                          "traffic": recorded_traffic("simt_gemm_kernel"),
-                         "peak_note": "%d SMs x 128 fp32 lanes x 2 FLOP x 2.07 GHz max clock "
-                                      "(derived)" % num_sms,
+                         "peak_note": "%d SMs x 128 fp32 lanes x 2 FLOP x %.0f MHz max SM clock "
+                                      "(%s; derived)" % (num_sms, peaks["sm_max_mhz"],
+                                                         peaks["sm_clock_source"]),
                          "kernel_ms_mean": kernel_ms, "kernel_ms_min": min(launch_ms)},
             "clocks": clocks,
             "e2e": e2e,
@@ -655,7 +726,9 @@ def run_ours(args):
 
 
 def run_only(args):
-    """One kernel's workload alone, for profiler captures (not the contract line)."""
+    """One kernel's workload alone, `--warmup` then `--steps` launches, for
+    profiler captures (not the contract line; numbers taken under a profiler
+    are not bench values)."""
     import torch
 
     import dense_gemm_12_gb300 as g
@@ -663,26 +736,39 @@ def run_only(args):
     device = torch.device("cuda", 0)
     torch.cuda.set_device(device)
     g.load_library(build_if_missing=True)
-    peaks = load_peaks()
     stream_obj = torch.cuda.current_stream(device)
+    s = stream_obj.cuda_stream
     if args.only == "bf16":
-        out = bench_bf16_8192(torch, g, wl, peaks, device, stream_obj)
+        w, A, B = _bf16_8192_operands(torch, wl, device)
+        C = torch.empty((w.M, w.N), dtype=torch.float32, device=device)
+
+        def step(i):
+            g.gemm_bf16gemm(w.M, w.N, w.K, w.alpha, A.data_ptr(), w.K, B.data_ptr(), w.N,
+                            w.beta, C.data_ptr(), w.N, s)
     elif args.only == "decode":
-        out = bench_decode(torch, g, wl, peaks, device, stream_obj)
+        w = wl.WORKLOADS["decode_16"]
+        A, B, C = (t.to(device) for t in wl.workload_inputs(w))
+        Bs = [B, B.clone(), B.clone()]
+
+        def step(i):
+            g.gemm_bf16gemm(w.M, w.N, w.K, w.alpha, A.data_ptr(), w.K, Bs[i % 3].data_ptr(),
+                            w.N, w.beta, C.data_ptr(), w.N, s)
     else:
-        w = wl.WORKLOADS["sgemm_4092"]
-        w2 = wl.Workload(**{**w.__dict__, "seed": w.seed + 100, "name": "sgemm_4092_b"})
+        name = {"sgemm": "sgemm_4092", "sgemm4096": "sgemm_4096",
+                "ragged": "sgemm_ragged"}[args.only]
+        w = wl.WORKLOADS[name]
+        w2 = wl.Workload(**{**w.__dict__, "seed": w.seed + 100, "name": name + "_b"})
         sets = [tuple(t.to(device) for t in wl.workload_inputs(x)) for x in (w, w2)]
-        step = sgemm_step_fn(g, sets, w, stream_obj.cuda_stream)
-        for i in range(args.warmup):
-            step(i)
-        ms = time_launches(torch, step, args.steps, stream_obj)
-        out = {"workload": "fp32 SGEMM 4092^3", "ms_per_launch": ms,
-               "gflops_median": w.flops / (statistics.median(ms) * 1e-3) / 1e9}
-    st = g.gemm_check_device_error(stream_obj.cuda_stream)
+        step = sgemm_step_fn(g, sets, w, s)
+    for i in range(args.warmup):
+        step(i)
+    ms = time_launches(torch, step, args.steps, stream_obj)
+    st = g.gemm_check_device_error(s)
     if st != 0:
         raise RuntimeError("device error: " + g.gemm_status_string(st))
-    print(json.dumps({"only": args.only, **out}), flush=True)
+    print(json.dumps({"only": args.only, "workload": w.name, "ms_per_launch": ms,
+                      "gflops_median": w.flops / (statistics.median(ms) * 1e-3) / 1e9}),
+          flush=True)
 
 
 def main():

@@ -18,8 +18,11 @@ namespace g12 {
 namespace {
 
 // Scratch capacity: 4 MiB per device.  The first kStaticCounters words are
-// the arrival counters (one per 128-column group, so N <= 4096 * 128), the
-// rest holds partial sums.
+// the arrival counters (one per 128-column group), the rest holds partial
+// sums: CTAs x segment slots x 16 rows x 128 columns.  The partial sums bind
+// first: with more column groups than SMs each CTA needs 3 slots up to twice
+// as many groups as SMs (152 x 3 x 2048 floats on a 152-SM GB300) and 4
+// beyond, which no longer fits -- so N <= 256 x SMs (38,912 on 152 SMs).
 constexpr size_t kStaticScratchBytes = size_t{4} << 20;
 constexpr int64_t kStaticCounters = 4096;
 constexpr int64_t kStaticPartialFloats =
@@ -112,21 +115,31 @@ extern "C" gemm_status_t gemm_bf16gemm_decode_static(int64_t M, int64_t N, int64
       !abi_encode_bf16_2d(&tmB, B, N, K, ldb, 64, static_cast<uint32_t>(decode_b_box_rows())))
     return GEMM_ERR_LAUNCH;
 
-  // The counters must start at zero.  The kernel leaves them at zero after a
-  // completed launch, but a launch that gave up part-way may not have.
-  if (cudaMemsetAsync(scratch, 0, counters * sizeof(uint32_t), cs) != cudaSuccess) {
-    cudaGetLastError();
-    return GEMM_ERR_LAUNCH;
-  }
   DecodeArgs a{};
   a.M = static_cast<int>(M);
   a.N = n;
   a.K = k;
   a.epi = plain_epilogue(alpha, beta, C, ldc);
-  a.counters = scratch;
-  a.workspace = reinterpret_cast<float*>(scratch + kStaticCounters);
   a.err = err_word;
   a.cluster = decode_cluster(m, n, k, num_sms);
+  // One CTA per column group, or clusters that add their partial sums in
+  // shared memory: the kernel touches no scratch, so none is passed and
+  // nothing is cleared (a memset between two launches would also keep this
+  // launch from overlapping the previous kernel's last CTAs).  Only when the
+  // column groups outnumber the SMs do runs of groups meet in the array.
+  if (grid == counters || a.cluster > 1) {
+    a.counters = nullptr;
+    a.workspace = nullptr;
+  } else {
+    // The counters must start at zero.  The kernel leaves them at zero after
+    // a completed launch, but a launch that gave up part-way may not have.
+    if (cudaMemsetAsync(scratch, 0, counters * sizeof(uint32_t), cs) != cudaSuccess) {
+      cudaGetLastError();
+      return GEMM_ERR_LAUNCH;
+    }
+    a.counters = scratch;
+    a.workspace = reinterpret_cast<float*>(scratch + kStaticCounters);
+  }
   const cudaError_t e = launch_tc_decode(a, &tmA, &tmB, grid, cs);
   if (e != cudaSuccess) {
     cudaGetLastError();

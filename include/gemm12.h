@@ -249,15 +249,19 @@ gemm_status_t gemm_bf16gemm_epilogue(int64_t M, int64_t N, int64_t K, float alph
  * Instead of allocating its split-K scratch (partial sums and per-column-group
  * arrival counters) the call uses one fixed array of 4 MiB that the library
  * holds on every device it is loaded onto, until the process exits.  It calls
- * no cudaMalloc or cudaFree.  Limits: at most 4096 column groups of 128
- * (N <= 524288) and a partial-sum area of about one million floats; shapes
- * that need more return GEMM_ERR_UNSUPPORTED, as do M > 16 and operands the
- * TMA engine cannot describe (base not 16-byte aligned, or a row pitch that
- * is not a multiple of 16 bytes) -- use gemm_bf16gemm for those.  M == 0 or
- * N == 0 does nothing; K == 0 or alpha == 0 computes C <- beta*C.
+ * no cudaMalloc or cudaFree.  Limit: the array holds the partial sums of
+ * up to twice as many 128-column groups as the device has SMs, so
+ * N <= 256 x SMs (N <= 38,912 on a 152-SM GB300; any K).  Larger N returns
+ * GEMM_ERR_UNSUPPORTED, as do M > 16 and operands the TMA engine cannot
+ * describe (base not 16-byte aligned, or a row pitch that is not a multiple
+ * of 16 bytes) -- use gemm_bf16gemm for those.  M == 0 or N == 0 does
+ * nothing; K == 0 or alpha == 0 computes C <- beta*C.
  *
- * Every call on a device shares that one array, and each call first clears
- * the counters it needs (an asynchronous memset on `stream`).  Calls whose
+ * The array is used only when the column groups outnumber the SMs
+ * (N > 128 x SMs); fewer groups run with no scratch at all, as in
+ * gemm_bf16gemm.  Every call on a device shares that one array, and a call
+ * that uses it first clears its counters (an asynchronous memset on
+ * `stream`).  Calls whose
  * work overlaps on the GPU -- on different streams, or from different host
  * threads -- race on the array and give wrong results: serialise them.  The
  * first call on each device looks up the array's device address (once, with

@@ -1,0 +1,101 @@
+"""Bit-exact parity at the benchmark sizes, under automatic dispatch.
+
+Small integers in [-4, 4] make every partial sum an integer below 2^24
+(|sum| <= 16 K: 65,472 at K = 4092, 131,072 at K = 8192), so fp32
+accumulation is exact in any order and any split, and alpha = 1.5,
+beta = -0.5 scale exactly: the kernels must reproduce the oracle's result
+bit for bit ("GEMM Worklog I: Naive to Tiled", opening equation).  Unlike
+the bound used for random inputs (2e-6 sqrt(K) fp32, 8e-3 bf16), equality
+also catches a single lost k-slab or TMA box anywhere in the schedule.
+
+Each case runs the benchmark's shape through the plain entry point, so it
+takes the same launch plan as the timed run (the plan depends on the shape
+only): fp32 4092^3 with its stream-K tail, 3000x5000x1999 (on a staged
+copy of A) with its last tiles cut along k, bf16 8192^3 on CTA pairs with
+its last round split along k, and the decode shape.  fp32 results are compared in full;
+bf16 8192^3 on 512 rows: the first and last row of every 128-row tile (so
+both tiles of every CTA pair and every tile boundary) and 6 more per tile.
+"""
+import numpy as np
+import pytest
+import torch
+
+import dense_gemm_12_gb300 as g
+from dense_gemm_12_gb300.workloads import make_inputs
+from gpu_helpers import check_device_error, oracle_bf16, oracle_sgemm
+
+pytestmark = pytest.mark.gpu
+
+INT = ("int", None)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(gemm_lib, cuda_device):
+    yield
+
+
+def _bits(x):
+    return np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+
+
+def _device_gemm(fn, A, B, C, alpha, beta):
+    M, K = A.shape
+    N = B.shape[1]
+    dA, dB, dC = A.cuda(), B.cuda(), C.cuda()
+    st = fn(M, N, K, alpha, dA.data_ptr(), K, dB.data_ptr(), N, beta, dC.data_ptr(), N, 0)
+    torch.cuda.synchronize()
+    assert st == 0, g.gemm_status_string(st)
+    check_device_error()
+    return dC.cpu()
+
+
+@pytest.mark.parametrize("M,N,K,tail", [
+    (4092, 4092, 4092, "stream"),   # 512 wide tiles: 456 whole, stream-K over the rest
+    (3000, 5000, 1999, "split"),    # staged A; 480 wide tiles, the last 24 cut along k
+])
+def test_fp32_full_matrix_exact(M, N, K, tail):
+    cfg, _ = g.gemm_get_config(0, M, N, K)
+    assert cfg["kernel"] == "wide", cfg
+    assert (cfg["split"] == g.SPLIT_STREAM) if tail == "stream" else (cfg["split"] > 1), cfg
+    A, B, C = make_inputs(M, N, K, INT, INT, INT, seed=M + K)
+    out = _device_gemm(g.gemm_sgemm, A, B, C, 1.5, -0.5)
+    ref32, _, _ = oracle_sgemm(A, B, C, 1.5, -0.5, want64=False)
+    diff = _bits(out.numpy()) != _bits(ref32)
+    assert not diff.any(), "%d elements differ, first at %s" % (
+        int(diff.sum()), np.argwhere(diff)[0].tolist())
+
+
+def _tile_rows(M, tile=128, extra=6, seed=0):
+    gen = np.random.default_rng(seed)
+    rows = []
+    for t0 in range(0, M, tile):
+        t1 = min(M, t0 + tile)
+        rows += [t0, t1 - 1]
+        rows += list(gen.choice(np.arange(t0 + 1, t1 - 1), size=min(extra, t1 - t0 - 2),
+                                replace=False))
+    return np.unique(np.array(rows, dtype=np.int64))
+
+
+def test_bf16_8192_exact_on_every_tile():
+    M = N = K = 8192
+    cfg, _ = g.gemm_get_config(1, M, N, K)
+    assert cfg["kernel"] == "cta_pair", cfg
+    A, B, C = make_inputs(M, N, K, INT, INT, INT, seed=8192, dtype="bf16")
+    out = _device_gemm(g.gemm_bf16gemm, A, B, C, 1.5, -0.5)
+    rows = _tile_rows(M)
+    assert len(rows) == 512
+    idx = torch.from_numpy(rows)
+    ref32, _, _ = oracle_bf16(A[idx].contiguous(), B, C[idx].contiguous(), 1.5, -0.5,
+                              want64=False)
+    diff = _bits(out[idx].numpy()) != _bits(ref32)
+    assert not diff.any(), "%d elements differ, first at row %d col %d" % (
+        int(diff.sum()), rows[np.argwhere(diff)[0][0]], np.argwhere(diff)[0][1])
+
+
+def test_decode_workload_shape_exact():
+    M, N, K = 16, 12288, 4096
+    assert g.gemm_select_path(1, M, N, K, 1.0, 1 << 20, K, 1 << 20, N) == "tc_decode"
+    A, B, C = make_inputs(M, N, K, INT, INT, INT, seed=16, dtype="bf16")
+    out = _device_gemm(g.gemm_bf16gemm, A, B, C, 1.0, 1.0)
+    ref32, _, _ = oracle_bf16(A, B, C, 1.0, 1.0, want64=False)
+    assert np.array_equal(_bits(out.numpy()), _bits(ref32))
