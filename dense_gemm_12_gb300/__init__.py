@@ -24,7 +24,7 @@ __all__ = [
     "gemm_bf16gemm_fused", "bf16gemm_fused", "GemmOutput",
     "gemm_sgemm_config", "gemm_bf16gemm_config", "gemm_get_config", "gemm_get_model_config",
     "GemmConfig", "KERNELS", "SPLIT_STREAM",
-    "gemm_status_string", "gemm_check_device_error", "gemm_shutdown",
+    "gemm_status_string", "gemm_check_device_error", "gemm_shutdown", "gemm_release_stream",
     "gemm_select_path", "gemm_split_parts", "gemm_quantization", "gemm_version", "sgemm", "bf16gemm",
     "STATUS", "PATHS",
 ]
@@ -129,6 +129,8 @@ def load_library(build_if_missing: bool = False):
         lib.gemm_check_device_error.restype = cint
         lib.gemm_shutdown.argtypes = []
         lib.gemm_shutdown.restype = cint
+        lib.gemm_release_stream.argtypes = [vp]
+        lib.gemm_release_stream.restype = cint
         lib.gemm_select_path.argtypes = [cint, i64, i64, i64, f32, vp, i64, vp, i64]
         lib.gemm_select_path.restype = cint
         lib.gemm_quantization.argtypes = [i64, i64, i64, i64, i64, i64,
@@ -236,6 +238,11 @@ def gemm_check_device_error(stream=0) -> int:
 
 def gemm_shutdown() -> int:
     return load_library().gemm_shutdown()
+
+
+def gemm_release_stream(stream=0) -> int:
+    """Free the scratch and staging buffers kept for `stream` (stream-ordered)."""
+    return load_library().gemm_release_stream(stream)
 
 
 def gemm_select_path(is_bf16, M, N, K, alpha, A, lda, B, ldb) -> str:

@@ -165,68 +165,79 @@ gemm_status_t run_scale(int64_t M, int64_t N, float beta, float* C, int64_t ldc,
 
 int c_vec4_ok(const float* C, int64_t ldc) { return (aligned16(C) && (ldc % 4 == 0)) ? 1 : 0; }
 
+// Whether `stream` is capturing into a CUDA graph.  A failed query counts as
+// capturing, so that nothing is allocated.
+bool capturing(cudaStream_t stream) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+    cudaGetLastError();
+    return true;
+  }
+  return cs != cudaStreamCaptureStatusNone;
+}
+
+// Replaces *buf (of *have bytes) by a stream-ordered allocation of `bytes`
+// on `stream`: the old buffer is released after the work already queued on
+// the stream (its only user), the new one is ready for the work queued after
+// this call.  Nothing waits on the host.
+gemm_status_t regrow(void** buf, int64_t* have, int64_t bytes, cudaStream_t stream) {
+  if (*buf != nullptr && cudaFreeAsync(*buf, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_LAUNCH;
+  }
+  *buf = nullptr;
+  *have = 0;
+  if (cudaMallocAsync(buf, static_cast<size_t>(bytes), stream) != cudaSuccess) {
+    cudaGetLastError();
+    *buf = nullptr;
+    return GEMM_ERR_NO_MEMORY;
+  }
+  *have = bytes;
+  return GEMM_OK;
+}
+
 // The scratch area of `stream` on this device, grown to at least the given
-// sizes (new counters start at zero).  Caller holds st.ws_mutex.
+// sizes (new counters start at zero).  Growth is stream-ordered on `stream`
+// and never blocks the host.  Inside a stream capture nothing is allocated:
+// a scratch area too small returns GEMM_ERR_NO_MEMORY, and the caller plans
+// the launch without one.  Caller holds st.ws_mutex.
 gemm_status_t ensure_scratch(DeviceState& st, cudaStream_t stream, int64_t floats,
                              int64_t counters, Scratch** out) {
   Scratch& sc = st.scratch[static_cast<void*>(stream)];
   *out = &sc;
   if (sc.ws_floats >= floats && sc.counter_count >= counters) return GEMM_OK;
-  // Growing: the old buffers may still be used by this stream's kernels.
-  if (cudaStreamSynchronize(stream) != cudaSuccess) {
-    cudaGetLastError();
-    return GEMM_ERR_LAUNCH;
-  }
+  if (capturing(stream)) return GEMM_ERR_NO_MEMORY;
   if (sc.ws_floats < floats) {
-    if (sc.ws) cudaFree(sc.ws);
-    sc.ws = nullptr;
-    sc.ws_floats = 0;
-    if (cudaMalloc(reinterpret_cast<void**>(&sc.ws), floats * sizeof(float)) != cudaSuccess) {
-      cudaGetLastError();
-      sc.ws = nullptr;
-      return GEMM_ERR_NO_MEMORY;
-    }
-    sc.ws_floats = floats;
+    int64_t bytes = 0;
+    const gemm_status_t s = regrow(reinterpret_cast<void**>(&sc.ws), &bytes,
+                                   floats * static_cast<int64_t>(sizeof(float)), stream);
+    sc.ws_floats = bytes / static_cast<int64_t>(sizeof(float));
+    if (s != GEMM_OK) return s;
   }
   if (sc.counter_count < counters) {
-    if (sc.counters) cudaFree(sc.counters);
-    sc.counters = nullptr;
-    sc.counter_count = 0;
-    if (cudaMalloc(reinterpret_cast<void**>(&sc.counters), counters * sizeof(uint32_t)) !=
-        cudaSuccess) {
-      cudaGetLastError();
-      sc.counters = nullptr;
-      return GEMM_ERR_NO_MEMORY;
-    }
-    if (cudaMemset(sc.counters, 0, counters * sizeof(uint32_t)) != cudaSuccess) {
+    int64_t bytes = 0;
+    const gemm_status_t s = regrow(reinterpret_cast<void**>(&sc.counters), &bytes,
+                                   counters * static_cast<int64_t>(sizeof(uint32_t)), stream);
+    sc.counter_count = bytes / static_cast<int64_t>(sizeof(uint32_t));
+    if (s != GEMM_OK) return s;
+    if (cudaMemsetAsync(sc.counters, 0, static_cast<size_t>(bytes), stream) != cudaSuccess) {
       cudaGetLastError();
       return GEMM_ERR_LAUNCH;
     }
-    sc.counter_count = counters;
   }
   return GEMM_OK;
 }
 
 // The operand staging area of `stream` on this device, grown to at least
-// `bytes`.  Caller holds st.ws_mutex.
+// `bytes` (stream-ordered, as ensure_scratch; nothing is allocated inside a
+// stream capture).  Caller holds st.ws_mutex.
 gemm_status_t ensure_stage(DeviceState& st, cudaStream_t stream, int64_t bytes, uint8_t** out) {
   Scratch& sc = st.scratch[static_cast<void*>(stream)];
   if (sc.stage_bytes < bytes) {
-    // Growing: the old buffer may still be read by this stream's kernels.
-    if (cudaStreamSynchronize(stream) != cudaSuccess) {
-      cudaGetLastError();
-      return GEMM_ERR_LAUNCH;
-    }
-    if (sc.stage) cudaFree(sc.stage);
-    sc.stage = nullptr;
-    sc.stage_bytes = 0;
-    if (cudaMalloc(reinterpret_cast<void**>(&sc.stage), static_cast<size_t>(bytes)) !=
-        cudaSuccess) {
-      cudaGetLastError();
-      sc.stage = nullptr;
-      return GEMM_ERR_NO_MEMORY;
-    }
-    sc.stage_bytes = bytes;
+    if (capturing(stream)) return GEMM_ERR_NO_MEMORY;
+    const gemm_status_t s = regrow(reinterpret_cast<void**>(&sc.stage), &sc.stage_bytes, bytes,
+                                   stream);
+    if (s != GEMM_OK) return s;
   }
   *out = sc.stage;
   return GEMM_OK;
@@ -368,21 +379,45 @@ TileConfig resolve_config(bool bf16, int64_t M, int64_t N, int64_t K, int num_sm
 
 namespace {
 
-gemm_status_t plan_simt(DeviceState* st, cudaStream_t cs, SimtArgs& a, const SimtPlan& pl,
+// The plan `pl` with every tile run whole (no split, no stream-K tail): what
+// a launch runs when it cannot have its scratch area.
+SimtPlan simt_plan_whole(const SimtPlan& pl, int M, int N, int num_sms) {
+  SimtPlan w = pl;
+  const int tiles = ((M + kSimtBM - 1) / kSimtBM) * ((N + simt_bn(pl.wide) - 1) / simt_bn(pl.wide));
+  w.full_items = tiles;
+  w.split = 1;
+  w.sk_workers = 0;
+  w.grid = tiles < num_sms ? tiles : num_sms;
+  w.ws_floats = 0;
+  w.counters = 0;
+  return w;
+}
+
+// Fills the work plan fields of `a` from `pl`, with this stream's scratch
+// area when the plan splits tiles.  Without scratch (inside a stream capture
+// on a stream whose area is too small, or out of memory) `pl` becomes the
+// plan of whole tiles: same kernel, same result bound.
+gemm_status_t plan_simt(DeviceState* st, cudaStream_t cs, SimtArgs& a, SimtPlan& pl,
                         std::unique_lock<std::mutex>& lock) {
+  a.ws = nullptr;
+  a.counters = nullptr;
+  if (pl.split != 1 || pl.sk_workers != 0) {
+    if (!lock.owns_lock()) lock.lock();
+    Scratch* sc = nullptr;
+    const gemm_status_t s = ensure_scratch(*st, cs, pl.ws_floats, pl.counters, &sc);
+    if (s == GEMM_OK) {
+      a.ws = sc->ws;
+      a.counters = sc->counters;
+    } else if (s == GEMM_ERR_NO_MEMORY) {
+      pl = simt_plan_whole(pl, a.M, a.N, st->num_sms);
+    } else {
+      return s;
+    }
+  }
   a.full_items = pl.full_items;
   a.split = pl.split;
   a.sk_workers = pl.sk_workers;
   a.group_m = pl.group_m;
-  a.ws = nullptr;
-  a.counters = nullptr;
-  if (pl.split == 1 && pl.sk_workers == 0) return GEMM_OK;
-  if (!lock.owns_lock()) lock.lock();
-  Scratch* sc = nullptr;
-  const gemm_status_t s = ensure_scratch(*st, cs, pl.ws_floats, pl.counters, &sc);
-  if (s != GEMM_OK) return s;
-  a.ws = sc->ws;
-  a.counters = sc->counters;
   return GEMM_OK;
 }
 
@@ -728,21 +763,31 @@ static gemm_status_t run_bf16_tensor_core(DeviceState* st, gemm_path_t path, int
         !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, N, K, ldb, 64, b_rows,
                    CU_TENSOR_MAP_SWIZZLE_128B))
       return GEMM_ERR_LAUNCH;
-    a.full_items = pl.full_items;
-    a.split = pl.split;
-    a.group_m = pl.group_m;
+    TcPlan run = pl;
     a.ws = nullptr;
     a.counters = nullptr;
-    if (pl.split == 1) return from_cuda(launch_tc_bf16(a, pl, &tmA, &tmB, cs));
-    // Split items: the stream's scratch stays locked until the launch is
-    // queued, so no other thread can regrow it underneath.
-    if (!lock.owns_lock()) lock.lock();
-    Scratch* sc = nullptr;
-    const gemm_status_t s = ensure_scratch(*st, cs, pl.ws_floats, pl.counters, &sc);
-    if (s != GEMM_OK) return s;
-    a.ws = sc->ws;
-    a.counters = sc->counters;
-    return from_cuda(launch_tc_bf16(a, pl, &tmA, &tmB, cs));
+    if (pl.split > 1) {
+      // Split items: the stream's scratch stays locked until the launch is
+      // queued, so no other thread can regrow it underneath.  Without scratch
+      // (inside a stream capture, or out of memory) every item runs whole.
+      if (!lock.owns_lock()) lock.lock();
+      Scratch* sc = nullptr;
+      const gemm_status_t s = ensure_scratch(*st, cs, pl.ws_floats, pl.counters, &sc);
+      if (s == GEMM_OK) {
+        a.ws = sc->ws;
+        a.counters = sc->counters;
+      } else if (s == GEMM_ERR_NO_MEMORY) {
+        const TileConfig whole{pl.pair ? GEMM_KERNEL_CTA_PAIR : GEMM_KERNEL_SINGLE_CTA, 1,
+                               pl.group_m};
+        run = tc_plan(a.M, a.N, a.K, st->num_sms, &whole);
+      } else {
+        return s;
+      }
+    }
+    a.full_items = run.full_items;
+    a.split = run.split;
+    a.group_m = run.group_m;
+    return from_cuda(launch_tc_bf16(a, run, &tmA, &tmB, cs));
   }
   // GEMM_PATH_TC_DECODE
   if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, K, M, lda, 64,
@@ -771,6 +816,13 @@ static gemm_status_t run_bf16_tensor_core(DeviceState* st, gemm_path_t path, int
   Scratch* sc = nullptr;
   gemm_status_t s = ensure_scratch(*st, cs, decode_workspace_floats(a.M, a.N, a.K, grid),
                                    decode_counter_count(a.N), &sc);
+  if (s == GEMM_ERR_NO_MEMORY) {
+    // No scratch for the runs of column groups (inside a stream capture, or
+    // out of memory): the single-CTA tile kernel with whole tiles needs none.
+    const gemm_config_t whole{GEMM_KERNEL_SINGLE_CTA, 1, 0};
+    return run_bf16_tensor_core(st, GEMM_PATH_TC_BF16, M, N, K, A, lda, B, ldb, epi, cs, &whole,
+                                lock);
+  }
   if (s != GEMM_OK) return s;
   a.workspace = sc->ws;
   a.counters = sc->counters;
@@ -831,7 +883,7 @@ static gemm_status_t bf16gemm_impl(int64_t M, int64_t N, int64_t K, float alpha,
     // the CUDA-core kernel's table entries are the fp32 ones
     gemm_config_t simt_cfg{GEMM_KERNEL_AUTO, cfg ? cfg->split : 0, cfg ? cfg->group_m : 0};
     const TileConfig tc = resolve_config(false, M, N, K, st->num_sms, &simt_cfg, nullptr);
-    const SimtPlan pl = simt_plan(a.M, a.N, a.K, st->num_sms, &tc, false);
+    SimtPlan pl = simt_plan(a.M, a.N, a.K, st->num_sms, &tc, false);
     s = plan_simt(st, cs, a, pl, lock);
     if (s != GEMM_OK) return s;
     return from_cuda(launch_simt(a, pl, kLoadConvertBf16, kLoadConvertBf16, nullptr, nullptr,
@@ -1030,14 +1082,41 @@ gemm_status_t gemm_shutdown(void) {
       result = GEMM_ERR_LAUNCH;
       continue;
     }
+    // Stream-ordered allocations, released on the legacy stream once the
+    // device is idle (the streams they were made on may no longer exist).
     for (auto& kv : st.scratch) {
-      if (kv.second.ws) cudaFree(kv.second.ws);
-      if (kv.second.counters) cudaFree(kv.second.counters);
-      if (kv.second.stage) cudaFree(kv.second.stage);
+      if (kv.second.ws) cudaFreeAsync(kv.second.ws, 0);
+      if (kv.second.counters) cudaFreeAsync(kv.second.counters, 0);
+      if (kv.second.stage) cudaFreeAsync(kv.second.stage, 0);
     }
     st.scratch.clear();
+    if (cudaDeviceSynchronize() != cudaSuccess) {
+      cudaGetLastError();
+      result = GEMM_ERR_LAUNCH;
+    }
   }
   cudaSetDevice(cur);
+  return result;
+}
+
+gemm_status_t gemm_release_stream(void* stream) {
+  gemm_status_t s;
+  DeviceState* st = device_state(&s);
+  if (st == nullptr) return s;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  std::lock_guard<std::mutex> lock(st->ws_mutex);
+  auto it = st->scratch.find(stream);
+  if (it == st->scratch.end()) return GEMM_OK;
+  if (capturing(cs)) return GEMM_ERR_INVALID_VALUE;
+  Scratch& sc = it->second;
+  gemm_status_t result = GEMM_OK;
+  for (void* p : {static_cast<void*>(sc.ws), static_cast<void*>(sc.counters),
+                  static_cast<void*>(sc.stage)})
+    if (p != nullptr && cudaFreeAsync(p, cs) != cudaSuccess) {
+      cudaGetLastError();
+      result = GEMM_ERR_LAUNCH;
+    }
+  st->scratch.erase(it);
   return result;
 }
 

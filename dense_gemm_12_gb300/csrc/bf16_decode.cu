@@ -50,31 +50,21 @@
 namespace g12 {
 namespace {
 
-#ifndef G12_DECODE_NSUB
-#define G12_DECODE_NSUB 1
-#endif
 constexpr int BN = kDecBN;                 // MMA M: 128 columns of C per MMA tile
-constexpr int NSUB = G12_DECODE_NSUB;      // MMA tiles per n-group
+constexpr int NSUB = 1;                    // MMA tiles per n-group
 constexpr int NW = NSUB * BN;              // columns of C per n-group
 constexpr int kBoxesPerTile = BN / 64;     // 64-column TMA boxes per MMA tile
 // Accumulator rows held by each epilogue warp (one 32-lane TMEM quarter each).
 constexpr int kRowsPerQuarter = 32;
-#ifndef G12_DECODE_BK
-#define G12_DECODE_BK 128
-#endif
-constexpr int BK = G12_DECODE_BK;          // k per stage (one unit)
+constexpr int BK = 128;                    // k per stage (one unit)
 static_assert(BK == 64 || BK == 128, "k per stage must be 64 or 128");
 constexpr int kABoxes = BK / 64;           // BMr x 64 boxes of A per stage
 constexpr int kBoxBytesB = BK * 64 * 2;                   // one 64-column box of B
 constexpr int kStageBytesB = NSUB * kBoxesPerTile * kBoxBytesB;
 // Rows of C the output stage handles at a time (one 32x32b.x16 TMEM load).
 constexpr int kChunk = 16;
-#ifndef G12_DECODE_SMEM_KB
-#define G12_DECODE_SMEM_KB 220
-#endif
-#ifndef G12_DECODE_EARLY_UNITS
-#define G12_DECODE_EARLY_UNITS 4
-#endif
+// Shared memory the stage ring of one CTA may use.
+constexpr int kRingSmemKb = 220;
 // How long the combining CTA of a column group polls for the other
 // contributors' partial sums before it falls back to publishing its own.
 constexpr uint64_t kHandoffWaitNs = 20000;
@@ -82,14 +72,11 @@ constexpr uint64_t kHandoffWaitNs = 20000;
 // kernel in the stream (measured on back-to-back launches at N = 12288:
 // 0 units 17.92 us, 2 17.75, 4 17.68, 6 17.65, 8 17.77 -- more delays the
 // CTA's own first TMA loads).
-constexpr int kEarlyUnits = G12_DECODE_EARLY_UNITS;
-#ifndef G12_DECODE_ISSUERS
-#define G12_DECODE_ISSUERS 2
-#endif
+constexpr int kEarlyUnits = 4;
 // Threads issuing tcgen05.mma, each in its own warp and taking every
 // kIssuers-th stage into its own accumulator: with N = 16 the issue cost of
 // an MMA, not the tensor core, bounds how fast one thread can consume B.
-constexpr int kIssuers = G12_DECODE_ISSUERS;
+constexpr int kIssuers = 2;
 static_assert(kIssuers == 1 || kIssuers == 2, "one or two MMA issuers");
 constexpr int kThreads = 192 + (kIssuers - 1) * 32;
 constexpr int kEpiThreads = 128;
@@ -103,7 +90,7 @@ struct DecCfg {
   static constexpr int kChunks = BMR / kChunk;
   static constexpr int kStageBytesA = BMR * BK * 2;                  // 4, 8 or 16 KB
   static constexpr int kStageBytes = kStageBytesB + kStageBytesA;    // multiple of 1024
-  static constexpr int kStageBudget = (G12_DECODE_SMEM_KB * 1024) / kStageBytes;
+  static constexpr int kStageBudget = (kRingSmemKb * 1024) / kStageBytes;
   // Stages are a multiple of the issuer count, so that every stage is always
   // consumed by the same issuer.  An issuer then waits for the rounds of its
   // stages strictly in order; if two issuers alternated on one stage, one

@@ -45,17 +45,12 @@ namespace g12 {
 namespace {
 
 constexpr int BM = kTcBM, BN = kTcBN, BK = kTcBK;
-#ifndef G12_TC_STAGES
-#define G12_TC_STAGES 4
-#endif
 // Split overhead per part and round, in k-block times of the tensor core
 // (~0.35 us each; see tail_split): storing a 128 KB partial per CTA, and for a
 // tile's last part reading the others and writing the tile, measured at
 // roughly 3 us per part.
-#ifndef G12_TC_FIXUP_KB
-#define G12_TC_FIXUP_KB 8.0
-#endif
-constexpr int STAGES = G12_TC_STAGES;
+constexpr double kTcFixupKb = 8.0;
+constexpr int STAGES = 4;
 constexpr int kStageBytesA = BM * BK * 2;            // 16 KB
 constexpr int kStageBytesB = BK * BN * 2;            // 32 KB
 constexpr int kBoxBytesB = BK * 64 * 2;              // one 64-column box, 8 KB
@@ -574,15 +569,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 //                 both when the MMAs have read the stage;
 //   tmem_full[b]  in each CTA, from the commit after a tile's last k-block;
 //   tmem_empty[b] even CTA only: one arrival per epilogue warp of both CTAs.
-#ifndef G12_TC_PAIR_BK
-#define G12_TC_PAIR_BK 128
-#endif
-constexpr int PBK = G12_TC_PAIR_BK;                      // k per stage (64 or 128)
+constexpr int PBK = 128;                                 // k per stage (64 or 128)
 static_assert(PBK == 64 || PBK == 128, "pair kernel k-block");
-#ifndef G12_TC_PAIR_STAGES
-#define G12_TC_PAIR_STAGES (PBK == 64 ? 6 : 3)
-#endif
-constexpr int PS = G12_TC_PAIR_STAGES;
+constexpr int PS = PBK == 64 ? 6 : 3;                    // stages of the ring
 constexpr int kPairBN = BN / 2;                         // B columns held per CTA
 constexpr int kABoxBytes = BM * 64 * 2;                 // one 64-wide swizzled A box, 16 KB
 constexpr int kPairStageBytesA = BM * PBK * 2;          // PBK / 64 A boxes
@@ -848,7 +837,7 @@ TcPlan tc_plan(int M, int N, int K, int num_sms, const TileConfig* fixed) {
   // a pinned split is capped at one k-block per part
   pl.split = (fixed != nullptr && fixed->split > 0)
                  ? (fixed->split < num_kb ? fixed->split : num_kb)
-                 : tail_split(items, num_kb, workers, G12_TC_FIXUP_KB * BK / kblock);
+                 : tail_split(items, num_kb, workers, kTcFixupKb * BK / kblock);
   if (pl.split < 1) pl.split = 1;
   const int tail_items = items >= workers ? items % workers : items;
   if (tail_items == 0) pl.split = 1;

@@ -44,16 +44,8 @@ constexpr int BM = kSimtBM, BK = kSimtBK;
 // Unroll depth of the 4-k-step loop, per tile width (measured: the wide
 // tile is 1.3 % faster at 4092^3 with 4 than with 8, the narrow one 3.5 %
 // slower at 2048^3).
-#ifndef G12_SIMT_KQ_UNROLL_WIDE
-#define G12_SIMT_KQ_UNROLL_WIDE 4
-#endif
-#ifndef G12_SIMT_KQ_UNROLL_NARROW
-#define G12_SIMT_KQ_UNROLL_NARROW 8
-#endif
-#ifndef G12_SIMT_STAGES
-#define G12_SIMT_STAGES 4
-#endif
-constexpr int STAGES = G12_SIMT_STAGES;
+constexpr int kKqUnrollWide = 4, kKqUnrollNarrow = 8;
+constexpr int STAGES = 4;
 // The block is launched with 384 threads x 168 registers = 64512.
 constexpr int kLaunchRegs = 168;
 constexpr int kComputeWarps = 8;
@@ -69,7 +61,7 @@ struct Geom {
   static constexpr int kAcc = 8 * kCols;                // accumulators per lane
   static constexpr int kStageBytesB = BK * BN * 4;      // rows of BN x 4 B, not swizzled
   static constexpr int kStageBytes = kStageBytesA + kStageBytesB;
-  static constexpr int kKqUnroll = BN == 256 ? G12_SIMT_KQ_UNROLL_WIDE : G12_SIMT_KQ_UNROLL_NARROW;
+  static constexpr int kKqUnroll = BN == 256 ? kKqUnrollWide : kKqUnrollNarrow;
 };
 
 struct __align__(8) SimtSmemTail {

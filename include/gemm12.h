@@ -58,19 +58,32 @@
  *             arrival counters).  The
  *             library allocates it per device and per stream the first time a
  *             call on that stream needs it (or more of it), keeps and reuses
- *             it, and gemm_shutdown() frees it; calls on different streams
- *             never share scratch, calls on one stream are ordered by it.
- *             The staging copies of operands the TMA engine cannot describe
- *             (see Alignment) live in a second per-stream buffer, kept,
- *             grown and freed the same way (at most the size of the copied
- *             operands, rows padded to 16 bytes).
- *             Growing a stream's scratch synchronises that stream, so the
- *             first such call on a stream must come before that stream is
- *             captured into a CUDA graph.  Allocation failure returns
- *             GEMM_ERR_NO_MEMORY, except for a staging copy of gemm_sgemm or
- *             gemm_bf16gemm, which then runs the generic-load kernel on the
- *             operands as given.  See also gemm_bf16gemm_decode_static,
- *             which allocates nothing.
+ *             it, and frees it in gemm_release_stream(stream) or
+ *             gemm_shutdown(); calls on different streams never share
+ *             scratch, calls on one stream are ordered by it.  The staging
+ *             copies of operands the TMA engine cannot describe (see
+ *             Alignment) live in a second per-stream buffer, kept, grown and
+ *             freed the same way (at most the size of the copied operands,
+ *             rows padded to 16 bytes).  Allocation is stream-ordered
+ *             (cudaMallocAsync / cudaFreeAsync on `stream`, from the
+ *             device's default memory pool): growing never blocks the host,
+ *             the old buffer is released after the work already queued on
+ *             the stream.
+ *             Without the scratch it needs -- out of memory, or inside a
+ *             stream capture (CUDA graph), where the library allocates
+ *             nothing -- a call still runs: split tiles run whole instead
+ *             (same kernel), a decode launch that needs scratch runs on the
+ *             single-CTA tile kernel, and an operand that cannot be staged
+ *             is read by the generic-load kernels.  The result stays within
+ *             the same error bound but may differ in the last bits from a
+ *             call that had its scratch; to capture exactly the eager plan,
+ *             make one call of the shape on the stream before capturing it.
+ *             gemm_bf16gemm_fused, whose output stage exists only in the
+ *             tensor-core kernels, returns GEMM_ERR_NO_MEMORY instead when
+ *             an operand needs staging and no staging buffer can be had.
+ *             The first call of the library on a device (it looks up the
+ *             device's properties) must come before any capture.  See also
+ *             gemm_bf16gemm_decode_static, which allocates nothing.
  */
 #ifndef GEMM12_H
 #define GEMM12_H
@@ -272,6 +285,17 @@ gemm_status_t gemm_bf16gemm_decode_static(int64_t M, int64_t N, int64_t K, float
                                           const void *B, int64_t ldb,
                                           float beta, float *C, int64_t ldc, void *stream);
 
+/*
+ * gemm_release_stream -- frees the scratch and staging buffers the library
+ * keeps for `stream` on the current device (see Memory above), stream-ordered
+ * after the work already queued on that stream; a later call on the stream
+ * allocates them again.  Call it before destroying a stream that has run
+ * GEMMs, so that the buffers do not outlive it.  Returns GEMM_OK (also when
+ * the stream has none), GEMM_ERR_INVALID_VALUE while the stream is being
+ * captured, GEMM_ERR_LAUNCH if a free could not be queued.
+ */
+gemm_status_t gemm_release_stream(void *stream);
+
 /* Static, NUL-terminated description of a status code (never NULL). */
 const char *gemm_status_string(gemm_status_t status);
 
@@ -288,7 +312,8 @@ const char *gemm_status_string(gemm_status_t status);
  */
 gemm_status_t gemm_check_device_error(void *stream);
 
-/* Free the per-device decode workspaces.  Call with no GEMM in flight. */
+/* Free the scratch and staging buffers of every stream on every device
+ * (see Memory above).  Call with no GEMM in flight. */
 gemm_status_t gemm_shutdown(void);
 
 /* Kernel paths a call can take (reported by gemm_select_path). */

@@ -1,19 +1,30 @@
 """Library calls captured into a CUDA graph and replayed.
 
-The header's rule: a stream's first call that needs split-K scratch must
-come before that stream is captured (growing scratch synchronises the
-stream).  After such a warm-up, every launch path -- the CUDA-core kernel
+After one eager call of each shape on the capturing stream (which creates
+that stream's split-K scratch), every launch path -- the CUDA-core kernel
 with a split tail, the CTA-pair kernel with a split tail, the fused output
-stage with fp8 output and amax, the decode kernel split over all SMs, all of
-them launched with programmatic dependent launch -- must capture, and every
+stage with fp8 output and amax, the decode kernel in clusters, all of them
+launched with programmatic dependent launch -- must capture, and every
 replay must reproduce the eager results bit for bit.
+
+Inside a capture the library allocates nothing: a first call on a new
+stream whose plan needs scratch runs whole tiles instead (the decode kernel's
+runs of column groups fall back to the single-CTA tile kernel, an operand
+that would be staged is read by the generic loads).  Those captures must
+succeed and their replays must match the oracle -- bit for bit on small
+integers, where every order of summation is exact.  Growing a stream's
+scratch outside a capture is stream-ordered and must not wait for the work
+already queued on the stream.
 """
+import time
+
+import numpy as np
 import pytest
 import torch
 
 import dense_gemm_12_gb300 as g
 from dense_gemm_12_gb300.workloads import make_inputs
-from gpu_helpers import check_device_error
+from gpu_helpers import check_device_error, oracle_bf16, oracle_sgemm
 
 pytestmark = pytest.mark.gpu
 
@@ -73,4 +84,90 @@ def test_capture_and_replay_matches_eager():
             s.synchronize()
             for got, want in zip((out1, out2, out3, d8.view(torch.uint8), amax), eager):
                 assert torch.equal(got.view(torch.uint8), want.view(torch.uint8))
+    check_device_error()
+
+
+INT = ("int", None)
+
+
+def _sms():
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+def _first_call_cases():
+    sms = _sms()
+    return [
+        # (name, is_bf16, M, N, K, lda): each plan needs scratch or staging
+        ("fp32_split_tail", False, 128 * 13, 128 * 13, 2048, 2048),
+        ("fp32_staged_A", False, 1024, 1024, 1025, 1025),   # 2^31 FLOPs: staged
+        ("bf16_pair_split_tail", True, 512, 10240, 4096, 4096),
+        ("decode_runs_of_groups", True, 16, 128 * (sms + 10), 1024, 1024),
+    ]
+
+
+@pytest.mark.parametrize("case", range(4))
+def test_first_call_inside_capture_allocates_nothing(case):
+    name, bf16, M, N, K, lda = _first_call_cases()[case]
+    if bf16:
+        A, B, C = make_inputs(M, N, K, INT, INT, INT, seed=60 + case, dtype="bf16")
+    else:
+        A, B, C = make_inputs(M, N, K, INT, INT, INT, seed=60 + case)
+    dA, dB, dC0 = A.cuda(), B.cuda(), C.cuda()
+    out = torch.empty_like(dC0)
+    fn = g.gemm_bf16gemm if bf16 else g.gemm_sgemm
+    s = torch.cuda.Stream()            # new: the library holds nothing for it
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            out.copy_(dC0)
+            st = fn(M, N, K, 1.5, dA.data_ptr(), lda, dB.data_ptr(), N, -0.5, out.data_ptr(), N,
+                    s.cuda_stream)
+        assert st == 0, (name, g.gemm_status_string(st))
+        ref32, _, _ = (oracle_bf16 if bf16 else oracle_sgemm)(A, B, C, 1.5, -0.5, want64=False)
+        for _ in range(2):
+            out.fill_(float("nan"))
+            graph.replay()
+            s.synchronize()
+            assert np.array_equal(out.cpu().numpy().view(np.uint32), ref32.view(np.uint32)), name
+        # the same call eager afterwards creates the scratch and takes the
+        # planned path; on integers it gives the same bits
+        out.copy_(dC0)
+        assert fn(M, N, K, 1.5, dA.data_ptr(), lda, dB.data_ptr(), N, -0.5, out.data_ptr(), N,
+                  s.cuda_stream) == 0
+        s.synchronize()
+        assert np.array_equal(out.cpu().numpy().view(np.uint32), ref32.view(np.uint32)), name
+        assert g.gemm_release_stream(s.cuda_stream) == 0
+    check_device_error()
+
+
+def test_scratch_growth_does_not_wait_for_queued_work():
+    # a long GEMM queued first; then a call on the same new stream whose plan
+    # needs scratch.  Growing the scratch is stream-ordered, so the call
+    # returns while the long GEMM still runs.
+    big = 6144
+    A0, B0, _ = make_inputs(big, big, big, seed=70, with_c=False)
+    dA0, dB0 = A0.cuda(), B0.cuda()
+    dC0 = torch.empty(big, big, device="cuda")
+    M, N, K = 128 * 13, 128 * 13, 2048
+    A, B, C = make_inputs(M, N, K, INT, INT, INT, seed=71)
+    dA, dB, dC = A.cuda(), B.cuda(), C.cuda()
+    assert g.gemm_split_parts(0, M, N, K) > 1
+    s = torch.cuda.Stream()
+    done = torch.cuda.Event()
+    torch.cuda.synchronize()
+    assert g.gemm_sgemm(big, big, big, 1.0, dA0.data_ptr(), big, dB0.data_ptr(), big, 0.0,
+                        dC0.data_ptr(), big, s.cuda_stream) == 0
+    t0 = time.perf_counter()
+    assert g.gemm_sgemm(M, N, K, 1.5, dA.data_ptr(), K, dB.data_ptr(), N, -0.5, dC.data_ptr(),
+                        N, s.cuda_stream) == 0
+    host_s = time.perf_counter() - t0
+    done.record(s)
+    still_running = not done.query()
+    s.synchronize()
+    # 6144^3 fp32 takes ~7 ms on the GPU; the second call must not have waited for it
+    assert still_running and host_s < 3e-3, host_s
+    ref32, _, _ = oracle_sgemm(A, B, C, 1.5, -0.5, want64=False)
+    assert np.array_equal(dC.cpu().numpy().view(np.uint32), ref32.view(np.uint32))
+    assert g.gemm_release_stream(s.cuda_stream) == 0
+    assert g.gemm_release_stream(s.cuda_stream) == 0   # nothing left: still fine
     check_device_error()
