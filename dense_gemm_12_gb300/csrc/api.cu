@@ -344,7 +344,7 @@ bool config_fields_valid(const gemm_config_t* c, bool bf16) {
   const bool kernel_ok = c->kernel == GEMM_KERNEL_AUTO || c->kernel == GEMM_KERNEL_SINGLE_CTA ||
                          (bf16 && c->kernel == GEMM_KERNEL_CTA_PAIR) ||
                          (!bf16 && c->kernel == GEMM_KERNEL_WIDE);
-  const bool split_ok = (c->split >= 0 && c->split <= 8) || (!bf16 && c->split == GEMM_SPLIT_STREAM);
+  const bool split_ok = (c->split >= 0 && c->split <= 8) || c->split == GEMM_SPLIT_STREAM;
   return kernel_ok && split_ok && c->group_m >= 0 && c->group_m <= 64;
 }
 
@@ -618,7 +618,7 @@ int gemm_split_parts(int is_bf16, int64_t M, int64_t N, int64_t K) {
   const TileConfig tc = resolve_config(is_bf16 != 0, M, N, K, st->num_sms, nullptr, nullptr);
   if (is_bf16) {
     if (decode_path(M, N, K)) return 1;
-    return tc_plan(m, n, k, st->num_sms, &tc).split;
+    return tc_plan_max_parts(tc_plan(m, n, k, st->num_sms, &tc), m, n, k);
   }
   return simt_plan_max_parts(simt_plan(m, n, k, st->num_sms, &tc, true), m, n, k);
 }
@@ -766,7 +766,7 @@ static gemm_status_t run_bf16_tensor_core(DeviceState* st, gemm_path_t path, int
     TcPlan run = pl;
     a.ws = nullptr;
     a.counters = nullptr;
-    if (pl.split > 1) {
+    if (pl.split > 1 || pl.sk_workers > 0) {
       // Split items: the stream's scratch stays locked until the launch is
       // queued, so no other thread can regrow it underneath.  Without scratch
       // (inside a stream capture, or out of memory) every item runs whole.
@@ -786,6 +786,7 @@ static gemm_status_t run_bf16_tensor_core(DeviceState* st, gemm_path_t path, int
     }
     a.full_items = run.full_items;
     a.split = run.split;
+    a.sk_workers = run.sk_workers;
     a.group_m = run.group_m;
     return from_cuda(launch_tc_bf16(a, run, &tmA, &tmB, cs));
   }
@@ -921,8 +922,8 @@ static gemm_status_t get_config(int is_bf16, int64_t M, int64_t N, int64_t K, ge
   const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
   if (is_bf16) {
     const TcPlan pl = tc_plan(m, n, k, st->num_sms, &tc);
-    *out = gemm_config_t{pl.pair ? GEMM_KERNEL_CTA_PAIR : GEMM_KERNEL_SINGLE_CTA, pl.split,
-                         pl.group_m};
+    *out = gemm_config_t{pl.pair ? GEMM_KERNEL_CTA_PAIR : GEMM_KERNEL_SINGLE_CTA,
+                         pl.sk_workers > 0 ? GEMM_SPLIT_STREAM : pl.split, pl.group_m};
   } else {
     const SimtPlan pl = simt_plan(m, n, k, st->num_sms, &tc, true);
     *out = gemm_config_t{pl.wide ? GEMM_KERNEL_WIDE : GEMM_KERNEL_SINGLE_CTA,

@@ -95,31 +95,83 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
 }
 
 // One work unit: item (tile or pair tile), its k-block range and, for a
-// split item, its part index and tail index (part = -1 for a whole item).
+// tail item cut along k, its tail index, its part index among the item's
+// parts (k order), the item's number of parts and the unit's own workspace
+// slot (tail = -1 for a whole item).  An empty unit (kb0 == kb1: a stream-K
+// worker whose range lies inside one item has no second segment) is skipped
+// by every role.
 struct Unit {
-  int item, kb0, kb1, part, tail;
+  int item, kb0, kb1, tail, part, parts, slot;
 };
 
+// Units of the launch: the whole items, then either `split` parts of every
+// tail item (unit full_items + t * split + q), or, with stream-K, two
+// segment slots per worker (unit full_items + s * G + j is segment s of
+// worker j; see sk_lo).  Workers walk units in strides of G, so worker j
+// meets exactly its own segments.
 __device__ __forceinline__ int num_units(const TcArgs& p, int num_items) {
+  if (p.sk_workers > 0) return p.full_items + 2 * p.sk_workers;
   return p.full_items + (num_items - p.full_items) * p.split;
 }
 
-__device__ __forceinline__ Unit unit_of(const TcArgs& p, int u, int num_kb) {
+// Workspace slot of part q (k order) of tail item t.
+__device__ __forceinline__ int part_slot(const TcArgs& p, int t, int q, int num_kb, int64_t W) {
+  if (p.sk_workers == 0) return t * p.split + q;
+  const int64_t G = p.sk_workers;
+  const int64_t j = sk_worker(static_cast<int64_t>(t) * num_kb, W, G) + q;
+  return static_cast<int>(2 * j + (sk_lo(j, W, G) < static_cast<int64_t>(t) * num_kb ? 1 : 0));
+}
+
+__device__ __forceinline__ Unit unit_of(const TcArgs& p, int u, int num_kb, int num_items) {
   Unit w;
+  w.tail = -1;
+  w.part = 0;
+  w.parts = 1;
+  w.slot = -1;
   if (u < p.full_items) {
     w.item = u;
     w.kb0 = 0;
     w.kb1 = num_kb;
-    w.part = -1;
-    w.tail = -1;
     return w;
   }
   const int v = u - p.full_items;
-  w.tail = v / p.split;
-  w.part = v - w.tail * p.split;
+  if (p.sk_workers == 0) {
+    w.tail = v / p.split;
+    w.part = v - w.tail * p.split;
+    w.parts = p.split;
+    w.slot = v;
+    w.item = p.full_items + w.tail;
+    w.kb0 = w.part * num_kb / p.split;
+    w.kb1 = (w.part + 1) * num_kb / p.split;
+    return w;
+  }
+  // Stream-K: the tail's W k-blocks, item after item, in contiguous ranges
+  // [sk_lo(j), sk_lo(j + 1)) per worker j; a range touches one or two items.
+  const int64_t G = p.sk_workers;
+  const int s = v / p.sk_workers;
+  const int64_t j = v - s * p.sk_workers;
+  const int64_t W = static_cast<int64_t>(num_items - p.full_items) * num_kb;
+  const int64_t lo = sk_lo(j, W, G), hi = sk_lo(j + 1, W, G);
+  int64_t t = lo / num_kb;
+  int64_t a = lo - t * num_kb, b = min(hi - t * num_kb, static_cast<int64_t>(num_kb));
+  w.item = p.full_items;
+  w.kb0 = w.kb1 = 0;
+  if (s == 1) {
+    if (hi <= (t + 1) * num_kb) return w;  // the range ends inside its first item
+    ++t;
+    a = 0;
+    b = hi - t * num_kb;
+  }
+  if (a >= b) return w;
+  const int64_t first = sk_worker(t * num_kb, W, G);
+  const int64_t last = sk_worker((t + 1) * num_kb - 1, W, G);
+  w.tail = static_cast<int>(t);
   w.item = p.full_items + w.tail;
-  w.kb0 = w.part * num_kb / p.split;
-  w.kb1 = (w.part + 1) * num_kb / p.split;
+  w.kb0 = static_cast<int>(a);
+  w.kb1 = static_cast<int>(b);
+  w.part = static_cast<int>(j - first);
+  w.parts = static_cast<int>(last - first + 1);
+  w.slot = static_cast<int>(2 * j + s);
   return w;
 }
 
@@ -291,18 +343,21 @@ __device__ __forceinline__ void epi_bar() {
 
 // Output stage of one work unit, run by the 4 epilogue warps of a CTA (thread
 // et = TMEM lane et = row et of the CTA's 128-row tile).  taddr: this warp's
-// lanes of the accumulator.  slot: this CTA's index among the split items'
-// counters (-1 for a whole item).
+// lanes of the accumulator.  cpi / rank: CTAs per item (1, or 2 on pairs) and
+// this CTA's rank in it; every CTA of an item keeps its own counter (tail
+// index * cpi + rank) and its own partial sums (slot * cpi + rank).
 //
-// A split part stores its partial sums (thread-major float4s, coalesced per
-// warp), then counts its arrival; the last of the `split` parts re-reads its
-// own accumulator and adds all parts in part order -- a fixed order, so the
-// result does not depend on which part finishes last -- and writes D.
+// A part of a split item stores its partial sums (thread-major float4s,
+// coalesced per warp), then counts its arrival; the last of the item's parts
+// re-reads its own accumulator and adds all parts in k order -- a fixed
+// order, so the result does not depend on which part finishes last -- and
+// writes D.
 template <bool FUSED>
-__device__ __forceinline__ void epilogue_unit(const TcArgs& p, uint32_t taddr, float4* stg,
-                                              int row_base, int tn, int slot, int part, int et,
+__device__ __forceinline__ void epilogue_unit(const TcArgs& p, const Unit& w, uint32_t taddr,
+                                              float4* stg, int row_base, int tn, int cpi,
+                                              int rank, int num_kb, int64_t W, int et,
                                               int* last_flag, float& amax_acc) {
-  if (slot < 0) {
+  if (w.tail < 0) {
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
       uint32_t r[32];
@@ -313,9 +368,11 @@ __device__ __forceinline__ void epilogue_unit(const TcArgs& p, uint32_t taddr, f
     return;
   }
   float4* const ws4 = reinterpret_cast<float4*>(p.ws);
-  const int64_t slot_base = static_cast<int64_t>(slot) * p.split;  // in parts
+  auto part_base = [&](int slot) {
+    return ws4 + (static_cast<int64_t>(slot) * cpi + rank) * (kPartFloats / 4);
+  };
   {
-    float4* mine = ws4 + (slot_base + part) * (kPartFloats / 4);
+    float4* mine = part_base(w.slot);
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
       uint32_t r[32];
@@ -328,14 +385,15 @@ __device__ __forceinline__ void epilogue_unit(const TcArgs& p, uint32_t taddr, f
                            __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3])));
     }
   }
+  const int counter = w.tail * cpi + rank;
   epi_bar();
   if (et == 0) {
-    const uint32_t before = atomic_add_acq_rel_gpu(p.counters + slot, 1u);
-    *last_flag = (before == static_cast<uint32_t>(p.split - 1)) ? 1 : 0;
+    const uint32_t before = atomic_add_acq_rel_gpu(p.counters + counter, 1u);
+    *last_flag = (before == static_cast<uint32_t>(w.parts - 1)) ? 1 : 0;
   }
   epi_bar();
   if (*reinterpret_cast<volatile int*>(last_flag)) {
-    // Parts are added in part order; the other parts' partial sums are read
+    // Parts are added in k order; the other parts' partial sums are read
     // two parts per round trip (the loads of a pair are independent), and
     // this part's own accumulator comes from TMEM.
     const float4 zero4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
@@ -346,12 +404,15 @@ __device__ __forceinline__ void epilogue_unit(const TcArgs& p, uint32_t taddr, f
       for (int i = 0; i < 32; ++i) sum[i] = 0.0f;
       uint32_t r[32];
 #pragma unroll 1
-      for (int q0 = 0; q0 < p.split; q0 += 2) {
-        const bool has_b = q0 + 1 < p.split;
-        const bool load_a = q0 != part;
-        const bool load_b = has_b && q0 + 1 != part;
-        const float4* src_a = ws4 + (slot_base + q0) * (kPartFloats / 4) + c * 8 * kEpiThreads + et;
-        const float4* src_b = src_a + kPartFloats / 4;
+      for (int q0 = 0; q0 < w.parts; q0 += 2) {
+        const bool has_b = q0 + 1 < w.parts;
+        const bool load_a = q0 != w.part;
+        const bool load_b = has_b && q0 + 1 != w.part;
+        const float4* src_a =
+            part_base(part_slot(p, w.tail, q0, num_kb, W)) + c * 8 * kEpiThreads + et;
+        const float4* src_b =
+            has_b ? part_base(part_slot(p, w.tail, q0 + 1, num_kb, W)) + c * 8 * kEpiThreads + et
+                  : src_a;
         float4 va[8], vb[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
@@ -389,7 +450,7 @@ __device__ __forceinline__ void epilogue_unit(const TcArgs& p, uint32_t taddr, f
       for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(sum[i]);
       store_chunk<FUSED>(p, stg, row_base, tn * BN + c * 32, r, amax_acc);
     }
-    if (et == 0) p.counters[slot] = 0u;
+    if (et == 0) p.counters[counter] = 0u;
   }
   epi_bar();  // last_flag is rewritten by the next split unit
 }
@@ -409,7 +470,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tiles_m = (p.M + BM - 1) / BM;
   const int tiles_n = (p.N + BN - 1) / BN;
   const int num_kb = (p.K + BK - 1) / BK;
-  const int units = num_units(p, tiles_m * tiles_n);
+  const int num_items = tiles_m * tiles_n;
+  const int units = num_units(p, num_items);
+  const int64_t W = static_cast<int64_t>(num_items - p.full_items) * num_kb;  // stream-K tail
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -447,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t it = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-        const Unit w = unit_of(p, u, num_kb);
+        const Unit w = unit_of(p, u, num_kb, num_items);
         int tm, tn;
         tile_coords(w.item, tiles_m, tiles_n, p.group_m, tm, tn);
         for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
@@ -480,9 +543,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t j = 0;
       bool ok = true;
       bool issued = false;
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++j) {
-        const Unit w = unit_of(p, u, num_kb);
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        const Unit w = unit_of(p, u, num_kb, num_items);
+        if (w.kb0 == w.kb1) continue;
         const uint32_t ab = j & 1u, ar = j >> 1;
+        ++j;
         if (!mbar_wait(&tail->tmem_empty[ab], (ar & 1u) ^ 1u, abort_flag, p.err)) {
           ok = false;
           break;
@@ -528,18 +593,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     float4* stg = reinterpret_cast<float4*>(epi_stage + quarter * 4096);
     float amax_acc = 0.0f;
     uint32_t j = 0;
-    for (int u = blockIdx.x; u < units; u += gridDim.x, ++j) {
-      const Unit w = unit_of(p, u, num_kb);
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      const Unit w = unit_of(p, u, num_kb, num_items);
+      if (w.kb0 == w.kb1) continue;
       int tm, tn;
       tile_coords(w.item, tiles_m, tiles_n, p.group_m, tm, tn);
       const uint32_t ab = j & 1u, ar = j >> 1;
+      ++j;
       const bool ok = mbar_wait(&tail->tmem_full[ab], ar & 1u, abort_flag, p.err);
       // Leave together if a wait ran out anywhere (see named_bar_any).
       if (named_bar_any(kEpiBarAny, kEpiThreads, !ok)) break;
       tc_fence_after_sync();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + ab * BN;
-      epilogue_unit<FUSED>(p, taddr, stg, tm * BM + quarter * 32, tn, w.tail, w.part, et,
-                    &tail->last_flag, amax_acc);
+      epilogue_unit<FUSED>(p, w, taddr, stg, tm * BM + quarter * 32, tn, 1, 0, num_kb, W, et,
+                           &tail->last_flag, amax_acc);
       tc_fence_before_sync();
       mbar_arrive(&tail->tmem_empty[ab]);
     }
@@ -611,8 +678,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tiles_m = (p.M + BM - 1) / BM;
   const int tiles_n = (p.N + BN - 1) / BN;
   const int pairs_m = (tiles_m + 1) / 2;
-  const int units = num_units(p, pairs_m * tiles_n);
+  const int num_items = pairs_m * tiles_n;
+  const int units = num_units(p, num_items);
   const int num_kb = (p.K + PBK - 1) / PBK;
+  const int64_t W = static_cast<int64_t>(num_items - p.full_items) * num_kb;  // stream-K tail
   const uint32_t rank = cluster_cta_rank() & 1u;
   const bool even = (rank == 0);
   const int first_item = static_cast<int>(blockIdx.x) / 2;
@@ -657,7 +726,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t it = 0;
       bool ok = true;
       for (int u = first_item; u < units && ok; u += item_stride) {
-        const Unit w = unit_of(p, u, num_kb);
+        const Unit w = unit_of(p, u, num_kb, num_items);
         int pm, tn;
         tile_coords(w.item, pairs_m, tiles_n, p.group_m, pm, tn);
         const int tm = pm * 2 + static_cast<int>(rank);
@@ -700,9 +769,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t j = 0;
       bool ok = true;
       bool issued = false;
-      for (int u = first_item; u < units && ok; u += item_stride, ++j) {
-        const Unit w = unit_of(p, u, num_kb);
+      for (int u = first_item; u < units && ok; u += item_stride) {
+        const Unit w = unit_of(p, u, num_kb, num_items);
+        if (w.kb0 == w.kb1) continue;
         const uint32_t ab = j & 1u, ar = j >> 1;
+        ++j;
         if (!mbar_wait(&tail->tmem_empty[ab], (ar & 1u) ^ 1u, abort_flag, p.err)) {
           ok = false;
           break;
@@ -754,20 +825,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     float amax_acc = 0.0f;
     const uint32_t tmem_empty0 = mapa_shared(smem_u32(&tail->tmem_empty[0]), 0);
     uint32_t j = 0;
-    for (int u = first_item; u < units; u += item_stride, ++j) {
-      const Unit w = unit_of(p, u, num_kb);
+    for (int u = first_item; u < units; u += item_stride) {
+      const Unit w = unit_of(p, u, num_kb, num_items);
+      if (w.kb0 == w.kb1) continue;
       int pm, tn;
       tile_coords(w.item, pairs_m, tiles_n, p.group_m, pm, tn);
       const int tm = pm * 2 + static_cast<int>(rank);
       const uint32_t ab = j & 1u, ar = j >> 1;
+      ++j;
       const bool ok = mbar_wait(&tail->tmem_full[ab], ar & 1u, abort_flag, p.err);
       if (named_bar_any(kEpiBarAny, kEpiThreads, !ok)) break;
       tc_fence_after_sync();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + ab * BN;
       // each CTA of the pair owns the counter and partials of its 128 rows
-      const int slot = w.tail < 0 ? -1 : w.tail * 2 + static_cast<int>(rank);
-      epilogue_unit<FUSED>(p, taddr, stg, tm * BM + quarter * 32, tn, slot, w.part, et,
-                    &tail->last_flag, amax_acc);
+      epilogue_unit<FUSED>(p, w, taddr, stg, tm * BM + quarter * 32, tn, 2,
+                           static_cast<int>(rank), num_kb, W, et, &tail->last_flag, amax_acc);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(tmem_empty0 + ab * static_cast<uint32_t>(sizeof(uint64_t)));
@@ -834,12 +906,25 @@ TcPlan tc_plan(int M, int N, int K, int num_sms, const TileConfig* fixed) {
   const int ctas_per_item = pl.pair ? 2 : 1;
   const int items = pl.pair ? ((tiles_m + 1) / 2) * tiles_n : tiles_m * tiles_n;
   const int workers = pl.pair ? pair_max_clusters(num_sms) : num_sms;
+  const int tail_items = items >= workers ? items % workers : items;
+  // Stream-K (pinned, or chosen by the dispatch table): the tail items'
+  // k-blocks dealt out to all workers, at least one each (with fewer k-blocks
+  // than workers the equal split below is used instead).
+  if (fixed != nullptr && fixed->split == GEMM_SPLIT_STREAM && tail_items > 0 &&
+      static_cast<int64_t>(tail_items) * num_kb >= workers) {
+    pl.split = 1;
+    pl.sk_workers = workers;
+    pl.full_items = items - tail_items;
+    pl.grid = ctas_per_item * workers;
+    pl.ws_floats = 2 * static_cast<int64_t>(workers) * ctas_per_item * kPartFloats;
+    pl.counters = static_cast<int64_t>(tail_items) * ctas_per_item;
+    return pl;
+  }
   // a pinned split is capped at one k-block per part
   pl.split = (fixed != nullptr && fixed->split > 0)
                  ? (fixed->split < num_kb ? fixed->split : num_kb)
                  : tail_split(items, num_kb, workers, kTcFixupKb * BK / kblock);
   if (pl.split < 1) pl.split = 1;
-  const int tail_items = items >= workers ? items % workers : items;
   if (tail_items == 0) pl.split = 1;
   const int tail = pl.split > 1 ? tail_items : 0;
   pl.full_items = items - tail;
@@ -848,6 +933,22 @@ TcPlan tc_plan(int M, int N, int K, int num_sms, const TileConfig* fixed) {
   pl.ws_floats = static_cast<int64_t>(tail) * pl.split * ctas_per_item * kPartFloats;
   pl.counters = static_cast<int64_t>(tail) * ctas_per_item;
   return pl;
+}
+
+int tc_plan_max_parts(const TcPlan& pl, int M, int N, int K) {
+  if (pl.sk_workers == 0) return pl.split;
+  const int tiles_m = (M + BM - 1) / BM;
+  const int tiles_n = (N + BN - 1) / BN;
+  const int items = pl.pair ? ((tiles_m + 1) / 2) * tiles_n : tiles_m * tiles_n;
+  const int64_t num_kb = (K + (pl.pair ? PBK : BK) - 1) / (pl.pair ? PBK : BK);
+  const int64_t tail = items - pl.full_items;
+  const int64_t W = tail * num_kb, G = pl.sk_workers;
+  int most = 1;
+  for (int64_t t = 0; t < tail; ++t) {
+    const int64_t parts = sk_worker((t + 1) * num_kb - 1, W, G) - sk_worker(t * num_kb, W, G) + 1;
+    if (parts > most) most = static_cast<int>(parts);
+  }
+  return most;
 }
 
 cudaError_t launch_tc_bf16(const TcArgs& a, const TcPlan& plan, const CUtensorMap* tmA,

@@ -111,12 +111,15 @@ struct TcArgs {
   uint32_t* err;
   // Work plan (see tc_plan): work items are tiles (128 x 256) or, on CTA
   // pairs, pair tiles (256 x 256) in raster order.  Items [0, full_items) run
-  // whole; every later one is cut into `split` k-ranges whose partial sums
-  // meet in `ws` (128 x 256 floats per part and CTA) and are added, in part
-  // order, by the last part to arrive on its counter in `counters` (one per
-  // item and CTA, zero between launches).
+  // whole; the later ("tail") items are either cut into `split` equal
+  // k-ranges each (sk_workers == 0), or, with sk_workers = G > 0, their
+  // k-blocks taken together are dealt out evenly to G workers (stream-K, see
+  // sk_lo).  Partial sums meet in `ws` (128 x 256 floats per part and CTA)
+  // and are added, in k order, by the last part to arrive on its item's
+  // counter in `counters` (one per tail item and CTA, zero between launches).
   int full_items;
   int split;
+  int sk_workers;
   float* ws;
   uint32_t* counters;
   int group_m;     // raster group height in tile rows (pair-tile rows on pairs)
@@ -127,14 +130,18 @@ struct TcPlan {
   bool pair;          // CTA-pair kernel or single-CTA kernel
   int full_items;
   int split;
+  int sk_workers;     // > 0: stream-K tail over this many workers (split is then 1)
   int grid;           // CTAs to launch (pairs: twice the clusters)
   int group_m;
   int64_t ws_floats;  // workspace the split items need
   int64_t counters;   // counters the split items need
 };
-// `fixed` pins kernel, split and group height; nullptr: the pair kernel for
-// M > 128, the cost model's split, groups of 8.
+// `fixed` pins kernel, split (GEMM_SPLIT_STREAM: a stream-K tail) and group
+// height; nullptr: the pair kernel for M > 128, the cost model's split,
+// groups of 8.
 TcPlan tc_plan(int M, int N, int K, int num_sms, const TileConfig* fixed);
+// Largest number of parts any tail item of the plan is cut into (1 = none).
+int tc_plan_max_parts(const TcPlan& pl, int M, int N, int K);
 // k-rows of B per TMA box of the single-CTA (pair = false) or pair kernel.
 int tc_b_box_rows(bool pair);
 

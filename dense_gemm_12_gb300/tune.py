@@ -52,7 +52,7 @@ def candidates(is_bf16: bool, M: int, K: int):
     kernels = ["single_cta"] if is_bf16 else ["single_cta", "wide"]
     if is_bf16 and M > 128:
         kernels = ["cta_pair", "single_cta"]
-    splits = SPLITS if is_bf16 else SPLITS + [-1]   # -1: the stream-K tail (fp32)
+    splits = SPLITS + [-1]   # -1: the stream-K tail
     num_kb = -(-K // (64 if is_bf16 else 32))
     for kernel, split, group in itertools.product(kernels, splits, GROUPS):
         if split <= num_kb:

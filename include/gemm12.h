@@ -359,7 +359,7 @@ gemm_path_t gemm_select_path(int is_bf16, int64_t M, int64_t N, int64_t K,
  * grid's last round ("A GEMM Kernel, Step by Step": the partial last wave of
  * "The fringe and the last wave", filled by the split-K of "What is left").
  * 1 means no item is split.  Under the stream-K tail (GEMM_SPLIT_STREAM)
- * the tail tiles are cut into differing numbers of k-ranges; the largest is
+ * the tail items are cut into differing numbers of k-ranges; the largest is
  * reported.  `is_bf16`
  * selects gemm_bf16gemm's tensor-core tile kernels instead of gemm_sgemm's
  * CUDA-core kernel; the decode kernel (bf16, small M) plans its
@@ -392,17 +392,19 @@ typedef enum {
                                     as many tiles)                             */
 } gemm_kernel_t;
 
-/* gemm_config_t.split value (fp32 only): stream-K tail.  The k-blocks of all
- * tiles past the last whole round are dealt out evenly to the persistent
- * CTAs in contiguous ranges that may cross a tile boundary; each tile's
- * partial sums are added in k order by the last range to finish it. */
+/* gemm_config_t.split value: stream-K tail.  The k-blocks of all work items
+ * past the last whole round are dealt out evenly to the persistent workers
+ * (CTAs, or CTA pairs) in contiguous ranges that may cross an item boundary;
+ * each item's partial sums are added in k order by the last range to finish
+ * it.  bf16: used when those k-blocks are at least as many as the workers,
+ * else the equal split of the cost model runs instead. */
 #define GEMM_SPLIT_STREAM (-1)
 
 typedef struct {
     int kernel;   /* a gemm_kernel_t                                          */
     int split;    /* k-ranges per work item of the persistent grid's last
                      round: 0 = automatic, 1 = none, 2..8 (capped at one
-                     k-block per range), or GEMM_SPLIT_STREAM (fp32)          */
+                     k-block per range), or GEMM_SPLIT_STREAM                 */
     int group_m;  /* raster order: work items walk column by column through
                      groups of this many item rows; 0 = automatic, 1..64     */
 } gemm_config_t;
@@ -416,7 +418,7 @@ typedef struct {
  * decode kernel runs only under GEMM_KERNEL_AUTO).  The fp32 path has two
  * tile widths (GEMM_KERNEL_SINGLE_CTA: 128 x 128, GEMM_KERNEL_WIDE:
  * 128 x 256); GEMM_KERNEL_CTA_PAIR is invalid there, and GEMM_KERNEL_WIDE
- * and GEMM_SPLIT_STREAM are invalid for bf16.  The fields are ignored on
+ * is invalid for bf16.  The fields are ignored on
  * the paths without tiles (M, N, K or alpha zero: nothing to configure).
  * Errors: fields out of range give
  * GEMM_ERR_INVALID_VALUE; otherwise as the plain calls.  Operands that TMA

@@ -55,8 +55,8 @@ def test_candidates_respect_kernel_and_k():
     assert max(x["split"] for x in c) == 2
     c = list(tune.candidates(False, 4092, 4092))
     assert {x["kernel"] for x in c} == {"single_cta", "wide"}
-    assert -1 in {x["split"] for x in c}                        # stream-K tail, fp32 only
-    assert -1 not in {x["split"] for x in tune.candidates(True, 1024, 4096)}
+    assert -1 in {x["split"] for x in c}                        # stream-K tail
+    assert -1 in {x["split"] for x in tune.candidates(True, 1024, 4096)}
 
 
 def _result(M, auto_ms, best_ms, is_bf16=1):

@@ -57,6 +57,46 @@ def test_bf16_every_config_exact(M, N, K):
     check_device_error()
 
 
+# Stream-K tails of the tensor-core kernels (split = -1).  The tail's k-blocks
+# (tail items x k-blocks per item; 128-deep on pairs, 64 on one CTA) must be
+# at least the workers -- 76 resident pairs or 152 CTAs on a GB300 -- or the
+# equal split runs instead; each shape below has more.
+@pytest.mark.parametrize("kernel,M,N,K", [
+    ("cta_pair", 1024, 2048, 4096),    # 32 pair tiles, all in the tail: 1024 k-blocks
+    ("cta_pair", 2048, 10240, 2048),   # 320 pair tiles: 4 whole rounds + 16 in the tail
+    ("cta_pair", 1000, 4100, 1500),    # ragged M, N and K (partial last k-block)
+    ("single_cta", 128, 4096, 4096),   # 16 tiles, 1024 k-blocks
+    ("single_cta", 200, 3000, 1000),   # 24 tiles, ragged
+])
+def test_bf16_stream_k_exact_and_repeatable(kernel, M, N, K):
+    A, B, C = make_inputs(M, N, K, ("int", None), ("int", None), ("int", None), seed=M + K,
+                          dtype="bf16")
+    ref32, _, _ = oracle_bf16(A, B, C, 1.5, -0.5)
+    for gm in (1, 8):
+        cfg = {"kernel": kernel, "split": -1, "group_m": gm}
+        first = None
+        for _ in range(2):
+            st, out = _run(True, A, B, C, 1.5, -0.5, cfg)
+            assert st == 0, cfg
+            assert np.array_equal(out.numpy().view(np.uint32), ref32.view(np.uint32)), cfg
+            if first is not None:
+                assert torch.equal(out, first)
+            first = out
+    check_device_error()
+
+
+@pytest.mark.parametrize("kernel,M,N,K", [("cta_pair", 1000, 4100, 1500),
+                                          ("single_cta", 128, 4096, 4096)])
+def test_bf16_stream_k_random_within_bound(kernel, M, N, K):
+    A, B, C = make_inputs(M, N, K, ("normal", 1.0), ("normal", 0.05), ("uniform", None),
+                          seed=7 + M, dtype="bf16")
+    _, ref64, den = oracle_bf16(A, B, C, 0.7, 0.3)
+    st, out = _run(True, A, B, C, 0.7, 0.3, {"kernel": kernel, "split": -1, "group_m": 0})
+    assert st == 0
+    assert ratio(out, ref64, den) <= TOL_BF16
+    check_device_error()
+
+
 @pytest.mark.parametrize("M,N,K", [(100, 260, 1024), (1000, 1300, 600), (2048, 1280, 1024),
                                    (2600, 2900, 333)])
 def test_fp32_every_config_exact(M, N, K):
@@ -134,7 +174,7 @@ def test_invalid_configs_rejected():
     B = torch.zeros(K, N, dtype=torch.bfloat16, device="cuda")
     C = torch.zeros(M, N, device="cuda")
     s = torch.cuda.current_stream().cuda_stream
-    bad = [{"kernel": 3}, {"split": 9}, {"split": -1}, {"group_m": 65}, {"group_m": -2}]
+    bad = [{"kernel": 3}, {"split": 9}, {"split": -2}, {"group_m": 65}, {"group_m": -2}]
     for cfg in bad:
         assert g.gemm_bf16gemm_config(M, N, K, 1.0, A.data_ptr(), K, B.data_ptr(), N, 0.0,
                                       C.data_ptr(), N, cfg, s) == 1, cfg
