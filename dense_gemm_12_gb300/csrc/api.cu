@@ -808,7 +808,7 @@ static gemm_status_t run_bf16_tensor_core(DeviceState* st, gemm_path_t path, int
   a.cluster = decode_cluster(a.M, a.N, a.K, st->num_sms);
   // One CTA per column group, or clusters that exchange their partial sums
   // in shared memory: no scratch is touched.
-  if (grid == decode_counter_count(a.N) || a.cluster > 1) {
+  if (grid == decode_groups(a.N) || a.cluster > 1) {
     a.workspace = nullptr;
     a.counters = nullptr;
     return from_cuda(launch_tc_decode(a, &tmA, &tmB, grid, cs));
@@ -816,7 +816,7 @@ static gemm_status_t run_bf16_tensor_core(DeviceState* st, gemm_path_t path, int
   if (!lock.owns_lock()) lock.lock();
   Scratch* sc = nullptr;
   gemm_status_t s = ensure_scratch(*st, cs, decode_workspace_floats(a.M, a.N, a.K, grid),
-                                   decode_counter_count(a.N), &sc);
+                                   decode_counter_count(a.M, a.N), &sc);
   if (s == GEMM_ERR_NO_MEMORY) {
     // No scratch for the runs of column groups (inside a stream capture, or
     // out of memory): the single-CTA tile kernel with whole tiles needs none.

@@ -286,9 +286,30 @@ __device__ __forceinline__ void cluster_reduce_store(const DecodeArgs& p, uint32
     cluster_reduce_store_s<FUSED, BMR, 8>(p, part, ept);
 }
 
+// The arguments row block rb of a launch sees: rows [rb * BMR, rb * BMR + BMR)
+// of the product, C, D and the residual (M counts only those rows), and its
+// own arrival counters (n_groups per block) and workspace (ws_floats per
+// block).  Row block 0 sees the launch's own arguments.
+template <int BMR>
+__device__ __forceinline__ DecodeArgs row_block(const DecodeArgs& a, int rb, int n_groups,
+                                                int64_t ws_floats) {
+  DecodeArgs p = a;
+  const int64_t m0 = static_cast<int64_t>(rb) * BMR;
+  const int64_t rows = static_cast<int64_t>(a.M) - m0;
+  p.M = static_cast<int>(rows < BMR ? rows : BMR);
+  const Epilogue& e = a.epi;
+  const int d_bytes = e.d_type == kOutF32 ? 4 : (e.d_type == kOutBf16 ? 2 : 1);
+  if (e.C != nullptr) p.epi.C = e.C + m0 * e.ldc;
+  p.epi.D = static_cast<uint8_t*>(e.D) + m0 * e.ldd * d_bytes;
+  if (e.R != nullptr) p.epi.R = e.R + m0 * e.ldr;
+  if (a.counters != nullptr) p.counters = a.counters + static_cast<int64_t>(rb) * n_groups;
+  if (a.workspace != nullptr) p.workspace = a.workspace + rb * ws_floats;
+  return p;
+}
+
 template <bool FUSED, int BMR>
 __global__ void __launch_bounds__(kThreads, 1)
-    tc_decode_kernel(const __grid_constant__ DecodeArgs p, const __grid_constant__ CUtensorMap tmA,
+    tc_decode_kernel(const __grid_constant__ DecodeArgs pa, const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB) {
   using Cfg = DecCfg<BMR>;
   constexpr int BMr = BMR;
@@ -306,7 +327,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const Split sp = make_split(p.N, p.K, gridDim.x);
+  const Split sp = make_split(pa.N, pa.K, gridDim.x);
+  // This CTA's row block (blockIdx.y; one unless M exceeds the instance's rows).
+  const int row0 = static_cast<int>(blockIdx.y) * BMr;
+  const DecodeArgs p = row_block<BMR>(pa, static_cast<int>(blockIdx.y), (pa.N + NW - 1) / NW,
+                                      static_cast<int64_t>(gridDim.x) * sp.segs_max *
+                                          kPartialFloats);
   const int64_t u_begin = run_start(sp, blockIdx.x);
   const int64_t u_end = run_start(sp, static_cast<int64_t>(blockIdx.x) + 1);
 
@@ -374,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(sb + b * kBoxBytesB, &tmB, ng * NW + b * 64, kb * BK, &tail->full[s]);
 #pragma unroll
         for (int a = 0; a < kABoxes; ++a)
-          tma_load_2d(sa + a * (BMr * 64 * 2), &tmA, kb * BK + a * 64, 0, &tail->full[s]);
+          tma_load_2d(sa + a * (BMr * 64 * 2), &tmA, kb * BK + a * 64, row0, &tail->full[s]);
       }
       // This CTA has issued all its loads: the next kernel in the stream may
       // start launching (it waits for this grid's completion before use).
@@ -765,7 +791,7 @@ cudaError_t launch_rows(const DecodeArgs& a, const CUtensorMap* tmA, const CUten
   // Programmatic stream serialization: this launch may begin while the
   // previous kernel in the stream drains (see grid_dependency_wait).
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(num_ctas);
+  cfg.gridDim = dim3(num_ctas, decode_row_blocks(a.M));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
@@ -793,18 +819,24 @@ int decode_b_box_rows() { return BK; }
 
 int decode_rows(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : 64; }
 
+int decode_row_blocks(int M) { return M <= kDecBlockRows ? 1 : (M + kDecBlockRows - 1) / kDecBlockRows; }
+
+int64_t decode_groups(int N) { return (N + NW - 1) / NW; }
+
 int decode_cluster(int M, int N, int K, int num_sms) {
   const int64_t groups = (N + NW - 1) / NW;
   const int64_t kb_total = (K + BK - 1) / BK;
-  const int64_t slots = num_sms;
+  const int blocks = decode_row_blocks(M);
+  const int64_t slots = num_sms / blocks;  // SMs per row block
   if (groups * 5 >= slots * 3) return 1;  // whole groups, or runs of them
   // The largest power of two S <= 8 (portable cluster size) with at least
-  // one k-block per CTA and all groups' clusters resident at once (more would
-  // run in two waves: 16 clusters of 8 took twice as long as 8).
+  // one k-block per CTA and all groups' clusters (of every row block)
+  // resident at once (more would run in two waves: 16 clusters of 8 took
+  // twice as long as 8).
   const int rows = decode_rows(M);
   int S = 1;
   while (S < 8 && groups * S * 2 <= slots && S * 2 <= kb_total &&
-         groups <= decode_max_clusters(S * 2, rows))
+         groups * blocks <= decode_max_clusters(S * 2, rows))
     S *= 2;
   return S;
 }
@@ -812,7 +844,7 @@ int decode_cluster(int M, int N, int K, int num_sms) {
 int decode_grid(int M, int N, int K, int num_sms) {
   const int64_t groups = (N + NW - 1) / NW;
   const int64_t units = groups * ((K + BK - 1) / BK);
-  const int64_t slots = num_sms;
+  const int64_t slots = num_sms / decode_row_blocks(M);  // SMs per row block
   // Enough column groups to keep most SMs streaming (>= ~60 % of them): one
   // CTA per group, so no group's k range is split and no partial sums are
   // exchanged.  Fewer groups: clusters of S CTAs per group split its k range
@@ -829,10 +861,10 @@ int decode_grid(int M, int N, int K, int num_sms) {
 
 int64_t decode_workspace_floats(int M, int N, int K, int num_ctas) {
   const Split s = make_split(N, K, num_ctas);
-  return static_cast<int64_t>(num_ctas) * s.segs_max * decode_rows(M) * NW;
+  return static_cast<int64_t>(num_ctas) * s.segs_max * decode_rows(M) * NW * decode_row_blocks(M);
 }
 
-int64_t decode_counter_count(int N) { return (N + NW - 1) / NW; }
+int64_t decode_counter_count(int M, int N) { return decode_groups(N) * decode_row_blocks(M); }
 
 cudaError_t launch_tc_decode(const DecodeArgs& a, const CUtensorMap* tmA, const CUtensorMap* tmB,
                              int num_ctas, cudaStream_t stream) {

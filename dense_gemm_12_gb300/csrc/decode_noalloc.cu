@@ -103,7 +103,7 @@ extern "C" gemm_status_t gemm_bf16gemm_decode_static(int64_t M, int64_t N, int64
   const int n = static_cast<int>(N), k = static_cast<int>(K);
   const int m = static_cast<int>(M);
   const int grid = decode_grid(m, n, k, num_sms);
-  const int64_t counters = decode_counter_count(n);
+  const int64_t counters = decode_counter_count(m, n);
   const int64_t partials = decode_workspace_floats(m, n, k, grid);
   if (counters > kStaticCounters || partials > kStaticPartialFloats) return GEMM_ERR_UNSUPPORTED;
 
@@ -127,7 +127,7 @@ extern "C" gemm_status_t gemm_bf16gemm_decode_static(int64_t M, int64_t N, int64
   // nothing is cleared (a memset between two launches would also keep this
   // launch from overlapping the previous kernel's last CTAs).  Only when the
   // column groups outnumber the SMs do runs of groups meet in the array.
-  if (grid == counters || a.cluster > 1) {
+  if (grid == decode_groups(n) || a.cluster > 1) {
     a.counters = nullptr;
     a.workspace = nullptr;
   } else {

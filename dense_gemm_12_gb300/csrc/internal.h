@@ -155,7 +155,8 @@ struct DecodeArgs {
   int M, N, K;
   Epilogue epi;
   float* workspace;     // partial sums, see decode_workspace_floats
-  uint32_t* counters;   // one arrival counter per 128-column n-tile, zeroed
+  uint32_t* counters;   // one arrival counter per 128-column n-tile and row
+                        // block, zeroed
   uint32_t* err;
   int cluster;          // > 1: clusters of this many CTAs split each column
                         // group's k range (decode_cluster); 0 or 1: none
@@ -163,19 +164,26 @@ struct DecodeArgs {
 
 // bf16 decode GEMM (M <= kDecMaxM): tcgen05 with the operands swapped
 // (D^T = B^T A^T, MMA M = 128 over N, MMA N = 16, 32 or 64 over M), split
-// over K.
+// over K.  M > 64 runs in row blocks of 64 (the launch's y dimension), each
+// streaming B for its own rows at the same time as the others.  num_ctas:
+// CTAs per row block (decode_grid).
 cudaError_t launch_tc_decode(const DecodeArgs& a, const CUtensorMap* tmA,
                              const CUtensorMap* tmB, int num_ctas, cudaStream_t stream);
 constexpr int kDecBN = 128, kDecBM = 16;
-// Largest M the decode kernel takes (instances for 16, 32 and 64 rows: the
-// MMA's N); larger M runs on the tile kernels.
-constexpr int kDecMaxM = 64;
+// Rows of the largest kernel instance (the MMA's N) and so of a row block.
+constexpr int kDecBlockRows = 64;
+// Largest M the decode kernel takes (two row blocks); larger M runs on the
+// tile kernels.
+constexpr int kDecMaxM = 128;
 // Whether automatic dispatch runs a bf16 M x N x K GEMM on the decode kernel:
-// every M <= 32, and 32 < M <= 64 up to N = 16384.  Measured against the tile
-// kernels (back-to-back launches, us): M = 17, 32, 48, 64 at 4096 x 4096:
-// 10.3, 10.2, 11.9, 11.9 against 27.0-28.7; M = 64 at 8192 x 8192 27.8 vs
-// 49.8, at 12288 x 4096 24.6 vs 43.3; but at N = 28672 (more column groups
-// than SMs) 52.8 vs 51.1 on the tile kernel.
+// every M <= 32, and 32 < M <= 128 up to N = 16384 (two row blocks above 64
+// rows).  Measured against the tile kernels (back-to-back launches, us):
+// M = 17, 32, 48, 64 at 4096 x 4096: 10.3, 10.2, 11.9, 11.9 against
+// 27.0-28.7; M = 64 at 8192 x 8192 27.8 vs 49.8, at 12288 x 4096 24.6 vs
+// 43.3; M = 72-128 at N = 1024, 4096, 8192, 12288, 16384 (K = 4096): 8.7,
+// 13.8, 20.9, 35.0, 41.9 against 27.9, 27.4, 36.1, 43.6, 45.6 on the
+// single-CTA tile kernel (K = 8192 at N = 16384: 65.6 vs 65.8); but M = 64
+// at N = 28672 (more column groups than SMs) 52.8 vs 51.1 on the tile kernel.
 inline bool decode_path(int64_t M, int64_t N, int64_t K) {
   (void)K;
   if (M > kDecMaxM) return false;
@@ -183,11 +191,17 @@ inline bool decode_path(int64_t M, int64_t N, int64_t K) {
 }
 // Rows of the kernel instance a launch with M rows uses (16, 32 or 64).
 int decode_rows(int M);
+// Row blocks of a decode launch with M rows (1, or 2 for M > 64).
+int decode_row_blocks(int M);
+// 128-column groups of C (one arrival counter each, per row block).
+int64_t decode_groups(int N);
 // k-rows of B per TMA box of the decode kernel (the A box is always 64 wide).
 int decode_b_box_rows();
-// Workspace floats and counters a decode launch of this shape needs.
+// Workspace floats and counters a decode launch of this shape needs (all row
+// blocks together).
 int64_t decode_workspace_floats(int M, int N, int K, int num_ctas);
-int64_t decode_counter_count(int N);
+int64_t decode_counter_count(int M, int N);
+// CTAs per row block.
 int decode_grid(int M, int N, int K, int num_sms);
 // CTAs per cluster of the decode launch (1: no clusters): when the column
 // groups are few, the CTAs of a cluster split one group's k range and add

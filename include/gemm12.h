@@ -132,8 +132,9 @@ gemm_status_t gemm_sgemm(int64_t M, int64_t N, int64_t K, float alpha,
  * cores with the accumulator in tensor memory.  Small M takes the
  * bandwidth-bound decode kernel (the "decode GEMV (M <= 16)" case of "Tiled
  * matrix multiplication", "Avoid when", widened here to every M <= 32, and
- * to 32 < M <= 64 up to N = 16384, where it measured faster than the tile
- * kernels; gemm_select_path reports GEMM_PATH_TC_DECODE), which splits K across CTAs
+ * to 32 < M <= 128 up to N = 16384 -- above 64 rows as two row blocks --
+ * where it measured faster than the tile kernels; gemm_select_path reports
+ * GEMM_PATH_TC_DECODE), which splits K across CTAs
  * ("Split-K" in the same page's "Variants and alternatives") and reduces the
  * partial sums in a fixed order, so results are deterministic.  Error bound:
  * 8e-3 of |alpha|*(|A||B|)_ij + |beta|*|C_ij| against the exact product of the

@@ -77,13 +77,16 @@ P = 1 << 20
     (dict(bf16=0, M=64, N=64, K=64, A=P + 4), "simt_generic"),     # A not 16-B aligned
     (dict(bf16=0, M=64, N=64, K=64, ldb=66), "simt_generic"),      # B pitch 264 B
     (dict(bf16=1, M=8192, N=8192, K=8192), "tc_bf16_pair"),
-    (dict(bf16=1, M=128, N=8192, K=8192), "tc_bf16"),
+    (dict(bf16=1, M=128, N=8192, K=8192), "tc_decode"),          # two row blocks of 64
+    (dict(bf16=1, M=128, N=16392, K=8192), "tc_bf16"),
     (dict(bf16=1, M=129, N=8192, K=8192), "tc_bf16_pair"),
     (dict(bf16=1, M=16, N=12288, K=4096), "tc_decode"),
     (dict(bf16=1, M=1, N=12288, K=4096), "tc_decode"),
     (dict(bf16=1, M=17, N=12288, K=4096), "tc_decode"),
     (dict(bf16=1, M=64, N=4096, K=4096), "tc_decode"),
-    (dict(bf16=1, M=65, N=4096, K=4096), "tc_bf16"),
+    (dict(bf16=1, M=65, N=4096, K=4096), "tc_decode"),
+    (dict(bf16=1, M=65, N=16384, K=4096), "tc_decode"),
+    (dict(bf16=1, M=65, N=16512, K=4096), "tc_bf16"),
     (dict(bf16=1, M=32, N=28672, K=4096), "tc_decode"),
     (dict(bf16=1, M=33, N=16384, K=8192), "tc_decode"),
     (dict(bf16=1, M=33, N=16392, K=4096), "tc_bf16"),            # wide N: tile kernels

@@ -27,16 +27,19 @@ def _inputs(M, N, K, seed, dist=("normal", 1.0), dist_c=("uniform", None)):
 
 
 def test_single_tile_integers_exact():
-    # one 128 x 256 tile, one k-block: exercises the descriptors directly
+    # one 128 x 256 tile, one k-block, on the single-CTA tile kernel (pinned:
+    # automatic dispatch sends this shape to the decode kernel): exercises the
+    # descriptors directly
     M, N, K = 128, 256, 64
     A, B, C = make_inputs(M, N, K, ("int", None), ("int", None), ("int", None), seed=1,
                           dtype="bf16")
-    out, st, _, _, dC = run_bf16gemm(A, B, C, 1.0, 0.0)
+    dA, dB, dC = A.cuda(), B.cuda(), torch.full((M, N), float("nan"), device="cuda")
+    st = g.gemm_bf16gemm_config(M, N, K, 1.0, dA.data_ptr(), K, dB.data_ptr(), N, 0.0,
+                                dC.data_ptr(), N, {"kernel": "single_cta"}, 0)
+    torch.cuda.synchronize()
     assert st == 0
-    assert g.gemm_select_path(1, M, N, K, 1.0, 1 << 20, K, 1 << 20, N) == "tc_bf16"
     ref32, _, _ = oracle_bf16(A, B, C, 1.0, 0.0)
-    assert np.array_equal(out.numpy(), ref32)
-    assert dC.untouched_outside()
+    assert np.array_equal(dC.cpu().numpy(), ref32)
     check_device_error()
 
 
@@ -58,10 +61,11 @@ def test_ragged_tensor_core(M, N, K):
     A, B, C = _inputs(M, N, K, seed=M + N + K)
     out, st, _, _, dC = run_bf16gemm(A, B, C, 0.7, 0.3)
     assert st == 0
-    # M <= 64 runs the decode kernel (small M is bound by streaming B); the
-    # tile kernels at small M are covered with pinned configurations in
-    # test_gpu_config.py
-    expect = "tc_decode" if M <= 64 else "tc_bf16" if M <= 128 else "tc_bf16_pair"
+    # small M runs the decode kernel (bound by streaming B): M <= 32, and
+    # M <= 128 (two row blocks above 64) up to N = 16384; the tile kernels at
+    # small M are covered with pinned configurations in test_gpu_config.py
+    decode = M <= 32 or (M <= 128 and N <= 16384)
+    expect = "tc_decode" if decode else "tc_bf16" if M <= 128 else "tc_bf16_pair"
     assert g.gemm_select_path(1, M, N, K, 0.7, 1 << 20, K, 1 << 20, N) == expect
     _, ref64, den = oracle_bf16(A, B, C, 0.7, 0.3)
     r = ratio(out, ref64, den)
@@ -131,7 +135,7 @@ def test_full_8192_sampled_rows():
 
 @pytest.mark.parametrize("M,N,K", [
     (512, 10240, 4096),   # pair kernel: 80 pair tiles on at most 76 clusters
-    (128, 2048, 4096),    # single-CTA kernel: 8 tiles on 152 SMs
+    (128, 16640, 4096),   # single-CTA kernel: 65 tiles on 152 SMs
 ])
 def test_split_integers_exact(M, N, K):
     # |partial sums| <= 16 K < 2^24: exact in fp32 in any order and any split
@@ -149,7 +153,7 @@ def test_split_integers_exact(M, N, K):
 @pytest.mark.parametrize("M,N,K", [
     (512, 10240, 4096),   # pair kernel
     (500, 10232, 4000),   # pair kernel, ragged M, N and K (last part ends on a partial k-block)
-    (100, 1024, 4096),    # single-CTA kernel
+    (100, 16640, 4096),   # single-CTA kernel
 ])
 def test_split_matches_oracle_and_repeats(M, N, K):
     assert g.gemm_split_parts(1, M, N, K) > 1

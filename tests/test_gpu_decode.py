@@ -1,5 +1,6 @@
-"""Decode-shaped bf16 GEMM (M <= 16) on the GPU: the swapped-operand tcgen05
-kernel with split-K and the fixed-order fix-up, against the CPU oracle.
+"""Decode-shaped bf16 GEMM (small M, up to 128 rows in two row blocks) on the
+GPU: the swapped-operand tcgen05 kernel with split-K and the fixed-order
+fix-up, against the CPU oracle.
 
 Bound: 8e-3 of |alpha| (|A||B|)_ij + |beta||C_ij| (same bf16-rounded inputs);
 bit-exact on small integers; bitwise identical across repeated launches (the
@@ -82,6 +83,40 @@ def test_decode_cluster_split_integers_exact(M, N, K):
 ])
 def test_decode_wide_rows_integers_exact(M, N, K):
     _cluster_exact(M, N, K)
+
+
+# 64 < M <= 128: two row blocks of 64 rows (the launch's y dimension), each
+# streaming B for its own rows; the second sees rows 64.. of A, C and D.
+@pytest.mark.parametrize("M,N,K", [
+    (65, 4096, 1024),    # one row in the second block; clusters of 2
+    (96, 1024, 4096),    # 8 column groups x 2 row blocks: clusters of 4
+    (128, 8192, 2048),   # 64 groups x 2 row blocks = 128 CTAs: whole groups
+    (100, 1000, 296),    # ragged N and K
+    (128, 200, 8192),    # 2 groups, the last one mostly past N
+])
+def test_decode_two_row_blocks_integers_exact(M, N, K):
+    assert g.gemm_select_path(1, M, N, K, 1.0, 1 << 20, K, 1 << 20, N) == "tc_decode"
+    _cluster_exact(M, N, K)
+
+
+@pytest.mark.parametrize("M,N,K", [(72, 4096, 4096), (128, 8192, 1024),
+                                   (96, 16384, 1024)])   # more groups than SMs per block
+def test_decode_two_row_blocks_random_within_bound(M, N, K):
+    A, B, C = make_inputs(M, N, K, ("normal", 1.0), ("normal", 0.02), ("uniform", None),
+                          seed=M + N, dtype="bf16")
+    out, st, _, _, dC = run_bf16gemm(A, B, C, 0.5, 1.0, ldc=N + 5)
+    assert st == 0
+    _, ref64, den = oracle_bf16(A, B, C, 0.5, 1.0)
+    assert ratio(out, ref64, den) <= TOL_BF16
+    assert dC.untouched_outside()
+    check_device_error()
+
+
+def test_decode_beyond_two_row_blocks_takes_tile_kernels():
+    assert g.gemm_select_path(1, 129, 4096, 4096, 1.0, 1 << 20, 4096, 1 << 20, 4096) == \
+        "tc_bf16_pair"
+    assert g.gemm_select_path(1, 100, 16392, 4096, 1.0, 1 << 20, 4096, 1 << 20, 16392) == \
+        "tc_bf16"
 
 
 def _cluster_exact(M, N, K):

@@ -78,7 +78,7 @@ def test_decode_kernel_epilogues(act, out):
 
 
 @pytest.mark.parametrize("M,N,K,act,out", [
-    (100, 1024, 4096, "gelu", "bf16"),   # single-CTA kernel, tiles split along k
+    (100, 16640, 4096, "gelu", "bf16"),  # single-CTA kernel, tiles split along k
     (512, 10240, 4096, "relu", "f32"),   # pair kernel, last round split along k
 ])
 def test_split_tiles_epilogue(M, N, K, act, out):

@@ -112,9 +112,10 @@ INT_SHAPES = [
     (8, 1000, 512),       # decode kernel (M <= 16), clusters of 4
     (40, 1000, 512),      # decode kernel, 64-row instance
     (24, 16384, 256),     # decode kernel, 32-row instance, whole column groups
-    (100, 520, 256),      # single-CTA kernel, ragged N
+    (100, 520, 256),      # decode kernel, two row blocks of 64
+    (100, 16392, 256),    # single-CTA kernel, ragged N
     (384, 512, 256),      # CTA-pair kernel, odd number of tile rows
-    (100, 1024, 4096),    # single-CTA kernel, tiles split along k
+    (100, 16640, 4096),   # single-CTA kernel, tiles split along k
 ]
 
 
@@ -148,7 +149,8 @@ def test_empty_product_integers_exact(M, N, K):
 @pytest.mark.parametrize("M,N,K", [
     (16, 12288, 1024),    # decode kernel
     (64, 4096, 2048),     # decode kernel, 64-row instance, clusters of 4
-    (128, 2048, 512),     # single-CTA kernel
+    (128, 16640, 512),    # single-CTA kernel
+    (120, 2048, 512),     # decode kernel, two row blocks
     (640, 1280, 1000),    # CTA-pair kernel, ragged K
     (512, 10240, 4096),   # CTA-pair kernel, last round split along k
 ])

@@ -121,7 +121,8 @@ def _fused_relu(M, N, K, lda, ldb, seed):
 @pytest.mark.parametrize("M,N,K,lda,ldb", [
     (16, 63, 64, 64, 63),        # decode kernel on the staged B
     (8, 1000, 777, 777, 1000),   # decode, A pitch 1554 B
-    (40, 300, 130, 131, 300),    # single-CTA tile kernel, small
+    (40, 300, 130, 131, 300),    # decode kernel, 64-row instance, small
+    (100, 300, 130, 131, 300),   # decode kernel, two row blocks
     (300, 520, 270, 270, 521),   # CTA pairs
 ])
 def test_fused_output_stage_on_staged_operands(M, N, K, lda, ldb):
