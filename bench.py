@@ -57,8 +57,10 @@ def parse_args():
     p.add_argument("--no-parts", action="store_true", help="headline workload only")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--brief-parts", action="store_true",
+                   help="profiler runs: one short trial per part (not bench values)")
     p.add_argument("--only", choices=["sgemm", "sgemm4096", "sgemm256", "ragged", "bf16",
-                                      "decode"],
+                                      "decode", "decode_graph"],
                    default=None,
                    help="time one kernel's workload alone (profiling runs); prints its part")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -264,6 +266,12 @@ def time_window(torch, step, reps, stream_obj, first=0):
     return a.elapsed_time(b)
 
 
+# --brief-parts (profiler runs only: a launch list of the whole command):
+# one short trial per part instead of the protocol's; its numbers are not
+# bench values.
+BRIEF = {"on": False}
+
+
 def measure_part(torch, step, stream_obj, gpu_index, units_per_call=1, warmup=3,
                  min_trial_ms=MIN_TRIAL_MS, trials=TRIALS):
     """The timing protocol of every part: `warmup` untimed calls, then
@@ -272,6 +280,8 @@ def measure_part(torch, step, stream_obj, gpu_index, units_per_call=1, warmup=3,
     trials.  A call may run several launches (`units_per_call`, e.g. a CUDA
     graph); times are reported per launch.  Returns the per-launch median,
     the spread over trials, R and the clock record."""
+    if BRIEF["on"]:
+        min_trial_ms, trials = 1.0, 1
     for i in range(warmup):
         step(i)
     torch.cuda.synchronize()
@@ -746,14 +756,33 @@ def run_only(args):
         def step(i):
             g.gemm_bf16gemm(w.M, w.N, w.K, w.alpha, A.data_ptr(), w.K, B.data_ptr(), w.N,
                             w.beta, C.data_ptr(), w.N, s)
-    elif args.only == "decode":
+    elif args.only in ("decode", "decode_graph"):
         w = wl.WORKLOADS["decode_16"]
         A, B, C = (t.to(device) for t in wl.workload_inputs(w))
         Bs = [B, B.clone(), B.clone()]
 
-        def step(i):
+        def launch(i, stream):
             g.gemm_bf16gemm(w.M, w.N, w.K, w.alpha, A.data_ptr(), w.K, Bs[i % 3].data_ptr(),
-                            w.N, w.beta, C.data_ptr(), w.N, s)
+                            w.N, w.beta, C.data_ptr(), w.N, stream)
+        step = lambda i: launch(i, s)
+        if args.only == "decode_graph":
+            # `steps` launches captured once and replayed as one graph per step
+            for i in range(3):
+                step(i)
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            cap = torch.cuda.Stream()
+            with torch.cuda.stream(cap):
+                graph.capture_begin()
+                for i in range(args.steps):
+                    launch(i, cap.cuda_stream)
+                graph.capture_end()
+            torch.cuda.synchronize()
+            stream_obj = cap
+
+            def step(i):
+                with torch.cuda.stream(cap):   # replay() launches on the current stream
+                    graph.replay()
     else:
         name = {"sgemm": "sgemm_4092", "sgemm4096": "sgemm_4096", "sgemm256": "sgemm_256",
                 "ragged": "sgemm_ragged"}[args.only]
@@ -764,6 +793,8 @@ def run_only(args):
     for i in range(args.warmup):
         step(i)
     ms = time_launches(torch, step, args.steps, stream_obj)
+    if args.only == "decode_graph":     # each step replayed a graph of `steps` launches
+        ms = [x / args.steps for x in ms]
     st = g.gemm_check_device_error(s)
     if st != 0:
         raise RuntimeError("device error: " + g.gemm_status_string(st))
@@ -774,6 +805,7 @@ def run_only(args):
 
 def main():
     args = parse_args()
+    BRIEF["on"] = args.brief_parts
     if args.only:
         run_only(args)
         return
