@@ -1,4 +1,4 @@
-// bf16_decode.cu -- decode-shaped GEMM (small M, up to 64): C = alpha * A * B +
+// bf16_decode.cu -- decode-shaped GEMM (small M, up to 128): C = alpha * A * B +
 // beta * C with bf16 A (M x K) and B (K x N), fp32 accumulation and fp32 C.
 //
 // "Tiled matrix multiplication" ("Avoid when") notes that a decode GEMV with
@@ -11,7 +11,9 @@
 // the product is computed transposed, D^T = B^T A^T: the MMA's M runs over
 // 128 columns of C and its N over the rows of A: the kernel has instances
 // for N = 16, 32 and 64 (a launch with M rows takes the smallest that holds
-// them), and no row of the MMA's M is padding.
+// them), and no row of the MMA's M is padding.  M > 64 runs as row blocks of
+// 64 rows (the grid's y dimension, see row_block), each streaming B for its
+// own rows at the same time.
 //
 // Work split.  B is cut into n-groups of 128 columns; a unit is one n-group x
 // 128 values of k (32 KB of B, fetched as two 64 x 128 TMA boxes).  With at
