@@ -4,8 +4,9 @@ The header allows calls from several host threads on different streams; the
 split-K paths then need each stream's own scratch (partial sums, arrival
 counters), created and grown on first use under a lock.  Each thread runs
 GEMMs whose work is split along k -- the CUDA-core kernel with a pinned
-split, the CTA-pair kernel's split tail, the decode kernel's runs of column
-groups combined through scratch, and its cluster split, which needs none --
+split, the CTA-pair kernel's split tail and a pinned stream-K tail, the
+decode kernel's runs of column groups combined through scratch (one row
+block, and two), and its cluster split, which needs none --
 in a different order and with scratch growing at different times, and
 every result must equal, bit for bit, the same call run alone beforehand
 (fixed plans sum their parts in a fixed order, so results are reproducible).
@@ -80,6 +81,27 @@ def _cases():
                              1.0, out.data_ptr(), 4096, stream.cuda_stream)
         assert st == 0
     cases.append(("decode_cluster", decode_cluster, (40, 4096)))
+    # bf16 CTA-pair kernel with a pinned stream-K tail: partial sums of every
+    # worker's segments in the stream's scratch
+    def pair_stream_k(stream, out):
+        out.copy_(C20)
+        st = g.gemm_bf16gemm_config(512, 10240, 4096, 1.0, dA2.data_ptr(), 4096, dB2.data_ptr(),
+                                    10240, 0.5, out.data_ptr(), 10240,
+                                    {"kernel": "cta_pair", "split": -1}, stream.cuda_stream)
+        assert st == 0
+    cases.append(("bf16_pair_stream_k", pair_stream_k, (512, 10240)))
+    # decode kernel, two row blocks of 64 with more column groups than SMs per
+    # block: each block's runs of groups meet in its own part of the scratch
+    A5, B5, C5 = make_inputs(100, 16384, 1024, ("normal", 1.0), ("normal", 0.05),
+                             ("uniform", None), seed=45, dtype="bf16")
+    dA5, dB5, C50 = A5.cuda(), B5.cuda(), C5.cuda()
+
+    def decode_rows(stream, out):
+        out.copy_(C50)
+        st = g.gemm_bf16gemm(100, 16384, 1024, 1.0, dA5.data_ptr(), 1024, dB5.data_ptr(), 16384,
+                             1.0, out.data_ptr(), 16384, stream.cuda_stream)
+        assert st == 0
+    cases.append(("decode_two_row_blocks", decode_rows, (100, 16384)))
     return cases
 
 
