@@ -47,7 +47,21 @@ def ceil_log2(x: int) -> int:
     return b
 
 
-def candidates(is_bf16: bool, M: int, K: int):
+def bf16_stream_k_runs(kernel: str, M: int, N: int, K: int, num_sms: int) -> bool:
+    """Whether a pinned stream-K tail really runs for this bf16 shape: the
+    tail items' k-blocks must be at least the workers (CTAs, or about half as
+    many CTA pairs); otherwise the library runs the equal split instead, the
+    same launch as another candidate."""
+    pair = kernel == "cta_pair"
+    tiles_m, tiles_n = -(-M // 128), -(-N // 256)
+    items = (-(-tiles_m // 2) if pair else tiles_m) * tiles_n
+    workers = num_sms // 2 if pair else num_sms
+    num_kb = -(-K // (128 if pair else 64))
+    tail = items % workers if items >= workers else items
+    return tail > 0 and tail * num_kb >= workers
+
+
+def candidates(is_bf16: bool, M: int, N: int, K: int, num_sms: int = 152):
     """Every pinned configuration worth timing for a shape."""
     kernels = ["single_cta"] if is_bf16 else ["single_cta", "wide"]
     if is_bf16 and M > 128:
@@ -55,8 +69,11 @@ def candidates(is_bf16: bool, M: int, K: int):
     splits = SPLITS + [-1]   # -1: the stream-K tail
     num_kb = -(-K // (64 if is_bf16 else 32))
     for kernel, split, group in itertools.product(kernels, splits, GROUPS):
-        if split <= num_kb:
-            yield {"kernel": kernel, "split": split, "group_m": group}
+        if split > num_kb:
+            continue
+        if split == -1 and is_bf16 and not bf16_stream_k_runs(kernel, M, N, K, num_sms):
+            continue
+        yield {"kernel": kernel, "split": split, "group_m": group}
 
 
 def table_lines(entries, num_sms: int, gpu: str, date: str):
@@ -120,6 +137,7 @@ def _time(torch, g, is_bf16, M, N, K, tensors, cfg, stream, reps):
 
 def sweep_shape(torch, g, is_bf16, M, N, K, stream, reps=5, confirm_reps=20):
     dev = torch.device("cuda", torch.cuda.current_device())
+    num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
     gen = torch.Generator(device=dev).manual_seed(M * 131 + N * 17 + K)
     dt = torch.bfloat16 if is_bf16 else torch.float32
     A = torch.randn(M, K, device=dev, generator=gen).to(dt)
@@ -136,7 +154,7 @@ def sweep_shape(torch, g, is_bf16, M, N, K, stream, reps=5, confirm_reps=20):
     den = (A.float().abs() @ B.float().abs())
     tol = (8e-3 if is_bf16 else 2e-6 * math.sqrt(K)) * den
     timed, rejected = [], []
-    for cfg in candidates(is_bf16, M, K):
+    for cfg in candidates(is_bf16, M, N, K, num_sms):
         _run(torch, g, is_bf16, M, N, K, tensors, cfg, stream)
         torch.cuda.synchronize()
         if not bool(((C - ref).abs() <= tol).all()):

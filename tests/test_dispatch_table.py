@@ -48,15 +48,26 @@ def test_ceil_log2_buckets():
 
 
 def test_candidates_respect_kernel_and_k():
-    c = list(tune.candidates(True, 64, 4096))
+    c = list(tune.candidates(True, 64, 4096, 4096))
     assert {x["kernel"] for x in c} == {"single_cta"}          # M <= 128: no pairs
-    c = list(tune.candidates(True, 1024, 128))                  # 2 k-blocks
+    c = list(tune.candidates(True, 1024, 4096, 128))            # 2 k-blocks
     assert {x["kernel"] for x in c} == {"single_cta", "cta_pair"}
     assert max(x["split"] for x in c) == 2
-    c = list(tune.candidates(False, 4092, 4092))
+    c = list(tune.candidates(False, 4092, 4092, 4092))
     assert {x["kernel"] for x in c} == {"single_cta", "wide"}
     assert -1 in {x["split"] for x in c}                        # stream-K tail
-    assert -1 in {x["split"] for x in tune.candidates(True, 1024, 4096)}
+    c = list(tune.candidates(True, 1024, 4096, 4096))
+    assert {x["kernel"] for x in c if x["split"] == -1} == {"cta_pair", "single_cta"}
+
+
+def test_bf16_stream_k_candidates_only_where_it_runs():
+    # pair kernel on 152 SMs: 76 workers; the tail's k-blocks must reach them
+    assert tune.bf16_stream_k_runs("cta_pair", 1024, 2048, 4096, 152)      # 32 items x 32
+    assert not tune.bf16_stream_k_runs("cta_pair", 256, 256, 256, 152)     # 1 item x 2
+    assert not tune.bf16_stream_k_runs("cta_pair", 4864, 1024, 4096, 152)  # 76 items: no tail
+    assert tune.bf16_stream_k_runs("single_cta", 128, 4096, 4096, 152)     # 16 x 64
+    assert not tune.bf16_stream_k_runs("single_cta", 128, 512, 256, 152)   # 2 x 4
+    assert -1 not in {x["split"] for x in tune.candidates(True, 256, 256, 256)}
 
 
 def _result(M, auto_ms, best_ms, is_bf16=1):
