@@ -88,7 +88,6 @@ constexpr int kSecondIssuerWarp = 6;
 template <int BMR>
 struct DecCfg {
   static_assert(BMR == 16 || BMR == 32 || BMR == 64, "rows of a decode launch");
-  static constexpr int BMr = BMR;
   static constexpr int kChunks = BMR / kChunk;
   static constexpr int kStageBytesA = BMR * BK * 2;                  // 4, 8 or 16 KB
   static constexpr int kStageBytes = kStageBytesB + kStageBytesA;    // multiple of 1024
