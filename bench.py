@@ -96,6 +96,9 @@ def load_peaks():
     else:
         peaks = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
                  "source": "fallback"}
+    # median SM clock sampled under load during those measurements (mostly
+    # the seconds-long loop behind the sustained bf16 figure)
+    peaks["sustained_sm_mhz"] = (d.get("clocks_under_load") or {}).get("sm_mhz_median")
     if d.get("sm_max_mhz"):
         peaks["sm_max_mhz"], peaks["sm_clock_source"] = float(d["sm_max_mhz"]), "MEASURED_PEAKS.json"
     else:
@@ -334,6 +337,18 @@ def _bf16_8192_operands(torch, wl, device):
     return w, A.to(device), B.to(device)
 
 
+def per_clock(tflops, clocks, peaks):
+    """A power-capped bf16 part's rate per GHz of its median SM clock, against
+    the sustained cuBLAS figure per GHz of the clock it was measured at: the
+    comparison without the box-to-box spread of the power-capped clock."""
+    mhz, ref_mhz = (clocks or {}).get("sm_mhz"), peaks.get("sustained_sm_mhz")
+    if not mhz or not ref_mhz:
+        return None
+    ours, ref = tflops / (mhz / 1e3), peaks["bf16_tflops_sustained"] / (ref_mhz / 1e3)
+    return {"tflops_per_ghz": ours, "sm_mhz": mhz, "sustained_tflops_per_ghz": ref,
+            "sustained_sm_mhz": ref_mhz, "ratio": ours / ref}
+
+
 def bench_bf16_8192(torch, g, wl, peaks, device, stream_obj, gpu_index):
     w, A, B = _bf16_8192_operands(torch, wl, device)
     C = torch.empty((w.M, w.N), dtype=torch.float32, device=device)
@@ -361,6 +376,7 @@ def bench_bf16_8192(torch, g, wl, peaks, device, stream_obj, gpu_index):
                      "frac": tflops / sus, "frac_of_burst": tflops / burst,
                      "traffic": recorded_traffic("tc_bf16_pair_kernel"),
                      "peak_note": BF16_PEAK_NOTE % (peaks["source"], sus, burst)},
+        "per_clock": per_clock(tflops, t["clocks"], peaks),
         "sustained": {"value": s_tflops * 1e3, "unit": "GFLOP/s",
                       "seconds": sustained["trial_ms_median"] / 1e3,
                       "launches": sustained["launches_per_trial"],
