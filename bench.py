@@ -732,7 +732,7 @@ def run_ours(args):
                              % (TRIALS, MIN_TRIAL_MS))
 
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:   # N = 1 only
         cpu = cpu_oracle_sample(wl, args.cpu_seconds)
         cpu.pop("seconds", None)
 
