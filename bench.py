@@ -553,6 +553,20 @@ def cpu_oracle_sample(wl, target_seconds):
 
 
 # ------------------------------------------------------------------ main arms
+# The pages' own measurements of this path (other hardware; context, not
+# targets): "A GEMM Kernel, Step by Step" on an RTX A6000 at 4092^3 fp32, and
+# "GEMM Worklog I: Naive to Tiled" ("4. Benchmark Results on NVIDIA A100") at
+# 4096^3 fp32.
+PAGES_CONTEXT = {
+    "note": "figures the pages report on other GPUs; context only, not targets",
+    "rtx_a6000_fp32_4092": {"cublas_gflops": 23249.6, "naive_gflops": 309.0,
+                            "warptiling_gflops": 21779.3},
+    "a100_fp32_4096": {"naive_tflops": 0.26, "naive_frac_of_peak": 0.013,
+                       "tiled_32x32_tflops": 7.12, "tiled_32x32_frac_of_peak": 0.365,
+                       "cublas_tflops": 18.32, "cublas_frac_of_peak": 0.939},
+}
+
+
 def headline_config(world):
     """The `config` of the JSON line, identical in both arms."""
     return {"workload": "fp32 SGEMM M=N=K=4092, alpha=0.7, beta=0.3, A,B,C ~ U[-1,1), row-major",
@@ -751,6 +765,7 @@ def run_ours(args):
                                                          peaks["sm_clock_source"]),
                          "kernel_ms_mean": kernel_ms, "kernel_ms_min": min(launch_ms)},
             "clocks": clocks,
+            "context": PAGES_CONTEXT,
             "e2e": e2e,
             "gpu_launches": args.steps,
             "cpu_baseline": cpu,
