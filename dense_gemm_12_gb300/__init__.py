@@ -25,7 +25,7 @@ __all__ = [
     "gemm_sgemm_config", "gemm_bf16gemm_config", "gemm_get_config", "gemm_get_model_config",
     "GemmConfig", "KERNELS", "SPLIT_STREAM",
     "gemm_status_string", "gemm_check_device_error", "gemm_shutdown", "gemm_release_stream",
-    "gemm_select_path", "gemm_split_parts", "gemm_quantization", "gemm_version", "sgemm", "bf16gemm",
+    "gemm_select_path", "gemm_split_parts", "gemm_split_cluster", "gemm_quantization", "gemm_version", "sgemm", "bf16gemm",
     "STATUS", "PATHS",
 ]
 
@@ -138,6 +138,8 @@ def load_library(build_if_missing: bool = False):
         lib.gemm_quantization.restype = cint
         lib.gemm_split_parts.argtypes = [cint, i64, i64, i64]
         lib.gemm_split_parts.restype = cint
+        lib.gemm_split_cluster.argtypes = [i64, i64, i64, cfg_p]
+        lib.gemm_split_cluster.restype = cint
         lib.gemm_version.argtypes = []
         lib.gemm_version.restype = cint
         _lib = lib
@@ -258,6 +260,13 @@ def gemm_select_path(is_bf16, M, N, K, alpha, A, lda, B, ldb) -> str:
 def gemm_split_parts(is_bf16, M, N, K) -> int:
     """k-ranges per work item of the last round (1 = no split; 0 = no device)."""
     return load_library().gemm_split_parts(int(bool(is_bf16)), M, N, K)
+
+
+def gemm_split_cluster(M, N, K, config=None) -> int:
+    """fp32 with TMA operands: the cluster size S whose CTAs add a tile's k-parts
+    in distributed shared memory, 1 if they meet in global memory or nothing is
+    split, 0 for invalid input or no device.  `config` as for gemm_sgemm_config."""
+    return load_library().gemm_split_cluster(M, N, K, _config(config))
 
 
 def gemm_quantization(M, N, BM, BN, num_sms, ctas_per_sm) -> dict:

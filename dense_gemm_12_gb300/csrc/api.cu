@@ -390,6 +390,7 @@ SimtPlan simt_plan_whole(const SimtPlan& pl, int M, int N, int num_sms) {
   w.grid = tiles < num_sms ? tiles : num_sms;
   w.ws_floats = 0;
   w.counters = 0;
+  w.cluster = 0;
   return w;
 }
 
@@ -401,7 +402,7 @@ gemm_status_t plan_simt(DeviceState* st, cudaStream_t cs, SimtArgs& a, SimtPlan&
                         std::unique_lock<std::mutex>& lock) {
   a.ws = nullptr;
   a.counters = nullptr;
-  if (pl.split != 1 || pl.sk_workers != 0) {
+  if ((pl.split != 1 || pl.sk_workers != 0) && pl.cluster <= 1) {
     if (!lock.owns_lock()) lock.lock();
     Scratch* sc = nullptr;
     const gemm_status_t s = ensure_scratch(*st, cs, pl.ws_floats, pl.counters, &sc);
@@ -418,6 +419,7 @@ gemm_status_t plan_simt(DeviceState* st, cudaStream_t cs, SimtArgs& a, SimtPlan&
   a.split = pl.split;
   a.sk_workers = pl.sk_workers;
   a.group_m = pl.group_m;
+  a.cluster = pl.cluster;
   return GEMM_OK;
 }
 
@@ -623,6 +625,20 @@ int gemm_split_parts(int is_bf16, int64_t M, int64_t N, int64_t K) {
   return simt_plan_max_parts(simt_plan(m, n, k, st->num_sms, &tc, true), m, n, k);
 }
 
+int gemm_split_cluster(int64_t M, int64_t N, int64_t K, const gemm_config_t* cfg) {
+  if (M < 0 || N < 0 || K < 0 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX ||
+      !config_fields_valid(cfg, false))
+    return 0;
+  gemm_status_t s;
+  DeviceState* st = device_state(&s);
+  if (st == nullptr) return 0;
+  if (M == 0 || N == 0 || K == 0) return 1;
+  const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
+  const TileConfig tc = resolve_config(false, M, N, K, st->num_sms, cfg, nullptr);
+  SimtPlan pl = simt_plan(m, n, k, st->num_sms, &tc, true);
+  return simt_use_cluster(pl, m, n) ? pl.cluster : 1;
+}
+
 gemm_status_t gemm_quantization(int64_t M, int64_t N, int64_t BM, int64_t BN, int64_t num_sms,
                                 int64_t ctas_per_sm, gemm_quantization_t* out) {
   if (out == nullptr || M < 0 || N < 0 || BM <= 0 || BN <= 0 || num_sms <= 0 || ctas_per_sm <= 0)
@@ -720,6 +736,9 @@ static gemm_status_t sgemm_impl(int64_t M, int64_t N, int64_t K, float alpha, co
         mb = kLoadTma;
     }
   }
+  // Tiles that all fit in one round add their k-parts through distributed
+  // shared memory.
+  if (ma == kLoadTma && mb == kLoadTma) simt_use_cluster(pl, a.M, a.N);
   s = plan_simt(st, cs, a, pl, lock);
   if (s != GEMM_OK) return s;
   return from_cuda(launch_simt(a, pl, ma, mb, ma == kLoadTma ? &tmA : nullptr,

@@ -41,6 +41,10 @@ struct SimtArgs {
   float* ws;
   uint32_t* counters;
   int group_m;     // raster group height in tile rows
+  // > 1: every tile runs in this one round, cut into `cluster` (= split)
+  // parts that form a thread-block cluster and add their partial sums
+  // through distributed shared memory: no workspace, no counters.
+  int cluster;
 };
 
 // A launch configuration of the tile kernels: gemm_config_t of the C ABI
@@ -65,8 +69,16 @@ struct SimtPlan {
   int group_m;
   int64_t ws_floats;   // workspace the split tiles need
   int64_t counters;    // counters the split tiles need
+  int cluster;         // > 1: the parts of each tile form a cluster (see SimtArgs)
 };
 SimtPlan simt_plan(int M, int N, int K, int num_sms, const TileConfig* fixed, bool allow_wide);
+// Largest cluster of k-parts (the portable cluster size).
+constexpr int kSimtMaxCluster = 8;
+// Turns a plan whose tiles all run in one round, each cut into 2..8 equal
+// k-parts, into its cluster form (pl.cluster = pl.split, no workspace) when
+// every tile's cluster can be resident at once on the current device.  For
+// 128-wide tiles with both operands on TMA only; returns whether it did.
+bool simt_use_cluster(SimtPlan& pl, int M, int N);
 // Largest number of parts any tail tile of the plan is cut into (1 = none).
 int simt_plan_max_parts(const SimtPlan& pl, int M, int N, int K);
 

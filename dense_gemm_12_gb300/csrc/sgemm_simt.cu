@@ -26,12 +26,16 @@
 //   * the tiles of the last, partial round are cut along k -- into equal
 //     parts, or (stream-K) by dealing their k-blocks out evenly to all CTAs --
 //     so that the last round keeps every SM busy ("A GEMM Kernel, Step by
-//     Step", "The fringe and the last wave" and "What is left").
+//     Step", "The fringe and the last wave" and "What is left");
+//   * when every tile fits in one round, the k-parts of a tile can instead
+//     form a thread-block cluster and add their partial sums through
+//     distributed shared memory, with no round trip through global memory.
 // Operands TMA cannot describe (unaligned base or pitch, or bf16 to be widened)
 // are loaded by four producer warps with cp.async / plain loads into the same
 // shared-memory layout, so the compute warps are identical in every variant.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "internal.h"
@@ -67,6 +71,8 @@ struct Geom {
 struct __align__(8) SimtSmemTail {
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
+  uint64_t ready;   // cluster fix-up: every CTA's partial sums are stored
+  uint64_t done;    // cluster fix-up: every CTA has read this one's
   int abort_flag;
   int last_flag;
 };
@@ -443,10 +449,172 @@ __device__ __forceinline__ void epilogue(const SimtArgs& p, const float (&acc)[8
   }
 }
 
-template <int MODE_A, int MODE_B, int BN>
+// ------------------------------------------------- cluster fix-up (split)
+// The cluster handshake.  Every thread arrives once on the cluster barrier
+// right after the mbarriers are initialised (non-blocking), so the idle
+// producer threads can exit at once, as in the unclustered kernel -- idle
+// warps left resident through the k loop, even asleep, measured 4-5 % slower
+// k loops.  The compute warps wait on that one phase before their first
+// access to another CTA; the later steps use the `ready` and `done`
+// mbarriers, arrived on from every CTA of the cluster (release at cluster
+// scope) and waited on with a bound.
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Bounded wait with acquire at cluster scope; as mbar_wait when `abort_flag`
+// is given, else with the limit alone and no record.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity,
+                                                  volatile int* abort_flag, uint32_t* err_word,
+                                                  uint64_t limit_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait_cluster(bar, parity)) {
+    if (abort_flag != nullptr && *abort_flag) return false;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      if (abort_flag != nullptr) {
+        *abort_flag = 1;
+        atomicOr(err_word, kErrWaitTimeout);
+      }
+      return false;
+    }
+  }
+  return true;
+}
+
+// Arrive on mbarrier `bar` (same offset) in every CTA of the cluster: thread
+// r < S of the calling threads arrives on CTA r's, all in one instruction.
+// Called after a barrier of the compute threads, so each arrival (a release
+// at cluster scope) also covers the other threads' earlier accesses.
+__device__ __forceinline__ void mbar_arrive_all(uint64_t* bar, int S, int ctid) {
+  if (ctid < S) mbar_arrive_cluster(mapa_shared(smem_u32(bar), static_cast<uint32_t>(ctid)));
+}
+
+// 128-bit load from the shared memory of a CTA of the cluster (address from
+// mapa_shared).  Ordered against the partial sums' stores by the cluster
+// barriers around the reduction.
+__device__ __forceinline__ float4 ld_shared_cluster_v4(uint32_t cluster_addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(cluster_addr));
+  return v;
+}
+
+// Float4 groups of the 128 x 128 tile one compute thread reduces in a
+// cluster of S >= 2 CTAs: at most 4096 / (2 * 256).
+constexpr int kClusterMaxGroups = (BM * 128 / 4) / (2 * kComputeThreads);
+
+// The partial sums of the cluster's S k-parts of one 128 x 128 tile lie in
+// each CTA's shared memory as a row-major tile (`part_u32`: its shared
+// address, the same in every CTA).  CTA `rank` takes an S-th of the tile's
+// float4 groups (group g of this thread: cluster_group) and adds the S
+// partials of each in rank (= k) order starting from zero -- the order of
+// the global-memory fix-up, so both give the same bits.  All of a thread's
+// loads from one CTA are in flight at once: S round trips in all.
+__device__ __forceinline__ int cluster_group(int S, int rank, int ctid, int g, int* q1) {
+  constexpr int kGroups = BM * 128 / 4;
+  *q1 = static_cast<int>(static_cast<int64_t>(rank + 1) * kGroups / S);
+  return static_cast<int>(static_cast<int64_t>(rank) * kGroups / S) + ctid + g * kComputeThreads;
+}
+
+__device__ __forceinline__ void cluster_gather(uint32_t part_u32, int S, int rank, int ctid,
+                                               float4 (&sum)[kClusterMaxGroups]) {
+  constexpr int G = kClusterMaxGroups;
+#pragma unroll
+  for (int g = 0; g < G; ++g) sum[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int r = 0; r < S; ++r) {
+    float4 v[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      int q1;
+      const int q = cluster_group(S, rank, ctid, g, &q1);
+      v[g] = q < q1 ? ld_shared_cluster_v4(mapa_shared(part_u32 + static_cast<uint32_t>(q) * 16u,
+                                                       static_cast<uint32_t>(r)))
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      sum[g].x += v[g].x;
+      sum[g].y += v[g].y;
+      sum[g].z += v[g].z;
+      sum[g].w += v[g].w;
+    }
+  }
+}
+
+// C = alpha * sum + beta * C for the groups of cluster_gather, with the
+// edge masks.  All old C values are loaded before any store (a load after a
+// store to C would wait for it): one round trip to memory.
+__device__ __forceinline__ void cluster_store(const SimtArgs& p, int S, int rank, int tm, int tn,
+                                              int ctid, const float4 (&sum)[kClusterMaxGroups]) {
+  constexpr int G = kClusterMaxGroups;
+  const bool read_c = (p.beta != 0.0f);
+  float old[G][4];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    int q1;
+    const int q = cluster_group(S, rank, ctid, g, &q1);
+    const int row = tm * BM + (q >> 5);
+    const int col = tn * 128 + (q & 31) * 4;
+    const float* c_row = p.C + static_cast<int64_t>(row) * p.ldc;
+    const bool live = read_c && q < q1 && row < p.M;
+    if (live && p.c_vec4 && col + 3 < p.N) {
+      const float4 o = *reinterpret_cast<const float4*>(c_row + col);
+      old[g][0] = o.x;
+      old[g][1] = o.y;
+      old[g][2] = o.z;
+      old[g][3] = o.w;
+    } else {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) old[g][c] = (live && col + c < p.N) ? c_row[col + c] : 0.0f;
+    }
+  }
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    int q1;
+    const int q = cluster_group(S, rank, ctid, g, &q1);
+    const int row = tm * BM + (q >> 5);
+    const int col = tn * 128 + (q & 31) * 4;
+    if (q >= q1 || row >= p.M) continue;
+    float* c_row = p.C + static_cast<int64_t>(row) * p.ldc;
+    const float x[4] = {sum[g].x, sum[g].y, sum[g].z, sum[g].w};
+    float y[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) y[c] = read_c ? fmaf(p.alpha, x[c], p.beta * old[g][c]) : p.alpha * x[c];
+    if (p.c_vec4 && col + 3 < p.N) {
+      *reinterpret_cast<float4*>(c_row + col) = make_float4(y[0], y[1], y[2], y[3]);
+    } else {
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        if (col + c < p.N) c_row[col + c] = y[c];
+    }
+  }
+}
+
+// CLUSTER: the launch is a grid of clusters of p.cluster CTAs, one per k-part
+// of a tile (full_items = 0, split = p.cluster, one item per CTA); the parts
+// are added through distributed shared memory instead of the workspace.
+template <int MODE_A, int MODE_B, int BN, bool CLUSTER>
 __global__ void __launch_bounds__(SimtTraits<MODE_A, MODE_B>::kThreads, 1)
     simt_gemm_kernel(const SimtArgs p, const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB) {
+  static_assert(!CLUSTER || BN == 128, "the cluster fix-up is written for 128 x 128 tiles");
   using T = SimtTraits<MODE_A, MODE_B>;
   using Gm = Geom<BN>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -470,6 +638,8 @@ __global__ void __launch_bounds__(SimtTraits<MODE_A, MODE_B>::kThreads, 1)
       mbar_init(&tail->full[s], T::kFullCount);
       mbar_init(&tail->empty[s], kComputeWarps);
     }
+    mbar_init(&tail->ready, CLUSTER ? static_cast<uint32_t>(p.cluster) : 1u);
+    mbar_init(&tail->done, CLUSTER ? static_cast<uint32_t>(p.cluster) : 1u);
     tail->abort_flag = 0;
     tail->last_flag = 0;
     fence_barrier_init();
@@ -477,6 +647,7 @@ __global__ void __launch_bounds__(SimtTraits<MODE_A, MODE_B>::kThreads, 1)
   if (MODE_A == kLoadTma && threadIdx.x == kComputeThreads) tma_prefetch_desc(&tmA);
   if (MODE_B == kLoadTma && threadIdx.x == kComputeThreads) tma_prefetch_desc(&tmB);
   __syncthreads();
+  if (CLUSTER) cluster_arrive_release();  // this CTA's barriers are initialised
   volatile int* abort_flag = &tail->abort_flag;
   // Launched with programmatic stream serialization: the set-up above touches
   // no global memory and may overlap the previous kernel's last CTAs; both
@@ -553,7 +724,7 @@ __global__ void __launch_bounds__(SimtTraits<MODE_A, MODE_B>::kThreads, 1)
   uint32_t it = 0;
   for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
     const SimtItem w = simt_item(p, item, tiles_m, tiles_n, num_kb);
-    if (w.kb0 == w.kb1) continue;  // an empty stream-K segment
+    if (!CLUSTER && w.kb0 == w.kb1) continue;  // an empty stream-K segment
     uint64_t acc2[8][Gm::kCols / 2];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
@@ -573,7 +744,48 @@ __global__ void __launch_bounds__(SimtTraits<MODE_A, MODE_B>::kThreads, 1)
       if (lane == 0) mbar_arrive(&tail->empty[s]);
     }
     // Leave together if a wait ran out anywhere (see named_bar_any).
-    if (named_bar_any(1, kComputeThreads, failed)) return;
+    const bool any_failed = named_bar_any(1, kComputeThreads, failed);
+    if (CLUSTER) {
+      // Every compute warp is past its last stage (the barrier above), so
+      // the ring is free: the partial sums go to its first 64 KB as a
+      // row-major 128 x 128 tile.  After a wait ran out the ring may still
+      // be receiving copies: nothing is written or read, but the CTA still
+      // arrives on every barrier its peers wait for.
+      if (!any_failed) {
+        float* part = reinterpret_cast<float*>(smem);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+          for (int q = 0; q < Gm::kCols / 2; q += 2) {
+            float4 v;
+            unpack2(acc2[i][q], v.x, v.y);
+            unpack2(acc2[i][q + 1], v.z, v.w);
+            const int row = wm * 32 + rg + 4 * i;
+            const int col = wn * 64 + cg * 4 + 32 * (q / 2);
+            *reinterpret_cast<float4*>(part + row * 128 + col) = v;
+          }
+      }
+      cluster_wait_acquire();  // every CTA of the cluster has its barriers
+      compute_bar();           // this CTA's partial sums are all stored
+      mbar_arrive_all(&tail->ready, p.cluster, ctid);
+      if (ctid == 0)
+        tail->last_flag =
+            mbar_wait_cluster(&tail->ready, 0, abort_flag, p.err, kWaitLimitNs) ? 1 : 0;
+      compute_bar();
+      const bool reduce = tail->last_flag && !any_failed;
+      const int rank = static_cast<int>(cluster_cta_rank());
+      float4 sum[kClusterMaxGroups];
+      if (reduce) cluster_gather(smem_u32(smem), p.cluster, rank, ctid, sum);
+      compute_bar();  // this CTA's reads of the other CTAs are done
+      mbar_arrive_all(&tail->done, p.cluster, ctid);
+      if (reduce) cluster_store(p, p.cluster, rank, w.tm, w.tn, ctid, sum);
+      // The CTA (its shared memory) stays until every CTA has read it.  The
+      // wait ignores this CTA's abort flag and outlasts a peer's bounded wait
+      // on `ready`, after which that peer arrives here too.
+      if (ctid == 0) mbar_wait_cluster(&tail->done, 0, nullptr, nullptr, 2 * kWaitLimitNs);
+      return;
+    }
+    if (any_failed) return;
     float acc[8][Gm::kCols];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
@@ -644,26 +856,30 @@ __global__ void __launch_bounds__(SimtTraits<MODE_A, MODE_B>::kThreads, 1)
   }
 }
 
-template <int MODE_A, int MODE_B, int BN>
+template <int MODE_A, int MODE_B, int BN, bool CLUSTER = false>
 cudaError_t launch_variant(const SimtArgs& a, int grid, const CUtensorMap* tmA,
                            const CUtensorMap* tmB, cudaStream_t stream) {
   using T = SimtTraits<MODE_A, MODE_B>;
   constexpr size_t kSmem = smem_bytes<BN>();
-  auto kernel = simt_gemm_kernel<MODE_A, MODE_B, BN>;
+  auto kernel = simt_gemm_kernel<MODE_A, MODE_B, BN, CLUSTER>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmem));
   if (e != cudaSuccess) return e;
   CUtensorMap dummy{};
   cudaLaunchConfig_t cfg{};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = CLUSTER ? static_cast<unsigned>(a.cluster) : 1u;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(T::kThreads);
   cfg.dynamicSmemBytes = kSmem;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = CLUSTER ? 2 : 1;
   e = cudaLaunchKernelEx(&cfg, kernel, a, tmA ? *tmA : dummy, tmB ? *tmB : dummy);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -820,6 +1036,57 @@ SimtPlan simt_plan(int M, int N, int K, int num_sms, const TileConfig* fixed, bo
   return pl;
 }
 
+// Clusters of S CTAs of the cluster instance that can be resident at once on
+// the current device (one CTA per SM; a cluster must fit in one GPC).
+// Queried once per device and size.
+int simt_max_clusters(int S) {
+  constexpr int kMaxDev = 64;
+  static std::atomic<int> cache[kMaxDev][kSimtMaxCluster + 1];  // 0 = not yet known
+  int dev = 0;
+  if (S < 2 || S > kSimtMaxCluster || cudaGetDevice(&dev) != cudaSuccess || dev < 0 ||
+      dev >= kMaxDev) {
+    cudaGetLastError();
+    return 0;
+  }
+  const int known = cache[dev][S].load(std::memory_order_relaxed);
+  if (known != 0) return known;
+  using T = SimtTraits<kLoadTma, kLoadTma>;
+  constexpr size_t kSmem = smem_bytes<128>();
+  auto kernel = simt_gemm_kernel<kLoadTma, kLoadTma, 128, true>;
+  int n = 0;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kSmem)) == cudaSuccess) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(S));
+    cfg.blockDim = dim3(T::kThreads);
+    cfg.dynamicSmemBytes = kSmem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(S);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) n = 0;
+  }
+  cudaGetLastError();
+  if (n > 0) cache[dev][S].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+bool simt_use_cluster(SimtPlan& pl, int M, int N) {
+  pl.cluster = 0;
+  if (pl.wide || pl.sk_workers != 0 || pl.full_items != 0 || pl.split < 2 ||
+      pl.split > kSimtMaxCluster)
+    return false;
+  const int tiles = ((M + BM - 1) / BM) * ((N + 127) / 128);
+  if (pl.grid != tiles * pl.split || tiles > simt_max_clusters(pl.split)) return false;
+  pl.cluster = pl.split;
+  pl.ws_floats = 0;
+  pl.counters = 0;
+  return true;
+}
+
 int simt_plan_max_parts(const SimtPlan& pl, int M, int N, int K) {
   if (pl.sk_workers == 0) return pl.split;
   const int bn = simt_bn(pl.wide);
@@ -839,6 +1106,16 @@ int simt_plan_max_parts(const SimtPlan& pl, int M, int N, int K) {
 cudaError_t launch_simt(const SimtArgs& a, const SimtPlan& plan, LoadMode mode_a,
                         LoadMode mode_b, const CUtensorMap* tmA, const CUtensorMap* tmB,
                         cudaStream_t stream) {
+  if (a.cluster > 1) {
+    // Every CTA must have its one item and its cluster (each waits for the
+    // others at the cluster barriers): see simt_use_cluster.
+    const int tiles = ((a.M + BM - 1) / BM) * ((a.N + 127) / 128);
+    if (plan.wide || mode_a != kLoadTma || mode_b != kLoadTma || a.cluster > kSimtMaxCluster ||
+        a.full_items != 0 || a.sk_workers != 0 || a.split != a.cluster ||
+        plan.grid != tiles * a.cluster)
+      return cudaErrorInvalidValue;
+    return launch_variant<kLoadTma, kLoadTma, 128, true>(a, plan.grid, tmA, tmB, stream);
+  }
   // The planner picks the wide tile only when both operands are on TMA.
   if (plan.wide) {
     if (mode_a != kLoadTma || mode_b != kLoadTma) return cudaErrorInvalidValue;

@@ -1,0 +1,183 @@
+"""The CUDA-core kernel's cluster fix-up: when every 128 x 128 tile runs in
+the first round, cut into S = 2..8 k-ranges, the S CTAs of a tile form a
+thread-block cluster and add their partial sums through distributed shared
+memory instead of the stream's global workspace.
+
+The partial sums are the same and are added in the same (k) order, so the
+result must be bit-identical to the global-memory fix-up, which the
+generic-load kernel (an A pitch TMA cannot describe) still takes; on small
+integers both must equal the oracle bit for bit.  The mode needs no scratch,
+so a first call inside a stream capture keeps its split.
+"""
+import numpy as np
+import pytest
+import torch
+
+import dense_gemm_12_gb300 as g
+from dense_gemm_12_gb300.workloads import make_inputs
+from gpu_helpers import check_device_error, oracle_sgemm, ratio
+
+pytestmark = pytest.mark.gpu
+
+INT = ("int", None)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(gemm_lib, cuda_device):
+    yield
+
+
+def _call(A, B, C, alpha, beta, cfg, lda=None, ldc=None, stream=None):
+    """gemm_sgemm_config on device copies; A is laid out with pitch lda and C
+    with pitch ldc (the columns past K / N hold sentinels)."""
+    M, K = A.shape
+    N = B.shape[1]
+    lda = lda or K
+    ldc = ldc or N
+    dA = torch.full((M, lda), 7.0, device="cuda")
+    dA[:, :K] = A.cuda()
+    dC = torch.full((M, ldc), -3.0, device="cuda")
+    dC[:, :N] = C.cuda()
+    dB = B.cuda()
+    h = stream.cuda_stream if stream is not None else torch.cuda.current_stream().cuda_stream
+    st = g.gemm_sgemm_config(M, N, K, alpha, dA.data_ptr(), lda, dB.data_ptr(), N, beta,
+                             dC.data_ptr(), ldc, cfg, h)
+    torch.cuda.synchronize()
+    assert st == 0, g.gemm_status_string(st)
+    out = dC.cpu()
+    assert torch.all(out[:, N:] == -3.0), "write past N"
+    return out[:, :N].contiguous()
+
+
+# (M, N, K, S): tiles x S <= 152, ragged M, N and K, S from 2 to 8
+CASES = [
+    (200, 300, 32 * 2 * 3 + 7, 2),
+    (256, 384, 1000, 3),
+    (129, 1000, 4 * 32 * 4, 4),
+    (100, 520, 1111, 5),
+    (384, 256, 6 * 32 * 4 + 31, 6),
+    (77, 250, 7 * 32 * 5, 7),
+    (300, 260, 2048, 8),
+]
+
+
+@pytest.mark.parametrize("M,N,K,S", CASES)
+def test_cluster_fixup_exact_on_integers(M, N, K, S):
+    cfg = {"kernel": "single_cta", "split": S, "group_m": 1}
+    assert g.gemm_split_cluster(M, N, K, cfg) == S
+    A, B, C = make_inputs(M, N, K, INT, INT, INT, seed=M + S)
+    ref32, _, _ = oracle_sgemm(A, B, C, 1.5, -0.5, want64=False)
+    out = _call(A, B, C, 1.5, -0.5, cfg)
+    assert np.array_equal(out.numpy().view(np.uint32), ref32.view(np.uint32))
+    # an odd C pitch: no float4 rows, the scalar output path
+    out = _call(A, B, C, 1.5, -0.5, cfg, ldc=N + 1)
+    assert np.array_equal(out.numpy().view(np.uint32), ref32.view(np.uint32))
+    check_device_error()
+
+
+@pytest.mark.parametrize("M,N,K,S", CASES[::2])
+def test_cluster_fixup_bits_equal_global_fixup(M, N, K, S):
+    # random inputs: the cluster form (TMA operands) against the same split
+    # through the workspace (A at an unaligned pitch: generic loads)
+    cfg = {"kernel": "single_cta", "split": S, "group_m": 3}
+    A, B, C = make_inputs(M, N, K, ("uniform", None), ("uniform", None), ("uniform", None),
+                          seed=11 * S)
+    lda = K + 1 if (K + 1) % 4 else K + 2   # rows not 16-byte aligned
+    assert g.gemm_select_path(0, M, N, K, 0.7, 1 << 20, lda, 1 << 20, N) == "simt_generic"
+    a = _call(A, B, C, 0.7, 0.3, cfg)
+    b = _call(A, B, C, 0.7, 0.3, cfg, lda=lda)
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    _, ref64, den = oracle_sgemm(A, B, C, 0.7, 0.3)
+    assert ratio(a, ref64, den) <= 2e-6 * K ** 0.5
+    check_device_error()
+
+
+def test_beta_zero_ignores_nan_c():
+    M, N, K, S = 200, 300, 512, 4
+    cfg = {"kernel": "single_cta", "split": S}
+    assert g.gemm_split_cluster(M, N, K, cfg) == S
+    A, B, C = make_inputs(M, N, K, INT, INT, INT, seed=5)
+    ref32, _, _ = oracle_sgemm(A, B, torch.zeros_like(C), 2.0, 0.0, want64=False)
+    out = _call(A, B, torch.full_like(C, float("nan")), 2.0, 0.0, cfg)
+    assert np.array_equal(out.numpy().view(np.uint32), ref32.view(np.uint32))
+
+
+def test_automatic_dispatch_uses_clusters_for_small_shapes():
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    # 256^3: four tiles, each cut along k -- the fix-up runs in clusters
+    assert g.gemm_split_parts(0, 256, 256, 256) > 1
+    assert g.gemm_split_cluster(256, 256, 256) == g.gemm_split_parts(0, 256, 256, 256)
+    # the 4092^3 plan has whole rounds: no clusters
+    assert g.gemm_split_cluster(4092, 4092, 4092) == 1
+    # more tiles than SMs: the split tail meets in global memory
+    assert g.gemm_split_cluster(128 * 13, 128 * 13, 2048) == 1
+    # pinned: the wide tile, stream-K and no split never use clusters
+    assert g.gemm_split_cluster(256, 256, 256, {"kernel": "wide", "split": 4}) == 1
+    assert g.gemm_split_cluster(256, 256, 256, {"split": -1}) == 1
+    assert g.gemm_split_cluster(256, 256, 256, {"split": 1}) == 1
+    # tiles x S above the SM count cannot all run at once
+    tiles = sms // 2 + 1
+    assert g.gemm_split_cluster(128 * tiles, 128, 4096, {"kernel": "single_cta", "split": 2}) == 1
+    assert g.gemm_split_cluster(-1, 256, 256) == 0
+    assert g.gemm_split_cluster(256, 256, 256, {"split": 9}) == 0
+    A, B, C = make_inputs(256, 256, 256, INT, INT, INT, seed=8)
+    ref32, _, _ = oracle_sgemm(A, B, C, 1.0, 1.0, want64=False)
+    dA, dB, dC = A.cuda(), B.cuda(), C.cuda()
+    assert g.gemm_sgemm(256, 256, 256, 1.0, dA.data_ptr(), 256, dB.data_ptr(), 256, 1.0,
+                        dC.data_ptr(), 256, torch.cuda.current_stream().cuda_stream) == 0
+    assert np.array_equal(dC.cpu().numpy().view(np.uint32), ref32.view(np.uint32))
+
+
+def test_first_call_inside_capture_keeps_its_split():
+    # a new stream has no scratch, and a capture allocates none: the global
+    # fix-up would fall back to whole tiles (other sums, other bits on random
+    # inputs); the cluster fix-up needs none and gives the eager call's bits
+    M, N, K = 1024, 1024, 2048
+    S = g.gemm_split_parts(0, M, N, K)
+    assert S > 1 and g.gemm_split_cluster(M, N, K) == S
+    A, B, C = make_inputs(M, N, K, ("uniform", None), ("uniform", None), ("uniform", None),
+                          seed=21)
+    dA, dB, dC = A.cuda(), B.cuda(), C.cuda()
+    out = torch.empty_like(dC)
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            out.copy_(dC)
+            assert g.gemm_sgemm(M, N, K, 0.7, dA.data_ptr(), K, dB.data_ptr(), N, 0.3,
+                                out.data_ptr(), N, s.cuda_stream) == 0
+        out.fill_(float("nan"))
+        graph.replay()
+        s.synchronize()
+        captured = out.clone()
+        out.copy_(dC)
+        assert g.gemm_sgemm(M, N, K, 0.7, dA.data_ptr(), K, dB.data_ptr(), N, 0.3,
+                            out.data_ptr(), N, s.cuda_stream) == 0
+        s.synchronize()
+    assert torch.equal(captured.view(torch.int32), out.view(torch.int32))
+    assert g.gemm_release_stream(s.cuda_stream) == 0
+    check_device_error()
+
+
+def test_two_streams_at_once():
+    # no shared scratch: two cluster launches on two streams overlap freely
+    M, N, K, S = 512, 512, 2048, 4
+    cfg = {"kernel": "single_cta", "split": S}
+    assert g.gemm_split_cluster(M, N, K, cfg) == S
+    ins = [make_inputs(M, N, K, INT, INT, INT, seed=30 + i) for i in range(2)]
+    dev = [[t.cuda() for t in x] for x in ins]
+    streams = [torch.cuda.Stream() for _ in range(2)]
+    torch.cuda.synchronize()
+    for _ in range(3):
+        for (dA, dB, dC), s in zip(dev, streams):
+            assert g.gemm_sgemm_config(M, N, K, 1.0, dA.data_ptr(), K, dB.data_ptr(), N, 1.0,
+                                       dC.data_ptr(), N, cfg, s.cuda_stream) == 0
+    torch.cuda.synchronize()
+    for (A, B, C), (_, _, dC) in zip(ins, dev):
+        # C <- A B + C three times over
+        ref = C
+        for _ in range(3):
+            ref32, _, _ = oracle_sgemm(A, B, ref, 1.0, 1.0, want64=False)
+            ref = torch.from_numpy(ref32)
+        assert np.array_equal(dC.cpu().numpy().view(np.uint32), ref32.view(np.uint32))
+    check_device_error()
