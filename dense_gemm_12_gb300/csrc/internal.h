@@ -79,6 +79,10 @@ constexpr int kSimtMaxCluster = 8;
 // every tile's cluster can be resident at once on the current device.  For
 // 128-wide tiles with both operands on TMA only; returns whether it did.
 bool simt_use_cluster(SimtPlan& pl, int M, int N);
+// Clusters of S (2..8) CTAs of the cluster form that can be resident at once
+// on the current device (one CTA per SM; a cluster must fit in one GPC), 0
+// if unknown.  Queried once per device and size.
+int simt_max_clusters(int S);
 // Largest number of parts any tail tile of the plan is cut into (1 = none).
 int simt_plan_max_parts(const SimtPlan& pl, int M, int N, int K);
 

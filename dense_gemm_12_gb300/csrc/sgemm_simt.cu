@@ -902,10 +902,12 @@ cudaError_t launch_width(const SimtArgs& a, int grid, LoadMode mode_a, LoadMode 
 }
 
 // ------------------------------------------------------------- planning
-// Measured cost of cutting a tile into parts: about 2 k-block times per part
-// (storing its partial sums, and for the last part reading the others and
-// writing the tile), in k-blocks of the tile's own width.
-constexpr double kSplitFixupKb = 2.0;
+// Measured cost of cutting a tile into parts through the workspace, in
+// k-blocks of the tile's own width per part (storing its partial sums, and
+// for the last part reading the others and writing the tile): per-CTA
+// timestamps put the end of the last part 7.4, 11 and 19 us after the end of
+// the k loops for 2, 4 and 8 parts (k-blocks of ~2.5 us): 1.0-1.5 per part.
+constexpr double kSplitFixupKb = 1.2;
 // A k-block of a 128 x 256 tile costs about 1.86 k-blocks of a 128 x 128 tile
 // (twice the FMAs at ~7 % better FMA-pipe use: fewer shared-memory reads per
 // FMA, and the 4-fold unroll of its k loop).  Measured on shapes that both
@@ -915,17 +917,44 @@ constexpr double kWideKbCost = 1.86;
 // Least k-blocks per stream-K range the cost model picks (a pinned stream-K
 // tail goes down to one).
 constexpr int kStreamMinKb = 4;
-// Measured fixed cost of each of a stream-K worker's (up to two) segments, in
-// k-blocks: storing its partial tile, the arrival, and restarting the k loop.
-// Fitted on the shapes where short ranges made stream-K lose to an equal
-// split (e.g. 128x1024x1024: 33 us split in 8, 52 us stream-K).
-constexpr double kStreamSegmentKb = 3.0;
+// Stream-K overhead in k-blocks: a fixed cost per segment (a worker runs up
+// to two: storing its partial tile, the arrival, restarting the k loop) and a
+// cost per partial tile the finishing worker reads.  Fitted on 128 x 1024 x 8192 and
+// 256 x 1024 x 8192 (8 and 16 tiles of 256 k-blocks on 152 workers: 81.5
+// and 99.5 us, about 4 + 0.67 k-blocks per part beyond the k loop), and it
+// keeps stream-K behind the cluster split where ranges are short
+// (128 x 1024 x 1024: 18.9 us in 8 parts, 52 us stream-K).
+constexpr double kStreamSegmentKb = 2.0;
+constexpr double kStreamPartKb = 0.67;
+
+// Measured cost of the cluster fix-up per part, in k-blocks: 256^3 runs in
+// 16.3, 12.4 and 10.8 us cut into 2, 4 and 8 parts (one k-block of a part
+// there ~2.2 us, each part's share of the fix-up ~0.2 us).
+constexpr double kClusterFixupKb = 0.15;
 
 struct TailChoice {
   int split;        // equal parts per tail tile (1 = none)
   int sk_workers;   // > 0: stream-K instead
   double cost;      // in k-blocks of this tile width
 };
+
+// Cost, in k-blocks, of `tiles` 128-wide tiles cut into S parts that all run
+// at once as clusters of S: the longest part plus the fix-up.
+double cluster_cost(int num_kb, int S) {
+  return static_cast<double>((num_kb + S - 1) / S) + kClusterFixupKb * S;
+}
+
+// The cheapest number of parts S (2..8, at most one per k-block) into which
+// `tiles` 128-wide tiles can be cut so that all S x tiles CTAs run at once as
+// clusters of S (see simt_use_cluster), or 1 if there is none.
+int cluster_parts(int tiles, int num_kb, int num_sms) {
+  int best = 1;
+  for (int S = 2; S <= kSimtMaxCluster && S <= num_kb; ++S)
+    if (static_cast<int64_t>(tiles) * S <= num_sms && tiles <= simt_max_clusters(S) &&
+        (best == 1 || cluster_cost(num_kb, S) < cluster_cost(num_kb, best)))
+      best = S;
+  return best;
+}
 
 // Cost, in k-blocks, of the tail of `tail` tiles cut into S equal parts
 // each, run R = ceil(tail S / workers) rounds deep.
@@ -943,10 +972,11 @@ double stream_cost(int tail, int num_kb, int G) {
   const int64_t W = static_cast<int64_t>(tail) * num_kb;
   const int64_t per = (W + G - 1) / G;
   const int parts = (G + tail - 1) / tail + 1;
-  return static_cast<double>(per) + 2 * kStreamSegmentKb + 0.5 * kSplitFixupKb * parts;
+  return static_cast<double>(per) + 2 * kStreamSegmentKb + kStreamPartKb * parts;
 }
 
-TailChoice choose_tail(int tail, int num_kb, int num_sms, const TileConfig* fixed) {
+// `cluster`: every tile is in the tail and the cluster fix-up is possible.
+TailChoice choose_tail(int tail, int num_kb, int num_sms, const TileConfig* fixed, bool cluster) {
   TailChoice c{1, 0, 0.0};
   if (tail <= 0) return c;
   const int64_t W = static_cast<int64_t>(tail) * num_kb;
@@ -963,6 +993,14 @@ TailChoice choose_tail(int tail, int num_kb, int num_sms, const TileConfig* fixe
   }
   c.split = tail_split(tail, num_kb, num_sms, kSplitFixupKb);
   c.cost = split_cost(tail, c.split, num_kb, num_sms);
+  if (cluster) {
+    const int S = cluster_parts(tail, num_kb, num_sms);
+    const double cc = cluster_cost(num_kb, S);
+    if (S > 1 && cc < c.cost) {
+      c.split = S;
+      c.cost = cc;
+    }
+  }
   int G = num_sms;
   if (W / G < kStreamMinKb) G = static_cast<int>(W / kStreamMinKb);
   if (G >= tail && G > 1) {
@@ -977,13 +1015,15 @@ TailChoice choose_tail(int tail, int num_kb, int num_sms, const TileConfig* fixe
 }
 
 // Estimated time of the whole launch in 128 x 128 k-block units.
+// `tma_operands`: both operands on TMA, which the cluster fix-up needs.
 double plan_time(int M, int N, int num_kb, int num_sms, bool wide, const TileConfig* fixed,
-                 TailChoice* tail_out, int* full_out) {
+                 bool tma_operands, TailChoice* tail_out, int* full_out) {
   const int bn = simt_bn(wide);
   const int tiles = ((M + BM - 1) / BM) * ((N + bn - 1) / bn);
   const int tail = tiles >= num_sms ? tiles % num_sms : tiles;
   const int full = tiles - tail;
-  const TailChoice t = choose_tail(tail, num_kb, num_sms, fixed);
+  const TailChoice t =
+      choose_tail(tail, num_kb, num_sms, fixed, tma_operands && !wide && full == 0);
   *tail_out = t;
   *full_out = full;
   const double kb = (static_cast<double>(full) / num_sms) * num_kb + t.cost;
@@ -1004,13 +1044,13 @@ SimtPlan simt_plan(int M, int N, int K, int num_sms, const TileConfig* fixed, bo
   const int pinned_kernel = fixed != nullptr ? fixed->kernel : GEMM_KERNEL_AUTO;
   TailChoice tn{}, tw{};
   int full_n = 0, full_w = 0;
-  const double time_n = plan_time(M, N, num_kb, num_sms, false, fixed, &tn, &full_n);
+  const double time_n = plan_time(M, N, num_kb, num_sms, false, fixed, allow_wide, &tn, &full_n);
   bool wide = allow_wide && pinned_kernel == GEMM_KERNEL_WIDE;
   if (allow_wide && pinned_kernel == GEMM_KERNEL_AUTO) {
-    const double time_w = plan_time(M, N, num_kb, num_sms, true, fixed, &tw, &full_w);
+    const double time_w = plan_time(M, N, num_kb, num_sms, true, fixed, true, &tw, &full_w);
     wide = time_w < time_n;
   } else if (wide) {
-    plan_time(M, N, num_kb, num_sms, true, fixed, &tw, &full_w);
+    plan_time(M, N, num_kb, num_sms, true, fixed, true, &tw, &full_w);
   }
   const TailChoice& t = wide ? tw : tn;
   const int bn = simt_bn(wide);
@@ -1036,9 +1076,6 @@ SimtPlan simt_plan(int M, int N, int K, int num_sms, const TileConfig* fixed, bo
   return pl;
 }
 
-// Clusters of S CTAs of the cluster instance that can be resident at once on
-// the current device (one CTA per SM; a cluster must fit in one GPC).
-// Queried once per device and size.
 int simt_max_clusters(int S) {
   constexpr int kMaxDev = 64;
   static std::atomic<int> cache[kMaxDev][kSimtMaxCluster + 1];  // 0 = not yet known

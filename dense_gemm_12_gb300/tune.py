@@ -28,6 +28,8 @@ import argparse
 import datetime
 import itertools
 import math
+import os
+import re
 import statistics
 import sys
 
@@ -37,6 +39,9 @@ BF16_NK = [256, 1024, 4096, 8192]
 FP32_M = [128, 256, 512, 1024, 2048, 4092]
 FP32_NK = [256, 1024, 4092, 8192]
 SPLITS = [1, 2, 3, 4, 6, 8]
+# fp32 also tries 5 and 7: the largest k-split whose thread-block clusters
+# all fit at once is often one of them (the CUDA-core kernel's cluster fix-up)
+FP32_SPLITS = [1, 2, 3, 4, 5, 6, 7, 8]
 GROUPS = [4, 8, 16]
 
 
@@ -66,7 +71,7 @@ def candidates(is_bf16: bool, M: int, N: int, K: int, num_sms: int = 152):
     kernels = ["single_cta"] if is_bf16 else ["single_cta", "wide"]
     if is_bf16 and M > 128:
         kernels = ["cta_pair", "single_cta"]
-    splits = SPLITS + [-1]   # -1: the stream-K tail
+    splits = (SPLITS if is_bf16 else FP32_SPLITS) + [-1]   # -1: the stream-K tail
     num_kb = -(-K // (64 if is_bf16 else 32))
     for kernel, split, group in itertools.product(kernels, splits, GROUPS):
         if split > num_kb:
@@ -182,7 +187,33 @@ def sweep_shape(torch, g, is_bf16, M, N, K, stream, reps=5, confirm_reps=20):
             "candidates": len(timed)}
 
 
-def summary_lines(results, chosen, gpu, num_sms, command):
+TABLE_ENTRY = re.compile(r"^\s*\{(\d+), (\d+), (\d+), (\d+), (\d+), (-?\d+), (\d+)\},\s*//\s*"
+                         r"(\d+)x(\d+)x(\d+): ([\d.]+) ms, cost model ([\d.]+) ms")
+
+
+def kept_entries(table_text: str, is_bf16: int):
+    """Entries of one type in an existing table (what a sweep of the other
+    type alone keeps), as table_lines takes them."""
+    names = {1: "single_cta", 2: "cta_pair", 3: "wide"}
+    out = []
+    for line in table_text.splitlines():
+        m = TABLE_ENTRY.match(line)
+        if m is None or int(m.group(1)) != is_bf16:
+            continue
+        v = m.groups()
+        out.append({"is_bf16": is_bf16, "M": int(v[7]), "N": int(v[8]), "K": int(v[9]),
+                    "kernel": names[int(v[4])], "split": int(v[5]), "group_m": int(v[6]),
+                    "best_ms": float(v[10]), "auto_ms": float(v[11])})
+    return out
+
+
+def kept_rows(summary_text: str, is_bf16: int):
+    """Class rows of one type in an existing summary."""
+    tag = "| bf16 |" if is_bf16 else "| fp32 |"
+    return [line for line in summary_text.splitlines() if line.startswith(tag)]
+
+
+def summary_lines(results, chosen, gpu, num_sms, command, kept=()):
     flops = lambda r: 2.0 * r["M"] * r["N"] * r["K"]
     lines = ["# Launch-configuration sweep of the tile kernels", "",
              "Command (%s, %d SMs):" % (gpu, num_sms), "", "    " + command, "",
@@ -195,6 +226,10 @@ def summary_lines(results, chosen, gpu, num_sms, command):
              "to `csrc/dispatch_table.inc`.", "",
              "| type | M x N x K | model (kernel, split, group) | ms | TFLOP/s | best | ms "
              "| TFLOP/s | gain | |", "|---|---|---|---:|---:|---|---:|---:|---:|---|"]
+    if kept:
+        lines[-2:-2] = ["Rows of the other type are kept from the previous sweep that wrote "
+                        "this file (a sweep of one type, --only).", ""]
+    lines += list(kept)
     chosen_keys = {(c["is_bf16"], c["M"], c["N"], c["K"]) for c in chosen}
     for r in results:
         a = r["auto"]
@@ -249,12 +284,23 @@ def main(argv=None):
     if st != 0:
         raise RuntimeError("device error during the sweep: " + g.gemm_status_string(st))
     chosen = choose(results, args.margin)
+    # a sweep of one type keeps the other type's entries and summary rows
+    kept_table, kept_summary = [], []
+    if args.only is not None:
+        other = 0 if args.only == "bf16" else 1
+        if os.path.exists(args.table):
+            kept_table = kept_entries(open(args.table).read(), other)
+        if os.path.exists(args.summary):
+            kept_summary = kept_rows(open(args.summary).read(), other)
     date = datetime.date.today().isoformat()
     with open(args.table, "w") as f:
-        f.write(table_lines(chosen, num_sms, props.name, date))
+        f.write(table_lines(kept_table + chosen, num_sms, props.name, date))
     command = "python -m dense_gemm_12_gb300.tune " + " ".join(argv or sys.argv[1:])
     with open(args.summary, "w") as f:
-        f.write(summary_lines(results, chosen, props.name, num_sms, command))
+        f.write(summary_lines(results, chosen, props.name, num_sms, command,
+                              kept_summary if args.only == "fp32" else ()))
+        if args.only == "bf16":
+            f.write("\n".join(kept_summary) + "\n" if kept_summary else "")
     print("%d of %d classes written to the table" % (len(chosen), len(results)))
 
 

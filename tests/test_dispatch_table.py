@@ -102,3 +102,22 @@ def test_table_writer_keeps_wide_and_stream_entries():
     r.update(kernel="wide", split=-1, group_m=8)
     sms, rows = parse_table(tune.table_lines([r], 152, "GPU", "2026-01-01"))
     assert rows[0] == (0, 12, 10, 10, 3, -1, 8)
+
+
+def test_one_type_sweep_keeps_the_other_types_entries():
+    # re-rendering the committed table's parsed entries of both types gives
+    # the same entries back, so a sweep of one type loses none of the other's
+    text = open(TABLE).read()
+    kept = tune.kept_entries(text, 1) + tune.kept_entries(text, 0)
+    _, rows = parse_table(text)
+    _, again = parse_table(tune.table_lines(kept, 152, "GPU", "today"))
+    assert sorted(again) == sorted(rows)
+    assert all(e["is_bf16"] == 1 for e in tune.kept_entries(text, 1))
+    rows = tune.kept_rows("| bf16 | 1x1x1 | a |\n| fp32 | 2x2x2 | b |\nother\n", 0)
+    assert rows == ["| fp32 | 2x2x2 | b |"]
+
+
+def test_fp32_candidates_include_every_cluster_size():
+    c = list(tune.candidates(False, 512, 512, 2048))
+    assert {x["split"] for x in c} >= {1, 2, 3, 4, 5, 6, 7, 8, -1}
+    assert 5 not in {x["split"] for x in tune.candidates(True, 1024, 1024, 4096)}
