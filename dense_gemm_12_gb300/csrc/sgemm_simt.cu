@@ -365,26 +365,31 @@ __device__ __forceinline__ void compute_stage_x2(const uint8_t* sA, const uint8_
 // C = alpha * acc + beta * C for the thread's 8 x kCols micro-tile, kRows rows
 // at a time: the old values of a chunk's rows are all loaded before any of
 // them is stored, so their round trips overlap (a load issued after a store
-// to a possibly aliasing address would wait for it).  The narrow tile takes
-// all 8 rows at once; the wide tile one row (4 float4) at a time, as more old
-// values next to its 128 accumulators would spill.
+// to a possibly aliasing address would wait for it).  Batch sizes below.
 template <int BN>
 __device__ __forceinline__ void epilogue(const SimtArgs& p, const float (&acc)[8][Geom<BN>::kCols],
                                          int tm, int tn, int wm, int wn, int rg, int cg) {
   constexpr int kGroups = Geom<BN>::kColGroups;
-  constexpr int kRows = BN == 128 ? 8 : 1;
   const bool read_c = (p.beta != 0.0f);
   const int row0 = tm * BM + wm * 32 + rg;
   const int col0 = tn * BN + wn * (BN / 2) + cg * 4;
   const bool vec = p.c_vec4 && col0 + 32 * (kGroups - 1) + 3 < p.N;
+  if (vec) {
+    // Rows in flight per batch: all 8 on the narrow tile; 2 on the wide one,
+    // whose 128 accumulators leave room for 32 old values but not 64 (4 rows
+    // spilled, and made the k loop 1.5 % slower; 1 row left 8 serial round
+    // trips to memory: 2 rows took 4092^3 with beta != 0 from 2.055 to
+    // 2.044 ms).  A running row pointer keeps the addresses in two registers.
+    constexpr int kRows = BN == 128 ? 8 : 2;
+    const int64_t row_step = 4 * p.ldc;
+    float* c_next = p.C + static_cast<int64_t>(row0) * p.ldc + col0;
 #pragma unroll
-  for (int i0 = 0; i0 < 8; i0 += kRows) {
-    if (vec) {
+    for (int i0 = 0; i0 < 8; i0 += kRows) {
       float4 old[kRows][kGroups];
 #pragma unroll
       for (int r = 0; r < kRows; ++r) {
         const int row = row0 + 4 * (i0 + r);
-        const float* c_row = p.C + static_cast<int64_t>(row) * p.ldc + col0;
+        const float* c_row = c_next + r * row_step;
 #pragma unroll
         for (int h = 0; h < kGroups; ++h)
           old[r][h] = (read_c && row < p.M) ? *reinterpret_cast<const float4*>(c_row + 32 * h)
@@ -395,7 +400,7 @@ __device__ __forceinline__ void epilogue(const SimtArgs& p, const float (&acc)[8
         const int i = i0 + r;
         const int row = row0 + 4 * i;
         if (row >= p.M) continue;
-        float* c_row = p.C + static_cast<int64_t>(row) * p.ldc + col0;
+        float* c_row = c_next + r * row_step;
 #pragma unroll
         for (int h = 0; h < kGroups; ++h) {
           float4 v = make_float4(acc[i][4 * h], acc[i][4 * h + 1], acc[i][4 * h + 2],
@@ -414,37 +419,43 @@ __device__ __forceinline__ void epilogue(const SimtArgs& p, const float (&acc)[8
           *reinterpret_cast<float4*>(c_row + 32 * h) = v;
         }
       }
-    } else {
-      float old[kRows][4 * kGroups];
+      c_next += kRows * row_step;
+    }
+    return;
+  }
+  // Edge tiles and C rows without float4 alignment: element by element.
+  constexpr int kRows = BN == 128 ? 8 : 1;
 #pragma unroll
-      for (int r = 0; r < kRows; ++r) {
-        const int row = row0 + 4 * (i0 + r);
-        const float* c_row = p.C + static_cast<int64_t>(row) * p.ldc;
+  for (int i0 = 0; i0 < 8; i0 += kRows) {
+    float old[kRows][4 * kGroups];
 #pragma unroll
-        for (int h = 0; h < kGroups; ++h)
+    for (int r = 0; r < kRows; ++r) {
+      const int row = row0 + 4 * (i0 + r);
+      const float* c_row = p.C + static_cast<int64_t>(row) * p.ldc;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int col = col0 + 32 * h + c;
-            old[r][4 * h + c] = (read_c && row < p.M && col < p.N) ? c_row[col] : 0.0f;
+      for (int h = 0; h < kGroups; ++h)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int col = col0 + 32 * h + c;
+          old[r][4 * h + c] = (read_c && row < p.M && col < p.N) ? c_row[col] : 0.0f;
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) {
+      const int i = i0 + r;
+      const int row = row0 + 4 * i;
+      if (row >= p.M) continue;
+      float* c_row = p.C + static_cast<int64_t>(row) * p.ldc;
+#pragma unroll
+      for (int h = 0; h < kGroups; ++h)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int col = col0 + 32 * h + c;
+          if (col < p.N) {
+            const float x = acc[i][4 * h + c];
+            c_row[col] = read_c ? fmaf(p.alpha, x, p.beta * old[r][4 * h + c]) : p.alpha * x;
           }
-      }
-#pragma unroll
-      for (int r = 0; r < kRows; ++r) {
-        const int i = i0 + r;
-        const int row = row0 + 4 * i;
-        if (row >= p.M) continue;
-        float* c_row = p.C + static_cast<int64_t>(row) * p.ldc;
-#pragma unroll
-        for (int h = 0; h < kGroups; ++h)
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int col = col0 + 32 * h + c;
-            if (col < p.N) {
-              const float x = acc[i][4 * h + c];
-              c_row[col] = read_c ? fmaf(p.alpha, x, p.beta * old[r][4 * h + c]) : p.alpha * x;
-            }
-          }
-      }
+        }
     }
   }
 }
