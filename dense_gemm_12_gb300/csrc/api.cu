@@ -252,8 +252,8 @@ gemm_status_t ensure_stage(DeviceState& st, cudaStream_t stream, int64_t bytes, 
 // FLOPs, and N >= 256 when A is copied (M >= 256 for B), which keeps the
 // copy under ~2 % of the GEMM.  bf16: the tensor cores are ~25x faster than
 // the CUDA-core fallback, so any tile-kernel shape of at least 2^24 FLOPs is
-// copied (and then run on the tile kernels or, for M <= 64, the decode
-// kernel); M <= 16 keeps the fallback.
+// copied (and then run on the tile kernels or the decode kernel, whichever
+// automatic dispatch picks for the shape); M <= 16 keeps the fallback.
 bool stage_wanted(bool bf16, int64_t M, int64_t N, int64_t K, bool a_ok, bool b_ok) {
   if (a_ok && b_ok) return false;
   const double flops = 2.0 * static_cast<double>(M) * static_cast<double>(N) *

@@ -188,26 +188,37 @@ cudaError_t launch_tc_decode(const DecodeArgs& a, const CUtensorMap* tmA,
 constexpr int kDecBN = 128, kDecBM = 16;
 // Rows of the largest kernel instance (the MMA's N) and so of a row block.
 constexpr int kDecBlockRows = 64;
-// Largest M the decode kernel takes (two row blocks); larger M runs on the
+// Largest M the decode kernel takes (eight row blocks); larger M runs on the
 // tile kernels.
-constexpr int kDecMaxM = 128;
-// Whether automatic dispatch runs a bf16 M x N x K GEMM on the decode kernel:
-// every M <= 32, and 32 < M <= 128 up to N = 16384 (two row blocks above 64
-// rows).  Measured against the tile kernels (back-to-back launches, us):
+constexpr int kDecMaxM = 512;
+// Whether automatic dispatch runs a bf16 M x N x K GEMM on the decode kernel.
+// Every M <= 32.  32 < M <= 128 up to N = 16384 (two row blocks above 64
+// rows); measured against the tile kernels (back-to-back launches, us):
 // M = 17, 32, 48, 64 at 4096 x 4096: 10.3, 10.2, 11.9, 11.9 against
 // 27.0-28.7; M = 64 at 8192 x 8192 27.8 vs 49.8, at 12288 x 4096 24.6 vs
 // 43.3; M = 72-128 at N = 1024, 4096, 8192, 12288, 16384 (K = 4096): 8.7,
 // 13.8, 20.9, 35.0, 41.9 against 27.9, 27.4, 36.1, 43.6, 45.6 on the
 // single-CTA tile kernel (K = 8192 at N = 16384: 65.6 vs 65.8); but M = 64
 // at N = 28672 (more column groups than SMs) 52.8 vs 51.1 on the tile kernel.
+// 128 < M <= 512 (3 to 8 row blocks, each reading all of B, from L2 after
+// the first): while the 128-column groups times the row blocks stay within
+// about one round of a 152-SM GPU -- at most 128, or 160 for K >= 4096,
+// where the tile kernels' fixed costs weigh less.  Measured over M = 160-512,
+// N = 1024-16384, K = 1024-8192 (us, decode vs tile kernels): 256 x 4096 x
+// 4096 19.1 vs 29.9, 512 x 1024 x 4096 14.3 vs 30.7, 512 x 2048 x 8192 30.2
+// vs 40.2, 320 x 4096 x 4096 (160 units) 27.7 vs 32.2; beyond the bound the
+// tile kernels win (256 x 8192 x 4096 38.2 vs 34.0, 512 x 4096 x 4096 35.4
+// vs 34.3, 320 x 4096 x 1024 18.9 vs 18.5).
 inline bool decode_path(int64_t M, int64_t N, int64_t K) {
-  (void)K;
   if (M > kDecMaxM) return false;
-  return M <= 32 || N <= 16384;
+  if (M <= 32) return true;
+  if (M <= 128) return N <= 16384;
+  const int64_t units = ((N + kDecBN - 1) / kDecBN) * ((M + kDecBlockRows - 1) / kDecBlockRows);
+  return units <= (K >= 4096 ? 160 : 128);
 }
 // Rows of the kernel instance a launch with M rows uses (16, 32 or 64).
 int decode_rows(int M);
-// Row blocks of a decode launch with M rows (1, or 2 for M > 64).
+// Row blocks of a decode launch with M rows (ceil(M / 64), 1 to 8).
 int decode_row_blocks(int M);
 // 128-column groups of C (one arrival counter each, per row block).
 int64_t decode_groups(int N);

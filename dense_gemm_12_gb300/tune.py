@@ -33,7 +33,8 @@ import re
 import statistics
 import sys
 
-# (bf16 with M <= 64 runs the decode kernel, which plans itself: no classes)
+# (bf16 shapes that automatic dispatch sends to the decode kernel -- M <= 32,
+# and larger M with few column groups -- have no class: see main)
 BF16_M = [256, 1024, 2048, 4096, 8192]
 BF16_NK = [256, 1024, 4096, 8192]
 FP32_M = [128, 256, 512, 1024, 2048, 4092]
@@ -213,7 +214,9 @@ def kept_rows(summary_text: str, is_bf16: int):
     return [line for line in summary_text.splitlines() if line.startswith(tag)]
 
 
-def summary_lines(results, chosen, gpu, num_sms, command, kept=()):
+def summary_lines(results, chosen, gpu, num_sms, command, kept=(), kept_after=()):
+    """Markdown summary; `kept` / `kept_after`: class rows of the other type,
+    kept from the previous summary, placed before / after the new rows."""
     flops = lambda r: 2.0 * r["M"] * r["N"] * r["K"]
     lines = ["# Launch-configuration sweep of the tile kernels", "",
              "Command (%s, %d SMs):" % (gpu, num_sms), "", "    " + command, "",
@@ -226,7 +229,7 @@ def summary_lines(results, chosen, gpu, num_sms, command, kept=()):
              "to `csrc/dispatch_table.inc`.", "",
              "| type | M x N x K | model (kernel, split, group) | ms | TFLOP/s | best | ms "
              "| TFLOP/s | gain | |", "|---|---|---|---:|---:|---|---:|---:|---:|---|"]
-    if kept:
+    if kept or kept_after:
         lines[-2:-2] = ["Rows of the other type are kept from the previous sweep that wrote "
                         "this file (a sweep of one type, --only).", ""]
     lines += list(kept)
@@ -244,6 +247,7 @@ def summary_lines(results, chosen, gpu, num_sms, command, kept=()):
                          flops(r) / r["best_ms"] / 1e9 if r["best_ms"] else 0.0, 100 * gain,
                          "table" if (r["is_bf16"], r["M"], r["N"], r["K"]) in chosen_keys
                          else ""))
+    lines += list(kept_after)
     bad = [(r, c) for r in results for c in r["rejected"]]
     lines += ["", "Configurations rejected by the result check: %d." % len(bad)]
     for r, c in bad:
@@ -273,6 +277,10 @@ def main(argv=None):
         shapes += [(True, M, N, K) for M in BF16_M for N in BF16_NK for K in BF16_NK]
     if args.only in (None, "fp32"):
         shapes += [(False, M, N, K) for M in FP32_M for N in FP32_NK for K in FP32_NK]
+    # shapes automatic dispatch sends to the decode kernel (which plans itself
+    # and never reads the table) have no class
+    shapes = [s for s in shapes if not (s[0] and g.gemm_select_path(
+        1, s[1], s[2], s[3], 1.0, 1 << 20, s[3], 1 << 20, s[2]) == "tc_decode")]
     results = []
     for is_bf16, M, N, K in shapes:
         r = sweep_shape(torch, g, is_bf16, M, N, K, stream)
@@ -298,9 +306,8 @@ def main(argv=None):
     command = "python -m dense_gemm_12_gb300.tune " + " ".join(argv or sys.argv[1:])
     with open(args.summary, "w") as f:
         f.write(summary_lines(results, chosen, props.name, num_sms, command,
-                              kept_summary if args.only == "fp32" else ()))
-        if args.only == "bf16":
-            f.write("\n".join(kept_summary) + "\n" if kept_summary else "")
+                              kept_summary if args.only == "fp32" else (),
+                              kept_summary if args.only == "bf16" else ()))
     print("%d of %d classes written to the table" % (len(chosen), len(results)))
 
 

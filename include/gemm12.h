@@ -131,10 +131,11 @@ gemm_status_t gemm_sgemm(int64_t M, int64_t N, int64_t K, float alpha,
  * shared memory by asynchronous copies) runs on the 5th-generation tensor
  * cores with the accumulator in tensor memory.  Small M takes the
  * bandwidth-bound decode kernel (the "decode GEMV (M <= 16)" case of "Tiled
- * matrix multiplication", "Avoid when", widened here to every M <= 32, and
- * to 32 < M <= 128 up to N = 16384 -- above 64 rows as two row blocks --
- * where it measured faster than the tile kernels; gemm_select_path reports
- * GEMM_PATH_TC_DECODE), which splits K across CTAs
+ * matrix multiplication", "Avoid when", widened here to every M <= 32, to
+ * 32 < M <= 128 up to N = 16384, and to 128 < M <= 512 while ceil(N / 128)
+ * x ceil(M / 64) <= 128 (160 for K >= 4096) -- above 64 rows as row blocks
+ * of 64 -- where it measured faster than the tile kernels; gemm_select_path
+ * reports GEMM_PATH_TC_DECODE), which splits K across CTAs
  * ("Split-K" in the same page's "Variants and alternatives") and reduces the
  * partial sums in a fixed order, so results are deterministic.  Error bound:
  * 8e-3 of |alpha|*(|A||B|)_ij + |beta|*|C_ij| against the exact product of the

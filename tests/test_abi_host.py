@@ -79,7 +79,12 @@ P = 1 << 20
     (dict(bf16=1, M=8192, N=8192, K=8192), "tc_bf16_pair"),
     (dict(bf16=1, M=128, N=8192, K=8192), "tc_decode"),          # two row blocks of 64
     (dict(bf16=1, M=128, N=16392, K=8192), "tc_bf16"),
-    (dict(bf16=1, M=129, N=8192, K=8192), "tc_bf16_pair"),
+    (dict(bf16=1, M=129, N=8192, K=8192), "tc_bf16_pair"),        # 64 groups x 3 row blocks
+    (dict(bf16=1, M=256, N=4096, K=4096), "tc_decode"),           # 32 groups x 4 row blocks
+    (dict(bf16=1, M=512, N=2048, K=1024), "tc_decode"),           # 16 x 8
+    (dict(bf16=1, M=320, N=4096, K=4096), "tc_decode"),           # 160, K >= 4096
+    (dict(bf16=1, M=320, N=4096, K=1024), "tc_bf16_pair"),        # 160 at small K
+    (dict(bf16=1, M=513, N=1024, K=1024), "tc_bf16_pair"),        # beyond eight row blocks
     (dict(bf16=1, M=16, N=12288, K=4096), "tc_decode"),
     (dict(bf16=1, M=1, N=12288, K=4096), "tc_decode"),
     (dict(bf16=1, M=17, N=12288, K=4096), "tc_decode"),

@@ -33,8 +33,8 @@ def test_committed_table_is_well_formed():
         assert kernel != 3 or is_bf16 == 0
         assert 1 <= split <= 8 or (split == -1 and is_bf16 == 0)
         assert 1 <= group <= 64
-        # bf16 with M <= 64 runs the decode kernel, which never reads the table
-        assert not (is_bf16 and lm <= 6), "dead bf16 entry for M <= 64"
+        # bf16 with M <= 32 runs the decode kernel, which never reads the table
+        assert not (is_bf16 and lm <= 5), "dead bf16 entry for M <= 32"
 
 
 def test_sweep_grid_leaves_decode_shapes_out():
@@ -121,3 +121,12 @@ def test_fp32_candidates_include_every_cluster_size():
     c = list(tune.candidates(False, 512, 512, 2048))
     assert {x["split"] for x in c} >= {1, 2, 3, 4, 5, 6, 7, 8, -1}
     assert 5 not in {x["split"] for x in tune.candidates(True, 1024, 1024, 4096)}
+
+
+def test_no_bf16_entry_for_a_decode_shape(gemm_lib):
+    # the class's measured shape must take the tile kernels under automatic
+    # dispatch, else the entry is never read (host-only path query)
+    for e in tune.kept_entries(open(TABLE).read(), 1):
+        M, N, K = e["M"], e["N"], e["K"]
+        assert gemm_lib.gemm_select_path(1, M, N, K, 1.0, 1 << 20, K, 1 << 20, N) != "tc_decode", \
+            (M, N, K)

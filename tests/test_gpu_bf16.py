@@ -61,10 +61,14 @@ def test_ragged_tensor_core(M, N, K):
     A, B, C = _inputs(M, N, K, seed=M + N + K)
     out, st, _, _, dC = run_bf16gemm(A, B, C, 0.7, 0.3)
     assert st == 0
-    # small M runs the decode kernel (bound by streaming B): M <= 32, and
-    # M <= 128 (two row blocks above 64) up to N = 16384; the tile kernels at
-    # small M are covered with pinned configurations in test_gpu_config.py
-    decode = M <= 32 or (M <= 128 and N <= 16384)
+    # small M runs the decode kernel (bound by streaming B): M <= 32; M <= 128
+    # (two row blocks above 64) up to N = 16384; M <= 512 (row blocks of 64)
+    # while column groups x row blocks stay within 128 (160 for K >= 4096).
+    # The tile kernels at small M are covered with pinned configurations in
+    # test_gpu_config.py
+    units = -(-N // 128) * -(-M // 64)
+    decode = M <= 32 or (M <= 128 and N <= 16384) or \
+        (M <= 512 and units <= (160 if K >= 4096 else 128))
     expect = "tc_decode" if decode else "tc_bf16" if M <= 128 else "tc_bf16_pair"
     assert g.gemm_select_path(1, M, N, K, 0.7, 1 << 20, K, 1 << 20, N) == expect
     _, ref64, den = oracle_bf16(A, B, C, 0.7, 0.3)

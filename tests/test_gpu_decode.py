@@ -1,4 +1,4 @@
-"""Decode-shaped bf16 GEMM (small M, up to 128 rows in two row blocks) on the
+"""Decode-shaped bf16 GEMM (small M, up to 512 rows in row blocks of 64) on the
 GPU: the swapped-operand tcgen05 kernel with split-K and the fixed-order
 fix-up, against the CPU oracle.
 
@@ -112,11 +112,42 @@ def test_decode_two_row_blocks_random_within_bound(M, N, K):
     check_device_error()
 
 
-def test_decode_beyond_two_row_blocks_takes_tile_kernels():
-    assert g.gemm_select_path(1, 129, 4096, 4096, 1.0, 1 << 20, 4096, 1 << 20, 4096) == \
-        "tc_bf16_pair"
-    assert g.gemm_select_path(1, 100, 16392, 4096, 1.0, 1 << 20, 4096, 1 << 20, 16392) == \
-        "tc_bf16"
+# 128 < M <= 512: three to eight row blocks, each reading all of B (from L2
+# after the first); the last block may be mostly past M.
+@pytest.mark.parametrize("M,N,K", [
+    (160, 1000, 1024),   # 3 blocks, the last with 32 rows; ragged N
+    (256, 4096, 4096),   # 4 blocks x 32 groups = 128 CTAs: whole groups
+    (320, 2048, 2048),   # 5 blocks x 16 groups
+    (512, 1024, 8192),   # 8 blocks x 8 groups: clusters of 2 per group
+    (500, 296, 1000),    # 8 blocks, the last with 52 rows; ragged N and K
+    (384, 3328, 4096),   # 26 groups > 25 SMs per block: runs of groups
+])
+def test_decode_many_row_blocks_integers_exact(M, N, K):
+    assert g.gemm_select_path(1, M, N, K, 1.0, 1 << 20, K, 1 << 20, N) == "tc_decode"
+    _cluster_exact(M, N, K)
+
+
+@pytest.mark.parametrize("M,N,K", [(200, 4000, 4096), (448, 1500, 2048)])
+def test_decode_many_row_blocks_random_within_bound(M, N, K):
+    A, B, C = make_inputs(M, N, K, ("normal", 1.0), ("normal", 0.02), ("uniform", None),
+                          seed=M + N, dtype="bf16")
+    out, st, _, _, dC = run_bf16gemm(A, B, C, 0.5, 1.0, ldc=N + 5)
+    assert st == 0
+    _, ref64, den = oracle_bf16(A, B, C, 0.5, 1.0)
+    assert ratio(out, ref64, den) <= TOL_BF16
+    assert dC.untouched_outside()
+    check_device_error()
+
+
+def test_decode_range_boundaries():
+    path = lambda M, N, K: g.gemm_select_path(1, M, N, K, 1.0, 1 << 20, K, 1 << 20, N)
+    assert path(129, 4096, 4096) == "tc_decode"      # 32 groups x 3 blocks
+    assert path(512, 2048, 1024) == "tc_decode"      # 16 x 8 = 128
+    assert path(320, 4096, 4096) == "tc_decode"      # 32 x 5 = 160, K >= 4096
+    assert path(320, 4096, 1024) == "tc_bf16_pair"   # 160 > 128 at small K
+    assert path(256, 8192, 4096) == "tc_bf16_pair"   # 64 x 4 = 256
+    assert path(513, 1024, 1024) == "tc_bf16_pair"   # beyond eight row blocks
+    assert path(100, 16392, 4096) == "tc_bf16"       # M <= 128 beyond N = 16384
 
 
 def _cluster_exact(M, N, K):

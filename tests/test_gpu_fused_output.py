@@ -114,7 +114,8 @@ INT_SHAPES = [
     (24, 16384, 256),     # decode kernel, 32-row instance, whole column groups
     (100, 520, 256),      # decode kernel, two row blocks of 64
     (100, 16392, 256),    # single-CTA kernel, ragged N
-    (384, 512, 256),      # CTA-pair kernel, odd number of tile rows
+    (384, 512, 256),      # decode kernel, six row blocks of 64
+    (640, 512, 256),      # CTA-pair kernel, odd number of tile rows
     (100, 16640, 4096),   # single-CTA kernel, tiles split along k
 ]
 
@@ -136,7 +137,8 @@ def test_integers_exact(M, N, K, out, d_scale):
     assert amax == float(np.max(np.abs(v)))
 
 
-@pytest.mark.parametrize("M,N,K", [(8, 1000, 512), (100, 520, 256), (384, 512, 256)])
+@pytest.mark.parametrize("M,N,K", [(8, 1000, 512), (100, 520, 256), (384, 512, 256),
+                                   (640, 512, 256)])
 def test_empty_product_integers_exact(M, N, K):
     # alpha = 0: the output stage alone (v = act(beta*C + bias) + R)
     A, B, C, bias, res = _int_case(M, N, K, seed=7)

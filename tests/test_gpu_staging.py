@@ -69,10 +69,12 @@ def test_fp32_staged_matches_generic_loader_result_bound():
 
 
 @pytest.mark.parametrize("M,N,K,lda,ldb,offsets,kernel", [
-    (512, 640, 257, 258, 640, (0, 0, 0), "pair"),     # A pitch 516 B
-    (100, 512, 333, 333, 517, (0, 0, 0), "single"),   # both pitches odd
-    (384, 768, 512, 512, 768, (1, 0, 0), "pair"),     # A base 2 bytes off
-    (256, 256, 1000, 1001, 257, (0, 5, 0), "pair"),   # B pitch and base
+    (512, 640, 257, 258, 640, (0, 0, 0), "decode"),   # A pitch 516 B; 8 row blocks
+    (100, 512, 333, 333, 517, (0, 0, 0), "decode"),   # both pitches odd
+    (384, 768, 512, 512, 768, (1, 0, 0), "decode"),   # A base 2 bytes off
+    (640, 768, 512, 512, 768, (1, 0, 0), "pair"),     # A base 2 bytes off
+    (256, 256, 1000, 1001, 257, (0, 5, 0), "decode"),  # B pitch and base
+    (1024, 256, 1000, 1001, 257, (0, 5, 0), "pair"),  # B pitch and base
 ])
 def test_bf16_staged_tensor_cores_exact_on_integers(M, N, K, lda, ldb, offsets, kernel):
     A, B, C = make_inputs(M, N, K, INT, INT, INT, seed=M * 7 + K, dtype="bf16")
@@ -123,7 +125,8 @@ def _fused_relu(M, N, K, lda, ldb, seed):
     (8, 1000, 777, 777, 1000),   # decode, A pitch 1554 B
     (40, 300, 130, 131, 300),    # decode kernel, 64-row instance, small
     (100, 300, 130, 131, 300),   # decode kernel, two row blocks
-    (300, 520, 270, 270, 521),   # CTA pairs
+    (300, 520, 270, 270, 521),   # decode kernel, five row blocks
+    (640, 520, 270, 270, 521),   # CTA pairs
 ])
 def test_fused_output_stage_on_staged_operands(M, N, K, lda, ldb):
     _fused_relu(M, N, K, lda, ldb, seed=M + N)
