@@ -138,7 +138,7 @@ def load_library(build_if_missing: bool = False):
         lib.gemm_quantization.restype = cint
         lib.gemm_split_parts.argtypes = [cint, i64, i64, i64]
         lib.gemm_split_parts.restype = cint
-        lib.gemm_split_cluster.argtypes = [i64, i64, i64, cfg_p]
+        lib.gemm_split_cluster.argtypes = [cint, i64, i64, i64, cfg_p]
         lib.gemm_split_cluster.restype = cint
         lib.gemm_version.argtypes = []
         lib.gemm_version.restype = cint
@@ -262,11 +262,11 @@ def gemm_split_parts(is_bf16, M, N, K) -> int:
     return load_library().gemm_split_parts(int(bool(is_bf16)), M, N, K)
 
 
-def gemm_split_cluster(M, N, K, config=None) -> int:
-    """fp32 with TMA operands: the cluster size S whose CTAs add a tile's k-parts
-    in distributed shared memory, 1 if they meet in global memory or nothing is
-    split, 0 for invalid input or no device.  `config` as for gemm_sgemm_config."""
-    return load_library().gemm_split_cluster(M, N, K, _config(config))
+def gemm_split_cluster(is_bf16, M, N, K, config=None) -> int:
+    """TMA operands: the cluster size S whose CTAs add a tile's k-parts in
+    distributed shared memory, 1 if they meet in global memory or nothing is
+    split, 0 for invalid input or no device.  `config` as for the _config calls."""
+    return load_library().gemm_split_cluster(int(bool(is_bf16)), M, N, K, _config(config))
 
 
 def gemm_quantization(M, N, BM, BN, num_sms, ctas_per_sm) -> dict:

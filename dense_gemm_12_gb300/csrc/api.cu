@@ -625,16 +625,26 @@ int gemm_split_parts(int is_bf16, int64_t M, int64_t N, int64_t K) {
   return simt_plan_max_parts(simt_plan(m, n, k, st->num_sms, &tc, true), m, n, k);
 }
 
-int gemm_split_cluster(int64_t M, int64_t N, int64_t K, const gemm_config_t* cfg) {
+int gemm_split_cluster(int is_bf16, int64_t M, int64_t N, int64_t K, const gemm_config_t* cfg) {
+  const bool bf16 = is_bf16 != 0;
   if (M < 0 || N < 0 || K < 0 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX ||
-      !config_fields_valid(cfg, false))
+      !config_fields_valid(cfg, bf16))
     return 0;
   gemm_status_t s;
   DeviceState* st = device_state(&s);
   if (st == nullptr) return 0;
   if (M == 0 || N == 0 || K == 0) return 1;
   const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
-  const TileConfig tc = resolve_config(false, M, N, K, st->num_sms, cfg, nullptr);
+  const TileConfig tc = resolve_config(bf16, M, N, K, st->num_sms, cfg, nullptr);
+  if (bf16) {
+    // the decode kernel (automatic dispatch only) plans its own clusters
+    if (decode_path(M, N, K) && (cfg == nullptr || cfg->kernel == GEMM_KERNEL_AUTO)) return 1;
+    TcPlan pl = tc_plan(m, n, k, st->num_sms, &tc);
+    Epilogue plain{};
+    plain.alpha = 1.0f;
+    plain.d_scale = 1.0f;
+    return tc_use_cluster(pl, m, n, plain) ? pl.cluster : 1;
+  }
   SimtPlan pl = simt_plan(m, n, k, st->num_sms, &tc, true);
   return simt_use_cluster(pl, m, n) ? pl.cluster : 1;
 }
@@ -775,7 +785,10 @@ static gemm_status_t run_bf16_tensor_core(DeviceState* st, gemm_path_t path, int
     a.epi = epi;
     a.err = st->err_word;
     const TileConfig tc = resolve_config(true, M, N, K, st->num_sms, cfg, nullptr);
-    const TcPlan pl = tc_plan(a.M, a.N, a.K, st->num_sms, &tc);
+    TcPlan pl = tc_plan(a.M, a.N, a.K, st->num_sms, &tc);
+    // Tiles that all fit in one round add their k-parts through distributed
+    // shared memory (single-CTA kernel).
+    tc_use_cluster(pl, a.M, a.N, epi);
     const uint32_t b_rows = static_cast<uint32_t>(tc_b_box_rows(pl.pair));
     if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, K, M, lda, 64, kTcBM,
                    CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -785,7 +798,7 @@ static gemm_status_t run_bf16_tensor_core(DeviceState* st, gemm_path_t path, int
     TcPlan run = pl;
     a.ws = nullptr;
     a.counters = nullptr;
-    if (pl.split > 1 || pl.sk_workers > 0) {
+    if ((pl.split > 1 || pl.sk_workers > 0) && pl.cluster <= 1) {
       // Split items: the stream's scratch stays locked until the launch is
       // queued, so no other thread can regrow it underneath.  Without scratch
       // (inside a stream capture, or out of memory) every item runs whole.
@@ -807,6 +820,7 @@ static gemm_status_t run_bf16_tensor_core(DeviceState* st, gemm_path_t path, int
     a.split = run.split;
     a.sk_workers = run.sk_workers;
     a.group_m = run.group_m;
+    a.cluster = run.cluster;
     return from_cuda(launch_tc_bf16(a, run, &tmA, &tmB, cs));
   }
   // GEMM_PATH_TC_DECODE

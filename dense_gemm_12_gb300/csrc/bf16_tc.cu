@@ -455,7 +455,53 @@ __device__ __forceinline__ void epilogue_unit(const TcArgs& p, const Unit& w, ui
   epi_bar();  // last_flag is rewritten by the next split unit
 }
 
+// The cluster form's reduction: CTA `rank` of a cluster of S takes the
+// 32-column chunks [rank * 8 / S, (rank + 1) * 8 / S) of the tile; for each,
+// every epilogue thread adds its row's 32 values from the S CTAs' partial
+// sums (stored in each CTA's shared memory at `part_u32` in the workspace
+// layout) in rank (= k) order, starting from zero -- the order and the
+// arithmetic of the workspace fix-up -- and runs the chunk through the output
+// stage.  The 8 loads from one CTA are in flight together: S round trips per
+// chunk.
 template <bool FUSED>
+__device__ __forceinline__ void cluster_chunks(const TcArgs& p, uint32_t part_u32, int S,
+                                               int rank, float4* stg, int row_base, int tn,
+                                               int et, float& amax_acc) {
+  const int c0 = rank * (BN / 32) / S, c1 = (rank + 1) * (BN / 32) / S;
+#pragma unroll 1
+  for (int c = c0; c < c1; ++c) {
+    float sum[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) sum[i] = 0.0f;
+#pragma unroll 1
+    for (int src = 0; src < S; ++src) {
+      float4 v[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        v[q] = ld_shared_cluster_v4(mapa_shared(
+            part_u32 + static_cast<uint32_t>(((c * 8 + q) * kEpiThreads + et) * 16),
+            static_cast<uint32_t>(src)));
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        sum[4 * q] += v[q].x;
+        sum[4 * q + 1] += v[q].y;
+        sum[4 * q + 2] += v[q].z;
+        sum[4 * q + 3] += v[q].w;
+      }
+    }
+    uint32_t r[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(sum[i]);
+    store_chunk<FUSED>(p, stg, row_base, tn * BN + c * 32, r, amax_acc);
+  }
+}
+
+// CLUSTER: one unit per CTA -- a k-part of a tile, full_items = 0, split =
+// p.cluster -- and the parts of a tile form a cluster that adds its partial
+// sums through distributed shared memory (cluster_chunks) instead of the
+// workspace.  Every thread of the CTA reaches the two cluster barriers after
+// its role, also after a bounded wait ran out, so none can hang there.
+template <bool FUSED, bool CLUSTER>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bf16_kernel(const __grid_constant__ TcArgs p, const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB) {
@@ -503,6 +549,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // global access below follows its completion.
   grid_dependency_wait();
   if (threadIdx.x == 0) grid_launch_dependents();
+  float amax_acc = 0.0f;
+  bool parts_stored = false;  // CLUSTER: this CTA's partial sums are in shared memory
 
   if (warp == 0) {
     // -------------------------------------------------------- TMA producer
@@ -591,7 +639,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     const int et = quarter * 32 + lane;
     float4* stg = reinterpret_cast<float4*>(epi_stage + quarter * 4096);
-    float amax_acc = 0.0f;
     uint32_t j = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       const Unit w = unit_of(p, u, num_kb, num_items);
@@ -605,12 +652,49 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (named_bar_any(kEpiBarAny, kEpiThreads, !ok)) break;
       tc_fence_after_sync();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + ab * BN;
-      epilogue_unit<FUSED>(p, w, taddr, stg, tm * BM + quarter * 32, tn, 1, 0, num_kb, W, et,
-                           &tail->last_flag, amax_acc);
+      if (CLUSTER) {
+        // The MMAs are done and this CTA has no further unit, so the ring
+        // is free: the part's 128 x 256 partial sums go to its first 128 KB,
+        // laid out as in the workspace (thread-major float4s).
+        float4* part = reinterpret_cast<float4*>(smem);
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(taddr + c * 32, r);
+          tc_wait_ld();
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            part[(c * 8 + q) * kEpiThreads + et] =
+                make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                            __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+        }
+        parts_stored = true;
+      } else {
+        epilogue_unit<FUSED>(p, w, taddr, stg, tm * BM + quarter * 32, tn, 1, 0, num_kb, W, et,
+                             &tail->last_flag, amax_acc);
+      }
       tc_fence_before_sync();
       mbar_arrive(&tail->tmem_empty[ab]);
     }
-    if (FUSED) epi_flush_amax(p.epi, amax_acc);
+    if (FUSED && !CLUSTER) epi_flush_amax(p.epi, amax_acc);
+  }
+
+  if (CLUSTER) {
+    __syncwarp();
+    cluster_sync();  // every part's partial sums are in its shared memory
+    // parts_stored is the same in all epilogue threads (they leave the loop
+    // together); without it some part is missing and the error word is set.
+    if (warp >= 2 && parts_stored) {
+      const int quarter = warp & 3;
+      int tm, tn;
+      tile_coords(static_cast<int>(blockIdx.x) / p.cluster, tiles_m, tiles_n, p.group_m, tm, tn);
+      cluster_chunks<FUSED>(p, smem_u32(smem), p.cluster, static_cast<int>(cluster_cta_rank()),
+                            reinterpret_cast<float4*>(epi_stage + quarter * 4096),
+                            tm * BM + quarter * 32, tn, quarter * 32 + lane, amax_acc);
+      if (FUSED) epi_flush_amax(p.epi, amax_acc);
+    }
+    __syncwarp();
+    cluster_sync();  // no CTA leaves while another may still read its shared memory
   }
 
   tc_fence_before_sync();
@@ -892,7 +976,61 @@ static int pair_max_clusters(int num_sms) {
   return clusters;
 }
 
+// Clusters of S single-CTA kernels (cluster form) that can be resident at
+// once on the current device (one CTA per SM; a cluster must fit in one GPC).
+// Queried once per device, size and instance.
+static int single_max_clusters(int S, bool fused) {
+  constexpr int kMaxDev = 64;
+  static std::atomic<int> cache[kMaxDev][9][2];  // 0 = not yet known
+  int dev = 0;
+  if (S < 2 || S > 8 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) {
+    cudaGetLastError();
+    return 0;
+  }
+  const int known = cache[dev][S][fused ? 1 : 0].load(std::memory_order_relaxed);
+  if (known != 0) return known;
+  auto kernel = fused ? tc_bf16_kernel<true, true> : tc_bf16_kernel<false, true>;
+  int n = 0;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kSmemBytes)) == cudaSuccess) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(S));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(S);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) n = 0;
+  }
+  cudaGetLastError();
+  if (n > 0) cache[dev][S][fused ? 1 : 0].store(n, std::memory_order_relaxed);
+  return n;
+}
+
 int tc_b_box_rows(bool pair) { return pair ? PBK : BK; }
+
+// Whether an output stage needs the general (fused) kernel instance.
+static bool tc_fused(const Epilogue& ep) {
+  return ep.bias != nullptr || ep.act != kActNone || ep.R != nullptr || ep.d_type != kOutF32 ||
+         ep.d_scale != 1.0f || ep.amax != nullptr;
+}
+
+bool tc_use_cluster(TcPlan& pl, int M, int N, const Epilogue& epi) {
+  const bool fused = tc_fused(epi);
+  pl.cluster = 0;
+  if (pl.pair || pl.sk_workers != 0 || pl.full_items != 0 || pl.split < 2 || pl.split > 8)
+    return false;
+  const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  if (pl.grid != tiles * pl.split || tiles > single_max_clusters(pl.split, fused)) return false;
+  pl.cluster = pl.split;
+  pl.ws_floats = 0;
+  pl.counters = 0;
+  return true;
+}
 
 TcPlan tc_plan(int M, int N, int K, int num_sms, const TileConfig* fixed) {
   TcPlan pl{};
@@ -954,9 +1092,7 @@ int tc_plan_max_parts(const TcPlan& pl, int M, int N, int K) {
 cudaError_t launch_tc_bf16(const TcArgs& a, const TcPlan& plan, const CUtensorMap* tmA,
                            const CUtensorMap* tmB, cudaStream_t stream) {
   if (plan.grid < 1) return cudaSuccess;
-  const Epilogue& ep = a.epi;
-  const bool fused = ep.bias != nullptr || ep.act != kActNone || ep.R != nullptr ||
-                     ep.d_type != kOutF32 || ep.d_scale != 1.0f || ep.amax != nullptr;
+  const bool fused = tc_fused(a.epi);
   if (plan.pair) {
     auto kernel = fused ? tc_bf16_pair_kernel<true> : tc_bf16_pair_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -980,20 +1116,34 @@ cudaError_t launch_tc_bf16(const TcArgs& a, const TcPlan& plan, const CUtensorMa
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
   }
-  auto kernel = fused ? tc_bf16_kernel<true> : tc_bf16_kernel<false>;
+  const bool cluster = a.cluster > 1;
+  if (cluster) {
+    // Every CTA must have its one unit and its cluster (each waits for the
+    // others at the cluster barriers): see tc_use_cluster.
+    const int tiles = ((a.M + BM - 1) / BM) * ((a.N + BN - 1) / BN);
+    if (a.cluster > 8 || a.full_items != 0 || a.sk_workers != 0 || a.split != a.cluster ||
+        plan.grid != tiles * a.cluster)
+      return cudaErrorInvalidValue;
+  }
+  auto kernel = cluster ? (fused ? tc_bf16_kernel<true, true> : tc_bf16_kernel<false, true>)
+                        : (fused ? tc_bf16_kernel<true, false> : tc_bf16_kernel<false, false>);
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cluster ? static_cast<unsigned>(a.cluster) : 1u;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.gridDim = dim3(plan.grid);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = cluster ? 2 : 1;
   e = cudaLaunchKernelEx(&cfg, kernel, a, *tmA, *tmB);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

@@ -139,6 +139,10 @@ struct TcArgs {
   float* ws;
   uint32_t* counters;
   int group_m;     // raster group height in tile rows (pair-tile rows on pairs)
+  // > 1 (single-CTA kernel only): every tile runs in this one round, cut into
+  // `cluster` (= split) parts that form a thread-block cluster and add their
+  // partial sums through distributed shared memory: no workspace, no counters.
+  int cluster;
 };
 
 // Launch plan of the bf16 tensor-core GEMM for one shape.
@@ -151,6 +155,7 @@ struct TcPlan {
   int group_m;
   int64_t ws_floats;  // workspace the split items need
   int64_t counters;   // counters the split items need
+  int cluster;        // > 1: the parts of each tile form a cluster (see TcArgs)
 };
 // `fixed` pins kernel, split (GEMM_SPLIT_STREAM: a stream-K tail) and group
 // height; nullptr: the pair kernel for M > 128, the cost model's split,
@@ -158,6 +163,11 @@ struct TcPlan {
 TcPlan tc_plan(int M, int N, int K, int num_sms, const TileConfig* fixed);
 // Largest number of parts any tail item of the plan is cut into (1 = none).
 int tc_plan_max_parts(const TcPlan& pl, int M, int N, int K);
+// Turns a single-CTA plan whose tiles all run in one round, each cut into
+// 2..8 equal k-parts, into its cluster form (pl.cluster = pl.split, no
+// workspace) when every tile's cluster can be resident at once on the
+// current device; returns whether it did.
+bool tc_use_cluster(TcPlan& pl, int M, int N, const Epilogue& epi);
 // k-rows of B per TMA box of the single-CTA (pair = false) or pair kernel.
 int tc_b_box_rows(bool pair);
 

@@ -330,6 +330,17 @@ __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t cluster_addr) {
   return v;
 }
 
+// 128-bit load from the shared memory of a CTA of the cluster (address from
+// mapa_shared).  Ordered against the stores it reads by the caller's
+// synchronisation (cluster barriers, or mbarriers with cluster scope).
+__device__ __forceinline__ float4 ld_shared_cluster_v4(uint32_t cluster_addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(cluster_addr));
+  return v;
+}
+
 // Arrive (release at cluster scope) on an mbarrier given by its
 // shared::cluster address, possibly in another CTA of the cluster.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {

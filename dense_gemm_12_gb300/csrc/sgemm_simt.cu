@@ -516,17 +516,6 @@ __device__ __forceinline__ void mbar_arrive_all(uint64_t* bar, int S, int ctid) 
   if (ctid < S) mbar_arrive_cluster(mapa_shared(smem_u32(bar), static_cast<uint32_t>(ctid)));
 }
 
-// 128-bit load from the shared memory of a CTA of the cluster (address from
-// mapa_shared).  Ordered against the partial sums' stores by the cluster
-// barriers around the reduction.
-__device__ __forceinline__ float4 ld_shared_cluster_v4(uint32_t cluster_addr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(cluster_addr));
-  return v;
-}
-
 // Float4 groups of the 128 x 128 tile one compute thread reduces in a
 // cluster of S >= 2 CTAs: at most 4096 / (2 * 256).
 constexpr int kClusterMaxGroups = (BM * 128 / 4) / (2 * kComputeThreads);

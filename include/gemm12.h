@@ -460,21 +460,23 @@ gemm_status_t gemm_get_model_config(int is_bf16, int64_t M, int64_t N, int64_t K
                                     gemm_config_t *out);
 
 /*
- * gemm_split_cluster -- host-side diagnostics for gemm_sgemm / _config with
- * operands the TMA engine can describe: when every tile of the problem runs
- * in the first round and each is cut into S = 2..8 k-ranges, the S CTAs of a
- * tile form a thread-block cluster and add their partial sums through
- * distributed shared memory, in k order, instead of through the stream's
- * global-memory workspace (the same sums, so the same bits; no scratch is
- * needed, also inside a stream capture).  That needs the 128-wide tile and
- * all the clusters resident at once on the device.  Returns S when this
- * configuration (`cfg`, or nullptr for automatic dispatch) runs so, 1 when
- * it does not, 0 for invalid sizes or fields or when there is no usable
- * sm_103a device.  The pages' kernels have no counterpart: their split-K
- * partials meet in global memory ("A GEMM Kernel, Step by Step", "What is
- * left").
+ * gemm_split_cluster -- host-side diagnostics for gemm_sgemm / gemm_bf16gemm
+ * (and their _config forms) with operands the TMA engine can describe: when
+ * every tile of the problem runs in the first round and each is cut into
+ * S = 2..8 k-ranges, the S CTAs of a tile form a thread-block cluster and add
+ * their partial sums through distributed shared memory, in k order, instead
+ * of through the stream's global-memory workspace (the same sums, so the same
+ * bits; no scratch is needed, also inside a stream capture).  That needs the
+ * 128-wide fp32 tile or the single-CTA bf16 kernel (128 x 256 tiles), and
+ * all the clusters resident at once on the device.  `is_bf16` selects
+ * gemm_bf16gemm's rules (its decode kernel, which plans its own clusters,
+ * reports 1).  Returns S when this configuration (`cfg`, or nullptr for
+ * automatic dispatch) runs so, 1 when it does not, 0 for invalid sizes or
+ * fields or when there is no usable sm_103a device.  The pages' kernels have
+ * no counterpart: their split-K partials meet in global memory ("A GEMM
+ * Kernel, Step by Step", "What is left").
  */
-int gemm_split_cluster(int64_t M, int64_t N, int64_t K, const gemm_config_t *cfg);
+int gemm_split_cluster(int is_bf16, int64_t M, int64_t N, int64_t K, const gemm_config_t *cfg);
 
 /*
  * Tile and wave quantization of a launch ("A GEMM Kernel, Step by Step",
