@@ -39,10 +39,10 @@ BF16_M = [256, 1024, 2048, 4096, 8192]
 BF16_NK = [256, 1024, 4096, 8192]
 FP32_M = [128, 256, 512, 1024, 2048, 4092]
 FP32_NK = [256, 1024, 4092, 8192]
-SPLITS = [1, 2, 3, 4, 6, 8]
-# fp32 also tries 5 and 7: the largest k-split whose thread-block clusters
-# all fit at once is often one of them (the CUDA-core kernel's cluster fix-up)
-FP32_SPLITS = [1, 2, 3, 4, 5, 6, 7, 8]
+# Every k-split up to 8: with the cluster fix-up (the CUDA-core kernel's
+# 128-wide tiles, the single-CTA tcgen05 kernel) the largest split whose
+# thread-block clusters all fit at once is often 5 or 7.
+SPLITS = [1, 2, 3, 4, 5, 6, 7, 8]
 GROUPS = [4, 8, 16]
 
 
@@ -72,7 +72,7 @@ def candidates(is_bf16: bool, M: int, N: int, K: int, num_sms: int = 152):
     kernels = ["single_cta"] if is_bf16 else ["single_cta", "wide"]
     if is_bf16 and M > 128:
         kernels = ["cta_pair", "single_cta"]
-    splits = (SPLITS if is_bf16 else FP32_SPLITS) + [-1]   # -1: the stream-K tail
+    splits = SPLITS + [-1]   # -1: the stream-K tail
     num_kb = -(-K // (64 if is_bf16 else 32))
     for kernel, split, group in itertools.product(kernels, splits, GROUPS):
         if split > num_kb:
