@@ -35,10 +35,10 @@ import sys
 
 # (bf16 shapes that automatic dispatch sends to the decode kernel -- M <= 32,
 # and larger M with few column groups -- have no class: see main)
-BF16_M = [256, 1024, 2048, 4096, 8192]
-BF16_NK = [256, 1024, 4096, 8192]
+BF16_M = [256, 512, 1024, 2048, 4096, 8192]
+BF16_NK = [256, 512, 1024, 2048, 4096, 8192]
 FP32_M = [128, 256, 512, 1024, 2048, 4092]
-FP32_NK = [256, 1024, 4092, 8192]
+FP32_NK = [256, 512, 1024, 2048, 4092, 8192]
 # Every k-split up to 8: with the cluster fix-up (the CUDA-core kernel's
 # 128-wide tiles, the single-CTA tcgen05 kernel) the largest split whose
 # thread-block clusters all fit at once is often 5 or 7.
