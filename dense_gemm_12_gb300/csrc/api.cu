@@ -602,7 +602,19 @@ gemm_path_t gemm_select_path(int is_bf16, int64_t M, int64_t N, int64_t K, float
                              const void* A, int64_t lda, const void* B, int64_t ldb) {
   if (check_common(M, N, K, lda, ldb, N > 1 ? N : 1) != GEMM_OK) return GEMM_PATH_NONE;
   const bool bf16 = is_bf16 != 0;
-  const gemm_path_t p = select_path(bf16, M, N, K, alpha, A, lda, B, ldb);
+  gemm_path_t p = select_path(bf16, M, N, K, alpha, A, lda, B, ldb);
+  if (p == GEMM_PATH_TC_BF16 || p == GEMM_PATH_TC_BF16_PAIR) {
+    // the tile kernel automatic dispatch runs (the sweep's table may pick
+    // single CTAs for M > 128); without a usable device, the M rule
+    gemm_status_t s;
+    DeviceState* st = device_state(&s);
+    if (st != nullptr) {
+      const TileConfig tc = resolve_config(true, M, N, K, st->num_sms, nullptr, nullptr);
+      const TcPlan pl = tc_plan(static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
+                                st->num_sms, &tc);
+      p = pl.pair ? GEMM_PATH_TC_BF16_PAIR : GEMM_PATH_TC_BF16;
+    }
+  }
   const int eb = bf16 ? 2 : 4;
   if ((p == GEMM_PATH_SIMT_GENERIC || p == GEMM_PATH_SIMT_BF16) &&
       stage_wanted(bf16, M, N, K, tma_ok(A, lda, eb), tma_ok(B, ldb, eb)))

@@ -325,12 +325,14 @@ typedef enum {
     GEMM_PATH_SIMT_TMA = 2,       /* fp32 CUDA-core kernel, TMA operands    */
     GEMM_PATH_SIMT_GENERIC = 3,   /* fp32 CUDA-core kernel, generic loads   */
     GEMM_PATH_TC_BF16 = 4,        /* bf16 tensor-core (tcgen05) kernel,
-                                     one CTA per 128x256 tile (M <= 128)   */
+                                     one CTA per 128x256 tile (M <= 128,
+                                     and small problems: see below)        */
     GEMM_PATH_TC_DECODE = 5,      /* bf16 tensor-core split-K decode kernel */
     GEMM_PATH_SIMT_BF16 = 6,      /* bf16 operands TMA cannot describe:
                                      widened to fp32 on the CUDA cores     */
     GEMM_PATH_TC_BF16_PAIR = 7,   /* bf16 tensor-core kernel on CTA pairs:
-                                     two SMs per 256x256 tile (M > 128)    */
+                                     two SMs per 256x256 tile (M > 128,
+                                     unless single CTAs: see below)        */
     GEMM_PATH_SIMT_STAGED = 8,    /* fp32 operands TMA cannot describe are
                                      first copied into an aligned staging
                                      buffer, then GEMM_PATH_SIMT_TMA       */
@@ -348,6 +350,10 @@ typedef enum {
  * least 2^31 FLOPs (2*M*N*K) and N >= 256 if A is copied, M >= 256 if B is;
  * bf16 with M > 16 and at least 2^24 FLOPs.  Otherwise GEMM_PATH_SIMT_GENERIC
  * or GEMM_PATH_SIMT_BF16 (also when the staging buffer cannot be allocated).
+ * Between the two bf16 tile kernels it reports the one automatic dispatch
+ * runs on the current device (the sweep's table picks single CTAs for many
+ * small problems with M > 128); with no usable device, the one-CTA kernel for
+ * M <= 128 and CTA pairs above.
  * Pointers are only inspected for alignment, never dereferenced.  Returns
  * GEMM_PATH_NONE (and writes nothing) for arguments the call would reject.
  */

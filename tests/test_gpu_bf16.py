@@ -69,7 +69,8 @@ def test_ragged_tensor_core(M, N, K):
     units = -(-N // 128) * -(-M // 64)
     decode = M <= 32 or (M <= 128 and N <= 16384) or \
         (M <= 512 and units <= (160 if K >= 4096 else 128))
-    expect = "tc_decode" if decode else "tc_bf16" if M <= 128 else "tc_bf16_pair"
+    single = g.gemm_get_config(1, M, N, K)[0]["kernel"] == "single_cta"
+    expect = "tc_decode" if decode else "tc_bf16" if single else "tc_bf16_pair"
     assert g.gemm_select_path(1, M, N, K, 0.7, 1 << 20, K, 1 << 20, N) == expect
     _, ref64, den = oracle_bf16(A, B, C, 0.7, 0.3)
     r = ratio(out, ref64, den)
