@@ -1032,12 +1032,29 @@ bool tc_use_cluster(TcPlan& pl, int M, int N, const Epilogue& epi) {
   return true;
 }
 
+// Whether automatic dispatch takes the CTA-pair kernel: on large problems
+// only -- at least 128 single-CTA tiles with K > 2048, or 256 with K > 1024.
+// The launch-configuration sweep over M, N, K = 256 .. 8192 found the pair
+// kernel fastest there (by up to 3 %) and the single-CTA kernel, with its
+// cluster split where every tile fits in one round, everywhere else (by up
+// to 65 %: short k loops fill the pair kernel's 128-deep ring slowly, and
+// few tiles leave SMs idle).
+static bool tc_prefer_pair(int tiles, int K) {
+  return (K > 2048 && tiles >= 128) || (K > 1024 && tiles >= 256);
+}
+
+// Cost, in k-blocks, of cutting each of `tiles` single-CTA tiles into S
+// parts that all run at once as clusters: the longest part plus the
+// cluster fix-up (~1 k-block per part, from the sweep's choices).
+constexpr double kTcClusterFixupKb = 1.0;
+
 TcPlan tc_plan(int M, int N, int K, int num_sms, const TileConfig* fixed) {
   TcPlan pl{};
   const int tiles_m = (M + BM - 1) / BM;
   const int tiles_n = (N + BN - 1) / BN;
   const bool pinned = fixed != nullptr && fixed->kernel != GEMM_KERNEL_AUTO;
-  pl.pair = pinned ? fixed->kernel == GEMM_KERNEL_CTA_PAIR : tiles_m >= 2;
+  pl.pair = pinned ? fixed->kernel == GEMM_KERNEL_CTA_PAIR
+                   : (tiles_m >= 2 && tc_prefer_pair(tiles_m * tiles_n, K));
   const int kblock = pl.pair ? PBK : BK;
   const int num_kb = (K + kblock - 1) / kblock;
   pl.group_m = (fixed != nullptr && fixed->group_m > 0) ? fixed->group_m : 8;
@@ -1062,6 +1079,23 @@ TcPlan tc_plan(int M, int N, int K, int num_sms, const TileConfig* fixed) {
   pl.split = (fixed != nullptr && fixed->split > 0)
                  ? (fixed->split < num_kb ? fixed->split : num_kb)
                  : tail_split(items, num_kb, workers, kTcFixupKb * BK / kblock);
+  if (!pl.pair && items < workers && (fixed == nullptr || fixed->split == 0)) {
+    // Every tile in one round: the cluster split (see tc_use_cluster) costs
+    // far less than the workspace's, so take the cheapest S whose clusters
+    // can all be resident, or none.
+    int best = 1;
+    double best_cost = num_kb;
+    for (int S = 2; S <= 8 && S <= num_kb; ++S) {
+      if (static_cast<int64_t>(items) * S > workers || items > single_max_clusters(S, false))
+        continue;
+      const double cost = static_cast<double>((num_kb + S - 1) / S) + kTcClusterFixupKb * S;
+      if (cost < best_cost - 1e-9) {
+        best = S;
+        best_cost = cost;
+      }
+    }
+    pl.split = best;
+  }
   if (pl.split < 1) pl.split = 1;
   if (tail_items == 0) pl.split = 1;
   const int tail = pl.split > 1 ? tail_items : 0;
