@@ -916,8 +916,14 @@ cudaError_t launch_width(const SimtArgs& a, int grid, LoadMode mode_a, LoadMode 
 // k-blocks of the tile's own width per part (storing its partial sums, and
 // for the last part reading the others and writing the tile): per-CTA
 // timestamps put the end of the last part 7.4, 11 and 19 us after the end of
-// the k loops for 2, 4 and 8 parts (k-blocks of ~2.5 us): 1.0-1.5 per part.
-constexpr double kSplitFixupKb = 1.2;
+// the k loops for 2, 4 and 8 parts (k-blocks of ~2.5 us): 1.0-1.5 per part,
+// with each thread's partial stored contiguously.  Stored warp-coalesced it
+// costs less; 0.8 leaves the fewest sweep classes whose fastest plan the
+// model misses (26 of 216 with the stream-K constants below; 0.3, closer to
+// the ~0.2 per part of 16 tiles of 64 k-blocks -- 8 parts through the
+// workspace 31.6 us, 6 in clusters 38.1 us -- left 34: it over-picks the
+// 128 x 256 tile with equal splits where narrow stream-K tails win).
+constexpr double kSplitFixupKb = 0.8;
 // A k-block of a 128 x 256 tile costs about 1.86 k-blocks of a 128 x 128 tile
 // (twice the FMAs at ~7 % better FMA-pipe use: fewer shared-memory reads per
 // FMA, and the 4-fold unroll of its k loop).  Measured on shapes that both
@@ -929,13 +935,13 @@ constexpr double kWideKbCost = 1.86;
 constexpr int kStreamMinKb = 4;
 // Stream-K overhead in k-blocks: a fixed cost per segment (a worker runs up
 // to two: storing its partial tile, the arrival, restarting the k loop) and a
-// cost per partial tile the finishing worker reads.  Fitted on 128 x 1024 x 8192 and
-// 256 x 1024 x 8192 (8 and 16 tiles of 256 k-blocks on 152 workers: 81.5
-// and 99.5 us, about 4 + 0.67 k-blocks per part beyond the k loop), and it
-// keeps stream-K behind the cluster split where ranges are short
-// (128 x 1024 x 1024: 18.9 us in 8 parts, 52 us stream-K).
+// cost per partial tile the finishing worker reads.  Refitted after the
+// partials were stored warp-coalesced (before: 0.67 per part): 256 x 256 x
+// 8192, 128 x 256 x 8192, 256 x 512 x 4092 and 1024 x 1024 x 2048 on 152
+// workers (39, 77, 20 and 4 parts per tile) ran in 53.4, 71, 40.2 and 81.4
+// us, k-blocks of ~2.5 us: 0.25-0.4 per part beyond the k loop.
 constexpr double kStreamSegmentKb = 2.0;
-constexpr double kStreamPartKb = 0.67;
+constexpr double kStreamPartKb = 0.27;
 
 // Measured cost of the cluster fix-up per part, in k-blocks: 256^3 runs in
 // 16.3, 12.4 and 10.8 us cut into 2, 4 and 8 parts (one k-block of a part

@@ -133,7 +133,10 @@ def test_first_call_inside_capture_keeps_its_split():
     # a new stream has no scratch, and a capture allocates none: the global
     # fix-up would fall back to whole tiles (other sums, other bits on random
     # inputs); the cluster fix-up needs none and gives the eager call's bits
-    M, N, K = 1024, 1024, 2048
+    # the first shape whose automatic plan splits in clusters (the plan comes
+    # from the cost model or the sweep's table)
+    shapes = [(256, 256, 512), (256, 256, 256), (384, 384, 1024), (640, 384, 768)]
+    M, N, K = next((m, n, k) for m, n, k in shapes if g.gemm_split_cluster(0, m, n, k) > 1)
     S = g.gemm_split_parts(0, M, N, K)
     assert S > 1 and g.gemm_split_cluster(0, M, N, K) == S
     A, B, C = make_inputs(M, N, K, ("uniform", None), ("uniform", None), ("uniform", None),
