@@ -833,7 +833,15 @@ static gemm_status_t run_bf16_tensor_core(DeviceState* st, gemm_path_t path, int
     a.sk_workers = run.sk_workers;
     a.group_m = run.group_m;
     a.cluster = run.cluster;
-    return from_cuda(launch_tc_bf16(a, run, &tmA, &tmB, cs));
+    // The plain output stage with beta == 0 writes whole tiles by TMA when
+    // D's base and row pitch allow a tensor map.
+    CUtensorMap tmD;
+    a.d_tma = 0;
+    if (!tc_fused(epi) && epi.beta == 0.0f && tma_ok(epi.D, epi.ldd, 4) &&
+        encode_2d(&tmD, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, epi.D, N, M, epi.ldd,
+                  kTcStoreBoxCols, kTcStoreBoxRows, CU_TENSOR_MAP_SWIZZLE_128B))
+      a.d_tma = 1;
+    return from_cuda(launch_tc_bf16(a, run, &tmA, &tmB, a.d_tma ? &tmD : nullptr, cs));
   }
   // GEMM_PATH_TC_DECODE
   if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, K, M, lda, 64,

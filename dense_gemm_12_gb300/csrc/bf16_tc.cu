@@ -76,8 +76,10 @@ struct __align__(8) TcSmemTail {
   int last_flag;
 };
 
-// Output staging: 4 KB (32 rows x 32 fp32) per epilogue warp.
-constexpr int kEpiStageBytes = kEpiWarps * 32 * 32 * 4;
+// Output staging per epilogue warp: two 4 KB buffers of 32 rows x 32 fp32
+// (the TMA output stage alternates between them; store_chunk uses the first).
+constexpr int kEpiWarpStageBytes = 2 * 32 * 32 * 4;
+constexpr int kEpiStageBytes = kEpiWarps * kEpiWarpStageBytes;
 constexpr size_t kSmemBytes = 1024 + STAGES * kStageBytes + kEpiStageBytes + sizeof(TcSmemTail);
 static_assert(kSmemBytes <= 227 * 1024, "single-CTA kernel shared memory");
 
@@ -341,6 +343,92 @@ __device__ __forceinline__ void epi_bar() {
   asm volatile("bar.sync %0, %1;" ::"n"(kEpiBarSync), "n"(kEpiThreads) : "memory");
 }
 
+// Plain output stage (fp32 D = alpha * acc; beta == 0, nothing fused) of one
+// whole unit through TMA stores.  The warp's 32 rows leave in chunks of 32
+// rows x 32 columns: scaled in registers, written to one of the warp's two
+// 4 KB staging buffers (rows of 128 B whose 16-byte pieces are XOR-swizzled by
+// row % 8, the tensor map's 128-byte swizzle, so the 32 lanes' stores fall in
+// distinct banks) and stored by one TMA copy, which the tensor map clips at
+// the matrix edges.  Lane 0 issues the copies; before a buffer is rewritten it
+// waits until the copy issued from it two chunks earlier has read it.  The
+// accumulator columns of the next chunk are read from TMEM while this chunk
+// is staged.  Far fewer instructions per element than the store_chunk path,
+// whose issue latency bounds the kernel on problems with a short k loop.
+static_assert(kTcStoreBoxCols == 32 && kTcStoreBoxRows == 32 && kEpiWarpStageBytes == 2 * 4096,
+              "TMA output stage: two 32 x 32 fp32 buffers per epilogue warp");
+
+// Waits for this thread's TMEM loads; r is tied to the wait so that no use of
+// the loaded registers is scheduled before it.
+__device__ __forceinline__ void tc_wait_ld_into(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                 "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                 "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                 "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
+
+// One chunk: buffer `buf` (byte offset in the warp's staging), columns
+// col0 .. col0 + 31 of rows row_base .. row_base + 31.
+__device__ __forceinline__ void stage_chunk_tma(const CUtensorMap* tmD, const uint32_t (&r)[32],
+                                                float alpha, uint32_t stg, uint32_t buf, int col0,
+                                                int row_base) {
+  const uint32_t lane = threadIdx.x & 31;
+  if (lane == 0) bulk_wait_group_read<1>();
+  __syncwarp();
+  const uint32_t row_addr = stg + buf + lane * 128u;
+#pragma unroll
+  for (uint32_t q = 0; q < 8; ++q)
+    st_shared_v4(row_addr + ((q ^ (lane & 7u)) << 4), alpha * __uint_as_float(r[4 * q]),
+                 alpha * __uint_as_float(r[4 * q + 1]), alpha * __uint_as_float(r[4 * q + 2]),
+                 alpha * __uint_as_float(r[4 * q + 3]));
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(tmD, stg + buf, col0, row_base);
+    bulk_commit_group();
+  }
+}
+
+// seq: chunks this warp has staged so far; the buffers alternate across units
+// too, so the copy two chunks back always read the buffer being rewritten.
+__device__ __forceinline__ void store_unit_tma(const TcArgs& p, const CUtensorMap* tmD,
+                                               uint32_t taddr, uint32_t stg, int row_base,
+                                               int col_base, uint32_t& seq) {
+  if (row_base >= p.M) return;
+  const float alpha = p.epi.alpha;
+  // chunks holding at least one column < N (uniform over the warp)
+  const int chunks = min(BN / 32, (p.N - col_base + 31) / 32);
+  const uint32_t buf0 = (seq & 1u) * 4096u, buf1 = 4096u - buf0;
+  seq += static_cast<uint32_t>(chunks);
+  uint32_t ra[32], rb[32];
+  tmem_ld_32x32b_x32(taddr, ra);
+  tc_wait_ld_into(ra);
+#pragma unroll 1
+  for (int c = 0; c < chunks; c += 2) {
+    const bool next = c + 1 < chunks;
+    if (next) tmem_ld_32x32b_x32(taddr + (c + 1) * 32, rb);
+    stage_chunk_tma(tmD, ra, alpha, stg, buf0, col_base + c * 32, row_base);
+    if (!next) break;
+    tc_wait_ld_into(rb);
+    if (c + 2 < chunks) tmem_ld_32x32b_x32(taddr + (c + 2) * 32, ra);
+    stage_chunk_tma(tmD, rb, alpha, stg, buf1, col_base + (c + 1) * 32, row_base);
+    tc_wait_ld_into(ra);
+  }
+}
+
+// Before the staging area is written by other code: every TMA store issued
+// from it has read it.
+__device__ __forceinline__ void staging_release(const TcArgs& p) {
+  if (p.d_tma) {
+    if ((threadIdx.x & 31) == 0) bulk_wait_group_read<0>();
+    __syncwarp();
+  }
+}
+
 // Output stage of one work unit, run by the 4 epilogue warps of a CTA (thread
 // et = TMEM lane et = row et of the CTA's 128-row tile).  taddr: this warp's
 // lanes of the accumulator.  cpi / rank: CTAs per item (1, or 2 on pairs) and
@@ -353,11 +441,16 @@ __device__ __forceinline__ void epi_bar() {
 // order, so the result does not depend on which part finishes last -- and
 // writes D.
 template <bool FUSED>
-__device__ __forceinline__ void epilogue_unit(const TcArgs& p, const Unit& w, uint32_t taddr,
+__device__ __forceinline__ void epilogue_unit(const TcArgs& p, const CUtensorMap* tmD,
+                                              uint32_t& tma_seq, const Unit& w, uint32_t taddr,
                                               float4* stg, int row_base, int tn, int cpi,
                                               int rank, int num_kb, int64_t W, int et,
                                               int* last_flag, float& amax_acc) {
   if (w.tail < 0) {
+    if (!FUSED && p.d_tma) {
+      store_unit_tma(p, tmD, taddr, smem_u32(stg), row_base, tn * BN, tma_seq);
+      return;
+    }
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
       uint32_t r[32];
@@ -367,6 +460,7 @@ __device__ __forceinline__ void epilogue_unit(const TcArgs& p, const Unit& w, ui
     }
     return;
   }
+  if (!FUSED) staging_release(p);
   float4* const ws4 = reinterpret_cast<float4*>(p.ws);
   auto part_base = [&](int slot) {
     return ws4 + (static_cast<int64_t>(slot) * cpi + rank) * (kPartFloats / 4);
@@ -504,7 +598,8 @@ __device__ __forceinline__ void cluster_chunks(const TcArgs& p, uint32_t part_u3
 template <bool FUSED, bool CLUSTER>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bf16_kernel(const __grid_constant__ TcArgs p, const __grid_constant__ CUtensorMap tmA,
-                   const __grid_constant__ CUtensorMap tmB) {
+                   const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmD) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = align_smem<1024>(smem_raw);
   uint8_t* epi_stage = smem + STAGES * kStageBytes;
@@ -638,7 +733,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // -------------------------------------------------------- epilogue
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     const int et = quarter * 32 + lane;
-    float4* stg = reinterpret_cast<float4*>(epi_stage + quarter * 4096);
+    float4* stg = reinterpret_cast<float4*>(epi_stage + quarter * kEpiWarpStageBytes);
+    uint32_t tma_seq = 0;  // chunks staged by the TMA output stage (buffer parity)
     uint32_t j = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       const Unit w = unit_of(p, u, num_kb, num_items);
@@ -670,13 +766,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         parts_stored = true;
       } else {
-        epilogue_unit<FUSED>(p, w, taddr, stg, tm * BM + quarter * 32, tn, 1, 0, num_kb, W, et,
-                             &tail->last_flag, amax_acc);
+        epilogue_unit<FUSED>(p, &tmD, tma_seq, w, taddr, stg, tm * BM + quarter * 32, tn, 1, 0, num_kb,
+                             W, et, &tail->last_flag, amax_acc);
       }
       tc_fence_before_sync();
       mbar_arrive(&tail->tmem_empty[ab]);
     }
     if (FUSED && !CLUSTER) epi_flush_amax(p.epi, amax_acc);
+    // The TMA stores of the output stage are complete before the CTA leaves.
+    if (!FUSED && p.d_tma) {
+      if (lane == 0) bulk_wait_group_all();
+      __syncwarp();
+    }
   }
 
   if (CLUSTER) {
@@ -689,7 +790,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int tm, tn;
       tile_coords(static_cast<int>(blockIdx.x) / p.cluster, tiles_m, tiles_n, p.group_m, tm, tn);
       cluster_chunks<FUSED>(p, smem_u32(smem), p.cluster, static_cast<int>(cluster_cta_rank()),
-                            reinterpret_cast<float4*>(epi_stage + quarter * 4096),
+                            reinterpret_cast<float4*>(epi_stage + quarter * kEpiWarpStageBytes),
                             tm * BM + quarter * 32, tn, quarter * 32 + lane, amax_acc);
       if (FUSED) epi_flush_amax(p.epi, amax_acc);
     }
@@ -750,7 +851,8 @@ static_assert(kPairSmemBytes <= 227 * 1024, "pair kernel shared memory");
 template <bool FUSED>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bf16_pair_kernel(const __grid_constant__ TcArgs p, const __grid_constant__ CUtensorMap tmA,
-                        const __grid_constant__ CUtensorMap tmB) {
+                        const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmD) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = align_smem<1024>(smem_raw);
   uint8_t* epi_stage = smem + PS * kPairStageBytes;
@@ -905,9 +1007,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // -------------------------------------------------------- epilogue
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     const int et = quarter * 32 + lane;
-    float4* stg = reinterpret_cast<float4*>(epi_stage + quarter * 4096);
+    float4* stg = reinterpret_cast<float4*>(epi_stage + quarter * kEpiWarpStageBytes);
     float amax_acc = 0.0f;
     const uint32_t tmem_empty0 = mapa_shared(smem_u32(&tail->tmem_empty[0]), 0);
+    uint32_t tma_seq = 0;  // chunks staged by the TMA output stage (buffer parity)
     uint32_t j = 0;
     for (int u = first_item; u < units; u += item_stride) {
       const Unit w = unit_of(p, u, num_kb, num_items);
@@ -922,13 +1025,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after_sync();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + ab * BN;
       // each CTA of the pair owns the counter and partials of its 128 rows
-      epilogue_unit<FUSED>(p, w, taddr, stg, tm * BM + quarter * 32, tn, 2,
+      epilogue_unit<FUSED>(p, &tmD, tma_seq, w, taddr, stg, tm * BM + quarter * 32, tn, 2,
                            static_cast<int>(rank), num_kb, W, et, &tail->last_flag, amax_acc);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(tmem_empty0 + ab * static_cast<uint32_t>(sizeof(uint64_t)));
     }
     if (FUSED) epi_flush_amax(p.epi, amax_acc);
+    // The TMA stores of the output stage are complete before the CTA leaves.
+    if (!FUSED && p.d_tma) {
+      if (lane == 0) bulk_wait_group_all();
+      __syncwarp();
+    }
   }
 
   tc_fence_before_sync();
@@ -1014,7 +1122,7 @@ static int single_max_clusters(int S, bool fused) {
 int tc_b_box_rows(bool pair) { return pair ? PBK : BK; }
 
 // Whether an output stage needs the general (fused) kernel instance.
-static bool tc_fused(const Epilogue& ep) {
+bool tc_fused(const Epilogue& ep) {
   return ep.bias != nullptr || ep.act != kActNone || ep.R != nullptr || ep.d_type != kOutF32 ||
          ep.d_scale != 1.0f || ep.amax != nullptr;
 }
@@ -1124,7 +1232,12 @@ int tc_plan_max_parts(const TcPlan& pl, int M, int N, int K) {
 }
 
 cudaError_t launch_tc_bf16(const TcArgs& a, const TcPlan& plan, const CUtensorMap* tmA,
-                           const CUtensorMap* tmB, cudaStream_t stream) {
+                           const CUtensorMap* tmB, const CUtensorMap* tmD, cudaStream_t stream) {
+  // tmD is read only when a.d_tma is set; any valid map stands in otherwise.
+  if (tmD == nullptr) {
+    if (a.d_tma) return cudaErrorInvalidValue;
+    tmD = tmB;
+  }
   if (plan.grid < 1) return cudaSuccess;
   const bool fused = tc_fused(a.epi);
   if (plan.pair) {
@@ -1146,7 +1259,7 @@ cudaError_t launch_tc_bf16(const TcArgs& a, const TcPlan& plan, const CUtensorMa
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    e = cudaLaunchKernelEx(&cfg, kernel, a, *tmA, *tmB);
+    e = cudaLaunchKernelEx(&cfg, kernel, a, *tmA, *tmB, *tmD);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
   }
@@ -1178,7 +1291,7 @@ cudaError_t launch_tc_bf16(const TcArgs& a, const TcPlan& plan, const CUtensorMa
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = cluster ? 2 : 1;
-  e = cudaLaunchKernelEx(&cfg, kernel, a, *tmA, *tmB);
+  e = cudaLaunchKernelEx(&cfg, kernel, a, *tmA, *tmB, *tmD);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -143,6 +143,10 @@ struct TcArgs {
   // `cluster` (= split) parts that form a thread-block cluster and add their
   // partial sums through distributed shared memory: no workspace, no counters.
   int cluster;
+  // 1: the plain output stage (fp32 D = alpha * acc, beta == 0) writes whole
+  // units through TMA stores described by the kernel's D tensor map (fp32,
+  // dims {N, M}, row pitch ldd, box 32 x 32, 128-byte swizzle).
+  int d_tma;
 };
 
 // Launch plan of the bf16 tensor-core GEMM for one shape.
@@ -174,7 +178,12 @@ int tc_b_box_rows(bool pair);
 // bf16 tensor-core GEMM (tcgen05, accumulator in TMEM): 128 x 256 tiles on
 // one CTA, or 256 x 256 tiles on CTA pairs, as planned by tc_plan.
 cudaError_t launch_tc_bf16(const TcArgs& a, const TcPlan& plan, const CUtensorMap* tmA,
-                           const CUtensorMap* tmB, cudaStream_t stream);
+                           const CUtensorMap* tmB, const CUtensorMap* tmD, cudaStream_t stream);
+// The output stage `ep` does more than fp32 D = alpha * acc + beta * C (bias,
+// activation, residual, scaling, another output type or amax).
+bool tc_fused(const Epilogue& ep);
+// Box of the D tensor map for the TMA output stage (see TcArgs::d_tma).
+constexpr int kTcStoreBoxCols = 32, kTcStoreBoxRows = 32;
 constexpr int kTcBM = 128, kTcBN = 256, kTcBK = 64;
 
 struct DecodeArgs {
