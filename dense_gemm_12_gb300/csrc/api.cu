@@ -797,7 +797,10 @@ static gemm_status_t run_bf16_tensor_core(DeviceState* st, gemm_path_t path, int
     a.epi = epi;
     a.err = st->err_word;
     const TileConfig tc = resolve_config(true, M, N, K, st->num_sms, cfg, nullptr);
-    TcPlan pl = tc_plan(a.M, a.N, a.K, st->num_sms, &tc);
+    // The plain output stage with beta == 0 writes whole tiles by TMA when
+    // D's base and row pitch allow a tensor map.
+    const bool tma_out = !tc_fused(epi) && epi.beta == 0.0f && tma_ok(epi.D, epi.ldd, 4);
+    TcPlan pl = tc_plan(a.M, a.N, a.K, st->num_sms, &tc, tma_out);
     // Tiles that all fit in one round add their k-parts through distributed
     // shared memory (single-CTA kernel).
     tc_use_cluster(pl, a.M, a.N, epi);
@@ -823,7 +826,7 @@ static gemm_status_t run_bf16_tensor_core(DeviceState* st, gemm_path_t path, int
       } else if (s == GEMM_ERR_NO_MEMORY) {
         const TileConfig whole{pl.pair ? GEMM_KERNEL_CTA_PAIR : GEMM_KERNEL_SINGLE_CTA, 1,
                                pl.group_m};
-        run = tc_plan(a.M, a.N, a.K, st->num_sms, &whole);
+        run = tc_plan(a.M, a.N, a.K, st->num_sms, &whole, tma_out);
       } else {
         return s;
       }
@@ -833,13 +836,10 @@ static gemm_status_t run_bf16_tensor_core(DeviceState* st, gemm_path_t path, int
     a.sk_workers = run.sk_workers;
     a.group_m = run.group_m;
     a.cluster = run.cluster;
-    // The plain output stage with beta == 0 writes whole tiles by TMA when
-    // D's base and row pitch allow a tensor map.
     CUtensorMap tmD;
     a.d_tma = 0;
-    if (!tc_fused(epi) && epi.beta == 0.0f && tma_ok(epi.D, epi.ldd, 4) &&
-        encode_2d(&tmD, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, epi.D, N, M, epi.ldd,
-                  kTcStoreBoxCols, kTcStoreBoxRows, CU_TENSOR_MAP_SWIZZLE_128B))
+    if (tma_out && encode_2d(&tmD, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, epi.D, N, M, epi.ldd,
+                             kTcStoreBoxCols, kTcStoreBoxRows, CU_TENSOR_MAP_SWIZZLE_128B))
       a.d_tma = 1;
     return from_cuda(launch_tc_bf16(a, run, &tmA, &tmB, a.d_tma ? &tmD : nullptr, cs));
   }

@@ -556,11 +556,11 @@ __device__ __forceinline__ void epilogue_unit(const TcArgs& p, const CUtensorMap
 // layout) in rank (= k) order, starting from zero -- the order and the
 // arithmetic of the workspace fix-up -- and runs the chunk through the output
 // stage.  The 8 loads from one CTA are in flight together: S round trips per
-// chunk.
+// chunk.  The plain beta == 0 output leaves through the TMA output stage.
 template <bool FUSED>
-__device__ __forceinline__ void cluster_chunks(const TcArgs& p, uint32_t part_u32, int S,
-                                               int rank, float4* stg, int row_base, int tn,
-                                               int et, float& amax_acc) {
+__device__ __forceinline__ void cluster_chunks(const TcArgs& p, const CUtensorMap* tmD,
+                                               uint32_t part_u32, int S, int rank, float4* stg,
+                                               int row_base, int tn, int et, float& amax_acc) {
   const int c0 = rank * (BN / 32) / S, c1 = (rank + 1) * (BN / 32) / S;
 #pragma unroll 1
   for (int c = c0; c < c1; ++c) {
@@ -586,7 +586,19 @@ __device__ __forceinline__ void cluster_chunks(const TcArgs& p, uint32_t part_u3
     uint32_t r[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(sum[i]);
-    store_chunk<FUSED>(p, stg, row_base, tn * BN + c * 32, r, amax_acc);
+    if (!FUSED && p.d_tma) {
+      const int col0 = tn * BN + c * 32;
+      if (row_base < p.M && col0 < p.N)
+        stage_chunk_tma(tmD, r, p.epi.alpha, smem_u32(stg), ((c - c0) & 1) * 4096u, col0,
+                        row_base);
+    } else {
+      store_chunk<FUSED>(p, stg, row_base, tn * BN + c * 32, r, amax_acc);
+    }
+  }
+  // The TMA stores are complete before the CTA leaves.
+  if (!FUSED && p.d_tma) {
+    if ((threadIdx.x & 31) == 0) bulk_wait_group_all();
+    __syncwarp();
   }
 }
 
@@ -789,7 +801,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int quarter = warp & 3;
       int tm, tn;
       tile_coords(static_cast<int>(blockIdx.x) / p.cluster, tiles_m, tiles_n, p.group_m, tm, tn);
-      cluster_chunks<FUSED>(p, smem_u32(smem), p.cluster, static_cast<int>(cluster_cta_rank()),
+      cluster_chunks<FUSED>(p, &tmD, smem_u32(smem), p.cluster,
+                            static_cast<int>(cluster_cta_rank()),
                             reinterpret_cast<float4*>(epi_stage + quarter * kEpiWarpStageBytes),
                             tm * BM + quarter * 32, tn, quarter * 32 + lane, amax_acc);
       if (FUSED) epi_flush_amax(p.epi, amax_acc);
@@ -1141,22 +1154,28 @@ bool tc_use_cluster(TcPlan& pl, int M, int N, const Epilogue& epi) {
 }
 
 // Whether automatic dispatch takes the CTA-pair kernel: on large problems
-// only -- at least 128 single-CTA tiles with K > 2048, or 256 with K > 1024.
+// only -- at least 128 single-CTA tiles with K > 2048, or 256 with K > 512.
 // The launch-configuration sweep over M, N, K = 256 .. 8192 found the pair
-// kernel fastest there (by up to 3 %) and the single-CTA kernel, with its
-// cluster split where every tile fits in one round, everywhere else (by up
-// to 65 %: short k loops fill the pair kernel's 128-deep ring slowly, and
-// few tiles leave SMs idle).
+// kernel fastest there (by up to 15 % at K = 1024, since the output stage
+// writes through TMA) and the single-CTA kernel everywhere else (short k
+// loops fill the pair kernel's 128-deep ring slowly, and few tiles leave SMs
+// idle).
 static bool tc_prefer_pair(int tiles, int K) {
-  return (K > 2048 && tiles >= 128) || (K > 1024 && tiles >= 256);
+  return (K > 2048 && tiles >= 128) || (K > 512 && tiles >= 256);
 }
 
-// Cost, in k-blocks, of cutting each of `tiles` single-CTA tiles into S
-// parts that all run at once as clusters: the longest part plus the
-// cluster fix-up (~1 k-block per part, from the sweep's choices).
-constexpr double kTcClusterFixupKb = 1.0;
+// Cost, in k-blocks, of cutting each single-CTA tile into S > 1 parts that
+// all run at once as clusters: the longest part plus the cluster fix-up --
+// the partial sums copied out of TMEM, two cluster barriers, the reduction
+// and the reduced tile's output stage.  Fitted on the launch-configuration
+// sweep's one-round classes: with the TMA output stage, whose whole tiles
+// leave quickly, ~9.5 k-blocks plus ~2.75 per part (at K = 512 and 1024 a
+// split of 2 or 4 lost 10-27 % to whole tiles; at K = 4096, 4 parts won);
+// with the staged output stage, ~1 k-block per part.
+constexpr double kTcClusterFixedKb = 9.5, kTcClusterPartKb = 2.75;
+constexpr double kTcClusterPartKbStaged = 1.0;
 
-TcPlan tc_plan(int M, int N, int K, int num_sms, const TileConfig* fixed) {
+TcPlan tc_plan(int M, int N, int K, int num_sms, const TileConfig* fixed, bool tma_out) {
   TcPlan pl{};
   const int tiles_m = (M + BM - 1) / BM;
   const int tiles_n = (N + BN - 1) / BN;
@@ -1196,7 +1215,9 @@ TcPlan tc_plan(int M, int N, int K, int num_sms, const TileConfig* fixed) {
     for (int S = 2; S <= 8 && S <= num_kb; ++S) {
       if (static_cast<int64_t>(items) * S > workers || items > single_max_clusters(S, false))
         continue;
-      const double cost = static_cast<double>((num_kb + S - 1) / S) + kTcClusterFixupKb * S;
+      const double cost = static_cast<double>((num_kb + S - 1) / S) +
+                          (tma_out ? kTcClusterFixedKb + kTcClusterPartKb * S
+                                   : kTcClusterPartKbStaged * S);
       if (cost < best_cost - 1e-9) {
         best = S;
         best_cost = cost;

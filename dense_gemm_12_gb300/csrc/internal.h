@@ -164,7 +164,10 @@ struct TcPlan {
 // `fixed` pins kernel, split (GEMM_SPLIT_STREAM: a stream-K tail) and group
 // height; nullptr: the pair kernel for M > 128, the cost model's split,
 // groups of 8.
-TcPlan tc_plan(int M, int N, int K, int num_sms, const TileConfig* fixed);
+// tma_out: the output stage writes whole tiles through TMA stores (plain fp32
+// output with beta == 0 and a D that TMA can describe), which makes whole
+// tiles cheaper against split ones; the planning queries assume it.
+TcPlan tc_plan(int M, int N, int K, int num_sms, const TileConfig* fixed, bool tma_out = true);
 // Largest number of parts any tail item of the plan is cut into (1 = none).
 int tc_plan_max_parts(const TcPlan& pl, int M, int N, int K);
 // Turns a single-CTA plan whose tiles all run in one round, each cut into

@@ -222,7 +222,7 @@ def summary_lines(results, chosen, gpu, num_sms, command, kept=(), kept_after=()
              "Command (%s, %d SMs):" % (gpu, num_sms), "", "    " + command, "",
              "Per class (ceil(log2) of M, N, K), one representative shape; model = "
              "the cost model's choice without the table (split of the last round, -1 = "
-             "stream-K; pair kernel for bf16 M > 128; fp32 tile width single_cta = "
+             "stream-K; bf16 CTA pairs on large problems, single CTAs otherwise; fp32 tile width single_cta = "
              "128x128 or wide = 128x256; raster groups of 8); best = fastest pinned "
              "configuration; both re-timed in turn (4 x 5 back-to-back launches, median).  Entries "
              "marked `table` beat the model by more than the margin and were written "

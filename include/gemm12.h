@@ -139,7 +139,9 @@ gemm_status_t gemm_sgemm(int64_t M, int64_t N, int64_t K, float alpha,
  * ("Split-K" in the same page's "Variants and alternatives") and reduces the
  * partial sums in a fixed order, so results are deterministic.  Error bound:
  * 8e-3 of |alpha|*(|A||B|)_ij + |beta|*|C_ij| against the exact product of the
- * bf16 values.
+ * bf16 values.  With beta == 0, a 16-byte aligned C and ldc a multiple of 4,
+ * the tile kernels write C through TMA stores (faster when the output
+ * dominates, e.g. K <= 1024); the results are the same either way.
  */
 gemm_status_t gemm_bf16gemm(int64_t M, int64_t N, int64_t K, float alpha,
                             const void *A, int64_t lda,
@@ -351,8 +353,9 @@ typedef enum {
  * bf16 with M > 16 and at least 2^24 FLOPs.  Otherwise GEMM_PATH_SIMT_GENERIC
  * or GEMM_PATH_SIMT_BF16 (also when the staging buffer cannot be allocated).
  * Between the two bf16 tile kernels it reports the one automatic dispatch
- * runs on the current device (the sweep's table picks single CTAs for many
- * small problems with M > 128); with no usable device, the one-CTA kernel for
+ * runs on the current device (CTA pairs for large problems -- at least 128
+ * tiles of 128 x 256 with K > 2048, or 256 with K > 512 -- unless the sweep's
+ * table says otherwise); with no usable device, the one-CTA kernel for
  * M <= 128 and CTA pairs above.
  * Pointers are only inspected for alignment, never dereferenced.  Returns
  * GEMM_PATH_NONE (and writes nothing) for arguments the call would reject.

@@ -233,6 +233,20 @@ def test_bf16_cluster_fixup_exact_on_integers(M, N, K, S):
     check_device_error()
 
 
+@pytest.mark.parametrize("M,N,K,S", BF16_CASES[::2])
+def test_bf16_cluster_tma_output_exact_on_integers(M, N, K, S):
+    # beta = 0: each CTA's share of the reduced tile leaves through TMA stores,
+    # clipped at the ragged edges; padded rows keep their padding
+    cfg = {"kernel": "single_cta", "split": S, "group_m": 1}
+    assert g.gemm_split_cluster(1, M, N, K, cfg) == S
+    A, B, C = make_inputs(M, N, K, INT, INT, INT, seed=M + 3 * S, dtype="bf16")
+    ref32, _, _ = oracle_bf16(A, B, C, 1.5, 0.0, want64=False)
+    for ldc in (None, N + 4, N + 1):
+        out = _bf16_call(A, B, C, 1.5, 0.0, cfg, ldc=ldc)
+        assert np.array_equal(out.numpy().view(np.uint32), ref32.view(np.uint32))
+    check_device_error()
+
+
 @pytest.mark.parametrize("M,N,K,S", BF16_CASES[1::2])
 def test_bf16_cluster_fixup_random_within_bound_and_repeatable(M, N, K, S):
     cfg = {"kernel": "single_cta", "split": S}

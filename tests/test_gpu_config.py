@@ -44,16 +44,47 @@ BF16_CONFIGS = [
 ]
 
 
+# beta = 0 with a plain fp32 output writes whole tiles through TMA stores (the
+# split parts' fix-up keeps the staged output stage); beta != 0 reads C.
+@pytest.mark.parametrize("beta", [-0.5, 0.0])
 @pytest.mark.parametrize("M,N,K", [(8, 520, 1024), (100, 1000, 1024), (300, 776, 2048),
                                    (1024, 1024, 512)])
-def test_bf16_every_config_exact(M, N, K):
+def test_bf16_every_config_exact(M, N, K, beta):
     A, B, C = make_inputs(M, N, K, ("int", None), ("int", None), ("int", None), seed=M + N,
                           dtype="bf16")
-    ref32, _, _ = oracle_bf16(A, B, C, 1.5, -0.5)
+    ref32, _, _ = oracle_bf16(A, B, C, 1.5, beta)
     for cfg in BF16_CONFIGS + [None, {"split": 2}, {"group_m": 64}]:
-        st, out = _run(True, A, B, C, 1.5, -0.5, cfg)
+        st, out = _run(True, A, B, C, 1.5, beta, cfg)
         assert st == 0, cfg
         assert np.array_equal(out.numpy(), ref32), cfg
+    check_device_error()
+
+
+@pytest.mark.parametrize("cfg", [{"kernel": "single_cta", "split": 1},
+                                 {"kernel": "single_cta", "split": 3},
+                                 {"kernel": "cta_pair", "split": 1},
+                                 {"kernel": "cta_pair", "split": 2},
+                                 {"kernel": "cta_pair", "split": -1}])
+def test_bf16_tma_output_edges_and_padded_rows(cfg):
+    # ragged M and N (the tensor map clips the last tiles), rows of ldc > N
+    # whose padding must stay untouched, and a pitch TMA cannot describe
+    # (ldc = N + 1: the staged output stage instead); beta = 0
+    M, N, K = 1000, 1300, 1500
+    A, B, C = make_inputs(M, N, K, ("int", None), ("int", None), ("int", None), seed=31,
+                          dtype="bf16")
+    ref32, _, _ = oracle_bf16(A, B, C, -2.0, 0.0)
+    dA, dB = A.cuda(), B.cuda()
+    for ldc in (N, N + 12, N + 1):
+        dC = torch.full((M, ldc), -7.0, device="cuda")
+        st = g.gemm_bf16gemm_config(M, N, K, -2.0, dA.data_ptr(), K, dB.data_ptr(), N, 0.0,
+                                    dC.data_ptr(), ldc, cfg,
+                                    torch.cuda.current_stream().cuda_stream)
+        torch.cuda.synchronize()
+        assert st == 0, (cfg, ldc)
+        out = dC.cpu()
+        assert torch.all(out[:, N:] == -7.0), (cfg, ldc)
+        assert np.array_equal(out[:, :N].numpy().view(np.uint32), ref32.view(np.uint32)), \
+            (cfg, ldc)
     check_device_error()
 
 
@@ -71,12 +102,12 @@ def test_bf16_every_config_exact(M, N, K):
 def test_bf16_stream_k_exact_and_repeatable(kernel, M, N, K):
     A, B, C = make_inputs(M, N, K, ("int", None), ("int", None), ("int", None), seed=M + K,
                           dtype="bf16")
-    ref32, _, _ = oracle_bf16(A, B, C, 1.5, -0.5)
-    for gm in (1, 8):
+    for gm, beta in ((1, -0.5), (8, 0.0)):
+        ref32, _, _ = oracle_bf16(A, B, C, 1.5, beta)
         cfg = {"kernel": kernel, "split": -1, "group_m": gm}
         first = None
         for _ in range(2):
-            st, out = _run(True, A, B, C, 1.5, -0.5, cfg)
+            st, out = _run(True, A, B, C, 1.5, beta, cfg)
             assert st == 0, cfg
             assert np.array_equal(out.numpy().view(np.uint32), ref32.view(np.uint32)), cfg
             if first is not None:
