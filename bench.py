@@ -45,7 +45,7 @@ METRIC = "GFLOP/s and % of roofline: fp32 4092^3 SIMT, bf16 8192^3 tcgen05, M=16
 SM_LANES_FP32 = 128        # fp32 FFMA lanes per SM (4 partitions x 32)
 MIN_TRIAL_MS = 200.0       # each timed trial of a part lasts at least this long
 TRIALS = 5                 # trials per part; the median is reported
-E2E_TRIALS = 3             # end-to-end trials (median reported)
+E2E_TRIALS = 5             # end-to-end trials (median reported)
 SUSTAINED_MS = 2000.0      # the sustained bf16 part runs back to back this long
 
 
@@ -713,7 +713,7 @@ def run_ours(args):
         # ~1 ms) and drain (the last step's output copy, ~0.35 ms) are a small
         # part of the time: at 20 steps they were 3 % of it.
         n_e2e = min(max(args.steps, 60), 200)
-        # Three trials, the median reported: the host link is shared with the
+        # Five trials, the median reported: the host link is shared with the
         # machine's other work, and a trial can run ~1 ms per step slower on the
         # copies alone (the GEMM's own time does not move).
         trial_ms = []
