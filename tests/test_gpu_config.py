@@ -88,6 +88,24 @@ def test_bf16_tma_output_edges_and_padded_rows(cfg):
     check_device_error()
 
 
+@pytest.mark.parametrize("M,N,K,cfg", [
+    (600, 8, 300, None),                                   # one tile column of 8 < the 32-wide box
+    (1000, 20, 520, {"kernel": "cta_pair", "split": 1}),
+    (700, 36, 1000, {"kernel": "single_cta", "split": 2}),
+    (777, 30, 200, None),                                  # ldc * 4 not a multiple of 16: staged
+])
+def test_bf16_narrow_outputs_beta_zero_exact(M, N, K, cfg):
+    # tile kernels (M > 512 keeps these off the decode kernel) with outputs
+    # narrower than one TMA store box; beta = 0
+    A, B, C = make_inputs(M, N, K, ("int", None), ("int", None), ("int", None), seed=N + K,
+                          dtype="bf16")
+    ref32, _, _ = oracle_bf16(A, B, C, 1.5, 0.0)
+    st, out = _run(True, A, B, C, 1.5, 0.0, cfg)
+    assert st == 0
+    assert np.array_equal(out.numpy().view(np.uint32), ref32.view(np.uint32))
+    check_device_error()
+
+
 # Stream-K tails of the tensor-core kernels (split = -1).  The tail's k-blocks
 # (tail items x k-blocks per item; 128-deep on pairs, 64 on one CTA) must be
 # at least the workers -- 76 resident pairs or 152 CTAs on a GB300 -- or the
