@@ -9,10 +9,11 @@ the bound used for random inputs (2e-6 sqrt(K) fp32, 8e-3 bf16), equality
 also catches a single lost k-slab or TMA box anywhere in the schedule.
 
 Each case runs the benchmark's shape through the plain entry point, so it
-takes the same launch plan as the timed run (the plan depends on the shape
-only): fp32 4092^3 with its stream-K tail, 3000x5000x1999 (on a staged
-copy of A) with its last tiles cut along k, bf16 8192^3 on CTA pairs with
-its last round split along k, and the decode shape.  fp32 results are compared in full;
+takes the same launch plan as the timed run: fp32 4092^3 with its stream-K
+tail, 3000x5000x1999 (on a staged copy of A) with its last tiles cut along k,
+bf16 8192^3 on CTA pairs with its last round split along k (with the
+benchmark's beta = 0, through the TMA output stage, and with beta != 0), and
+the decode shape.  fp32 results are compared in full;
 bf16 8192^3 on 512 rows: the first and last row of every 128-row tile (so
 both tiles of every CTA pair and every tile boundary) and 6 more per tile.
 """
@@ -76,16 +77,19 @@ def _tile_rows(M, tile=128, extra=6, seed=0):
     return np.unique(np.array(rows, dtype=np.int64))
 
 
-def test_bf16_8192_exact_on_every_tile():
+# beta = 0 is the benchmark's own configuration: its output leaves through
+# the TMA output stage; beta != 0 takes the staged output stage.
+@pytest.mark.parametrize("alpha,beta", [(1.5, -0.5), (1.0, 0.0)])
+def test_bf16_8192_exact_on_every_tile(alpha, beta):
     M = N = K = 8192
     cfg, _ = g.gemm_get_config(1, M, N, K)
     assert cfg["kernel"] == "cta_pair", cfg
     A, B, C = make_inputs(M, N, K, INT, INT, INT, seed=8192, dtype="bf16")
-    out = _device_gemm(g.gemm_bf16gemm, A, B, C, 1.5, -0.5)
+    out = _device_gemm(g.gemm_bf16gemm, A, B, C, alpha, beta)
     rows = _tile_rows(M)
     assert len(rows) == 512
     idx = torch.from_numpy(rows)
-    ref32, _, _ = oracle_bf16(A[idx].contiguous(), B, C[idx].contiguous(), 1.5, -0.5,
+    ref32, _, _ = oracle_bf16(A[idx].contiguous(), B, C[idx].contiguous(), alpha, beta,
                               want64=False)
     diff = _bits(out[idx].numpy()) != _bits(ref32)
     assert not diff.any(), "%d elements differ, first at row %d col %d" % (
